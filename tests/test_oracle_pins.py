@@ -1,0 +1,361 @@
+"""Pins of the CPU oracle against values that the pages or mathematics fix.
+
+Each test ties one oracle function to something other than the oracle:
+hand-checked values (tests/golden), closed forms, invariants of the owner
+semantics, torch.optim.AdamW, torch.nn.utils.clip_grad_norm_ and torch's
+bf16 cast.  A plausible slip in the oracle (a dropped term, a wrong scale,
+a swapped mesh index) fails at least one of them.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import ALREADY_REDUCED, LOCAL_SHARD, PARTIAL_SUM, REPLICA_AVG
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+TAGS = {"REPLICA_AVG": REPLICA_AVG, "PARTIAL_SUM": PARTIAL_SUM,
+        "LOCAL_SHARD": LOCAL_SHARD, "ALREADY_REDUCED": ALREADY_REDUCED}
+
+
+def bf16(x):
+    """float values -> bf16 bit patterns (torch's round-to-nearest-even)."""
+    t = torch.as_tensor(np.asarray(x, np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def bits_to_f32(bits):
+    return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def load(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# --------------------------------------------------------------------------
+# Owner semantics, hand-checked (golden/hand_checked_world4.json)
+# --------------------------------------------------------------------------
+def test_hand_checked_single_microbatch(orc):
+    g = load("hand_checked_world4.json")
+    geo = g["geometry"]
+    vals = g["rank_values"]
+    P = 16
+    grads = np.zeros((1, 4, P), np.uint16)
+    for k, v in enumerate(vals):
+        grads[0, k, :] = bf16([v] * P)
+    for name, exp in g["expected_acc"].items():
+        acc = oracle.reduce_bucket(TAGS[name], geo["tp"], geo["dp_replicate"], geo["dp_shard"],
+                                   P, P, grads)
+        assert acc.shape[0] == len(exp)
+        for c, row in enumerate(exp):
+            assert np.all(acc[c] == row[0]), (name, c, acc[c][:4], row)
+
+
+def test_hand_checked_two_microbatches(orc):
+    g = load("hand_checked_world4.json")["two_microbatch_case"]
+    geo = g["geometry"]
+    P = 8
+    grads = np.zeros((2, 4, P), np.uint16)
+    for j, vals in enumerate(g["rank_values_per_microbatch"]):
+        for k, v in enumerate(vals):
+            grads[j, k, :] = bf16([v] * P)
+    for name, exp in g["expected_acc"].items():
+        acc = oracle.reduce_bucket(TAGS[name], geo["tp"], geo["dp_replicate"], geo["dp_shard"],
+                                   P, P, grads)
+        for c, row in enumerate(exp):
+            assert np.all(acc[c] == row[0]), (name, c, acc[c][:4], row)
+        # G = acc / M: the norm of a constant bucket is P * (acc/M)^2
+        s = oracle.norm_sq(acc, 2)
+        want = sum(P * (row[0] / 2) ** 2 for row in exp)
+        assert s == want
+
+
+def test_dp_mesh_rank_order(orc):
+    g = load("hand_checked_world4.json")["dp_mesh_2x4"]
+    geo = g["geometry"]
+    for r, row in enumerate(g["ranks"]):
+        for s, want in enumerate(row):
+            assert oracle.rank(r, s, 0, geo["dp_shard"], geo["tp"]) == want
+
+
+def test_padding_ignored_and_zero(orc):
+    """Input padding may hold NaN; outputs there are exactly zero."""
+    P, used = 16, 5
+    grads = np.full((2, 4, P), 0x7FC0, np.uint16)  # NaN everywhere
+    grads[:, :, :used] = bf16(np.arange(1, used + 1))
+    for tag in range(4):
+        acc = oracle.reduce_bucket(tag, 2, 1, 2, P, used, grads)
+        assert np.all(np.isfinite(acc))
+        assert np.all(acc[:, used:] == 0.0)
+
+
+# --------------------------------------------------------------------------
+# Identical copies x: RA -> x, PS -> tp*x, LS -> x, AR -> x (per microbatch)
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("tp,dr,ds", [(2, 1, 2), (2, 2, 4), (4, 1, 2), (1, 2, 4), (3, 1, 3)])
+def test_identical_copies(orc, tp, dr, ds):
+    rng = np.random.default_rng(7)
+    R, P = tp * dr * ds, 40
+    x = bf16(rng.normal(0, 1e-2, P))
+    xv = bits_to_f32(x).astype(np.float64)
+    grads = np.broadcast_to(x, (1, R, P)).copy()
+    exp = {REPLICA_AVG: xv, PARTIAL_SUM: tp * xv, LOCAL_SHARD: xv, ALREADY_REDUCED: xv}
+    for tag, want in exp.items():
+        acc = oracle.reduce_bucket(tag, tp, dr, ds, P, P, grads)
+        for c in range(acc.shape[0]):
+            np.testing.assert_allclose(acc[c], want, rtol=1e-15, atol=0)
+
+
+# --------------------------------------------------------------------------
+# No double reduction, no TP sync of local shards
+# --------------------------------------------------------------------------
+def test_already_reduced_ignores_other_ranks(orc):
+    rng = np.random.default_rng(1)
+    tp, dr, ds, P = 2, 2, 2, 24
+    R = tp * dr * ds
+    grads = bf16(rng.normal(0, 1, (2, R, P)))
+    base = oracle.reduce_bucket(ALREADY_REDUCED, tp, dr, ds, P, P, grads)
+    pert = grads.copy()
+    pert[:, 1:, :] = bf16(rng.normal(0, 5, (2, R - 1, P)))
+    again = oracle.reduce_bucket(ALREADY_REDUCED, tp, dr, ds, P, P, pert)
+    assert np.array_equal(base, again)
+    # ... and rank 0's copy is what it returns, summed over microbatches
+    want = bits_to_f32(grads[0, 0]).astype(np.float64) + bits_to_f32(grads[1, 0])
+    assert np.array_equal(base[0], want)
+
+
+def test_local_shard_not_synchronised_across_tp(orc):
+    rng = np.random.default_rng(2)
+    tp, dr, ds, P = 2, 2, 2, 24
+    R = tp * dr * ds
+    grads = bf16(rng.normal(0, 1, (1, R, P)))
+    base = oracle.reduce_bucket(LOCAL_SHARD, tp, dr, ds, P, P, grads)
+    for tprime in range(tp):
+        pert = grads.copy()
+        for r in range(dr):
+            for s in range(ds):
+                k = oracle.rank(r, s, tprime, ds, tp)
+                pert[0, k] = bf16(rng.normal(0, 3, P))
+        again = oracle.reduce_bucket(LOCAL_SHARD, tp, dr, ds, P, P, pert)
+        for t in range(tp):
+            if t == tprime:
+                assert not np.array_equal(base[t], again[t])
+            else:
+                assert np.array_equal(base[t], again[t])
+
+
+def test_partial_sum_is_a_sum_not_the_local_value(orc):
+    """The Megatron-FSDP bug class on the issue page: copying the local grad
+    without resolving a TP Partial placement loses the sum."""
+    tp, dr, ds, P = 2, 1, 1, 8
+    grads = np.zeros((1, 2, P), np.uint16)
+    grads[0, 0] = bf16([1.0] * P)
+    grads[0, 1] = bf16([2.0] * P)
+    acc = oracle.reduce_bucket(PARTIAL_SUM, tp, dr, ds, P, P, grads)
+    assert np.all(acc[0] == 3.0)
+    acc = oracle.reduce_bucket(REPLICA_AVG, tp, dr, ds, P, P, grads)
+    assert np.all(acc[0] == 1.5)
+
+
+# --------------------------------------------------------------------------
+# Accumulation equals one large batch
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("tag", [REPLICA_AVG, PARTIAL_SUM, LOCAL_SHARD])
+def test_accumulation_equals_large_batch(orc, tag):
+    """M microbatches over dp ranks give the same G as one microbatch over a
+    world whose replica axis is M times larger (mean of means = mean)."""
+    rng = np.random.default_rng(3)
+    tp, dr, ds, M, P = 2, 1, 2, 4, 32
+    R = tp * dr * ds
+    grads = bf16(rng.normal(0, 1e-2, (M, R, P)))
+    acc = oracle.reduce_bucket(tag, tp, dr, ds, P, P, grads)
+    G = acc / M
+    # One microbatch; replica index r' = j * dr + r; rank order keeps the
+    # replica axis slowest, so the big world is the microbatches stacked.
+    big = grads.reshape(1, M * R, P)
+    acc_big = oracle.reduce_bucket(tag, tp, M * dr, ds, P, P, big)
+    np.testing.assert_allclose(G, acc_big, rtol=1e-13, atol=1e-18)
+
+
+# --------------------------------------------------------------------------
+# Norm and clipping
+# --------------------------------------------------------------------------
+def test_norm_closed_form(orc):
+    n, M, a = 1000, 4, 0.375
+    acc = np.full(n, a, np.float64)
+    assert oracle.norm_sq(acc, M) == n * (a / M) ** 2
+    assert oracle.norm_sq(np.zeros(0), 1) == 0.0
+
+
+def test_clip_special_cases(orc):
+    # ||G|| <= max_norm or clipping off: coefficient exactly 1
+    assert oracle.clip_coef(0.25, 1.0) == 1.0
+    assert oracle.clip_coef(0.0, 1.0) == 1.0
+    assert oracle.clip_coef(1e6, 0.0) == 1.0
+    assert oracle.clip_coef(1e6, -1.0) == 1.0
+    # above: max/(norm + 1e-6)
+    assert oracle.clip_coef(4.0, 1.0) == 1.0 / (2.0 + 1e-6)
+    assert math.isnan(oracle.clip_coef(float("nan"), 1.0))
+    assert oracle.clip_coef(float("inf"), 1.0) == 0.0
+
+
+@pytest.mark.parametrize("max_norm", [0.5, 1.0, 3.0, 100.0])
+def test_clip_matches_torch_clip_grad_norm(orc, max_norm):
+    rng = np.random.default_rng(4)
+    arrs = [rng.normal(0, 0.3, n) for n in (17, 64, 5)]
+    ts = [torch.nn.Parameter(torch.zeros(a.size, dtype=torch.float64)) for a in arrs]
+    for t, a in zip(ts, arrs):
+        t.grad = torch.tensor(a, dtype=torch.float64)
+    total = torch.nn.utils.clip_grad_norm_(ts, max_norm, foreach=False)
+    acc = np.concatenate(arrs)
+    s = oracle.norm_sq(acc, 1)
+    assert math.isclose(math.sqrt(s), float(total), rel_tol=1e-14)
+    c = oracle.clip_coef(s, max_norm)
+    clipped = np.concatenate([t.grad.numpy() for t in ts])
+    np.testing.assert_allclose(c * acc, clipped, rtol=1e-14, atol=0)
+
+
+# --------------------------------------------------------------------------
+# AdamW
+# --------------------------------------------------------------------------
+HP = (1e-3, 0.9, 0.999, 1e-8, 0.01)
+
+
+def test_adamw_step1_closed_form(orc):
+    rng = np.random.default_rng(5)
+    n = 256
+    g = rng.normal(0, 1e-3, n)
+    p0 = rng.normal(0, 0.02, n).astype(np.float32)
+    z = np.zeros(n, np.float32)
+    lr, b1, b2, eps, wd = HP
+    p1, m1, v1, bits = oracle.adamw(g, n, 1, 1.0, HP, 1, p0, z, z)
+    want = p0.astype(np.float64) * (1 - lr * wd) - lr * g / (np.abs(g) + eps)
+    np.testing.assert_allclose(p1, want, rtol=1e-6, atol=1e-9)
+    np.testing.assert_allclose(m1, (1 - b1) * g, rtol=1e-6)
+    np.testing.assert_allclose(v1, (1 - b2) * g * g, rtol=1e-6)
+
+
+def test_adamw_zero_gradient(orc):
+    rng = np.random.default_rng(6)
+    n = 64
+    p0 = rng.normal(0, 0.02, n).astype(np.float32)
+    z = np.zeros(n, np.float32)
+    p1, m1, v1, _ = oracle.adamw(np.zeros(n), n, 1, 1.0, HP, 1, p0, z, z)
+    assert np.all(m1 == 0) and np.all(v1 == 0)
+    np.testing.assert_array_equal(p1, (p0.astype(np.float64) * (1 - HP[0] * HP[4])).astype(np.float32))
+
+
+def test_adamw_padding_written_zero(orc):
+    n, used = 16, 5
+    p0 = np.full(n, 0.5, np.float32)
+    mv = np.full(n, 0.25, np.float32)
+    p1, m1, v1, bits = oracle.adamw(np.ones(n), used, 1, 1.0, HP, 3, p0, mv, mv)
+    assert np.all(p1[used:] == 0) and np.all(m1[used:] == 0) and np.all(v1[used:] == 0)
+    assert np.all(bits[used:] == 0)
+    assert np.all(p1[:used] != 0)
+
+
+@pytest.mark.parametrize("hp", [(1e-3, 0.9, 0.999, 1e-8, 0.01), (3e-4, 0.8, 0.95, 1e-6, 0.1)])
+def test_adamw_multistep_matches_torch(orc, hp):
+    """Steps 1..5 against torch.optim.AdamW (fp64 CPU), with the clipped,
+    microbatch-averaged gradient g = c * acc / M."""
+    rng = np.random.default_rng(8)
+    n, M, c = 100, 4, 0.625
+    p0 = rng.normal(0, 0.02, n).astype(np.float32)
+    param = torch.nn.Parameter(torch.tensor(p0, dtype=torch.float64))
+    opt = torch.optim.AdamW([param], lr=hp[0], betas=(hp[1], hp[2]), eps=hp[3],
+                            weight_decay=hp[4], foreach=False)
+    master, m, v = p0.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)
+    for step in range(1, 6):
+        acc = rng.normal(0, 1e-3, n) * M
+        param.grad = torch.tensor(c * acc / M, dtype=torch.float64)
+        opt.step()
+        master, m, v, bits = oracle.adamw(acc, n, M, c, hp, step, master, m, v)
+        ref = param.detach().numpy()
+        np.testing.assert_allclose(master, ref, rtol=1e-6, atol=1e-9)
+        st = opt.state[param]
+        np.testing.assert_allclose(m, st["exp_avg"].numpy(), rtol=1e-5, atol=1e-12)
+        np.testing.assert_allclose(v, st["exp_avg_sq"].numpy(), rtol=1e-5, atol=1e-15)
+        # bf16 output is the rounded fp32 master
+        np.testing.assert_array_equal(bits, bf16(master))
+
+
+# --------------------------------------------------------------------------
+# bf16 rounding against torch's cast
+# --------------------------------------------------------------------------
+def test_bf16_rne_matches_torch(orc):
+    rng = np.random.default_rng(9)
+    vals = np.concatenate([
+        rng.normal(0, 1, 2000).astype(np.float32),
+        rng.normal(0, 1e-30, 200).astype(np.float32),
+        np.array([0.0, -0.0, np.inf, -np.inf, 3.4e38, -3.4e38, 1e-45, 1.0 + 2 ** -8,
+                  1.0 + 3 * 2 ** -8, 1.0 + 2 ** -9], np.float32),
+    ])
+    # exact ties: low 16 bits = 0x8000
+    ties = (rng.integers(0, 2 ** 31, 200, dtype=np.uint32) & 0xFFFF0000 | 0x8000).view(np.float32)
+    ties = ties[np.isfinite(ties)]
+    vals = np.concatenate([vals, ties])
+    want = bf16(vals)
+    got = np.array([oracle.bf16_rne(float(x)) for x in vals], np.uint16)
+    np.testing.assert_array_equal(got, want)
+    assert (oracle.bf16_rne(float("nan")) & 0x7FC0) == 0x7FC0
+
+
+# --------------------------------------------------------------------------
+# Plan: hand-derived layouts and rejections (golden/plan_layouts.json)
+# --------------------------------------------------------------------------
+PLAN_CASES = load("plan_layouts.json")
+
+
+@pytest.mark.parametrize("case", PLAN_CASES["cases"], ids=lambda c: c["name"])
+def test_plan_hand_derived(orc, case):
+    p = oracle.plan(case["numel"], case["owner"], case["world"], case["tp"], case["dp_replicate"],
+                    case["dp_shard"], case["bucket_bytes"])
+    assert p.dp_shard == case["dp_shard_resolved"]
+    for key in ("t_bucket", "t_offset", "b_tag", "b_used", "b_padded", "b_rank_off", "b_state_off"):
+        assert list(getattr(p, key)) == case[key], key
+    assert p.n_rank_pad == case["n_rank_pad"]
+    assert p.n_state_pad == case["n_state_pad"]
+    for b in range(p.n_buckets):
+        assert int(p.b_padded[b]) % (8 * p.dp_shard) == 0
+
+
+@pytest.mark.parametrize("case", PLAN_CASES["rejections"], ids=lambda c: c["why"])
+def test_plan_rejections(orc, case):
+    with pytest.raises(oracle.OracleError) as ei:
+        oracle.plan(case["numel"], case["owner"], case["world"], case["tp"], case["dp_replicate"],
+                    case["dp_shard"], case["bucket_bytes"])
+    assert ei.value.code == case["status"]
+
+
+def test_plan_workload_invariants(orc):
+    """Each tensor sits in exactly one bucket of its own tag, without
+    overlap; LOCAL_SHARD takes numel/tp per rank; buckets respect the byte
+    cap unless they hold a single tensor."""
+    import workloads
+    for cid in workloads.ALL_IDS:
+        w = workloads.get(cid)
+        p = oracle.plan(w.numels, w.owners, w.world, w.tp, w.dp_replicate, w.dp_shard,
+                        w.bucket_bytes)
+        members = {b: [] for b in range(p.n_buckets)}
+        for i, t in enumerate(w.tensors):
+            b = int(p.t_bucket[i])
+            assert int(p.b_tag[b]) == t.owner
+            per_rank = t.numel // w.tp if t.owner == LOCAL_SHARD else t.numel
+            members[b].append((int(p.t_offset[i]), per_rank))
+        for b, segs in members.items():
+            segs.sort()
+            pos = 0
+            for off, n in segs:
+                assert off == pos
+                pos += n
+            assert pos == int(p.b_used[b])
+            if len(segs) > 1:
+                assert 2 * pos <= w.bucket_bytes
+        n_unique = sum(int(p.b_used[b]) * p.copies(b) for b in range(p.n_buckets))
+        assert n_unique == w.n_unique
