@@ -1,0 +1,321 @@
+// C-ABI entry points of libgrs: argument checks ("fail before fitting"),
+// device table upload, stream-ordered launches, device flag readback.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <string>
+
+#include "internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+grs_status fail(grs_status s, const std::string& msg) {
+  g_last_error = msg;
+  return s;
+}
+
+grs_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(GRS_ERR_CUDA, std::string(what) + ": " + cudaGetErrorName(e) + " (" +
+                                cudaGetErrorString(e) + ")");
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Runs the body with the plan's device current, restoring the caller's.
+class DeviceGuard {
+ public:
+  explicit DeviceGuard(int dev) {
+    ok_ = cudaGetDevice(&prev_) == cudaSuccess;
+    if (ok_ && prev_ != dev) {
+      ok_ = cudaSetDevice(dev) == cudaSuccess;
+      switched_ = ok_;
+    }
+  }
+  ~DeviceGuard() {
+    if (switched_) cudaSetDevice(prev_);
+  }
+  bool ok() const { return ok_; }
+
+ private:
+  int prev_ = 0;
+  bool ok_ = false;
+  bool switched_ = false;
+};
+
+grs_status check_plan_device(const grs_plan* p) {
+  if (p == nullptr) return fail(GRS_ERR_INVALID_ARG, "plan is NULL");
+  if (p->device < 0) return fail(GRS_ERR_NO_DEVICE, "plan was created with GRS_PLAN_HOST_ONLY");
+  return GRS_OK;
+}
+
+template <typename T>
+cudaError_t upload(T** dst, const std::vector<T>& src) {
+  const size_t bytes = (src.empty() ? 1 : src.size()) * sizeof(T);
+  cudaError_t e = cudaMalloc(reinterpret_cast<void**>(dst), bytes);
+  if (e != cudaSuccess) return e;
+  if (!src.empty()) e = cudaMemcpy(*dst, src.data(), src.size() * sizeof(T), cudaMemcpyHostToDevice);
+  return e;
+}
+
+void free_device(grs_plan* p) {
+  cudaFree(p->d_units);
+  cudaFree(p->d_red_prefix);
+  cudaFree(p->d_upd_prefix);
+  cudaFree(p->d_jobs);
+  cudaFree(p->d_flags);
+  p->d_units = nullptr;
+  p->d_red_prefix = p->d_upd_prefix = nullptr;
+  p->d_jobs = nullptr;
+  p->d_flags = nullptr;
+}
+
+}  // namespace
+
+extern "C" {
+
+grs_status grs_plan_create(const int64_t* numels, const int32_t* owners, int32_t n_tensors,
+                           int32_t world, int32_t tp, int32_t dp_replicate, int32_t dp_shard,
+                           int64_t bucket_bytes, uint32_t flags, grs_plan** out) {
+  if (out == nullptr) return fail(GRS_ERR_INVALID_ARG, "out is NULL");
+  grs_plan* p = new (std::nothrow) grs_plan();
+  if (p == nullptr) return fail(GRS_ERR_INVALID_ARG, "host allocation failed");
+  std::string why;
+  const grs_status st =
+      grs::build_plan(numels, owners, n_tensors, world, tp, dp_replicate, dp_shard, bucket_bytes, p, &why);
+  if (st != GRS_OK) {
+    delete p;
+    return fail(st, why);
+  }
+  if ((flags & GRS_PLAN_HOST_ONLY) == 0) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p->sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = upload(&p->d_units, p->units);
+    if (e == cudaSuccess) e = upload(&p->d_red_prefix, p->red_prefix);
+    if (e == cudaSuccess) e = upload(&p->d_upd_prefix, p->upd_prefix);
+    if (e == cudaSuccess) e = upload(&p->d_jobs, p->jobs);
+    if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&p->d_flags), grs::FLAG_COUNT * sizeof(int));
+    if (e == cudaSuccess) e = cudaMemset(p->d_flags, 0, grs::FLAG_COUNT * sizeof(int));
+    if (e != cudaSuccess) {
+      free_device(p);
+      delete p;
+      return cuda_fail(e, "grs_plan_create: device tables");
+    }
+    p->device = dev;
+  }
+  *out = p;
+  return GRS_OK;
+}
+
+void grs_plan_destroy(grs_plan* p) {
+  if (p == nullptr) return;
+  if (p->device >= 0) {
+    DeviceGuard g(p->device);
+    free_device(p);
+  }
+  delete p;
+}
+
+grs_status grs_plan_query(const grs_plan* p, grs_plan_info* o) {
+  if (p == nullptr || o == nullptr) return fail(GRS_ERR_INVALID_ARG, "NULL argument");
+  std::memset(o, 0, sizeof(*o));
+  o->n_tensors = static_cast<int32_t>(p->numel.size());
+  o->n_buckets = static_cast<int32_t>(p->buckets.size());
+  o->world = p->world;
+  o->tp = p->tp;
+  o->dp_replicate = p->dp_replicate;
+  o->dp_shard = p->dp_shard;
+  o->dp = p->dp;
+  o->device = p->device;
+  o->n_unique = p->n_unique;
+  o->n_rank_pad = p->n_rank_pad;
+  o->n_state_pad = p->n_state_pad;
+  o->workspace_bytes = p->workspace_bytes;
+  o->n_reduce_tiles = p->n_red_tiles;
+  return GRS_OK;
+}
+
+grs_status grs_bucket_info(const grs_plan* p, int32_t b, grs_bucket_desc* o) {
+  if (p == nullptr || o == nullptr) return fail(GRS_ERR_INVALID_ARG, "NULL argument");
+  if (b < 0 || b >= static_cast<int32_t>(p->buckets.size()))
+    return fail(GRS_ERR_INVALID_ARG, "bucket index out of range");
+  const grs::Bucket& bk = p->buckets[b];
+  std::memset(o, 0, sizeof(*o));
+  o->tag = bk.tag;
+  o->copies = bk.copies;
+  o->group_size = bk.group_size;
+  o->n_tensors = bk.n_tensors;
+  o->used = bk.used;
+  o->padded = bk.padded;
+  o->shard_len = bk.shard_len;
+  o->rank_offset = bk.rank_off;
+  o->state_offset = bk.state_off;
+  return GRS_OK;
+}
+
+grs_status grs_tensor_info(const grs_plan* p, int32_t i, grs_tensor_desc* o) {
+  if (p == nullptr || o == nullptr) return fail(GRS_ERR_INVALID_ARG, "NULL argument");
+  if (i < 0 || i >= static_cast<int32_t>(p->numel.size()))
+    return fail(GRS_ERR_INVALID_ARG, "tensor index out of range");
+  std::memset(o, 0, sizeof(*o));
+  o->bucket = p->t_bucket[i];
+  o->owner = p->owner[i];
+  o->numel = p->numel[i];
+  o->per_rank = (p->owner[i] == GRS_LOCAL_SHARD) ? p->numel[i] / p->tp : p->numel[i];
+  o->bucket_offset = p->t_offset[i];
+  return GRS_OK;
+}
+
+static grs_status reduce_common(const grs_plan* p, const uint16_t* const* rank_grads, float* acc,
+                                int32_t accumulate, int32_t emit, void* workspace, void* stream,
+                                int32_t unit_begin, int32_t unit_end, int64_t state_base,
+                                int64_t rank_base, int32_t tag, const char* who) {
+  if (rank_grads == nullptr || acc == nullptr)
+    return fail(GRS_ERR_INVALID_ARG, std::string(who) + ": rank_grads/acc is NULL");
+  if (emit && workspace == nullptr)
+    return fail(GRS_ERR_INVALID_ARG, std::string(who) + ": emit_norm_partials needs a workspace");
+  if (!aligned16(acc) || (workspace != nullptr && !aligned16(workspace)))
+    return fail(GRS_ERR_ALIGNMENT, std::string(who) + ": acc/workspace not 16-byte aligned");
+  // Ranks actually read: every rank, or rank 0 only for an ALREADY_REDUCED bucket.
+  const int32_t nread = (tag == GRS_ALREADY_REDUCED) ? 1 : p->world;
+  for (int32_t k = 0; k < nread; ++k) {
+    if (rank_grads[k] == nullptr)
+      return fail(GRS_ERR_INVALID_ARG, std::string(who) + ": rank " + std::to_string(k) + " buffer is NULL");
+    if (!aligned16(rank_grads[k]))
+      return fail(GRS_ERR_ALIGNMENT, std::string(who) + ": rank " + std::to_string(k) +
+                                         " buffer not 16-byte aligned");
+  }
+  DeviceGuard g(p->device);
+  if (!g.ok()) return fail(GRS_ERR_CUDA, std::string(who) + ": cannot select the plan's device");
+  grs::ReduceLaunch l;
+  const uint16_t* ranks[GRS_MAX_WORLD] = {};
+  for (int32_t k = 0; k < p->world; ++k) ranks[k] = (k < nread) ? rank_grads[k] : rank_grads[0];
+  l.ranks = ranks;
+  l.acc = acc;
+  l.partials = emit ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + grs::ws_partials_offset())
+                    : nullptr;
+  l.unit_begin = unit_begin;
+  l.unit_end = unit_end;
+  l.state_base = state_base;
+  l.rank_base = rank_base;
+  l.accumulate = accumulate ? 1 : 0;
+  const int e = grs::launch_reduce(p, l, stream);
+  if (e != 0) return cuda_fail(static_cast<cudaError_t>(e), who);
+  return GRS_OK;
+}
+
+grs_status grs_reduce_bucket(const grs_plan* p, int32_t b, const uint16_t* const* rank_grads, float* acc,
+                             int32_t accumulate, int32_t emit, void* workspace, void* stream) {
+  grs_status st = check_plan_device(p);
+  if (st != GRS_OK) return st;
+  if (b < 0 || b >= static_cast<int32_t>(p->buckets.size()))
+    return fail(GRS_ERR_INVALID_ARG, "grs_reduce_bucket: bucket index out of range");
+  const grs::Bucket& bk = p->buckets[b];
+  return reduce_common(p, rank_grads, acc, accumulate, emit, workspace, stream, bk.unit0,
+                       bk.unit0 + bk.copies, bk.state_off, bk.rank_off, bk.tag, "grs_reduce_bucket");
+}
+
+grs_status grs_reduce_all(const grs_plan* p, const uint16_t* const* rank_grads, float* acc,
+                          int32_t accumulate, int32_t emit, void* workspace, void* stream) {
+  grs_status st = check_plan_device(p);
+  if (st != GRS_OK) return st;
+  bool only_ar = true;
+  for (const auto& bk : p->buckets) only_ar = only_ar && bk.tag == GRS_ALREADY_REDUCED;
+  return reduce_common(p, rank_grads, acc, accumulate, emit, workspace, stream, 0,
+                       static_cast<int32_t>(p->units.size()), 0, 0,
+                       only_ar ? GRS_ALREADY_REDUCED : GRS_REPLICA_AVG, "grs_reduce_all");
+}
+
+grs_status grs_accumulate(const grs_plan* p, int32_t b, float* acc, const float* mb, void* stream) {
+  grs_status st = check_plan_device(p);
+  if (st != GRS_OK) return st;
+  if (b < 0 || b >= static_cast<int32_t>(p->buckets.size()))
+    return fail(GRS_ERR_INVALID_ARG, "grs_accumulate: bucket index out of range");
+  if (acc == nullptr || mb == nullptr) return fail(GRS_ERR_INVALID_ARG, "grs_accumulate: NULL buffer");
+  if (!aligned16(acc) || !aligned16(mb)) return fail(GRS_ERR_ALIGNMENT, "grs_accumulate: not 16-byte aligned");
+  DeviceGuard g(p->device);
+  if (!g.ok()) return fail(GRS_ERR_CUDA, "grs_accumulate: cannot select the plan's device");
+  const int e = grs::launch_accumulate(p, b, acc, mb, stream);
+  if (e != 0) return cuda_fail(static_cast<cudaError_t>(e), "grs_accumulate");
+  return GRS_OK;
+}
+
+grs_status grs_grad_norm_sq(const grs_plan* p, const float* acc, int32_t n_micro, void* workspace,
+                            int32_t partials_ready, double* d_norm_sq, void* stream) {
+  grs_status st = check_plan_device(p);
+  if (st != GRS_OK) return st;
+  if (workspace == nullptr || d_norm_sq == nullptr || (!partials_ready && acc == nullptr))
+    return fail(GRS_ERR_INVALID_ARG, "grs_grad_norm_sq: NULL argument");
+  if (n_micro < 1) return fail(GRS_ERR_INVALID_ARG, "grs_grad_norm_sq: n_micro must be >= 1");
+  if (!aligned16(workspace) || (acc != nullptr && !aligned16(acc)) ||
+      (reinterpret_cast<uintptr_t>(d_norm_sq) & 7u) != 0)
+    return fail(GRS_ERR_ALIGNMENT, "grs_grad_norm_sq: misaligned pointer");
+  DeviceGuard g(p->device);
+  if (!g.ok()) return fail(GRS_ERR_CUDA, "grs_grad_norm_sq: cannot select the plan's device");
+  const int e = grs::launch_norm(p, acc, n_micro, workspace, partials_ready, d_norm_sq, stream);
+  if (e != 0) return cuda_fail(static_cast<cudaError_t>(e), "grs_grad_norm_sq");
+  return GRS_OK;
+}
+
+grs_status grs_clip_adamw_step(const grs_plan* p, const grs_adamw* hp, const double* d_norm_sq,
+                               const float* acc, float* master, float* m, float* v,
+                               uint16_t* params_bf16, void* stream) {
+  grs_status st = check_plan_device(p);
+  if (st != GRS_OK) return st;
+  if (hp == nullptr || acc == nullptr || master == nullptr || m == nullptr || v == nullptr ||
+      params_bf16 == nullptr)
+    return fail(GRS_ERR_INVALID_ARG, "grs_clip_adamw_step: NULL argument");
+  if (hp->step < 1 || hp->n_micro < 1)
+    return fail(GRS_ERR_INVALID_ARG, "grs_clip_adamw_step: step and n_micro must be >= 1");
+  if (hp->max_norm > 0.0f && d_norm_sq == nullptr)
+    return fail(GRS_ERR_INVALID_ARG, "grs_clip_adamw_step: clipping needs d_norm_sq");
+  if (!aligned16(acc) || !aligned16(master) || !aligned16(m) || !aligned16(v) || !aligned16(params_bf16))
+    return fail(GRS_ERR_ALIGNMENT, "grs_clip_adamw_step: buffer not 16-byte aligned");
+  DeviceGuard g(p->device);
+  if (!g.ok()) return fail(GRS_ERR_CUDA, "grs_clip_adamw_step: cannot select the plan's device");
+  const int e = grs::launch_update(p, hp, d_norm_sq, acc, master, m, v, params_bf16, stream);
+  if (e != 0) return cuda_fail(static_cast<cudaError_t>(e), "grs_clip_adamw_step");
+  return GRS_OK;
+}
+
+grs_status grs_gather_params(const grs_plan* p, const uint16_t* params_bf16, uint16_t* const* tensor_ptrs,
+                             void* stream) {
+  grs_status st = check_plan_device(p);
+  if (st != GRS_OK) return st;
+  if (params_bf16 == nullptr || tensor_ptrs == nullptr)
+    return fail(GRS_ERR_INVALID_ARG, "grs_gather_params: NULL argument");
+  if (!aligned16(params_bf16)) return fail(GRS_ERR_ALIGNMENT, "grs_gather_params: params not 16-byte aligned");
+  for (size_t i = 0; i < p->numel.size(); ++i)
+    if (tensor_ptrs[i] != nullptr && (reinterpret_cast<uintptr_t>(tensor_ptrs[i]) & 1u) != 0)
+      return fail(GRS_ERR_ALIGNMENT, "grs_gather_params: tensor pointer not 2-byte aligned");
+  DeviceGuard g(p->device);
+  if (!g.ok()) return fail(GRS_ERR_CUDA, "grs_gather_params: cannot select the plan's device");
+  const int e = grs::launch_gather(p, params_bf16, tensor_ptrs, stream);
+  if (e != 0) return cuda_fail(static_cast<cudaError_t>(e), "grs_gather_params");
+  return GRS_OK;
+}
+
+grs_status grs_check_device_errors(const grs_plan* p, void* stream) {
+  grs_status st = check_plan_device(p);
+  if (st != GRS_OK) return st;
+  DeviceGuard g(p->device);
+  if (!g.ok()) return fail(GRS_ERR_CUDA, "grs_check_device_errors: cannot select the plan's device");
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "grs_check_device_errors: stream");
+  int h[grs::FLAG_COUNT] = {};
+  e = cudaMemcpy(h, p->d_flags, sizeof(h), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "grs_check_device_errors: flags");
+  e = cudaMemset(p->d_flags, 0, sizeof(h));
+  if (e != cudaSuccess) return cuda_fail(e, "grs_check_device_errors: clear flags");
+  if (h[grs::FLAG_TIMEOUT]) return fail(GRS_ERR_TIMEOUT, "a bounded device wait timed out");
+  if (h[grs::FLAG_NONFINITE]) return fail(GRS_ERR_NONFINITE, "global gradient norm is not finite");
+  return GRS_OK;
+}
+
+const char* grs_last_error(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

@@ -1,0 +1,162 @@
+// Device helpers for sm_103a: mbarriers with bounded waits, 1-D bulk TMA
+// copies, bf16 unpacking, flags.  Inline PTX written for this library.
+#pragma once
+
+#include <cstdint>
+
+#include "internal.h"
+
+namespace grs {
+
+// A device wait gives up after this long and raises FLAG_TIMEOUT.
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait until the phase with `parity` has completed.  Gives up (returns
+// false, raises FLAG_TIMEOUT) after WAIT_LIMIT_NS or when *abort is set by
+// another thread of the block.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int* flags,
+                                                  volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (global_ns() - t0 > WAIT_LIMIT_NS) {
+      atomicOr(flags + FLAG_TIMEOUT, 1);
+      *abort = 1;
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// 1-D bulk copy global -> shared, completion counted on `bar` in bytes.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1], %2, [%3];" ::"r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(const void* p) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(smem_addr(p)));
+  return v;
+}
+
+// bf16 pair in one 32-bit word -> two floats (exact: bf16 is the high half
+// of binary32).
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ void add_bf16x8(float (&a)[8], const uint4& w) {
+  a[0] = __fadd_rn(a[0], bf16_lo(w.x));
+  a[1] = __fadd_rn(a[1], bf16_hi(w.x));
+  a[2] = __fadd_rn(a[2], bf16_lo(w.y));
+  a[3] = __fadd_rn(a[3], bf16_hi(w.y));
+  a[4] = __fadd_rn(a[4], bf16_lo(w.z));
+  a[5] = __fadd_rn(a[5], bf16_hi(w.z));
+  a[6] = __fadd_rn(a[6], bf16_lo(w.w));
+  a[7] = __fadd_rn(a[7], bf16_hi(w.w));
+}
+
+__device__ __forceinline__ void set_bf16x8(float (&a)[8], const uint4& w) {
+  a[0] = bf16_lo(w.x);
+  a[1] = bf16_hi(w.x);
+  a[2] = bf16_lo(w.y);
+  a[3] = bf16_hi(w.y);
+  a[4] = bf16_lo(w.z);
+  a[5] = bf16_hi(w.z);
+  a[6] = bf16_lo(w.w);
+  a[7] = bf16_hi(w.w);
+}
+
+// Last unit u with prefix[u] <= tile (prefix has n_units + 1 entries).
+__device__ __forceinline__ int find_unit(const int64_t* __restrict__ prefix, int lo, int hi,
+                                         int64_t tile) {
+  // invariant: prefix[lo] <= tile < prefix[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(prefix + mid) <= tile)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  return lo;
+}
+
+// Sum over the warp with a fixed butterfly (every lane gets the result).
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = __fadd_rn(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+
+__device__ __forceinline__ double warp_sum(double x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = __dadd_rn(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+
+}  // namespace grs

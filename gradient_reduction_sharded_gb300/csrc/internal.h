@@ -1,0 +1,129 @@
+// Internal types shared by the host plan builder, the C-ABI layer and the
+// CUDA launchers of libgrs.  Not part of the public interface.
+#pragma once
+
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "grs.h"
+
+namespace grs {
+
+// Reduction tiles: a tile carries STAGE_GRAD_BYTES of bf16 input (all the
+// group's rank rows for T elements), so T = STAGE_GRAD_BYTES / (2 * group),
+// capped at RED_MAX_T and a multiple of 8.
+constexpr int64_t STAGE_GRAD_BYTES = 32768;
+constexpr int64_t RED_MAX_T = 4096;
+// Update (clip + AdamW) and accumulate tiles.
+constexpr int64_t UPD_T = 2048;
+
+// One "unit" is one state row of one bucket: bucket b, tp row t.
+struct UnitDesc {
+  int64_t state_off;  // first element in the state arrays
+  int64_t rank_off;   // first element in each rank's gradient buffer
+  int64_t padded;     // P: elements of the row (multiple of 8)
+  int64_t used;       // valid elements; [used, padded) is padding
+  int64_t red_tile0;  // first global reduction tile
+  int64_t upd_tile0;  // first global update tile
+  int32_t red_T;      // elements per reduction tile
+  int32_t g_start;    // group ranks: g_start + i * g_stride, i < g_count
+  int32_t g_stride;
+  int32_t g_count;
+  float scale;        // 1/R, 1/dp or 1 by tag
+  int32_t bucket;
+};
+static_assert(sizeof(UnitDesc) == 72, "UnitDesc layout");
+
+struct Bucket {
+  int32_t tag = 0;
+  int32_t copies = 1;
+  int32_t group_size = 1;
+  int32_t n_tensors = 0;
+  int64_t used = 0;
+  int64_t padded = 0;
+  int64_t shard_len = 0;
+  int64_t rank_off = 0;
+  int64_t state_off = 0;
+  int32_t unit0 = 0;  // first unit of the bucket (copies consecutive units)
+};
+
+// Segmented-copy job of the gather: `len` elements from state offset
+// `src` to element `dst` of tensor `tensor`.
+struct GatherJob {
+  int64_t src;
+  int64_t dst;
+  int64_t len;
+  int64_t chunk0;  // first global chunk of this job
+  int32_t tensor;
+  int32_t pad_;
+};
+constexpr int64_t GATHER_CHUNK = 8192;
+
+}  // namespace grs
+
+struct grs_plan {
+  // inputs
+  std::vector<int64_t> numel;
+  std::vector<int32_t> owner;
+  int32_t world = 0, tp = 0, dp_replicate = 0, dp_shard = 0, dp = 0;
+  int64_t bucket_bytes = 0;
+  // layout
+  std::vector<int32_t> t_bucket;
+  std::vector<int64_t> t_offset;
+  std::vector<grs::Bucket> buckets;
+  std::vector<grs::UnitDesc> units;
+  std::vector<int64_t> red_prefix;  // [n_units + 1] first reduction tile per unit
+  std::vector<int64_t> upd_prefix;  // [n_units + 1] first update tile per unit
+  std::vector<grs::GatherJob> jobs; // by tensor, LOCAL_SHARD: tp jobs
+  std::vector<int32_t> tensor_job0; // [n_tensors + 1]
+  int64_t n_unique = 0, n_rank_pad = 0, n_state_pad = 0;
+  int64_t n_red_tiles = 0, n_upd_tiles = 0, n_gather_chunks = 0;
+  int64_t workspace_bytes = 0;
+  // device side (absent for host-only plans)
+  int device = -1;
+  int sm_count = 0;
+  grs::UnitDesc* d_units = nullptr;
+  int64_t* d_red_prefix = nullptr;
+  int64_t* d_upd_prefix = nullptr;
+  grs::GatherJob* d_jobs = nullptr;
+  int* d_flags = nullptr;  // [4]: timeout, nonfinite, reserved
+};
+
+namespace grs {
+
+// Workspace layout: [n_red_tiles floats: per-tile partial sums of acc^2]
+//                   [NORM_L2_BLOCKS doubles: second-level partials]
+constexpr int NORM_L2_BLOCKS = 128;
+inline int64_t ws_partials_offset() { return 0; }
+inline int64_t ws_level2_offset(int64_t n_red_tiles) {
+  return ((n_red_tiles * 4 + 255) / 256) * 256;
+}
+
+// Device flags
+enum : int { FLAG_TIMEOUT = 0, FLAG_NONFINITE = 1, FLAG_COUNT = 4 };
+
+// host plan builder (plan.cpp)
+grs_status build_plan(const int64_t* numels, const int32_t* owners, int32_t n, int32_t world,
+                      int32_t tp, int32_t dp_replicate, int32_t dp_shard, int64_t bucket_bytes,
+                      grs_plan* p, std::string* why);
+
+// launchers (kernels_*.cu); all return cudaGetLastError() as int
+struct ReduceLaunch {
+  const uint16_t* const* ranks;  // host array [world]
+  float* acc;
+  float* partials;  // nullptr: no norm epilogue
+  int32_t unit_begin, unit_end;
+  int64_t state_base, rank_base;
+  int32_t accumulate;
+};
+int launch_reduce(const grs_plan* p, const ReduceLaunch& a, void* stream);
+int launch_norm(const grs_plan* p, const float* acc, int32_t n_micro, void* workspace,
+                int32_t partials_ready, double* d_norm_sq, void* stream);
+int launch_update(const grs_plan* p, const grs_adamw* hp, const double* d_norm_sq, const float* acc,
+                  float* master, float* m, float* v, uint16_t* params, void* stream);
+int launch_accumulate(const grs_plan* p, int32_t bucket, float* acc, const float* mb, void* stream);
+int launch_gather(const grs_plan* p, const uint16_t* params, uint16_t* const* tensor_ptrs,
+                  void* stream);
+
+}  // namespace grs

@@ -1,0 +1,112 @@
+// Gather of bf16 parameters from the bucket-ordered full-parameter buffer
+// back into per-tensor storage ("Cosmos 3 ... distributed parallelism",
+// section 2: parameters are all-gathered across shards for the forward;
+// LOCAL_SHARD tensors are reassembled from their tp rows in dim-0 order).
+//
+// A segmented copy: the plan holds one job per (tensor, state row); each
+// block copies one GATHER_CHUNK slice of one job.  Tensors are packed back
+// to back inside buckets, so source and destination alignments differ per
+// job: when both are 16-byte co-aligned the body moves 16-byte vectors,
+// otherwise 4-byte or 2-byte words.
+#include <cuda_runtime.h>
+
+#include "device.cuh"
+#include "internal.h"
+
+namespace grs {
+
+namespace {
+
+constexpr int GATHER_THREADS = 256;
+constexpr int GATHER_MAX_PTRS = 256;  // tensor pointers per launch (2 KB of parameters)
+
+struct GatherArgs {
+  uint16_t* dst[GATHER_MAX_PTRS];
+  const uint16_t* params;
+  const GatherJob* jobs;
+  int32_t tensor_begin;  // dst[0] is this tensor
+  int32_t job_begin, job_end;
+  int64_t chunk_begin;
+};
+
+__device__ __forceinline__ int find_job(const GatherJob* jobs, int lo, int hi, int64_t chunk) {
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (jobs[mid].chunk0 <= chunk)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  return lo;
+}
+
+__global__ void __launch_bounds__(GATHER_THREADS) gather_kernel(const __grid_constant__ GatherArgs a) {
+  const int64_t chunk = a.chunk_begin + blockIdx.x;
+  const int j = find_job(a.jobs, a.job_begin, a.job_end, chunk);
+  const GatherJob jb = a.jobs[j];
+  uint16_t* dbase = a.dst[jb.tensor - a.tensor_begin];
+  if (dbase == nullptr) return;
+  const int64_t off = (chunk - jb.chunk0) * GATHER_CHUNK;
+  const int64_t rem = jb.len - off;
+  const int64_t n = rem < GATHER_CHUNK ? rem : GATHER_CHUNK;
+  const uint16_t* src = a.params + jb.src + off;
+  uint16_t* dst = dbase + jb.dst + off;
+  const uintptr_t sa = reinterpret_cast<uintptr_t>(src);
+  const uintptr_t da = reinterpret_cast<uintptr_t>(dst);
+  if (((sa ^ da) & 15) == 0) {
+    // head up to a 16-byte boundary, 16-byte body, tail
+    const int64_t head = static_cast<int64_t>(((16 - (sa & 15)) & 15) >> 1) < n
+                             ? static_cast<int64_t>(((16 - (sa & 15)) & 15) >> 1)
+                             : n;
+    for (int64_t i = threadIdx.x; i < head; i += GATHER_THREADS) dst[i] = src[i];
+    const int64_t nv = (n - head) >> 3;
+    const uint4* s4 = reinterpret_cast<const uint4*>(src + head);
+    uint4* d4 = reinterpret_cast<uint4*>(dst + head);
+    for (int64_t i = threadIdx.x; i < nv; i += GATHER_THREADS) d4[i] = __ldcs(s4 + i);
+    for (int64_t i = head + nv * 8 + threadIdx.x; i < n; i += GATHER_THREADS) dst[i] = src[i];
+  } else if (((sa ^ da) & 3) == 0) {
+    const int64_t head = ((sa & 3) != 0 && n > 0) ? 1 : 0;
+    if (threadIdx.x == 0 && head) dst[0] = src[0];
+    const int64_t nw = (n - head) >> 1;
+    const uint32_t* s2 = reinterpret_cast<const uint32_t*>(src + head);
+    uint32_t* d2 = reinterpret_cast<uint32_t*>(dst + head);
+    for (int64_t i = threadIdx.x; i < nw; i += GATHER_THREADS) d2[i] = s2[i];
+    if (threadIdx.x == 0 && head + nw * 2 < n) dst[n - 1] = src[n - 1];
+  } else {
+    for (int64_t i = threadIdx.x; i < n; i += GATHER_THREADS) dst[i] = src[i];
+  }
+}
+
+}  // namespace
+
+int launch_gather(const grs_plan* p, const uint16_t* params, uint16_t* const* tensor_ptrs,
+                  void* stream) {
+  const int32_t n = static_cast<int32_t>(p->numel.size());
+  for (int32_t t0 = 0; t0 < n; t0 += GATHER_MAX_PTRS) {
+    const int32_t t1 = t0 + GATHER_MAX_PTRS < n ? t0 + GATHER_MAX_PTRS : n;
+    GatherArgs a;
+    bool any = false;
+    for (int32_t i = 0; i < GATHER_MAX_PTRS; ++i) {
+      a.dst[i] = (t0 + i < t1) ? tensor_ptrs[t0 + i] : nullptr;
+      any = any || a.dst[i] != nullptr;
+    }
+    if (!any) continue;
+    a.params = params;
+    a.jobs = p->d_jobs;
+    a.tensor_begin = t0;
+    a.job_begin = p->tensor_job0[t0];
+    a.job_end = p->tensor_job0[t1];
+    if (a.job_end <= a.job_begin) continue;
+    a.chunk_begin = p->jobs[a.job_begin].chunk0;
+    const int64_t chunk_end =
+        a.job_end < static_cast<int32_t>(p->jobs.size()) ? p->jobs[a.job_end].chunk0 : p->n_gather_chunks;
+    if (chunk_end <= a.chunk_begin) continue;
+    gather_kernel<<<static_cast<unsigned>(chunk_end - a.chunk_begin), GATHER_THREADS, 0,
+                    static_cast<cudaStream_t>(stream)>>>(a);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return static_cast<int>(e);
+  }
+  return 0;
+}
+
+}  // namespace grs

@@ -1,0 +1,269 @@
+// Owner-tagged reduction of R simulated ranks' bf16 gradients into an fp32
+// accumulator, with the reduce-scatter's shard layout, microbatch
+// accumulation and an optional fused norm epilogue.
+//
+// What it computes ("refactor(distributed): establish shared native TP
+// replica ownership", "Why this needs separate work" and "Preserved
+// prototype and evidence" — FP32 reduction of BF16 gradients): for each
+// element e of a state row,
+//     acc[e] (= | +=) scale * sum_{k in group, ascending} float(g_k[e])
+// and, on the last microbatch, per-tile partial sums of acc^2 for the
+// global norm.
+//
+// How (GB300): a persistent grid, one CTA per SM.  Warp 0 is a TMA producer:
+// for every tile it issues one 1-D bulk copy (cp.async.bulk) per rank row of
+// the tile's reduction group, plus the old accumulator tile when
+// accumulating, into a 4-stage shared-memory ring guarded by mbarriers.
+// Warps 1..4 consume a stage: 16-byte shared loads of 8 bf16 per rank,
+// fp32 adds in rank order, scale (and fused add of the old value), padding
+// masked to zero, coalesced 16-byte stores, and a fixed-order warp
+// butterfly for the norm partial.  The producer folds the four warp
+// partials of a tile into one fp32 value in fixed order when the stage is
+// recycled, so the partial of a tile never depends on the grid size.
+// All mbarrier waits are bounded (device.cuh).
+#include <cuda_runtime.h>
+
+#include "device.cuh"
+#include "internal.h"
+
+namespace grs {
+
+namespace {
+
+constexpr int RED_CWARPS = 4;
+constexpr int RED_CTHREADS = 32 * RED_CWARPS;
+constexpr int RED_THREADS = 32 + RED_CTHREADS;
+constexpr int RED_STAGES = 4;
+constexpr int RED_STAGE_BYTES = static_cast<int>(STAGE_GRAD_BYTES + RED_MAX_T * 4);
+
+struct StageMeta {
+  int64_t tile;
+  int64_t e0;
+  int32_t unit;
+  int32_t n;
+};
+
+constexpr size_t RED_SMEM_BYTES = size_t(RED_STAGES) * RED_STAGE_BYTES  // ring
+                                  + 2 * RED_STAGES * sizeof(uint64_t)    // full/empty barriers
+                                  + RED_STAGES * sizeof(StageMeta)       // tile of each stage
+                                  + RED_STAGES * RED_CWARPS * sizeof(float)  // warp partials
+                                  + 16;                                   // abort flag
+
+struct ReduceArgs {
+  const uint16_t* ranks[GRS_MAX_WORLD];
+  float* acc;
+  float* partials;
+  const UnitDesc* units;
+  const int64_t* prefix;
+  int* flags;
+  int64_t state_base;
+  int64_t rank_base;
+  int64_t tile_begin;
+  int64_t tile_end;
+  int32_t unit_begin;
+  int32_t unit_end;
+  int32_t accumulate;
+};
+
+__device__ __forceinline__ float fold_partials(const float* wp) {
+  float s = wp[0];
+#pragma unroll
+  for (int w = 1; w < RED_CWARPS; ++w) s = __fadd_rn(s, wp[w]);
+  return s;
+}
+
+__global__ void __launch_bounds__(RED_THREADS, 1) reduce_kernel(const __grid_constant__ ReduceArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* ring = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(RED_STAGES) * RED_STAGE_BYTES);
+  uint64_t* empty = full + RED_STAGES;
+  StageMeta* meta = reinterpret_cast<StageMeta*>(empty + RED_STAGES);
+  float* wp = reinterpret_cast<float*>(meta + RED_STAGES);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(wp + RED_STAGES * RED_CWARPS);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < RED_STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], RED_CWARPS);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  const int64_t stride = gridDim.x;
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    const uint64_t pol = l2_policy_evict_first();
+    int64_t iter = 0;
+    bool ok = true;
+    for (int64_t tile = a.tile_begin + blockIdx.x; tile < a.tile_end; tile += stride, ++iter) {
+      const int s = static_cast<int>(iter % RED_STAGES);
+      const uint32_t ph = static_cast<uint32_t>((iter / RED_STAGES) & 1);
+      int good = 1;
+      if (lane == 0) good = mbar_wait_bounded(&empty[s], ph ^ 1u, a.flags, abort_flag) ? 1 : 0;
+      good = __shfl_sync(0xffffffffu, good, 0);
+      if (!good) {
+        ok = false;
+        break;
+      }
+      if (lane == 0 && a.partials != nullptr && iter >= RED_STAGES)
+        a.partials[meta[s].tile] = fold_partials(wp + s * RED_CWARPS);
+      const int u = find_unit(a.prefix, a.unit_begin, a.unit_end, tile);
+      const UnitDesc* ud = a.units + u;
+      const int64_t T = ud->red_T;
+      const int64_t e0 = (tile - ud->red_tile0) * T;
+      const int64_t rem = ud->padded - e0;
+      const int32_t n = static_cast<int32_t>(rem < T ? rem : T);
+      const int32_t gc = ud->g_count;
+      const int32_t gs = ud->g_start;
+      const int32_t gst = ud->g_stride;
+      const uint32_t grad_bytes = static_cast<uint32_t>(gc) * static_cast<uint32_t>(n) * 2u;
+      const uint32_t bytes = grad_bytes + (a.accumulate ? static_cast<uint32_t>(n) * 4u : 0u);
+      uint8_t* st = ring + size_t(s) * RED_STAGE_BYTES;
+      if (lane == 0) {
+        meta[s].tile = tile;
+        meta[s].e0 = e0;
+        meta[s].unit = u;
+        meta[s].n = n;
+        mbar_arrive_expect_tx(&full[s], bytes);
+      }
+      __syncwarp();
+      const int64_t roff = ud->rank_off - a.rank_base + e0;
+      for (int i = lane; i < gc; i += 32)
+        bulk_g2s(st + size_t(i) * n * 2, a.ranks[gs + i * gst] + roff, static_cast<uint32_t>(n) * 2u,
+                 &full[s], pol);
+      if (a.accumulate && lane == 0)
+        bulk_g2s(st + grad_bytes, a.acc + (ud->state_off - a.state_base) + e0,
+                 static_cast<uint32_t>(n) * 4u, &full[s]);
+    }
+    if (lane == 0) {
+      const int64_t first = iter > RED_STAGES ? iter - RED_STAGES : 0;
+      if (ok) {
+        // Drain: the last stages' partials become final once consumers release them.
+        for (int64_t k = first; k < iter; ++k) {
+          const int s = static_cast<int>(k % RED_STAGES);
+          if (!mbar_wait_bounded(&empty[s], static_cast<uint32_t>((k / RED_STAGES) & 1), a.flags,
+                                 abort_flag))
+            break;
+          if (a.partials != nullptr) a.partials[meta[s].tile] = fold_partials(wp + s * RED_CWARPS);
+        }
+      }
+      if (*abort_flag) {
+        // Let every copy this CTA issued land before the CTA exits.
+        volatile int no_abort = 0;
+        for (int64_t k = first; k < iter; ++k) {
+          const int s = static_cast<int>(k % RED_STAGES);
+          if (!mbar_wait_bounded(&full[s], static_cast<uint32_t>((k / RED_STAGES) & 1), a.flags,
+                                 &no_abort))
+            break;
+        }
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- consumers
+    const int ct = threadIdx.x - 32;
+    const int cw = ct >> 5;
+    int64_t iter = 0;
+    for (int64_t tile = a.tile_begin + blockIdx.x; tile < a.tile_end; tile += stride, ++iter) {
+      const int s = static_cast<int>(iter % RED_STAGES);
+      const uint32_t ph = static_cast<uint32_t>((iter / RED_STAGES) & 1);
+      if (!mbar_wait_bounded(&full[s], ph, a.flags, abort_flag)) break;
+      const StageMeta md = meta[s];
+      const UnitDesc* ud = a.units + md.unit;
+      const float scale = ud->scale;
+      const int64_t used = ud->used;
+      const int32_t gc = ud->g_count;
+      const int32_t n = md.n;
+      float* out = a.acc + (ud->state_off - a.state_base) + md.e0;
+      const uint8_t* st = ring + size_t(s) * RED_STAGE_BYTES;
+      const size_t row = size_t(n) * 2;
+      const float* old = reinterpret_cast<const float*>(st + size_t(gc) * row);
+      float psum = 0.0f;
+      for (int c = ct; c < (n >> 3); c += RED_CTHREADS) {
+        const uint8_t* p = st + size_t(c) * 16;
+        float v[8];
+        set_bf16x8(v, lds128(p));
+        int i = 1;
+        for (; i + 3 < gc; i += 4) {
+          const uint4 w0 = lds128(p + (i + 0) * row);
+          const uint4 w1 = lds128(p + (i + 1) * row);
+          const uint4 w2 = lds128(p + (i + 2) * row);
+          const uint4 w3 = lds128(p + (i + 3) * row);
+          add_bf16x8(v, w0);
+          add_bf16x8(v, w1);
+          add_bf16x8(v, w2);
+          add_bf16x8(v, w3);
+        }
+        for (; i < gc; ++i) add_bf16x8(v, lds128(p + i * row));
+        float o[8];
+        if (a.accumulate) {
+          const uint4 q0 = lds128(old + c * 8);
+          const uint4 q1 = lds128(old + c * 8 + 4);
+          const float ov[8] = {__uint_as_float(q0.x), __uint_as_float(q0.y), __uint_as_float(q0.z),
+                               __uint_as_float(q0.w), __uint_as_float(q1.x), __uint_as_float(q1.y),
+                               __uint_as_float(q1.z), __uint_as_float(q1.w)};
+#pragma unroll
+          for (int q = 0; q < 8; ++q) o[q] = __fmaf_rn(v[q], scale, ov[q]);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) o[q] = __fmul_rn(v[q], scale);
+        }
+        const int64_t e = md.e0 + int64_t(c) * 8;
+        if (e + 8 > used) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            if (e + q >= used) o[q] = 0.0f;
+        }
+        float4* o4 = reinterpret_cast<float4*>(out + int64_t(c) * 8);
+        o4[0] = make_float4(o[0], o[1], o[2], o[3]);
+        o4[1] = make_float4(o[4], o[5], o[6], o[7]);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) psum = __fmaf_rn(o[q], o[q], psum);
+      }
+      if (a.partials != nullptr) {
+        psum = warp_sum(psum);
+        if (lane == 0) wp[s * RED_CWARPS + cw] = psum;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+  }
+}
+
+bool g_attr_set[64] = {};
+
+}  // namespace
+
+int launch_reduce(const grs_plan* p, const ReduceLaunch& l, void* stream) {
+  ReduceArgs a;
+  for (int k = 0; k < GRS_MAX_WORLD; ++k) a.ranks[k] = k < p->world ? l.ranks[k] : nullptr;
+  a.acc = l.acc;
+  a.partials = l.partials;
+  a.units = p->d_units;
+  a.prefix = p->d_red_prefix;
+  a.flags = p->d_flags;
+  a.state_base = l.state_base;
+  a.rank_base = l.rank_base;
+  a.unit_begin = l.unit_begin;
+  a.unit_end = l.unit_end;
+  a.tile_begin = p->red_prefix[l.unit_begin];
+  a.tile_end = p->red_prefix[l.unit_end];
+  a.accumulate = l.accumulate;
+  const int64_t tiles = a.tile_end - a.tile_begin;
+  if (tiles <= 0) return 0;
+  if (p->device >= 0 && p->device < 64 && !g_attr_set[p->device]) {
+    cudaError_t e = cudaFuncSetAttribute(reduce_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(RED_SMEM_BYTES));
+    if (e != cudaSuccess) return static_cast<int>(e);
+    g_attr_set[p->device] = true;
+  }
+  const int64_t grid = tiles < p->sm_count ? tiles : p->sm_count;
+  reduce_kernel<<<static_cast<unsigned>(grid), RED_THREADS, RED_SMEM_BYTES,
+                  static_cast<cudaStream_t>(stream)>>>(a);
+  return static_cast<int>(cudaGetLastError());
+}
+
+}  // namespace grs

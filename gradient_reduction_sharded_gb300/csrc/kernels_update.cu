@@ -1,0 +1,286 @@
+// Global norm (deterministic, two levels), fused clip + AdamW + bf16 cast,
+// and the fp32 accumulate kernel.
+//
+// Norm ("refactor(distributed): establish shared native TP replica
+// ownership", "Proposed scope": global norms and clipping): per-tile fp32
+// partial sums of acc^2 (written by the reduction's epilogue, or here by
+// pass 1 in the very same order), then fp64 across tiles in a fixed tree.
+// The grid never changes a partial, so the norm is bit-reproducible.
+//
+// Update: AdamW with decoupled weight decay (Loshchilov & Hutter, in the
+// form torch.optim.AdamW documents it) on the clipped, microbatch-averaged
+// gradient, fp32 state, bf16 round-to-nearest-even output in the
+// bucket-ordered full-parameter layout.  Each thread streams 8 elements:
+// 2 x 16 B of every fp32 array in, 2 x 16 B of each state array and 16 B of
+// bf16 out (30 bytes per element, the kernel's whole traffic).
+#include <cuda_bf16.h>
+#include <cmath>
+#include <cuda_runtime.h>
+
+#include "device.cuh"
+#include "internal.h"
+
+namespace grs {
+
+namespace {
+
+constexpr int NORM1_THREADS = 128;  // must equal the reduction's consumer threads
+constexpr int NORM2_THREADS = 256;
+constexpr int UPD_THREADS = 256;
+static_assert(UPD_T == UPD_THREADS * 8, "one 8-element group per thread per tile");
+
+// ----------------------------------------------------------------- norm pass 1
+// Same thread -> chunk map and the same fp32 operation order as the
+// reduction's fused epilogue: thread c of 128 sums chunks c, c+128, ... of
+// 8 elements with fmaf(x, x, s); warp butterfly; warps folded 0..3.
+__global__ void __launch_bounds__(NORM1_THREADS) norm_pass1_kernel(const float* __restrict__ acc,
+                                                                   const UnitDesc* __restrict__ units,
+                                                                   const int64_t* __restrict__ prefix,
+                                                                   int32_t n_units, int64_t n_tiles,
+                                                                   float* __restrict__ partials) {
+  __shared__ float wp[NORM1_THREADS / 32];
+  const int lane = threadIdx.x & 31;
+  const int w = threadIdx.x >> 5;
+  for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    const int u = find_unit(prefix, 0, n_units, tile);
+    const UnitDesc* ud = units + u;
+    const int64_t T = ud->red_T;
+    const int64_t e0 = (tile - ud->red_tile0) * T;
+    const int64_t rem = ud->padded - e0;
+    const int n = static_cast<int>(rem < T ? rem : T);
+    const float* src = acc + ud->state_off + e0;
+    float psum = 0.0f;
+    for (int c = threadIdx.x; c < (n >> 3); c += NORM1_THREADS) {
+      const float4 x0 = __ldcs(reinterpret_cast<const float4*>(src + c * 8));
+      const float4 x1 = __ldcs(reinterpret_cast<const float4*>(src + c * 8 + 4));
+      const float o[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+      for (int q = 0; q < 8; ++q) psum = __fmaf_rn(o[q], o[q], psum);
+    }
+    psum = warp_sum(psum);
+    if (lane == 0) wp[w] = psum;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float s = wp[0];
+#pragma unroll
+      for (int k = 1; k < NORM1_THREADS / 32; ++k) s = __fadd_rn(s, wp[k]);
+      partials[tile] = s;
+    }
+    __syncthreads();
+  }
+}
+
+// ----------------------------------------------------------------- norm pass 2
+// Block b of NORM_L2_BLOCKS sums its contiguous range of tile partials in
+// fp64: thread t takes indices t, t+256, ... in order, then a fixed tree.
+__device__ __forceinline__ double block_sum_fixed(double x, double* red) {
+  const int lane = threadIdx.x & 31;
+  const int w = threadIdx.x >> 5;
+  x = warp_sum(x);
+  if (lane == 0) red[w] = x;
+  __syncthreads();
+  double s = 0.0;
+  if (threadIdx.x == 0) {
+    s = red[0];
+    for (int k = 1; k < static_cast<int>(blockDim.x >> 5); ++k) s = __dadd_rn(s, red[k]);
+  }
+  return s;
+}
+
+__global__ void __launch_bounds__(NORM2_THREADS) norm_level2_kernel(const float* __restrict__ partials,
+                                                                    int64_t n, double* __restrict__ level2) {
+  __shared__ double red[NORM2_THREADS / 32];
+  const int64_t chunk = (n + NORM_L2_BLOCKS - 1) / NORM_L2_BLOCKS;
+  const int64_t lo = blockIdx.x * chunk;
+  const int64_t hi = lo + chunk < n ? lo + chunk : n;
+  double s = 0.0;
+  for (int64_t i = lo + threadIdx.x; i < hi; i += NORM2_THREADS)
+    s = __dadd_rn(s, static_cast<double>(partials[i]));
+  s = block_sum_fixed(s, red);
+  if (threadIdx.x == 0) level2[blockIdx.x] = s;
+}
+
+__global__ void __launch_bounds__(NORM_L2_BLOCKS) norm_final_kernel(const double* __restrict__ level2,
+                                                                     double inv_m2, double* __restrict__ out,
+                                                                     int* __restrict__ flags) {
+  __shared__ double red[NORM_L2_BLOCKS / 32];
+  double s = block_sum_fixed(level2[threadIdx.x], red);
+  if (threadIdx.x == 0) {
+    s = __dmul_rn(s, inv_m2);
+    *out = s;
+    if (!isfinite(s)) atomicOr(flags + FLAG_NONFINITE, 1);
+  }
+}
+
+// ----------------------------------------------------------------- update
+struct UpdateArgs {
+  const float* acc;
+  float* master;
+  float* m;
+  float* v;
+  uint16_t* params;
+  const double* norm_sq;
+  const UnitDesc* units;
+  const int64_t* prefix;
+  int32_t n_units;
+  float decay;       // 1 - lr * wd
+  float b1, omb1;    // beta1, 1 - beta1
+  float b2, omb2;    // beta2, 1 - beta2
+  float eps;
+  float step_size;   // lr / (1 - beta1^t)
+  float inv_bc2_sqrt;// 1 / sqrt(1 - beta2^t)
+  float max_norm;    // <= 0: no clipping
+  float inv_m;       // 1 / n_micro
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__global__ void __launch_bounds__(UPD_THREADS) update_kernel(const __grid_constant__ UpdateArgs a) {
+  // Clip coefficient c = min(1, max_norm / (sqrt(S) + 1e-6)), NaN kept,
+  // evaluated by every thread in fp32 from the device-resident S.
+  float gscale = a.inv_m;
+  if (a.max_norm > 0.0f) {
+    const float cr = a.max_norm / (sqrtf(static_cast<float>(*a.norm_sq)) + 1e-6f);
+    gscale = __fmul_rn((cr < 1.0f || isnan(cr)) ? cr : 1.0f, a.inv_m);
+  }
+  const int u = find_unit(a.prefix, 0, a.n_units, blockIdx.x);
+  const UnitDesc* ud = a.units + u;
+  const int64_t e0 = (static_cast<int64_t>(blockIdx.x) - ud->upd_tile0) * UPD_T;
+  const int64_t el = e0 + int64_t(threadIdx.x) * 8;  // element within the unit
+  if (el >= ud->padded) return;
+  const int64_t i = ud->state_off + el;
+  const int64_t used = ud->used;
+
+  const float4 g0 = __ldcs(reinterpret_cast<const float4*>(a.acc + i));
+  const float4 g1 = __ldcs(reinterpret_cast<const float4*>(a.acc + i + 4));
+  const float4 p0 = __ldcs(reinterpret_cast<const float4*>(a.master + i));
+  const float4 p1 = __ldcs(reinterpret_cast<const float4*>(a.master + i + 4));
+  const float4 m0 = __ldcs(reinterpret_cast<const float4*>(a.m + i));
+  const float4 m1 = __ldcs(reinterpret_cast<const float4*>(a.m + i + 4));
+  const float4 v0 = __ldcs(reinterpret_cast<const float4*>(a.v + i));
+  const float4 v1 = __ldcs(reinterpret_cast<const float4*>(a.v + i + 4));
+  float G[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+  float P[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+  float M[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+  float V[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const float g = __fmul_rn(G[q], gscale);
+    float p = __fmul_rn(P[q], a.decay);
+    const float mm = __fmaf_rn(a.b1, M[q], __fmul_rn(a.omb1, g));
+    const float vv = __fmaf_rn(a.b2, V[q], __fmul_rn(__fmul_rn(a.omb2, g), g));
+    const float denom = __fadd_rn(__fmul_rn(__fsqrt_rn(vv), a.inv_bc2_sqrt), a.eps);
+    p = __fsub_rn(p, __fmul_rn(a.step_size, __fdiv_rn(mm, denom)));
+    const bool pad = el + q >= used;
+    P[q] = pad ? 0.0f : p;
+    M[q] = pad ? 0.0f : mm;
+    V[q] = pad ? 0.0f : vv;
+  }
+  __stcs(reinterpret_cast<float4*>(a.master + i), make_float4(P[0], P[1], P[2], P[3]));
+  __stcs(reinterpret_cast<float4*>(a.master + i + 4), make_float4(P[4], P[5], P[6], P[7]));
+  __stcs(reinterpret_cast<float4*>(a.m + i), make_float4(M[0], M[1], M[2], M[3]));
+  __stcs(reinterpret_cast<float4*>(a.m + i + 4), make_float4(M[4], M[5], M[6], M[7]));
+  __stcs(reinterpret_cast<float4*>(a.v + i), make_float4(V[0], V[1], V[2], V[3]));
+  __stcs(reinterpret_cast<float4*>(a.v + i + 4), make_float4(V[4], V[5], V[6], V[7]));
+  uint4 h;
+  h.x = pack_bf16x2(P[0], P[1]);
+  h.y = pack_bf16x2(P[2], P[3]);
+  h.z = pack_bf16x2(P[4], P[5]);
+  h.w = pack_bf16x2(P[6], P[7]);
+  __stcs(reinterpret_cast<uint4*>(a.params + i), h);
+}
+
+// ----------------------------------------------------------------- accumulate
+__global__ void __launch_bounds__(UPD_THREADS) accumulate_kernel(float* __restrict__ acc,
+                                                                 const float* __restrict__ mb,
+                                                                 const UnitDesc* __restrict__ units,
+                                                                 const int64_t* __restrict__ prefix,
+                                                                 int32_t unit_begin, int32_t unit_end,
+                                                                 int64_t tile_begin, int64_t state_base) {
+  const int64_t tile = tile_begin + blockIdx.x;
+  const int u = find_unit(prefix, unit_begin, unit_end, tile);
+  const UnitDesc* ud = units + u;
+  const int64_t el = (tile - ud->upd_tile0) * UPD_T + int64_t(threadIdx.x) * 8;
+  if (el >= ud->padded) return;
+  const int64_t i = ud->state_off - state_base + el;
+  float4* a4 = reinterpret_cast<float4*>(acc + i);
+  const float4* b4 = reinterpret_cast<const float4*>(mb + i);
+  float4 x0 = a4[0], x1 = a4[1];
+  const float4 y0 = __ldg(b4), y1 = __ldg(b4 + 1);
+  float o[8] = {__fadd_rn(x0.x, y0.x), __fadd_rn(x0.y, y0.y), __fadd_rn(x0.z, y0.z),
+                __fadd_rn(x0.w, y0.w), __fadd_rn(x1.x, y1.x), __fadd_rn(x1.y, y1.y),
+                __fadd_rn(x1.z, y1.z), __fadd_rn(x1.w, y1.w)};
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    if (el + q >= ud->used) o[q] = 0.0f;
+  a4[0] = make_float4(o[0], o[1], o[2], o[3]);
+  a4[1] = make_float4(o[4], o[5], o[6], o[7]);
+}
+
+}  // namespace
+
+int launch_norm(const grs_plan* p, const float* acc, int32_t n_micro, void* workspace,
+                int32_t partials_ready, double* d_norm_sq, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* partials = reinterpret_cast<float*>(ws + ws_partials_offset());
+  double* level2 = reinterpret_cast<double*>(ws + ws_level2_offset(p->n_red_tiles));
+  if (!partials_ready && p->n_red_tiles > 0) {
+    const int64_t grid = p->n_red_tiles < int64_t(p->sm_count) * 16 ? p->n_red_tiles
+                                                                    : int64_t(p->sm_count) * 16;
+    norm_pass1_kernel<<<static_cast<unsigned>(grid), NORM1_THREADS, 0, s>>>(
+        acc, p->d_units, p->d_red_prefix, static_cast<int32_t>(p->units.size()), p->n_red_tiles,
+        partials);
+  }
+  norm_level2_kernel<<<NORM_L2_BLOCKS, NORM2_THREADS, 0, s>>>(partials, p->n_red_tiles, level2);
+  const double inv_m = 1.0 / static_cast<double>(n_micro);
+  norm_final_kernel<<<1, NORM_L2_BLOCKS, 0, s>>>(level2, inv_m * inv_m, d_norm_sq, p->d_flags);
+  return static_cast<int>(cudaGetLastError());
+}
+
+int launch_update(const grs_plan* p, const grs_adamw* hp, const double* d_norm_sq, const float* acc,
+                  float* master, float* m, float* v, uint16_t* params, void* stream) {
+  if (p->n_upd_tiles <= 0) return 0;
+  UpdateArgs a;
+  a.acc = acc;
+  a.master = master;
+  a.m = m;
+  a.v = v;
+  a.params = params;
+  a.norm_sq = d_norm_sq;
+  a.units = p->d_units;
+  a.prefix = p->d_upd_prefix;
+  a.n_units = static_cast<int32_t>(p->units.size());
+  const double lr = hp->lr, b1 = hp->beta1, b2 = hp->beta2, wd = hp->weight_decay;
+  const double bc1 = 1.0 - std::pow(b1, static_cast<double>(hp->step));
+  const double bc2 = 1.0 - std::pow(b2, static_cast<double>(hp->step));
+  a.decay = static_cast<float>(1.0 - lr * wd);
+  a.b1 = hp->beta1;
+  a.omb1 = static_cast<float>(1.0 - b1);
+  a.b2 = hp->beta2;
+  a.omb2 = static_cast<float>(1.0 - b2);
+  a.eps = hp->eps;
+  a.step_size = static_cast<float>(lr / bc1);
+  a.inv_bc2_sqrt = static_cast<float>(1.0 / std::sqrt(bc2));
+  a.max_norm = hp->max_norm > 0.0f ? hp->max_norm : 0.0f;
+  a.inv_m = static_cast<float>(1.0 / static_cast<double>(hp->n_micro));
+  update_kernel<<<static_cast<unsigned>(p->n_upd_tiles), UPD_THREADS, 0,
+                  static_cast<cudaStream_t>(stream)>>>(a);
+  return static_cast<int>(cudaGetLastError());
+}
+
+int launch_accumulate(const grs_plan* p, int32_t bucket, float* acc, const float* mb, void* stream) {
+  const Bucket& bk = p->buckets[bucket];
+  const int32_t ub = bk.unit0, ue = bk.unit0 + bk.copies;
+  const int64_t t0 = p->upd_prefix[ub], t1 = p->upd_prefix[ue];
+  if (t1 <= t0) return 0;
+  accumulate_kernel<<<static_cast<unsigned>(t1 - t0), UPD_THREADS, 0,
+                      static_cast<cudaStream_t>(stream)>>>(acc, mb, p->d_units, p->d_upd_prefix, ub, ue,
+                                                           t0, bk.state_off);
+  return static_cast<int>(cudaGetLastError());
+}
+
+}  // namespace grs

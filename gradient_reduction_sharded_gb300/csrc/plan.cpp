@@ -1,0 +1,200 @@
+// Host-side reduction plan: owner routing, buckets, padding, shards, tile
+// tables.  Pure C++ (no CUDA); the C-ABI layer uploads the tables.
+//
+// Rules ("refactor(distributed): establish shared native TP replica
+// ownership", "Why this needs separate work" and "Proposed scope": one
+// owner per parameter, unsupported compositions rejected; "Cosmos 3 ...
+// distributed parallelism", section 1: dp_replicate x dp_shard = world,
+// dp_shard = -1 auto; Mixle "Distributed Transformer Training", "Optimizer
+// and checkpoint semantics": plan from the logical parameter list):
+//  * buckets are tag-homogeneous, in tag order RA, PS, LS, AR, model order
+//    within a tag, greedy on per-rank bf16 bytes, tensors never split;
+//  * a LOCAL_SHARD tensor holds numel/tp elements per rank;
+//  * buckets are padded to a multiple of 8 * dp_shard elements so every
+//    shard starts on a 16-byte boundary;
+//  * state rows: tp per LOCAL_SHARD bucket, one otherwise.
+#include <algorithm>
+#include <string>
+
+#include "internal.h"
+
+namespace grs {
+
+namespace {
+
+int64_t round_up(int64_t x, int64_t q) { return (x + q - 1) / q * q; }
+
+int32_t group_size_of(int32_t tag, const grs_plan& p) {
+  switch (tag) {
+    case GRS_REPLICA_AVG:
+    case GRS_PARTIAL_SUM:
+      return p.world;
+    case GRS_LOCAL_SHARD:
+      return p.dp;
+    default:
+      return 1;
+  }
+}
+
+}  // namespace
+
+grs_status build_plan(const int64_t* numels, const int32_t* owners, int32_t n, int32_t world,
+                      int32_t tp, int32_t dp_replicate, int32_t dp_shard, int64_t bucket_bytes,
+                      grs_plan* p, std::string* why) {
+  if (n <= 0 || numels == nullptr || owners == nullptr) {
+    *why = "plan needs at least one tensor (numels/owners non-null)";
+    return GRS_ERR_INVALID_ARG;
+  }
+  if (bucket_bytes <= 0) {
+    *why = "bucket_bytes must be positive";
+    return GRS_ERR_INVALID_ARG;
+  }
+  if (world <= 0 || world > GRS_MAX_WORLD || tp <= 0 || dp_replicate <= 0 ||
+      (dp_shard <= 0 && dp_shard != -1)) {
+    *why = "degrees must be positive (dp_shard may be -1) and world <= GRS_MAX_WORLD";
+    return GRS_ERR_INVALID_ARG;
+  }
+  if (dp_shard == -1) {
+    if (world % (tp * dp_replicate) != 0) {
+      *why = "dp_shard=-1: world is not a multiple of tp * dp_replicate";
+      return GRS_ERR_UNSUPPORTED_COMPOSITION;
+    }
+    dp_shard = world / (tp * dp_replicate);
+  }
+  if (static_cast<int64_t>(tp) * dp_replicate * dp_shard != world) {
+    *why = "tp * dp_replicate * dp_shard != world";
+    return GRS_ERR_UNSUPPORTED_COMPOSITION;
+  }
+  for (int32_t i = 0; i < n; ++i) {
+    if (owners[i] < GRS_REPLICA_AVG || owners[i] > GRS_ALREADY_REDUCED) {
+      *why = "tensor " + std::to_string(i) + ": unknown owner tag " + std::to_string(owners[i]);
+      return GRS_ERR_INVALID_ARG;
+    }
+    if (numels[i] < 0) {
+      *why = "tensor " + std::to_string(i) + ": negative numel";
+      return GRS_ERR_SHAPE;
+    }
+    if (owners[i] == GRS_LOCAL_SHARD && numels[i] % tp != 0) {
+      *why = "tensor " + std::to_string(i) + ": LOCAL_SHARD numel not divisible by tp";
+      return GRS_ERR_SHAPE;
+    }
+  }
+
+  p->numel.assign(numels, numels + n);
+  p->owner.assign(owners, owners + n);
+  p->world = world;
+  p->tp = tp;
+  p->dp_replicate = dp_replicate;
+  p->dp_shard = dp_shard;
+  p->dp = dp_replicate * dp_shard;
+  p->bucket_bytes = bucket_bytes;
+  p->t_bucket.assign(n, -1);
+  p->t_offset.assign(n, 0);
+  p->buckets.clear();
+  p->n_unique = 0;
+  for (int32_t i = 0; i < n; ++i) p->n_unique += numels[i];
+
+  // Greedy, tag-homogeneous buckets.
+  for (int32_t tag = GRS_REPLICA_AVG; tag <= GRS_ALREADY_REDUCED; ++tag) {
+    Bucket* cur = nullptr;
+    for (int32_t i = 0; i < n; ++i) {
+      if (owners[i] != tag) continue;
+      const int64_t per_rank = (tag == GRS_LOCAL_SHARD) ? numels[i] / tp : numels[i];
+      if (cur != nullptr && cur->used > 0 && 2 * (cur->used + per_rank) > bucket_bytes) cur = nullptr;
+      if (cur == nullptr) {
+        p->buckets.emplace_back();
+        cur = &p->buckets.back();
+        cur->tag = tag;
+        cur->copies = (tag == GRS_LOCAL_SHARD) ? tp : 1;
+        cur->group_size = group_size_of(tag, *p);
+      }
+      p->t_bucket[i] = static_cast<int32_t>(p->buckets.size() - 1);
+      p->t_offset[i] = cur->used;
+      cur->used += per_rank;
+      cur->n_tensors += 1;
+    }
+  }
+
+  // Padding, shards, offsets, units and tiles.
+  const int64_t quantum = 8 * static_cast<int64_t>(dp_shard);
+  p->units.clear();
+  p->red_prefix.assign(1, 0);
+  p->upd_prefix.assign(1, 0);
+  int64_t rank_off = 0, state_off = 0, red_tiles = 0, upd_tiles = 0;
+  for (size_t b = 0; b < p->buckets.size(); ++b) {
+    Bucket& bk = p->buckets[b];
+    bk.padded = round_up(bk.used, quantum);
+    bk.shard_len = bk.padded / dp_shard;
+    bk.rank_off = rank_off;
+    bk.state_off = state_off;
+    bk.unit0 = static_cast<int32_t>(p->units.size());
+    int64_t T = STAGE_GRAD_BYTES / (2 * static_cast<int64_t>(bk.group_size));
+    T = std::min<int64_t>(RED_MAX_T, std::max<int64_t>(8, T / 8 * 8));
+    for (int32_t t = 0; t < bk.copies; ++t) {
+      UnitDesc u{};
+      u.state_off = state_off + static_cast<int64_t>(t) * bk.padded;
+      u.rank_off = rank_off;
+      u.padded = bk.padded;
+      u.used = bk.used;
+      u.red_tile0 = red_tiles;
+      u.upd_tile0 = upd_tiles;
+      u.red_T = static_cast<int32_t>(T);
+      u.bucket = static_cast<int32_t>(b);
+      switch (bk.tag) {
+        case GRS_REPLICA_AVG:  // average across TP and DP: all ranks
+          u.g_start = 0; u.g_stride = 1; u.g_count = world;
+          u.scale = 1.0f / static_cast<float>(world);
+          break;
+        case GRS_PARTIAL_SUM:  // sum across TP, average across DP
+          u.g_start = 0; u.g_stride = 1; u.g_count = world;
+          u.scale = 1.0f / static_cast<float>(p->dp);
+          break;
+        case GRS_LOCAL_SHARD:  // the DP group of tp index t only
+          u.g_start = t; u.g_stride = tp; u.g_count = p->dp;
+          u.scale = 1.0f / static_cast<float>(p->dp);
+          break;
+        default:  // ALREADY_REDUCED: canonical rank 0, no reduction
+          u.g_start = 0; u.g_stride = 1; u.g_count = 1;
+          u.scale = 1.0f;
+          break;
+      }
+      red_tiles += (bk.padded + T - 1) / T;
+      upd_tiles += (bk.padded + UPD_T - 1) / UPD_T;
+      p->units.push_back(u);
+      p->red_prefix.push_back(red_tiles);
+      p->upd_prefix.push_back(upd_tiles);
+    }
+    rank_off += bk.padded;
+    state_off += static_cast<int64_t>(bk.copies) * bk.padded;
+  }
+  p->n_rank_pad = rank_off;
+  p->n_state_pad = state_off;
+  p->n_red_tiles = red_tiles;
+  p->n_upd_tiles = upd_tiles;
+  p->workspace_bytes =
+      ws_level2_offset(red_tiles) + static_cast<int64_t>(NORM_L2_BLOCKS) * sizeof(double);
+
+  // Gather jobs: one per (tensor, state row).
+  p->jobs.clear();
+  p->tensor_job0.assign(1, 0);
+  int64_t chunks = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    const Bucket& bk = p->buckets[p->t_bucket[i]];
+    const int64_t per_rank = (owners[i] == GRS_LOCAL_SHARD) ? numels[i] / tp : numels[i];
+    for (int32_t t = 0; t < bk.copies; ++t) {
+      GatherJob j{};
+      j.src = bk.state_off + static_cast<int64_t>(t) * bk.padded + p->t_offset[i];
+      j.dst = static_cast<int64_t>(t) * per_rank;
+      j.len = per_rank;
+      j.chunk0 = chunks;
+      j.tensor = i;
+      chunks += (per_rank + GATHER_CHUNK - 1) / GATHER_CHUNK;
+      p->jobs.push_back(j);
+    }
+    p->tensor_job0.push_back(static_cast<int32_t>(p->jobs.size()));
+  }
+  p->n_gather_chunks = chunks;
+  return GRS_OK;
+}
+
+}  // namespace grs

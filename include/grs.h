@@ -1,0 +1,277 @@
+/*
+ * grs.h — ownership-aware sharded gradient reduction and AdamW for GB300.
+ *
+ * C ABI of libgrs.so.  Plain pointers and sizes only: host pointers are
+ * marked "host", device pointers "device".  Every entry point returns a
+ * grs_status; on failure a thread-local message is available from
+ * grs_last_error().  Nothing here synchronises with the host except
+ * grs_check_device_errors(), and nothing allocates device memory except
+ * grs_plan_create() (its small tables and error flags).
+ *
+ * The operation follows these web pages (cited by title and section):
+ *   [ISSUE]  "refactor(distributed): establish shared native TP replica
+ *            ownership" (NeMo Automodel issue) — "Why this needs separate
+ *            work" (the four owner semantics), "Preserved prototype and
+ *            evidence" (FP32 reduction hook, accumulation, clipping),
+ *            "Proposed scope and acceptance criteria" (one reduction owner
+ *            per parameter; reject unsupported compositions).
+ *   [COSMOS] "Cosmos 3 training framework > distributed parallelism" —
+ *            section 1 (dp_shard / dp_replicate; -1 = whole world;
+ *            dp_replicate x dp_shard = world), section 2 (2x4 dp_mesh:
+ *            all-reduce across replicas, all-gather across shards).
+ *   [MIXLE]  "Distributed Transformer Training" (Mixle integration note) —
+ *            "Backend split" (fail before fitting), "Optimizer and
+ *            checkpoint semantics" (routes planned from logical parameters
+ *            before wrapping; Adam state).
+ *
+ * Simulated ranks.  The R = world ranks of a tp x dp_replicate x dp_shard
+ * job are buffers in one GPU's memory.  Rank index of mesh coordinate
+ * (replica r, shard s, tensor-parallel index t):
+ *     rank = (r * dp_shard + s) * tp + t
+ * ([COSMOS] section 2: replica 0 holds g0..g3, so replicas are the slow
+ * axis; the tp index is innermost).
+ *
+ * Layouts (all element counts, not bytes):
+ *   per-rank gradient buffer  bf16 [n_rank_pad]: the buckets' per-rank
+ *       slices back to back; bucket b occupies [rank_offset, +padded).
+ *       A LOCAL_SHARD tensor contributes numel/tp elements per rank: rank
+ *       with tp index t holds the t-th contiguous chunk of the row-major
+ *       logical tensor.
+ *   state (accumulator, fp32 master, first and second moment, bf16
+ *       parameters) [n_state_pad]: per bucket, `copies` rows of `padded`
+ *       elements at state_offset (copies = tp for LOCAL_SHARD: row t holds
+ *       the reduction over the ranks of tp index t; 1 otherwise).  Each
+ *       row splits into dp_shard contiguous shards of shard_len elements:
+ *       shard s is what rank (r, s, t) owns after the reduce-scatter.
+ *   Padding (bucket element index >= used) is ignored on input, may hold
+ *       anything (NaN included), and is written as exact zeros in every
+ *       output.
+ */
+#ifndef GRS_H
+#define GRS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GRS_MAX_WORLD 128
+
+/* Owner tag of a parameter ([ISSUE] "Why this needs separate work").
+ *  GRS_REPLICA_AVG      complete gradients from redundant computation:
+ *                       averaged across TP (and DP)             scale 1/R
+ *  GRS_PARTIAL_SUM      partial contributions (head/sequence sharding):
+ *                       summed across TP, averaged across DP    scale 1/dp
+ *  GRS_LOCAL_SHARD      TP/EP/model-owned shard: never synchronised across
+ *                       TP, averaged over its own DP group      scale 1/dp
+ *  GRS_ALREADY_REDUCED  reduced by another owner: never reduced again;
+ *                       rank 0's copy is taken as is            scale 1   */
+typedef enum grs_owner {
+  GRS_REPLICA_AVG = 0,
+  GRS_PARTIAL_SUM = 1,
+  GRS_LOCAL_SHARD = 2,
+  GRS_ALREADY_REDUCED = 3
+} grs_owner;
+
+typedef enum grs_status {
+  GRS_OK = 0,
+  GRS_ERR_INVALID_ARG = 1,              /* null/out-of-range argument       */
+  GRS_ERR_UNSUPPORTED_COMPOSITION = 2,  /* degrees do not compose to world  */
+  GRS_ERR_SHAPE = 3,                    /* numel < 0, LOCAL_SHARD % tp != 0 */
+  GRS_ERR_ALIGNMENT = 4,                /* device pointer not 16-B aligned  */
+  GRS_ERR_CUDA = 5,                     /* CUDA runtime error (message set) */
+  GRS_ERR_TIMEOUT = 6,                  /* a bounded device wait gave up    */
+  GRS_ERR_NONFINITE = 7,                /* global gradient norm is NaN/Inf  */
+  GRS_ERR_NO_DEVICE = 8                 /* plan was created host-only       */
+} grs_status;
+
+/* grs_plan_create flags */
+#define GRS_PLAN_HOST_ONLY 1u /* build host tables only (queries work, launches fail) */
+
+typedef struct grs_plan grs_plan; /* opaque; owned by the caller via create/destroy */
+
+typedef struct grs_plan_info {
+  int32_t n_tensors;
+  int32_t n_buckets;
+  int32_t world;          /* R */
+  int32_t tp;
+  int32_t dp_replicate;
+  int32_t dp_shard;       /* resolved (never -1) */
+  int32_t dp;             /* dp_replicate * dp_shard */
+  int32_t device;         /* CUDA device of the tables, -1 when host-only */
+  int64_t n_unique;       /* N: logical parameter elements */
+  int64_t n_rank_pad;     /* elements of each rank's gradient buffer */
+  int64_t n_state_pad;    /* elements of accumulator / master / m / v / params */
+  int64_t workspace_bytes;/* device workspace needed by reduce / norm calls */
+  int64_t n_reduce_tiles; /* norm partial slots (one per reduction tile) */
+} grs_plan_info;
+
+typedef struct grs_bucket_desc {
+  int32_t tag;            /* grs_owner of every tensor in the bucket */
+  int32_t copies;         /* state rows: tp for LOCAL_SHARD, else 1 */
+  int32_t group_size;     /* ranks reduced per output element (R, dp or 1) */
+  int32_t n_tensors;
+  int64_t used;           /* per-rank elements holding tensor data */
+  int64_t padded;         /* per-rank elements incl. padding (multiple of 8*dp_shard) */
+  int64_t shard_len;      /* padded / dp_shard */
+  int64_t rank_offset;    /* offset of the bucket in each rank buffer */
+  int64_t state_offset;   /* offset of row 0 in the state arrays */
+} grs_bucket_desc;
+
+typedef struct grs_tensor_desc {
+  int32_t bucket;
+  int32_t owner;
+  int64_t numel;          /* logical elements */
+  int64_t per_rank;       /* numel/tp for LOCAL_SHARD, else numel */
+  int64_t bucket_offset;  /* element offset inside the bucket (per rank and per state row) */
+} grs_tensor_desc;
+
+/* AdamW hyper-parameters (decoupled weight decay, Loshchilov & Hutter;
+ * the form torch.optim.AdamW documents) and clipping. */
+typedef struct grs_adamw {
+  float lr;
+  float beta1;
+  float beta2;
+  float eps;
+  float weight_decay;
+  float max_norm;         /* <= 0: clipping off */
+  int32_t step;           /* 1-based index of this update (bias correction) */
+  int32_t n_micro;        /* M: the accumulator holds the sum of M microbatches */
+} grs_adamw;
+
+/* ---------------------------------------------------------------- plan */
+
+/* Build the reduction plan from the logical parameter list, in model order
+ * ([MIXLE] "Optimizer and checkpoint semantics": routes planned from
+ * stable logical parameters before wrapping).
+ *   numels, owners : host arrays [n_tensors]; owners are grs_owner values.
+ *   world          : number of simulated ranks, 1..GRS_MAX_WORLD.
+ *   tp, dp_replicate, dp_shard : degrees; dp_shard = -1 resolves to
+ *                    world / (tp * dp_replicate) ([COSMOS] section 1).
+ *   bucket_bytes   : cap on a bucket's per-rank bf16 bytes; a tensor larger
+ *                    than the cap gets a bucket of its own.
+ *   flags          : 0 or GRS_PLAN_HOST_ONLY.  Without it the plan's device
+ *                    tables go to the current CUDA device.
+ * Buckets hold one owner tag each, in tag order REPLICA_AVG, PARTIAL_SUM,
+ * LOCAL_SHARD, ALREADY_REDUCED, model order inside a tag, filled greedily,
+ * tensors packed back to back, padded to a multiple of 8 * dp_shard.
+ * Errors (nothing is launched or allocated; [MIXLE] "Backend split": fail
+ * before fitting; [ISSUE] "Proposed scope": reject unsupported
+ * compositions): n_tensors <= 0, bad tag, bucket_bytes <= 0, a degree <= 0
+ * (dp_shard may be -1) -> INVALID_ARG; tp*dp_replicate*dp_shard != world
+ * -> UNSUPPORTED_COMPOSITION; numel < 0 or LOCAL_SHARD numel % tp != 0 ->
+ * SHAPE; device table upload failure -> CUDA.  *out is set only on OK. */
+grs_status grs_plan_create(const int64_t* numels, const int32_t* owners, int32_t n_tensors,
+                           int32_t world, int32_t tp, int32_t dp_replicate, int32_t dp_shard,
+                           int64_t bucket_bytes, uint32_t flags, grs_plan** out);
+
+/* Free the plan and its device tables.  NULL is a no-op.  The caller must
+ * ensure no launch using the plan is still in flight. */
+void grs_plan_destroy(grs_plan* plan);
+
+/* Plan queries (host only; no CUDA call). */
+grs_status grs_plan_query(const grs_plan* plan, grs_plan_info* out);
+grs_status grs_bucket_info(const grs_plan* plan, int32_t bucket, grs_bucket_desc* out);
+grs_status grs_tensor_info(const grs_plan* plan, int32_t tensor, grs_tensor_desc* out);
+
+/* ---------------------------------------------------------- hot path */
+
+/* Reduce one bucket of one microbatch: for every output element e of every
+ * row of bucket b,
+ *     acc[e] (= | +=) scale(tag) * sum_{k in group} float(g_k[e])
+ * in fp32 with ranks k in ascending order ([ISSUE] "Preserved prototype":
+ * FP32 reduction of BF16 gradients; "Why this needs separate work": the
+ * group and scale come from the owner tag).  This is the reduce-scatter of
+ * the bucket over dp_shard plus the all-reduce over dp_replicate plus the
+ * TP reduction ([COSMOS] section 2), all shards computed.
+ *   rank_grads : host array [world] of device pointers; rank_grads[k]
+ *                points at rank k's copy of THIS bucket (bf16 bits,
+ *                [padded] elements).  Only the ranks of the tag's group are
+ *                read (ALREADY_REDUCED reads rank 0 only).
+ *   acc        : device fp32 [copies * padded]: this bucket's state rows.
+ *   accumulate : 0 overwrite (first microbatch), 1 add (later ones).
+ *   emit_norm_partials : 1 on the last microbatch: also write the bucket's
+ *                per-tile sums of acc^2 into the workspace, so that
+ *                grs_grad_norm_sq needs no second pass over acc.
+ *   workspace  : device, >= workspace_bytes; required when emitting.
+ * Errors: INVALID_ARG, ALIGNMENT (every pointer 16-B aligned), NO_DEVICE,
+ * CUDA (launch failure). */
+grs_status grs_reduce_bucket(const grs_plan* plan, int32_t bucket, const uint16_t* const* rank_grads,
+                             float* acc, int32_t accumulate, int32_t emit_norm_partials,
+                             void* workspace, void* stream);
+
+/* The same for every bucket in one launch.
+ *   rank_grads : host array [world] of device pointers to each rank's
+ *                whole gradient buffer (bf16 bits, [n_rank_pad]).
+ *   acc        : device fp32 [n_state_pad]. */
+grs_status grs_reduce_all(const grs_plan* plan, const uint16_t* const* rank_grads, float* acc,
+                          int32_t accumulate, int32_t emit_norm_partials, void* workspace,
+                          void* stream);
+
+/* acc_b += mb_b over bucket b's rows (fp32), padding kept at zero: adds a
+ * separately reduced microbatch gradient into the accumulator ([ISSUE]
+ * "Proposed scope": gradient accumulation).  Both device [copies*padded]. */
+grs_status grs_accumulate(const grs_plan* plan, int32_t bucket, float* acc, const float* mb,
+                          void* stream);
+
+/* Global squared gradient norm S = sum_e (acc[e]/n_micro)^2 over every
+ * unique element (each state element once; LOCAL_SHARD rows each count;
+ * padding is zero), kept on the device in *d_norm_sq ([ISSUE] "Proposed
+ * scope": global norms for clipping).  Deterministic: fixed tiles, fixed
+ * summation trees, fp32 inside a tile and fp64 across tiles.
+ *   acc            : device fp32 [n_state_pad] (read unless partials_ready).
+ *   partials_ready : 1 when every bucket's last reduce emitted its
+ *                    partials into `workspace` (no pass over acc).
+ *   d_norm_sq      : device double [1].
+ * A non-finite S raises the device flag reported as NONFINITE by
+ * grs_check_device_errors; the step still proceeds (NaN propagates). */
+grs_status grs_grad_norm_sq(const grs_plan* plan, const float* acc, int32_t n_micro,
+                            void* workspace, int32_t partials_ready, double* d_norm_sq,
+                            void* stream);
+
+/* Clip + AdamW + bf16 cast, fused, over all n_state_pad elements:
+ *   c = min(1, max_norm / (sqrt(S) + 1e-6))   (1 when max_norm <= 0)
+ *   g = c * acc / n_micro
+ *   p = p*(1 - lr*wd); m = b1*m + (1-b1)*g; v = b2*v + (1-b2)*g^2
+ *   p = p - lr/(1-b1^step) * m / (sqrt(v)/sqrt(1-b2^step) + eps)
+ *   params_bf16 = round-to-nearest-even(p)
+ * ([ISSUE] "Proposed scope": clipping on/off, optimizer updates; AdamW per
+ * Loshchilov & Hutter as torch.optim.AdamW documents it).  S is read on
+ * the device: no host synchronisation.  The bf16 output is written in the
+ * bucket-ordered full-parameter layout, i.e. the all-gathered parameters
+ * ([COSMOS] section 2).
+ *   hp        : host struct.  d_norm_sq: device double (may be NULL when
+ *               max_norm <= 0).  acc: device fp32 (read only).  master, m,
+ *               v: device fp32, updated in place.  params_bf16: device
+ *               bf16 bits.  All [n_state_pad].
+ * Errors: INVALID_ARG (step < 1, n_micro < 1, NULL), ALIGNMENT, NO_DEVICE,
+ * CUDA. */
+grs_status grs_clip_adamw_step(const grs_plan* plan, const grs_adamw* hp, const double* d_norm_sq,
+                               const float* acc, float* master, float* m, float* v,
+                               uint16_t* params_bf16, void* stream);
+
+/* Gather: copy every tensor from the bucket-ordered bf16 parameter buffer
+ * to its own full logical tensor ([COSMOS] section 2: all-gather of
+ * parameters across shards; LOCAL_SHARD tensors reassembled from their tp
+ * rows in dim-0 order).
+ *   params_bf16 : device [n_state_pad].
+ *   tensor_ptrs : host array [n_tensors] of device pointers, each to
+ *                 numel bf16 elements; NULL entries are skipped.  Any
+ *                 alignment is accepted. */
+grs_status grs_gather_params(const grs_plan* plan, const uint16_t* params_bf16,
+                             uint16_t* const* tensor_ptrs, void* stream);
+
+/* Synchronise `stream`, read and clear the plan's device flags.  Returns
+ * TIMEOUT if a bounded device wait gave up, NONFINITE if a global norm was
+ * NaN/Inf since the last check, else OK (or CUDA). */
+grs_status grs_check_device_errors(const grs_plan* plan, void* stream);
+
+/* Message of the last failing call on this thread ("" if none). */
+const char* grs_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GRS_H */

@@ -1,0 +1,209 @@
+"""Shared helpers of the GPU parity tests: seeded inputs on the device, the
+CUDA path through the C ABI, the oracle on the same bytes, comparisons.
+
+Inputs come from `workloads` (seeded torch generators); expected values come
+only from `oracle` applied to those inputs copied to the host.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import List, Optional
+
+import numpy as np
+import torch
+
+import oracle
+import workloads
+
+NAN_BF16 = 0x7FC0
+RTOL, ATOL = 1e-5, 1e-7
+
+
+def grs():
+    from gradient_reduction_sharded_gb300 import grs as g
+    return g
+
+
+@dataclass
+class Case:
+    """A plan plus the device buffers of one update."""
+    numels: List[int]
+    owners: List[int]
+    world: int
+    tp: int
+    dp_replicate: int
+    dp_shard: int
+    bucket_bytes: int
+    n_micro: int
+    grad_std: float
+    seed_base: int
+    hp: tuple = (1e-3, 0.9, 0.999, 1e-8, 0.01)
+    max_norm: float = 1.0
+    master_std: float = 0.02
+
+
+def case_from_workload(cid: int) -> Case:
+    w = workloads.get(cid)
+    a = w.adamw
+    return Case(w.numels, w.owners, w.world, w.tp, w.dp_replicate, w.dp_shard, w.bucket_bytes,
+                w.n_micro, w.grad_std, cid, (a.lr, a.beta1, a.beta2, a.eps, a.weight_decay),
+                a.max_norm, w.master_std)
+
+
+class Run:
+    """Device-side state of one case: plan, rank buffers per microbatch,
+    accumulator, optimizer state, workspace."""
+
+    def __init__(self, c: Case, device="cuda", poison_padding=True, step_seed=0):
+        g = grs()
+        self.c = c
+        self.dev = torch.device(device)
+        self.op = oracle.plan(c.numels, c.owners, c.world, c.tp, c.dp_replicate, c.dp_shard,
+                              c.bucket_bytes)
+        self.plan = g.grs_plan_create(c.numels, c.owners, c.world, c.tp, c.dp_replicate,
+                                      c.dp_shard, c.bucket_bytes)
+        self.info = g.grs_plan_query(self.plan)
+        nrp, nsp = self.info["n_rank_pad"], self.info["n_state_pad"]
+        self.nrp, self.nsp = nrp, nsp
+        self.poison = poison_padding
+        self.grads = [[torch.empty(max(nrp, 8), dtype=torch.bfloat16, device=self.dev)
+                       for _ in range(c.world)] for _ in range(c.n_micro)]
+        self.fill_grads(step_seed)
+        self.acc = torch.empty(max(nsp, 8), dtype=torch.float32, device=self.dev)
+        self.master = workloads.normal_f32(max(nsp, 8), c.master_std,
+                                           workloads.master_seed(c.seed_base), device=self.dev)
+        self.m = torch.zeros(max(nsp, 8), dtype=torch.float32, device=self.dev)
+        self.v = torch.zeros(max(nsp, 8), dtype=torch.float32, device=self.dev)
+        self.params = torch.empty(max(nsp, 8), dtype=torch.int16, device=self.dev)
+        self.ws = torch.zeros(max(self.info["workspace_bytes"], 16) // 4 + 4, dtype=torch.float32,
+                              device=self.dev)
+        self.norm = torch.zeros(1, dtype=torch.float64, device=self.dev)
+        self.step = 0
+
+    def fill_grads(self, step_seed=0):
+        c = self.c
+        for j in range(c.n_micro):
+            for k in range(c.world):
+                seed = workloads.grad_seed(c.seed_base, j + 1000 * step_seed, k)
+                workloads.normal_bf16(self.nrp, c.grad_std, seed, device=self.dev,
+                                      out=self.grads[j][k][:self.nrp])
+                if self.poison:
+                    bits = self.grads[j][k].view(torch.int16)
+                    for b in range(self.op.n_buckets):
+                        ro = int(self.op.b_rank_off[b])
+                        bits[ro + int(self.op.b_used[b]):ro + int(self.op.b_padded[b])] = NAN_BF16
+
+    def stream(self) -> int:
+        return torch.cuda.current_stream(self.dev).cuda_stream
+
+    def ptrs(self, j):
+        return [t.data_ptr() for t in self.grads[j]]
+
+    def reduce(self, per_bucket=False, emit=True):
+        g = grs()
+        c = self.c
+        s = self.stream()
+        for j in range(c.n_micro):
+            last = emit and j == c.n_micro - 1
+            if per_bucket:
+                for b in range(self.info["n_buckets"]):
+                    d = g.grs_bucket_info(self.plan, b)
+                    rp = [p + 2 * d["rank_offset"] for p in self.ptrs(j)]
+                    g.grs_reduce_bucket(self.plan, b, rp, self.acc.data_ptr() + 4 * d["state_offset"],
+                                        int(j > 0), int(last), self.ws.data_ptr(), s)
+            else:
+                g.grs_reduce_all(self.plan, self.ptrs(j), self.acc.data_ptr(), int(j > 0), int(last),
+                                 self.ws.data_ptr(), s)
+
+    def norm_sq(self, partials_ready=True):
+        g = grs()
+        g.grs_grad_norm_sq(self.plan, self.acc.data_ptr(), self.c.n_micro, self.ws.data_ptr(),
+                           int(partials_ready), self.norm.data_ptr(), self.stream())
+
+    def adamw(self, max_norm=None):
+        g = grs()
+        c = self.c
+        self.step += 1
+        mn = c.max_norm if max_norm is None else max_norm
+        hp = g.make_adamw(c.hp[0], c.hp[1], c.hp[2], c.hp[3], c.hp[4], mn, self.step, c.n_micro)
+        g.grs_clip_adamw_step(self.plan, hp, self.norm.data_ptr(), self.acc.data_ptr(),
+                              self.master.data_ptr(), self.m.data_ptr(), self.v.data_ptr(),
+                              self.params.data_ptr(), self.stream())
+
+    def update(self, per_bucket=False, partials_ready=True, max_norm=None):
+        self.reduce(per_bucket=per_bucket, emit=partials_ready)
+        self.norm_sq(partials_ready=partials_ready)
+        self.adamw(max_norm=max_norm)
+
+    def check_flags(self) -> int:
+        return grs().grs_check_device_errors(self.plan, self.stream())
+
+    def close(self):
+        if self.plan:
+            torch.cuda.synchronize(self.dev)
+            grs().grs_plan_destroy(self.plan)
+            self.plan = None
+
+    # ---------------------------------------------------------------- oracle side
+    def bucket_inputs(self, b) -> np.ndarray:
+        """[M][R][P] uint16 of bucket b, copied to the host."""
+        ro = int(self.op.b_rank_off[b])
+        P = int(self.op.b_padded[b])
+        arr = torch.stack([torch.stack([t[ro:ro + P] for t in mb]) for mb in self.grads])
+        return arr.view(torch.int16).cpu().numpy().view(np.uint16)
+
+    def state_host(self):
+        n = self.nsp
+        return (self.master[:n].cpu().numpy().copy(), self.m[:n].cpu().numpy().copy(),
+                self.v[:n].cpu().numpy().copy())
+
+
+def oracle_update(run: Run, master0, m0, v0, step: int, max_norm=None, threads=1):
+    c = run.c
+    mn = c.max_norm if max_norm is None else max_norm
+    return oracle.full_update(run.op, run.bucket_inputs, c.n_micro, c.hp, mn, step, master0, m0, v0,
+                              threads=threads)
+
+
+def assert_close(got, want, what, rtol=RTOL, atol=ATOL):
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    assert got.shape == want.shape, (what, got.shape, want.shape)
+    both_nan = np.isnan(got) & np.isnan(want)
+    err = np.abs(got - want)
+    bad = ~both_nan & ~(err <= atol + rtol * np.abs(want))
+    if bad.any():
+        i = np.flatnonzero(bad)[:5]
+        raise AssertionError(f"{what}: {bad.sum()} of {bad.size} outside rel {rtol}/abs {atol}; "
+                             f"first {i.tolist()} got {got[i].tolist()} want {want[i].tolist()}")
+
+
+def bf16_ordered(bits):
+    b = np.asarray(bits).astype(np.int64) & 0xFFFF
+    mag = b & 0x7FFF
+    return np.where(b & 0x8000, -mag, mag)
+
+
+def assert_bf16_within_1ulp(got_bits, want_bits, what):
+    g = np.asarray(got_bits).view(np.uint16) if np.asarray(got_bits).dtype != np.uint16 else got_bits
+    w = np.asarray(want_bits, np.uint16)
+    gn = (g & 0x7FFF) > 0x7F80
+    wn = (w & 0x7FFF) > 0x7F80
+    assert np.array_equal(gn, wn), f"{what}: NaN positions differ"
+    d = np.abs(bf16_ordered(g) - bf16_ordered(w))
+    d[gn] = 0
+    if (d > 1).any():
+        i = np.flatnonzero(d > 1)[:5]
+        raise AssertionError(f"{what}: {int((d > 1).sum())} values beyond 1 bf16 ulp at {i.tolist()}: "
+                             f"got {g[i].tolist()} want {w[i].tolist()}")
+
+
+def padding_mask(op) -> np.ndarray:
+    """True at state elements that are padding."""
+    mask = np.zeros(op.n_state_pad, bool)
+    for b in range(op.n_buckets):
+        P = int(op.b_padded[b])
+        for t in range(op.copies(b)):
+            o = int(op.b_state_off[b]) + t * P
+            mask[o + int(op.b_used[b]):o + P] = True
+    return mask

@@ -1,0 +1,165 @@
+"""Host-side checks of libgrs (no GPU): exports, plan tables against the
+oracle's independent plan (bit-exact), rejections, host-only behaviour."""
+import ctypes
+import json
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def grs():
+    from gradient_reduction_sharded_gb300 import _build
+    _build.build()
+    from gradient_reduction_sharded_gb300 import grs as g
+    return g
+
+
+def declared_functions():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if not h.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s*(grs_[a-z0-9_]+)\s*\(",
+                            text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_symbol(grs):
+    names = declared_functions()
+    assert "grs_reduce_bucket" in names and "grs_clip_adamw_step" in names
+    lib = ctypes.CDLL(grs.LIB_PATH)
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+    # the binding wraps every declared function
+    assert set(names) <= set(grs.EXPORTED), set(names) - set(grs.EXPORTED)
+
+
+def _compare_plan(grs, h, op, numels, owners):
+    info = grs.grs_plan_query(h)
+    assert info["n_buckets"] == op.n_buckets
+    assert info["dp_shard"] == op.dp_shard
+    assert info["dp"] == op.dp
+    assert info["n_rank_pad"] == op.n_rank_pad
+    assert info["n_state_pad"] == op.n_state_pad
+    assert info["n_unique"] == int(sum(numels))
+    for b in range(op.n_buckets):
+        d = grs.grs_bucket_info(h, b)
+        assert d["tag"] == int(op.b_tag[b])
+        assert d["used"] == int(op.b_used[b])
+        assert d["padded"] == int(op.b_padded[b])
+        assert d["rank_offset"] == int(op.b_rank_off[b])
+        assert d["state_offset"] == int(op.b_state_off[b])
+        assert d["shard_len"] == op.shard_len(b)
+        assert d["copies"] == op.copies(b)
+    for i in range(len(numels)):
+        t = grs.grs_tensor_info(h, i)
+        assert t["bucket"] == int(op.t_bucket[i])
+        assert t["bucket_offset"] == int(op.t_offset[i])
+        assert t["numel"] == numels[i]
+        assert t["owner"] == owners[i]
+
+
+@pytest.mark.parametrize("cid", workloads.ALL_IDS)
+def test_plan_matches_oracle_workloads(grs, orc, cid):
+    w = workloads.get(cid)
+    op = oracle.plan(w.numels, w.owners, w.world, w.tp, w.dp_replicate, w.dp_shard, w.bucket_bytes)
+    h = grs.grs_plan_create(w.numels, w.owners, w.world, w.tp, w.dp_replicate, w.dp_shard,
+                            w.bucket_bytes, grs.GRS_PLAN_HOST_ONLY)
+    try:
+        _compare_plan(grs, h, op, w.numels, w.owners)
+    finally:
+        grs.grs_plan_destroy(h)
+
+
+GOLD = json.load(open(os.path.join(ROOT, "tests", "golden", "plan_layouts.json")))
+
+
+@pytest.mark.parametrize("case", GOLD["cases"], ids=lambda c: c["name"])
+def test_plan_matches_hand_layouts(grs, orc, case):
+    h = grs.grs_plan_create(case["numel"], case["owner"], case["world"], case["tp"],
+                            case["dp_replicate"], case["dp_shard"], case["bucket_bytes"],
+                            grs.GRS_PLAN_HOST_ONLY)
+    try:
+        op = oracle.plan(case["numel"], case["owner"], case["world"], case["tp"],
+                         case["dp_replicate"], case["dp_shard"], case["bucket_bytes"])
+        _compare_plan(grs, h, op, case["numel"], case["owner"])
+        info = grs.grs_plan_query(h)
+        assert info["n_rank_pad"] == case["n_rank_pad"]
+        assert info["n_state_pad"] == case["n_state_pad"]
+    finally:
+        grs.grs_plan_destroy(h)
+
+
+@pytest.mark.parametrize("case", GOLD["rejections"], ids=lambda c: c["why"])
+def test_plan_rejections_match(grs, case):
+    with pytest.raises(grs.GrsError) as ei:
+        grs.grs_plan_create(case["numel"], case["owner"], case["world"], case["tp"],
+                            case["dp_replicate"], case["dp_shard"], case["bucket_bytes"],
+                            grs.GRS_PLAN_HOST_ONLY)
+    assert ei.value.status == case["status"]
+    assert grs.grs_last_error() != ""
+
+
+def test_world_above_limit_rejected(grs):
+    with pytest.raises(grs.GrsError) as ei:
+        grs.grs_plan_create([8], [0], 256, 1, 1, 256, 64, grs.GRS_PLAN_HOST_ONLY)
+    assert ei.value.status == grs.GRS_ERR_INVALID_ARG
+
+
+def test_random_plans_match_oracle(grs, orc):
+    rng = np.random.default_rng(1234)
+    for trial in range(150):
+        tp = int(rng.choice([1, 2, 3, 4]))
+        dr = int(rng.choice([1, 2, 3]))
+        ds = int(rng.choice([1, 2, 3, 4, 5]))
+        n = int(rng.integers(1, 30))
+        owners = [int(x) for x in rng.integers(0, 4, n)]
+        numels = []
+        for o in owners:
+            k = int(rng.integers(0, 300))
+            numels.append(k * tp if o == oracle.LOCAL_SHARD else k)
+        bb = int(rng.choice([2, 16, 64, 250, 1000, 1 << 20]))
+        world = tp * dr * ds
+        dsa = -1 if rng.random() < 0.2 else ds
+        op = oracle.plan(numels, owners, world, tp, dr, dsa, bb)
+        h = grs.grs_plan_create(numels, owners, world, tp, dr, dsa, bb, grs.GRS_PLAN_HOST_ONLY)
+        try:
+            _compare_plan(grs, h, op, numels, owners)
+        finally:
+            grs.grs_plan_destroy(h)
+
+
+def test_host_only_plan_refuses_launches(grs):
+    h = grs.grs_plan_create([64], [0], 2, 1, 1, 2, 1 << 20, grs.GRS_PLAN_HOST_ONLY)
+    try:
+        assert grs.grs_plan_query(h)["device"] == -1
+        with pytest.raises(grs.GrsError) as ei:
+            grs.grs_reduce_all(h, [16, 16], 16, 0, 0, None, 0)
+        assert ei.value.status == grs.GRS_ERR_NO_DEVICE
+        with pytest.raises(grs.GrsError) as ei:
+            hp = grs.make_adamw(1e-3, 0.9, 0.999, 1e-8, 0.0, 1.0, 1, 1)
+            grs.grs_clip_adamw_step(h, hp, 16, 16, 16, 16, 16, 16, 0)
+        assert ei.value.status == grs.GRS_ERR_NO_DEVICE
+    finally:
+        grs.grs_plan_destroy(h)
+
+
+def test_query_bounds(grs):
+    h = grs.grs_plan_create([64, 8], [0, 1], 1, 1, 1, 1, 1 << 20, grs.GRS_PLAN_HOST_ONLY)
+    try:
+        with pytest.raises(grs.GrsError):
+            grs.grs_bucket_info(h, 2)
+        with pytest.raises(grs.GrsError):
+            grs.grs_tensor_info(h, -1)
+    finally:
+        grs.grs_plan_destroy(h)
