@@ -2,7 +2,16 @@
 
 The compute path is libgrs.so (hand-written sm_103a CUDA kernels behind the
 C ABI in include/grs.h); `grs` is its thin ctypes binding with the same
-names.  Importing this package fails if the library has not been built.
+names.  Importing `grs` (or any of its names from this package) fails if
+the library has not been built: there is no fallback.
 """
-from . import grs  # noqa: F401  (fails loudly when libgrs.so is missing)
-from .grs import *  # noqa: F401,F403
+import importlib
+
+
+def __getattr__(name):
+    if name.startswith("_"):
+        raise AttributeError(name)  # private names and submodules such as _build
+    mod = importlib.import_module(__name__ + ".grs")
+    if name == "grs":
+        return mod
+    return getattr(mod, name)

@@ -184,18 +184,34 @@ def bf16_ordered(bits):
     return np.where(b & 0x8000, -mag, mag)
 
 
-def assert_bf16_within_1ulp(got_bits, want_bits, what):
-    g = np.asarray(got_bits).view(np.uint16) if np.asarray(got_bits).dtype != np.uint16 else got_bits
+def bf16_value(bits):
+    return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def assert_bf16_cast(got_bits, got_master, want_bits, want_master, what, rtol=RTOL, atol=ATOL):
+    """bf16 parameters.  (1) The kernel's bf16 is the round-to-nearest-even of
+    its own fp32 master, bit for bit (torch's CPU cast decides, in fp32).
+    (2) Against the oracle: within 1 bf16 ulp, widened by the fp32 master
+    tolerance where the masters themselves may differ by that much (values
+    near zero, where a bf16 ulp is far below abs 1e-7)."""
+    g = np.asarray(got_bits).view(np.uint16)
     w = np.asarray(want_bits, np.uint16)
-    gn = (g & 0x7FFF) > 0x7F80
-    wn = (w & 0x7FFF) > 0x7F80
+    rne = torch.from_numpy(np.asarray(got_master, np.float32)).to(torch.bfloat16)
+    rne = rne.view(torch.int16).numpy().view(np.uint16)
+    gn = np.isnan(bf16_value(g))
+    bad = (g != rne) & ~gn
+    assert not bad.any(), f"{what}: bf16 is not the RNE of the fp32 master at {np.flatnonzero(bad)[:5]}"
+    wn = np.isnan(bf16_value(w))
     assert np.array_equal(gn, wn), f"{what}: NaN positions differ"
-    d = np.abs(bf16_ordered(g) - bf16_ordered(w))
+    gv, wv = bf16_value(g), bf16_value(w)
+    ulp = np.abs(bf16_value(w ^ 1) - wv)  # spacing at the oracle's value
+    lim = ulp + atol + rtol * np.abs(np.asarray(want_master, np.float64))
+    d = np.abs(gv - wv)
     d[gn] = 0
-    if (d > 1).any():
-        i = np.flatnonzero(d > 1)[:5]
-        raise AssertionError(f"{what}: {int((d > 1).sum())} values beyond 1 bf16 ulp at {i.tolist()}: "
-                             f"got {g[i].tolist()} want {w[i].tolist()}")
+    if (d > lim).any():
+        i = np.flatnonzero(d > lim)[:5]
+        raise AssertionError(f"{what}: {int((d > lim).sum())} bf16 values beyond tolerance at "
+                             f"{i.tolist()}: got {g[i].tolist()} want {w[i].tolist()}")
 
 
 def padding_mask(op) -> np.ndarray:
