@@ -185,7 +185,7 @@ def run_gpu(args, rank, world_size, local_rank):
     import oracle  # CPU baseline leg only
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
-    w = workloads.get(args.workload)
+    w = workloads.get(args.workload, args.blocks)
     op = oracle.plan(w.numels, w.owners, w.world, w.tp, w.dp_replicate, w.dp_shard,
                      w.bucket_bytes)
     mb = mandatory_bytes(op, w.n_micro, w.world)
@@ -241,7 +241,7 @@ def run_gpu(args, rank, world_size, local_rank):
     clk = clocks.stop()
 
     # ---------------------------------------------------------------- e2e
-    e2e = run_e2e(u, args, torch)
+    e2e = None if args.no_e2e else run_e2e(u, args, torch)
 
     status = u.grs.grs_check_device_errors(u.plan, u.stream)
     u.close()
@@ -427,7 +427,7 @@ def cpu_baseline(w, op, mb, args, host=None):
 def run_reference(args, rank, world_size):
     """The oracle as the reference arm, on host cores, rank 0 only."""
     import oracle
-    w = workloads.get(args.workload)
+    w = workloads.get(args.workload, args.blocks)
     op = oracle.plan(w.numels, w.owners, w.world, w.tp, w.dp_replicate, w.dp_shard,
                      w.bucket_bytes)
     mb = mandatory_bytes(op, w.n_micro, w.world)
@@ -458,6 +458,9 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", type=int, default=1, choices=workloads.ALL_IDS)
+    ap.add_argument("--blocks", type=int, default=0,
+                    help="shrink workload 1 to this many blocks (small profiling case)")
+    ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--impl", default="grs", choices=["grs", "reference"])
     ap.add_argument("--soak", type=float, default=1.5, help="untimed seconds before timing")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -36,15 +36,19 @@ def _deps_mtime() -> float:
     return max(os.path.getmtime(f) for f in files)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile every source to an object and link libgrs.so (static cudart)."""
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps_mtime() and not extra_flags:
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), out: str = None) -> str:
+    """Compile every source to an object and link libgrs.so (static cudart).
+    `extra_flags` (e.g. -D overrides of tile constants) with `out` builds a
+    variant library elsewhere."""
+    lib = out or LIB
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= _deps_mtime() and not extra_flags:
+        return lib
+    build_dir = os.path.join(os.path.dirname(lib), "_build") if out else BUILD
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(build_dir, os.path.splitext(src)[0] + ".o")
         cmd = [cc, "-c", os.path.join(CSRC, src), "-o", obj, *_flags(extra_flags)]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -55,13 +59,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with cf.ThreadPoolExecutor(len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [cc, "-shared", "-o", tmp, *objs, *ARCH, "-Xcompiler", "-fPIC", "-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

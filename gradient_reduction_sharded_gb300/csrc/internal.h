@@ -12,9 +12,28 @@ namespace grs {
 
 // Reduction tiles: a tile carries STAGE_GRAD_BYTES of bf16 input (all the
 // group's rank rows for T elements), so T = STAGE_GRAD_BYTES / (2 * group),
-// capped at RED_MAX_T and a multiple of 8.
-constexpr int64_t STAGE_GRAD_BYTES = 32768;
-constexpr int64_t RED_MAX_T = 4096;
+// capped at RED_MAX_T, a multiple of 8, and small enough that two stages
+// (rank rows plus the old accumulator tile) fit in the shared-memory ring.
+// Measured on GB300: each rank row of a tile is one bulk copy, and copies
+// of 4 KB and more keep HBM busy where 1-2 KB copies do not.
+#ifndef GRS_STAGE_GRAD_BYTES
+#define GRS_STAGE_GRAD_BYTES 65536
+#endif
+#ifndef GRS_RED_MAX_T
+#define GRS_RED_MAX_T 8192
+#endif
+#ifndef GRS_RED_CWARPS
+#define GRS_RED_CWARPS 8
+#endif
+#ifndef GRS_RED_RING_KB
+#define GRS_RED_RING_KB 216
+#endif
+constexpr int64_t RED_RING_BYTES = int64_t(GRS_RED_RING_KB) * 1024;
+constexpr int64_t STAGE_GRAD_BYTES = GRS_STAGE_GRAD_BYTES;
+constexpr int64_t RED_MAX_T = GRS_RED_MAX_T;
+// Consumer warps of the reduction; the norm pass over acc uses the same
+// count so that both produce bit-identical per-tile partials.
+constexpr int RED_CWARPS = GRS_RED_CWARPS;
 // Update (clip + AdamW) and accumulate tiles.
 constexpr int64_t UPD_T = 2048;
 
@@ -94,11 +113,16 @@ namespace grs {
 
 // Workspace layout: [n_red_tiles floats: per-tile partial sums of acc^2]
 //                   [NORM_L2_BLOCKS doubles: second-level partials]
+//                   [one 32-bit ticket counter, zero between calls]
 constexpr int NORM_L2_BLOCKS = 128;
 inline int64_t ws_partials_offset() { return 0; }
 inline int64_t ws_level2_offset(int64_t n_red_tiles) {
   return ((n_red_tiles * 4 + 255) / 256) * 256;
 }
+inline int64_t ws_ticket_offset(int64_t n_red_tiles) {
+  return ws_level2_offset(n_red_tiles) + NORM_L2_BLOCKS * 8;
+}
+inline int64_t ws_bytes(int64_t n_red_tiles) { return ws_ticket_offset(n_red_tiles) + 256; }
 
 // Device flags
 enum : int { FLAG_TIMEOUT = 0, FLAG_NONFINITE = 1, FLAG_COUNT = 4 };

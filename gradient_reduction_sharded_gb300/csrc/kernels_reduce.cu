@@ -13,11 +13,14 @@
 // How (GB300): a persistent grid, one CTA per SM.  Warp 0 is a TMA producer:
 // for every tile it issues one 1-D bulk copy (cp.async.bulk) per rank row of
 // the tile's reduction group, plus the old accumulator tile when
-// accumulating, into a 4-stage shared-memory ring guarded by mbarriers.
-// Warps 1..4 consume a stage: 16-byte shared loads of 8 bf16 per rank,
+// accumulating, into a shared-memory ring (as many stages of the largest
+// tile as fit in the ring budget, at most 8) guarded by mbarriers.  Unit tables
+// are walked forward, never searched, and the consumers get each tile's
+// metadata through shared memory.
+// The consumer warps take a stage: 16-byte shared loads of 8 bf16 per rank,
 // fp32 adds in rank order, scale (and fused add of the old value), padding
 // masked to zero, coalesced 16-byte stores, and a fixed-order warp
-// butterfly for the norm partial.  The producer folds the four warp
+// butterfly for the norm partial.  The producer folds the consumer warps'
 // partials of a tile into one fp32 value in fixed order when the stage is
 // recycled, so the partial of a tile never depends on the grid size.
 // All mbarrier waits are bounded (device.cuh).
@@ -30,24 +33,29 @@ namespace grs {
 
 namespace {
 
-constexpr int RED_CWARPS = 4;
+#ifndef GRS_RED_MAX_STAGES
+#define GRS_RED_MAX_STAGES 8
+#endif
 constexpr int RED_CTHREADS = 32 * RED_CWARPS;
 constexpr int RED_THREADS = 32 + RED_CTHREADS;
-constexpr int RED_STAGES = 4;
-constexpr int RED_STAGE_BYTES = static_cast<int>(STAGE_GRAD_BYTES + RED_MAX_T * 4);
+constexpr int RED_MAX_STAGES = GRS_RED_MAX_STAGES;
 
+// Everything a consumer needs about the tile in one stage (written by the
+// producer before it arms the stage's barrier, so consumers touch no global
+// tables).
 struct StageMeta {
   int64_t tile;
-  int64_t e0;
-  int32_t unit;
-  int32_t n;
+  int64_t out_off;  // acc element offset of the tile's first element
+  int32_t n;        // elements in the tile (multiple of 8)
+  int32_t valid;    // elements before the padding starts (0..n)
+  int32_t gc;       // rank rows in the stage
+  float scale;
 };
 
-constexpr size_t RED_SMEM_BYTES = size_t(RED_STAGES) * RED_STAGE_BYTES  // ring
-                                  + 2 * RED_STAGES * sizeof(uint64_t)    // full/empty barriers
-                                  + RED_STAGES * sizeof(StageMeta)       // tile of each stage
-                                  + RED_STAGES * RED_CWARPS * sizeof(float)  // warp partials
-                                  + 16;                                   // abort flag
+constexpr size_t RED_SMEM_TAIL = 2 * RED_MAX_STAGES * sizeof(uint64_t)        // full/empty
+                                 + RED_MAX_STAGES * sizeof(StageMeta)          // tile metadata
+                                 + RED_MAX_STAGES * RED_CWARPS * sizeof(float) // warp partials
+                                 + 16;                                          // abort flag
 
 struct ReduceArgs {
   const uint16_t* ranks[GRS_MAX_WORLD];
@@ -63,6 +71,8 @@ struct ReduceArgs {
   int32_t unit_begin;
   int32_t unit_end;
   int32_t accumulate;
+  int32_t stages;       // ring depth (<= RED_MAX_STAGES)
+  int32_t stage_bytes;  // bytes per stage (multiple of 128)
 };
 
 __device__ __forceinline__ float fold_partials(const float* wp) {
@@ -74,17 +84,18 @@ __device__ __forceinline__ float fold_partials(const float* wp) {
 
 __global__ void __launch_bounds__(RED_THREADS, 1) reduce_kernel(const __grid_constant__ ReduceArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
+  const int S = a.stages;
   uint8_t* ring = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(RED_STAGES) * RED_STAGE_BYTES);
-  uint64_t* empty = full + RED_STAGES;
-  StageMeta* meta = reinterpret_cast<StageMeta*>(empty + RED_STAGES);
-  float* wp = reinterpret_cast<float*>(meta + RED_STAGES);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(wp + RED_STAGES * RED_CWARPS);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(S) * a.stage_bytes);
+  uint64_t* empty = full + RED_MAX_STAGES;
+  StageMeta* meta = reinterpret_cast<StageMeta*>(empty + RED_MAX_STAGES);
+  float* wp = reinterpret_cast<float*>(meta + RED_MAX_STAGES);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(wp + RED_MAX_STAGES * RED_CWARPS);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < RED_STAGES; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], RED_CWARPS);
     }
@@ -99,9 +110,29 @@ __global__ void __launch_bounds__(RED_THREADS, 1) reduce_kernel(const __grid_con
     const uint64_t pol = l2_policy_evict_first();
     int64_t iter = 0;
     bool ok = true;
+    // The CTA's tiles increase monotonically, so the unit only moves forward.
+    int u = a.unit_begin;
+    int64_t u_next = __ldg(a.prefix + u + 1);
+    UnitDesc ud = a.units[u];
     for (int64_t tile = a.tile_begin + blockIdx.x; tile < a.tile_end; tile += stride, ++iter) {
-      const int s = static_cast<int>(iter % RED_STAGES);
-      const uint32_t ph = static_cast<uint32_t>((iter / RED_STAGES) & 1);
+      const int s = static_cast<int>(iter % S);
+      const uint32_t ph = static_cast<uint32_t>((iter / S) & 1);
+      if (tile >= u_next) {
+        do {
+          ++u;
+          u_next = __ldg(a.prefix + u + 1);
+        } while (tile >= u_next);
+        ud = a.units[u];
+      }
+      const int64_t T = ud.red_T;
+      const int64_t e0 = (tile - ud.red_tile0) * T;
+      const int64_t rem = ud.padded - e0;
+      const int32_t n = static_cast<int32_t>(rem < T ? rem : T);
+      const int64_t vrem = ud.used - e0;
+      const int32_t valid = static_cast<int32_t>(vrem <= 0 ? 0 : (vrem < n ? vrem : n));
+      const uint32_t grad_bytes = static_cast<uint32_t>(ud.g_count) * static_cast<uint32_t>(n) * 2u;
+      const uint32_t bytes = grad_bytes + (a.accumulate ? static_cast<uint32_t>(n) * 4u : 0u);
+      const int64_t out_off = ud.state_off - a.state_base + e0;
       int good = 1;
       if (lane == 0) good = mbar_wait_bounded(&empty[s], ph ^ 1u, a.flags, abort_flag) ? 1 : 0;
       good = __shfl_sync(0xffffffffu, good, 0);
@@ -109,44 +140,33 @@ __global__ void __launch_bounds__(RED_THREADS, 1) reduce_kernel(const __grid_con
         ok = false;
         break;
       }
-      if (lane == 0 && a.partials != nullptr && iter >= RED_STAGES)
-        a.partials[meta[s].tile] = fold_partials(wp + s * RED_CWARPS);
-      const int u = find_unit(a.prefix, a.unit_begin, a.unit_end, tile);
-      const UnitDesc* ud = a.units + u;
-      const int64_t T = ud->red_T;
-      const int64_t e0 = (tile - ud->red_tile0) * T;
-      const int64_t rem = ud->padded - e0;
-      const int32_t n = static_cast<int32_t>(rem < T ? rem : T);
-      const int32_t gc = ud->g_count;
-      const int32_t gs = ud->g_start;
-      const int32_t gst = ud->g_stride;
-      const uint32_t grad_bytes = static_cast<uint32_t>(gc) * static_cast<uint32_t>(n) * 2u;
-      const uint32_t bytes = grad_bytes + (a.accumulate ? static_cast<uint32_t>(n) * 4u : 0u);
-      uint8_t* st = ring + size_t(s) * RED_STAGE_BYTES;
+      uint8_t* st = ring + size_t(s) * a.stage_bytes;
       if (lane == 0) {
-        meta[s].tile = tile;
-        meta[s].e0 = e0;
-        meta[s].unit = u;
-        meta[s].n = n;
+        if (a.partials != nullptr && iter >= S) a.partials[meta[s].tile] = fold_partials(wp + s * RED_CWARPS);
+        StageMeta& md = meta[s];
+        md.tile = tile;
+        md.out_off = out_off;
+        md.n = n;
+        md.valid = valid;
+        md.gc = ud.g_count;
+        md.scale = ud.scale;
         mbar_arrive_expect_tx(&full[s], bytes);
       }
       __syncwarp();
-      const int64_t roff = ud->rank_off - a.rank_base + e0;
-      for (int i = lane; i < gc; i += 32)
-        bulk_g2s(st + size_t(i) * n * 2, a.ranks[gs + i * gst] + roff, static_cast<uint32_t>(n) * 2u,
-                 &full[s], pol);
+      const int64_t roff = ud.rank_off - a.rank_base + e0;
+      for (int i = lane; i < ud.g_count; i += 32)
+        bulk_g2s(st + size_t(i) * n * 2, a.ranks[ud.g_start + i * ud.g_stride] + roff,
+                 static_cast<uint32_t>(n) * 2u, &full[s], pol);
       if (a.accumulate && lane == 0)
-        bulk_g2s(st + grad_bytes, a.acc + (ud->state_off - a.state_base) + e0,
-                 static_cast<uint32_t>(n) * 4u, &full[s]);
+        bulk_g2s(st + grad_bytes, a.acc + out_off, static_cast<uint32_t>(n) * 4u, &full[s]);
     }
     if (lane == 0) {
-      const int64_t first = iter > RED_STAGES ? iter - RED_STAGES : 0;
+      const int64_t first = iter > S ? iter - S : 0;
       if (ok) {
         // Drain: the last stages' partials become final once consumers release them.
         for (int64_t k = first; k < iter; ++k) {
-          const int s = static_cast<int>(k % RED_STAGES);
-          if (!mbar_wait_bounded(&empty[s], static_cast<uint32_t>((k / RED_STAGES) & 1), a.flags,
-                                 abort_flag))
+          const int s = static_cast<int>(k % S);
+          if (!mbar_wait_bounded(&empty[s], static_cast<uint32_t>((k / S) & 1), a.flags, abort_flag))
             break;
           if (a.partials != nullptr) a.partials[meta[s].tile] = fold_partials(wp + s * RED_CWARPS);
         }
@@ -155,9 +175,8 @@ __global__ void __launch_bounds__(RED_THREADS, 1) reduce_kernel(const __grid_con
         // Let every copy this CTA issued land before the CTA exits.
         volatile int no_abort = 0;
         for (int64_t k = first; k < iter; ++k) {
-          const int s = static_cast<int>(k % RED_STAGES);
-          if (!mbar_wait_bounded(&full[s], static_cast<uint32_t>((k / RED_STAGES) & 1), a.flags,
-                                 &no_abort))
+          const int s = static_cast<int>(k % S);
+          if (!mbar_wait_bounded(&full[s], static_cast<uint32_t>((k / S) & 1), a.flags, &no_abort))
             break;
         }
       }
@@ -168,17 +187,14 @@ __global__ void __launch_bounds__(RED_THREADS, 1) reduce_kernel(const __grid_con
     const int cw = ct >> 5;
     int64_t iter = 0;
     for (int64_t tile = a.tile_begin + blockIdx.x; tile < a.tile_end; tile += stride, ++iter) {
-      const int s = static_cast<int>(iter % RED_STAGES);
-      const uint32_t ph = static_cast<uint32_t>((iter / RED_STAGES) & 1);
+      const int s = static_cast<int>(iter % S);
+      const uint32_t ph = static_cast<uint32_t>((iter / S) & 1);
       if (!mbar_wait_bounded(&full[s], ph, a.flags, abort_flag)) break;
       const StageMeta md = meta[s];
-      const UnitDesc* ud = a.units + md.unit;
-      const float scale = ud->scale;
-      const int64_t used = ud->used;
-      const int32_t gc = ud->g_count;
+      const int32_t gc = md.gc;
       const int32_t n = md.n;
-      float* out = a.acc + (ud->state_off - a.state_base) + md.e0;
-      const uint8_t* st = ring + size_t(s) * RED_STAGE_BYTES;
+      float* out = a.acc + md.out_off;
+      const uint8_t* st = ring + size_t(s) * a.stage_bytes;
       const size_t row = size_t(n) * 2;
       const float* old = reinterpret_cast<const float*>(st + size_t(gc) * row);
       float psum = 0.0f;
@@ -206,18 +222,18 @@ __global__ void __launch_bounds__(RED_THREADS, 1) reduce_kernel(const __grid_con
                                __uint_as_float(q0.w), __uint_as_float(q1.x), __uint_as_float(q1.y),
                                __uint_as_float(q1.z), __uint_as_float(q1.w)};
 #pragma unroll
-          for (int q = 0; q < 8; ++q) o[q] = __fmaf_rn(v[q], scale, ov[q]);
+          for (int q = 0; q < 8; ++q) o[q] = __fmaf_rn(v[q], md.scale, ov[q]);
         } else {
 #pragma unroll
-          for (int q = 0; q < 8; ++q) o[q] = __fmul_rn(v[q], scale);
+          for (int q = 0; q < 8; ++q) o[q] = __fmul_rn(v[q], md.scale);
         }
-        const int64_t e = md.e0 + int64_t(c) * 8;
-        if (e + 8 > used) {
+        const int el = c * 8;
+        if (el + 8 > md.valid) {
 #pragma unroll
           for (int q = 0; q < 8; ++q)
-            if (e + q >= used) o[q] = 0.0f;
+            if (el + q >= md.valid) o[q] = 0.0f;
         }
-        float4* o4 = reinterpret_cast<float4*>(out + int64_t(c) * 8);
+        float4* o4 = reinterpret_cast<float4*>(out + el);
         o4[0] = make_float4(o[0], o[1], o[2], o[3]);
         o4[1] = make_float4(o[4], o[5], o[6], o[7]);
 #pragma unroll
@@ -230,6 +246,73 @@ __global__ void __launch_bounds__(RED_THREADS, 1) reduce_kernel(const __grid_con
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
+  }
+}
+
+// Direct-load variant (compile with -DGRS_REDUCE_DIRECT): one block of
+// RED_CTHREADS threads per tile, each thread loads its 8 elements of every rank row with
+// 16-byte non-allocating global loads and keeps them in registers.  Same
+// per-tile partial order as the staged kernel.
+__global__ void __launch_bounds__(RED_CTHREADS) reduce_direct_kernel(const __grid_constant__ ReduceArgs a) {
+  __shared__ float wps[RED_CWARPS];
+  const int64_t tile = a.tile_begin + blockIdx.x;
+  const int u = find_unit(a.prefix, a.unit_begin, a.unit_end, tile);
+  const UnitDesc* ud = a.units + u;
+  const int64_t T = ud->red_T;
+  const int64_t e0 = (tile - ud->red_tile0) * T;
+  const int64_t rem = ud->padded - e0;
+  const int n = static_cast<int>(rem < T ? rem : T);
+  const int64_t vrem = ud->used - e0;
+  const int valid = static_cast<int>(vrem <= 0 ? 0 : (vrem < n ? vrem : n));
+  const int gc = ud->g_count, gs = ud->g_start, gst = ud->g_stride;
+  const float scale = ud->scale;
+  const int64_t roff = ud->rank_off - a.rank_base + e0;
+  float* out = a.acc + (ud->state_off - a.state_base) + e0;
+  float psum = 0.0f;
+  for (int c = threadIdx.x; c < (n >> 3); c += RED_CTHREADS) {
+    float v[8];
+    {
+      const uint4 w = __ldcs(reinterpret_cast<const uint4*>(a.ranks[gs] + roff) + c);
+      set_bf16x8(v, w);
+    }
+    int i = 1;
+    for (; i + 7 < gc; i += 8) {
+      uint4 w[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        w[q] = __ldcs(reinterpret_cast<const uint4*>(a.ranks[gs + (i + q) * gst] + roff) + c);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) add_bf16x8(v, w[q]);
+    }
+    for (; i < gc; ++i)
+      add_bf16x8(v, __ldcs(reinterpret_cast<const uint4*>(a.ranks[gs + i * gst] + roff) + c));
+    float o[8];
+    float4* o4 = reinterpret_cast<float4*>(out + c * 8);
+    if (a.accumulate) {
+      const float4 q0 = o4[0], q1 = o4[1];
+      const float ov[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+      for (int q = 0; q < 8; ++q) o[q] = __fmaf_rn(v[q], scale, ov[q]);
+    } else {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) o[q] = __fmul_rn(v[q], scale);
+    }
+    const int el = c * 8;
+    if (el + 8 > valid) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (el + q >= valid) o[q] = 0.0f;
+    }
+    o4[0] = make_float4(o[0], o[1], o[2], o[3]);
+    o4[1] = make_float4(o[4], o[5], o[6], o[7]);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) psum = __fmaf_rn(o[q], o[q], psum);
+  }
+  if (a.partials != nullptr) {
+    psum = warp_sum(psum);
+    if ((threadIdx.x & 31) == 0) wps[threadIdx.x >> 5] = psum;
+    __syncthreads();
+    if (threadIdx.x == 0) a.partials[tile] = fold_partials(wps);
   }
 }
 
@@ -254,15 +337,33 @@ int launch_reduce(const grs_plan* p, const ReduceLaunch& l, void* stream) {
   a.accumulate = l.accumulate;
   const int64_t tiles = a.tile_end - a.tile_begin;
   if (tiles <= 0) return 0;
+  // Stage size: the largest tile of the launched units (rank rows plus the
+  // old accumulator tile when accumulating), rounded to 128 bytes.
+  int64_t need = 128;
+  for (int32_t u = l.unit_begin; u < l.unit_end; ++u) {
+    const UnitDesc& d = p->units[u];
+    const int64_t b = int64_t(d.g_count) * d.red_T * 2 + (l.accumulate ? int64_t(d.red_T) * 4 : 0);
+    need = b > need ? b : need;
+  }
+  need = (need + 127) / 128 * 128;
+  int stages = static_cast<int>(RED_RING_BYTES / need);  // >= 2 by the plan's tile cap
+  stages = stages > RED_MAX_STAGES ? RED_MAX_STAGES : stages;
+  if (stages < 2) return static_cast<int>(cudaErrorInvalidConfiguration);
+  a.stages = stages;
+  a.stage_bytes = static_cast<int32_t>(need);
+  const size_t smem = size_t(stages) * need + RED_SMEM_TAIL;
   if (p->device >= 0 && p->device < 64 && !g_attr_set[p->device]) {
     cudaError_t e = cudaFuncSetAttribute(reduce_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(RED_SMEM_BYTES));
+                                         static_cast<int>(RED_RING_BYTES + RED_SMEM_TAIL));
     if (e != cudaSuccess) return static_cast<int>(e);
     g_attr_set[p->device] = true;
   }
+#ifdef GRS_REDUCE_DIRECT
+  reduce_direct_kernel<<<static_cast<unsigned>(tiles), RED_CTHREADS, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  return static_cast<int>(cudaGetLastError());
+#endif
   const int64_t grid = tiles < p->sm_count ? tiles : p->sm_count;
-  reduce_kernel<<<static_cast<unsigned>(grid), RED_THREADS, RED_SMEM_BYTES,
-                  static_cast<cudaStream_t>(stream)>>>(a);
+  reduce_kernel<<<static_cast<unsigned>(grid), RED_THREADS, smem, static_cast<cudaStream_t>(stream)>>>(a);
   return static_cast<int>(cudaGetLastError());
 }
 

@@ -24,15 +24,16 @@ namespace grs {
 
 namespace {
 
-constexpr int NORM1_THREADS = 128;  // must equal the reduction's consumer threads
+constexpr int NORM1_THREADS = 32 * RED_CWARPS;  // the reduction's consumer threads
 constexpr int NORM2_THREADS = 256;
 constexpr int UPD_THREADS = 256;
 static_assert(UPD_T == UPD_THREADS * 8, "one 8-element group per thread per tile");
 
 // ----------------------------------------------------------------- norm pass 1
 // Same thread -> chunk map and the same fp32 operation order as the
-// reduction's fused epilogue: thread c of 128 sums chunks c, c+128, ... of
-// 8 elements with fmaf(x, x, s); warp butterfly; warps folded 0..3.
+// reduction's fused epilogue: thread c of NORM1_THREADS sums chunks c,
+// c+NORM1_THREADS, ... of 8 elements with fmaf(x, x, s); warp butterfly;
+// warps folded in order.
 __global__ void __launch_bounds__(NORM1_THREADS) norm_pass1_kernel(const float* __restrict__ acc,
                                                                    const UnitDesc* __restrict__ units,
                                                                    const int64_t* __restrict__ prefix,
@@ -87,9 +88,18 @@ __device__ __forceinline__ double block_sum_fixed(double x, double* red) {
   return s;
 }
 
-__global__ void __launch_bounds__(NORM2_THREADS) norm_level2_kernel(const float* __restrict__ partials,
-                                                                    int64_t n, double* __restrict__ level2) {
+// One launch: block b sums its contiguous range of tile partials in fp64
+// (thread t takes indices t, t+256, ... in order, then a fixed tree) into
+// level2[b]; the block that finishes last (a ticket counter in the
+// workspace, reset by that block) sums level2[0..NORM_L2_BLOCKS) in a fixed
+// tree.  Which block is last varies, the order of every addition does not.
+__global__ void __launch_bounds__(NORM2_THREADS) norm_finish_kernel(const float* __restrict__ partials,
+                                                                    int64_t n, double* __restrict__ level2,
+                                                                    unsigned int* __restrict__ ticket,
+                                                                    double inv_m2, double* __restrict__ out,
+                                                                    int* __restrict__ flags) {
   __shared__ double red[NORM2_THREADS / 32];
+  __shared__ bool last;
   const int64_t chunk = (n + NORM_L2_BLOCKS - 1) / NORM_L2_BLOCKS;
   const int64_t lo = blockIdx.x * chunk;
   const int64_t hi = lo + chunk < n ? lo + chunk : n;
@@ -97,18 +107,22 @@ __global__ void __launch_bounds__(NORM2_THREADS) norm_level2_kernel(const float*
   for (int64_t i = lo + threadIdx.x; i < hi; i += NORM2_THREADS)
     s = __dadd_rn(s, static_cast<double>(partials[i]));
   s = block_sum_fixed(s, red);
-  if (threadIdx.x == 0) level2[blockIdx.x] = s;
-}
-
-__global__ void __launch_bounds__(NORM_L2_BLOCKS) norm_final_kernel(const double* __restrict__ level2,
-                                                                     double inv_m2, double* __restrict__ out,
-                                                                     int* __restrict__ flags) {
-  __shared__ double red[NORM_L2_BLOCKS / 32];
-  double s = block_sum_fixed(level2[threadIdx.x], red);
   if (threadIdx.x == 0) {
-    s = __dmul_rn(s, inv_m2);
-    *out = s;
-    if (!isfinite(s)) atomicOr(flags + FLAG_NONFINITE, 1);
+    level2[blockIdx.x] = s;
+    __threadfence();
+    last = atomicAdd(ticket, 1u) == NORM_L2_BLOCKS - 1;
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  double x = threadIdx.x < NORM_L2_BLOCKS ? __ldcg(level2 + threadIdx.x) : 0.0;
+  __syncthreads();  // red[] is reused
+  x = block_sum_fixed(x, red);
+  if (threadIdx.x == 0) {
+    x = __dmul_rn(x, inv_m2);
+    *out = x;
+    if (!isfinite(x)) atomicOr(flags + FLAG_NONFINITE, 1);
+    *ticket = 0u;
   }
 }
 
@@ -235,9 +249,10 @@ int launch_norm(const grs_plan* p, const float* acc, int32_t n_micro, void* work
         acc, p->d_units, p->d_red_prefix, static_cast<int32_t>(p->units.size()), p->n_red_tiles,
         partials);
   }
-  norm_level2_kernel<<<NORM_L2_BLOCKS, NORM2_THREADS, 0, s>>>(partials, p->n_red_tiles, level2);
+  unsigned int* ticket = reinterpret_cast<unsigned int*>(ws + ws_ticket_offset(p->n_red_tiles));
   const double inv_m = 1.0 / static_cast<double>(n_micro);
-  norm_final_kernel<<<1, NORM_L2_BLOCKS, 0, s>>>(level2, inv_m * inv_m, d_norm_sq, p->d_flags);
+  norm_finish_kernel<<<NORM_L2_BLOCKS, NORM2_THREADS, 0, s>>>(partials, p->n_red_tiles, level2, ticket,
+                                                             inv_m * inv_m, d_norm_sq, p->d_flags);
   return static_cast<int>(cudaGetLastError());
 }
 

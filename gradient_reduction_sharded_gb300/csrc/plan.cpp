@@ -128,7 +128,8 @@ grs_status build_plan(const int64_t* numels, const int32_t* owners, int32_t n, i
     bk.rank_off = rank_off;
     bk.state_off = state_off;
     bk.unit0 = static_cast<int32_t>(p->units.size());
-    int64_t T = STAGE_GRAD_BYTES / (2 * static_cast<int64_t>(bk.group_size));
+    const int64_t gsz = bk.group_size;
+    int64_t T = std::min<int64_t>(STAGE_GRAD_BYTES / (2 * gsz), RED_RING_BYTES / (2 * (2 * gsz + 4)));
     T = std::min<int64_t>(RED_MAX_T, std::max<int64_t>(8, T / 8 * 8));
     for (int32_t t = 0; t < bk.copies; ++t) {
       UnitDesc u{};
@@ -171,8 +172,7 @@ grs_status build_plan(const int64_t* numels, const int32_t* owners, int32_t n, i
   p->n_state_pad = state_off;
   p->n_red_tiles = red_tiles;
   p->n_upd_tiles = upd_tiles;
-  p->workspace_bytes =
-      ws_level2_offset(red_tiles) + static_cast<int64_t>(NORM_L2_BLOCKS) * sizeof(double);
+  p->workspace_bytes = ws_bytes(red_tiles);
 
   // Gather jobs: one per (tensor, state row).
   p->jobs.clear();

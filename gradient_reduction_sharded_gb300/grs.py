@@ -12,7 +12,9 @@ import os
 from typing import Dict, Optional, Sequence
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libgrs.so")
+# GRS_LIBRARY may name another build of the same library (e.g. a variant
+# compiled with different tile constants); default: the in-tree build.
+LIB_PATH = os.environ.get("GRS_LIBRARY") or os.path.join(_HERE, "libgrs.so")
 
 GRS_REPLICA_AVG, GRS_PARTIAL_SUM, GRS_LOCAL_SHARD, GRS_ALREADY_REDUCED = 0, 1, 2, 3
 GRS_OK = 0

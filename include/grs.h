@@ -104,7 +104,7 @@ typedef struct grs_plan_info {
   int64_t n_unique;       /* N: logical parameter elements */
   int64_t n_rank_pad;     /* elements of each rank's gradient buffer */
   int64_t n_state_pad;    /* elements of accumulator / master / m / v / params */
-  int64_t workspace_bytes;/* device workspace needed by reduce / norm calls */
+  int64_t workspace_bytes;/* device workspace needed by reduce / norm calls; zero it once */
   int64_t n_reduce_tiles; /* norm partial slots (one per reduction tile) */
 } grs_plan_info;
 
@@ -195,7 +195,9 @@ grs_status grs_tensor_info(const grs_plan* plan, int32_t tensor, grs_tensor_desc
  *   emit_norm_partials : 1 on the last microbatch: also write the bucket's
  *                per-tile sums of acc^2 into the workspace, so that
  *                grs_grad_norm_sq needs no second pass over acc.
- *   workspace  : device, >= workspace_bytes; required when emitting.
+ *   workspace  : device, >= workspace_bytes, zero-filled once before its
+ *                first use (the library leaves its counter at zero after
+ *                every call); required when emitting.
  * Errors: INVALID_ARG, ALIGNMENT (every pointer 16-B aligned), NO_DEVICE,
  * CUDA (launch failure). */
 grs_status grs_reduce_bucket(const grs_plan* plan, int32_t bucket, const uint16_t* const* rank_grads,
@@ -225,6 +227,8 @@ grs_status grs_accumulate(const grs_plan* plan, int32_t bucket, float* acc, cons
  *   partials_ready : 1 when every bucket's last reduce emitted its
  *                    partials into `workspace` (no pass over acc).
  *   d_norm_sq      : device double [1].
+ *   workspace      : as for grs_reduce_bucket (zero-filled before first use).
+ * Calls sharing one workspace must not overlap on the GPU.
  * A non-finite S raises the device flag reported as NONFINITE by
  * grs_check_device_errors; the step still proceeds (NaN propagates). */
 grs_status grs_grad_norm_sq(const grs_plan* plan, const float* acc, int32_t n_micro,

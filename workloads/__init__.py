@@ -122,15 +122,16 @@ def _tiny() -> Workload:
 # 16 blocks x 4 [1024,1024] matrices: 3 REPLICA_AVG + 1 LOCAL_SHARD each,
 # plus 16 PARTIAL_SUM norm vectors [1024].
 # ---------------------------------------------------------------------------
-def _synthetic67m() -> Workload:
+def _synthetic67m(blocks: int = 16) -> Workload:
     ts = []
-    for i in range(16):
+    for i in range(blocks):
         ts.append(Tensor(f"blk{i}.norm", (1024,), PARTIAL_SUM))
         ts.append(Tensor(f"blk{i}.w0", (1024, 1024), REPLICA_AVG))
         ts.append(Tensor(f"blk{i}.w1", (1024, 1024), REPLICA_AVG))
         ts.append(Tensor(f"blk{i}.w2", (1024, 1024), REPLICA_AVG))
         ts.append(Tensor(f"blk{i}.w_tp", (1024, 1024), LOCAL_SHARD))
-    return Workload(1, "synthetic-67M-world16", ts, tp=2, dp_replicate=2, dp_shard=4,
+    name = "synthetic-67M-world16" if blocks == 16 else f"synthetic-{blocks}blk-world16"
+    return Workload(1, name, ts, tp=2, dp_replicate=2, dp_shard=4,
                     n_micro=1, grad_std=1e-3,
                     adamw=AdamW(1e-3, 0.9, 0.999, 1e-8, 0.01, 1.0))
 
@@ -212,7 +213,11 @@ def _llama3b() -> Workload:
                     adamw=AdamW(3e-4, 0.9, 0.999, 1e-8, 0.1, 1.0))
 
 
-def get(cid: int) -> Workload:
+def get(cid: int, blocks: int = 0) -> Workload:
+    """Workload `cid`.  `blocks` > 0 shrinks workload 1 to that many blocks
+    (same tensor shapes and geometry; used for small profiling cases)."""
+    if cid == 1 and blocks > 0:
+        return _synthetic67m(blocks)
     return {0: _tiny, 1: _synthetic67m, 2: _llama1b, 3: _qwen3_moe, 4: _llama3b}[cid]()
 
 
