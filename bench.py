@@ -327,16 +327,30 @@ def run_e2e(u: GpuUpdate, args, torch):
             "steps": steps, "path": "pinned host buffers -> device copies -> C-ABI calls -> host"}
 
 
+def csrc_hash() -> str:
+    """Hash of the kernel sources, to tell whether stored counters still apply."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "gradient_reduction_sharded_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def load_traffic(kernel: str, w):
-    """DRAM bytes per launch from the committed ncu summary, if it matches."""
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    workload was not captured or the kernels changed since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             t = json.load(f)
-        ent = t.get(f"{kernel}:{w.name}")
-        return None if ent is None else ent.get("bytes_per_launch")
     except (OSError, ValueError):
         return None
+    if t.get("csrc_sha256_16") != csrc_hash():
+        return None
+    ent = t.get(f"{kernel}:{w.name}")
+    return None if ent is None else ent.get("bytes_per_launch")
 
 
 # --------------------------------------------------------------------------- CPU arm
