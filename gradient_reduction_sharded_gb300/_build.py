@@ -14,7 +14,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgrs.so")
 
-SOURCES = ["plan.cpp", "api.cu", "kernels_reduce.cu", "kernels_update.cu", "kernels_gather.cu"]
+SOURCES = ["plan.cpp", "api.cu", "kernels_reduce.cu", "kernels_update.cu", "kernels_gather.cu",
+           "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

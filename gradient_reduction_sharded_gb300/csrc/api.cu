@@ -75,6 +75,10 @@ void free_device(grs_plan* p) {
 
 }  // namespace
 
+namespace grs {
+void set_last_error(const std::string& msg) { g_last_error = msg; }
+}  // namespace grs
+
 extern "C" {
 
 grs_status grs_plan_create(const int64_t* numels, const int32_t* owners, int32_t n_tensors,

@@ -127,6 +127,9 @@ inline int64_t ws_bytes(int64_t n_red_tiles) { return ws_ticket_offset(n_red_til
 // Device flags
 enum : int { FLAG_TIMEOUT = 0, FLAG_NONFINITE = 1, FLAG_COUNT = 4 };
 
+// Sets the message grs_last_error() returns on this thread (api.cu).
+void set_last_error(const std::string& msg);
+
 // host plan builder (plan.cpp)
 grs_status build_plan(const int64_t* numels, const int32_t* owners, int32_t n, int32_t world,
                       int32_t tp, int32_t dp_replicate, int32_t dp_shard, int64_t bucket_bytes,

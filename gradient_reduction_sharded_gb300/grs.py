@@ -28,6 +28,7 @@ GRS_ERR_NONFINITE = 7
 GRS_ERR_NO_DEVICE = 8
 GRS_PLAN_HOST_ONLY = 1
 GRS_MAX_WORLD = 128
+GRS_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED_COMPOSITION", 3: "SHAPE",
                 4: "ALIGNMENT", 5: "CUDA", 6: "TIMEOUT", 7: "NONFINITE", 8: "NO_DEVICE"}
@@ -93,6 +94,7 @@ _sig = {
     "grs_clip_adamw_step": ([_vp, _P(grs_adamw), _vp, _vp, _vp, _vp, _vp, _vp, _vp], ctypes.c_int),
     "grs_gather_params": ([_vp, _vp, _P(_vp), _vp], ctypes.c_int),
     "grs_check_device_errors": ([_vp, _vp], ctypes.c_int),
+    "grs_grad_norm_sq_noalloc": ([_vp, _vp, ctypes.c_int32, _vp, _vp], ctypes.c_int),
     "grs_last_error": ([], ctypes.c_char_p),
 }
 for _name, (_args, _res) in _sig.items():
@@ -192,6 +194,13 @@ def grs_gather_params(plan: int, params_bf16: int, tensor_ptrs: Sequence[Optiona
                       stream: int) -> None:
     _check(_lib.grs_gather_params(plan, params_bf16, _ptrs(tensor_ptrs), stream),
            "grs_gather_params")
+
+
+def grs_grad_norm_sq_noalloc(plan: int, acc: int, n_micro: int, d_norm_sq: int, stream: int) -> None:
+    """Global squared norm with the library's static scratch (no workspace,
+    no allocation); for callers that cannot allocate device memory."""
+    _check(_lib.grs_grad_norm_sq_noalloc(plan, acc, n_micro, d_norm_sq, stream),
+           "grs_grad_norm_sq_noalloc")
 
 
 def grs_check_device_errors(plan: int, stream: int) -> int:

@@ -267,6 +267,38 @@ grs_status grs_clip_adamw_step(const grs_plan* plan, const grs_adamw* hp, const 
 grs_status grs_gather_params(const grs_plan* plan, const uint16_t* params_bf16,
                              uint16_t* const* tensor_ptrs, void* stream);
 
+/* ------------------------------------------------- allocation-free variant */
+
+/* Size of the library's own scratch array for grs_grad_norm_sq_noalloc. */
+#define GRS_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/* The pages have no counterpart to this entry point: it is a convenience
+ * for callers that cannot allocate device memory — e.g. a process whose
+ * framework caching allocator already holds (nearly) all of the GPU's
+ * memory, latency-critical code that cannot take the device synchronisation
+ * an allocation may cause, or a host that only receives device pointers
+ * from another runtime.
+ *
+ * Computes the same global squared norm as grs_grad_norm_sq with
+ * partials_ready = 0 (a pass over the accumulator, then the fixed-order
+ * fp64 finish; bit-identical results) but needs no workspace: the scratch
+ * is a file-scope device array of GRS_NOALLOC_SCRATCH_BYTES (4 MiB) that
+ * every GPU loading the library holds until the process exits.
+ *   acc       : device fp32 [n_state_pad] (read).
+ *   d_norm_sq : device double [1] (written).
+ * The caller passes the input and the output; nothing is allocated (no
+ * cudaMalloc/cudaFree, no allocating library call).  The first call on a
+ * device looks up the array's device address with that device current;
+ * make that first call before any stream capture.  All calls share the
+ * array and it keeps the last call's contents (its counter is cleared on
+ * the stream before each launch); calls that overlap on the GPU — from two
+ * streams or two threads — race and must be serialised by the caller.
+ * Errors: INVALID_ARG (NULL, n_micro < 1), ALIGNMENT, NO_DEVICE, SHAPE when
+ * the plan needs more scratch than the array holds (more than about a
+ * million reduction tiles; the message gives both sizes), CUDA. */
+grs_status grs_grad_norm_sq_noalloc(const grs_plan* plan, const float* acc, int32_t n_micro,
+                                    double* d_norm_sq, void* stream);
+
 /* Synchronise `stream`, read and clear the plan's device flags.  Returns
  * TIMEOUT if a bounded device wait gave up, NONFINITE if a global norm was
  * NaN/Inf since the last check, else OK (or CUDA). */
