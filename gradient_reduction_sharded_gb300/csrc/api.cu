@@ -119,6 +119,7 @@ void grs_plan_destroy(grs_plan* p) {
   if (p == nullptr) return;
   if (p->device >= 0) {
     DeviceGuard g(p->device);
+    grs::destroy_host_step_resources(p);
     free_device(p);
   }
   delete p;

@@ -107,6 +107,7 @@ struct grs_plan {
   int64_t* d_upd_prefix = nullptr;
   grs::GatherJob* d_jobs = nullptr;
   int* d_flags = nullptr;  // [4]: timeout, nonfinite, reserved
+  void* host_step_resources = nullptr;  // copy stream + events of grs_step_from_host
 };
 
 namespace grs {
@@ -129,6 +130,8 @@ enum : int { FLAG_TIMEOUT = 0, FLAG_NONFINITE = 1, FLAG_COUNT = 4 };
 
 // Sets the message grs_last_error() returns on this thread (api.cu).
 void set_last_error(const std::string& msg);
+// Frees the copy stream and events grs_step_from_host created (host_step.cu).
+void destroy_host_step_resources(grs_plan* p);
 
 // host plan builder (plan.cpp)
 grs_status build_plan(const int64_t* numels, const int32_t* owners, int32_t n, int32_t world,

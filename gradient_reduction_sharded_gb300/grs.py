@@ -95,6 +95,8 @@ _sig = {
     "grs_gather_params": ([_vp, _vp, _P(_vp), _vp], ctypes.c_int),
     "grs_check_device_errors": ([_vp, _vp], ctypes.c_int),
     "grs_grad_norm_sq_noalloc": ([_vp, _vp, ctypes.c_int32, _vp, _vp], ctypes.c_int),
+    "grs_step_from_host": ([_vp, _P(grs_adamw), _P(_vp), _P(_vp), _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                            _vp, _vp, _vp], ctypes.c_int),
     "grs_last_error": ([], ctypes.c_char_p),
 }
 for _name, (_args, _res) in _sig.items():
@@ -194,6 +196,15 @@ def grs_gather_params(plan: int, params_bf16: int, tensor_ptrs: Sequence[Optiona
                       stream: int) -> None:
     _check(_lib.grs_gather_params(plan, params_bf16, _ptrs(tensor_ptrs), stream),
            "grs_gather_params")
+
+
+def grs_step_from_host(plan: int, hp: grs_adamw, host_grads: Sequence[int], dev_stage: Sequence[int],
+                       acc: int, master: int, m: int, v: int, params_bf16: int, workspace: int,
+                       d_norm_sq: int, host_params: Optional[int], host_norm_sq: Optional[int],
+                       stream: int) -> None:
+    _check(_lib.grs_step_from_host(plan, ctypes.byref(hp), _ptrs(host_grads), _ptrs(dev_stage), acc,
+                                   master, m, v, params_bf16, workspace, d_norm_sq, host_params,
+                                   host_norm_sq, stream), "grs_step_from_host")
 
 
 def grs_grad_norm_sq_noalloc(plan: int, acc: int, n_micro: int, d_norm_sq: int, stream: int) -> None:

@@ -267,6 +267,36 @@ grs_status grs_clip_adamw_step(const grs_plan* plan, const grs_adamw* hp, const 
 grs_status grs_gather_params(const grs_plan* plan, const uint16_t* params_bf16,
                              uint16_t* const* tensor_ptrs, void* stream);
 
+/* One whole update from host-resident gradients ([ISSUE] "Preserved
+ * prototype": asynchronous FP32 reduction hook; "Proposed scope": overlap
+ * during backward).  Per microbatch and bucket: the bucket's rank rows are
+ * copied host->device on the plan's own copy stream (one cudaMemcpyAsync per
+ * rank read by the owner group; ALREADY_REDUCED copies rank 0 only) while the
+ * previous bucket is reduced on `stream`; then the norm finish, clip + AdamW
+ * + bf16 cast, and (optionally) the bf16 parameters and the squared norm are
+ * copied back to the host.  Same results as the device-buffer calls.
+ *   hp            : host struct; hp->n_micro microbatches.
+ *   host_grads    : host array [n_micro * world] of HOST pointers (pinned
+ *                   memory for full speed), microbatch-major (j*world + k),
+ *                   each [n_rank_pad] bf16 bits.
+ *   dev_stage     : host array [2 * world] of device pointers (only the
+ *                   first `world` are used when n_micro == 1), each
+ *                   [n_rank_pad] bf16, 16-byte aligned: two staging halves
+ *                   alternating across microbatches.
+ *   acc, master, m, v, params_bf16, workspace, d_norm_sq : as for the
+ *                   device calls.
+ *   host_params   : host [n_state_pad] bf16 bits, or NULL (no read-back).
+ *   host_norm_sq  : host double [1], or NULL.
+ * The host buffers must stay valid until `stream` has run the call's work;
+ * the read-backs are complete after the caller synchronises `stream`.  The
+ * first call creates the plan's copy stream and events (freed by
+ * grs_plan_destroy).  Errors: INVALID_ARG, ALIGNMENT, NO_DEVICE, CUDA. */
+grs_status grs_step_from_host(const grs_plan* plan, const grs_adamw* hp,
+                              const uint16_t* const* host_grads, uint16_t* const* dev_stage,
+                              float* acc, float* master, float* m, float* v, uint16_t* params_bf16,
+                              void* workspace, double* d_norm_sq, uint16_t* host_params,
+                              double* host_norm_sq, void* stream);
+
 /* ------------------------------------------------- allocation-free variant */
 
 /* Size of the library's own scratch array for grs_grad_norm_sq_noalloc. */

@@ -304,3 +304,45 @@ def test_argument_errors():
         assert run.check_flags() == 0
     finally:
         run.close()
+
+
+@pytest.mark.parametrize("name", ["multi-tile-world16-M2", "odd-ds3-M3", "tiny-world4"])
+def test_step_from_host_matches_device_path(name):
+    """grs_step_from_host (host gradients, pipelined copies, per-bucket
+    reductions) gives the device path's results bit for bit, and reads the
+    parameters and the norm back to the host; two steps in a row."""
+    g = grs()
+    c = SMALL[name]
+    a = Run(c)
+    b = Run(c)
+    try:
+        W, M = c.world, c.n_micro
+        host = [torch.empty(a.grads[j][k].numel(), dtype=torch.int16).pin_memory()
+                for j in range(M) for k in range(W)]
+        stage = [torch.empty(a.grads[0][0].numel(), dtype=torch.bfloat16, device="cuda")
+                 for _ in range(2 * W)]
+        out_params = torch.empty(a.nsp, dtype=torch.int16).pin_memory()
+        out_norm = torch.empty(1, dtype=torch.float64).pin_memory()
+        s = b.stream()
+        for step in (1, 2):
+            if step == 2:
+                a.fill_grads(step_seed=2)
+            for j in range(M):
+                for k in range(W):
+                    host[j * W + k].copy_(a.grads[j][k].view(torch.int16))
+            a.update()
+            hp = g.make_adamw(c.hp[0], c.hp[1], c.hp[2], c.hp[3], c.hp[4], c.max_norm, step, M)
+            g.grs_step_from_host(b.plan, hp, [t.data_ptr() for t in host], [t.data_ptr() for t in stage],
+                                 b.acc.data_ptr(), b.master.data_ptr(), b.m.data_ptr(), b.v.data_ptr(),
+                                 b.params.data_ptr(), b.ws.data_ptr(), b.norm.data_ptr(),
+                                 out_params.data_ptr(), out_norm.data_ptr(), s)
+            torch.cuda.synchronize()
+            assert b.check_flags() == 0
+            for x, y in ((a.acc, b.acc), (a.norm, b.norm), (a.master, b.master), (a.m, b.m),
+                         (a.v, b.v), (a.params, b.params)):
+                assert torch.equal(x[:max(1, min(x.numel(), a.nsp))], y[:max(1, min(y.numel(), a.nsp))])
+            assert torch.equal(out_params, b.params[:a.nsp].cpu())
+            assert float(out_norm[0]) == float(b.norm.cpu()[0])
+    finally:
+        a.close()
+        b.close()
