@@ -15,7 +15,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgrs.so")
 
 SOURCES = ["plan.cpp", "api.cu", "kernels_reduce.cu", "kernels_update.cu", "kernels_gather.cu",
-           "noalloc.cu", "host_step.cu"]
+           "noalloc.cu", "host_step.cu", "kernels_masked.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -62,6 +62,14 @@ cudaError_t upload(T** dst, const std::vector<T>& src) {
 }
 
 void free_device(grs_plan* p) {
+  cudaFree(p->d_seg_start);
+  cudaFree(p->d_seg_tensor);
+  cudaFree(p->d_bucket_seg0);
+  cudaFree(p->d_tensor_live);
+  p->d_tensor_live = nullptr;
+  p->d_seg_start = nullptr;
+  p->d_seg_tensor = nullptr;
+  p->d_bucket_seg0 = nullptr;
   cudaFree(p->d_units);
   cudaFree(p->d_red_prefix);
   cudaFree(p->d_upd_prefix);
@@ -84,12 +92,24 @@ extern "C" {
 grs_status grs_plan_create(const int64_t* numels, const int32_t* owners, int32_t n_tensors,
                            int32_t world, int32_t tp, int32_t dp_replicate, int32_t dp_shard,
                            int64_t bucket_bytes, uint32_t flags, grs_plan** out) {
+  return grs_plan_create_ex(numels, owners, nullptr, n_tensors, world, tp, dp_replicate, dp_shard,
+                            bucket_bytes, flags, out);
+}
+
+grs_status grs_plan_create_ex(const int64_t* numels, const int32_t* owners, const uint32_t* tensor_flags,
+                              int32_t n_tensors, int32_t world, int32_t tp, int32_t dp_replicate,
+                              int32_t dp_shard, int64_t bucket_bytes, uint32_t flags, grs_plan** out) {
   if (out == nullptr) return fail(GRS_ERR_INVALID_ARG, "out is NULL");
   grs_plan* p = new (std::nothrow) grs_plan();
   if (p == nullptr) return fail(GRS_ERR_INVALID_ARG, "host allocation failed");
   std::string why;
-  const grs_status st =
-      grs::build_plan(numels, owners, n_tensors, world, tp, dp_replicate, dp_shard, bucket_bytes, p, &why);
+  if ((flags & ~(GRS_PLAN_HOST_ONLY | GRS_PLAN_FP32_GRADS)) != 0) {
+    delete p;
+    return fail(GRS_ERR_INVALID_ARG, "grs_plan_create: unknown flag bits");
+  }
+  const int32_t esize = (flags & GRS_PLAN_FP32_GRADS) ? 4 : 2;
+  const grs_status st = grs::build_plan(numels, owners, tensor_flags, n_tensors, world, tp, dp_replicate,
+                                        dp_shard, bucket_bytes, esize, p, &why);
   if (st != GRS_OK) {
     delete p;
     return fail(st, why);
@@ -102,6 +122,10 @@ grs_status grs_plan_create(const int64_t* numels, const int32_t* owners, int32_t
     if (e == cudaSuccess) e = upload(&p->d_red_prefix, p->red_prefix);
     if (e == cudaSuccess) e = upload(&p->d_upd_prefix, p->upd_prefix);
     if (e == cudaSuccess) e = upload(&p->d_jobs, p->jobs);
+    if (e == cudaSuccess) e = upload(&p->d_seg_start, p->seg_start);
+    if (e == cudaSuccess) e = upload(&p->d_seg_tensor, p->seg_tensor);
+    if (e == cudaSuccess) e = upload(&p->d_bucket_seg0, p->bucket_seg0);
+    if (e == cudaSuccess) e = upload(&p->d_tensor_live, p->tensor_live);
     if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&p->d_flags), grs::FLAG_COUNT * sizeof(int));
     if (e == cudaSuccess) e = cudaMemset(p->d_flags, 0, grs::FLAG_COUNT * sizeof(int));
     if (e != cudaSuccess) {
@@ -141,6 +165,7 @@ grs_status grs_plan_query(const grs_plan* p, grs_plan_info* o) {
   o->n_state_pad = p->n_state_pad;
   o->workspace_bytes = p->workspace_bytes;
   o->n_reduce_tiles = p->n_red_tiles;
+  o->grad_bytes = p->grad_esize;
   return GRS_OK;
 }
 
@@ -170,12 +195,13 @@ grs_status grs_tensor_info(const grs_plan* p, int32_t i, grs_tensor_desc* o) {
   o->bucket = p->t_bucket[i];
   o->owner = p->owner[i];
   o->numel = p->numel[i];
-  o->per_rank = (p->owner[i] == GRS_LOCAL_SHARD) ? p->numel[i] / p->tp : p->numel[i];
+  o->per_rank = p->t_bucket[i] < 0 ? 0 : (p->owner[i] == GRS_LOCAL_SHARD) ? p->numel[i] / p->tp : p->numel[i];
   o->bucket_offset = p->t_offset[i];
+  o->flags = p->tensor_flags[i];
   return GRS_OK;
 }
 
-static grs_status reduce_common(const grs_plan* p, const uint16_t* const* rank_grads, float* acc,
+static grs_status reduce_common(const grs_plan* p, const void* const* rank_grads, float* acc,
                                 int32_t accumulate, int32_t emit, void* workspace, void* stream,
                                 int32_t unit_begin, int32_t unit_end, int64_t state_base,
                                 int64_t rank_base, int32_t tag, const char* who) {
@@ -197,7 +223,7 @@ static grs_status reduce_common(const grs_plan* p, const uint16_t* const* rank_g
   DeviceGuard g(p->device);
   if (!g.ok()) return fail(GRS_ERR_CUDA, std::string(who) + ": cannot select the plan's device");
   grs::ReduceLaunch l;
-  const uint16_t* ranks[GRS_MAX_WORLD] = {};
+  const void* ranks[GRS_MAX_WORLD] = {};
   for (int32_t k = 0; k < p->world; ++k) ranks[k] = (k < nread) ? rank_grads[k] : rank_grads[0];
   l.ranks = ranks;
   l.acc = acc;
@@ -213,7 +239,7 @@ static grs_status reduce_common(const grs_plan* p, const uint16_t* const* rank_g
   return GRS_OK;
 }
 
-grs_status grs_reduce_bucket(const grs_plan* p, int32_t b, const uint16_t* const* rank_grads, float* acc,
+grs_status grs_reduce_bucket(const grs_plan* p, int32_t b, const void* const* rank_grads, float* acc,
                              int32_t accumulate, int32_t emit, void* workspace, void* stream) {
   grs_status st = check_plan_device(p);
   if (st != GRS_OK) return st;
@@ -224,7 +250,7 @@ grs_status grs_reduce_bucket(const grs_plan* p, int32_t b, const uint16_t* const
                        bk.unit0 + bk.copies, bk.state_off, bk.rank_off, bk.tag, "grs_reduce_bucket");
 }
 
-grs_status grs_reduce_all(const grs_plan* p, const uint16_t* const* rank_grads, float* acc,
+grs_status grs_reduce_all(const grs_plan* p, const void* const* rank_grads, float* acc,
                           int32_t accumulate, int32_t emit, void* workspace, void* stream) {
   grs_status st = check_plan_device(p);
   if (st != GRS_OK) return st;
@@ -301,6 +327,46 @@ grs_status grs_gather_params(const grs_plan* p, const uint16_t* params_bf16, uin
   if (!g.ok()) return fail(GRS_ERR_CUDA, "grs_gather_params: cannot select the plan's device");
   const int e = grs::launch_gather(p, params_bf16, tensor_ptrs, stream);
   if (e != 0) return cuda_fail(static_cast<cudaError_t>(e), "grs_gather_params");
+  return GRS_OK;
+}
+
+grs_status grs_grad_norm_sq_masked(const grs_plan* p, const float* acc, int32_t n_micro,
+                                   const uint8_t* d_tensor_used, void* workspace, double* d_norm_sq,
+                                   void* stream) {
+  grs_status st = check_plan_device(p);
+  if (st != GRS_OK) return st;
+  if (acc == nullptr || d_tensor_used == nullptr || workspace == nullptr || d_norm_sq == nullptr)
+    return fail(GRS_ERR_INVALID_ARG, "grs_grad_norm_sq_masked: NULL argument");
+  if (n_micro < 1) return fail(GRS_ERR_INVALID_ARG, "grs_grad_norm_sq_masked: n_micro must be >= 1");
+  if (!aligned16(acc) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(d_norm_sq) & 7u) != 0)
+    return fail(GRS_ERR_ALIGNMENT, "grs_grad_norm_sq_masked: misaligned pointer");
+  DeviceGuard g(p->device);
+  if (!g.ok()) return fail(GRS_ERR_CUDA, "grs_grad_norm_sq_masked: cannot select the plan's device");
+  const int e = grs::launch_norm_masked(p, acc, n_micro, d_tensor_used, workspace, d_norm_sq, stream);
+  if (e != 0) return cuda_fail(static_cast<cudaError_t>(e), "grs_grad_norm_sq_masked");
+  return GRS_OK;
+}
+
+grs_status grs_clip_adamw_step_masked(const grs_plan* p, const grs_adamw* hp, const double* d_norm_sq,
+                                      const float* acc, float* master, float* m, float* v,
+                                      uint16_t* params_bf16, const uint8_t* d_tensor_used,
+                                      int32_t* d_tensor_steps, void* workspace, void* stream) {
+  grs_status st = check_plan_device(p);
+  if (st != GRS_OK) return st;
+  if (hp == nullptr || acc == nullptr || master == nullptr || m == nullptr || v == nullptr ||
+      params_bf16 == nullptr || d_tensor_used == nullptr || d_tensor_steps == nullptr || workspace == nullptr)
+    return fail(GRS_ERR_INVALID_ARG, "grs_clip_adamw_step_masked: NULL argument");
+  if (hp->n_micro < 1) return fail(GRS_ERR_INVALID_ARG, "grs_clip_adamw_step_masked: n_micro must be >= 1");
+  if (hp->max_norm > 0.0f && d_norm_sq == nullptr)
+    return fail(GRS_ERR_INVALID_ARG, "grs_clip_adamw_step_masked: clipping needs d_norm_sq");
+  if (!aligned16(acc) || !aligned16(master) || !aligned16(m) || !aligned16(v) || !aligned16(params_bf16) ||
+      !aligned16(workspace) || (reinterpret_cast<uintptr_t>(d_tensor_steps) & 3u) != 0)
+    return fail(GRS_ERR_ALIGNMENT, "grs_clip_adamw_step_masked: misaligned pointer");
+  DeviceGuard g(p->device);
+  if (!g.ok()) return fail(GRS_ERR_CUDA, "grs_clip_adamw_step_masked: cannot select the plan's device");
+  const int e = grs::launch_update_masked(p, hp, d_norm_sq, acc, master, m, v, params_bf16, d_tensor_used,
+                                          d_tensor_steps, workspace, stream);
+  if (e != 0) return cuda_fail(static_cast<cudaError_t>(e), "grs_clip_adamw_step_masked");
   return GRS_OK;
 }
 

@@ -78,7 +78,7 @@ void destroy_host_step_resources(grs_plan* p) {
 }  // namespace grs
 
 extern "C" grs_status grs_step_from_host(const grs_plan* pc, const grs_adamw* hp,
-                                         const uint16_t* const* host_grads, uint16_t* const* dev_stage,
+                                         const void* const* host_grads, void* const* dev_stage,
                                          float* acc, float* master, float* m, float* v,
                                          uint16_t* params_bf16, void* workspace, double* d_norm_sq,
                                          uint16_t* host_params, double* host_norm_sq, void* stream) {
@@ -95,7 +95,7 @@ extern "C" grs_status grs_step_from_host(const grs_plan* pc, const grs_adamw* hp
         return fail(GRS_ERR_INVALID_ARG, "grs_step_from_host: host gradient pointer is NULL");
   for (int32_t s = 0; s < (M > 1 ? 2 : 1); ++s)
     for (int32_t k = 0; k < W; ++k) {
-      const uint16_t* d = dev_stage[size_t(s) * W + k];
+      const void* d = dev_stage[size_t(s) * W + k];
       if (d == nullptr) return fail(GRS_ERR_INVALID_ARG, "grs_step_from_host: staging pointer is NULL");
       if ((reinterpret_cast<uintptr_t>(d) & 15u) != 0)
         return fail(GRS_ERR_ALIGNMENT, "grs_step_from_host: staging buffer not 16-byte aligned");
@@ -123,19 +123,22 @@ extern "C" grs_status grs_step_from_host(const grs_plan* pc, const grs_adamw* hp
       cudaError_t e = cudaSuccess;
       if (j >= 2) e = cudaStreamWaitEvent(r->copy, ev_red, 0);  // staging half is free again
       const int32_t nread = bk.tag == GRS_ALREADY_REDUCED ? 1 : W;
-      const size_t bytes = size_t(bk.padded) * 2;
+      const size_t es = static_cast<size_t>(p->grad_esize);
+      const size_t bytes = size_t(bk.padded) * es;
+      const size_t boff = size_t(bk.rank_off) * es;
       for (int32_t k = 0; k < nread && e == cudaSuccess && bytes > 0; ++k)
-        e = cudaMemcpyAsync(dev_stage[size_t(half) * W + k] + bk.rank_off,
-                            host_grads[size_t(j) * W + k] + bk.rank_off, bytes, cudaMemcpyHostToDevice,
-                            r->copy);
+        e = cudaMemcpyAsync(static_cast<uint8_t*>(dev_stage[size_t(half) * W + k]) + boff,
+                            static_cast<const uint8_t*>(host_grads[size_t(j) * W + k]) + boff, bytes,
+                            cudaMemcpyHostToDevice, r->copy);
       if (e == cudaSuccess) e = cudaEventRecord(ev_copy, r->copy);
       if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, ev_copy, 0);
       if (e != cudaSuccess) {
         st = fail(GRS_ERR_CUDA, std::string("grs_step_from_host: copy: ") + cudaGetErrorString(e));
         break;
       }
-      const uint16_t* ranks[GRS_MAX_WORLD] = {};
-      for (int32_t k = 0; k < W; ++k) ranks[k] = dev_stage[size_t(half) * W + (k < nread ? k : 0)] + bk.rank_off;
+      const void* ranks[GRS_MAX_WORLD] = {};
+      for (int32_t k = 0; k < W; ++k)
+        ranks[k] = static_cast<const uint8_t*>(dev_stage[size_t(half) * W + (k < nread ? k : 0)]) + boff;
       st = grs_reduce_bucket(p, static_cast<int32_t>(b), ranks, acc + bk.state_off, j > 0 ? 1 : 0,
                              j == M - 1 ? 1 : 0, workspace, stream);
       if (st != GRS_OK) break;

@@ -10,8 +10,8 @@
 
 namespace grs {
 
-// Reduction tiles: a tile carries STAGE_GRAD_BYTES of bf16 input (all the
-// group's rank rows for T elements), so T = STAGE_GRAD_BYTES / (2 * group),
+// Reduction tiles: a tile carries STAGE_GRAD_BYTES of gradient input (all the
+// group's rank rows for T elements), so T = STAGE_GRAD_BYTES / (esize * group),
 // capped at RED_MAX_T, a multiple of 8, and small enough that two stages
 // (rank rows plus the old accumulator tile) fit in the shared-memory ring.
 // Measured on GB300: each rank row of a tile is one bulk copy, and copies
@@ -85,7 +85,10 @@ struct grs_plan {
   // inputs
   std::vector<int64_t> numel;
   std::vector<int32_t> owner;
+  std::vector<uint32_t> tensor_flags;  // GRS_TENSOR_* per tensor
+  std::vector<uint8_t> tensor_live;    // 1 unless frozen (has state in the plan)
   int32_t world = 0, tp = 0, dp_replicate = 0, dp_shard = 0, dp = 0;
+  int32_t grad_esize = 2;  // bytes per gradient element: 2 (bf16) or 4 (fp32)
   int64_t bucket_bytes = 0;
   // layout
   std::vector<int32_t> t_bucket;
@@ -95,6 +98,12 @@ struct grs_plan {
   std::vector<int64_t> red_prefix;  // [n_units + 1] first reduction tile per unit
   std::vector<int64_t> upd_prefix;  // [n_units + 1] first update tile per unit
   std::vector<grs::GatherJob> jobs; // by tensor, LOCAL_SHARD: tp jobs
+  // Tensor segments of every bucket in offset order: segments
+  // [bucket_seg0[b], bucket_seg0[b+1]) start at seg_start[] (per-rank element
+  // offset inside the bucket) and belong to tensor seg_tensor[].
+  std::vector<int64_t> seg_start;
+  std::vector<int32_t> seg_tensor;
+  std::vector<int32_t> bucket_seg0;
   std::vector<int32_t> tensor_job0; // [n_tensors + 1]
   int64_t n_unique = 0, n_rank_pad = 0, n_state_pad = 0;
   int64_t n_red_tiles = 0, n_upd_tiles = 0, n_gather_chunks = 0;
@@ -106,6 +115,10 @@ struct grs_plan {
   int64_t* d_red_prefix = nullptr;
   int64_t* d_upd_prefix = nullptr;
   grs::GatherJob* d_jobs = nullptr;
+  int64_t* d_seg_start = nullptr;
+  int32_t* d_seg_tensor = nullptr;
+  int32_t* d_bucket_seg0 = nullptr;
+  uint8_t* d_tensor_live = nullptr;
   int* d_flags = nullptr;  // [4]: timeout, nonfinite, reserved
   void* host_step_resources = nullptr;  // copy stream + events of grs_step_from_host
 };
@@ -123,7 +136,10 @@ inline int64_t ws_level2_offset(int64_t n_red_tiles) {
 inline int64_t ws_ticket_offset(int64_t n_red_tiles) {
   return ws_level2_offset(n_red_tiles) + NORM_L2_BLOCKS * 8;
 }
+// Bytes the norm needs (partials, level 2, ticket).
 inline int64_t ws_bytes(int64_t n_red_tiles) { return ws_ticket_offset(n_red_tiles) + 256; }
+// Per-tensor update factors of the masked update ([n_tensors] float2) follow.
+inline int64_t ws_factors_offset(int64_t n_red_tiles) { return ws_bytes(n_red_tiles); }
 
 // Device flags
 enum : int { FLAG_TIMEOUT = 0, FLAG_NONFINITE = 1, FLAG_COUNT = 4 };
@@ -134,13 +150,13 @@ void set_last_error(const std::string& msg);
 void destroy_host_step_resources(grs_plan* p);
 
 // host plan builder (plan.cpp)
-grs_status build_plan(const int64_t* numels, const int32_t* owners, int32_t n, int32_t world,
-                      int32_t tp, int32_t dp_replicate, int32_t dp_shard, int64_t bucket_bytes,
-                      grs_plan* p, std::string* why);
+grs_status build_plan(const int64_t* numels, const int32_t* owners, const uint32_t* tensor_flags,
+                      int32_t n, int32_t world, int32_t tp, int32_t dp_replicate, int32_t dp_shard,
+                      int64_t bucket_bytes, int32_t grad_esize, grs_plan* p, std::string* why);
 
 // launchers (kernels_*.cu); all return cudaGetLastError() as int
 struct ReduceLaunch {
-  const uint16_t* const* ranks;  // host array [world]
+  const void* const* ranks;  // host array [world]
   float* acc;
   float* partials;  // nullptr: no norm epilogue
   int32_t unit_begin, unit_end;
@@ -155,5 +171,13 @@ int launch_update(const grs_plan* p, const grs_adamw* hp, const double* d_norm_s
 int launch_accumulate(const grs_plan* p, int32_t bucket, float* acc, const float* mb, void* stream);
 int launch_gather(const grs_plan* p, const uint16_t* params, uint16_t* const* tensor_ptrs,
                   void* stream);
+// Second half of the norm: tile partials in `workspace` -> *d_norm_sq.
+int launch_norm_finish(const grs_plan* p, int32_t n_micro, void* workspace, double* d_norm_sq,
+                       void* stream);
+int launch_norm_masked(const grs_plan* p, const float* acc, int32_t n_micro, const uint8_t* used,
+                       void* workspace, double* d_norm_sq, void* stream);
+int launch_update_masked(const grs_plan* p, const grs_adamw* hp, const double* d_norm_sq,
+                         const float* acc, float* master, float* m, float* v, uint16_t* params,
+                         const uint8_t* used, int32_t* steps, void* workspace, void* stream);
 
 }  // namespace grs

@@ -1,0 +1,269 @@
+// Per-step tensor masks: parameters without a gradient this step.
+//
+// "refactor(distributed): establish shared native TP replica ownership",
+// "Proposed scope": validate frozen/unused parameters.  A parameter whose
+// gradient is absent this step (PyTorch's grad None) is skipped the way
+// clip_grad_norm_ and torch.optim.AdamW skip it: it adds nothing to the
+// global norm, and its master, moments, bf16 copy and step count stay as
+// they are.  Every other tensor advances its own step count, so its bias
+// correction follows the number of updates it actually received.
+//
+// Element -> tensor: each bucket row holds its tensors back to back; the
+// plan's segment table (start offset, tensor) per bucket is searched once
+// per thread and then walked forward.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+
+#include "device.cuh"
+#include "internal.h"
+
+namespace grs {
+
+namespace {
+
+constexpr int MNORM_THREADS = 32 * RED_CWARPS;  // same tiles and order as the unmasked pass
+constexpr int MUPD_THREADS = 256;
+static_assert(UPD_T == MUPD_THREADS * 8, "one 8-element group per thread per tile");
+
+// Last segment in [lo, hi) whose start is <= e (the first segment starts at 0).
+__device__ __forceinline__ int find_seg(const int64_t* __restrict__ start, int lo, int hi, int64_t e) {
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(start + mid) <= e)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  return lo;
+}
+
+struct Segs {
+  const int64_t* start;
+  const int32_t* tensor;
+  const int32_t* bucket_seg0;
+};
+
+__global__ void __launch_bounds__(MNORM_THREADS) norm_pass1_masked_kernel(
+    const float* __restrict__ acc, const UnitDesc* __restrict__ units, const int64_t* __restrict__ prefix,
+    int32_t n_units, int64_t n_tiles, Segs sg, const uint8_t* __restrict__ used_mask,
+    float* __restrict__ partials) {
+  __shared__ float wp[MNORM_THREADS / 32];
+  const int lane = threadIdx.x & 31;
+  const int w = threadIdx.x >> 5;
+  for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    const int u = find_unit(prefix, 0, n_units, tile);
+    const UnitDesc* ud = units + u;
+    const int64_t T = ud->red_T;
+    const int64_t e0 = (tile - ud->red_tile0) * T;
+    const int64_t rem = ud->padded - e0;
+    const int n = static_cast<int>(rem < T ? rem : T);
+    const float* src = acc + ud->state_off + e0;
+    const int lo = __ldg(sg.bucket_seg0 + ud->bucket), hi = __ldg(sg.bucket_seg0 + ud->bucket + 1);
+    float psum = 0.0f;
+    for (int c = threadIdx.x; c < (n >> 3); c += MNORM_THREADS) {
+      const float4 x0 = __ldcs(reinterpret_cast<const float4*>(src + c * 8));
+      const float4 x1 = __ldcs(reinterpret_cast<const float4*>(src + c * 8 + 4));
+      float o[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+      const int64_t e = e0 + int64_t(c) * 8;
+      int s = e < ud->used ? find_seg(sg.start, lo, hi, e) : lo;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (e + q >= ud->used) {
+          o[q] = 0.0f;
+          continue;
+        }
+        while (s + 1 < hi && __ldg(sg.start + s + 1) <= e + q) ++s;
+        if (!__ldg(used_mask + __ldg(sg.tensor + s))) o[q] = 0.0f;
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) psum = __fmaf_rn(o[q], o[q], psum);
+    }
+    psum = warp_sum(psum);
+    if (lane == 0) wp[w] = psum;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float s = wp[0];
+#pragma unroll
+      for (int k = 1; k < MNORM_THREADS / 32; ++k) s = __fadd_rn(s, wp[k]);
+      partials[tile] = s;
+    }
+    __syncthreads();
+  }
+}
+
+// Per tensor: advance the step count of tensors with a gradient and derive
+// their bias-corrected factors (lr / (1 - b1^t), 1 / sqrt(1 - b2^t)) in fp64.
+__global__ void tensor_factors_kernel(int32_t n, const uint8_t* __restrict__ live,
+                                      const uint8_t* __restrict__ used_mask, int32_t* __restrict__ steps,
+                                      float2* __restrict__ factors, double lr, double b1, double b2) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  if (live[i] && used_mask[i]) {
+    const int t = steps[i] + 1;
+    steps[i] = t;
+    const double bc1 = 1.0 - pow(b1, static_cast<double>(t));
+    const double bc2 = 1.0 - pow(b2, static_cast<double>(t));
+    factors[i] = make_float2(static_cast<float>(lr / bc1), static_cast<float>(1.0 / sqrt(bc2)));
+  } else {
+    factors[i] = make_float2(0.0f, 0.0f);
+  }
+}
+
+struct MaskedArgs {
+  const float* acc;
+  float* master;
+  float* m;
+  float* v;
+  uint16_t* params;
+  const double* norm_sq;
+  const UnitDesc* units;
+  const int64_t* prefix;
+  Segs sg;
+  const uint8_t* used_mask;
+  const float2* factors;
+  int32_t n_units;
+  float decay, b1, omb1, b2, omb2, eps;
+  float max_norm;
+  float inv_m;
+};
+
+__device__ __forceinline__ uint16_t bf16_rn(float x) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(x);
+  return *reinterpret_cast<const uint16_t*>(&h);
+}
+
+__global__ void __launch_bounds__(MUPD_THREADS) update_masked_kernel(const __grid_constant__ MaskedArgs a) {
+  float gscale = a.inv_m;
+  if (a.max_norm > 0.0f) {
+    const float cr = a.max_norm / (sqrtf(static_cast<float>(*a.norm_sq)) + 1e-6f);
+    gscale = __fmul_rn((cr < 1.0f || isnan(cr)) ? cr : 1.0f, a.inv_m);
+  }
+  const int u = find_unit(a.prefix, 0, a.n_units, blockIdx.x);
+  const UnitDesc* ud = a.units + u;
+  const int64_t el = (static_cast<int64_t>(blockIdx.x) - ud->upd_tile0) * UPD_T + int64_t(threadIdx.x) * 8;
+  if (el >= ud->padded) return;
+  const int64_t i = ud->state_off + el;
+  const int64_t used = ud->used;
+  const int lo = __ldg(a.sg.bucket_seg0 + ud->bucket), hi = __ldg(a.sg.bucket_seg0 + ud->bucket + 1);
+  int s = el < used ? find_seg(a.sg.start, lo, hi, el) : lo;
+
+  const float4 g0 = __ldcs(reinterpret_cast<const float4*>(a.acc + i));
+  const float4 g1 = __ldcs(reinterpret_cast<const float4*>(a.acc + i + 4));
+  const float4 p0 = reinterpret_cast<const float4*>(a.master + i)[0];
+  const float4 p1 = reinterpret_cast<const float4*>(a.master + i + 4)[0];
+  const float4 m0 = reinterpret_cast<const float4*>(a.m + i)[0];
+  const float4 m1 = reinterpret_cast<const float4*>(a.m + i + 4)[0];
+  const float4 v0 = reinterpret_cast<const float4*>(a.v + i)[0];
+  const float4 v1 = reinterpret_cast<const float4*>(a.v + i + 4)[0];
+  const float G[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+  float P[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+  float M[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+  float V[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+  bool write[8];
+  bool all = true;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int64_t e = el + q;
+    if (e >= used) {  // padding: exact zeros
+      P[q] = M[q] = V[q] = 0.0f;
+      write[q] = true;
+      continue;
+    }
+    while (s + 1 < hi && __ldg(a.sg.start + s + 1) <= e) ++s;
+    const int32_t t = __ldg(a.sg.tensor + s);
+    write[q] = __ldg(a.used_mask + t) != 0;
+    all = all && write[q];
+    if (!write[q]) continue;  // no gradient this step: state stays
+    const float2 f = a.factors[t];
+    const float g = __fmul_rn(G[q], gscale);
+    float p = __fmul_rn(P[q], a.decay);
+    const float mm = __fmaf_rn(a.b1, M[q], __fmul_rn(a.omb1, g));
+    const float vv = __fmaf_rn(a.b2, V[q], __fmul_rn(__fmul_rn(a.omb2, g), g));
+    const float denom = __fadd_rn(__fmul_rn(__fsqrt_rn(vv), f.y), a.eps);
+    p = __fsub_rn(p, __fmul_rn(f.x, __fdiv_rn(mm, denom)));
+    P[q] = p;
+    M[q] = mm;
+    V[q] = vv;
+  }
+  if (all) {
+    reinterpret_cast<float4*>(a.master + i)[0] = make_float4(P[0], P[1], P[2], P[3]);
+    reinterpret_cast<float4*>(a.master + i + 4)[0] = make_float4(P[4], P[5], P[6], P[7]);
+    reinterpret_cast<float4*>(a.m + i)[0] = make_float4(M[0], M[1], M[2], M[3]);
+    reinterpret_cast<float4*>(a.m + i + 4)[0] = make_float4(M[4], M[5], M[6], M[7]);
+    reinterpret_cast<float4*>(a.v + i)[0] = make_float4(V[0], V[1], V[2], V[3]);
+    reinterpret_cast<float4*>(a.v + i + 4)[0] = make_float4(V[4], V[5], V[6], V[7]);
+    uint4 h;
+    h.x = uint32_t(bf16_rn(P[0])) | (uint32_t(bf16_rn(P[1])) << 16);
+    h.y = uint32_t(bf16_rn(P[2])) | (uint32_t(bf16_rn(P[3])) << 16);
+    h.z = uint32_t(bf16_rn(P[4])) | (uint32_t(bf16_rn(P[5])) << 16);
+    h.w = uint32_t(bf16_rn(P[6])) | (uint32_t(bf16_rn(P[7])) << 16);
+    reinterpret_cast<uint4*>(a.params + i)[0] = h;
+  } else {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if (!write[q]) continue;
+      a.master[i + q] = P[q];
+      a.m[i + q] = M[q];
+      a.v[i + q] = V[q];
+      a.params[i + q] = bf16_rn(P[q]);
+    }
+  }
+}
+
+}  // namespace
+
+int launch_norm_masked(const grs_plan* p, const float* acc, int32_t n_micro, const uint8_t* used,
+                       void* workspace, double* d_norm_sq, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + ws_partials_offset());
+  if (p->n_red_tiles > 0) {
+    const int64_t grid = p->n_red_tiles < int64_t(p->sm_count) * 16 ? p->n_red_tiles
+                                                                    : int64_t(p->sm_count) * 16;
+    norm_pass1_masked_kernel<<<static_cast<unsigned>(grid), MNORM_THREADS, 0, s>>>(
+        acc, p->d_units, p->d_red_prefix, static_cast<int32_t>(p->units.size()), p->n_red_tiles,
+        Segs{p->d_seg_start, p->d_seg_tensor, p->d_bucket_seg0}, used, partials);
+    const int e = static_cast<int>(cudaGetLastError());
+    if (e != 0) return e;
+  }
+  return launch_norm_finish(p, n_micro, workspace, d_norm_sq, stream);
+}
+
+int launch_update_masked(const grs_plan* p, const grs_adamw* hp, const double* d_norm_sq,
+                         const float* acc, float* master, float* m, float* v, uint16_t* params,
+                         const uint8_t* used, int32_t* steps, void* workspace, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int32_t n = static_cast<int32_t>(p->numel.size());
+  float2* factors = reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) + ws_factors_offset(p->n_red_tiles));
+  tensor_factors_kernel<<<(n + 255) / 256, 256, 0, s>>>(n, p->d_tensor_live, used, steps, factors, hp->lr,
+                                                         hp->beta1, hp->beta2);
+  int e = static_cast<int>(cudaGetLastError());
+  if (e != 0 || p->n_upd_tiles <= 0) return e;
+  MaskedArgs a;
+  a.acc = acc;
+  a.master = master;
+  a.m = m;
+  a.v = v;
+  a.params = params;
+  a.norm_sq = d_norm_sq;
+  a.units = p->d_units;
+  a.prefix = p->d_upd_prefix;
+  a.sg = Segs{p->d_seg_start, p->d_seg_tensor, p->d_bucket_seg0};
+  a.used_mask = used;
+  a.factors = factors;
+  a.n_units = static_cast<int32_t>(p->units.size());
+  const double lr = hp->lr, wd = hp->weight_decay;
+  a.decay = static_cast<float>(1.0 - lr * wd);
+  a.b1 = hp->beta1;
+  a.omb1 = static_cast<float>(1.0 - static_cast<double>(hp->beta1));
+  a.b2 = hp->beta2;
+  a.omb2 = static_cast<float>(1.0 - static_cast<double>(hp->beta2));
+  a.eps = hp->eps;
+  a.max_norm = hp->max_norm > 0.0f ? hp->max_norm : 0.0f;
+  a.inv_m = static_cast<float>(1.0 / static_cast<double>(hp->n_micro));
+  update_masked_kernel<<<static_cast<unsigned>(p->n_upd_tiles), MUPD_THREADS, 0, s>>>(a);
+  return static_cast<int>(cudaGetLastError());
+}
+
+}  // namespace grs

@@ -10,6 +10,9 @@
 // and, on the last microbatch, per-tile partial sums of acc^2 for the
 // global norm.
 //
+// Input: bf16 gradients, or fp32 ones for plans created with
+// GRS_PLAN_FP32_GRADS (tiles sized for 4-byte elements).
+//
 // How (GB300): a persistent grid, one CTA per SM.  Warp 0 is a TMA producer:
 // for every tile it issues one 1-D bulk copy (cp.async.bulk) per rank row of
 // the tile's reduction group, plus the old accumulator tile when
@@ -58,7 +61,7 @@ constexpr size_t RED_SMEM_TAIL = 2 * RED_MAX_STAGES * sizeof(uint64_t)        //
                                  + 16;                                          // abort flag
 
 struct ReduceArgs {
-  const uint16_t* ranks[GRS_MAX_WORLD];
+  const void* ranks[GRS_MAX_WORLD];  // bf16 bits or fp32, by the plan
   float* acc;
   float* partials;
   const UnitDesc* units;
@@ -82,7 +85,59 @@ __device__ __forceinline__ float fold_partials(const float* wp) {
   return s;
 }
 
+// Sum of eight elements over the rank rows, in rank order.
+// bf16 rows (16 bytes per 8 elements): plain fp32 adds — a sum of bf16
+// values is exact in fp32 unless an input is 2^24 times smaller than the
+// largest, so the result is the correctly rounded sum in practice.
+// fp32 rows (32 bytes): Knuth's TwoSum keeps each add's rounding error in a
+// compensation term added at the end, so the sum is accurate relative to
+// the result, not to the operands (where gradients nearly cancel, AdamW's
+// g / (|g| + eps) would otherwise magnify an operand-relative error).
+template <typename E>
+struct Sum8;
+template <>
+struct Sum8<uint16_t> {
+  float v[8];
+  __device__ __forceinline__ void set(const uint8_t* p) { set_bf16x8(v, lds128(p)); }
+  __device__ __forceinline__ void add(const uint8_t* p) { add_bf16x8(v, lds128(p)); }
+  __device__ __forceinline__ void finish(float (&o)[8]) const {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) o[q] = v[q];
+  }
+};
+template <>
+struct Sum8<float> {
+  float v[8], c[8];
+  __device__ __forceinline__ void set(const uint8_t* p) {
+    const uint4 a = lds128(p), b = lds128(p + 16);
+    v[0] = __uint_as_float(a.x); v[1] = __uint_as_float(a.y); v[2] = __uint_as_float(a.z); v[3] = __uint_as_float(a.w);
+    v[4] = __uint_as_float(b.x); v[5] = __uint_as_float(b.y); v[6] = __uint_as_float(b.z); v[7] = __uint_as_float(b.w);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) c[q] = 0.0f;
+  }
+  __device__ __forceinline__ void two_sum(int q, float x) {
+    const float t = __fadd_rn(v[q], x);
+    const float z = __fsub_rn(t, v[q]);
+    const float err = __fadd_rn(__fsub_rn(v[q], __fsub_rn(t, z)), __fsub_rn(x, z));
+    c[q] = __fadd_rn(c[q], err);
+    v[q] = t;
+  }
+  __device__ __forceinline__ void add(const uint8_t* p) {
+    const uint4 a = lds128(p), b = lds128(p + 16);
+    two_sum(0, __uint_as_float(a.x)); two_sum(1, __uint_as_float(a.y));
+    two_sum(2, __uint_as_float(a.z)); two_sum(3, __uint_as_float(a.w));
+    two_sum(4, __uint_as_float(b.x)); two_sum(5, __uint_as_float(b.y));
+    two_sum(6, __uint_as_float(b.z)); two_sum(7, __uint_as_float(b.w));
+  }
+  __device__ __forceinline__ void finish(float (&o)[8]) const {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) o[q] = __fadd_rn(v[q], c[q]);
+  }
+};
+
+template <typename E>
 __global__ void __launch_bounds__(RED_THREADS, 1) reduce_kernel(const __grid_constant__ ReduceArgs a) {
+  constexpr uint32_t ESZ = sizeof(E);
   extern __shared__ __align__(128) uint8_t smem[];
   const int S = a.stages;
   uint8_t* ring = smem;
@@ -130,7 +185,7 @@ __global__ void __launch_bounds__(RED_THREADS, 1) reduce_kernel(const __grid_con
       const int32_t n = static_cast<int32_t>(rem < T ? rem : T);
       const int64_t vrem = ud.used - e0;
       const int32_t valid = static_cast<int32_t>(vrem <= 0 ? 0 : (vrem < n ? vrem : n));
-      const uint32_t grad_bytes = static_cast<uint32_t>(ud.g_count) * static_cast<uint32_t>(n) * 2u;
+      const uint32_t grad_bytes = static_cast<uint32_t>(ud.g_count) * static_cast<uint32_t>(n) * ESZ;
       const uint32_t bytes = grad_bytes + (a.accumulate ? static_cast<uint32_t>(n) * 4u : 0u);
       const int64_t out_off = ud.state_off - a.state_base + e0;
       int good = 1;
@@ -155,8 +210,8 @@ __global__ void __launch_bounds__(RED_THREADS, 1) reduce_kernel(const __grid_con
       __syncwarp();
       const int64_t roff = ud.rank_off - a.rank_base + e0;
       for (int i = lane; i < ud.g_count; i += 32)
-        bulk_g2s(st + size_t(i) * n * 2, a.ranks[ud.g_start + i * ud.g_stride] + roff,
-                 static_cast<uint32_t>(n) * 2u, &full[s], pol);
+        bulk_g2s(st + size_t(i) * n * ESZ, static_cast<const E*>(a.ranks[ud.g_start + i * ud.g_stride]) + roff,
+                 static_cast<uint32_t>(n) * ESZ, &full[s], pol);
       if (a.accumulate && lane == 0)
         bulk_g2s(st + grad_bytes, a.acc + out_off, static_cast<uint32_t>(n) * 4u, &full[s]);
     }
@@ -195,25 +250,17 @@ __global__ void __launch_bounds__(RED_THREADS, 1) reduce_kernel(const __grid_con
       const int32_t n = md.n;
       float* out = a.acc + md.out_off;
       const uint8_t* st = ring + size_t(s) * a.stage_bytes;
-      const size_t row = size_t(n) * 2;
+      const size_t row = size_t(n) * ESZ;
       const float* old = reinterpret_cast<const float*>(st + size_t(gc) * row);
       float psum = 0.0f;
       for (int c = ct; c < (n >> 3); c += RED_CTHREADS) {
-        const uint8_t* p = st + size_t(c) * 16;
+        const uint8_t* p = st + size_t(c) * 8 * ESZ;
+        Sum8<E> sum;
+        sum.set(p);
+#pragma unroll 4
+        for (int i = 1; i < gc; ++i) sum.add(p + i * row);
         float v[8];
-        set_bf16x8(v, lds128(p));
-        int i = 1;
-        for (; i + 3 < gc; i += 4) {
-          const uint4 w0 = lds128(p + (i + 0) * row);
-          const uint4 w1 = lds128(p + (i + 1) * row);
-          const uint4 w2 = lds128(p + (i + 2) * row);
-          const uint4 w3 = lds128(p + (i + 3) * row);
-          add_bf16x8(v, w0);
-          add_bf16x8(v, w1);
-          add_bf16x8(v, w2);
-          add_bf16x8(v, w3);
-        }
-        for (; i < gc; ++i) add_bf16x8(v, lds128(p + i * row));
+        sum.finish(v);
         float o[8];
         if (a.accumulate) {
           const uint4 q0 = lds128(old + c * 8);
@@ -249,74 +296,7 @@ __global__ void __launch_bounds__(RED_THREADS, 1) reduce_kernel(const __grid_con
   }
 }
 
-// Direct-load variant (compile with -DGRS_REDUCE_DIRECT): one block of
-// RED_CTHREADS threads per tile, each thread loads its 8 elements of every rank row with
-// 16-byte non-allocating global loads and keeps them in registers.  Same
-// per-tile partial order as the staged kernel.
-__global__ void __launch_bounds__(RED_CTHREADS) reduce_direct_kernel(const __grid_constant__ ReduceArgs a) {
-  __shared__ float wps[RED_CWARPS];
-  const int64_t tile = a.tile_begin + blockIdx.x;
-  const int u = find_unit(a.prefix, a.unit_begin, a.unit_end, tile);
-  const UnitDesc* ud = a.units + u;
-  const int64_t T = ud->red_T;
-  const int64_t e0 = (tile - ud->red_tile0) * T;
-  const int64_t rem = ud->padded - e0;
-  const int n = static_cast<int>(rem < T ? rem : T);
-  const int64_t vrem = ud->used - e0;
-  const int valid = static_cast<int>(vrem <= 0 ? 0 : (vrem < n ? vrem : n));
-  const int gc = ud->g_count, gs = ud->g_start, gst = ud->g_stride;
-  const float scale = ud->scale;
-  const int64_t roff = ud->rank_off - a.rank_base + e0;
-  float* out = a.acc + (ud->state_off - a.state_base) + e0;
-  float psum = 0.0f;
-  for (int c = threadIdx.x; c < (n >> 3); c += RED_CTHREADS) {
-    float v[8];
-    {
-      const uint4 w = __ldcs(reinterpret_cast<const uint4*>(a.ranks[gs] + roff) + c);
-      set_bf16x8(v, w);
-    }
-    int i = 1;
-    for (; i + 7 < gc; i += 8) {
-      uint4 w[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        w[q] = __ldcs(reinterpret_cast<const uint4*>(a.ranks[gs + (i + q) * gst] + roff) + c);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) add_bf16x8(v, w[q]);
-    }
-    for (; i < gc; ++i)
-      add_bf16x8(v, __ldcs(reinterpret_cast<const uint4*>(a.ranks[gs + i * gst] + roff) + c));
-    float o[8];
-    float4* o4 = reinterpret_cast<float4*>(out + c * 8);
-    if (a.accumulate) {
-      const float4 q0 = o4[0], q1 = o4[1];
-      const float ov[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-#pragma unroll
-      for (int q = 0; q < 8; ++q) o[q] = __fmaf_rn(v[q], scale, ov[q]);
-    } else {
-#pragma unroll
-      for (int q = 0; q < 8; ++q) o[q] = __fmul_rn(v[q], scale);
-    }
-    const int el = c * 8;
-    if (el + 8 > valid) {
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        if (el + q >= valid) o[q] = 0.0f;
-    }
-    o4[0] = make_float4(o[0], o[1], o[2], o[3]);
-    o4[1] = make_float4(o[4], o[5], o[6], o[7]);
-#pragma unroll
-    for (int q = 0; q < 8; ++q) psum = __fmaf_rn(o[q], o[q], psum);
-  }
-  if (a.partials != nullptr) {
-    psum = warp_sum(psum);
-    if ((threadIdx.x & 31) == 0) wps[threadIdx.x >> 5] = psum;
-    __syncthreads();
-    if (threadIdx.x == 0) a.partials[tile] = fold_partials(wps);
-  }
-}
-
-bool g_attr_set[64] = {};
+bool g_attr_set[2][64] = {};
 
 }  // namespace
 
@@ -342,7 +322,7 @@ int launch_reduce(const grs_plan* p, const ReduceLaunch& l, void* stream) {
   int64_t need = 128;
   for (int32_t u = l.unit_begin; u < l.unit_end; ++u) {
     const UnitDesc& d = p->units[u];
-    const int64_t b = int64_t(d.g_count) * d.red_T * 2 + (l.accumulate ? int64_t(d.red_T) * 4 : 0);
+    const int64_t b = int64_t(d.g_count) * d.red_T * p->grad_esize + (l.accumulate ? int64_t(d.red_T) * 4 : 0);
     need = b > need ? b : need;
   }
   need = (need + 127) / 128 * 128;
@@ -352,18 +332,20 @@ int launch_reduce(const grs_plan* p, const ReduceLaunch& l, void* stream) {
   a.stages = stages;
   a.stage_bytes = static_cast<int32_t>(need);
   const size_t smem = size_t(stages) * need + RED_SMEM_TAIL;
-  if (p->device >= 0 && p->device < 64 && !g_attr_set[p->device]) {
-    cudaError_t e = cudaFuncSetAttribute(reduce_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(RED_RING_BYTES + RED_SMEM_TAIL));
+  const bool f32 = p->grad_esize == 4;
+  if (p->device >= 0 && p->device < 64 && !g_attr_set[f32][p->device]) {
+    cudaError_t e = f32 ? cudaFuncSetAttribute(reduce_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(RED_RING_BYTES + RED_SMEM_TAIL))
+                        : cudaFuncSetAttribute(reduce_kernel<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(RED_RING_BYTES + RED_SMEM_TAIL));
     if (e != cudaSuccess) return static_cast<int>(e);
-    g_attr_set[p->device] = true;
+    g_attr_set[f32][p->device] = true;
   }
-#ifdef GRS_REDUCE_DIRECT
-  reduce_direct_kernel<<<static_cast<unsigned>(tiles), RED_CTHREADS, 0, static_cast<cudaStream_t>(stream)>>>(a);
-  return static_cast<int>(cudaGetLastError());
-#endif
   const int64_t grid = tiles < p->sm_count ? tiles : p->sm_count;
-  reduce_kernel<<<static_cast<unsigned>(grid), RED_THREADS, smem, static_cast<cudaStream_t>(stream)>>>(a);
+  if (f32)
+    reduce_kernel<float><<<static_cast<unsigned>(grid), RED_THREADS, smem, static_cast<cudaStream_t>(stream)>>>(a);
+  else
+    reduce_kernel<uint16_t><<<static_cast<unsigned>(grid), RED_THREADS, smem, static_cast<cudaStream_t>(stream)>>>(a);
   return static_cast<int>(cudaGetLastError());
 }
 

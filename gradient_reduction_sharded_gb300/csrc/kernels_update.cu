@@ -239,20 +239,28 @@ __global__ void __launch_bounds__(UPD_THREADS) accumulate_kernel(float* __restri
 int launch_norm(const grs_plan* p, const float* acc, int32_t n_micro, void* workspace,
                 int32_t partials_ready, double* d_norm_sq, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  float* partials = reinterpret_cast<float*>(ws + ws_partials_offset());
-  double* level2 = reinterpret_cast<double*>(ws + ws_level2_offset(p->n_red_tiles));
+  float* partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + ws_partials_offset());
   if (!partials_ready && p->n_red_tiles > 0) {
     const int64_t grid = p->n_red_tiles < int64_t(p->sm_count) * 16 ? p->n_red_tiles
                                                                     : int64_t(p->sm_count) * 16;
     norm_pass1_kernel<<<static_cast<unsigned>(grid), NORM1_THREADS, 0, s>>>(
         acc, p->d_units, p->d_red_prefix, static_cast<int32_t>(p->units.size()), p->n_red_tiles,
         partials);
+    const int e = static_cast<int>(cudaGetLastError());
+    if (e != 0) return e;
   }
+  return launch_norm_finish(p, n_micro, workspace, d_norm_sq, stream);
+}
+
+int launch_norm_finish(const grs_plan* p, int32_t n_micro, void* workspace, double* d_norm_sq,
+                       void* stream) {
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* partials = reinterpret_cast<float*>(ws + ws_partials_offset());
+  double* level2 = reinterpret_cast<double*>(ws + ws_level2_offset(p->n_red_tiles));
   unsigned int* ticket = reinterpret_cast<unsigned int*>(ws + ws_ticket_offset(p->n_red_tiles));
   const double inv_m = 1.0 / static_cast<double>(n_micro);
-  norm_finish_kernel<<<NORM_L2_BLOCKS, NORM2_THREADS, 0, s>>>(partials, p->n_red_tiles, level2, ticket,
-                                                             inv_m * inv_m, d_norm_sq, p->d_flags);
+  norm_finish_kernel<<<NORM_L2_BLOCKS, NORM2_THREADS, 0, static_cast<cudaStream_t>(stream)>>>(
+      partials, p->n_red_tiles, level2, ticket, inv_m * inv_m, d_norm_sq, p->d_flags);
   return static_cast<int>(cudaGetLastError());
 }
 

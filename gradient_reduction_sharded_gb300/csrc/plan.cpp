@@ -8,7 +8,8 @@
 // dp_shard = -1 auto; Mixle "Distributed Transformer Training", "Optimizer
 // and checkpoint semantics": plan from the logical parameter list):
 //  * buckets are tag-homogeneous, in tag order RA, PS, LS, AR, model order
-//    within a tag, greedy on per-rank bf16 bytes, tensors never split;
+//    within a tag, greedy on per-rank bf16 bytes (2 bytes per element, also
+//    for fp32 gradient plans, so both share one layout), tensors never split;
 //  * a LOCAL_SHARD tensor holds numel/tp elements per rank;
 //  * buckets are padded to a multiple of 8 * dp_shard elements so every
 //    shard starts on a 16-byte boundary;
@@ -38,9 +39,9 @@ int32_t group_size_of(int32_t tag, const grs_plan& p) {
 
 }  // namespace
 
-grs_status build_plan(const int64_t* numels, const int32_t* owners, int32_t n, int32_t world,
-                      int32_t tp, int32_t dp_replicate, int32_t dp_shard, int64_t bucket_bytes,
-                      grs_plan* p, std::string* why) {
+grs_status build_plan(const int64_t* numels, const int32_t* owners, const uint32_t* tensor_flags,
+                      int32_t n, int32_t world, int32_t tp, int32_t dp_replicate, int32_t dp_shard,
+                      int64_t bucket_bytes, int32_t grad_esize, grs_plan* p, std::string* why) {
   if (n <= 0 || numels == nullptr || owners == nullptr) {
     *why = "plan needs at least one tensor (numels/owners non-null)";
     return GRS_ERR_INVALID_ARG;
@@ -78,27 +79,39 @@ grs_status build_plan(const int64_t* numels, const int32_t* owners, int32_t n, i
       *why = "tensor " + std::to_string(i) + ": LOCAL_SHARD numel not divisible by tp";
       return GRS_ERR_SHAPE;
     }
+    if (tensor_flags != nullptr && (tensor_flags[i] & ~GRS_TENSOR_FROZEN) != 0) {
+      *why = "tensor " + std::to_string(i) + ": unknown tensor flag bits";
+      return GRS_ERR_INVALID_ARG;
+    }
   }
+  // A frozen tensor (no gradient, no optimizer state) takes no place in the plan.
+  auto frozen = [&](int32_t i) { return tensor_flags != nullptr && (tensor_flags[i] & GRS_TENSOR_FROZEN) != 0; };
 
   p->numel.assign(numels, numels + n);
   p->owner.assign(owners, owners + n);
+  p->tensor_flags.assign(n, 0u);
+  if (tensor_flags != nullptr) p->tensor_flags.assign(tensor_flags, tensor_flags + n);
+  p->tensor_live.assign(n, 1);
+  for (int32_t i = 0; i < n; ++i) p->tensor_live[i] = frozen(i) ? 0 : 1;
   p->world = world;
   p->tp = tp;
   p->dp_replicate = dp_replicate;
   p->dp_shard = dp_shard;
   p->dp = dp_replicate * dp_shard;
   p->bucket_bytes = bucket_bytes;
+  p->grad_esize = grad_esize;
   p->t_bucket.assign(n, -1);
   p->t_offset.assign(n, 0);
   p->buckets.clear();
   p->n_unique = 0;
-  for (int32_t i = 0; i < n; ++i) p->n_unique += numels[i];
+  for (int32_t i = 0; i < n; ++i)
+    if (!frozen(i)) p->n_unique += numels[i];
 
   // Greedy, tag-homogeneous buckets.
   for (int32_t tag = GRS_REPLICA_AVG; tag <= GRS_ALREADY_REDUCED; ++tag) {
     Bucket* cur = nullptr;
     for (int32_t i = 0; i < n; ++i) {
-      if (owners[i] != tag) continue;
+      if (owners[i] != tag || frozen(i)) continue;
       const int64_t per_rank = (tag == GRS_LOCAL_SHARD) ? numels[i] / tp : numels[i];
       if (cur != nullptr && cur->used > 0 && 2 * (cur->used + per_rank) > bucket_bytes) cur = nullptr;
       if (cur == nullptr) {
@@ -129,7 +142,8 @@ grs_status build_plan(const int64_t* numels, const int32_t* owners, int32_t n, i
     bk.state_off = state_off;
     bk.unit0 = static_cast<int32_t>(p->units.size());
     const int64_t gsz = bk.group_size;
-    int64_t T = std::min<int64_t>(STAGE_GRAD_BYTES / (2 * gsz), RED_RING_BYTES / (2 * (2 * gsz + 4)));
+    const int64_t es = grad_esize;
+    int64_t T = std::min<int64_t>(STAGE_GRAD_BYTES / (es * gsz), RED_RING_BYTES / (2 * (es * gsz + 4)));
     T = std::min<int64_t>(RED_MAX_T, std::max<int64_t>(8, T / 8 * 8));
     for (int32_t t = 0; t < bk.copies; ++t) {
       UnitDesc u{};
@@ -179,6 +193,10 @@ grs_status build_plan(const int64_t* numels, const int32_t* owners, int32_t n, i
   p->tensor_job0.assign(1, 0);
   int64_t chunks = 0;
   for (int32_t i = 0; i < n; ++i) {
+    if (p->t_bucket[i] < 0) {  // frozen: nothing to gather
+      p->tensor_job0.push_back(static_cast<int32_t>(p->jobs.size()));
+      continue;
+    }
     const Bucket& bk = p->buckets[p->t_bucket[i]];
     const int64_t per_rank = (owners[i] == GRS_LOCAL_SHARD) ? numels[i] / tp : numels[i];
     for (int32_t t = 0; t < bk.copies; ++t) {
@@ -194,6 +212,23 @@ grs_status build_plan(const int64_t* numels, const int32_t* owners, int32_t n, i
     p->tensor_job0.push_back(static_cast<int32_t>(p->jobs.size()));
   }
   p->n_gather_chunks = chunks;
+
+  // Segments per bucket, in offset order (tensors were appended in model
+  // order with increasing offsets inside each bucket).
+  std::vector<std::vector<int32_t>> members(p->buckets.size());
+  for (int32_t i = 0; i < n; ++i)
+    if (p->t_bucket[i] >= 0) members[p->t_bucket[i]].push_back(i);
+  p->seg_start.clear();
+  p->seg_tensor.clear();
+  p->bucket_seg0.assign(1, 0);
+  for (size_t b = 0; b < members.size(); ++b) {
+    for (int32_t i : members[b]) {
+      p->seg_start.push_back(p->t_offset[i]);
+      p->seg_tensor.push_back(i);
+    }
+    p->bucket_seg0.push_back(static_cast<int32_t>(p->seg_start.size()));
+  }
+  p->workspace_bytes = ws_factors_offset(red_tiles) + (static_cast<int64_t>(n) * 8 + 255) / 256 * 256;
   return GRS_OK;
 }
 

@@ -27,6 +27,8 @@ GRS_ERR_TIMEOUT = 6
 GRS_ERR_NONFINITE = 7
 GRS_ERR_NO_DEVICE = 8
 GRS_PLAN_HOST_ONLY = 1
+GRS_PLAN_FP32_GRADS = 2
+GRS_TENSOR_FROZEN = 1
 GRS_MAX_WORLD = 128
 GRS_NOALLOC_SCRATCH_BYTES = 4 << 20
 
@@ -47,7 +49,8 @@ class grs_plan_info(ctypes.Structure):
                 ("dp", ctypes.c_int32), ("device", ctypes.c_int32),
                 ("n_unique", ctypes.c_int64), ("n_rank_pad", ctypes.c_int64),
                 ("n_state_pad", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64),
-                ("n_reduce_tiles", ctypes.c_int64)]
+                ("n_reduce_tiles", ctypes.c_int64), ("grad_bytes", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 class grs_bucket_desc(ctypes.Structure):
@@ -61,7 +64,8 @@ class grs_bucket_desc(ctypes.Structure):
 class grs_tensor_desc(ctypes.Structure):
     _fields_ = [("bucket", ctypes.c_int32), ("owner", ctypes.c_int32),
                 ("numel", ctypes.c_int64), ("per_rank", ctypes.c_int64),
-                ("bucket_offset", ctypes.c_int64)]
+                ("bucket_offset", ctypes.c_int64), ("flags", ctypes.c_uint32),
+                ("reserved", ctypes.c_uint32)]
 
 
 class grs_adamw(ctypes.Structure):
@@ -82,6 +86,9 @@ _sig = {
     "grs_plan_create": ([_P(ctypes.c_int64), _P(ctypes.c_int32), ctypes.c_int32, ctypes.c_int32,
                          ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
                          ctypes.c_uint32, _P(_vp)], ctypes.c_int),
+    "grs_plan_create_ex": ([_P(ctypes.c_int64), _P(ctypes.c_int32), _P(ctypes.c_uint32), ctypes.c_int32,
+                            ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                            ctypes.c_int64, ctypes.c_uint32, _P(_vp)], ctypes.c_int),
     "grs_plan_destroy": ([_vp], None),
     "grs_plan_query": ([_vp, _P(grs_plan_info)], ctypes.c_int),
     "grs_bucket_info": ([_vp, ctypes.c_int32, _P(grs_bucket_desc)], ctypes.c_int),
@@ -93,6 +100,9 @@ _sig = {
     "grs_grad_norm_sq": ([_vp, _vp, ctypes.c_int32, _vp, ctypes.c_int32, _vp, _vp], ctypes.c_int),
     "grs_clip_adamw_step": ([_vp, _P(grs_adamw), _vp, _vp, _vp, _vp, _vp, _vp, _vp], ctypes.c_int),
     "grs_gather_params": ([_vp, _vp, _P(_vp), _vp], ctypes.c_int),
+    "grs_grad_norm_sq_masked": ([_vp, _vp, ctypes.c_int32, _vp, _vp, _vp, _vp], ctypes.c_int),
+    "grs_clip_adamw_step_masked": ([_vp, _P(grs_adamw), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                    _vp], ctypes.c_int),
     "grs_check_device_errors": ([_vp, _vp], ctypes.c_int),
     "grs_grad_norm_sq_noalloc": ([_vp, _vp, ctypes.c_int32, _vp, _vp], ctypes.c_int),
     "grs_step_from_host": ([_vp, _P(grs_adamw), _P(_vp), _P(_vp), _vp, _vp, _vp, _vp, _vp, _vp, _vp,
@@ -131,6 +141,19 @@ def grs_plan_create(numels: Sequence[int], owners: Sequence[int], world: int, tp
     out = _vp()
     _check(_lib.grs_plan_create(ne, ow, n, world, tp, dp_replicate, dp_shard, bucket_bytes, flags,
                                 ctypes.byref(out)), "grs_plan_create")
+    return out.value
+
+
+def grs_plan_create_ex(numels: Sequence[int], owners: Sequence[int], tensor_flags: Optional[Sequence[int]],
+                       world: int, tp: int, dp_replicate: int, dp_shard: int, bucket_bytes: int,
+                       flags: int = 0) -> int:
+    n = len(numels)
+    ne = (ctypes.c_int64 * max(1, n))(*numels)
+    ow = (ctypes.c_int32 * max(1, n))(*owners)
+    tf = None if tensor_flags is None else (ctypes.c_uint32 * max(1, n))(*tensor_flags)
+    out = _vp()
+    _check(_lib.grs_plan_create_ex(ne, ow, tf, n, world, tp, dp_replicate, dp_shard, bucket_bytes,
+                                   flags, ctypes.byref(out)), "grs_plan_create_ex")
     return out.value
 
 
@@ -212,6 +235,20 @@ def grs_grad_norm_sq_noalloc(plan: int, acc: int, n_micro: int, d_norm_sq: int, 
     no allocation); for callers that cannot allocate device memory."""
     _check(_lib.grs_grad_norm_sq_noalloc(plan, acc, n_micro, d_norm_sq, stream),
            "grs_grad_norm_sq_noalloc")
+
+
+def grs_grad_norm_sq_masked(plan: int, acc: int, n_micro: int, d_tensor_used: int, workspace: int,
+                            d_norm_sq: int, stream: int) -> None:
+    _check(_lib.grs_grad_norm_sq_masked(plan, acc, n_micro, d_tensor_used, workspace, d_norm_sq, stream),
+           "grs_grad_norm_sq_masked")
+
+
+def grs_clip_adamw_step_masked(plan: int, hp: grs_adamw, d_norm_sq: Optional[int], acc: int, master: int,
+                               m: int, v: int, params_bf16: int, d_tensor_used: int, d_tensor_steps: int,
+                               workspace: int, stream: int) -> None:
+    _check(_lib.grs_clip_adamw_step_masked(plan, ctypes.byref(hp), d_norm_sq, acc, master, m, v,
+                                           params_bf16, d_tensor_used, d_tensor_steps, workspace, stream),
+           "grs_clip_adamw_step_masked")
 
 
 def grs_check_device_errors(plan: int, stream: int) -> int:

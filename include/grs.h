@@ -88,7 +88,12 @@ typedef enum grs_status {
 } grs_status;
 
 /* grs_plan_create flags */
-#define GRS_PLAN_HOST_ONLY 1u /* build host tables only (queries work, launches fail) */
+#define GRS_PLAN_HOST_ONLY 1u  /* build host tables only (queries work, launches fail) */
+#define GRS_PLAN_FP32_GRADS 2u /* rank gradients are fp32 instead of bf16 ([ISSUE] "Proposed
+                                  scope": BF16/FP32); same layout, 4-byte elements */
+
+/* per-tensor flags (grs_plan_create_ex) */
+#define GRS_TENSOR_FROZEN 1u /* no gradient and no optimizer state: left out of the plan */
 
 typedef struct grs_plan grs_plan; /* opaque; owned by the caller via create/destroy */
 
@@ -106,6 +111,8 @@ typedef struct grs_plan_info {
   int64_t n_state_pad;    /* elements of accumulator / master / m / v / params */
   int64_t workspace_bytes;/* device workspace needed by reduce / norm calls; zero it once */
   int64_t n_reduce_tiles; /* norm partial slots (one per reduction tile) */
+  int32_t grad_bytes;     /* bytes per gradient element: 2 (bf16) or 4 (fp32) */
+  int32_t reserved;
 } grs_plan_info;
 
 typedef struct grs_bucket_desc {
@@ -121,11 +128,13 @@ typedef struct grs_bucket_desc {
 } grs_bucket_desc;
 
 typedef struct grs_tensor_desc {
-  int32_t bucket;
+  int32_t bucket;         /* -1 for a frozen tensor */
   int32_t owner;
   int64_t numel;          /* logical elements */
-  int64_t per_rank;       /* numel/tp for LOCAL_SHARD, else numel */
+  int64_t per_rank;       /* numel/tp for LOCAL_SHARD, else numel (0 when frozen) */
   int64_t bucket_offset;  /* element offset inside the bucket (per rank and per state row) */
+  uint32_t flags;         /* GRS_TENSOR_* as given to grs_plan_create_ex */
+  uint32_t reserved;
 } grs_tensor_desc;
 
 /* AdamW hyper-parameters (decoupled weight decay, Loshchilov & Hutter;
@@ -152,8 +161,10 @@ typedef struct grs_adamw {
  *                    world / (tp * dp_replicate) ([COSMOS] section 1).
  *   bucket_bytes   : cap on a bucket's per-rank bf16 bytes; a tensor larger
  *                    than the cap gets a bucket of its own.
- *   flags          : 0 or GRS_PLAN_HOST_ONLY.  Without it the plan's device
- *                    tables go to the current CUDA device.
+ *   flags          : GRS_PLAN_HOST_ONLY (no device tables; without it they go
+ *                    to the current CUDA device) and/or GRS_PLAN_FP32_GRADS
+ *                    (rank gradient buffers hold fp32; every "bf16 bits"
+ *                    gradient pointer below then points at floats).
  * Buckets hold one owner tag each, in tag order REPLICA_AVG, PARTIAL_SUM,
  * LOCAL_SHARD, ALREADY_REDUCED, model order inside a tag, filled greedily,
  * tensors packed back to back, padded to a multiple of 8 * dp_shard.
@@ -166,6 +177,16 @@ typedef struct grs_adamw {
 grs_status grs_plan_create(const int64_t* numels, const int32_t* owners, int32_t n_tensors,
                            int32_t world, int32_t tp, int32_t dp_replicate, int32_t dp_shard,
                            int64_t bucket_bytes, uint32_t flags, grs_plan** out);
+
+/* grs_plan_create with per-tensor flags ([ISSUE] "Proposed scope": frozen
+ * parameters and EP/model-owned exclusions).  tensor_flags: host array
+ * [n_tensors] of GRS_TENSOR_* bits, or NULL.  A GRS_TENSOR_FROZEN tensor
+ * keeps its index but gets no bucket, no rank-buffer space and no state:
+ * it is never reduced, clipped, updated or gathered.  Unknown bits ->
+ * INVALID_ARG. */
+grs_status grs_plan_create_ex(const int64_t* numels, const int32_t* owners, const uint32_t* tensor_flags,
+                              int32_t n_tensors, int32_t world, int32_t tp, int32_t dp_replicate,
+                              int32_t dp_shard, int64_t bucket_bytes, uint32_t flags, grs_plan** out);
 
 /* Free the plan and its device tables.  NULL is a no-op.  The caller must
  * ensure no launch using the plan is still in flight. */
@@ -187,8 +208,8 @@ grs_status grs_tensor_info(const grs_plan* plan, int32_t tensor, grs_tensor_desc
  * the bucket over dp_shard plus the all-reduce over dp_replicate plus the
  * TP reduction ([COSMOS] section 2), all shards computed.
  *   rank_grads : host array [world] of device pointers; rank_grads[k]
- *                points at rank k's copy of THIS bucket (bf16 bits,
- *                [padded] elements).  Only the ranks of the tag's group are
+ *                points at rank k's copy of THIS bucket ([padded] elements,
+ *                bf16 bits, or fp32 for GRS_PLAN_FP32_GRADS plans).  Only the ranks of the tag's group are
  *                read (ALREADY_REDUCED reads rank 0 only).
  *   acc        : device fp32 [copies * padded]: this bucket's state rows.
  *   accumulate : 0 overwrite (first microbatch), 1 add (later ones).
@@ -200,15 +221,15 @@ grs_status grs_tensor_info(const grs_plan* plan, int32_t tensor, grs_tensor_desc
  *                every call); required when emitting.
  * Errors: INVALID_ARG, ALIGNMENT (every pointer 16-B aligned), NO_DEVICE,
  * CUDA (launch failure). */
-grs_status grs_reduce_bucket(const grs_plan* plan, int32_t bucket, const uint16_t* const* rank_grads,
+grs_status grs_reduce_bucket(const grs_plan* plan, int32_t bucket, const void* const* rank_grads,
                              float* acc, int32_t accumulate, int32_t emit_norm_partials,
                              void* workspace, void* stream);
 
 /* The same for every bucket in one launch.
  *   rank_grads : host array [world] of device pointers to each rank's
- *                whole gradient buffer (bf16 bits, [n_rank_pad]).
+ *                whole gradient buffer ([n_rank_pad], bf16 bits or fp32).
  *   acc        : device fp32 [n_state_pad]. */
-grs_status grs_reduce_all(const grs_plan* plan, const uint16_t* const* rank_grads, float* acc,
+grs_status grs_reduce_all(const grs_plan* plan, const void* const* rank_grads, float* acc,
                           int32_t accumulate, int32_t emit_norm_partials, void* workspace,
                           void* stream);
 
@@ -256,14 +277,41 @@ grs_status grs_clip_adamw_step(const grs_plan* plan, const grs_adamw* hp, const 
                                const float* acc, float* master, float* m, float* v,
                                uint16_t* params_bf16, void* stream);
 
+/* Tensors without a gradient this step (PyTorch's grad None; [ISSUE]
+ * "Proposed scope": unused parameters).  d_tensor_used: device uint8
+ * [n_tensors], 1 = the tensor's rank-buffer region holds this step's
+ * gradient, 0 = no gradient.
+ *
+ * grs_grad_norm_sq_masked: like grs_grad_norm_sq with partials_ready = 0,
+ * but elements of tensors with used = 0 count as zero (clip_grad_norm_
+ * skips parameters without a gradient).  The fused reduce partials are not
+ * used.
+ *
+ * grs_clip_adamw_step_masked: like grs_clip_adamw_step for tensors with
+ * used = 1, each with its own step count: d_tensor_steps (device int32
+ * [n_tensors], zero before the first update, updated in place) is advanced
+ * for used tensors and its new value sets their bias correction (hp->step
+ * is ignored).  Tensors with used = 0 keep master, m, v, the bf16 copy and
+ * their step count unchanged (torch.optim.AdamW skips parameters without a
+ * gradient: no moment decay, no weight decay).  Entries of frozen tensors
+ * are ignored.  workspace as for the norm (the per-tensor factors live
+ * after the norm's part).  Padding stays exactly zero. */
+grs_status grs_grad_norm_sq_masked(const grs_plan* plan, const float* acc, int32_t n_micro,
+                                   const uint8_t* d_tensor_used, void* workspace, double* d_norm_sq,
+                                   void* stream);
+grs_status grs_clip_adamw_step_masked(const grs_plan* plan, const grs_adamw* hp, const double* d_norm_sq,
+                                      const float* acc, float* master, float* m, float* v,
+                                      uint16_t* params_bf16, const uint8_t* d_tensor_used,
+                                      int32_t* d_tensor_steps, void* workspace, void* stream);
+
 /* Gather: copy every tensor from the bucket-ordered bf16 parameter buffer
  * to its own full logical tensor ([COSMOS] section 2: all-gather of
  * parameters across shards; LOCAL_SHARD tensors reassembled from their tp
  * rows in dim-0 order).
  *   params_bf16 : device [n_state_pad].
  *   tensor_ptrs : host array [n_tensors] of device pointers, each to
- *                 numel bf16 elements; NULL entries are skipped.  Any
- *                 alignment is accepted. */
+ *                 numel bf16 elements; NULL entries (and frozen tensors)
+ *                 are skipped.  Any 2-byte alignment is accepted. */
 grs_status grs_gather_params(const grs_plan* plan, const uint16_t* params_bf16,
                              uint16_t* const* tensor_ptrs, void* stream);
 
@@ -278,10 +326,10 @@ grs_status grs_gather_params(const grs_plan* plan, const uint16_t* params_bf16,
  *   hp            : host struct; hp->n_micro microbatches.
  *   host_grads    : host array [n_micro * world] of HOST pointers (pinned
  *                   memory for full speed), microbatch-major (j*world + k),
- *                   each [n_rank_pad] bf16 bits.
+ *                   each [n_rank_pad] bf16 bits (fp32 for FP32_GRADS plans).
  *   dev_stage     : host array [2 * world] of device pointers (only the
  *                   first `world` are used when n_micro == 1), each
- *                   [n_rank_pad] bf16, 16-byte aligned: two staging halves
+ *                   [n_rank_pad] gradient elements, 16-byte aligned: two staging halves
  *                   alternating across microbatches.
  *   acc, master, m, v, params_bf16, workspace, d_norm_sq : as for the
  *                   device calls.
@@ -292,7 +340,7 @@ grs_status grs_gather_params(const grs_plan* plan, const uint16_t* params_bf16,
  * first call creates the plan's copy stream and events (freed by
  * grs_plan_destroy).  Errors: INVALID_ARG, ALIGNMENT, NO_DEVICE, CUDA. */
 grs_status grs_step_from_host(const grs_plan* plan, const grs_adamw* hp,
-                              const uint16_t* const* host_grads, uint16_t* const* dev_stage,
+                              const void* const* host_grads, void* const* dev_stage,
                               float* acc, float* master, float* m, float* v, uint16_t* params_bf16,
                               void* workspace, double* d_norm_sq, uint16_t* host_params,
                               double* host_norm_sq, void* stream);

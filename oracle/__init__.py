@@ -60,11 +60,19 @@ def lib():
                                       ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32,
                                       _i32p, _i32p, _i64p, _i32p, _i64p, _i64p, _i64p, _i64p]
             L.oracle_plan.restype = ctypes.c_int
+            L.oracle_plan_ex.argtypes = [_i64p, _i32p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                         ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
+                                         ctypes.c_int32, _i32p, _i32p, _i64p, _i32p, _i64p, _i64p,
+                                         _i64p, _i64p]
+            L.oracle_plan_ex.restype = ctypes.c_int
             L.oracle_rank.argtypes = [ctypes.c_int32] * 5
             L.oracle_rank.restype = ctypes.c_int32
             L.oracle_reduce_bucket.argtypes = [ctypes.c_int32] * 4 + [ctypes.c_int64, ctypes.c_int64,
                                                                       ctypes.c_int32, _u16p, _f64p]
             L.oracle_reduce_bucket.restype = ctypes.c_int
+            L.oracle_reduce_bucket_f32.argtypes = [ctypes.c_int32] * 4 + [ctypes.c_int64, ctypes.c_int64,
+                                                                          ctypes.c_int32, _f32p, _f64p]
+            L.oracle_reduce_bucket_f32.restype = ctypes.c_int
             L.oracle_norm_sq.argtypes = [_f64p, ctypes.c_int64, ctypes.c_int32]
             L.oracle_norm_sq.restype = ctypes.c_double
             L.oracle_clip_coef.argtypes = [ctypes.c_double, ctypes.c_double]
@@ -125,9 +133,24 @@ class OraclePlan:
     def shard_len(self, b: int) -> int:
         return int(self.b_padded[b]) // self.dp_shard
 
+    def per_rank(self, i: int) -> int:
+        if int(self.t_bucket[i]) < 0:
+            return 0
+        n = int(self.numel[i])
+        return n // self.tp if int(self.owner[i]) == LOCAL_SHARD else n
+
+    def tensor_rows(self, i: int):
+        """State ranges [lo, hi) of tensor i, one per bucket row."""
+        b = int(self.t_bucket[i])
+        if b < 0:
+            return []
+        P, o, n = int(self.b_padded[b]), int(self.t_offset[i]), self.per_rank(i)
+        return [(int(self.b_state_off[b]) + t * P + o, int(self.b_state_off[b]) + t * P + o + n)
+                for t in range(self.copies(b))]
+
 
 def plan(numels: Sequence[int], owners: Sequence[int], world: int, tp: int, dp_replicate: int,
-         dp_shard: int, bucket_bytes: int) -> OraclePlan:
+         dp_shard: int, bucket_bytes: int, tensor_flags: Optional[Sequence[int]] = None) -> OraclePlan:
     L = lib()
     n = len(numels)
     numel = np.ascontiguousarray(numels, dtype=np.int64)
@@ -144,8 +167,12 @@ def plan(numels: Sequence[int], owners: Sequence[int], world: int, tp: int, dp_r
     if n == 0:
         numel = np.zeros(1, np.int64)
         owner = np.zeros(1, np.int32)
-    st = L.oracle_plan(numel, owner, n, world, tp, dp_replicate, dp_shard, bucket_bytes, maxb,
-                       dims, tb, to, btag, bpad, bused, broff, bsoff)
+    fl = None
+    if tensor_flags is not None:
+        fl_arr = np.ascontiguousarray(list(tensor_flags) or [0], dtype=np.uint32)
+        fl = fl_arr.ctypes.data_as(ctypes.c_void_p)
+    st = L.oracle_plan_ex(numel, owner, fl, n, world, tp, dp_replicate, dp_shard, bucket_bytes, maxb,
+                          dims, tb, to, btag, bpad, bused, broff, bsoff)
     if st != OK:
         raise OracleError(st, "oracle_plan")
     nb = int(dims[3])
@@ -160,16 +187,18 @@ def rank(r: int, s: int, t: int, dp_shard: int, tp: int) -> int:
 
 def reduce_bucket(tag: int, tp: int, dp_replicate: int, dp_shard: int, P: int, used: int,
                   grads: np.ndarray) -> np.ndarray:
-    """grads: uint16 [M][R][P] -> fp64 acc [copies][P]."""
-    grads = np.ascontiguousarray(grads, dtype=np.uint16)
+    """grads: [M][R][P] uint16 (bf16 bits) or float32 -> fp64 acc [copies][P]."""
+    f32 = np.asarray(grads).dtype == np.float32
+    grads = np.ascontiguousarray(grads, dtype=np.float32 if f32 else np.uint16)
     M = grads.shape[0]
     R = tp * dp_replicate * dp_shard
     assert grads.shape == (M, R, P), (grads.shape, (M, R, P))
     copies = tp if tag == LOCAL_SHARD else 1
     acc = np.zeros((copies, P), np.float64)
-    st = lib().oracle_reduce_bucket(tag, tp, dp_replicate, dp_shard, P, used, M,
-                                    grads.reshape(-1) if grads.size else np.zeros(1, np.uint16),
-                                    acc.reshape(-1) if acc.size else np.zeros(1))
+    g = grads.reshape(-1) if grads.size else np.zeros(1, grads.dtype)
+    a = acc.reshape(-1) if acc.size else np.zeros(1)
+    fn = lib().oracle_reduce_bucket_f32 if f32 else lib().oracle_reduce_bucket
+    st = fn(tag, tp, dp_replicate, dp_shard, P, used, M, g, a)
     if st != OK:
         raise OracleError(st, "oracle_reduce_bucket")
     return acc
@@ -233,20 +262,48 @@ class UpdateResult:
     m: np.ndarray
     v: np.ndarray
     params_bf16: np.ndarray
+    # Optional brackets of master, m, v: the update evaluated at acc - delta
+    # and acc + delta, delta bounding an fp32 evaluation's accumulation error
+    # (see accumulation_error_bound).
+    lo: Optional[tuple] = None
+    hi: Optional[tuple] = None
+
+
+U32 = 2.0 ** -24  # unit roundoff of fp32
+
+
+def abs_inputs(g: np.ndarray) -> np.ndarray:
+    """|g| elementwise: bf16 bits with the sign cleared, or np.abs of fp32."""
+    g = np.asarray(g)
+    return np.abs(g) if g.dtype == np.float32 else (g & np.uint16(0x7FFF))
+
+
+def accumulation_error_bound(acc_abs: np.ndarray, M: int) -> np.ndarray:
+    """Forward error bound of accumulating a bucket row in fp32: every term
+    is added to a running fp32 sum (or, within a microbatch, compensated),
+    so |fl(acc) - acc| <= (M + 2) * u * sum |terms|, where acc_abs is the
+    same reduction of the absolute inputs (Higham, Accuracy and Stability of
+    Numerical Algorithms, recursive summation)."""
+    return (M + 2) * U32 * acc_abs
 
 
 def full_update(p: OraclePlan, grads_of, M: int, hp, max_norm: float, step: int,
                 master0: np.ndarray, m0: np.ndarray, v0: np.ndarray,
-                threads: int = 1) -> UpdateResult:
+                threads: int = 1, bounds: bool = False) -> UpdateResult:
     nsp = p.n_state_pad
     acc = np.zeros(nsp, np.float64)
+    delta = np.zeros(nsp, np.float64) if bounds else None
 
     def red(b):
         P = int(p.b_padded[b])
-        a = reduce_bucket(int(p.b_tag[b]), p.tp, p.dp_replicate, p.dp_shard, P,
-                          int(p.b_used[b]), grads_of(b))
+        g = grads_of(b)
+        a = reduce_bucket(int(p.b_tag[b]), p.tp, p.dp_replicate, p.dp_shard, P, int(p.b_used[b]), g)
         off = int(p.b_state_off[b])
         acc[off:off + a.size] = a.reshape(-1)
+        if bounds:
+            ab = reduce_bucket(int(p.b_tag[b]), p.tp, p.dp_replicate, p.dp_shard, P, int(p.b_used[b]),
+                               abs_inputs(g))
+            delta[off:off + ab.size] = accumulation_error_bound(ab.reshape(-1), M)
 
     if threads > 1:
         from concurrent.futures import ThreadPoolExecutor
@@ -257,15 +314,81 @@ def full_update(p: OraclePlan, grads_of, M: int, hp, max_norm: float, step: int,
             red(b)
     s = norm_sq(acc, M)
     c = clip_coef(s, max_norm)
-    master = np.zeros(nsp, np.float32)
-    mm = np.zeros(nsp, np.float32)
-    vv = np.zeros(nsp, np.float32)
-    bits = np.zeros(nsp, np.uint16)
+
+    def update(a):
+        master = np.zeros(nsp, np.float32)
+        mm = np.zeros(nsp, np.float32)
+        vv = np.zeros(nsp, np.float32)
+        bits = np.zeros(nsp, np.uint16)
+        for b in range(p.n_buckets):
+            P = int(p.b_padded[b])
+            for t in range(p.copies(b)):
+                o = int(p.b_state_off[b]) + t * P
+                r = adamw(a[o:o + P], int(p.b_used[b]), M, c, hp, step,
+                          master0[o:o + P], m0[o:o + P], v0[o:o + P])
+                master[o:o + P], mm[o:o + P], vv[o:o + P], bits[o:o + P] = r
+        return master, mm, vv, bits
+
+    master, mm, vv, bits = update(acc)
+    res = UpdateResult(acc, s, c, master, mm, vv, bits)
+    if bounds:
+        res.lo = update(acc - delta)[:3]
+        res.hi = update(acc + delta)[:3]
+    return res
+
+
+def full_update_masked(p: OraclePlan, grads_of, M: int, hp, max_norm: float, used, steps,
+                       master0: np.ndarray, m0: np.ndarray, v0: np.ndarray, params0: np.ndarray,
+                       threads: int = 1, bounds: bool = True):
+    """One update where tensor i has a gradient iff used[i] (PyTorch's grad
+    None otherwise): the norm sums used tensors only (clip_grad_norm_ skips
+    the others), and AdamW advances only used tensors, each with its own
+    step count (steps[i] before this update; torch.optim.AdamW keeps one per
+    parameter).  Unused tensors keep master, moments and bf16 copy.
+    Returns the result (with brackets when `bounds`) and the new step counts."""
+    nsp = p.n_state_pad
+    acc = np.zeros(nsp, np.float64)
+    delta = np.zeros(nsp, np.float64)
     for b in range(p.n_buckets):
         P = int(p.b_padded[b])
-        for t in range(p.copies(b)):
-            o = int(p.b_state_off[b]) + t * P
-            r = adamw(acc[o:o + P], int(p.b_used[b]), M, c, hp, step,
-                      master0[o:o + P], m0[o:o + P], v0[o:o + P])
-            master[o:o + P], mm[o:o + P], vv[o:o + P], bits[o:o + P] = r
-    return UpdateResult(acc, s, c, master, mm, vv, bits)
+        g = grads_of(b)
+        a = reduce_bucket(int(p.b_tag[b]), p.tp, p.dp_replicate, p.dp_shard, P, int(p.b_used[b]), g)
+        off = int(p.b_state_off[b])
+        acc[off:off + a.size] = a.reshape(-1)
+        if bounds:
+            ab = reduce_bucket(int(p.b_tag[b]), p.tp, p.dp_replicate, p.dp_shard, P, int(p.b_used[b]),
+                               abs_inputs(g))
+            delta[off:off + ab.size] = accumulation_error_bound(ab.reshape(-1), M)
+    s = 0.0
+    for i in range(len(p.numel)):
+        if used[i]:
+            for lo, hi in p.tensor_rows(i):
+                s += norm_sq(acc[lo:hi], M)
+    c = clip_coef(s, max_norm)
+    new_steps = list(steps)
+    for i in range(len(p.numel)):
+        if p.tensor_rows(i) and used[i]:
+            new_steps[i] = steps[i] + 1
+
+    def update(a):
+        master = np.zeros(nsp, np.float32)
+        mm = np.zeros(nsp, np.float32)
+        vv = np.zeros(nsp, np.float32)
+        bits = np.zeros(nsp, np.uint16)
+        for i in range(len(p.numel)):
+            for lo, hi in p.tensor_rows(i):
+                if used[i]:
+                    r = adamw(a[lo:hi], hi - lo, M, c, hp, new_steps[i], master0[lo:hi], m0[lo:hi],
+                              v0[lo:hi])
+                    master[lo:hi], mm[lo:hi], vv[lo:hi], bits[lo:hi] = r
+                else:
+                    master[lo:hi], mm[lo:hi], vv[lo:hi] = master0[lo:hi], m0[lo:hi], v0[lo:hi]
+                    bits[lo:hi] = params0[lo:hi]
+        return master, mm, vv, bits
+
+    master, mm, vv, bits = update(acc)
+    res = UpdateResult(acc, s, c, master, mm, vv, bits)
+    if bounds:
+        res.lo = update(acc - delta)[:3]
+        res.hi = update(acc + delta)[:3]
+    return res, new_steps

@@ -71,6 +71,20 @@ int oracle_plan(const int64_t* numel, const int32_t* owner, int32_t n,
                 int32_t* dims, int32_t* t_bucket, int64_t* t_offset,
                 int32_t* b_tag, int64_t* b_padded, int64_t* b_used,
                 int64_t* b_rank_off, int64_t* b_state_off) {
+  return oracle_plan_ex(numel, owner, 0, n, world, tp, dp_replicate, dp_shard, bucket_bytes,
+                        max_buckets, dims, t_bucket, t_offset, b_tag, b_padded, b_used, b_rank_off,
+                        b_state_off);
+}
+
+/* The plan with per-tensor flags ([ISSUE] "Proposed scope": frozen
+ * parameters).  A frozen tensor (flag bit 1) has no gradient and no
+ * optimizer state: it is left out of every bucket (t_bucket = -1). */
+int oracle_plan_ex(const int64_t* numel, const int32_t* owner, const uint32_t* flags, int32_t n,
+                   int32_t world, int32_t tp, int32_t dp_replicate, int32_t dp_shard,
+                   int64_t bucket_bytes, int32_t max_buckets,
+                   int32_t* dims, int32_t* t_bucket, int64_t* t_offset,
+                   int32_t* b_tag, int64_t* b_padded, int64_t* b_used,
+                   int64_t* b_rank_off, int64_t* b_state_off) {
   int32_t d[3];
   int st, i, tag, nb = 0;
   if (n <= 0 || numel == 0 || owner == 0) return OR_ERR_INVALID_ARG;
@@ -81,6 +95,11 @@ int oracle_plan(const int64_t* numel, const int32_t* owner, int32_t n,
     if (owner[i] < 0 || owner[i] > 3) return OR_ERR_INVALID_ARG;
     if (numel[i] < 0) return OR_ERR_SHAPE;
     if (owner[i] == OR_LOCAL_SHARD && numel[i] % tp != 0) return OR_ERR_SHAPE;
+    if (flags && (flags[i] & ~(uint32_t)OR_TENSOR_FROZEN)) return OR_ERR_INVALID_ARG;
+  }
+  for (i = 0; i < n; ++i) {
+    t_bucket[i] = -1;
+    t_offset[i] = 0;
   }
   for (tag = 0; tag < 4; ++tag) {
     int open = 0;
@@ -88,6 +107,7 @@ int oracle_plan(const int64_t* numel, const int32_t* owner, int32_t n,
     for (i = 0; i < n; ++i) {
       int64_t per_rank;
       if (owner[i] != tag) continue;
+      if (flags && (flags[i] & OR_TENSOR_FROZEN)) continue;
       per_rank = (tag == OR_LOCAL_SHARD) ? numel[i] / tp : numel[i];
       if (open && used > 0 && 2 * (used + per_rank) > bucket_bytes) {
         b_used[nb - 1] = used;
@@ -153,9 +173,19 @@ static double bf16_value(uint16_t bits) {
  * Microbatches ([ISSUE] "Proposed scope": gradient accumulation) are summed;
  * the mean over microbatches is taken where the gradient is used.
  * ------------------------------------------------------------------------ */
-int oracle_reduce_bucket(int32_t tag, int32_t tp, int32_t dp_replicate, int32_t dp_shard,
-                         int64_t P, int64_t used, int32_t M, const uint16_t* grads,
-                         double* acc) {
+/* Value of input element `i` of a gradient array, as fp64. */
+typedef double (*grad_value_fn)(const void* grads, int64_t i);
+
+static double value_bf16(const void* grads, int64_t i) {
+  return bf16_value(((const uint16_t*)grads)[i]);
+}
+
+static double value_f32(const void* grads, int64_t i) {
+  return (double)((const float*)grads)[i];
+}
+
+static int reduce_core(int32_t tag, int32_t tp, int32_t dp_replicate, int32_t dp_shard, int64_t P,
+                       int64_t used, int32_t M, const void* grads, grad_value_fn value, double* acc) {
   int32_t R = tp * dp_replicate * dp_shard;
   int32_t dp = dp_replicate * dp_shard;
   int32_t copies = (tag == OR_LOCAL_SHARD) ? tp : 1;
@@ -170,22 +200,22 @@ int oracle_reduce_bucket(int32_t tag, int32_t tp, int32_t dp_replicate, int32_t 
         continue;
       }
       for (j = 0; j < M; ++j) {
-        const uint16_t* mb = grads + (int64_t)j * R * P;
+        int64_t mb = (int64_t)j * R * P; /* first element of microbatch j */
         double dp_sum = 0.0;
         double reduced;
         if (tag == OR_ALREADY_REDUCED) {
-          reduced = bf16_value(mb[(int64_t)oracle_rank(0, 0, 0, dp_shard, tp) * P + e]);
+          reduced = value(grads, mb + (int64_t)oracle_rank(0, 0, 0, dp_shard, tp) * P + e);
         } else {
           for (r = 0; r < dp_replicate; ++r) {
             for (s = 0; s < dp_shard; ++s) {
               double tp_value;
               if (tag == OR_LOCAL_SHARD) {
                 /* no tensor-parallel reduction: this rank's own shard */
-                tp_value = bf16_value(mb[(int64_t)oracle_rank(r, s, c, dp_shard, tp) * P + e]);
+                tp_value = value(grads, mb + (int64_t)oracle_rank(r, s, c, dp_shard, tp) * P + e);
               } else {
                 double tp_sum = 0.0;
                 for (t = 0; t < tp; ++t)
-                  tp_sum += bf16_value(mb[(int64_t)oracle_rank(r, s, t, dp_shard, tp) * P + e]);
+                  tp_sum += value(grads, mb + (int64_t)oracle_rank(r, s, t, dp_shard, tp) * P + e);
                 tp_value = (tag == OR_REPLICA_AVG) ? tp_sum / tp : tp_sum;
               }
               dp_sum += tp_value;
@@ -199,6 +229,18 @@ int oracle_reduce_bucket(int32_t tag, int32_t tp, int32_t dp_replicate, int32_t 
     }
   }
   return OR_OK;
+}
+
+int oracle_reduce_bucket(int32_t tag, int32_t tp, int32_t dp_replicate, int32_t dp_shard,
+                         int64_t P, int64_t used, int32_t M, const uint16_t* grads,
+                         double* acc) {
+  return reduce_core(tag, tp, dp_replicate, dp_shard, P, used, M, grads, value_bf16, acc);
+}
+
+/* The same with fp32 gradients ([ISSUE] "Proposed scope": BF16/FP32). */
+int oracle_reduce_bucket_f32(int32_t tag, int32_t tp, int32_t dp_replicate, int32_t dp_shard,
+                             int64_t P, int64_t used, int32_t M, const float* grads, double* acc) {
+  return reduce_core(tag, tp, dp_replicate, dp_shard, P, used, M, grads, value_f32, acc);
 }
 
 /* Global squared norm of G = acc/M ([ISSUE] "Proposed scope": compare global

@@ -66,6 +66,18 @@ int oracle_plan(const int64_t* numel, const int32_t* owner, int32_t n,
                 int32_t* b_tag, int64_t* b_padded, int64_t* b_used,
                 int64_t* b_rank_off, int64_t* b_state_off);
 
+/* Tensor flag: frozen (no gradient, no state). */
+enum { OR_TENSOR_FROZEN = 1 };
+
+/* oracle_plan with per-tensor flags (NULL = none); frozen tensors get
+ * t_bucket = -1 and no space anywhere. */
+int oracle_plan_ex(const int64_t* numel, const int32_t* owner, const uint32_t* flags, int32_t n,
+                   int32_t world, int32_t tp, int32_t dp_replicate, int32_t dp_shard,
+                   int64_t bucket_bytes, int32_t max_buckets,
+                   int32_t* dims, int32_t* t_bucket, int64_t* t_offset,
+                   int32_t* b_tag, int64_t* b_padded, int64_t* b_used,
+                   int64_t* b_rank_off, int64_t* b_state_off);
+
 /* Rank index of mesh coordinate (replica r, shard s, tensor-parallel t). */
 int32_t oracle_rank(int32_t r, int32_t s, int32_t t, int32_t dp_shard, int32_t tp);
 
@@ -77,6 +89,10 @@ int32_t oracle_rank(int32_t r, int32_t s, int32_t t, int32_t dp_shard, int32_t t
 int oracle_reduce_bucket(int32_t tag, int32_t tp, int32_t dp_replicate, int32_t dp_shard,
                          int64_t P, int64_t used, int32_t M, const uint16_t* grads,
                          double* acc);
+
+/* The same with fp32 gradients: grads is [M][R][P] float. */
+int oracle_reduce_bucket_f32(int32_t tag, int32_t tp, int32_t dp_replicate, int32_t dp_shard,
+                             int64_t P, int64_t used, int32_t M, const float* grads, double* acc);
 
 /* Sum of (acc[e]/M)^2 over n values, fp64, in index order. */
 double oracle_norm_sq(const double* acc, int64_t n, int32_t M);

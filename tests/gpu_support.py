@@ -40,6 +40,8 @@ class Case:
     hp: tuple = (1e-3, 0.9, 0.999, 1e-8, 0.01)
     max_norm: float = 1.0
     master_std: float = 0.02
+    fp32_grads: bool = False
+    tensor_flags: Optional[List[int]] = None
 
 
 def case_from_workload(cid: int) -> Case:
@@ -59,14 +61,16 @@ class Run:
         self.c = c
         self.dev = torch.device(device)
         self.op = oracle.plan(c.numels, c.owners, c.world, c.tp, c.dp_replicate, c.dp_shard,
-                              c.bucket_bytes)
-        self.plan = g.grs_plan_create(c.numels, c.owners, c.world, c.tp, c.dp_replicate,
-                                      c.dp_shard, c.bucket_bytes)
+                              c.bucket_bytes, c.tensor_flags)
+        flags = g.GRS_PLAN_FP32_GRADS if c.fp32_grads else 0
+        self.plan = g.grs_plan_create_ex(c.numels, c.owners, c.tensor_flags, c.world, c.tp,
+                                         c.dp_replicate, c.dp_shard, c.bucket_bytes, flags)
         self.info = g.grs_plan_query(self.plan)
         nrp, nsp = self.info["n_rank_pad"], self.info["n_state_pad"]
         self.nrp, self.nsp = nrp, nsp
         self.poison = poison_padding
-        self.grads = [[torch.empty(max(nrp, 8), dtype=torch.bfloat16, device=self.dev)
+        gdt = torch.float32 if c.fp32_grads else torch.bfloat16
+        self.grads = [[torch.empty(max(nrp, 8), dtype=gdt, device=self.dev)
                        for _ in range(c.world)] for _ in range(c.n_micro)]
         self.fill_grads(step_seed)
         self.acc = torch.empty(max(nsp, 8), dtype=torch.float32, device=self.dev)
@@ -74,7 +78,7 @@ class Run:
                                            workloads.master_seed(c.seed_base), device=self.dev)
         self.m = torch.zeros(max(nsp, 8), dtype=torch.float32, device=self.dev)
         self.v = torch.zeros(max(nsp, 8), dtype=torch.float32, device=self.dev)
-        self.params = torch.empty(max(nsp, 8), dtype=torch.int16, device=self.dev)
+        self.params = self.master.to(torch.bfloat16).view(torch.int16).clone()
         self.ws = torch.zeros(max(self.info["workspace_bytes"], 16) // 4 + 4, dtype=torch.float32,
                               device=self.dev)
         self.norm = torch.zeros(1, dtype=torch.float64, device=self.dev)
@@ -85,13 +89,20 @@ class Run:
         for j in range(c.n_micro):
             for k in range(c.world):
                 seed = workloads.grad_seed(c.seed_base, j + 1000 * step_seed, k)
-                workloads.normal_bf16(self.nrp, c.grad_std, seed, device=self.dev,
-                                      out=self.grads[j][k][:self.nrp])
+                if c.fp32_grads:
+                    workloads.normal_f32(self.nrp, c.grad_std, seed, device=self.dev,
+                                         out=self.grads[j][k][:self.nrp])
+                else:
+                    workloads.normal_bf16(self.nrp, c.grad_std, seed, device=self.dev,
+                                          out=self.grads[j][k][:self.nrp])
                 if self.poison:
-                    bits = self.grads[j][k].view(torch.int16)
                     for b in range(self.op.n_buckets):
                         ro = int(self.op.b_rank_off[b])
-                        bits[ro + int(self.op.b_used[b]):ro + int(self.op.b_padded[b])] = NAN_BF16
+                        lo, hi = ro + int(self.op.b_used[b]), ro + int(self.op.b_padded[b])
+                        if c.fp32_grads:
+                            self.grads[j][k][lo:hi] = float("nan")
+                        else:
+                            self.grads[j][k].view(torch.int16)[lo:hi] = NAN_BF16
 
     def stream(self) -> int:
         return torch.cuda.current_stream(self.dev).cuda_stream
@@ -99,12 +110,13 @@ class Run:
     def ptrs(self, j):
         return [t.data_ptr() for t in self.grads[j]]
 
-    def reduce(self, per_bucket=False, emit=True):
+    def reduce(self, per_bucket=False, emit=True, n_micro=None):
         g = grs()
         c = self.c
         s = self.stream()
-        for j in range(c.n_micro):
-            last = emit and j == c.n_micro - 1
+        M = c.n_micro if n_micro is None else n_micro
+        for j in range(M):
+            last = emit and j == M - 1
             if per_bucket:
                 for b in range(self.info["n_buckets"]):
                     d = g.grs_bucket_info(self.plan, b)
@@ -135,6 +147,22 @@ class Run:
         self.norm_sq(partials_ready=partials_ready)
         self.adamw(max_norm=max_norm)
 
+    def masked_update(self, used_dev, steps_dev, n_micro=None, max_norm=None):
+        """Norm over used tensors and the per-tensor-step AdamW (the reduce
+        must have run)."""
+        g = grs()
+        c = self.c
+        M = c.n_micro if n_micro is None else n_micro
+        mn = c.max_norm if max_norm is None else max_norm
+        s = self.stream()
+        g.grs_grad_norm_sq_masked(self.plan, self.acc.data_ptr(), M, used_dev.data_ptr(),
+                                  self.ws.data_ptr(), self.norm.data_ptr(), s)
+        hp = g.make_adamw(c.hp[0], c.hp[1], c.hp[2], c.hp[3], c.hp[4], mn, 1, M)
+        g.grs_clip_adamw_step_masked(self.plan, hp, self.norm.data_ptr(), self.acc.data_ptr(),
+                                     self.master.data_ptr(), self.m.data_ptr(), self.v.data_ptr(),
+                                     self.params.data_ptr(), used_dev.data_ptr(), steps_dev.data_ptr(),
+                                     self.ws.data_ptr(), s)
+
     def check_flags(self) -> int:
         return grs().grs_check_device_errors(self.plan, self.stream())
 
@@ -146,10 +174,13 @@ class Run:
 
     # ---------------------------------------------------------------- oracle side
     def bucket_inputs(self, b) -> np.ndarray:
-        """[M][R][P] uint16 of bucket b, copied to the host."""
+        """[M][R][P] of bucket b copied to the host: uint16 bf16 bits, or
+        float32 for fp32-gradient plans."""
         ro = int(self.op.b_rank_off[b])
         P = int(self.op.b_padded[b])
         arr = torch.stack([torch.stack([t[ro:ro + P] for t in mb]) for mb in self.grads])
+        if self.c.fp32_grads:
+            return arr.cpu().numpy()
         return arr.view(torch.int16).cpu().numpy().view(np.uint16)
 
     def state_host(self):
@@ -162,7 +193,7 @@ def oracle_update(run: Run, master0, m0, v0, step: int, max_norm=None, threads=1
     c = run.c
     mn = c.max_norm if max_norm is None else max_norm
     return oracle.full_update(run.op, run.bucket_inputs, c.n_micro, c.hp, mn, step, master0, m0, v0,
-                              threads=threads)
+                              threads=threads, bounds=True)
 
 
 def assert_close(got, want, what, rtol=RTOL, atol=ATOL):
@@ -176,6 +207,29 @@ def assert_close(got, want, what, rtol=RTOL, atol=ATOL):
         i = np.flatnonzero(bad)[:5]
         raise AssertionError(f"{what}: {bad.sum()} of {bad.size} outside rel {rtol}/abs {atol}; "
                              f"first {i.tolist()} got {got[i].tolist()} want {want[i].tolist()}")
+
+
+def assert_close_bracketed(got, want, lo, hi, what, rtol=RTOL, atol=ATOL):
+    """rel/abs tolerance around the oracle's value, widened to the bracket
+    [min(lo, hi), max(lo, hi)] of the oracle's update at acc -/+ the fp32
+    accumulation error bound.  Away from ill-conditioned points the bracket
+    is far inside the tolerance; where AdamW's g / (|g| + eps) magnifies the
+    rounding an fp32 accumulator must make, it is what the arithmetic allows."""
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    a = np.asarray(lo, np.float64)
+    b = np.asarray(hi, np.float64)
+    lo = np.minimum(np.minimum(a, b), want)
+    hi = np.maximum(np.maximum(a, b), want)
+    both_nan = np.isnan(got) & np.isnan(want)
+    tol = atol + rtol * np.abs(want)
+    bad = ~both_nan & ~((got >= lo - tol) & (got <= hi + tol))
+    if bad.any():
+        i = np.flatnonzero(bad)[:5]
+        raise AssertionError(f"{what}: {bad.sum()} of {bad.size} outside the bracketed tolerance; first "
+                             f"{i.tolist()} got {got[i].tolist()} want {want[i].tolist()} "
+                             f"bracket {lo[i].tolist()}..{hi[i].tolist()}")
+    return int(((got < want - tol) | (got > want + tol)).sum())
 
 
 def bf16_ordered(bits):

@@ -10,8 +10,8 @@ import pytest
 import torch
 
 import oracle
-from gpu_support import (Case, Run, assert_bf16_cast, assert_close, case_from_workload, grs,
-                         oracle_update, padding_mask)
+from gpu_support import (Case, Run, assert_bf16_cast, assert_close, assert_close_bracketed,
+                         case_from_workload, grs, oracle_update, padding_mask)
 
 pytestmark = pytest.mark.gpu
 
@@ -35,9 +35,14 @@ def full_check(run: Run, res, what=""):
     norm = float(run.norm.cpu()[0])
     assert_close([norm], [res.norm_sq], f"{what} norm_sq")
     master, m, v = run.state_host()
-    assert_close(master, res.master, f"{what} master")
-    assert_close(m, res.m, f"{what} m")
-    assert_close(v, res.v, f"{what} v")
+    if res.lo is not None:
+        for name, got, want, lo, hi in zip(("master", "m", "v"), (master, m, v), (res.master, res.m, res.v),
+                                           res.lo, res.hi):
+            assert_close_bracketed(got, want, lo, hi, f"{what} {name}")
+    else:
+        assert_close(master, res.master, f"{what} master")
+        assert_close(m, res.m, f"{what} m")
+        assert_close(v, res.v, f"{what} v")
     for name, arr in (("master", master), ("m", m), ("v", v)):
         assert np.all(arr[pad] == 0), f"{what} {name} padding not zero"
     bits = run.params[:n].cpu().numpy().view(np.uint16)
@@ -61,6 +66,13 @@ def small_cases():
     cases["world1"] = Case([5000, 17, 300], [RA, PS, AR], 1, 1, 1, 1, 4096, 2, 1e-2, 15)
     cases["world3-non-pow2"] = Case([3001, 99, 330], [RA, PS, LS], 3, 1, 3, 1, 2048, 3, 1e-3, 16)
     cases["world6-auto-shard"] = Case([5000, 600, 36], [RA, LS, PS], 6, 2, 1, -1, 8192, 1, 1e-3, 17)
+    # fp32 gradient input (plan flag), many tiles, ragged tails, 3 microbatches
+    cases["fp32-grads-world8-M3"] = Case(
+        [70001, 1000, 40000 * 2, 77, 9999], [RA, PS, LS, AR, RA], 8, 2, 2, 2, 1 << 17, 3, 1e-3, 18,
+        fp32_grads=True)
+    cases["fp32-grads-world16"] = Case(
+        [100003, 1024, 65536 * 2, 4099], [RA, PS, LS, AR], 16, 2, 2, 4, 1 << 18, 1, 1e-3, 19,
+        fp32_grads=True)
     return cases
 
 
@@ -346,3 +358,87 @@ def test_step_from_host_matches_device_path(name):
     finally:
         a.close()
         b.close()
+
+
+def test_frozen_tensors_excluded():
+    """GRS_TENSOR_FROZEN tensors take no place in the plan: parity of the
+    update on the rest, and the gather leaves their storage untouched."""
+    c = Case([4096, 1000, 512 * 2, 96, 3000, 777], [RA, RA, LS, AR, PS, RA], 8, 2, 2, 2, 1 << 16, 2,
+             1e-3, 41, tensor_flags=[0, 1, 0, 0, 1, 0])
+    run = Run(c)
+    try:
+        assert grs().grs_tensor_info(run.plan, 1)["bucket"] == -1
+        master0, m0, v0 = run.state_host()
+        run.update()
+        res = oracle_update(run, master0, m0, v0, step=1)
+        full_check(run, res, "frozen")
+        outs = [torch.full((n,), 7, dtype=torch.int16, device="cuda") for n in c.numels]
+        grs().grs_gather_params(run.plan, run.params.data_ptr(), [t.data_ptr() for t in outs], run.stream())
+        torch.cuda.synchronize()
+        params = run.params[:run.nsp].cpu().numpy().view(np.uint16)
+        for i, n in enumerate(c.numels):
+            got = outs[i].cpu().numpy().view(np.uint16)
+            if c.tensor_flags[i]:
+                assert np.all(got == 7)
+            else:
+                assert np.array_equal(got, oracle.gather_tensor(run.op, i, params))
+    finally:
+        run.close()
+
+
+@pytest.mark.parametrize("fp32", [False, True])
+def test_unused_tensors_masked_update(fp32):
+    """Three steps with per-step masks of tensors that got no gradient
+    (grad None): masked norm + per-tensor-step AdamW against the oracle's
+    masked update, the oracle carrying its own state and step counts."""
+    c = Case([5000, 33, 4096 * 2, 17, 2048, 999, 64], [RA, RA, LS, AR, PS, RA, LS], 8, 2, 2, 2, 1 << 15,
+             2, 1e-3, 42, fp32_grads=fp32, tensor_flags=[0, 0, 0, 0, 0, 1, 0])
+    masks = [[1, 1, 1, 1, 1, 0, 1], [1, 0, 1, 0, 1, 0, 0], [0, 1, 1, 1, 0, 0, 1]]
+    run = Run(c)
+    try:
+        n = len(c.numels)
+        steps_dev = torch.zeros(n, dtype=torch.int32, device="cuda")
+        master, m, v = run.state_host()
+        bits = run.params[:run.nsp].cpu().numpy().view(np.uint16).copy()
+        steps = [0] * n
+        for k, used in enumerate(masks):
+            if k:
+                run.fill_grads(step_seed=k + 1)
+            used_dev = torch.tensor(used, dtype=torch.uint8, device="cuda")
+            run.reduce(emit=False)
+            run.masked_update(used_dev, steps_dev)
+            torch.cuda.synchronize()
+            assert run.check_flags() == 0
+            res, steps = oracle.full_update_masked(run.op, run.bucket_inputs, c.n_micro, c.hp, c.max_norm,
+                                                   used, steps, master, m, v, bits)
+            full_check(run, res, f"masked step {k + 1}")
+            got_steps = steps_dev.cpu().tolist()
+            for i in range(n):
+                if not c.tensor_flags[i]:
+                    assert got_steps[i] == steps[i], (i, got_steps, steps)
+            master, m, v, bits = res.master, res.m, res.v, res.params_bf16
+    finally:
+        run.close()
+
+
+def test_trailing_accumulation_window():
+    """A window that ends after 3 of 4 microbatches: the update averages the
+    3 accumulated microbatches (G = acc / 3)."""
+    c = SMALL["multi-tile-world16-M2"]
+    c = Case(c.numels, c.owners, c.world, c.tp, c.dp_replicate, c.dp_shard, c.bucket_bytes, 4,
+             c.grad_std, 43)
+    run = Run(c)
+    try:
+        master0, m0, v0 = run.state_host()
+        g = grs()
+        run.reduce(n_micro=3)
+        g.grs_grad_norm_sq(run.plan, run.acc.data_ptr(), 3, run.ws.data_ptr(), 1, run.norm.data_ptr(),
+                           run.stream())
+        hp = g.make_adamw(c.hp[0], c.hp[1], c.hp[2], c.hp[3], c.hp[4], c.max_norm, 1, 3)
+        g.grs_clip_adamw_step(run.plan, hp, run.norm.data_ptr(), run.acc.data_ptr(), run.master.data_ptr(),
+                              run.m.data_ptr(), run.v.data_ptr(), run.params.data_ptr(), run.stream())
+        res = oracle.full_update(run.op, lambda b: run.bucket_inputs(b)[:3], 3, c.hp, c.max_norm, 1,
+                                 master0, m0, v0, bounds=True)
+        full_check(run, res, "trailing window")
+    finally:
+        run.close()

@@ -51,7 +51,7 @@ def _compare_plan(grs, h, op, numels, owners):
     assert info["dp"] == op.dp
     assert info["n_rank_pad"] == op.n_rank_pad
     assert info["n_state_pad"] == op.n_state_pad
-    assert info["n_unique"] == int(sum(numels))
+    assert info["n_unique"] == int(sum(n for i, n in enumerate(numels) if int(op.t_bucket[i]) >= 0))
     for b in range(op.n_buckets):
         d = grs.grs_bucket_info(h, b)
         assert d["tag"] == int(op.b_tag[b])
@@ -86,12 +86,13 @@ GOLD = json.load(open(os.path.join(ROOT, "tests", "golden", "plan_layouts.json")
 
 @pytest.mark.parametrize("case", GOLD["cases"], ids=lambda c: c["name"])
 def test_plan_matches_hand_layouts(grs, orc, case):
-    h = grs.grs_plan_create(case["numel"], case["owner"], case["world"], case["tp"],
-                            case["dp_replicate"], case["dp_shard"], case["bucket_bytes"],
-                            grs.GRS_PLAN_HOST_ONLY)
+    h = grs.grs_plan_create_ex(case["numel"], case["owner"], case.get("tensor_flags"), case["world"],
+                               case["tp"], case["dp_replicate"], case["dp_shard"], case["bucket_bytes"],
+                               grs.GRS_PLAN_HOST_ONLY)
     try:
         op = oracle.plan(case["numel"], case["owner"], case["world"], case["tp"],
-                         case["dp_replicate"], case["dp_shard"], case["bucket_bytes"])
+                         case["dp_replicate"], case["dp_shard"], case["bucket_bytes"],
+                         case.get("tensor_flags"))
         _compare_plan(grs, h, op, case["numel"], case["owner"])
         info = grs.grs_plan_query(h)
         assert info["n_rank_pad"] == case["n_rank_pad"]
@@ -103,9 +104,9 @@ def test_plan_matches_hand_layouts(grs, orc, case):
 @pytest.mark.parametrize("case", GOLD["rejections"], ids=lambda c: c["why"])
 def test_plan_rejections_match(grs, case):
     with pytest.raises(grs.GrsError) as ei:
-        grs.grs_plan_create(case["numel"], case["owner"], case["world"], case["tp"],
-                            case["dp_replicate"], case["dp_shard"], case["bucket_bytes"],
-                            grs.GRS_PLAN_HOST_ONLY)
+        grs.grs_plan_create_ex(case["numel"], case["owner"], case.get("tensor_flags"), case["world"],
+                               case["tp"], case["dp_replicate"], case["dp_shard"], case["bucket_bytes"],
+                               grs.GRS_PLAN_HOST_ONLY)
     assert ei.value.status == case["status"]
     assert grs.grs_last_error() != ""
 
@@ -131,8 +132,11 @@ def test_random_plans_match_oracle(grs, orc):
         bb = int(rng.choice([2, 16, 64, 250, 1000, 1 << 20]))
         world = tp * dr * ds
         dsa = -1 if rng.random() < 0.2 else ds
-        op = oracle.plan(numels, owners, world, tp, dr, dsa, bb)
-        h = grs.grs_plan_create(numels, owners, world, tp, dr, dsa, bb, grs.GRS_PLAN_HOST_ONLY)
+        flags = [int(x) for x in (rng.random(n) < 0.2)] if trial % 2 else None
+        if flags is not None and all(flags):
+            flags[0] = 0
+        op = oracle.plan(numels, owners, world, tp, dr, dsa, bb, flags)
+        h = grs.grs_plan_create_ex(numels, owners, flags, world, tp, dr, dsa, bb, grs.GRS_PLAN_HOST_ONLY)
         try:
             _compare_plan(grs, h, op, numels, owners)
         finally:

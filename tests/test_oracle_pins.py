@@ -75,6 +75,33 @@ def test_hand_checked_two_microbatches(orc):
         assert s == want
 
 
+def test_hand_checked_fp32_gradients(orc):
+    """The same hand-checked values through the fp32-gradient entry."""
+    g = load("hand_checked_world4.json")
+    geo = g["geometry"]
+    P = 16
+    grads = np.zeros((1, 4, P), np.float32)
+    for k, v in enumerate(g["rank_values"]):
+        grads[0, k, :] = v
+    for name, exp in g["expected_acc"].items():
+        acc = oracle.reduce_bucket(TAGS[name], geo["tp"], geo["dp_replicate"], geo["dp_shard"],
+                                   P, P, grads)
+        for c, row in enumerate(exp):
+            assert np.all(acc[c] == row[0]), (name, c)
+
+
+@pytest.mark.parametrize("tag", [REPLICA_AVG, PARTIAL_SUM, LOCAL_SHARD, ALREADY_REDUCED])
+def test_fp32_and_bf16_entries_agree_on_bf16_values(orc, tag):
+    """fp32 inputs that are exactly bf16 values reduce to the same result as
+    the bf16 entry (the two decodings cannot disagree)."""
+    rng = np.random.default_rng(12)
+    tp, dr, ds, M, P = 2, 2, 2, 3, 40
+    bits = bf16(rng.normal(0, 1e-2, (M, tp * dr * ds, P)))
+    a = oracle.reduce_bucket(tag, tp, dr, ds, P, 33, bits)
+    b = oracle.reduce_bucket(tag, tp, dr, ds, P, 33, bits_to_f32(bits).reshape(bits.shape))
+    assert np.array_equal(a, b)
+
+
 def test_dp_mesh_rank_order(orc):
     g = load("hand_checked_world4.json")["dp_mesh_2x4"]
     geo = g["geometry"]
@@ -315,7 +342,7 @@ PLAN_CASES = load("plan_layouts.json")
 @pytest.mark.parametrize("case", PLAN_CASES["cases"], ids=lambda c: c["name"])
 def test_plan_hand_derived(orc, case):
     p = oracle.plan(case["numel"], case["owner"], case["world"], case["tp"], case["dp_replicate"],
-                    case["dp_shard"], case["bucket_bytes"])
+                    case["dp_shard"], case["bucket_bytes"], case.get("tensor_flags"))
     assert p.dp_shard == case["dp_shard_resolved"]
     for key in ("t_bucket", "t_offset", "b_tag", "b_used", "b_padded", "b_rank_off", "b_state_off"):
         assert list(getattr(p, key)) == case[key], key
@@ -329,7 +356,7 @@ def test_plan_hand_derived(orc, case):
 def test_plan_rejections(orc, case):
     with pytest.raises(oracle.OracleError) as ei:
         oracle.plan(case["numel"], case["owner"], case["world"], case["tp"], case["dp_replicate"],
-                    case["dp_shard"], case["bucket_bytes"])
+                    case["dp_shard"], case["bucket_bytes"], case.get("tensor_flags"))
     assert ei.value.code == case["status"]
 
 
@@ -359,3 +386,72 @@ def test_plan_workload_invariants(orc):
                 assert 2 * pos <= w.bucket_bytes
         n_unique = sum(int(p.b_used[b]) * p.copies(b) for b in range(p.n_buckets))
         assert n_unique == w.n_unique
+
+
+# --------------------------------------------------------------------------
+# Unused parameters (grad None) and frozen parameters against torch
+# --------------------------------------------------------------------------
+def test_masked_update_matches_torch_grad_none_semantics(orc):
+    """Four steps on a world-1 plan (the reduction is the identity), some
+    tensors without a gradient in some steps, one frozen tensor: the oracle's
+    masked update equals clip_grad_norm_ + torch.optim.AdamW, which skip
+    parameters whose grad is None (norm, moments, weight decay, step)."""
+    rng = np.random.default_rng(21)
+    numels = [24, 7, 16, 5]
+    flags = [0, 0, oracle_frozen(), 0]
+    hp = (1e-2, 0.9, 0.99, 1e-8, 0.05)
+    max_norm = 0.05
+    p = oracle.plan(numels, [REPLICA_AVG] * 4, 1, 1, 1, 1, 1 << 20, flags)
+    p0 = [rng.normal(0, 0.02, n).astype(np.float32) for n in numels]
+    params = [torch.nn.Parameter(torch.tensor(x, dtype=torch.float64)) for x in p0]
+    params[2].requires_grad_(False)
+    trainable = [params[i] for i in (0, 1, 3)]
+    opt = torch.optim.AdamW(trainable, lr=hp[0], betas=(hp[1], hp[2]), eps=hp[3], weight_decay=hp[4],
+                            foreach=False)
+    nsp = p.n_state_pad
+    master = np.zeros(nsp, np.float32)
+    for i in range(4):
+        for lo, hi in p.tensor_rows(i):
+            master[lo:hi] = p0[i]
+    m = np.zeros(nsp, np.float32)
+    v = np.zeros(nsp, np.float32)
+    bits = np.zeros(nsp, np.uint16)
+    steps = [0, 0, 0, 0]
+    masks = [[1, 1, 0, 1], [1, 0, 0, 1], [0, 1, 0, 1], [1, 1, 0, 0]]
+    for used in masks:
+        grads = [rng.normal(0, 0.03, n).astype(np.float32) for n in numels]
+        for i, prm in enumerate(params):
+            if i == 2:
+                continue
+            prm.grad = torch.tensor(grads[i], dtype=torch.float64) if used[i] else None
+        torch.nn.utils.clip_grad_norm_(trainable, max_norm, foreach=False)
+        opt.step()
+        host = np.zeros(p.n_rank_pad, np.float32)
+        for i in range(4):
+            b = int(p.t_bucket[i])
+            if b >= 0:
+                o = int(p.b_rank_off[b]) + int(p.t_offset[i])
+                host[o:o + numels[i]] = grads[i]
+
+        def grads_of(b, host=host):
+            ro, P = int(p.b_rank_off[b]), int(p.b_padded[b])
+            return host[ro:ro + P].reshape(1, 1, P)
+
+        res, steps = oracle.full_update_masked(p, grads_of, 1, hp, max_norm, used, steps, master, m, v, bits)
+        master, m, v, bits = res.master, res.m, res.v, res.params_bf16
+        for i in (0, 1, 3):
+            (lo, hi), = p.tensor_rows(i)
+            np.testing.assert_allclose(master[lo:hi], params[i].detach().numpy(), rtol=1e-6, atol=1e-9)
+            st = opt.state[params[i]]
+            if st:
+                # the oracle stores fp32 moments between steps; near a cancellation
+                # that rounding is absolute (~1e-10 for moments of size 1e-3)
+                np.testing.assert_allclose(m[lo:hi], st["exp_avg"].numpy(), rtol=1e-5, atol=1e-9)
+                np.testing.assert_allclose(v[lo:hi], st["exp_avg_sq"].numpy(), rtol=1e-5, atol=1e-13)
+                assert steps[i] == int(st["step"])
+        assert p.tensor_rows(2) == []
+    assert np.array_equal(params[2].detach().numpy(), p0[2].astype(np.float64))
+
+
+def oracle_frozen():
+    return 1
