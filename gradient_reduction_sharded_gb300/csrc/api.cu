@@ -370,6 +370,18 @@ grs_status grs_clip_adamw_step_masked(const grs_plan* p, const grs_adamw* hp, co
   return GRS_OK;
 }
 
+grs_status grs_selftest_bounded_wait(const grs_plan* p, int64_t limit_ns, void* stream) {
+  grs_status st = check_plan_device(p);
+  if (st != GRS_OK) return st;
+  if (limit_ns < 1000 || limit_ns > 2000000000LL)
+    return fail(GRS_ERR_INVALID_ARG, "grs_selftest_bounded_wait: limit_ns must be in [1 us, 2 s]");
+  DeviceGuard g(p->device);
+  if (!g.ok()) return fail(GRS_ERR_CUDA, "grs_selftest_bounded_wait: cannot select the plan's device");
+  const int e = grs::launch_bounded_wait_selftest(p, static_cast<uint64_t>(limit_ns), stream);
+  if (e != 0) return cuda_fail(static_cast<cudaError_t>(e), "grs_selftest_bounded_wait");
+  return GRS_OK;
+}
+
 grs_status grs_check_device_errors(const grs_plan* p, void* stream) {
   grs_status st = check_plan_device(p);
   if (st != GRS_OK) return st;

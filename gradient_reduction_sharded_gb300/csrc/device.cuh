@@ -53,10 +53,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait until the phase with `parity` has completed.  Gives up (returns
-// false, raises FLAG_TIMEOUT) after WAIT_LIMIT_NS or when *abort is set by
+// false, raises FLAG_TIMEOUT) after `limit_ns` or when *abort is set by
 // another thread of the block.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int* flags,
-                                                  volatile int* abort) {
+                                                  volatile int* abort, uint64_t limit_ns = WAIT_LIMIT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (;;) {
@@ -64,7 +64,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (global_ns() - t0 > WAIT_LIMIT_NS) {
+    if (global_ns() - t0 > limit_ns) {
       atomicOr(flags + FLAG_TIMEOUT, 1);
       *abort = 1;
       return false;

@@ -171,6 +171,7 @@ int launch_update(const grs_plan* p, const grs_adamw* hp, const double* d_norm_s
 int launch_accumulate(const grs_plan* p, int32_t bucket, float* acc, const float* mb, void* stream);
 int launch_gather(const grs_plan* p, const uint16_t* params, uint16_t* const* tensor_ptrs,
                   void* stream);
+int launch_bounded_wait_selftest(const grs_plan* p, uint64_t limit_ns, void* stream);
 // Second half of the norm: tile partials in `workspace` -> *d_norm_sq.
 int launch_norm_finish(const grs_plan* p, int32_t n_micro, void* workspace, double* d_norm_sq,
                        void* stream);

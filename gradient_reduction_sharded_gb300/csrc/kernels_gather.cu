@@ -77,7 +77,25 @@ __global__ void __launch_bounds__(GATHER_THREADS) gather_kernel(const __grid_con
   }
 }
 
+// Self-test of the bounded wait: one thread arms an mbarrier that nothing
+// will ever complete and waits on it through the same routine the
+// reduction's producer and consumers use.
+__global__ void bounded_wait_selftest_kernel(int* flags, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  abort_flag = 0;
+  fence_mbar_init();
+  mbar_wait_bounded(&bar, 0, flags, &abort_flag, limit_ns);
+}
+
 }  // namespace
+
+int launch_bounded_wait_selftest(const grs_plan* p, uint64_t limit_ns, void* stream) {
+  bounded_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(p->d_flags, limit_ns);
+  return static_cast<int>(cudaGetLastError());
+}
 
 int launch_gather(const grs_plan* p, const uint16_t* params, uint16_t* const* tensor_ptrs,
                   void* stream) {

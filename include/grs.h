@@ -377,6 +377,14 @@ grs_status grs_step_from_host(const grs_plan* plan, const grs_adamw* hp,
 grs_status grs_grad_norm_sq_noalloc(const grs_plan* plan, const float* acc, int32_t n_micro,
                                     double* d_norm_sq, void* stream);
 
+/* Failure-detection self-test: one kernel waits on an mbarrier that nothing
+ * completes, through the same bounded wait the reduction uses, gives up
+ * after limit_ns (1 us .. 2 s) and raises the plan's timeout flag; a
+ * following grs_check_device_errors returns GRS_ERR_TIMEOUT and the CUDA
+ * context stays usable ([MIXLE] "Backend split": failures surface as
+ * errors, not hangs). */
+grs_status grs_selftest_bounded_wait(const grs_plan* plan, int64_t limit_ns, void* stream);
+
 /* Synchronise `stream`, read and clear the plan's device flags.  Returns
  * TIMEOUT if a bounded device wait gave up, NONFINITE if a global norm was
  * NaN/Inf since the last check, else OK (or CUDA). */

@@ -18,7 +18,7 @@ import torch
 
 import oracle
 import workloads
-from gpu_support import assert_bf16_cast, assert_close
+from gpu_support import assert_bf16_cast, assert_close, assert_close_bracketed
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -115,6 +115,7 @@ def test_full_size_update_matches_oracle(cid):
         a = w.adamw
         hp = (a.lr, a.beta1, a.beta2, a.eps, a.weight_decay)
         want_acc, want_p, want_m, want_v, want_bits = [], [], [], [], []
+        lo_p, lo_m, lo_v, hi_p, hi_m, hi_v = [], [], [], [], [], []
         for b in range(op.n_buckets):
             pos = samples[b]
             ro, used = int(op.b_rank_off[b]), int(op.b_used[b])
@@ -124,6 +125,9 @@ def test_full_size_update_matches_oracle(cid):
             n_valid = int((pos < used).sum())
             acc = oracle.reduce_bucket(int(op.b_tag[b]), op.tp, op.dp_replicate, op.dp_shard,
                                        len(pos), n_valid, g)
+            delta = oracle.accumulation_error_bound(
+                oracle.reduce_bucket(int(op.b_tag[b]), op.tp, op.dp_replicate, op.dp_shard, len(pos),
+                                     n_valid, oracle.abs_inputs(g)), M)
             for t in range(op.copies(b)):
                 want_acc.append(acc[t])
                 off = sum(len(samples[bb]) * op.copies(bb) for bb in range(b)) + t * len(pos)
@@ -134,15 +138,20 @@ def test_full_size_update_matches_oracle(cid):
                 want_m.append(m1)
                 want_v.append(v1)
                 want_bits.append(bits)
+                for sign, dst in ((-1.0, (lo_p, lo_m, lo_v)), (1.0, (hi_p, hi_m, hi_v))):
+                    r = oracle.adamw(acc[t] + sign * delta[t], n_valid, M, c, hp, 1, m0, z, z)
+                    for d_, x in zip(dst, r[:3]):
+                        d_.append(x)
         got_acc = u.acc[sidx].cpu().numpy()
         got_p = u.master[sidx].cpu().numpy()
         got_m = u.m[sidx].cpu().numpy()
         got_v = u.v[sidx].cpu().numpy()
         got_bits = u.params[sidx].cpu().numpy().view(np.uint16)
         assert_close(got_acc, np.concatenate(want_acc), f"workload {cid} acc")
-        assert_close(got_p, np.concatenate(want_p), f"workload {cid} master")
-        assert_close(got_m, np.concatenate(want_m), f"workload {cid} m")
-        assert_close(got_v, np.concatenate(want_v), f"workload {cid} v")
+        cat = np.concatenate
+        assert_close_bracketed(got_p, cat(want_p), cat(lo_p), cat(hi_p), f"workload {cid} master")
+        assert_close_bracketed(got_m, cat(want_m), cat(lo_m), cat(hi_m), f"workload {cid} m")
+        assert_close_bracketed(got_v, cat(want_v), cat(lo_v), cat(hi_v), f"workload {cid} v")
         assert_bf16_cast(got_bits, got_p, np.concatenate(want_bits), np.concatenate(want_p),
                          f"workload {cid} params")
         pad = np.concatenate([np.repeat((samples[b] >= int(op.b_used[b]))[None], op.copies(b), 0).reshape(-1)

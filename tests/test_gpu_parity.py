@@ -442,3 +442,26 @@ def test_trailing_accumulation_window():
         full_check(run, res, "trailing window")
     finally:
         run.close()
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    """A device wait that nothing completes gives up after its limit, the
+    plan reports GRS_ERR_TIMEOUT, and the next update still runs correctly."""
+    g = grs()
+    c = SMALL["odd-ds2"]
+    run = Run(c)
+    try:
+        import time
+        t0 = time.time()
+        g.grs_selftest_bounded_wait(run.plan, 20_000_000, run.stream())  # 20 ms
+        assert run.check_flags() == g.GRS_ERR_TIMEOUT
+        assert time.time() - t0 < 5.0
+        assert run.check_flags() == 0
+        with pytest.raises(g.GrsError):
+            g.grs_selftest_bounded_wait(run.plan, 10, run.stream())
+        master0, m0, v0 = run.state_host()
+        run.update()
+        assert run.check_flags() == 0
+        full_check(run, oracle_update(run, master0, m0, v0, step=1), "after timeout")
+    finally:
+        run.close()
