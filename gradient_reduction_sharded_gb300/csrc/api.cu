@@ -370,6 +370,29 @@ grs_status grs_clip_adamw_step_masked(const grs_plan* p, const grs_adamw* hp, co
   return GRS_OK;
 }
 
+static grs_status state_logical_common(const grs_plan* p, const float* a, float* b, bool to_logical,
+                                       void* stream, const char* who) {
+  grs_status st = check_plan_device(p);
+  if (st != GRS_OK) return st;
+  if (a == nullptr || b == nullptr) return fail(GRS_ERR_INVALID_ARG, std::string(who) + ": NULL argument");
+  if ((reinterpret_cast<uintptr_t>(a) & 3u) != 0 || (reinterpret_cast<uintptr_t>(b) & 3u) != 0)
+    return fail(GRS_ERR_ALIGNMENT, std::string(who) + ": pointer not 4-byte aligned");
+  DeviceGuard g(p->device);
+  if (!g.ok()) return fail(GRS_ERR_CUDA, std::string(who) + ": cannot select the plan's device");
+  const int e = to_logical ? grs::launch_state_to_logical(p, a, b, stream)
+                           : grs::launch_state_from_logical(p, a, b, stream);
+  if (e != 0) return cuda_fail(static_cast<cudaError_t>(e), who);
+  return GRS_OK;
+}
+
+grs_status grs_state_to_logical(const grs_plan* p, const float* state, float* logical, void* stream) {
+  return state_logical_common(p, state, logical, true, stream, "grs_state_to_logical");
+}
+
+grs_status grs_state_from_logical(const grs_plan* p, const float* logical, float* state, void* stream) {
+  return state_logical_common(p, logical, state, false, stream, "grs_state_from_logical");
+}
+
 grs_status grs_selftest_bounded_wait(const grs_plan* p, int64_t limit_ns, void* stream) {
   grs_status st = check_plan_device(p);
   if (st != GRS_OK) return st;

@@ -70,10 +70,11 @@ struct Bucket {
 // Segmented-copy job of the gather: `len` elements from state offset
 // `src` to element `dst` of tensor `tensor`.
 struct GatherJob {
-  int64_t src;
-  int64_t dst;
+  int64_t src;      // state offset
+  int64_t dst;      // offset inside the logical tensor
   int64_t len;
-  int64_t chunk0;  // first global chunk of this job
+  int64_t chunk0;   // first global chunk of this job
+  int64_t logical;  // offset in the canonical logical order (all live tensors, model order)
   int32_t tensor;
   int32_t pad_;
 };
@@ -172,6 +173,9 @@ int launch_accumulate(const grs_plan* p, int32_t bucket, float* acc, const float
 int launch_gather(const grs_plan* p, const uint16_t* params, uint16_t* const* tensor_ptrs,
                   void* stream);
 int launch_bounded_wait_selftest(const grs_plan* p, uint64_t limit_ns, void* stream);
+// fp32 state arrays: bucket layout <-> canonical logical order.
+int launch_state_to_logical(const grs_plan* p, const float* state, float* logical, void* stream);
+int launch_state_from_logical(const grs_plan* p, const float* logical, float* state, void* stream);
 // Second half of the norm: tile partials in `workspace` -> *d_norm_sq.
 int launch_norm_finish(const grs_plan* p, int32_t n_micro, void* workspace, double* d_norm_sq,
                        void* stream);

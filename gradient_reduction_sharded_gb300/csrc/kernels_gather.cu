@@ -77,6 +77,37 @@ __global__ void __launch_bounds__(GATHER_THREADS) gather_kernel(const __grid_con
   }
 }
 
+// fp32 state <-> canonical logical order: the same segmented jobs, one
+// block per GATHER_CHUNK slice of a job, 16-byte vectors where source and
+// destination are co-aligned.
+template <bool kToLogical>
+__global__ void __launch_bounds__(GATHER_THREADS) state_logical_kernel(const GatherJob* __restrict__ jobs,
+                                                                        int32_t n_jobs, const float* __restrict__ src_base,
+                                                                        float* __restrict__ dst_base) {
+  const int64_t chunk = blockIdx.x;
+  const int j = find_job(jobs, 0, n_jobs, chunk);
+  const GatherJob jb = jobs[j];
+  const int64_t off = (chunk - jb.chunk0) * GATHER_CHUNK;
+  const int64_t rem = jb.len - off;
+  const int64_t n = rem < GATHER_CHUNK ? rem : GATHER_CHUNK;
+  const float* src = src_base + (kToLogical ? jb.src : jb.logical) + off;
+  float* dst = dst_base + (kToLogical ? jb.logical : jb.src) + off;
+  const uintptr_t sa = reinterpret_cast<uintptr_t>(src);
+  const uintptr_t da = reinterpret_cast<uintptr_t>(dst);
+  if (((sa ^ da) & 15) == 0) {
+    const int64_t h = static_cast<int64_t>(((16 - (sa & 15)) & 15) >> 2);
+    const int64_t head = h < n ? h : n;
+    for (int64_t i = threadIdx.x; i < head; i += GATHER_THREADS) dst[i] = src[i];
+    const int64_t nv = (n - head) >> 2;
+    const float4* s4 = reinterpret_cast<const float4*>(src + head);
+    float4* d4 = reinterpret_cast<float4*>(dst + head);
+    for (int64_t i = threadIdx.x; i < nv; i += GATHER_THREADS) d4[i] = __ldcs(s4 + i);
+    for (int64_t i = head + nv * 4 + threadIdx.x; i < n; i += GATHER_THREADS) dst[i] = src[i];
+  } else {
+    for (int64_t i = threadIdx.x; i < n; i += GATHER_THREADS) dst[i] = src[i];
+  }
+}
+
 // Self-test of the bounded wait: one thread arms an mbarrier that nothing
 // will ever complete and waits on it through the same routine the
 // reduction's producer and consumers use.
@@ -94,6 +125,25 @@ __global__ void bounded_wait_selftest_kernel(int* flags, uint64_t limit_ns) {
 
 int launch_bounded_wait_selftest(const grs_plan* p, uint64_t limit_ns, void* stream) {
   bounded_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(p->d_flags, limit_ns);
+  return static_cast<int>(cudaGetLastError());
+}
+
+int launch_state_to_logical(const grs_plan* p, const float* state, float* logical, void* stream) {
+  if (p->n_gather_chunks <= 0) return 0;
+  state_logical_kernel<true><<<static_cast<unsigned>(p->n_gather_chunks), GATHER_THREADS, 0,
+                               static_cast<cudaStream_t>(stream)>>>(
+      p->d_jobs, static_cast<int32_t>(p->jobs.size()), state, logical);
+  return static_cast<int>(cudaGetLastError());
+}
+
+int launch_state_from_logical(const grs_plan* p, const float* logical, float* state, void* stream) {
+  cudaError_t e = cudaMemsetAsync(state, 0, static_cast<size_t>(p->n_state_pad) * sizeof(float),
+                                  static_cast<cudaStream_t>(stream));  // padding = 0
+  if (e != cudaSuccess) return static_cast<int>(e);
+  if (p->n_gather_chunks <= 0) return 0;
+  state_logical_kernel<false><<<static_cast<unsigned>(p->n_gather_chunks), GATHER_THREADS, 0,
+                                static_cast<cudaStream_t>(stream)>>>(
+      p->d_jobs, static_cast<int32_t>(p->jobs.size()), logical, state);
   return static_cast<int>(cudaGetLastError());
 }
 

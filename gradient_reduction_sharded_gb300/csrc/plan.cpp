@@ -192,6 +192,7 @@ grs_status build_plan(const int64_t* numels, const int32_t* owners, const uint32
   p->jobs.clear();
   p->tensor_job0.assign(1, 0);
   int64_t chunks = 0;
+  int64_t logical = 0;  // canonical order: live tensors in model order, full logical extent
   for (int32_t i = 0; i < n; ++i) {
     if (p->t_bucket[i] < 0) {  // frozen: nothing to gather
       p->tensor_job0.push_back(static_cast<int32_t>(p->jobs.size()));
@@ -205,10 +206,12 @@ grs_status build_plan(const int64_t* numels, const int32_t* owners, const uint32
       j.dst = static_cast<int64_t>(t) * per_rank;
       j.len = per_rank;
       j.chunk0 = chunks;
+      j.logical = logical + static_cast<int64_t>(t) * per_rank;
       j.tensor = i;
       chunks += (per_rank + GATHER_CHUNK - 1) / GATHER_CHUNK;
       p->jobs.push_back(j);
     }
+    logical += numels[i];
     p->tensor_job0.push_back(static_cast<int32_t>(p->jobs.size()));
   }
   p->n_gather_chunks = chunks;

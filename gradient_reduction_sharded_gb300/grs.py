@@ -105,6 +105,8 @@ _sig = {
                                     _vp], ctypes.c_int),
     "grs_check_device_errors": ([_vp, _vp], ctypes.c_int),
     "grs_selftest_bounded_wait": ([_vp, ctypes.c_int64, _vp], ctypes.c_int),
+    "grs_state_to_logical": ([_vp, _vp, _vp, _vp], ctypes.c_int),
+    "grs_state_from_logical": ([_vp, _vp, _vp, _vp], ctypes.c_int),
     "grs_grad_norm_sq_noalloc": ([_vp, _vp, ctypes.c_int32, _vp, _vp], ctypes.c_int),
     "grs_step_from_host": ([_vp, _P(grs_adamw), _P(_vp), _P(_vp), _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                             _vp, _vp, _vp], ctypes.c_int),
@@ -250,6 +252,14 @@ def grs_clip_adamw_step_masked(plan: int, hp: grs_adamw, d_norm_sq: Optional[int
     _check(_lib.grs_clip_adamw_step_masked(plan, ctypes.byref(hp), d_norm_sq, acc, master, m, v,
                                            params_bf16, d_tensor_used, d_tensor_steps, workspace, stream),
            "grs_clip_adamw_step_masked")
+
+
+def grs_state_to_logical(plan: int, state: int, logical: int, stream: int) -> None:
+    _check(_lib.grs_state_to_logical(plan, state, logical, stream), "grs_state_to_logical")
+
+
+def grs_state_from_logical(plan: int, logical: int, state: int, stream: int) -> None:
+    _check(_lib.grs_state_from_logical(plan, logical, state, stream), "grs_state_from_logical")
 
 
 def grs_selftest_bounded_wait(plan: int, limit_ns: int, stream: int) -> None:

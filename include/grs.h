@@ -385,6 +385,21 @@ grs_status grs_grad_norm_sq_noalloc(const grs_plan* plan, const float* acc, int3
  * errors, not hangs). */
 grs_status grs_selftest_bounded_wait(const grs_plan* plan, int64_t limit_ns, void* stream);
 
+/* Layout conversion of an fp32 state array (master, m, v or the
+ * accumulator) between the plan's bucket layout [n_state_pad] and the
+ * canonical logical order [n_unique]: every live (not frozen) tensor in
+ * model order, each over its full logical extent (a LOCAL_SHARD tensor's tp
+ * rows concatenated in dim-0 order).  The logical order does not depend on
+ * tp, dp_replicate, dp_shard, owner tags or bucket size, so a checkpoint
+ * written under one plan restores exactly under another: state_to_logical
+ * with the writer's plan, state_from_logical with the reader's ([ISSUE]
+ * "Preserved prototype": checkpoints restored exactly across ownership
+ * changes, matching the next Adam update; [MIXLE] "Optimizer and checkpoint
+ * semantics").  state_from_logical writes every padding element as 0.
+ * Both pointers are device memory, 4-byte aligned. */
+grs_status grs_state_to_logical(const grs_plan* plan, const float* state, float* logical, void* stream);
+grs_status grs_state_from_logical(const grs_plan* plan, const float* logical, float* state, void* stream);
+
 /* Synchronise `stream`, read and clear the plan's device flags.  Returns
  * TIMEOUT if a bounded device wait gave up, NONFINITE if a global norm was
  * NaN/Inf since the last check, else OK (or CUDA). */

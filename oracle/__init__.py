@@ -87,6 +87,11 @@ def lib():
                                                ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                                _u16p, _u16p]
             L.oracle_gather_tensor.restype = None
+            for nm in ("oracle_gather_tensor_f32", "oracle_scatter_tensor_f32"):
+                f = getattr(L, nm)
+                f.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
+                              ctypes.c_int64, ctypes.c_int64, _f32p, _f32p]
+                f.restype = None
             _lib = L
     return _lib
 
@@ -245,6 +250,42 @@ def gather_tensor(p: OraclePlan, i: int, params_full: np.ndarray) -> np.ndarray:
         lib().oracle_gather_tensor(n, int(p.owner[i]), p.tp, int(p.b_state_off[b]),
                                    int(p.b_padded[b]), int(p.t_offset[i]), src, dst)
     return dst[:n]
+
+
+def to_logical(p: OraclePlan, state: np.ndarray) -> np.ndarray:
+    """fp32 state in bucket layout -> canonical logical order (live tensors in
+    model order, each over its full logical extent)."""
+    state = np.ascontiguousarray(state, dtype=np.float32).reshape(-1)
+    parts = []
+    for i in range(len(p.numel)):
+        b = int(p.t_bucket[i])
+        if b < 0:
+            continue
+        n = int(p.numel[i])
+        dst = np.zeros(max(1, n), np.float32)
+        if n:
+            lib().oracle_gather_tensor_f32(n, int(p.owner[i]), p.tp, int(p.b_state_off[b]),
+                                           int(p.b_padded[b]), int(p.t_offset[i]), state, dst)
+        parts.append(dst[:n])
+    return np.concatenate(parts) if parts else np.zeros(0, np.float32)
+
+
+def from_logical(p: OraclePlan, logical: np.ndarray) -> np.ndarray:
+    """Canonical logical order -> fp32 state in bucket layout (padding 0)."""
+    logical = np.ascontiguousarray(logical, dtype=np.float32).reshape(-1)
+    state = np.zeros(max(1, p.n_state_pad), np.float32)
+    pos = 0
+    for i in range(len(p.numel)):
+        b = int(p.t_bucket[i])
+        if b < 0:
+            continue
+        n = int(p.numel[i])
+        if n:
+            src = np.ascontiguousarray(logical[pos:pos + n])
+            lib().oracle_scatter_tensor_f32(n, int(p.owner[i]), p.tp, int(p.b_state_off[b]),
+                                            int(p.b_padded[b]), int(p.t_offset[i]), src, state)
+        pos += n
+    return state[:p.n_state_pad]
 
 
 # ---------------------------------------------------------------------------

@@ -341,3 +341,36 @@ void oracle_gather_tensor(int64_t numel, int32_t owner, int32_t tp, int64_t buck
     for (i = 0; i < numel; ++i) dst[i] = params_full[bucket_state_off + tensor_offset + i];
   }
 }
+
+/* fp32 state of one tensor, bucket layout <-> its full logical extent (the
+ * same placement as oracle_gather_tensor), for checkpoints ([ISSUE]
+ * "Preserved prototype": exact restore across ownership changes). */
+void oracle_gather_tensor_f32(int64_t numel, int32_t owner, int32_t tp, int64_t bucket_state_off,
+                              int64_t bucket_padded, int64_t tensor_offset, const float* state,
+                              float* dst) {
+  int64_t i;
+  if (owner == OR_LOCAL_SHARD) {
+    int64_t chunk = numel / tp;
+    int32_t t;
+    for (t = 0; t < tp; ++t)
+      for (i = 0; i < chunk; ++i)
+        dst[t * chunk + i] = state[bucket_state_off + (int64_t)t * bucket_padded + tensor_offset + i];
+  } else {
+    for (i = 0; i < numel; ++i) dst[i] = state[bucket_state_off + tensor_offset + i];
+  }
+}
+
+void oracle_scatter_tensor_f32(int64_t numel, int32_t owner, int32_t tp, int64_t bucket_state_off,
+                               int64_t bucket_padded, int64_t tensor_offset, const float* src,
+                               float* state) {
+  int64_t i;
+  if (owner == OR_LOCAL_SHARD) {
+    int64_t chunk = numel / tp;
+    int32_t t;
+    for (t = 0; t < tp; ++t)
+      for (i = 0; i < chunk; ++i)
+        state[bucket_state_off + (int64_t)t * bucket_padded + tensor_offset + i] = src[t * chunk + i];
+  } else {
+    for (i = 0; i < numel; ++i) state[bucket_state_off + tensor_offset + i] = src[i];
+  }
+}

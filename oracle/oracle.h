@@ -117,6 +117,15 @@ void oracle_gather_tensor(int64_t numel, int32_t owner, int32_t tp, int64_t buck
                           int64_t bucket_padded, int64_t tensor_offset,
                           const uint16_t* params_full, uint16_t* dst);
 
+/* fp32 state of one tensor: bucket layout -> logical (gather) and back
+ * (scatter; padding untouched). */
+void oracle_gather_tensor_f32(int64_t numel, int32_t owner, int32_t tp, int64_t bucket_state_off,
+                              int64_t bucket_padded, int64_t tensor_offset, const float* state,
+                              float* dst);
+void oracle_scatter_tensor_f32(int64_t numel, int32_t owner, int32_t tp, int64_t bucket_state_off,
+                               int64_t bucket_padded, int64_t tensor_offset, const float* src,
+                               float* state);
+
 #ifdef __cplusplus
 }
 #endif
