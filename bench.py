@@ -497,6 +497,97 @@ def run_reference(args, rank, world_size):
             "e2e": {"value": ms, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_overlap(args):
+    """Reduction overlapped with a simulated backward pass (a separate
+    measurement, not the bench line).  The backward is one bf16 GEMM per
+    bucket (tensor-core bound, --gemm n: n x n x n), in reverse bucket order
+    on its own stream, recording an event when each bucket's gradients are
+    'ready'; the reductions run on a side stream as soon as their events
+    fire, with the grid capped at --max-ctas CTAs, then the norm finish and
+    clip + AdamW.  Compared with the same work serialized (all GEMMs, then
+    the grouped reduction and the update)."""
+    import torch
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    w = workloads.get(args.workload, args.blocks)
+    u = GpuUpdate(w, device)
+    g = u.grs
+    nb = u.info["n_buckets"]
+    n = args.gemm
+    A = torch.randn(n, n, device=device, dtype=torch.bfloat16)
+    B = torch.randn(n, n, device=device, dtype=torch.bfloat16)
+    C = torch.empty(n, n, device=device, dtype=torch.bfloat16)
+    bk = [g.grs_bucket_info(u.plan, b) for b in range(nb)]
+    main = torch.cuda.current_stream(device)
+    back = torch.cuda.Stream(device)
+    side = torch.cuda.Stream(device)
+    a = w.adamw
+
+    def hp():
+        u.step_no += 1
+        return g.make_adamw(a.lr, a.beta1, a.beta2, a.eps, a.weight_decay, a.max_norm, u.step_no, w.n_micro)
+
+    def backward_only():
+        for b in reversed(range(nb)):
+            torch.matmul(A, B, out=C)
+
+    def serialized():
+        for _ in range(w.n_micro):
+            backward_only()
+        u.step()
+
+    def overlapped():
+        start = torch.cuda.Event()
+        start.record(main)
+        back.wait_event(start)
+        side.wait_event(start)
+        for j in range(w.n_micro):
+            for b in reversed(range(nb)):
+                ev = torch.cuda.Event()
+                with torch.cuda.stream(back):
+                    torch.matmul(A, B, out=C)
+                    ev.record(back)
+                d = bk[b]
+                rp = [p + 2 * d["rank_offset"] for p in u.ptrs[j]]
+                g.grs_reduce_bucket_ex(u.plan, b, rp, u.acc.data_ptr() + 4 * d["state_offset"], int(j > 0),
+                                       int(j == w.n_micro - 1), u.ws.data_ptr(), args.max_ctas,
+                                       ev.cuda_event, side.cuda_stream)
+        g.grs_grad_norm_sq(u.plan, u.acc.data_ptr(), w.n_micro, u.ws.data_ptr(), 1, u.norm.data_ptr(),
+                           side.cuda_stream)
+        g.grs_clip_adamw_step(u.plan, hp(), u.norm.data_ptr(), u.acc.data_ptr(), u.master.data_ptr(),
+                              u.m.data_ptr(), u.v.data_ptr(), u.params.data_ptr(), side.cuda_stream)
+        done = torch.cuda.Event()
+        done.record(side)
+        main.wait_event(done)
+        done2 = torch.cuda.Event()
+        done2.record(back)
+        main.wait_event(done2)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(main)
+        for _ in range(args.steps):
+            fn()
+        s1.record(main)
+        torch.cuda.synchronize()
+        return s0.elapsed_time(s1) / args.steps
+
+    t_back = timed(lambda: [backward_only() for _ in range(w.n_micro)])
+    t_ser = timed(serialized)
+    t_ovl = timed(overlapped)
+    status = g.grs_check_device_errors(u.plan, u.stream)
+    u.close()
+    return {"metric": "ms per step: simulated backward (bf16 GEMM per bucket) + reduce+clip+AdamW",
+            "unit": "ms/step", "workload": w.name, "gemm": n, "buckets": nb, "microbatches": w.n_micro,
+            "max_ctas": args.max_ctas, "backward_only": t_back, "serialized": t_ser, "overlapped": t_ovl,
+            "hidden_fraction_of_update": (t_ser - t_ovl) / max(1e-9, t_ser - t_back),
+            "device_status": status}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -506,6 +597,10 @@ def main():
     ap.add_argument("--blocks", type=int, default=0,
                     help="shrink workload 1 to this many blocks (small profiling case)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--overlap", action="store_true",
+                    help="measure the reduction overlapped with a simulated backward pass instead")
+    ap.add_argument("--gemm", type=int, default=4096)
+    ap.add_argument("--max-ctas", type=int, default=0, help="reduction grid cap in --overlap (0: all SMs)")
     ap.add_argument("--impl", default="grs", choices=["grs", "reference"])
     ap.add_argument("--soak", type=float, default=1.5, help="untimed seconds before timing")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -519,6 +614,9 @@ def main():
         if rank != 0:
             return
         print(json.dumps(run_reference(args, rank, world_size)), flush=True)
+        return
+    if args.overlap:
+        print(json.dumps(run_overlap(args)), flush=True)
         return
     if world_size > 1:
         import torch

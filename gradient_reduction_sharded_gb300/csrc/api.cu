@@ -204,7 +204,8 @@ grs_status grs_tensor_info(const grs_plan* p, int32_t i, grs_tensor_desc* o) {
 static grs_status reduce_common(const grs_plan* p, const void* const* rank_grads, float* acc,
                                 int32_t accumulate, int32_t emit, void* workspace, void* stream,
                                 int32_t unit_begin, int32_t unit_end, int64_t state_base,
-                                int64_t rank_base, int32_t tag, const char* who) {
+                                int64_t rank_base, int32_t tag, const char* who, int32_t max_ctas = 0,
+                                void* wait_event = nullptr) {
   if (rank_grads == nullptr || acc == nullptr)
     return fail(GRS_ERR_INVALID_ARG, std::string(who) + ": rank_grads/acc is NULL");
   if (emit && workspace == nullptr)
@@ -234,6 +235,12 @@ static grs_status reduce_common(const grs_plan* p, const void* const* rank_grads
   l.state_base = state_base;
   l.rank_base = rank_base;
   l.accumulate = accumulate ? 1 : 0;
+  l.max_ctas = max_ctas;
+  if (wait_event != nullptr) {
+    const cudaError_t we = cudaStreamWaitEvent(static_cast<cudaStream_t>(stream),
+                                               static_cast<cudaEvent_t>(wait_event), 0);
+    if (we != cudaSuccess) return cuda_fail(we, who);
+  }
   const int e = grs::launch_reduce(p, l, stream);
   if (e != 0) return cuda_fail(static_cast<cudaError_t>(e), who);
   return GRS_OK;
@@ -248,6 +255,20 @@ grs_status grs_reduce_bucket(const grs_plan* p, int32_t b, const void* const* ra
   const grs::Bucket& bk = p->buckets[b];
   return reduce_common(p, rank_grads, acc, accumulate, emit, workspace, stream, bk.unit0,
                        bk.unit0 + bk.copies, bk.state_off, bk.rank_off, bk.tag, "grs_reduce_bucket");
+}
+
+grs_status grs_reduce_bucket_ex(const grs_plan* p, int32_t b, const void* const* rank_grads, float* acc,
+                                int32_t accumulate, int32_t emit, void* workspace, int32_t max_ctas,
+                                void* wait_event, void* stream) {
+  grs_status st = check_plan_device(p);
+  if (st != GRS_OK) return st;
+  if (b < 0 || b >= static_cast<int32_t>(p->buckets.size()))
+    return fail(GRS_ERR_INVALID_ARG, "grs_reduce_bucket_ex: bucket index out of range");
+  if (max_ctas < 0) return fail(GRS_ERR_INVALID_ARG, "grs_reduce_bucket_ex: max_ctas must be >= 0");
+  const grs::Bucket& bk = p->buckets[b];
+  return reduce_common(p, rank_grads, acc, accumulate, emit, workspace, stream, bk.unit0,
+                       bk.unit0 + bk.copies, bk.state_off, bk.rank_off, bk.tag, "grs_reduce_bucket_ex",
+                       max_ctas, wait_event);
 }
 
 grs_status grs_reduce_all(const grs_plan* p, const void* const* rank_grads, float* acc,

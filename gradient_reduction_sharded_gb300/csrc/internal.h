@@ -163,6 +163,7 @@ struct ReduceLaunch {
   int32_t unit_begin, unit_end;
   int64_t state_base, rank_base;
   int32_t accumulate;
+  int32_t max_ctas = 0;  // cap on the persistent grid (0: one CTA per SM)
 };
 int launch_reduce(const grs_plan* p, const ReduceLaunch& a, void* stream);
 int launch_norm(const grs_plan* p, const float* acc, int32_t n_micro, void* workspace,

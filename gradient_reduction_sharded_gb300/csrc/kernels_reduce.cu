@@ -341,7 +341,9 @@ int launch_reduce(const grs_plan* p, const ReduceLaunch& l, void* stream) {
     if (e != cudaSuccess) return static_cast<int>(e);
     g_attr_set[f32][p->device] = true;
   }
-  const int64_t grid = tiles < p->sm_count ? tiles : p->sm_count;
+  int64_t cap = p->sm_count;
+  if (l.max_ctas > 0 && l.max_ctas < cap) cap = l.max_ctas;
+  const int64_t grid = tiles < cap ? tiles : cap;
   if (f32)
     reduce_kernel<float><<<static_cast<unsigned>(grid), RED_THREADS, smem, static_cast<cudaStream_t>(stream)>>>(a);
   else

@@ -96,6 +96,8 @@ _sig = {
     "grs_reduce_bucket": ([_vp, ctypes.c_int32, _P(_vp), _vp, ctypes.c_int32, ctypes.c_int32, _vp,
                            _vp], ctypes.c_int),
     "grs_reduce_all": ([_vp, _P(_vp), _vp, ctypes.c_int32, ctypes.c_int32, _vp, _vp], ctypes.c_int),
+    "grs_reduce_bucket_ex": ([_vp, ctypes.c_int32, _P(_vp), _vp, ctypes.c_int32, ctypes.c_int32, _vp,
+                              ctypes.c_int32, _vp, _vp], ctypes.c_int),
     "grs_accumulate": ([_vp, ctypes.c_int32, _vp, _vp, _vp], ctypes.c_int),
     "grs_grad_norm_sq": ([_vp, _vp, ctypes.c_int32, _vp, ctypes.c_int32, _vp, _vp], ctypes.c_int),
     "grs_clip_adamw_step": ([_vp, _P(grs_adamw), _vp, _vp, _vp, _vp, _vp, _vp, _vp], ctypes.c_int),
@@ -190,6 +192,15 @@ def grs_reduce_bucket(plan: int, bucket: int, rank_grads: Sequence[int], acc: in
                       emit_norm_partials: int, workspace: Optional[int], stream: int) -> None:
     _check(_lib.grs_reduce_bucket(plan, bucket, _ptrs(rank_grads), acc, accumulate,
                                   emit_norm_partials, workspace, stream), "grs_reduce_bucket")
+
+
+def grs_reduce_bucket_ex(plan: int, bucket: int, rank_grads: Sequence[int], acc: int, accumulate: int,
+                         emit_norm_partials: int, workspace: Optional[int], max_ctas: int,
+                         wait_event: Optional[int], stream: int) -> None:
+    """wait_event: a cudaEvent_t handle (torch.cuda.Event.cuda_event) or None."""
+    _check(_lib.grs_reduce_bucket_ex(plan, bucket, _ptrs(rank_grads), acc, accumulate,
+                                     emit_norm_partials, workspace, max_ctas, wait_event, stream),
+           "grs_reduce_bucket_ex")
 
 
 def grs_reduce_all(plan: int, rank_grads: Sequence[int], acc: int, accumulate: int,

@@ -225,6 +225,22 @@ grs_status grs_reduce_bucket(const grs_plan* plan, int32_t bucket, const void* c
                              float* acc, int32_t accumulate, int32_t emit_norm_partials,
                              void* workspace, void* stream);
 
+/* grs_reduce_bucket for overlap with the backward pass ([ISSUE] "Preserved
+ * prototype": asynchronous FP32 reduction hook; "Proposed scope": overlap
+ * during backward): buckets become ready one by one (in reverse model
+ * order during backward) and each is reduced as soon as its gradients
+ * exist, on a side stream, while the backward pass goes on.
+ *   wait_event : a cudaEvent_t recorded after the bucket's gradients were
+ *                written (on the producing stream), or NULL; `stream`
+ *                waits for it before the reduction.
+ *   max_ctas   : cap on the reduction's persistent grid (0 = one CTA per
+ *                SM), leaving the other SMs to concurrent kernels.
+ * Results (accumulator and norm partials) do not depend on the grid: they
+ * are bit-identical to grs_reduce_bucket / grs_reduce_all. */
+grs_status grs_reduce_bucket_ex(const grs_plan* plan, int32_t bucket, const void* const* rank_grads,
+                                float* acc, int32_t accumulate, int32_t emit_norm_partials,
+                                void* workspace, int32_t max_ctas, void* wait_event, void* stream);
+
 /* The same for every bucket in one launch.
  *   rank_grads : host array [world] of device pointers to each rank's
  *                whole gradient buffer ([n_rank_pad], bf16 bits or fp32).

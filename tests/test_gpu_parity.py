@@ -465,3 +465,49 @@ def test_bounded_wait_times_out_and_context_survives():
         full_check(run, oracle_update(run, master0, m0, v0, step=1), "after timeout")
     finally:
         run.close()
+
+
+def test_overlapped_reverse_order_reduction_matches_grouped():
+    """Buckets produced in reverse order on a 'backward' stream, each reduced
+    on a side stream as soon as its event fires, with a capped grid: the
+    accumulator and the norm equal the grouped launch's bit for bit."""
+    g = grs()
+    c = SMALL["multi-tile-world16-M2"]
+    ref = Run(c)
+    run = Run(c)
+    try:
+        ref.update()
+        torch.cuda.synchronize()
+        src = [[t.clone() for t in mb] for mb in run.grads]
+        for mb in run.grads:
+            for t in mb:
+                t.fill_(float("nan"))  # gradients do not exist yet
+        torch.cuda.synchronize()
+        producer = torch.cuda.Stream()
+        side = torch.cuda.Stream()
+        nb = run.info["n_buckets"]
+        for j in range(c.n_micro):
+            for b in reversed(range(nb)):
+                d = g.grs_bucket_info(run.plan, b)
+                lo, hi = d["rank_offset"], d["rank_offset"] + d["padded"]
+                ev = torch.cuda.Event()
+                with torch.cuda.stream(producer):
+                    for k in range(c.world):
+                        run.grads[j][k][lo:hi].copy_(src[j][k][lo:hi])
+                    ev.record(producer)
+                rp = [t.data_ptr() + 2 * d["rank_offset"] for t in run.grads[j]]
+                g.grs_reduce_bucket_ex(run.plan, b, rp, run.acc.data_ptr() + 4 * d["state_offset"], int(j > 0),
+                                       int(j == c.n_micro - 1), run.ws.data_ptr(), 16, ev.cuda_event,
+                                       side.cuda_stream)
+        with torch.cuda.stream(side):
+            g.grs_grad_norm_sq(run.plan, run.acc.data_ptr(), c.n_micro, run.ws.data_ptr(), 1,
+                               run.norm.data_ptr(), side.cuda_stream)
+            hp = g.make_adamw(c.hp[0], c.hp[1], c.hp[2], c.hp[3], c.hp[4], c.max_norm, 1, c.n_micro)
+            g.grs_clip_adamw_step(run.plan, hp, run.norm.data_ptr(), run.acc.data_ptr(), run.master.data_ptr(),
+                                  run.m.data_ptr(), run.v.data_ptr(), run.params.data_ptr(), side.cuda_stream)
+        torch.cuda.synchronize()
+        for x, y in ((ref.acc, run.acc), (ref.norm, run.norm), (ref.master, run.master), (ref.params, run.params)):
+            assert torch.equal(x, y)
+    finally:
+        ref.close()
+        run.close()
