@@ -8,6 +8,14 @@
 
 namespace grs {
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while its predecessor on the stream is still
+// running; pdl_wait() blocks until the predecessor has completed and its
+// writes are visible (a no-op for an ordinary launch), pdl_trigger() lets
+// this kernel's own successor start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // A device wait gives up after this long and raises FLAG_TIMEOUT.
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 

@@ -31,6 +31,7 @@
 
 #include "device.cuh"
 #include "internal.h"
+#include "launch.cuh"
 
 namespace grs {
 
@@ -149,6 +150,8 @@ __global__ void __launch_bounds__(RED_THREADS, 1) reduce_kernel(const __grid_con
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  pdl_wait();     // the previous kernel on the stream may still read acc
+  pdl_trigger();  // the norm finish / update may start launching
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
@@ -344,11 +347,9 @@ int launch_reduce(const grs_plan* p, const ReduceLaunch& l, void* stream) {
   int64_t cap = p->sm_count;
   if (l.max_ctas > 0 && l.max_ctas < cap) cap = l.max_ctas;
   const int64_t grid = tiles < cap ? tiles : cap;
-  if (f32)
-    reduce_kernel<float><<<static_cast<unsigned>(grid), RED_THREADS, smem, static_cast<cudaStream_t>(stream)>>>(a);
-  else
-    reduce_kernel<uint16_t><<<static_cast<unsigned>(grid), RED_THREADS, smem, static_cast<cudaStream_t>(stream)>>>(a);
-  return static_cast<int>(cudaGetLastError());
+  const cudaError_t e = f32 ? launch_k(reduce_kernel<float>, dim3(unsigned(grid)), dim3(RED_THREADS), smem, stream, a)
+                            : launch_k(reduce_kernel<uint16_t>, dim3(unsigned(grid)), dim3(RED_THREADS), smem, stream, a);
+  return static_cast<int>(e);
 }
 
 }  // namespace grs

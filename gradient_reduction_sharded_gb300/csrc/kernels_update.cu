@@ -19,6 +19,7 @@
 
 #include "device.cuh"
 #include "internal.h"
+#include "launch.cuh"
 
 namespace grs {
 
@@ -42,6 +43,8 @@ __global__ void __launch_bounds__(NORM1_THREADS) norm_pass1_kernel(const float* 
   __shared__ float wp[NORM1_THREADS / 32];
   const int lane = threadIdx.x & 31;
   const int w = threadIdx.x >> 5;
+  pdl_wait();
+  pdl_trigger();
   for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
     const int u = find_unit(prefix, 0, n_units, tile);
     const UnitDesc* ud = units + u;
@@ -100,6 +103,8 @@ __global__ void __launch_bounds__(NORM2_THREADS) norm_finish_kernel(const float*
                                                                     int* __restrict__ flags) {
   __shared__ double red[NORM2_THREADS / 32];
   __shared__ bool last;
+  pdl_wait();  // the partials come from the previous kernel
+  pdl_trigger();
   const int64_t chunk = (n + NORM_L2_BLOCKS - 1) / NORM_L2_BLOCKS;
   const int64_t lo = blockIdx.x * chunk;
   const int64_t hi = lo + chunk < n ? lo + chunk : n;
@@ -153,6 +158,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 __global__ void __launch_bounds__(UPD_THREADS) update_kernel(const __grid_constant__ UpdateArgs a) {
+  // Tiles run in reverse order: the reduction wrote its last tiles last, so
+  // their accumulator values are the ones still in L2.
+  const unsigned tile = GRS_UPD_REVERSE ? gridDim.x - 1u - blockIdx.x : blockIdx.x;
+  pdl_wait();  // S and acc come from the kernels before
+  pdl_trigger();
   // Clip coefficient c = min(1, max_norm / (sqrt(S) + 1e-6)), NaN kept,
   // evaluated by every thread in fp32 from the device-resident S.
   float gscale = a.inv_m;
@@ -160,9 +170,9 @@ __global__ void __launch_bounds__(UPD_THREADS) update_kernel(const __grid_consta
     const float cr = a.max_norm / (sqrtf(static_cast<float>(*a.norm_sq)) + 1e-6f);
     gscale = __fmul_rn((cr < 1.0f || isnan(cr)) ? cr : 1.0f, a.inv_m);
   }
-  const int u = find_unit(a.prefix, 0, a.n_units, blockIdx.x);
+  const int u = find_unit(a.prefix, 0, a.n_units, tile);
   const UnitDesc* ud = a.units + u;
-  const int64_t e0 = (static_cast<int64_t>(blockIdx.x) - ud->upd_tile0) * UPD_T;
+  const int64_t e0 = (static_cast<int64_t>(tile) - ud->upd_tile0) * UPD_T;
   const int64_t el = e0 + int64_t(threadIdx.x) * 8;  // element within the unit
   if (el >= ud->padded) return;
   const int64_t i = ud->state_off + el;
@@ -243,10 +253,10 @@ int launch_norm(const grs_plan* p, const float* acc, int32_t n_micro, void* work
   if (!partials_ready && p->n_red_tiles > 0) {
     const int64_t grid = p->n_red_tiles < int64_t(p->sm_count) * 16 ? p->n_red_tiles
                                                                     : int64_t(p->sm_count) * 16;
-    norm_pass1_kernel<<<static_cast<unsigned>(grid), NORM1_THREADS, 0, s>>>(
-        acc, p->d_units, p->d_red_prefix, static_cast<int32_t>(p->units.size()), p->n_red_tiles,
-        partials);
-    const int e = static_cast<int>(cudaGetLastError());
+    const int e = static_cast<int>(launch_k(norm_pass1_kernel, dim3(unsigned(grid)), dim3(NORM1_THREADS), 0, s,
+                                            acc, static_cast<const UnitDesc*>(p->d_units),
+                                            static_cast<const int64_t*>(p->d_red_prefix),
+                                            static_cast<int32_t>(p->units.size()), p->n_red_tiles, partials));
     if (e != 0) return e;
   }
   return launch_norm_finish(p, n_micro, workspace, d_norm_sq, stream);
@@ -259,9 +269,9 @@ int launch_norm_finish(const grs_plan* p, int32_t n_micro, void* workspace, doub
   double* level2 = reinterpret_cast<double*>(ws + ws_level2_offset(p->n_red_tiles));
   unsigned int* ticket = reinterpret_cast<unsigned int*>(ws + ws_ticket_offset(p->n_red_tiles));
   const double inv_m = 1.0 / static_cast<double>(n_micro);
-  norm_finish_kernel<<<NORM_L2_BLOCKS, NORM2_THREADS, 0, static_cast<cudaStream_t>(stream)>>>(
-      partials, p->n_red_tiles, level2, ticket, inv_m * inv_m, d_norm_sq, p->d_flags);
-  return static_cast<int>(cudaGetLastError());
+  return static_cast<int>(launch_k(norm_finish_kernel, dim3(NORM_L2_BLOCKS), dim3(NORM2_THREADS), 0, stream,
+                                   static_cast<const float*>(partials), p->n_red_tiles, level2, ticket,
+                                   inv_m * inv_m, d_norm_sq, p->d_flags));
 }
 
 int launch_update(const grs_plan* p, const grs_adamw* hp, const double* d_norm_sq, const float* acc,
@@ -290,9 +300,7 @@ int launch_update(const grs_plan* p, const grs_adamw* hp, const double* d_norm_s
   a.inv_bc2_sqrt = static_cast<float>(1.0 / std::sqrt(bc2));
   a.max_norm = hp->max_norm > 0.0f ? hp->max_norm : 0.0f;
   a.inv_m = static_cast<float>(1.0 / static_cast<double>(hp->n_micro));
-  update_kernel<<<static_cast<unsigned>(p->n_upd_tiles), UPD_THREADS, 0,
-                  static_cast<cudaStream_t>(stream)>>>(a);
-  return static_cast<int>(cudaGetLastError());
+  return static_cast<int>(launch_k(update_kernel, dim3(unsigned(p->n_upd_tiles)), dim3(UPD_THREADS), 0, stream, a));
 }
 
 int launch_accumulate(const grs_plan* p, int32_t bucket, float* acc, const float* mb, void* stream) {
