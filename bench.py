@@ -266,6 +266,9 @@ def run_gpu(args, rank, world_size, local_rank):
     upd_ms = [e[2].elapsed_time(e[3]) for e in ev]
     clk = clocks.stop()
 
+    # ---------------------------------------------------------------- gather
+    gather = run_gather(u, args, torch)
+
     # ---------------------------------------------------------------- e2e
     e2e = None if args.no_e2e else run_e2e(u, args, torch)
 
@@ -307,6 +310,7 @@ def run_gpu(args, rank, world_size, local_rank):
                      "algorithmic_bytes_per_launch": dk["bytes"]},
         "kernels": {k: {kk: vv for kk, vv in v.items()} for k, v in kern.items()},
         "e2e": e2e,
+        "gather": gather,
         "gpu_launches": u.launches_per_step * K,
         "kernel_timing": "second region of K steps with CUDA events between the kernels",
         "clocks": clk,
@@ -315,6 +319,29 @@ def run_gpu(args, rank, world_size, local_rank):
     if rank == 0 and world_size == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w, op, mb, args)
     return result
+
+
+def run_gather(u: GpuUpdate, args, torch):
+    """grs_gather_params to per-tensor bf16 storage, timed on its own (not part
+    of the update: parameters can also be used as views of the bucket-ordered
+    buffer).  Algorithmic bytes: read + write 2 bytes per parameter."""
+    w = u.w
+    outs = [torch.empty(n, dtype=torch.int16, device=u.dev) for n in w.numels]
+    ptrs = [t.data_ptr() for t in outs]
+    for _ in range(3):
+        u.grs.grs_gather_params(u.plan, u.params.data_ptr(), ptrs, u.stream)
+    torch.cuda.synchronize()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(args.steps):
+        u.grs.grs_gather_params(u.plan, u.params.data_ptr(), ptrs, u.stream)
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / args.steps
+    nbytes = 4 * w.n_unique
+    del outs
+    return {"ms": ms, "bytes": nbytes, "gbs": nbytes / (ms * 1e-3) / 1e9}
 
 
 def run_e2e(u: GpuUpdate, args, torch):

@@ -414,6 +414,20 @@ grs_status grs_state_from_logical(const grs_plan* p, const float* logical, float
   return state_logical_common(p, logical, state, false, stream, "grs_state_from_logical");
 }
 
+grs_status grs_check_already_reduced(const grs_plan* p, const void* const* rank_grads, void* stream) {
+  grs_status st = check_plan_device(p);
+  if (st != GRS_OK) return st;
+  if (rank_grads == nullptr) return fail(GRS_ERR_INVALID_ARG, "grs_check_already_reduced: NULL argument");
+  for (int32_t k = 0; k < p->world; ++k)
+    if (rank_grads[k] == nullptr)
+      return fail(GRS_ERR_INVALID_ARG, "grs_check_already_reduced: rank " + std::to_string(k) + " buffer is NULL");
+  DeviceGuard g(p->device);
+  if (!g.ok()) return fail(GRS_ERR_CUDA, "grs_check_already_reduced: cannot select the plan's device");
+  const int e = grs::launch_check_already_reduced(p, rank_grads, stream);
+  if (e != 0) return cuda_fail(static_cast<cudaError_t>(e), "grs_check_already_reduced");
+  return GRS_OK;
+}
+
 grs_status grs_selftest_bounded_wait(const grs_plan* p, int64_t limit_ns, void* stream) {
   grs_status st = check_plan_device(p);
   if (st != GRS_OK) return st;
@@ -440,6 +454,9 @@ grs_status grs_check_device_errors(const grs_plan* p, void* stream) {
   if (e != cudaSuccess) return cuda_fail(e, "grs_check_device_errors: clear flags");
   if (h[grs::FLAG_TIMEOUT]) return fail(GRS_ERR_TIMEOUT, "a bounded device wait timed out");
   if (h[grs::FLAG_NONFINITE]) return fail(GRS_ERR_NONFINITE, "global gradient norm is not finite");
+  if (h[grs::FLAG_AR_MISMATCH])
+    return fail(GRS_ERR_INVALID_ARG,
+                "an ALREADY_REDUCED gradient differs across ranks: it was not reduced by its owner");
   return GRS_OK;
 }
 

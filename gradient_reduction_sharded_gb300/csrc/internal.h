@@ -143,7 +143,7 @@ inline int64_t ws_bytes(int64_t n_red_tiles) { return ws_ticket_offset(n_red_til
 inline int64_t ws_factors_offset(int64_t n_red_tiles) { return ws_bytes(n_red_tiles); }
 
 // Device flags
-enum : int { FLAG_TIMEOUT = 0, FLAG_NONFINITE = 1, FLAG_COUNT = 4 };
+enum : int { FLAG_TIMEOUT = 0, FLAG_NONFINITE = 1, FLAG_AR_MISMATCH = 2, FLAG_COUNT = 4 };
 
 // Programmatic dependent launch between the path's kernels: measured on
 // GB300 (67M workload, back-to-back steps) at 0.6248 ms/step against 0.6214
@@ -184,6 +184,7 @@ int launch_accumulate(const grs_plan* p, int32_t bucket, float* acc, const float
 int launch_gather(const grs_plan* p, const uint16_t* params, uint16_t* const* tensor_ptrs,
                   void* stream);
 int launch_bounded_wait_selftest(const grs_plan* p, uint64_t limit_ns, void* stream);
+int launch_check_already_reduced(const grs_plan* p, const void* const* ranks, void* stream);
 // fp32 state arrays: bucket layout <-> canonical logical order.
 int launch_state_to_logical(const grs_plan* p, const float* state, float* logical, void* stream);
 int launch_state_from_logical(const grs_plan* p, const float* logical, float* state, void* stream);

@@ -121,7 +121,51 @@ __global__ void bounded_wait_selftest_kernel(int* flags, uint64_t limit_ns) {
   mbar_wait_bounded(&bar, 0, flags, &abort_flag, limit_ns);
 }
 
+// ALREADY_REDUCED check: every rank's copy of an already-reduced bucket
+// must equal rank 0's bit for bit (it was reduced by its owner before it
+// reached us, so all ranks hold the same values).  16-byte words compared;
+// padding included (callers may leave it unset, so only [0, used) counts).
+struct ArCheckArgs {
+  const void* ranks[GRS_MAX_WORLD];
+  const UnitDesc* unit;  // the ALREADY_REDUCED bucket's (single) row
+  int32_t world;
+  int32_t esize;
+  int* flags;
+};
+
+__global__ void __launch_bounds__(256) check_already_reduced_kernel(const __grid_constant__ ArCheckArgs a) {
+  const UnitDesc* ud = a.unit;
+  const int64_t el = static_cast<int64_t>(blockIdx.x) * UPD_T + int64_t(threadIdx.x) * 8;
+  if (el >= ud->used) return;
+  const int64_t n = ud->used - el < 8 ? ud->used - el : 8;
+  const int64_t base = (ud->rank_off + el) * a.esize;
+  const uint8_t* r0 = static_cast<const uint8_t*>(a.ranks[0]) + base;
+  bool same = true;
+  for (int k = 1; k < a.world && same; ++k) {
+    const uint8_t* rk = static_cast<const uint8_t*>(a.ranks[k]) + base;
+    for (int64_t i = 0; i < n * a.esize; ++i) same = same && (r0[i] == rk[i]);
+  }
+  if (!same) atomicOr(a.flags + FLAG_AR_MISMATCH, 1);
+}
+
 }  // namespace
+
+int launch_check_already_reduced(const grs_plan* p, const void* const* ranks, void* stream) {
+  ArCheckArgs a;
+  for (int k = 0; k < GRS_MAX_WORLD; ++k) a.ranks[k] = k < p->world ? ranks[k] : nullptr;
+  a.world = p->world;
+  a.esize = p->grad_esize;
+  a.flags = p->d_flags;
+  for (const Bucket& bk : p->buckets) {
+    if (bk.tag != GRS_ALREADY_REDUCED || bk.used == 0) continue;
+    a.unit = p->d_units + bk.unit0;
+    const int64_t tiles = (bk.used + UPD_T - 1) / UPD_T;
+    check_already_reduced_kernel<<<static_cast<unsigned>(tiles), 256, 0, static_cast<cudaStream_t>(stream)>>>(a);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return static_cast<int>(e);
+  }
+  return 0;
+}
 
 int launch_bounded_wait_selftest(const grs_plan* p, uint64_t limit_ns, void* stream) {
   bounded_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(p->d_flags, limit_ns);

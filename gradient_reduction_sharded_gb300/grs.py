@@ -107,6 +107,7 @@ _sig = {
                                     _vp], ctypes.c_int),
     "grs_check_device_errors": ([_vp, _vp], ctypes.c_int),
     "grs_selftest_bounded_wait": ([_vp, ctypes.c_int64, _vp], ctypes.c_int),
+    "grs_check_already_reduced": ([_vp, _P(_vp), _vp], ctypes.c_int),
     "grs_state_to_logical": ([_vp, _vp, _vp, _vp], ctypes.c_int),
     "grs_state_from_logical": ([_vp, _vp, _vp, _vp], ctypes.c_int),
     "grs_grad_norm_sq_noalloc": ([_vp, _vp, ctypes.c_int32, _vp, _vp], ctypes.c_int),
@@ -271,6 +272,10 @@ def grs_state_to_logical(plan: int, state: int, logical: int, stream: int) -> No
 
 def grs_state_from_logical(plan: int, logical: int, state: int, stream: int) -> None:
     _check(_lib.grs_state_from_logical(plan, logical, state, stream), "grs_state_from_logical")
+
+
+def grs_check_already_reduced(plan: int, rank_grads: Sequence[int], stream: int) -> None:
+    _check(_lib.grs_check_already_reduced(plan, _ptrs(rank_grads), stream), "grs_check_already_reduced")
 
 
 def grs_selftest_bounded_wait(plan: int, limit_ns: int, stream: int) -> None:

@@ -393,6 +393,15 @@ grs_status grs_step_from_host(const grs_plan* plan, const grs_adamw* hp,
 grs_status grs_grad_norm_sq_noalloc(const grs_plan* plan, const float* acc, int32_t n_micro,
                                     double* d_norm_sq, void* stream);
 
+/* Validation of ALREADY_REDUCED buckets ([ISSUE] "Why this needs separate
+ * work": an existing reduction must not be applied again, so the data it
+ * produced must already agree everywhere): compares every rank's copy of
+ * every ALREADY_REDUCED bucket with rank 0's, bit for bit, over the valid
+ * elements.  rank_grads as for grs_reduce_all (whole per-rank buffers).  A
+ * mismatch raises a device flag that the next grs_check_device_errors
+ * reports as GRS_ERR_INVALID_ARG. */
+grs_status grs_check_already_reduced(const grs_plan* plan, const void* const* rank_grads, void* stream);
+
 /* Failure-detection self-test: one kernel waits on an mbarrier that nothing
  * completes, through the same bounded wait the reduction uses, gives up
  * after limit_ns (1 us .. 2 s) and raises the plan's timeout flag; a
@@ -418,7 +427,8 @@ grs_status grs_state_from_logical(const grs_plan* plan, const float* logical, fl
 
 /* Synchronise `stream`, read and clear the plan's device flags.  Returns
  * TIMEOUT if a bounded device wait gave up, NONFINITE if a global norm was
- * NaN/Inf since the last check, else OK (or CUDA). */
+ * NaN/Inf since the last check, INVALID_ARG if grs_check_already_reduced
+ * found copies that differ, else OK (or CUDA). */
 grs_status grs_check_device_errors(const grs_plan* plan, void* stream);
 
 /* Message of the last failing call on this thread ("" if none). */

@@ -511,3 +511,27 @@ def test_overlapped_reverse_order_reduction_matches_grouped():
     finally:
         ref.close()
         run.close()
+
+
+def test_check_already_reduced_flags_disagreeing_copies():
+    g = grs()
+    c = Case([4096, 999, 777, 64 * 2], [RA, AR, AR, LS], 4, 2, 1, 2, 1 << 20, 1, 1e-2, 61)
+    run = Run(c)
+    try:
+        s = run.stream()
+        for b in range(run.op.n_buckets):  # make every AR copy equal rank 0's
+            if int(run.op.b_tag[b]) == AR:
+                ro, used = int(run.op.b_rank_off[b]), int(run.op.b_used[b])
+                for k in range(1, c.world):
+                    run.grads[0][k][ro:ro + used] = run.grads[0][0][ro:ro + used]
+        g.grs_check_already_reduced(run.plan, run.ptrs(0), s)
+        assert run.check_flags() == 0
+        ar = [b for b in range(run.op.n_buckets) if int(run.op.b_tag[b]) == AR][0]
+        e = int(run.op.b_rank_off[ar]) + int(run.op.b_used[ar]) - 1  # last valid element
+        run.grads[0][3][e] = run.grads[0][3][e] + 1.0
+        g.grs_check_already_reduced(run.plan, run.ptrs(0), s)
+        assert run.check_flags() == g.GRS_ERR_INVALID_ARG
+        assert "ALREADY_REDUCED" in g.grs_last_error()
+        assert run.check_flags() == 0
+    finally:
+        run.close()
