@@ -48,51 +48,56 @@ _f64p = np.ctypeslib.ndpointer(dtype=np.float64, flags="C_CONTIGUOUS")
 _u16p = np.ctypeslib.ndpointer(dtype=np.uint16, flags="C_CONTIGUOUS")
 
 
+def load_library(path: str):
+    """ctypes handle of an oracle shared library with every signature set."""
+    L = ctypes.CDLL(path)
+    L.oracle_resolve_dims.argtypes = [ctypes.c_int32] * 4 + [_i32p]
+    L.oracle_resolve_dims.restype = ctypes.c_int
+    L.oracle_plan.argtypes = [_i64p, _i32p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                              ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32,
+                              _i32p, _i32p, _i64p, _i32p, _i64p, _i64p, _i64p, _i64p]
+    L.oracle_plan.restype = ctypes.c_int
+    L.oracle_plan_ex.argtypes = [_i64p, _i32p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                 ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
+                                 ctypes.c_int32, _i32p, _i32p, _i64p, _i32p, _i64p, _i64p,
+                                 _i64p, _i64p]
+    L.oracle_plan_ex.restype = ctypes.c_int
+    L.oracle_rank.argtypes = [ctypes.c_int32] * 5
+    L.oracle_rank.restype = ctypes.c_int32
+    L.oracle_reduce_bucket.argtypes = [ctypes.c_int32] * 4 + [ctypes.c_int64, ctypes.c_int64,
+                                                              ctypes.c_int32, _u16p, _f64p]
+    L.oracle_reduce_bucket.restype = ctypes.c_int
+    L.oracle_reduce_bucket_f32.argtypes = [ctypes.c_int32] * 4 + [ctypes.c_int64, ctypes.c_int64,
+                                                                  ctypes.c_int32, _f32p, _f64p]
+    L.oracle_reduce_bucket_f32.restype = ctypes.c_int
+    L.oracle_norm_sq.argtypes = [_f64p, ctypes.c_int64, ctypes.c_int32]
+    L.oracle_norm_sq.restype = ctypes.c_double
+    L.oracle_clip_coef.argtypes = [ctypes.c_double, ctypes.c_double]
+    L.oracle_clip_coef.restype = ctypes.c_double
+    L.oracle_adamw.argtypes = [ctypes.c_int64, ctypes.c_int64, _f64p, ctypes.c_int32,
+                               ctypes.c_double, _f64p, ctypes.c_int32,
+                               _f32p, _f32p, _f32p, _f32p, _f32p, _f32p, _u16p]
+    L.oracle_adamw.restype = None
+    L.oracle_bf16_rne.argtypes = [ctypes.c_float]
+    L.oracle_bf16_rne.restype = ctypes.c_uint16
+    L.oracle_gather_tensor.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                       ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                       _u16p, _u16p]
+    L.oracle_gather_tensor.restype = None
+    for nm in ("oracle_gather_tensor_f32", "oracle_scatter_tensor_f32"):
+        f = getattr(L, nm)
+        f.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
+                      ctypes.c_int64, ctypes.c_int64, _f32p, _f32p]
+        f.restype = None
+    return L
+
+
 def lib():
     global _lib
     with _lock:
         if _lib is None:
             build()
-            L = ctypes.CDLL(_LIB_PATH)
-            L.oracle_resolve_dims.argtypes = [ctypes.c_int32] * 4 + [_i32p]
-            L.oracle_resolve_dims.restype = ctypes.c_int
-            L.oracle_plan.argtypes = [_i64p, _i32p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
-                                      ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32,
-                                      _i32p, _i32p, _i64p, _i32p, _i64p, _i64p, _i64p, _i64p]
-            L.oracle_plan.restype = ctypes.c_int
-            L.oracle_plan_ex.argtypes = [_i64p, _i32p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
-                                         ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
-                                         ctypes.c_int32, _i32p, _i32p, _i64p, _i32p, _i64p, _i64p,
-                                         _i64p, _i64p]
-            L.oracle_plan_ex.restype = ctypes.c_int
-            L.oracle_rank.argtypes = [ctypes.c_int32] * 5
-            L.oracle_rank.restype = ctypes.c_int32
-            L.oracle_reduce_bucket.argtypes = [ctypes.c_int32] * 4 + [ctypes.c_int64, ctypes.c_int64,
-                                                                      ctypes.c_int32, _u16p, _f64p]
-            L.oracle_reduce_bucket.restype = ctypes.c_int
-            L.oracle_reduce_bucket_f32.argtypes = [ctypes.c_int32] * 4 + [ctypes.c_int64, ctypes.c_int64,
-                                                                          ctypes.c_int32, _f32p, _f64p]
-            L.oracle_reduce_bucket_f32.restype = ctypes.c_int
-            L.oracle_norm_sq.argtypes = [_f64p, ctypes.c_int64, ctypes.c_int32]
-            L.oracle_norm_sq.restype = ctypes.c_double
-            L.oracle_clip_coef.argtypes = [ctypes.c_double, ctypes.c_double]
-            L.oracle_clip_coef.restype = ctypes.c_double
-            L.oracle_adamw.argtypes = [ctypes.c_int64, ctypes.c_int64, _f64p, ctypes.c_int32,
-                                       ctypes.c_double, _f64p, ctypes.c_int32,
-                                       _f32p, _f32p, _f32p, _f32p, _f32p, _f32p, _u16p]
-            L.oracle_adamw.restype = None
-            L.oracle_bf16_rne.argtypes = [ctypes.c_float]
-            L.oracle_bf16_rne.restype = ctypes.c_uint16
-            L.oracle_gather_tensor.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
-                                               ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
-                                               _u16p, _u16p]
-            L.oracle_gather_tensor.restype = None
-            for nm in ("oracle_gather_tensor_f32", "oracle_scatter_tensor_f32"):
-                f = getattr(L, nm)
-                f.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
-                              ctypes.c_int64, ctypes.c_int64, _f32p, _f32p]
-                f.restype = None
-            _lib = L
+            _lib = load_library(_LIB_PATH)
     return _lib
 
 

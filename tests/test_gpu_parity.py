@@ -70,6 +70,14 @@ def small_cases():
     cases["fp32-grads-world8-M3"] = Case(
         [70001, 1000, 40000 * 2, 77, 9999], [RA, PS, LS, AR, RA], 8, 2, 2, 2, 1 << 17, 3, 1e-3, 18,
         fp32_grads=True)
+    # maximum world (128 ranks: 1 KB-per-rank tiles) and 64 ranks with tp 4
+    cases["world128-max"] = Case([30001, 512, 4096 * 2, 100], [RA, PS, LS, AR], 128, 2, 8, 8, 1 << 16, 1,
+                                 1e-3, 22)
+    cases["world64-tp4-M2"] = Case([20000, 300, 4096 * 4, 9], [RA, PS, LS, AR], 64, 4, 4, 4, 1 << 15, 2,
+                                   1e-3, 23)
+    # degenerate: zero-size tensors, a bucket holding only zero-size tensors (no tiles)
+    cases["zero-size-tensors"] = Case([0, 1000, 0, 64, 0], [RA, RA, PS, AR, LS], 2, 1, 1, 2, 1 << 20, 1,
+                                      1e-2, 24)
     cases["fp32-grads-world16"] = Case(
         [100003, 1024, 65536 * 2, 4099], [RA, PS, LS, AR], 16, 2, 2, 4, 1 << 18, 1, 1e-3, 19,
         fp32_grads=True)

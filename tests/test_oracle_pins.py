@@ -455,3 +455,20 @@ def test_masked_update_matches_torch_grad_none_semantics(orc):
 
 def oracle_frozen():
     return 1
+
+
+def test_logical_layout_hand_derived(orc):
+    """The odd-size tiny plan (golden 'odd-sizes-ds2'): state = its own index.
+    Logical order: tensor 0 (RA, 21) = state[0:21]; tensor 1 (PS, 5) =
+    state[32:37]; tensor 2 (LS, 18: 9 per tp row) = rows t=0 state[48:57]
+    then t=1 state[64:73]; tensor 3 (AR, 3) = state[80:83]."""
+    p = oracle.plan([21, 5, 18, 3], [0, 1, 2, 3], 4, 2, 1, 2, 26214400)
+    st = np.arange(p.n_state_pad, dtype=np.float32)
+    want = np.concatenate([np.arange(0, 21), np.arange(32, 37), np.arange(48, 57), np.arange(64, 73),
+                           np.arange(80, 83)]).astype(np.float32)
+    lg = oracle.to_logical(p, st)
+    assert np.array_equal(lg, want)
+    back = oracle.from_logical(p, lg)
+    keep = np.zeros(p.n_state_pad, bool)
+    keep[want.astype(int)] = True
+    assert np.array_equal(back[keep], st[keep]) and np.all(back[~keep] == 0)
