@@ -1,0 +1,141 @@
+"""Robustness of the CUDA path: no writes outside the output buffers (guard
+canaries), results independent of the reduction's grid size, and two host
+threads driving separate plans on separate streams at once."""
+import threading
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_support import Case, Run, grs
+
+pytestmark = pytest.mark.gpu
+
+RA, PS, LS, AR = 0, 1, 2, 3
+GUARD = 4096  # elements of canary on each side
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    torch.cuda.init()
+
+
+def guarded(n, dtype, fill):
+    """A buffer of n elements with GUARD canary elements on both sides."""
+    full = torch.full((n + 2 * GUARD,), fill, dtype=dtype, device="cuda")
+    return full, full[GUARD:GUARD + n]
+
+
+def canaries_intact(full, fill):
+    lo, hi = full[:GUARD], full[-GUARD:]
+    if full.dtype.is_floating_point and np.isnan(fill):
+        return bool(torch.isnan(lo).all() and torch.isnan(hi).all())
+    return bool((lo == fill).all() and (hi == fill).all())
+
+
+def test_no_writes_outside_outputs():
+    g = grs()
+    c = Case([100003, 1024, 65536 * 2, 4099, 333, 70001, 8000], [RA, PS, LS, AR, PS, RA, LS], 16, 2, 2, 4,
+             1 << 18, 2, 1e-3, 71)
+    run = Run(c)
+    try:
+        nsp, s = run.nsp, run.stream()
+        bufs = {}
+        for name, dt, fill in (("acc", torch.float32, float("nan")), ("master", torch.float32, float("nan")),
+                               ("m", torch.float32, float("nan")), ("v", torch.float32, float("nan")),
+                               ("params", torch.int16, -12345)):
+            full, view = guarded(nsp, dt, fill)
+            src = getattr(run, name)[:nsp]
+            view.copy_(src)
+            bufs[name] = (full, view, fill)
+        ws_full, ws = guarded(run.ws.numel(), torch.float32, float("nan"))
+        ws.zero_()
+        nrm_full, nrm = guarded(1, torch.float64, float("nan"))
+        for j in range(c.n_micro):
+            g.grs_reduce_all(run.plan, run.ptrs(j), bufs["acc"][1].data_ptr(), int(j > 0), int(j == c.n_micro - 1),
+                             ws.data_ptr(), s)
+        g.grs_grad_norm_sq(run.plan, bufs["acc"][1].data_ptr(), c.n_micro, ws.data_ptr(), 1, nrm.data_ptr(), s)
+        hp = g.make_adamw(*c.hp, c.max_norm, 1, c.n_micro)
+        g.grs_clip_adamw_step(run.plan, hp, nrm.data_ptr(), bufs["acc"][1].data_ptr(), bufs["master"][1].data_ptr(),
+                              bufs["m"][1].data_ptr(), bufs["v"][1].data_ptr(), bufs["params"][1].data_ptr(), s)
+        g.grs_grad_norm_sq(run.plan, bufs["acc"][1].data_ptr(), c.n_micro, ws.data_ptr(), 0, nrm.data_ptr(), s)
+        outs = [guarded(n, torch.int16, 777) for n in c.numels]
+        g.grs_gather_params(run.plan, bufs["params"][1].data_ptr(), [v.data_ptr() for _, v in outs], s)
+        torch.cuda.synchronize()
+        assert run.check_flags() == 0
+        for name, (full, view, fill) in bufs.items():
+            assert canaries_intact(full, fill), name
+        assert canaries_intact(ws_full, float("nan"))
+        assert canaries_intact(nrm_full, float("nan"))
+        for full, _ in outs:
+            assert canaries_intact(full, 777)
+        assert torch.isfinite(bufs["master"][1]).all()
+    finally:
+        run.close()
+
+
+def test_results_do_not_depend_on_the_grid():
+    g = grs()
+    c = Case([100003, 1024, 65536 * 2, 4099, 333], [RA, PS, LS, AR, PS], 16, 2, 2, 4, 1 << 18, 1, 1e-3, 72)
+    run = Run(c)
+    try:
+        s = run.stream()
+        ref_acc = ref_part = None
+        for cap in (0, 1, 7, 152, 1000):
+            run.acc.fill_(7.0)
+            run.ws.zero_()
+            for b in range(run.info["n_buckets"]):
+                d = g.grs_bucket_info(run.plan, b)
+                rp = [p + 2 * d["rank_offset"] for p in run.ptrs(0)]
+                g.grs_reduce_bucket_ex(run.plan, b, rp, run.acc.data_ptr() + 4 * d["state_offset"], 0, 1,
+                                       run.ws.data_ptr(), cap, None, s)
+            torch.cuda.synchronize()
+            part = run.ws[:run.info["n_reduce_tiles"]].clone()
+            if ref_acc is None:
+                ref_acc, ref_part = run.acc.clone(), part
+            assert torch.equal(run.acc, ref_acc), cap
+            assert torch.equal(part, ref_part), cap
+    finally:
+        run.close()
+
+
+def test_two_threads_two_plans_two_streams():
+    cases = [Case([50001, 512, 8192 * 2, 77], [RA, PS, LS, AR], 8, 2, 2, 2, 1 << 16, 2, 1e-3, 73 + i)
+             for i in range(2)]
+    refs = []
+    for c in cases:  # sequential reference
+        r = Run(c)
+        r.update()
+        torch.cuda.synchronize()
+        refs.append([t.clone() for t in (r.acc, r.norm, r.master, r.m, r.v, r.params)])
+        r.close()
+    runs = [Run(c) for c in cases]
+    torch.cuda.synchronize()  # buffers initialised before the threads' streams use them
+    errors = []
+
+    def work(run):
+        try:
+            st = torch.cuda.Stream()
+            with torch.cuda.stream(st):
+                for _ in range(1):
+                    run.update()
+                st.synchronize()
+        except Exception as e:  # surfaced below
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(r,)) for r in runs]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    torch.cuda.synchronize()
+    try:
+        assert not errors, errors
+        for r, ref in zip(runs, refs):
+            for x, y in zip((r.acc, r.norm, r.master, r.m, r.v, r.params), ref):
+                assert torch.equal(x, y)
+    finally:
+        for r in runs:
+            r.close()
