@@ -139,3 +139,40 @@ def test_two_threads_two_plans_two_streams():
     finally:
         for r in runs:
             r.close()
+
+
+def test_step_captured_in_a_cuda_graph_matches_eager():
+    """One update (grouped reduction, masked norm, masked AdamW with device
+    step counters) captured once in a CUDA graph and replayed three times
+    equals three eager updates: the path is stream-ordered, allocation-free
+    and keeps its step counts on the device."""
+    c = Case([50001, 512, 8192 * 2, 77], [RA, PS, LS, AR], 8, 2, 2, 2, 1 << 16, 2, 1e-3, 81)
+    eager, graph_run = Run(c), Run(c)
+    try:
+        n = len(c.numels)
+        used = torch.ones(n, dtype=torch.uint8, device="cuda")
+        st_e = torch.zeros(n, dtype=torch.int32, device="cuda")
+        st_g = torch.zeros(n, dtype=torch.int32, device="cuda")
+        for _ in range(3):
+            eager.reduce(emit=False)
+            eager.masked_update(used, st_e)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            # the library needs no warm-up allocations: capture directly
+            with torch.cuda.graph(graph, stream=side):
+                graph_run.reduce(emit=False)
+                graph_run.masked_update(used, st_g)
+        torch.cuda.synchronize()
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+        assert st_g.tolist() == st_e.tolist() == [3] * n
+        for x, y in ((eager.acc, graph_run.acc), (eager.norm, graph_run.norm), (eager.master, graph_run.master),
+                     (eager.m, graph_run.m), (eager.v, graph_run.v), (eager.params, graph_run.params)):
+            assert torch.equal(x, y)
+    finally:
+        eager.close()
+        graph_run.close()
