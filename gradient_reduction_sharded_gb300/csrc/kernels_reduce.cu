@@ -137,7 +137,7 @@ struct Sum8<float> {
 };
 
 template <typename E>
-__global__ void __launch_bounds__(RED_THREADS, 1) reduce_kernel(const __grid_constant__ ReduceArgs a) {
+__global__ void __launch_bounds__(RED_THREADS, GRS_RED_CTAS_PER_SM) reduce_kernel(const __grid_constant__ ReduceArgs a) {
   constexpr uint32_t ESZ = sizeof(E);
   extern __shared__ __align__(128) uint8_t smem[];
   const int S = a.stages;
@@ -165,7 +165,7 @@ __global__ void __launch_bounds__(RED_THREADS, 1) reduce_kernel(const __grid_con
   const int64_t stride = gridDim.x;
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
-    const uint64_t pol = l2_policy_evict_first();
+    const uint64_t pol = GRS_RED_EVICT_FIRST ? l2_policy_evict_first() : l2_policy_evict_normal();
     int64_t iter = 0;
     bool ok = true;
     // The CTA's tiles increase monotonically, so the unit only moves forward.
@@ -344,7 +344,7 @@ int launch_reduce(const grs_plan* p, const ReduceLaunch& l, void* stream) {
     if (e != cudaSuccess) return static_cast<int>(e);
     g_attr_set[f32][p->device] = true;
   }
-  int64_t cap = p->sm_count;
+  int64_t cap = int64_t(p->sm_count) * GRS_RED_CTAS_PER_SM;
   if (l.max_ctas > 0 && l.max_ctas < cap) cap = l.max_ctas;
   const int64_t grid = tiles < cap ? tiles : cap;
   const cudaError_t e = f32 ? launch_k(reduce_kernel<float>, dim3(unsigned(grid)), dim3(RED_THREADS), smem, stream, a)
