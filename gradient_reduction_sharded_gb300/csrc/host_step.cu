@@ -23,7 +23,9 @@ std::mutex g_res_mu;
 
 struct Resources {
   cudaStream_t copy = nullptr;
-  cudaEvent_t start = nullptr;       // the caller's stream at entry
+  cudaEvent_t start = nullptr;       // the caller's stream at the first call's entry
+  cudaEvent_t prev_done = nullptr;   // after the last reduction of the previous call
+  bool have_prev = false;            // prev_done was recorded by a call that succeeded
   std::vector<cudaEvent_t> copied;   // [2][n_buckets]
   std::vector<cudaEvent_t> reduced;  // [2][n_buckets]
 };
@@ -42,6 +44,7 @@ grs_status ensure_resources(grs_plan* p) {
   const size_t ne = 2 * p->buckets.size();
   cudaError_t e = cudaStreamCreateWithFlags(&r->copy, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&r->start, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&r->prev_done, cudaEventDisableTiming);
   for (size_t i = 0; i < ne && e == cudaSuccess; ++i) {
     cudaEvent_t a = nullptr, b = nullptr;
     e = cudaEventCreateWithFlags(&a, cudaEventDisableTiming);
@@ -53,6 +56,7 @@ grs_status ensure_resources(grs_plan* p) {
     for (auto ev : r->copied) if (ev) cudaEventDestroy(ev);
     for (auto ev : r->reduced) if (ev) cudaEventDestroy(ev);
     if (r->start) cudaEventDestroy(r->start);
+    if (r->prev_done) cudaEventDestroy(r->prev_done);
     if (r->copy) cudaStreamDestroy(r->copy);
     delete r;
     return fail(GRS_ERR_CUDA, std::string("grs_step_from_host: stream/event creation: ") + cudaGetErrorString(e));
@@ -71,6 +75,7 @@ void destroy_host_step_resources(grs_plan* p) {
   for (auto ev : r->copied) cudaEventDestroy(ev);
   for (auto ev : r->reduced) cudaEventDestroy(ev);
   if (r->start) cudaEventDestroy(r->start);
+  if (r->prev_done) cudaEventDestroy(r->prev_done);
   if (r->copy) cudaStreamDestroy(r->copy);
   delete r;
   p->host_step_resources = nullptr;
@@ -108,10 +113,19 @@ extern "C" grs_status grs_step_from_host(const grs_plan* pc, const grs_adamw* hp
   Resources* r = resources(p);
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const size_t nb = p->buckets.size();
-  // The copy stream must not run ahead of work the caller queued earlier.
+  // The copies only write the staging halves.  On the first call they wait
+  // for everything the caller queued before; afterwards only for the
+  // previous call's reductions (the last readers of the staging halves), so
+  // this step's host-to-device copies overlap the previous step's update and
+  // read-back.
   if (st == GRS_OK) {
-    cudaError_t e = cudaEventRecord(r->start, cs);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(r->copy, r->start, 0);
+    cudaError_t e = cudaSuccess;
+    if (!r->have_prev) {
+      e = cudaEventRecord(r->start, cs);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(r->copy, r->start, 0);
+    } else {
+      e = cudaStreamWaitEvent(r->copy, r->prev_done, 0);
+    }
     if (e != cudaSuccess) st = fail(GRS_ERR_CUDA, std::string("grs_step_from_host: ") + cudaGetErrorString(e));
   }
   for (int32_t j = 0; j < M && st == GRS_OK; ++j) {
@@ -146,6 +160,13 @@ extern "C" grs_status grs_step_from_host(const grs_plan* pc, const grs_adamw* hp
       if (e != cudaSuccess) st = fail(GRS_ERR_CUDA, std::string("grs_step_from_host: ") + cudaGetErrorString(e));
     }
   }
+  if (st == GRS_OK) {
+    const cudaError_t e = cudaEventRecord(r->prev_done, cs);
+    if (e != cudaSuccess) st = fail(GRS_ERR_CUDA, std::string("grs_step_from_host: ") + cudaGetErrorString(e));
+  }
+  // A call that failed part-way may have left reductions queued; the next
+  // call then waits for all work on its stream again.
+  if (r != nullptr) r->have_prev = st == GRS_OK;
   if (st == GRS_OK) st = grs_grad_norm_sq(p, acc, M, workspace, 1, d_norm_sq, stream);
   if (st == GRS_OK) st = grs_clip_adamw_step(p, hp, d_norm_sq, acc, master, m, v, params_bf16, stream);
   if (st == GRS_OK && host_params != nullptr) {

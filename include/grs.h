@@ -354,7 +354,12 @@ grs_status grs_gather_params(const grs_plan* plan, const uint16_t* params_bf16,
  * The host buffers must stay valid until `stream` has run the call's work;
  * the read-backs are complete after the caller synchronises `stream`.  The
  * first call creates the plan's copy stream and events (freed by
- * grs_plan_destroy).  Errors: INVALID_ARG, ALIGNMENT, NO_DEVICE, CUDA. */
+ * grs_plan_destroy) and its copies wait for all work queued on `stream`
+ * before; later calls' copies wait only for the previous call's reductions,
+ * so consecutive steps overlap (step N+1's host-to-device copies run during
+ * step N's update and read-back).  The staging buffers therefore belong to
+ * these calls: do not touch them on other streams in between.  Errors:
+ * INVALID_ARG, ALIGNMENT, NO_DEVICE, CUDA. */
 grs_status grs_step_from_host(const grs_plan* plan, const grs_adamw* hp,
                               const void* const* host_grads, void* const* dev_stage,
                               float* acc, float* master, float* m, float* v, uint16_t* params_bf16,

@@ -368,6 +368,54 @@ def test_step_from_host_matches_device_path(name):
         b.close()
 
 
+@pytest.mark.parametrize("name", ["multi-tile-world16-M2", "odd-ds3-M3"])
+def test_step_from_host_back_to_back(name):
+    """Three grs_step_from_host calls queued without a synchronisation in
+    between (each with its own host gradients and read-back buffers): the
+    copies of step n+1 overlap step n's update, and every step's results
+    equal the device path's bit for bit."""
+    g = grs()
+    c = SMALL[name]
+    a = Run(c)
+    b = Run(c)
+    try:
+        W, M = c.world, c.n_micro
+        n = a.grads[0][0].numel()
+        steps = 3
+        host = [[torch.empty(n, dtype=torch.int16).pin_memory() for _ in range(M * W)] for _ in range(steps)]
+        outp = [torch.empty(a.nsp, dtype=torch.int16).pin_memory() for _ in range(steps)]
+        outn = [torch.empty(1, dtype=torch.float64).pin_memory() for _ in range(steps)]
+        stage = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(2 * W)]
+        want_params, want_norm = [], []
+        for t in range(steps):
+            if t:
+                a.fill_grads(step_seed=10 + t)
+            for j in range(M):
+                for k in range(W):
+                    host[t][j * W + k].copy_(a.grads[j][k].view(torch.int16))
+            a.update()
+            torch.cuda.synchronize()
+            want_params.append(a.params[:a.nsp].cpu().clone())
+            want_norm.append(float(a.norm.cpu()[0]))
+        s = b.stream()
+        for t in range(steps):
+            hp = g.make_adamw(c.hp[0], c.hp[1], c.hp[2], c.hp[3], c.hp[4], c.max_norm, t + 1, M)
+            g.grs_step_from_host(b.plan, hp, [x.data_ptr() for x in host[t]], [x.data_ptr() for x in stage],
+                                 b.acc.data_ptr(), b.master.data_ptr(), b.m.data_ptr(), b.v.data_ptr(),
+                                 b.params.data_ptr(), b.ws.data_ptr(), b.norm.data_ptr(),
+                                 outp[t].data_ptr(), outn[t].data_ptr(), s)
+        torch.cuda.synchronize()
+        assert b.check_flags() == 0
+        for t in range(steps):
+            assert torch.equal(outp[t], want_params[t]), f"step {t + 1}"
+            assert float(outn[t][0]) == want_norm[t], f"step {t + 1}"
+        for x, y in ((a.acc, b.acc), (a.master, b.master), (a.m, b.m), (a.v, b.v)):
+            assert torch.equal(x[:a.nsp], y[:a.nsp])
+    finally:
+        a.close()
+        b.close()
+
+
 def test_frozen_tensors_excluded():
     """GRS_TENSOR_FROZEN tensors take no place in the plan: parity of the
     update on the rest, and the gather leaves their storage untouched."""
