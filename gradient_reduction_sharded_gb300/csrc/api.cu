@@ -74,10 +74,12 @@ void free_device(grs_plan* p) {
   cudaFree(p->d_red_prefix);
   cudaFree(p->d_upd_prefix);
   cudaFree(p->d_jobs);
+  cudaFree(p->d_chunk_job);
   cudaFree(p->d_flags);
   p->d_units = nullptr;
   p->d_red_prefix = p->d_upd_prefix = nullptr;
   p->d_jobs = nullptr;
+  p->d_chunk_job = nullptr;
   p->d_flags = nullptr;
 }
 
@@ -122,6 +124,7 @@ grs_status grs_plan_create_ex(const int64_t* numels, const int32_t* owners, cons
     if (e == cudaSuccess) e = upload(&p->d_red_prefix, p->red_prefix);
     if (e == cudaSuccess) e = upload(&p->d_upd_prefix, p->upd_prefix);
     if (e == cudaSuccess) e = upload(&p->d_jobs, p->jobs);
+    if (e == cudaSuccess) e = upload(&p->d_chunk_job, p->chunk_job);
     if (e == cudaSuccess) e = upload(&p->d_seg_start, p->seg_start);
     if (e == cudaSuccess) e = upload(&p->d_seg_tensor, p->seg_tensor);
     if (e == cudaSuccess) e = upload(&p->d_bucket_seg0, p->bucket_seg0);

@@ -107,6 +107,7 @@ struct grs_plan {
   std::vector<int64_t> red_prefix;  // [n_units + 1] first reduction tile per unit
   std::vector<int64_t> upd_prefix;  // [n_units + 1] first update tile per unit
   std::vector<grs::GatherJob> jobs; // by tensor, LOCAL_SHARD: tp jobs
+  std::vector<int32_t> chunk_job;   // [n_gather_chunks]: the job each gather chunk belongs to
   // Tensor segments of every bucket in offset order: segments
   // [bucket_seg0[b], bucket_seg0[b+1]) start at seg_start[] (per-rank element
   // offset inside the bucket) and belong to tensor seg_tensor[].
@@ -124,6 +125,7 @@ struct grs_plan {
   int64_t* d_red_prefix = nullptr;
   int64_t* d_upd_prefix = nullptr;
   grs::GatherJob* d_jobs = nullptr;
+  int32_t* d_chunk_job = nullptr;
   int64_t* d_seg_start = nullptr;
   int32_t* d_seg_tensor = nullptr;
   int32_t* d_bucket_seg0 = nullptr;

@@ -3,11 +3,12 @@
 // section 2: parameters are all-gathered across shards for the forward;
 // LOCAL_SHARD tensors are reassembled from their tp rows in dim-0 order).
 //
-// A segmented copy: the plan holds one job per (tensor, state row); each
-// block copies one GATHER_CHUNK slice of one job.  Tensors are packed back
-// to back inside buckets, so source and destination alignments differ per
-// job: when both are 16-byte co-aligned the body moves 16-byte vectors,
-// otherwise 4-byte or 2-byte words.
+// A segmented copy: the plan holds one job per (tensor, state row) and, per
+// GATHER_CHUNK slice of a job, the job's index (one load finds a block's
+// job).  Each block copies one chunk.  Tensors are packed back to back
+// inside buckets, so source and destination alignments differ per job:
+// when both are 16-byte co-aligned the body moves 16-byte vectors, the whole
+// chunk's loads issued before its stores; otherwise 4-byte or 2-byte words.
 #include <cuda_runtime.h>
 
 #include "device.cuh"
@@ -20,51 +21,34 @@ namespace {
 constexpr int GATHER_THREADS = 256;
 constexpr int GATHER_MAX_PTRS = 256;  // tensor pointers per launch (2 KB of parameters)
 
-struct GatherArgs {
-  uint16_t* dst[GATHER_MAX_PTRS];
-  const uint16_t* params;
-  const GatherJob* jobs;
-  int32_t tensor_begin;  // dst[0] is this tensor
-  int32_t job_begin, job_end;
-  int64_t chunk_begin;
-};
-
-__device__ __forceinline__ int find_job(const GatherJob* jobs, int lo, int hi, int64_t chunk) {
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (jobs[mid].chunk0 <= chunk)
-      lo = mid;
-    else
-      hi = mid;
-  }
-  return lo;
-}
-
-__global__ void __launch_bounds__(GATHER_THREADS) gather_kernel(const __grid_constant__ GatherArgs a) {
-  const int64_t chunk = a.chunk_begin + blockIdx.x;
-  const int j = find_job(a.jobs, a.job_begin, a.job_end, chunk);
-  const GatherJob jb = a.jobs[j];
-  uint16_t* dbase = a.dst[jb.tensor - a.tensor_begin];
-  if (dbase == nullptr) return;
-  const int64_t off = (chunk - jb.chunk0) * GATHER_CHUNK;
-  const int64_t rem = jb.len - off;
-  const int64_t n = rem < GATHER_CHUNK ? rem : GATHER_CHUNK;
-  const uint16_t* src = a.params + jb.src + off;
-  uint16_t* dst = dbase + jb.dst + off;
+// Block-wide copy of n elements of T (2 or 4 bytes).  The 16-byte body puts
+// a whole chunk's loads in flight per thread (GATHER_CHUNK·sizeof(T)/16 over
+// the block) before storing, so a block costs one memory round trip.
+template <typename T>
+__device__ __forceinline__ void block_copy(const T* __restrict__ src, T* __restrict__ dst, int64_t n) {
+  constexpr int U = static_cast<int>(GATHER_CHUNK * sizeof(T) / 16 / GATHER_THREADS);
+  constexpr int PER_VEC = 16 / static_cast<int>(sizeof(T));
+  static_assert(U >= 1, "chunk smaller than one vector per thread");
   const uintptr_t sa = reinterpret_cast<uintptr_t>(src);
   const uintptr_t da = reinterpret_cast<uintptr_t>(dst);
   if (((sa ^ da) & 15) == 0) {
-    // head up to a 16-byte boundary, 16-byte body, tail
-    const int64_t head = static_cast<int64_t>(((16 - (sa & 15)) & 15) >> 1) < n
-                             ? static_cast<int64_t>(((16 - (sa & 15)) & 15) >> 1)
-                             : n;
+    const int64_t h = static_cast<int64_t>(((16 - (sa & 15)) & 15) / sizeof(T));
+    const int64_t head = h < n ? h : n;
     for (int64_t i = threadIdx.x; i < head; i += GATHER_THREADS) dst[i] = src[i];
-    const int64_t nv = (n - head) >> 3;
+    const int64_t nv = (n - head) / PER_VEC;
     const uint4* s4 = reinterpret_cast<const uint4*>(src + head);
     uint4* d4 = reinterpret_cast<uint4*>(dst + head);
-    for (int64_t i = threadIdx.x; i < nv; i += GATHER_THREADS) d4[i] = __ldcs(s4 + i);
-    for (int64_t i = head + nv * 8 + threadIdx.x; i < n; i += GATHER_THREADS) dst[i] = src[i];
-  } else if (((sa ^ da) & 3) == 0) {
+    int64_t i = threadIdx.x;
+    for (; i + int64_t(U - 1) * GATHER_THREADS < nv; i += int64_t(U) * GATHER_THREADS) {
+      uint4 r[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) r[u] = __ldcs(s4 + i + u * GATHER_THREADS);
+#pragma unroll
+      for (int u = 0; u < U; ++u) d4[i + u * GATHER_THREADS] = r[u];
+    }
+    for (; i < nv; i += GATHER_THREADS) d4[i] = __ldcs(s4 + i);
+    for (int64_t k = head + nv * PER_VEC + threadIdx.x; k < n; k += GATHER_THREADS) dst[k] = src[k];
+  } else if (sizeof(T) == 2 && ((sa ^ da) & 3) == 0) {
     const int64_t head = ((sa & 3) != 0 && n > 0) ? 1 : 0;
     if (threadIdx.x == 0 && head) dst[0] = src[0];
     const int64_t nw = (n - head) >> 1;
@@ -77,35 +61,38 @@ __global__ void __launch_bounds__(GATHER_THREADS) gather_kernel(const __grid_con
   }
 }
 
-// fp32 state <-> canonical logical order: the same segmented jobs, one
-// block per GATHER_CHUNK slice of a job, 16-byte vectors where source and
-// destination are co-aligned.
-template <bool kToLogical>
-__global__ void __launch_bounds__(GATHER_THREADS) state_logical_kernel(const GatherJob* __restrict__ jobs,
-                                                                        int32_t n_jobs, const float* __restrict__ src_base,
-                                                                        float* __restrict__ dst_base) {
-  const int64_t chunk = blockIdx.x;
-  const int j = find_job(jobs, 0, n_jobs, chunk);
-  const GatherJob jb = jobs[j];
+struct GatherArgs {
+  uint16_t* dst[GATHER_MAX_PTRS];
+  const uint16_t* params;
+  const GatherJob* jobs;
+  const int32_t* chunk_job;
+  int32_t tensor_begin;  // dst[0] is this tensor
+  int64_t chunk_begin;
+};
+
+__global__ void __launch_bounds__(GATHER_THREADS) gather_kernel(const __grid_constant__ GatherArgs a) {
+  const int64_t chunk = a.chunk_begin + blockIdx.x;
+  const GatherJob jb = a.jobs[a.chunk_job[chunk]];
+  uint16_t* dbase = a.dst[jb.tensor - a.tensor_begin];
+  if (dbase == nullptr) return;
   const int64_t off = (chunk - jb.chunk0) * GATHER_CHUNK;
   const int64_t rem = jb.len - off;
-  const int64_t n = rem < GATHER_CHUNK ? rem : GATHER_CHUNK;
-  const float* src = src_base + (kToLogical ? jb.src : jb.logical) + off;
-  float* dst = dst_base + (kToLogical ? jb.logical : jb.src) + off;
-  const uintptr_t sa = reinterpret_cast<uintptr_t>(src);
-  const uintptr_t da = reinterpret_cast<uintptr_t>(dst);
-  if (((sa ^ da) & 15) == 0) {
-    const int64_t h = static_cast<int64_t>(((16 - (sa & 15)) & 15) >> 2);
-    const int64_t head = h < n ? h : n;
-    for (int64_t i = threadIdx.x; i < head; i += GATHER_THREADS) dst[i] = src[i];
-    const int64_t nv = (n - head) >> 2;
-    const float4* s4 = reinterpret_cast<const float4*>(src + head);
-    float4* d4 = reinterpret_cast<float4*>(dst + head);
-    for (int64_t i = threadIdx.x; i < nv; i += GATHER_THREADS) d4[i] = __ldcs(s4 + i);
-    for (int64_t i = head + nv * 4 + threadIdx.x; i < n; i += GATHER_THREADS) dst[i] = src[i];
-  } else {
-    for (int64_t i = threadIdx.x; i < n; i += GATHER_THREADS) dst[i] = src[i];
-  }
+  block_copy(a.params + jb.src + off, dbase + jb.dst + off, rem < GATHER_CHUNK ? rem : GATHER_CHUNK);
+}
+
+// fp32 state <-> canonical logical order: the same segmented jobs and
+// chunks, one block per chunk.
+template <bool kToLogical>
+__global__ void __launch_bounds__(GATHER_THREADS) state_logical_kernel(const GatherJob* __restrict__ jobs,
+                                                                        const int32_t* __restrict__ chunk_job,
+                                                                        const float* __restrict__ src_base,
+                                                                        float* __restrict__ dst_base) {
+  const int64_t chunk = blockIdx.x;
+  const GatherJob jb = jobs[chunk_job[chunk]];
+  const int64_t off = (chunk - jb.chunk0) * GATHER_CHUNK;
+  const int64_t rem = jb.len - off;
+  block_copy(src_base + (kToLogical ? jb.src : jb.logical) + off,
+             dst_base + (kToLogical ? jb.logical : jb.src) + off, rem < GATHER_CHUNK ? rem : GATHER_CHUNK);
 }
 
 // Self-test of the bounded wait: one thread arms an mbarrier that nothing
@@ -176,7 +163,7 @@ int launch_state_to_logical(const grs_plan* p, const float* state, float* logica
   if (p->n_gather_chunks <= 0) return 0;
   state_logical_kernel<true><<<static_cast<unsigned>(p->n_gather_chunks), GATHER_THREADS, 0,
                                static_cast<cudaStream_t>(stream)>>>(
-      p->d_jobs, static_cast<int32_t>(p->jobs.size()), state, logical);
+      p->d_jobs, p->d_chunk_job, state, logical);
   return static_cast<int>(cudaGetLastError());
 }
 
@@ -187,7 +174,7 @@ int launch_state_from_logical(const grs_plan* p, const float* logical, float* st
   if (p->n_gather_chunks <= 0) return 0;
   state_logical_kernel<false><<<static_cast<unsigned>(p->n_gather_chunks), GATHER_THREADS, 0,
                                 static_cast<cudaStream_t>(stream)>>>(
-      p->d_jobs, static_cast<int32_t>(p->jobs.size()), logical, state);
+      p->d_jobs, p->d_chunk_job, logical, state);
   return static_cast<int>(cudaGetLastError());
 }
 
@@ -205,13 +192,14 @@ int launch_gather(const grs_plan* p, const uint16_t* params, uint16_t* const* te
     if (!any) continue;
     a.params = params;
     a.jobs = p->d_jobs;
+    a.chunk_job = p->d_chunk_job;
     a.tensor_begin = t0;
-    a.job_begin = p->tensor_job0[t0];
-    a.job_end = p->tensor_job0[t1];
-    if (a.job_end <= a.job_begin) continue;
-    a.chunk_begin = p->jobs[a.job_begin].chunk0;
+    const int32_t job_begin = p->tensor_job0[t0];
+    const int32_t job_end = p->tensor_job0[t1];
+    if (job_end <= job_begin) continue;
+    a.chunk_begin = p->jobs[job_begin].chunk0;
     const int64_t chunk_end =
-        a.job_end < static_cast<int32_t>(p->jobs.size()) ? p->jobs[a.job_end].chunk0 : p->n_gather_chunks;
+        job_end < static_cast<int32_t>(p->jobs.size()) ? p->jobs[job_end].chunk0 : p->n_gather_chunks;
     if (chunk_end <= a.chunk_begin) continue;
     gather_kernel<<<static_cast<unsigned>(chunk_end - a.chunk_begin), GATHER_THREADS, 0,
                     static_cast<cudaStream_t>(stream)>>>(a);

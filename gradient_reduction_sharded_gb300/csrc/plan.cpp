@@ -190,6 +190,7 @@ grs_status build_plan(const int64_t* numels, const int32_t* owners, const uint32
 
   // Gather jobs: one per (tensor, state row).
   p->jobs.clear();
+  p->chunk_job.clear();
   p->tensor_job0.assign(1, 0);
   int64_t chunks = 0;
   int64_t logical = 0;  // canonical order: live tensors in model order, full logical extent
@@ -208,7 +209,9 @@ grs_status build_plan(const int64_t* numels, const int32_t* owners, const uint32
       j.chunk0 = chunks;
       j.logical = logical + static_cast<int64_t>(t) * per_rank;
       j.tensor = i;
-      chunks += (per_rank + GATHER_CHUNK - 1) / GATHER_CHUNK;
+      const int64_t nc = (per_rank + GATHER_CHUNK - 1) / GATHER_CHUNK;
+      chunks += nc;
+      p->chunk_job.insert(p->chunk_job.end(), static_cast<size_t>(nc), static_cast<int32_t>(p->jobs.size()));
       p->jobs.push_back(j);
     }
     logical += numels[i];
