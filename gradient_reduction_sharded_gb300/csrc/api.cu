@@ -187,6 +187,27 @@ grs_status grs_bucket_info(const grs_plan* p, int32_t b, grs_bucket_desc* o) {
   o->shard_len = bk.shard_len;
   o->rank_offset = bk.rank_off;
   o->state_offset = bk.state_off;
+  o->n_segments = bk.copies * (p->bucket_seg0[b + 1] - p->bucket_seg0[b]);
+  return GRS_OK;
+}
+
+grs_status grs_segment_info(const grs_plan* p, int32_t b, int32_t i, grs_segment_desc* o) {
+  if (p == nullptr || o == nullptr) return fail(GRS_ERR_INVALID_ARG, "NULL argument");
+  if (b < 0 || b >= static_cast<int32_t>(p->buckets.size()))
+    return fail(GRS_ERR_INVALID_ARG, "bucket index out of range");
+  const grs::Bucket& bk = p->buckets[b];
+  const int32_t nt = p->bucket_seg0[b + 1] - p->bucket_seg0[b];
+  if (i < 0 || nt == 0 || i >= bk.copies * nt) return fail(GRS_ERR_INVALID_ARG, "segment index out of range");
+  const int32_t t = i / nt;
+  const int32_t tensor = p->seg_tensor[p->bucket_seg0[b] + i % nt];
+  const int64_t per_rank = (p->owner[tensor] == GRS_LOCAL_SHARD) ? p->numel[tensor] / p->tp : p->numel[tensor];
+  std::memset(o, 0, sizeof(*o));
+  o->tensor = tensor;
+  o->tp_index = t;
+  o->bucket_offset = p->t_offset[tensor];
+  o->tensor_offset = static_cast<int64_t>(t) * per_rank;
+  o->numel = per_rank;
+  o->state_offset = bk.state_off + static_cast<int64_t>(t) * bk.padded + p->t_offset[tensor];
   return GRS_OK;
 }
 

@@ -58,7 +58,14 @@ class grs_bucket_desc(ctypes.Structure):
                 ("group_size", ctypes.c_int32), ("n_tensors", ctypes.c_int32),
                 ("used", ctypes.c_int64), ("padded", ctypes.c_int64),
                 ("shard_len", ctypes.c_int64), ("rank_offset", ctypes.c_int64),
-                ("state_offset", ctypes.c_int64)]
+                ("state_offset", ctypes.c_int64), ("n_segments", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+class grs_segment_desc(ctypes.Structure):
+    _fields_ = [("tensor", ctypes.c_int32), ("tp_index", ctypes.c_int32),
+                ("bucket_offset", ctypes.c_int64), ("tensor_offset", ctypes.c_int64),
+                ("numel", ctypes.c_int64), ("state_offset", ctypes.c_int64)]
 
 
 class grs_tensor_desc(ctypes.Structure):
@@ -93,6 +100,7 @@ _sig = {
     "grs_plan_query": ([_vp, _P(grs_plan_info)], ctypes.c_int),
     "grs_bucket_info": ([_vp, ctypes.c_int32, _P(grs_bucket_desc)], ctypes.c_int),
     "grs_tensor_info": ([_vp, ctypes.c_int32, _P(grs_tensor_desc)], ctypes.c_int),
+    "grs_segment_info": ([_vp, ctypes.c_int32, ctypes.c_int32, _P(grs_segment_desc)], ctypes.c_int),
     "grs_reduce_bucket": ([_vp, ctypes.c_int32, _P(_vp), _vp, ctypes.c_int32, ctypes.c_int32, _vp,
                            _vp], ctypes.c_int),
     "grs_reduce_all": ([_vp, _P(_vp), _vp, ctypes.c_int32, ctypes.c_int32, _vp, _vp], ctypes.c_int),
@@ -186,6 +194,12 @@ def grs_bucket_info(plan: int, bucket: int) -> Dict[str, int]:
 def grs_tensor_info(plan: int, tensor: int) -> Dict[str, int]:
     o = grs_tensor_desc()
     _check(_lib.grs_tensor_info(plan, tensor, ctypes.byref(o)), "grs_tensor_info")
+    return _as_dict(o)
+
+
+def grs_segment_info(plan: int, bucket: int, segment: int) -> Dict[str, int]:
+    o = grs_segment_desc()
+    _check(_lib.grs_segment_info(plan, bucket, segment, ctypes.byref(o)), "grs_segment_info")
     return _as_dict(o)
 
 

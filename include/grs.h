@@ -125,7 +125,21 @@ typedef struct grs_bucket_desc {
   int64_t shard_len;      /* padded / dp_shard */
   int64_t rank_offset;    /* offset of the bucket in each rank buffer */
   int64_t state_offset;   /* offset of row 0 in the state arrays */
+  int32_t n_segments;     /* copies * n_tensors (see grs_segment_info) */
+  int32_t reserved;
 } grs_bucket_desc;
+
+/* One segment of a bucket: the part of one tensor that lives in one state
+ * row of the bucket (a LOCAL_SHARD tensor has one segment per tp rank, any
+ * other tensor one).  Segments tile each row's [0, used) back to back. */
+typedef struct grs_segment_desc {
+  int32_t tensor;         /* index in the plan's tensor list */
+  int32_t tp_index;       /* state row: the tp rank for LOCAL_SHARD buckets, else 0 */
+  int64_t bucket_offset;  /* element offset inside the bucket row (the same in every rank buffer) */
+  int64_t tensor_offset;  /* element offset inside the tensor's row-major flattening */
+  int64_t numel;          /* elements in the segment */
+  int64_t state_offset;   /* absolute offset in the state arrays and the full-parameter buffer */
+} grs_segment_desc;
 
 typedef struct grs_tensor_desc {
   int32_t bucket;         /* -1 for a frozen tensor */
@@ -196,6 +210,11 @@ void grs_plan_destroy(grs_plan* plan);
 grs_status grs_plan_query(const grs_plan* plan, grs_plan_info* out);
 grs_status grs_bucket_info(const grs_plan* plan, int32_t bucket, grs_bucket_desc* out);
 grs_status grs_tensor_info(const grs_plan* plan, int32_t tensor, grs_tensor_desc* out);
+/* Segment i of bucket b, 0 <= i < n_segments, in state-memory order: row
+ * t = i / n_tensors, then the bucket's tensors by increasing offset
+ * ([COSMOS] section 2: a LOCAL_SHARD tensor's tp slices are its dim-0
+ * chunks, rank t's chunk in row t).  Index out of range -> INVALID_ARG. */
+grs_status grs_segment_info(const grs_plan* plan, int32_t bucket, int32_t segment, grs_segment_desc* out);
 
 /* ---------------------------------------------------------- hot path */
 

@@ -67,6 +67,36 @@ def _compare_plan(grs, h, op, numels, owners):
         assert t["bucket_offset"] == int(op.t_offset[i])
         assert t["numel"] == numels[i]
         assert t["owner"] == owners[i]
+    _compare_segments(grs, h, op, numels)
+
+
+def _compare_segments(grs, h, op, numels):
+    """Segments against the oracle's tensor placement: row by row, the
+    bucket's tensors in model order, each at the oracle's offset and state
+    range; together they tile [0, used) of every row and cover every live
+    tensor's elements exactly once."""
+    covered = {i: 0 for i in range(len(numels)) if int(op.t_bucket[i]) >= 0}
+    for b in range(op.n_buckets):
+        members = [i for i in range(len(numels)) if int(op.t_bucket[i]) == b]
+        d = grs.grs_bucket_info(h, b)
+        assert d["n_segments"] == op.copies(b) * len(members)
+        for t in range(op.copies(b)):
+            pos = 0
+            for k, i in enumerate(members):
+                s = grs.grs_segment_info(h, b, t * len(members) + k)
+                assert s["tensor"] == i and s["tp_index"] == t
+                assert s["bucket_offset"] == int(op.t_offset[i]) == pos
+                assert s["numel"] == op.per_rank(i)
+                assert s["tensor_offset"] == t * op.per_rank(i)
+                assert s["state_offset"] == op.tensor_rows(i)[t][0]
+                pos += s["numel"]
+                covered[i] += s["numel"]
+            assert pos == int(op.b_used[b])
+        with pytest.raises(grs.GrsError):
+            grs.grs_segment_info(h, b, d["n_segments"])
+        with pytest.raises(grs.GrsError):
+            grs.grs_segment_info(h, b, -1)
+    assert all(covered[i] == numels[i] for i in covered)
 
 
 @pytest.mark.parametrize("cid", workloads.ALL_IDS)
