@@ -13,6 +13,10 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgrs.so")
+# The checked build (every kernel index verified against its buffer, see
+# GRS_CHECKED in csrc/internal.h): tests and debugging only.
+CHECKED_LIB = os.path.join(PKG, "checked", "libgrs.so")
+CHECKED_FLAGS = ("-DGRS_CHECKED=1",)
 
 SOURCES = ["plan.cpp", "api.cu", "kernels_reduce.cu", "kernels_update.cu", "kernels_gather.cu",
            "noalloc.cu", "host_step.cu", "kernels_masked.cu"]
@@ -42,7 +46,15 @@ def build(force: bool = False, verbose: bool = False, extra_flags=(), out: str =
     `extra_flags` (e.g. -D overrides of tile constants) with `out` builds a
     variant library elsewhere."""
     lib = out or LIB
-    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= _deps_mtime() and not extra_flags:
+    stamp = lib + ".flags"
+    want = " ".join(extra_flags)
+    have = None
+    if os.path.exists(stamp):
+        with open(stamp) as f:
+            have = f.read()
+    elif not extra_flags:
+        have = ""
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= _deps_mtime() and have == want:
         return lib
     build_dir = os.path.join(os.path.dirname(lib), "_build") if out else BUILD
     os.makedirs(build_dir, exist_ok=True)
@@ -66,7 +78,18 @@ def build(force: bool = False, verbose: bool = False, extra_flags=(), out: str =
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, lib)
+    if extra_flags:
+        with open(stamp, "w") as f:
+            f.write(want)
+    elif os.path.exists(stamp):
+        os.remove(stamp)
     return lib
+
+
+def build_checked(force: bool = False) -> str:
+    """The checked variant of libgrs.so (GRS_CHECKED=1), built beside the
+    package in checked/."""
+    return build(force=force, extra_flags=CHECKED_FLAGS, out=CHECKED_LIB)
 
 
 if __name__ == "__main__":

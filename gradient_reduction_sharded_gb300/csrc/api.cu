@@ -228,7 +228,8 @@ grs_status grs_tensor_info(const grs_plan* p, int32_t i, grs_tensor_desc* o) {
 static grs_status reduce_common(const grs_plan* p, const void* const* rank_grads, float* acc,
                                 int32_t accumulate, int32_t emit, void* workspace, void* stream,
                                 int32_t unit_begin, int32_t unit_end, int64_t state_base,
-                                int64_t rank_base, int32_t tag, const char* who, int32_t max_ctas = 0,
+                                int64_t rank_base, int64_t state_len, int64_t rank_len, int32_t tag,
+                                const char* who, int32_t max_ctas = 0,
                                 void* wait_event = nullptr) {
   if (rank_grads == nullptr || acc == nullptr)
     return fail(GRS_ERR_INVALID_ARG, std::string(who) + ": rank_grads/acc is NULL");
@@ -258,6 +259,8 @@ static grs_status reduce_common(const grs_plan* p, const void* const* rank_grads
   l.unit_end = unit_end;
   l.state_base = state_base;
   l.rank_base = rank_base;
+  l.state_len = state_len;
+  l.rank_len = rank_len;
   l.accumulate = accumulate ? 1 : 0;
   l.max_ctas = max_ctas;
   if (wait_event != nullptr) {
@@ -278,7 +281,8 @@ grs_status grs_reduce_bucket(const grs_plan* p, int32_t b, const void* const* ra
     return fail(GRS_ERR_INVALID_ARG, "grs_reduce_bucket: bucket index out of range");
   const grs::Bucket& bk = p->buckets[b];
   return reduce_common(p, rank_grads, acc, accumulate, emit, workspace, stream, bk.unit0,
-                       bk.unit0 + bk.copies, bk.state_off, bk.rank_off, bk.tag, "grs_reduce_bucket");
+                       bk.unit0 + bk.copies, bk.state_off, bk.rank_off, int64_t(bk.copies) * bk.padded,
+                       bk.padded, bk.tag, "grs_reduce_bucket");
 }
 
 grs_status grs_reduce_bucket_ex(const grs_plan* p, int32_t b, const void* const* rank_grads, float* acc,
@@ -291,8 +295,8 @@ grs_status grs_reduce_bucket_ex(const grs_plan* p, int32_t b, const void* const*
   if (max_ctas < 0) return fail(GRS_ERR_INVALID_ARG, "grs_reduce_bucket_ex: max_ctas must be >= 0");
   const grs::Bucket& bk = p->buckets[b];
   return reduce_common(p, rank_grads, acc, accumulate, emit, workspace, stream, bk.unit0,
-                       bk.unit0 + bk.copies, bk.state_off, bk.rank_off, bk.tag, "grs_reduce_bucket_ex",
-                       max_ctas, wait_event);
+                       bk.unit0 + bk.copies, bk.state_off, bk.rank_off, int64_t(bk.copies) * bk.padded,
+                       bk.padded, bk.tag, "grs_reduce_bucket_ex", max_ctas, wait_event);
 }
 
 grs_status grs_reduce_all(const grs_plan* p, const void* const* rank_grads, float* acc,
@@ -302,7 +306,7 @@ grs_status grs_reduce_all(const grs_plan* p, const void* const* rank_grads, floa
   bool only_ar = true;
   for (const auto& bk : p->buckets) only_ar = only_ar && bk.tag == GRS_ALREADY_REDUCED;
   return reduce_common(p, rank_grads, acc, accumulate, emit, workspace, stream, 0,
-                       static_cast<int32_t>(p->units.size()), 0, 0,
+                       static_cast<int32_t>(p->units.size()), 0, 0, p->n_state_pad, p->n_rank_pad,
                        only_ar ? GRS_ALREADY_REDUCED : GRS_REPLICA_AVG, "grs_reduce_all");
 }
 
@@ -476,6 +480,14 @@ grs_status grs_check_device_errors(const grs_plan* p, void* stream) {
   if (e != cudaSuccess) return cuda_fail(e, "grs_check_device_errors: flags");
   e = cudaMemset(p->d_flags, 0, sizeof(h));
   if (e != cudaSuccess) return cuda_fail(e, "grs_check_device_errors: clear flags");
+  if (h[grs::FLAG_BOUNDS]) {
+    static const char* const kSite[grs::SITE_COUNT] = {
+        "?", "reduce_kernel", "norm_pass1_kernel", "update_kernel", "accumulate_kernel", "gather_kernel",
+        "state_logical_kernel", "norm_pass1_masked_kernel", "update_masked_kernel",
+        "check_already_reduced_kernel"};
+    const int site = h[grs::FLAG_BOUNDS] > 0 && h[grs::FLAG_BOUNDS] < grs::SITE_COUNT ? h[grs::FLAG_BOUNDS] : 0;
+    return fail(GRS_ERR_BOUNDS, std::string("checked build: an index left its buffer in ") + kSite[site]);
+  }
   if (h[grs::FLAG_TIMEOUT]) return fail(GRS_ERR_TIMEOUT, "a bounded device wait timed out");
   if (h[grs::FLAG_NONFINITE]) return fail(GRS_ERR_NONFINITE, "global gradient norm is not finite");
   if (h[grs::FLAG_AR_MISMATCH])
@@ -485,5 +497,7 @@ grs_status grs_check_device_errors(const grs_plan* p, void* stream) {
 }
 
 const char* grs_last_error(void) { return g_last_error.c_str(); }
+
+uint32_t grs_build_features(void) { return GRS_CHECKED ? GRS_FEATURE_CHECKED : 0u; }
 
 }  // extern "C"

@@ -16,6 +16,19 @@ namespace grs {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Index checks of checked builds: GRS_CHECK(cond, flags, site) is `cond`,
+// and when it is false the site is recorded in flags[FLAG_BOUNDS] (the first
+// failure wins).  In ordinary builds it is `true` and compiles away.
+__device__ __forceinline__ bool check_or_flag(bool ok, int* flags, int site) {
+  if (!ok) atomicCAS(flags + FLAG_BOUNDS, 0, site);
+  return ok;
+}
+#if GRS_CHECKED
+#define GRS_CHECK(cond, flags, site) (::grs::check_or_flag((cond), (flags), (site)))
+#else
+#define GRS_CHECK(cond, flags, site) true
+#endif
+
 // A device wait gives up after this long and raises FLAG_TIMEOUT.
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 

@@ -10,6 +10,13 @@
 
 namespace grs {
 
+// Checked build: every kernel verifies the indices it derives against the
+// extents of the buffers they address (the sizes the C ABI documents),
+// skips a failing access and records the kernel in FLAG_BOUNDS.
+#ifndef GRS_CHECKED
+#define GRS_CHECKED 0
+#endif
+
 // Reduction tiles: a tile carries STAGE_GRAD_BYTES of gradient input (all the
 // group's rank rows for T elements), so T = STAGE_GRAD_BYTES / (esize * group),
 // capped at RED_MAX_T, a multiple of 8, and small enough that two stages
@@ -153,7 +160,22 @@ inline int64_t ws_bytes(int64_t n_red_tiles) { return ws_ticket_offset(n_red_til
 inline int64_t ws_factors_offset(int64_t n_red_tiles) { return ws_bytes(n_red_tiles); }
 
 // Device flags
-enum : int { FLAG_TIMEOUT = 0, FLAG_NONFINITE = 1, FLAG_AR_MISMATCH = 2, FLAG_COUNT = 4 };
+enum : int { FLAG_TIMEOUT = 0, FLAG_NONFINITE = 1, FLAG_AR_MISMATCH = 2, FLAG_BOUNDS = 3, FLAG_COUNT = 4 };
+
+// Kernels of checked builds (GRS_CHECKED=1) record the first failed index
+// check as one of these in FLAG_BOUNDS.
+enum : int {
+  SITE_REDUCE = 1,
+  SITE_NORM1 = 2,
+  SITE_UPDATE = 3,
+  SITE_ACCUMULATE = 4,
+  SITE_GATHER = 5,
+  SITE_STATE_LOGICAL = 6,
+  SITE_NORM1_MASKED = 7,
+  SITE_UPDATE_MASKED = 8,
+  SITE_AR_CHECK = 9,
+  SITE_COUNT = 10
+};
 
 // Programmatic dependent launch between the path's kernels: measured on
 // GB300 (67M workload, back-to-back steps) at 0.6248 ms/step against 0.6214
@@ -182,6 +204,7 @@ struct ReduceLaunch {
   float* partials;  // nullptr: no norm epilogue
   int32_t unit_begin, unit_end;
   int64_t state_base, rank_base;
+  int64_t state_len, rank_len;  // elements reachable from acc and from each rank pointer
   int32_t accumulate;
   int32_t max_ctas = 0;  // cap on the persistent grid (0: one CTA per SM)
 };

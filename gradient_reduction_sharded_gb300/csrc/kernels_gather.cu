@@ -66,17 +66,28 @@ struct GatherArgs {
   const uint16_t* params;
   const GatherJob* jobs;
   const int32_t* chunk_job;
+  int* flags;
+  int64_t n_state;       // elements of params
+  int32_t n_jobs;
   int32_t tensor_begin;  // dst[0] is this tensor
+  int32_t tensor_end;
   int64_t chunk_begin;
 };
 
 __global__ void __launch_bounds__(GATHER_THREADS) gather_kernel(const __grid_constant__ GatherArgs a) {
   const int64_t chunk = a.chunk_begin + blockIdx.x;
-  const GatherJob jb = a.jobs[a.chunk_job[chunk]];
+  const int32_t j = a.chunk_job[chunk];
+  if (!GRS_CHECK(j >= 0 && j < a.n_jobs, a.flags, SITE_GATHER)) return;
+  const GatherJob jb = a.jobs[j];
+  if (!GRS_CHECK(jb.tensor >= a.tensor_begin && jb.tensor < a.tensor_end, a.flags, SITE_GATHER)) return;
   uint16_t* dbase = a.dst[jb.tensor - a.tensor_begin];
   if (dbase == nullptr) return;
   const int64_t off = (chunk - jb.chunk0) * GATHER_CHUNK;
   const int64_t rem = jb.len - off;
+  if (!GRS_CHECK(off >= 0 && rem > 0 && jb.dst >= 0 && jb.src >= 0 &&
+                     jb.src + off + (rem < GATHER_CHUNK ? rem : GATHER_CHUNK) <= a.n_state,
+                 a.flags, SITE_GATHER))
+    return;
   block_copy(a.params + jb.src + off, dbase + jb.dst + off, rem < GATHER_CHUNK ? rem : GATHER_CHUNK);
 }
 
@@ -86,11 +97,20 @@ template <bool kToLogical>
 __global__ void __launch_bounds__(GATHER_THREADS) state_logical_kernel(const GatherJob* __restrict__ jobs,
                                                                         const int32_t* __restrict__ chunk_job,
                                                                         const float* __restrict__ src_base,
-                                                                        float* __restrict__ dst_base) {
+                                                                        float* __restrict__ dst_base, int32_t n_jobs,
+                                                                        int64_t n_state, int64_t n_logical,
+                                                                        int* __restrict__ flags) {
   const int64_t chunk = blockIdx.x;
-  const GatherJob jb = jobs[chunk_job[chunk]];
+  const int32_t j = chunk_job[chunk];
+  if (!GRS_CHECK(j >= 0 && j < n_jobs, flags, SITE_STATE_LOGICAL)) return;
+  const GatherJob jb = jobs[j];
   const int64_t off = (chunk - jb.chunk0) * GATHER_CHUNK;
   const int64_t rem = jb.len - off;
+  if (!GRS_CHECK(off >= 0 && rem > 0 && jb.src >= 0 && jb.logical >= 0 &&
+                     jb.src + off + (rem < GATHER_CHUNK ? rem : GATHER_CHUNK) <= n_state &&
+                     jb.logical + off + (rem < GATHER_CHUNK ? rem : GATHER_CHUNK) <= n_logical,
+                 flags, SITE_STATE_LOGICAL))
+    return;
   block_copy(src_base + (kToLogical ? jb.src : jb.logical) + off,
              dst_base + (kToLogical ? jb.logical : jb.src) + off, rem < GATHER_CHUNK ? rem : GATHER_CHUNK);
 }
@@ -115,6 +135,7 @@ __global__ void bounded_wait_selftest_kernel(int* flags, uint64_t limit_ns) {
 struct ArCheckArgs {
   const void* ranks[GRS_MAX_WORLD];
   const UnitDesc* unit;  // the ALREADY_REDUCED bucket's (single) row
+  int64_t rank_len;      // elements of each rank buffer
   int32_t world;
   int32_t esize;
   int* flags;
@@ -125,6 +146,8 @@ __global__ void __launch_bounds__(256) check_already_reduced_kernel(const __grid
   const int64_t el = static_cast<int64_t>(blockIdx.x) * UPD_T + int64_t(threadIdx.x) * 8;
   if (el >= ud->used) return;
   const int64_t n = ud->used - el < 8 ? ud->used - el : 8;
+  if (!GRS_CHECK(el >= 0 && ud->rank_off >= 0 && ud->rank_off + el + n <= a.rank_len, a.flags, SITE_AR_CHECK))
+    return;
   const int64_t base = (ud->rank_off + el) * a.esize;
   const uint8_t* r0 = static_cast<const uint8_t*>(a.ranks[0]) + base;
   bool same = true;
@@ -143,6 +166,7 @@ int launch_check_already_reduced(const grs_plan* p, const void* const* ranks, vo
   a.world = p->world;
   a.esize = p->grad_esize;
   a.flags = p->d_flags;
+  a.rank_len = p->n_rank_pad;
   for (const Bucket& bk : p->buckets) {
     if (bk.tag != GRS_ALREADY_REDUCED || bk.used == 0) continue;
     a.unit = p->d_units + bk.unit0;
@@ -163,7 +187,8 @@ int launch_state_to_logical(const grs_plan* p, const float* state, float* logica
   if (p->n_gather_chunks <= 0) return 0;
   state_logical_kernel<true><<<static_cast<unsigned>(p->n_gather_chunks), GATHER_THREADS, 0,
                                static_cast<cudaStream_t>(stream)>>>(
-      p->d_jobs, p->d_chunk_job, state, logical);
+      p->d_jobs, p->d_chunk_job, state, logical, static_cast<int32_t>(p->jobs.size()), p->n_state_pad,
+      p->n_unique, p->d_flags);
   return static_cast<int>(cudaGetLastError());
 }
 
@@ -174,7 +199,8 @@ int launch_state_from_logical(const grs_plan* p, const float* logical, float* st
   if (p->n_gather_chunks <= 0) return 0;
   state_logical_kernel<false><<<static_cast<unsigned>(p->n_gather_chunks), GATHER_THREADS, 0,
                                 static_cast<cudaStream_t>(stream)>>>(
-      p->d_jobs, p->d_chunk_job, logical, state);
+      p->d_jobs, p->d_chunk_job, logical, state, static_cast<int32_t>(p->jobs.size()), p->n_state_pad,
+      p->n_unique, p->d_flags);
   return static_cast<int>(cudaGetLastError());
 }
 
@@ -193,7 +219,11 @@ int launch_gather(const grs_plan* p, const uint16_t* params, uint16_t* const* te
     a.params = params;
     a.jobs = p->d_jobs;
     a.chunk_job = p->d_chunk_job;
+    a.flags = p->d_flags;
+    a.n_state = p->n_state_pad;
+    a.n_jobs = static_cast<int32_t>(p->jobs.size());
     a.tensor_begin = t0;
+    a.tensor_end = t1;
     const int32_t job_begin = p->tensor_job0[t0];
     const int32_t job_end = p->tensor_job0[t1];
     if (job_end <= job_begin) continue;

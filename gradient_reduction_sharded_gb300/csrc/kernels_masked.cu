@@ -43,12 +43,13 @@ struct Segs {
   const int64_t* start;
   const int32_t* tensor;
   const int32_t* bucket_seg0;
+  int32_t n_tensors;  // length of the per-tensor arrays (used mask, steps, factors)
 };
 
 __global__ void __launch_bounds__(MNORM_THREADS) norm_pass1_masked_kernel(
     const float* __restrict__ acc, const UnitDesc* __restrict__ units, const int64_t* __restrict__ prefix,
     int32_t n_units, int64_t n_tiles, Segs sg, const uint8_t* __restrict__ used_mask,
-    float* __restrict__ partials) {
+    float* __restrict__ partials, int64_t n_state, int* __restrict__ flags) {
   __shared__ float wp[MNORM_THREADS / 32];
   const int lane = threadIdx.x & 31;
   const int w = threadIdx.x >> 5;
@@ -58,7 +59,8 @@ __global__ void __launch_bounds__(MNORM_THREADS) norm_pass1_masked_kernel(
     const int64_t T = ud->red_T;
     const int64_t e0 = (tile - ud->red_tile0) * T;
     const int64_t rem = ud->padded - e0;
-    const int n = static_cast<int>(rem < T ? rem : T);
+    int n = static_cast<int>(rem < T ? rem : T);
+    if (!GRS_CHECK(e0 >= 0 && n > 0 && ud->state_off + e0 + n <= n_state, flags, SITE_NORM1_MASKED)) n = 0;
     const float* src = acc + ud->state_off + e0;
     const int lo = __ldg(sg.bucket_seg0 + ud->bucket), hi = __ldg(sg.bucket_seg0 + ud->bucket + 1);
     float psum = 0.0f;
@@ -75,7 +77,8 @@ __global__ void __launch_bounds__(MNORM_THREADS) norm_pass1_masked_kernel(
           continue;
         }
         while (s + 1 < hi && __ldg(sg.start + s + 1) <= e + q) ++s;
-        if (!__ldg(used_mask + __ldg(sg.tensor + s))) o[q] = 0.0f;
+        const int32_t t = __ldg(sg.tensor + s);
+        if (!GRS_CHECK(t >= 0 && t < sg.n_tensors, flags, SITE_NORM1_MASKED) || !__ldg(used_mask + t)) o[q] = 0.0f;
       }
 #pragma unroll
       for (int q = 0; q < 8; ++q) psum = __fmaf_rn(o[q], o[q], psum);
@@ -123,6 +126,8 @@ struct MaskedArgs {
   Segs sg;
   const uint8_t* used_mask;
   const float2* factors;
+  int* flags;
+  int64_t n_state;  // elements of acc, master, m, v and params
   int32_t n_units;
   float decay, b1, omb1, b2, omb2, eps;
   float max_norm;
@@ -146,6 +151,7 @@ __global__ void __launch_bounds__(MUPD_THREADS) update_masked_kernel(const __gri
   if (el >= ud->padded) return;
   const int64_t i = ud->state_off + el;
   const int64_t used = ud->used;
+  if (!GRS_CHECK(i >= 0 && i + 8 <= a.n_state, a.flags, SITE_UPDATE_MASKED)) return;
   const int lo = __ldg(a.sg.bucket_seg0 + ud->bucket), hi = __ldg(a.sg.bucket_seg0 + ud->bucket + 1);
   int s = el < used ? find_seg(a.sg.start, lo, hi, el) : lo;
 
@@ -173,7 +179,7 @@ __global__ void __launch_bounds__(MUPD_THREADS) update_masked_kernel(const __gri
     }
     while (s + 1 < hi && __ldg(a.sg.start + s + 1) <= e) ++s;
     const int32_t t = __ldg(a.sg.tensor + s);
-    write[q] = __ldg(a.used_mask + t) != 0;
+    write[q] = GRS_CHECK(t >= 0 && t < a.sg.n_tensors, a.flags, SITE_UPDATE_MASKED) && __ldg(a.used_mask + t) != 0;
     all = all && write[q];
     if (!write[q]) continue;  // no gradient this step: state stays
     const float2 f = a.factors[t];
@@ -223,7 +229,8 @@ int launch_norm_masked(const grs_plan* p, const float* acc, int32_t n_micro, con
                                                                     : int64_t(p->sm_count) * 16;
     norm_pass1_masked_kernel<<<static_cast<unsigned>(grid), MNORM_THREADS, 0, s>>>(
         acc, p->d_units, p->d_red_prefix, static_cast<int32_t>(p->units.size()), p->n_red_tiles,
-        Segs{p->d_seg_start, p->d_seg_tensor, p->d_bucket_seg0}, used, partials);
+        Segs{p->d_seg_start, p->d_seg_tensor, p->d_bucket_seg0, static_cast<int32_t>(p->numel.size())}, used, partials,
+        p->n_state_pad, p->d_flags);
     const int e = static_cast<int>(cudaGetLastError());
     if (e != 0) return e;
   }
@@ -249,9 +256,11 @@ int launch_update_masked(const grs_plan* p, const grs_adamw* hp, const double* d
   a.norm_sq = d_norm_sq;
   a.units = p->d_units;
   a.prefix = p->d_upd_prefix;
-  a.sg = Segs{p->d_seg_start, p->d_seg_tensor, p->d_bucket_seg0};
+  a.sg = Segs{p->d_seg_start, p->d_seg_tensor, p->d_bucket_seg0, static_cast<int32_t>(p->numel.size())};
   a.used_mask = used;
   a.factors = factors;
+  a.flags = p->d_flags;
+  a.n_state = p->n_state_pad;
   a.n_units = static_cast<int32_t>(p->units.size());
   const double lr = hp->lr, wd = hp->weight_decay;
   a.decay = static_cast<float>(1.0 - lr * wd);

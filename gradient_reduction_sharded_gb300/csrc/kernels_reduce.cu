@@ -70,6 +70,10 @@ struct ReduceArgs {
   int* flags;
   int64_t state_base;
   int64_t rank_base;
+  int64_t state_len;    // elements reachable from acc
+  int64_t rank_len;     // elements reachable from each rank pointer
+  int64_t n_partials;   // tiles of the plan (the partials array's length)
+  int32_t world;
   int64_t tile_begin;
   int64_t tile_end;
   int32_t unit_begin;
@@ -179,7 +183,7 @@ __global__ void __launch_bounds__(RED_THREADS, GRS_RED_CTAS_PER_SM) reduce_kerne
         do {
           ++u;
           u_next = __ldg(a.prefix + u + 1);
-        } while (tile >= u_next);
+        } while (tile >= u_next && (!GRS_CHECKED || u + 1 < a.unit_end));
         ud = a.units[u];
       }
       const int64_t T = ud.red_T;
@@ -191,6 +195,22 @@ __global__ void __launch_bounds__(RED_THREADS, GRS_RED_CTAS_PER_SM) reduce_kerne
       const uint32_t grad_bytes = static_cast<uint32_t>(ud.g_count) * static_cast<uint32_t>(n) * ESZ;
       const uint32_t bytes = grad_bytes + (a.accumulate ? static_cast<uint32_t>(n) * 4u : 0u);
       const int64_t out_off = ud.state_off - a.state_base + e0;
+      const int64_t roff = ud.rank_off - a.rank_base + e0;
+#if GRS_CHECKED
+      {
+        // Uniform across the warp: every lane leaves together.
+        const int64_t last_rank = int64_t(ud.g_start) + int64_t(ud.g_count - 1) * ud.g_stride;
+        const bool in = u < a.unit_end && e0 >= 0 && n > 0 && (n & 7) == 0 && e0 + n <= ud.padded &&
+                        bytes <= static_cast<uint32_t>(a.stage_bytes) && out_off >= 0 &&
+                        out_off + n <= a.state_len && roff >= 0 && roff + n <= a.rank_len && ud.g_count >= 1 &&
+                        ud.g_start >= 0 && last_rank < a.world && (a.partials == nullptr || tile < a.n_partials);
+        if (!GRS_CHECK(in, a.flags, SITE_REDUCE)) {
+          if (lane == 0) *abort_flag = 1;  // consumers leave their waits
+          ok = false;
+          break;
+        }
+      }
+#endif
       int good = 1;
       if (lane == 0) good = mbar_wait_bounded(&empty[s], ph ^ 1u, a.flags, abort_flag) ? 1 : 0;
       good = __shfl_sync(0xffffffffu, good, 0);
@@ -211,7 +231,6 @@ __global__ void __launch_bounds__(RED_THREADS, GRS_RED_CTAS_PER_SM) reduce_kerne
         mbar_arrive_expect_tx(&full[s], bytes);
       }
       __syncwarp();
-      const int64_t roff = ud.rank_off - a.rank_base + e0;
       for (int i = lane; i < ud.g_count; i += 32)
         bulk_g2s(st + size_t(i) * n * ESZ, static_cast<const E*>(a.ranks[ud.g_start + i * ud.g_stride]) + roff,
                  static_cast<uint32_t>(n) * ESZ, &full[s], pol);
@@ -313,6 +332,10 @@ int launch_reduce(const grs_plan* p, const ReduceLaunch& l, void* stream) {
   a.flags = p->d_flags;
   a.state_base = l.state_base;
   a.rank_base = l.rank_base;
+  a.state_len = l.state_len;
+  a.rank_len = l.rank_len;
+  a.n_partials = p->n_red_tiles;
+  a.world = p->world;
   a.unit_begin = l.unit_begin;
   a.unit_end = l.unit_end;
   a.tile_begin = p->red_prefix[l.unit_begin];

@@ -39,7 +39,8 @@ __global__ void __launch_bounds__(NORM1_THREADS) norm_pass1_kernel(const float* 
                                                                    const UnitDesc* __restrict__ units,
                                                                    const int64_t* __restrict__ prefix,
                                                                    int32_t n_units, int64_t n_tiles,
-                                                                   float* __restrict__ partials) {
+                                                                   float* __restrict__ partials, int64_t n_state,
+                                                                   int* __restrict__ flags) {
   __shared__ float wp[NORM1_THREADS / 32];
   const int lane = threadIdx.x & 31;
   const int w = threadIdx.x >> 5;
@@ -51,7 +52,9 @@ __global__ void __launch_bounds__(NORM1_THREADS) norm_pass1_kernel(const float* 
     const int64_t T = ud->red_T;
     const int64_t e0 = (tile - ud->red_tile0) * T;
     const int64_t rem = ud->padded - e0;
-    const int n = static_cast<int>(rem < T ? rem : T);
+    int n = static_cast<int>(rem < T ? rem : T);
+    // (uniform over the block: the same tile)
+    if (!GRS_CHECK(e0 >= 0 && n > 0 && ud->state_off + e0 + n <= n_state, flags, SITE_NORM1)) n = 0;
     const float* src = acc + ud->state_off + e0;
     float psum = 0.0f;
     for (int c = threadIdx.x; c < (n >> 3); c += NORM1_THREADS) {
@@ -141,6 +144,8 @@ struct UpdateArgs {
   const double* norm_sq;
   const UnitDesc* units;
   const int64_t* prefix;
+  int* flags;
+  int64_t n_state;   // elements of acc, master, m, v and params
   int32_t n_units;
   float decay;       // 1 - lr * wd
   float b1, omb1;    // beta1, 1 - beta1
@@ -177,6 +182,7 @@ __global__ void __launch_bounds__(UPD_THREADS) update_kernel(const __grid_consta
   if (el >= ud->padded) return;
   const int64_t i = ud->state_off + el;
   const int64_t used = ud->used;
+  if (!GRS_CHECK(e0 >= 0 && i >= 0 && i + 8 <= a.n_state, a.flags, SITE_UPDATE)) return;
 
   const float4 g0 = __ldcs(reinterpret_cast<const float4*>(a.acc + i));
   const float4 g1 = __ldcs(reinterpret_cast<const float4*>(a.acc + i + 4));
@@ -223,13 +229,15 @@ __global__ void __launch_bounds__(UPD_THREADS) accumulate_kernel(float* __restri
                                                                  const UnitDesc* __restrict__ units,
                                                                  const int64_t* __restrict__ prefix,
                                                                  int32_t unit_begin, int32_t unit_end,
-                                                                 int64_t tile_begin, int64_t state_base) {
+                                                                 int64_t tile_begin, int64_t state_base,
+                                                                 int64_t state_len, int* __restrict__ flags) {
   const int64_t tile = tile_begin + blockIdx.x;
   const int u = find_unit(prefix, unit_begin, unit_end, tile);
   const UnitDesc* ud = units + u;
   const int64_t el = (tile - ud->upd_tile0) * UPD_T + int64_t(threadIdx.x) * 8;
   if (el >= ud->padded) return;
   const int64_t i = ud->state_off - state_base + el;
+  if (!GRS_CHECK(el >= 0 && i >= 0 && i + 8 <= state_len, flags, SITE_ACCUMULATE)) return;
   float4* a4 = reinterpret_cast<float4*>(acc + i);
   const float4* b4 = reinterpret_cast<const float4*>(mb + i);
   float4 x0 = a4[0], x1 = a4[1];
@@ -256,7 +264,8 @@ int launch_norm(const grs_plan* p, const float* acc, int32_t n_micro, void* work
     const int e = static_cast<int>(launch_k(norm_pass1_kernel, dim3(unsigned(grid)), dim3(NORM1_THREADS), 0, s,
                                             acc, static_cast<const UnitDesc*>(p->d_units),
                                             static_cast<const int64_t*>(p->d_red_prefix),
-                                            static_cast<int32_t>(p->units.size()), p->n_red_tiles, partials));
+                                            static_cast<int32_t>(p->units.size()), p->n_red_tiles, partials,
+                                            p->n_state_pad, p->d_flags));
     if (e != 0) return e;
   }
   return launch_norm_finish(p, n_micro, workspace, d_norm_sq, stream);
@@ -286,6 +295,8 @@ int launch_update(const grs_plan* p, const grs_adamw* hp, const double* d_norm_s
   a.norm_sq = d_norm_sq;
   a.units = p->d_units;
   a.prefix = p->d_upd_prefix;
+  a.flags = p->d_flags;
+  a.n_state = p->n_state_pad;
   a.n_units = static_cast<int32_t>(p->units.size());
   const double lr = hp->lr, b1 = hp->beta1, b2 = hp->beta2, wd = hp->weight_decay;
   const double bc1 = 1.0 - std::pow(b1, static_cast<double>(hp->step));
@@ -310,7 +321,8 @@ int launch_accumulate(const grs_plan* p, int32_t bucket, float* acc, const float
   if (t1 <= t0) return 0;
   accumulate_kernel<<<static_cast<unsigned>(t1 - t0), UPD_THREADS, 0,
                       static_cast<cudaStream_t>(stream)>>>(acc, mb, p->d_units, p->d_upd_prefix, ub, ue,
-                                                           t0, bk.state_off);
+                                                           t0, bk.state_off, int64_t(bk.copies) * bk.padded,
+                                                           p->d_flags);
   return static_cast<int>(cudaGetLastError());
 }
 

@@ -26,6 +26,8 @@ GRS_ERR_CUDA = 5
 GRS_ERR_TIMEOUT = 6
 GRS_ERR_NONFINITE = 7
 GRS_ERR_NO_DEVICE = 8
+GRS_ERR_BOUNDS = 9
+GRS_FEATURE_CHECKED = 1
 GRS_PLAN_HOST_ONLY = 1
 GRS_PLAN_FP32_GRADS = 2
 GRS_TENSOR_FROZEN = 1
@@ -122,6 +124,7 @@ _sig = {
     "grs_step_from_host": ([_vp, _P(grs_adamw), _P(_vp), _P(_vp), _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                             _vp, _vp, _vp], ctypes.c_int),
     "grs_last_error": ([], ctypes.c_char_p),
+    "grs_build_features": ([], ctypes.c_uint32),
 }
 for _name, (_args, _res) in _sig.items():
     _f = getattr(_lib, _name)
@@ -133,6 +136,10 @@ EXPORTED = tuple(_sig)
 
 def grs_last_error() -> str:
     return (_lib.grs_last_error() or b"").decode()
+
+
+def grs_build_features() -> int:
+    return int(_lib.grs_build_features())
 
 
 def _check(status: int, func: str):

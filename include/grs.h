@@ -84,7 +84,8 @@ typedef enum grs_status {
   GRS_ERR_CUDA = 5,                     /* CUDA runtime error (message set) */
   GRS_ERR_TIMEOUT = 6,                  /* a bounded device wait gave up    */
   GRS_ERR_NONFINITE = 7,                /* global gradient norm is NaN/Inf  */
-  GRS_ERR_NO_DEVICE = 8                 /* plan was created host-only       */
+  GRS_ERR_NO_DEVICE = 8,                /* plan was created host-only       */
+  GRS_ERR_BOUNDS = 9                    /* checked build: an index left its buffer (library bug) */
 } grs_status;
 
 /* grs_plan_create flags */
@@ -450,10 +451,20 @@ grs_status grs_state_to_logical(const grs_plan* plan, const float* state, float*
 grs_status grs_state_from_logical(const grs_plan* plan, const float* logical, float* state, void* stream);
 
 /* Synchronise `stream`, read and clear the plan's device flags.  Returns
+ * BOUNDS if a checked build (below) found an index outside its buffer,
  * TIMEOUT if a bounded device wait gave up, NONFINITE if a global norm was
  * NaN/Inf since the last check, INVALID_ARG if grs_check_already_reduced
  * found copies that differ, else OK (or CUDA). */
 grs_status grs_check_device_errors(const grs_plan* plan, void* stream);
+
+/* Build features of the loaded library.  GRS_FEATURE_CHECKED: compiled with
+ * GRS_CHECKED=1 — every kernel checks each index it derives against the
+ * extent of the buffer it addresses (the sizes this header documents for
+ * that call) before the access; a failed check skips the access and raises
+ * a device flag that grs_check_device_errors reports as BOUNDS (the message
+ * names the kernel).  Slower; for tests and debugging. */
+#define GRS_FEATURE_CHECKED 1u
+uint32_t grs_build_features(void);
 
 /* Message of the last failing call on this thread ("" if none). */
 const char* grs_last_error(void);

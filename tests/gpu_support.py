@@ -169,7 +169,12 @@ class Run:
     def close(self):
         if self.plan:
             torch.cuda.synchronize(self.dev)
-            grs().grs_plan_destroy(self.plan)
+            g = grs()
+            if g.grs_build_features() & g.GRS_FEATURE_CHECKED:
+                # checked build: no kernel may have left a buffer
+                st = g.grs_check_device_errors(self.plan, self.stream())
+                assert st != g.GRS_ERR_BOUNDS, g.grs_last_error()
+            g.grs_plan_destroy(self.plan)
             self.plan = None
 
     # ---------------------------------------------------------------- oracle side

@@ -44,6 +44,12 @@ def test_library_exports_every_declared_symbol(grs):
     assert set(names) <= set(grs.EXPORTED), set(names) - set(grs.EXPORTED)
 
 
+def test_default_build_is_not_the_checked_one(grs):
+    if os.environ.get("GRS_LIBRARY"):
+        pytest.skip("another build of the library is loaded")
+    assert grs.grs_build_features() & grs.GRS_FEATURE_CHECKED == 0
+
+
 def _compare_plan(grs, h, op, numels, owners):
     info = grs.grs_plan_query(h)
     assert info["n_buckets"] == op.n_buckets
