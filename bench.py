@@ -265,6 +265,7 @@ def run_gpu(args, rank, world_size, local_rank):
     red_ms = [e[0].elapsed_time(e[1]) for e in ev]
     nrm_ms = [e[1].elapsed_time(e[2]) for e in ev]
     upd_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    upd_total = sorted(e[0].elapsed_time(e[3]) for e in ev)
     clk = clocks.stop()
 
     # ---------------------------------------------------------------- gather
@@ -285,10 +286,12 @@ def run_gpu(args, rank, world_size, local_rank):
     hbm_peak = peaks.get("hbm_gbs", 6800.0)
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
     kern = {
-        "reduce": {"ms": statistics.mean(red_ms), "bytes": mb["reduce"] / w.n_micro,
-                   "launches_per_step": w.n_micro},
-        "update": {"ms": statistics.mean(upd_ms), "bytes": mb["update"], "launches_per_step": 1},
-        "norm": {"ms": statistics.mean(nrm_ms), "bytes": None, "launches_per_step": 1},
+        "reduce": {"ms": statistics.mean(red_ms), "ms_median": statistics.median(red_ms),
+                   "bytes": mb["reduce"] / w.n_micro, "launches_per_step": w.n_micro},
+        "update": {"ms": statistics.mean(upd_ms), "ms_median": statistics.median(upd_ms),
+                   "bytes": mb["update"], "launches_per_step": 1},
+        "norm": {"ms": statistics.mean(nrm_ms), "ms_median": statistics.median(nrm_ms), "bytes": None,
+                 "launches_per_step": 1},
     }
     # reduce: average per launch over the microbatches of a step
     kern["reduce"]["ms_per_launch"] = kern["reduce"]["ms"] / w.n_micro
@@ -314,6 +317,9 @@ def run_gpu(args, rank, world_size, local_rank):
         "gather": gather,
         "gpu_launches": u.launches_per_step * K,
         "kernel_timing": "second region of K steps with CUDA events between the kernels",
+        "per_update_ms": {"median": statistics.median(upd_total), "min": upd_total[0],
+                          "max": upd_total[-1],
+                          "note": "second region, one update per event pair (events between kernels add a few us)"},
         "clocks": clk,
         "device_status": status,
     }
