@@ -36,26 +36,39 @@ METRIC = "ms per optimizer update (reduce+clip+AdamW)"
 UNIT = "ms/update"
 
 
-def mandatory_bytes(op, n_micro: int, world: int) -> dict:
-    """Algorithmic bytes of one update, per kernel.
-    Per unique padded element with reduction group R_e: reduce reads
-    2*M*R_e, writes acc 4 (first microbatch) or reads+writes 8 (later ones);
-    the update reads acc, master, m, v (16) and writes master, m, v (12) and
-    the bf16 parameter (2)."""
-    red = 0
-    n_state = 0
+def mandatory_bytes(buckets, n_micro: int, grad_bytes: int = 2) -> dict:
+    """Algorithmic bytes of one update, per kernel, from the bucket geometry
+    (one dict per bucket: copies, padded, group_size = R_e, the ranks reduced
+    per output element: R for REPLICA_AVG/PARTIAL_SUM, dp for LOCAL_SHARD, 1
+    for ALREADY_REDUCED).  Per unique padded element: the reduction reads
+    grad_bytes*M*R_e and writes acc 4 (first microbatch) or reads+writes it 8
+    (later ones); the update reads acc, master, m, v (16) and writes master,
+    m, v (12) and the bf16 parameter (2)."""
+    red = upd = last = 0
+    for d in buckets:
+        elems = int(d["copies"]) * int(d["padded"])
+        ge = int(d["group_size"])
+        red += elems * (grad_bytes * n_micro * ge + 4 + 8 * (n_micro - 1))
+        upd += 30 * elems
+        last += elems * (grad_bytes * ge + (4 if n_micro == 1 else 8))
+    return {"reduce": red, "update": upd, "total": red + upd, "reduce_last_mb": last}
+
+
+def library_buckets(grs, plan) -> list:
+    """The bucket geometry of a libgrs plan (grs_bucket_info per bucket)."""
+    nb = grs.grs_plan_query(plan)["n_buckets"]
+    return [grs.grs_bucket_info(plan, b) for b in range(nb)]
+
+
+def oracle_buckets(op) -> list:
+    """The same geometry from the oracle's own plan (CPU legs only)."""
+    out = []
     for b in range(op.n_buckets):
         tag = int(op.b_tag[b])
-        re = world if tag in (0, 1) else (op.dp if tag == 2 else 1)
-        elems = op.copies(b) * int(op.b_padded[b])
-        n_state += elems
-        red += elems * (2 * n_micro * re + 4 + 8 * (n_micro - 1))
-    return {"reduce": red, "update": 30 * n_state, "total": red + 30 * n_state,
-            "reduce_last_mb": sum(op.copies(b) * int(op.b_padded[b]) *
-                                  (2 * (world if int(op.b_tag[b]) in (0, 1) else
-                                        (op.dp if int(op.b_tag[b]) == 2 else 1)) +
-                                   (4 if n_micro == 1 else 8))
-                                  for b in range(op.n_buckets))}
+        ge = op.world if tag in (0, 1) else (op.dp if tag == 2 else 1)
+        out.append({"tag": tag, "copies": op.copies(b), "padded": int(op.b_padded[b]),
+                    "used": int(op.b_used[b]), "group_size": ge})
+    return out
 
 
 # --------------------------------------------------------------------------- clocks
@@ -142,20 +155,46 @@ def job_value(ms_per_step_max: float, world_size: int) -> float:
 
 
 # --------------------------------------------------------------------------- GPU arm
-class GpuUpdate:
-    """All device buffers of one workload and the three calls of one update."""
+# Variants of the update (the pages' validation list): the same workload with
+# fp32 rank gradients; with tensors that have no gradient this step; with
+# frozen tensors; or with a trailing accumulation window of fewer
+# microbatches.  The patterns are fixed and stated in the JSON line.
+VARIANTS = ("plain", "fp32-grads", "unused", "frozen")
 
-    def __init__(self, w: workloads.Workload, device):
+
+def unused_pattern(n_tensors: int) -> list:
+    """Tensors without a gradient this step: every 7th, starting at index 3."""
+    return [0 if i % 7 == 3 else 1 for i in range(n_tensors)]
+
+
+def frozen_pattern(n_tensors: int) -> list:
+    """Frozen tensors: the first quarter in model order (the lowest layers)."""
+    return [1 if i < n_tensors // 4 else 0 for i in range(n_tensors)]
+
+
+class GpuUpdate:
+    """All device buffers of one workload and the calls of one update."""
+
+    def __init__(self, w: workloads.Workload, device, variant: str = "plain", window: int = 0):
         import torch
         from gradient_reduction_sharded_gb300 import grs
         self.torch, self.grs, self.w, self.dev = torch, grs, w, device
-        self.plan = grs.grs_plan_create(w.numels, w.owners, w.world, w.tp, w.dp_replicate,
-                                        w.dp_shard, w.bucket_bytes)
+        self.variant = variant
+        self.n_micro = window if window > 0 else w.n_micro
+        if self.n_micro > w.n_micro:
+            raise ValueError(f"window {self.n_micro} > the workload's {w.n_micro} microbatches")
+        n = len(w.numels)
+        self.tensor_flags = frozen_pattern(n) if variant == "frozen" else None
+        self.grad_bytes = 4 if variant == "fp32-grads" else 2
+        flags = grs.GRS_PLAN_FP32_GRADS if variant == "fp32-grads" else 0
+        self.plan = grs.grs_plan_create_ex(w.numels, w.owners, self.tensor_flags, w.world, w.tp,
+                                           w.dp_replicate, w.dp_shard, w.bucket_bytes, flags)
         self.info = grs.grs_plan_query(self.plan)
+        self.buckets = library_buckets(grs, self.plan)
         nrp, nsp = self.info["n_rank_pad"], self.info["n_state_pad"]
-        self.grads = [[workloads.normal_bf16(nrp, w.grad_std, workloads.grad_seed(w.cid, j, k),
-                                             device=device)
-                       for k in range(w.world)] for j in range(w.n_micro)]
+        gen = workloads.normal_f32 if variant == "fp32-grads" else workloads.normal_bf16
+        self.grads = [[gen(nrp, w.grad_std, workloads.grad_seed(w.cid, j, k), device=device)
+                       for k in range(w.world)] for j in range(self.n_micro)]
         self.ptrs = [[t.data_ptr() for t in mb] for mb in self.grads]
         self.acc = torch.empty(nsp, dtype=torch.float32, device=device)
         self.master = workloads.normal_f32(nsp, w.master_std, workloads.master_seed(w.cid),
@@ -167,29 +206,61 @@ class GpuUpdate:
                               device=device)
         self.norm = torch.zeros(1, dtype=torch.float64, device=device)
         self.stream = torch.cuda.current_stream(device).cuda_stream
-        self.op = None
         self.step_no = 0
-        # kernels per step: one reduction per microbatch, the norm finish, the update
-        self.launches_per_step = w.n_micro + 2
+        self.used = None
+        if variant == "unused":
+            self.used_list = unused_pattern(n)
+            self.used = torch.tensor(self.used_list, dtype=torch.uint8, device=device)
+            self.tensor_steps = torch.zeros(n, dtype=torch.int32, device=device)
+        # kernels per step: one reduction per microbatch, the norm finish and the
+        # update; the masked path adds its norm pass and the per-tensor factors
+        self.launches_per_step = self.n_micro + (4 if self.used is not None else 2)
+
+    def algorithmic_bytes(self) -> dict:
+        """Per-kernel algorithmic bytes of one update of this variant."""
+        mb = mandatory_bytes(self.buckets, self.n_micro, self.grad_bytes)
+        mb["norm"] = 0  # fused into the last reduction
+        if self.used is not None:
+            # Tensors without a gradient need no norm read and no update;
+            # the reduction does not know the mask and runs as in the plain case.
+            idle = sum(n for n, u in zip(self.w.numels, self.used_list) if not u)
+            live = self.info["n_state_pad"] - idle
+            mb["norm"] = 4 * (live - (self.info["n_state_pad"] - self.info["n_unique"]))
+            mb["update"] = 30 * live
+            mb["total"] = mb["reduce"] + mb["norm"] + mb["update"]
+        return mb
 
     def reduce(self):
-        g, w = self.grs, self.w
-        for j in range(w.n_micro):
+        g = self.grs
+        emit = self.used is None
+        for j in range(self.n_micro):
             g.grs_reduce_all(self.plan, self.ptrs[j], self.acc.data_ptr(), int(j > 0),
-                             int(j == w.n_micro - 1), self.ws.data_ptr(), self.stream)
+                             int(emit and j == self.n_micro - 1), self.ws.data_ptr(), self.stream)
 
     def norm_sq(self):
-        self.grs.grs_grad_norm_sq(self.plan, self.acc.data_ptr(), self.w.n_micro,
-                                  self.ws.data_ptr(), 1, self.norm.data_ptr(), self.stream)
+        if self.used is not None:
+            self.grs.grs_grad_norm_sq_masked(self.plan, self.acc.data_ptr(), self.n_micro,
+                                             self.used.data_ptr(), self.ws.data_ptr(),
+                                             self.norm.data_ptr(), self.stream)
+        else:
+            self.grs.grs_grad_norm_sq(self.plan, self.acc.data_ptr(), self.n_micro,
+                                      self.ws.data_ptr(), 1, self.norm.data_ptr(), self.stream)
 
     def adamw(self):
         a = self.w.adamw
         self.step_no += 1
         hp = self.grs.make_adamw(a.lr, a.beta1, a.beta2, a.eps, a.weight_decay, a.max_norm,
-                                 self.step_no, self.w.n_micro)
-        self.grs.grs_clip_adamw_step(self.plan, hp, self.norm.data_ptr(), self.acc.data_ptr(),
-                                     self.master.data_ptr(), self.m.data_ptr(), self.v.data_ptr(),
-                                     self.params.data_ptr(), self.stream)
+                                 self.step_no, self.n_micro)
+        if self.used is not None:
+            self.grs.grs_clip_adamw_step_masked(self.plan, hp, self.norm.data_ptr(), self.acc.data_ptr(),
+                                                self.master.data_ptr(), self.m.data_ptr(),
+                                                self.v.data_ptr(), self.params.data_ptr(),
+                                                self.used.data_ptr(), self.tensor_steps.data_ptr(),
+                                                self.ws.data_ptr(), self.stream)
+        else:
+            self.grs.grs_clip_adamw_step(self.plan, hp, self.norm.data_ptr(), self.acc.data_ptr(),
+                                         self.master.data_ptr(), self.m.data_ptr(), self.v.data_ptr(),
+                                         self.params.data_ptr(), self.stream)
 
     def step(self):
         self.reduce()
@@ -203,15 +274,12 @@ class GpuUpdate:
 
 def run_gpu(args, rank, world_size, local_rank):
     import torch
-    import oracle  # CPU baseline leg only
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
     w = workloads.get(args.workload, args.blocks)
-    op = oracle.plan(w.numels, w.owners, w.world, w.tp, w.dp_replicate, w.dp_shard,
-                     w.bucket_bytes)
-    mb = mandatory_bytes(op, w.n_micro, w.world)
-    u = GpuUpdate(w, device)
-    u.op = op
+    u = GpuUpdate(w, device, args.variant, args.window)
+    mb = u.algorithmic_bytes()
+    plain = args.variant == "plain" and u.n_micro == w.n_micro
     clocks = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[0])
                           if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit()
                           else local_rank)
@@ -268,11 +336,12 @@ def run_gpu(args, rank, world_size, local_rank):
     upd_total = sorted(e[0].elapsed_time(e[3]) for e in ev)
     clk = clocks.stop()
 
+    # The gather and the end-to-end path run on the plain update only.
     # ---------------------------------------------------------------- gather
-    gather = run_gather(u, args, torch)
+    gather = run_gather(u, args, torch) if plain else None
 
     # ---------------------------------------------------------------- e2e
-    e2e = None if args.no_e2e else run_e2e(u, args, torch)
+    e2e = None if (args.no_e2e or not plain) else run_e2e(u, args, torch)
 
     status = u.grs.grs_check_device_errors(u.plan, u.stream)
     u.close()
@@ -285,27 +354,36 @@ def run_gpu(args, rank, world_size, local_rank):
         pass
     hbm_peak = peaks.get("hbm_gbs", 6800.0)
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
+    M = u.n_micro
+    masked = u.used is not None
     kern = {
         "reduce": {"ms": statistics.mean(red_ms), "ms_median": statistics.median(red_ms),
-                   "bytes": mb["reduce"] / w.n_micro, "launches_per_step": w.n_micro},
+                   "bytes": mb["reduce"] / M, "launches_per_step": M},
         "update": {"ms": statistics.mean(upd_ms), "ms_median": statistics.median(upd_ms),
-                   "bytes": mb["update"], "launches_per_step": 1},
-        "norm": {"ms": statistics.mean(nrm_ms), "ms_median": statistics.median(nrm_ms), "bytes": None,
-                 "launches_per_step": 1},
+                   "bytes": mb["update"], "launches_per_step": 2 if masked else 1},
+        "norm": {"ms": statistics.mean(nrm_ms), "ms_median": statistics.median(nrm_ms),
+                 "bytes": mb["norm"] if masked else None, "launches_per_step": 2 if masked else 1},
     }
     # reduce: average per launch over the microbatches of a step
-    kern["reduce"]["ms_per_launch"] = kern["reduce"]["ms"] / w.n_micro
+    kern["reduce"]["ms_per_launch"] = kern["reduce"]["ms"] / M
     kern["update"]["ms_per_launch"] = kern["update"]["ms"]
-    dom = "reduce" if kern["reduce"]["ms"] >= kern["update"]["ms"] else "update"
+    kern["norm"]["ms_per_launch"] = kern["norm"]["ms"]
+    dom = max(("reduce", "update", "norm"),
+              key=lambda k: kern[k]["ms"] if kern[k]["bytes"] else -1.0)
     dk = kern[dom]
     achieved = dk["bytes"] / (dk["ms_per_launch"] * 1e-3) / 1e9
-    traffic = load_traffic(dom, w)
+    traffic = load_traffic(dom, w, u.variant)
+    if masked:
+        kern["update"]["note"] = "per-tensor factors kernel + masked update"
+        kern["norm"]["note"] = "masked norm pass + norm finish"
     result = {
         "metric": METRIC, "value": job_value(ms_step, world_size), "unit": UNIT, "n_gpus": world_size,
         "steps": K, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": dict(w.describe(), grad_dtype="bf16", l2="inputs larger than L2 (no flush)",
-                       parallelism=f"replicas{world_size}" if world_size > 1 else "1 GPU, simulated ranks"),
+        "config": dict(w.describe(), grad_dtype="fp32" if u.grad_bytes == 4 else "bf16",
+                       l2="inputs larger than L2 (no flush)",
+                       parallelism=f"replicas{world_size}" if world_size > 1 else "1 GPU, simulated ranks",
+                       **variant_config(u)),
         "achieved_gbs_total": mb["total"] / (ms_step * world_size * 1e-3) / 1e9 if world_size == 1
         else mb["total"] / (ms_step * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm_peak,
@@ -324,8 +402,32 @@ def run_gpu(args, rank, world_size, local_rank):
         "device_status": status,
     }
     if rank == 0 and world_size == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(w, op, mb, args)
+        if plain:
+            result["cpu_baseline"] = cpu_baseline(w, mb, args)
+        else:
+            result["cpu_baseline"] = cpu_baseline_variant(w, u, mb, args)
     return result
+
+
+def variant_config(u: GpuUpdate) -> dict:
+    """The variant's keys for the JSON line's config (none for the plain update)."""
+    out = {}
+    if u.variant != "plain":
+        out["variant"] = u.variant
+    if u.n_micro != u.w.n_micro:
+        out["window"] = {"microbatches": u.n_micro, "of": u.w.n_micro}
+        out["microbatches"] = u.n_micro
+    if u.variant == "unused":
+        n_off = u.used_list.count(0)
+        out["unused"] = {"pattern": "every 7th tensor from index 3 has no gradient",
+                         "tensors": n_off,
+                         "elements": sum(n for n, k in zip(u.w.numels, u.used_list) if not k)}
+    if u.variant == "frozen":
+        out["frozen"] = {"pattern": "first quarter of the tensors in model order",
+                         "tensors": sum(u.tensor_flags),
+                         "elements": sum(n for n, f in zip(u.w.numels, u.tensor_flags) if f)}
+        out["params_trained"] = u.info["n_unique"]
+    return out
 
 
 def run_gather(u: GpuUpdate, args, torch):
@@ -369,10 +471,9 @@ def run_e2e(u: GpuUpdate, args, torch):
     out_params = torch.empty(u.params.numel(), dtype=torch.int16).pin_memory()
     out_norm = torch.empty(1, dtype=torch.float64).pin_memory()
     h2d = 0
-    op = u.op
-    for b in range(op.n_buckets):
-        nread = 1 if int(op.b_tag[b]) == 3 else W
-        h2d += M * nread * int(op.b_padded[b]) * 2
+    for d in u.buckets:  # ALREADY_REDUCED buckets copy rank 0's rows only
+        nread = 1 if int(d["tag"]) == 3 else W
+        h2d += M * nread * int(d["padded"]) * 2
     d2h = out_params.numel() * 2 + 8
     steps = max(3, min(args.steps, 10))
     a = w.adamw
@@ -402,7 +503,8 @@ def run_e2e(u: GpuUpdate, args, torch):
                     "reductions, bf16 parameters and norm read back"}
 
 
-KERNEL_SOURCES = ("kernels_reduce.cu", "kernels_update.cu", "device.cuh", "internal.h", "launch.cuh")
+KERNEL_SOURCES = ("kernels_reduce.cu", "kernels_update.cu", "kernels_masked.cu", "kernels_gather.cu",
+                  "device.cuh", "internal.h", "launch.cuh")
 
 
 def csrc_hash() -> str:
@@ -416,7 +518,7 @@ def csrc_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def load_traffic(kernel: str, w):
+def load_traffic(kernel: str, w, variant: str = "plain"):
     """DRAM bytes per launch from the committed ncu summary, or None when the
     workload was not captured or the kernels changed since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -427,50 +529,98 @@ def load_traffic(kernel: str, w):
         return None
     if t.get("csrc_sha256_16") != csrc_hash():
         return None
-    ent = t.get(f"{kernel}:{w.name}")
+    key = f"{kernel}:{w.name}" if variant == "plain" else f"{kernel}:{w.name}:{variant}"
+    ent = t.get(key)
     return None if ent is None else ent.get("bytes_per_launch")
 
 
 # --------------------------------------------------------------------------- CPU arm
-def _host_inputs(w, op, device=None):
-    """The workload's gradients as host uint16 arrays, generated exactly as the
-    GPU arm generates them (same seeds), one buffer per (microbatch, rank)."""
+def _host_inputs(w, n_rank_pad: int, n_micro: int = 0, fp32: bool = False, device=None):
+    """The workload's gradients as host arrays (uint16 bf16 bits, or float32
+    with fp32=True), generated exactly as the GPU arm generates them (same
+    seeds), one buffer per (microbatch, rank)."""
     import torch
     dev = device or ("cuda" if torch.cuda.is_available() else "cpu")
+    gen = workloads.normal_f32 if fp32 else workloads.normal_bf16
     out = []
-    for j in range(w.n_micro):
+    for j in range(n_micro or w.n_micro):
         row = []
         for k in range(w.world):
-            t = workloads.normal_bf16(op.n_rank_pad, w.grad_std, workloads.grad_seed(w.cid, j, k),
-                                      device=dev)
-            row.append(workloads.bf16_bits(t.cpu()))
+            t = gen(n_rank_pad, w.grad_std, workloads.grad_seed(w.cid, j, k), device=dev)
+            row.append(t.cpu().numpy() if fp32 else workloads.bf16_bits(t.cpu()))
             del t
         out.append(row)
     return out
 
 
-def _oracle_sample(w, op, host, buckets, threads=1):
+def _host_fetch(op, host, M):
+    """Bucket inputs [M][R][P] sliced from whole per-rank host buffers."""
+    def fetch(b):
+        ro, P = int(op.b_rank_off[b]), int(op.b_padded[b])
+        return np.stack([np.stack([h[ro:ro + P] for h in mb]) for mb in host[:M]])
+    return fetch
+
+
+def _device_bucket_inputs(op, grads, buckets, M, fp32):
+    """The sampled buckets' inputs [M][R][P] copied once from the GPU arm's own
+    device gradients (the same seeded bytes), so that only the sample is held
+    on the host."""
+    import torch
+    out = {}
+    for b in buckets:
+        ro, P = int(op.b_rank_off[b]), int(op.b_padded[b])
+        arr = np.stack([np.stack([g[ro:ro + P].view(torch.float32 if fp32 else torch.int16).cpu().numpy()
+                                  for g in mb]) for mb in grads[:M]])
+        out[b] = arr if fp32 else arr.view(np.uint16)
+    return out
+
+
+def _oracle_sample(w, op, host, buckets, threads=1, n_micro=0, used=None):
     """One oracle update restricted to `buckets` (reduce -> norm -> AdamW);
     with threads > 1 the buckets run in parallel (the oracle's C code drops
-    the GIL) and the norm is still summed in bucket order."""
+    the GIL) and the norm is still summed in bucket order.  With `used` (one
+    flag per tensor) tensors without a gradient add nothing to the norm and
+    are not updated."""
     import oracle
     from concurrent.futures import ThreadPoolExecutor
     a_ = w.adamw
     hp = (a_.lr, a_.beta1, a_.beta2, a_.eps, a_.weight_decay)
+    M = n_micro or w.n_micro
+
+    def rows(b):
+        """(row, lo, hi): the ranges of bucket b's tensors with a gradient."""
+        out = []
+        for i in range(len(op.numel)):
+            if int(op.t_bucket[i]) == b and used[i]:
+                o, n = int(op.t_offset[i]), op.per_rank(i)
+                out += [(t, o, o + n) for t in range(op.copies(b))]
+        return out
+
+    fetch = host.__getitem__ if isinstance(host, dict) else _host_fetch(op, host, M)
 
     def red(b):
-        ro, P = int(op.b_rank_off[b]), int(op.b_padded[b])
-        g = np.stack([np.stack([h[ro:ro + P] for h in mb]) for mb in host])
+        P = int(op.b_padded[b])
+        g = fetch(b)
         a = oracle.reduce_bucket(int(op.b_tag[b]), op.tp, op.dp_replicate, op.dp_shard, P,
                                  int(op.b_used[b]), g)
-        return a, oracle.norm_sq(a, w.n_micro)
+        if used is None:
+            return a, oracle.norm_sq(a, M)
+        ns = 0.0
+        for t, lo, hi in rows(b):
+            ns += oracle.norm_sq(a[t][lo:hi], M)
+        return a, ns
 
     def upd(args):
         b, a, c = args
-        P = int(op.b_padded[b])
-        z = np.zeros(P, np.float32)
-        for t in range(op.copies(b)):
-            oracle.adamw(a[t], int(op.b_used[b]), w.n_micro, c, hp, 1, z, z, z)
+        if used is None:
+            P = int(op.b_padded[b])
+            z = np.zeros(P, np.float32)
+            for t in range(op.copies(b)):
+                oracle.adamw(a[t], int(op.b_used[b]), M, c, hp, 1, z, z, z)
+            return
+        for t, lo, hi in rows(b):
+            z = np.zeros(hi - lo, np.float32)
+            oracle.adamw(a[t][lo:hi], hi - lo, M, c, hp, 1, z, z, z)
 
     with ThreadPoolExecutor(max(1, threads)) as ex:
         parts = list(ex.map(red, buckets))
@@ -502,22 +652,25 @@ def _sample_buckets(op, frac_target=0.35):
     return sorted(chosen)
 
 
-def _sample_bytes(op, buckets, n_micro, world):
-    tot = 0
-    for b in buckets:
-        tag = int(op.b_tag[b])
-        re = world if tag in (0, 1) else (op.dp if tag == 2 else 1)
-        elems = op.copies(b) * int(op.b_padded[b])
-        tot += elems * (2 * n_micro * re + 4 + 8 * (n_micro - 1) + 30)
-    return tot
+def _sample_bytes(op, buckets, n_micro, grad_bytes=2):
+    """Mandatory bytes of the sampled buckets (the plain update's formula)."""
+    geo = oracle_buckets(op)
+    return mandatory_bytes([geo[b] for b in buckets], n_micro, grad_bytes)["total"]
 
 
-def cpu_baseline(w, op, mb, args, host=None, target_s=10.0):
+def _oracle_plan(w, tensor_flags=None):
+    import oracle
+    return oracle.plan(w.numels, w.owners, w.world, w.tp, w.dp_replicate, w.dp_shard,
+                       w.bucket_bytes, tensor_flags)
+
+
+def cpu_baseline(w, mb, args, host=None, target_s=10.0):
     """The oracle as it stands, on this host: whole updates of the workload
     (every bucket: reduce -> norm -> AdamW), repeated until about target_s of
     CPU work, one thread; then the same with one thread per core (buckets in
     parallel)."""
-    host = host if host is not None else _host_inputs(w, op)
+    op = _oracle_plan(w)
+    host = host if host is not None else _host_inputs(w, op.n_rank_pad)
     buckets = list(range(op.n_buckets))
     reps, t0 = 0, time.perf_counter()
     while True:
@@ -538,16 +691,41 @@ def cpu_baseline(w, op, mb, args, host=None, target_s=10.0):
                           "note": f"one whole update, {min(nthr, op.n_buckets)} buckets in parallel"}}
 
 
+def cpu_baseline_variant(w, u, mb, args, target_s=10.0):
+    """The oracle on the variant's update (same plan flags, gradient type,
+    microbatch window and mask), one thread: whole updates when the update
+    moves at most 8 GB, otherwise one bucket per tag scaled to the whole
+    update by mandatory bytes.  Inputs: the GPU arm's own gradient bytes,
+    copied to the host once before the timing."""
+    op = _oracle_plan(w, u.tensor_flags)
+    M = u.n_micro
+    whole = mb["total"] <= 8e9
+    buckets = list(range(op.n_buckets)) if whole else _sample_buckets(op, frac_target=0.0)
+    host = _device_bucket_inputs(op, u.grads, buckets, M, u.grad_bytes == 4)
+    used = u.used_list if u.used is not None else None
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        _oracle_sample(w, op, host, buckets, n_micro=M, used=used)
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt >= target_s or reps >= 20:
+            break
+    scale = 1.0 if whole else mb["total"] / _sample_bytes(op, buckets, M, u.grad_bytes)
+    ms = dt * 1e3 / reps * scale
+    what = (f"{reps} whole updates of the variant" if whole else
+            f"{reps} updates of buckets {buckets} of {op.n_buckets}, scaled by bytes")
+    return {"value": ms, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{what}, one thread, {dt:.1f} s"}
+
+
 def run_reference(args, rank, world_size):
     """The oracle as the reference arm, on host cores, rank 0 only."""
-    import oracle
     w = workloads.get(args.workload, args.blocks)
-    op = oracle.plan(w.numels, w.owners, w.world, w.tp, w.dp_replicate, w.dp_shard,
-                     w.bucket_bytes)
-    mb = mandatory_bytes(op, w.n_micro, w.world)
-    host = _host_inputs(w, op)
+    op = _oracle_plan(w)
+    mb = mandatory_bytes(oracle_buckets(op), w.n_micro)
+    host = _host_inputs(w, op.n_rank_pad)
     buckets = _sample_buckets(op, frac_target=0.0)  # one bucket per tag: a bounded step
-    sb = _sample_bytes(op, buckets, w.n_micro, w.world)
+    sb = _sample_bytes(op, buckets, w.n_micro)
     for _ in range(args.warmup):
         _oracle_sample(w, op, host, buckets)
     t0 = time.perf_counter()
@@ -564,6 +742,167 @@ def run_reference(args, rank, world_size):
             "cpu_baseline": {"value": ms, "unit": UNIT, "cores": 1, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": ms, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def reshard_geometry(w):
+    """The reader geometry of the reshard measurement: HSDP -> FSDP (every DP
+    rank a shard) when the writer has replicas, else two replicas."""
+    dr, ds = w.dp_replicate, w.dp_shard
+    if dr > 1:
+        return w.tp, 1, dr * ds
+    if ds % 2 == 0:
+        return w.tp, 2, ds // 2
+    return w.tp, dr, ds
+
+
+def run_checkpoint(args):
+    """Checkpoint restore with reshard (a separate measurement, not the bench
+    line): master, m and v of the workload's plan moved to the canonical
+    logical order with the writer's plan (grs_state_to_logical) and into
+    another geometry's bucket layout (grs_state_from_logical).  Algorithmic
+    bytes per array: read + write 4 bytes per logical element for each
+    kernel (the reader also writes its padding zeros).  The end-to-end leg
+    saves the three arrays to shard files and loads them into the reader's
+    plan through checkpoint.save / checkpoint.load (host file I/O)."""
+    import shutil
+    import tempfile
+
+    import torch
+
+    from gradient_reduction_sharded_gb300 import checkpoint as ck
+    from gradient_reduction_sharded_gb300 import grs
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    w = workloads.get(args.workload, args.blocks)
+    tp, dr, ds = reshard_geometry(w)
+    spec_w = ck.PlanSpec(list(w.numels), list(w.owners), None, w.world, w.tp, w.dp_replicate,
+                         w.dp_shard, w.bucket_bytes)
+    spec_r = ck.PlanSpec(list(w.numels), list(w.owners), None, w.world, tp, dr, ds, w.bucket_bytes)
+    pw, pr = spec_w.create(), spec_r.create()
+    iw, ir = grs.grs_plan_query(pw), grs.grs_plan_query(pr)
+    N = iw["n_unique"]
+    names = ("master", "exp_avg", "exp_avg_sq")
+    src = {nm: workloads.normal_f32(iw["n_state_pad"], 0.02, 7_919 + w.cid + i, device=device)
+           for i, nm in enumerate(names)}
+    dst = {nm: torch.empty(ir["n_state_pad"], dtype=torch.float32, device=device) for nm in names}
+    logical = torch.empty(max(1, N), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device).cuda_stream
+    clocks = ClockSampler(0)
+    clocks.start()
+
+    def one(ev=None):
+        for nm in names:
+            if ev is not None:
+                ev[0].record()
+            grs.grs_state_to_logical(pw, src[nm].data_ptr(), logical.data_ptr(), stream)
+            if ev is not None:
+                ev[1].record()
+            grs.grs_state_from_logical(pr, logical.data_ptr(), dst[nm].data_ptr(), stream)
+            if ev is not None:
+                ev[2].record()
+                ev = ev[3:]
+
+    clocks.mark("load_start")
+    for _ in range(args.warmup):
+        one()
+    torch.cuda.synchronize()
+    K = args.steps
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(K):
+        one()
+    t1.record()
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / K
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(9)] for _ in range(K)]
+    for i in range(K):
+        one(evs[i])
+    torch.cuda.synchronize()
+    clocks.mark("load_end")
+    clk = clocks.stop()
+    to_ms = [e[3 * a].elapsed_time(e[3 * a + 1]) for e in evs for a in range(3)]
+    from_ms = [e[3 * a + 1].elapsed_time(e[3 * a + 2]) for e in evs for a in range(3)]
+    b_to = 8 * N
+    b_from = 8 * N + 4 * (ir["n_state_pad"] - N)
+    kern = {"state_to_logical": {"ms_per_launch": statistics.median(to_ms), "bytes": b_to,
+                                 "launches_per_step": 3},
+            "state_from_logical": {"ms_per_launch": statistics.median(from_ms), "bytes": b_from,
+                                   "launches_per_step": 3,
+                                   "note": "plus one padding-zero launch per call"}}
+    dom = max(kern, key=lambda k: kern[k]["ms_per_launch"])
+    achieved = kern[dom]["bytes"] / (kern[dom]["ms_per_launch"] * 1e-3) / 1e9
+    # correctness of what was timed: the reader's logical order equals the writer's
+    back = torch.empty_like(logical)
+    for nm in names:
+        grs.grs_state_to_logical(pr, dst[nm].data_ptr(), back.data_ptr(), stream)
+        grs.grs_state_to_logical(pw, src[nm].data_ptr(), logical.data_ptr(), stream)
+        torch.cuda.synchronize()
+        if not torch.equal(back, logical):
+            raise RuntimeError(f"reshard of {nm} does not round-trip")
+    # end to end through the checkpoint module: files on local disk
+    tmp = tempfile.mkdtemp(prefix="grs-bench-ckpt-")
+    try:
+        d = os.path.join(tmp, "ckpt")
+        torch.cuda.synchronize()
+        s0 = time.perf_counter()
+        ck.save(d, pw, spec_w, src, {"step": 1})
+        s1 = time.perf_counter()
+        ck.load(d, pr, dst)
+        s2 = time.perf_counter()
+        file_bytes = sum(os.path.getsize(os.path.join(d, f)) for f in os.listdir(d))
+    finally:
+        shutil.rmtree(tmp, ignore_errors=True)
+    status = grs.grs_check_device_errors(pr, stream)
+    grs.grs_plan_destroy(pw)
+    grs.grs_plan_destroy(pr)
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except OSError:
+        pass
+    hbm_peak = peaks.get("hbm_gbs", 6800.0)
+    res = {"metric": "ms per reshard restore of master, m and v (state -> logical -> other layout)",
+           "value": ms, "unit": "ms/restore", "n_gpus": 1, "steps": K, "warmup": args.warmup,
+           "ms_per_step": ms, "higher_is_better": False, "dtype": "f32", "data": "synthetic",
+           "config": {"workload": w.name, "params": N,
+                      "writer": {"tp": w.tp, "dp_replicate": w.dp_replicate, "dp_shard": w.dp_shard},
+                      "reader": {"tp": tp, "dp_replicate": dr, "dp_shard": ds},
+                      "arrays": len(names), "l2": "arrays larger than L2 (no flush)"},
+           "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm_peak,
+                        "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": load_traffic(dom, w, "checkpoint"),
+                        "peak_source": "measured" if "hbm_gbs" in peaks else "fallback",
+                        "algorithmic_bytes_per_launch": kern[dom]["bytes"]},
+           "kernels": kern,
+           "gpu_launches": 9 * K,
+           "e2e": {"save_ms": (s1 - s0) * 1e3, "load_ms": (s2 - s1) * 1e3, "file_bytes": file_bytes,
+                   "d2h_bytes": 4 * iw["n_state_pad"] * len(names),
+                   "h2d_bytes": 4 * iw["n_state_pad"] * len(names),
+                   "path": "checkpoint.save (D2H, shard files, digests, manifest, _SUCCESS) then "
+                           "checkpoint.load into the reader's plan (read, verify, H2D, two layout kernels)"},
+           "clocks": clk, "device_status": status}
+    if not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline_reshard(w, spec_r, src, names)
+    return res
+
+
+def cpu_baseline_reshard(w, spec_r, src, names, target_s=10.0):
+    """The oracle's layout functions on the same arrays, one thread."""
+    import oracle
+    opw = _oracle_plan(w)
+    opr = oracle.plan(spec_r.numels, spec_r.owners, spec_r.world, spec_r.tp, spec_r.dp_replicate,
+                      spec_r.dp_shard, spec_r.bucket_bytes)
+    host = {nm: src[nm].cpu().numpy() for nm in names}
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        for nm in names:
+            oracle.from_logical(opr, oracle.to_logical(opw, host[nm]))
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt >= target_s or reps >= 20:
+            break
+    return {"value": dt * 1e3 / reps, "unit": "ms/restore", "cores": 1, "kind": "oracle",
+            "sample": f"{reps} whole restores of the {len(names)} arrays, one thread, {dt:.1f} s"}
 
 
 def run_overlap(args):
@@ -673,6 +1012,13 @@ def main():
     ap.add_argument("--impl", default="grs", choices=["grs", "reference"])
     ap.add_argument("--soak", type=float, default=1.5, help="untimed seconds before timing")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--variant", default="plain", choices=VARIANTS,
+                    help="fp32-grads: fp32 rank gradients; unused: some tensors without a gradient "
+                         "(masked norm and update); frozen: some tensors frozen at plan time")
+    ap.add_argument("--checkpoint", action="store_true",
+                    help="measure checkpoint restore with reshard (layout kernels + files) instead")
+    ap.add_argument("--window", type=int, default=0,
+                    help="trailing accumulation window: reduce only the first M' microbatches, G = acc/M'")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -686,6 +1032,9 @@ def main():
         return
     if args.overlap:
         print(json.dumps(run_overlap(args)), flush=True)
+        return
+    if args.checkpoint:
+        print(json.dumps(run_checkpoint(args)), flush=True)
         return
     if world_size > 1:
         import torch

@@ -186,4 +186,66 @@ __device__ __forceinline__ double warp_sum(double x) {
   return x;
 }
 
+// Every element of a tile counts (the unmasked norm pass).
+struct KeepAll {
+  __device__ __forceinline__ bool operator()(int, int) const { return true; }
+};
+
+// Norm partial (sum of squares) of one reduction tile of nch 8-element
+// chunks, computed by ONE warp and bit-identical to the reduction's fused
+// epilogue, where RED_CWARPS consumer warps of 32 lanes share the tile:
+// consumer thread t = 32 v + l sums, in order, the chunks t, t + 32
+// RED_CWARPS, ... with fmaf(x, x, psum) over each chunk's 8 elements; each
+// warp's lanes are combined by warp_sum and the warps' sums folded in order
+// v = 0, 1, ...  Here the warp plays the consumer warps one after another
+// ("virtual warps"), with the loads of NW_BATCH of them in flight at once.
+// keep(c, q) == false zeros element 8c + q (a masked pass); virtual warps
+// without a chunk add +0 and are skipped.
+template <typename Keep>
+__device__ __forceinline__ float tile_partial_warp(const float* __restrict__ src, int nch, int lane, Keep& keep) {
+  constexpr int CT = 32 * RED_CWARPS;
+  constexpr int KMAX = static_cast<int>(RED_MAX_T / 8 / CT);  // chunks per consumer thread at most
+  constexpr int NW_BATCH = 4;
+  static_assert(KMAX >= 1 && RED_MAX_T % (8 * CT) == 0, "tile cap must be whole rounds of the consumer threads");
+  float s = 0.0f;
+  for (int v0 = 0; v0 < RED_CWARPS && 32 * v0 < nch; v0 += NW_BATCH) {
+    float4 x[NW_BATCH][KMAX][2];
+#pragma unroll
+    for (int b = 0; b < NW_BATCH; ++b) {
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k) {
+        const int c = 32 * (v0 + b) + lane + CT * k;
+        if (v0 + b < RED_CWARPS && c < nch) {
+          x[b][k][0] = __ldcs(reinterpret_cast<const float4*>(src + 8 * int64_t(c)));
+          x[b][k][1] = __ldcs(reinterpret_cast<const float4*>(src + 8 * int64_t(c) + 4));
+        } else {
+          x[b][k][0] = x[b][k][1] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < NW_BATCH; ++b) {
+      const int v = v0 + b;
+      if (v >= RED_CWARPS || 32 * v >= nch) break;  // warp-uniform
+      float psum = 0.0f;
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k) {
+        const int c = 32 * v + lane + CT * k;
+        if (c < nch) {
+          float o[8] = {x[b][k][0].x, x[b][k][0].y, x[b][k][0].z, x[b][k][0].w,
+                        x[b][k][1].x, x[b][k][1].y, x[b][k][1].z, x[b][k][1].w};
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            if (!keep(c, q)) o[q] = 0.0f;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) psum = __fmaf_rn(o[q], o[q], psum);
+        }
+      }
+      psum = warp_sum(psum);
+      s = v == 0 ? psum : __fadd_rn(s, psum);
+    }
+  }
+  return s;
+}
+
 }  // namespace grs

@@ -122,6 +122,10 @@ struct grs_plan {
   std::vector<int32_t> seg_tensor;
   std::vector<int32_t> bucket_seg0;
   std::vector<int32_t> tensor_job0; // [n_tensors + 1]
+  // Per reduction tile / per update tile: the tensor holding the whole tile,
+  // or -1 (the masked passes look a tile's mask bit up in one load).
+  std::vector<int32_t> red_tile_tensor;  // [n_red_tiles]
+  std::vector<int32_t> upd_tile_tensor;  // [n_upd_tiles]
   int64_t n_unique = 0, n_rank_pad = 0, n_state_pad = 0;
   int64_t n_red_tiles = 0, n_upd_tiles = 0, n_gather_chunks = 0;
   int64_t workspace_bytes = 0;
@@ -137,6 +141,8 @@ struct grs_plan {
   int32_t* d_seg_tensor = nullptr;
   int32_t* d_bucket_seg0 = nullptr;
   uint8_t* d_tensor_live = nullptr;
+  int32_t* d_red_tile_tensor = nullptr;
+  int32_t* d_upd_tile_tensor = nullptr;
   int* d_flags = nullptr;  // [4]: timeout, nonfinite, reserved
   void* host_step_resources = nullptr;  // copy stream + events of grs_step_from_host
 };

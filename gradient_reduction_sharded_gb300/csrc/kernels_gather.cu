@@ -115,6 +115,22 @@ __global__ void __launch_bounds__(GATHER_THREADS) state_logical_kernel(const Gat
              dst_base + (kToLogical ? jb.logical : jb.src) + off, rem < GATHER_CHUNK ? rem : GATHER_CHUNK);
 }
 
+// The padding of every state row, [used, padded), set to exact zeros: the
+// only state elements that no layout job writes (segments tile [0, used)).
+// One block per row; a row's padding is under 8 * dp_shard elements.
+__global__ void __launch_bounds__(256) zero_padding_kernel(const UnitDesc* __restrict__ units, int32_t n_units,
+                                                           float* __restrict__ state, int64_t n_state,
+                                                           int* __restrict__ flags) {
+  if (static_cast<int32_t>(blockIdx.x) >= n_units) return;
+  const UnitDesc ud = units[blockIdx.x];
+  const int64_t lo = ud.state_off + ud.used;
+  const int64_t hi = ud.state_off + ud.padded;
+  if (!GRS_CHECK(ud.state_off >= 0 && ud.used >= 0 && ud.used <= ud.padded && hi <= n_state, flags,
+                 SITE_STATE_LOGICAL))
+    return;
+  for (int64_t i = lo + threadIdx.x; i < hi; i += blockDim.x) state[i] = 0.0f;
+}
+
 // Self-test of the bounded wait: one thread arms an mbarrier that nothing
 // will ever complete and waits on it through the same routine the
 // reduction's producer and consumers use.
@@ -193,9 +209,13 @@ int launch_state_to_logical(const grs_plan* p, const float* state, float* logica
 }
 
 int launch_state_from_logical(const grs_plan* p, const float* logical, float* state, void* stream) {
-  cudaError_t e = cudaMemsetAsync(state, 0, static_cast<size_t>(p->n_state_pad) * sizeof(float),
-                                  static_cast<cudaStream_t>(stream));  // padding = 0
-  if (e != cudaSuccess) return static_cast<int>(e);
+  const int32_t n_units = static_cast<int32_t>(p->units.size());
+  if (n_units > 0) {
+    zero_padding_kernel<<<static_cast<unsigned>(n_units), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        p->d_units, n_units, state, p->n_state_pad, p->d_flags);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return static_cast<int>(e);
+  }
   if (p->n_gather_chunks <= 0) return 0;
   state_logical_kernel<false><<<static_cast<unsigned>(p->n_gather_chunks), GATHER_THREADS, 0,
                                 static_cast<cudaStream_t>(stream)>>>(

@@ -23,8 +23,14 @@ namespace grs {
 
 namespace {
 
-constexpr int MNORM_THREADS = 32 * RED_CWARPS;  // same tiles and order as the unmasked pass
+constexpr int MNORM_THREADS = 256;  // 8 warps, one reduction tile each (as the unmasked pass)
+constexpr int MNORM_BLOCKS_PER_SM = 8;
 constexpr int MUPD_THREADS = 256;
+// Resident blocks per SM the masked update is compiled for (register cap):
+// 4 (64 registers, a few bytes spilled) measured 8% faster than 3 (75).
+#ifndef GRS_MUPD_MIN_BLOCKS
+#define GRS_MUPD_MIN_BLOCKS 4
+#endif
 static_assert(UPD_T == MUPD_THREADS * 8, "one 8-element group per thread per tile");
 
 // Last segment in [lo, hi) whose start is <= e (the first segment starts at 0).
@@ -46,14 +52,82 @@ struct Segs {
   int32_t n_tensors;  // length of the per-tensor arrays (used mask, steps, factors)
 };
 
+// The tensor segment under a forward-moving bucket element: its index, end,
+// tensor and whether that tensor has a gradient this step.  Loaded once per
+// segment, not once per element.
+struct SegCursor {
+  int s;
+  int hi;         // one past the bucket's last segment
+  int64_t end;    // first element after segment s (the bucket's used count for the last)
+  int32_t t;      // tensor of segment s (-1 when out of range in a checked build)
+  bool on;        // tensor t has a gradient this step
+};
+
+__device__ __forceinline__ void seg_load(SegCursor& c, const Segs& sg, const uint8_t* __restrict__ used_mask,
+                                         int64_t used, int* flags, int site) {
+  c.end = c.s + 1 < c.hi ? __ldg(sg.start + c.s + 1) : used;
+  const int32_t t = __ldg(sg.tensor + c.s);
+  const bool ok = GRS_CHECK(t >= 0 && t < sg.n_tensors, flags, site);
+  c.t = ok ? t : -1;
+  c.on = ok && __ldg(used_mask + t) != 0;
+}
+
+// Cursor at element e (< used) of a bucket row whose segments are [lo, hi).
+__device__ __forceinline__ SegCursor seg_at(const Segs& sg, const uint8_t* __restrict__ used_mask, int lo, int hi,
+                                            int64_t e, int64_t used, int* flags, int site) {
+  SegCursor c;
+  c.s = find_seg(sg.start, lo, hi, e);
+  c.hi = hi;
+  seg_load(c, sg, used_mask, used, flags, site);
+  return c;
+}
+
+// Move the cursor forward to element e (< used); zero-length segments
+// (zero-size tensors) are stepped over.
+__device__ __forceinline__ void seg_advance(SegCursor& c, const Segs& sg, const uint8_t* __restrict__ used_mask,
+                                            int64_t e, int64_t used, int* flags, int site) {
+  while (e >= c.end && c.s + 1 < c.hi) {
+    ++c.s;
+    seg_load(c, sg, used_mask, used, flags, site);
+  }
+}
+
+// Element 8c + q of a tile counts iff it lies in [0, used) of its bucket row
+// and in a tensor with a gradient this step.  The cursor keeps the segment
+// of the last element asked for ([begin, end)) and seeks again (a binary
+// search) only when an element falls outside it.
+struct MaskKeep {
+  const Segs& sg;
+  const uint8_t* __restrict__ used_mask;
+  int lo, hi;
+  int64_t e0, used;
+  int* flags;
+  SegCursor cur;
+  int64_t begin;
+
+  __device__ __forceinline__ bool operator()(int c, int q) {
+    const int64_t e = e0 + 8 * int64_t(c) + q;
+    if (e >= used) return false;
+    if (e < begin || e >= cur.end) {
+      cur = seg_at(sg, used_mask, lo, hi, e, used, flags, SITE_NORM1_MASKED);
+      begin = __ldg(sg.start + cur.s);
+    }
+    return cur.on;
+  }
+};
+
+// The masked norm pass: one warp per reduction tile, the same partials as
+// the unmasked pass (tile_partial_warp) with elements of tensors without a
+// gradient counted as zero.  The tile's loads do not wait for the mask.
 __global__ void __launch_bounds__(MNORM_THREADS) norm_pass1_masked_kernel(
     const float* __restrict__ acc, const UnitDesc* __restrict__ units, const int64_t* __restrict__ prefix,
     int32_t n_units, int64_t n_tiles, Segs sg, const uint8_t* __restrict__ used_mask,
-    float* __restrict__ partials, int64_t n_state, int* __restrict__ flags) {
-  __shared__ float wp[MNORM_THREADS / 32];
+    const int32_t* __restrict__ tile_tensor, float* __restrict__ partials, int64_t n_state,
+    int* __restrict__ flags) {
   const int lane = threadIdx.x & 31;
-  const int w = threadIdx.x >> 5;
-  for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+  const int64_t n_warps = int64_t(gridDim.x) * (MNORM_THREADS / 32);
+  for (int64_t tile = int64_t(blockIdx.x) * (MNORM_THREADS / 32) + (threadIdx.x >> 5); tile < n_tiles;
+       tile += n_warps) {
     const int u = find_unit(prefix, 0, n_units, tile);
     const UnitDesc* ud = units + u;
     const int64_t T = ud->red_T;
@@ -61,38 +135,21 @@ __global__ void __launch_bounds__(MNORM_THREADS) norm_pass1_masked_kernel(
     const int64_t rem = ud->padded - e0;
     int n = static_cast<int>(rem < T ? rem : T);
     if (!GRS_CHECK(e0 >= 0 && n > 0 && ud->state_off + e0 + n <= n_state, flags, SITE_NORM1_MASKED)) n = 0;
-    const float* src = acc + ud->state_off + e0;
-    const int lo = __ldg(sg.bucket_seg0 + ud->bucket), hi = __ldg(sg.bucket_seg0 + ud->bucket + 1);
-    float psum = 0.0f;
-    for (int c = threadIdx.x; c < (n >> 3); c += MNORM_THREADS) {
-      const float4 x0 = __ldcs(reinterpret_cast<const float4*>(src + c * 8));
-      const float4 x1 = __ldcs(reinterpret_cast<const float4*>(src + c * 8 + 4));
-      float o[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-      const int64_t e = e0 + int64_t(c) * 8;
-      int s = e < ud->used ? find_seg(sg.start, lo, hi, e) : lo;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        if (e + q >= ud->used) {
-          o[q] = 0.0f;
-          continue;
-        }
-        while (s + 1 < hi && __ldg(sg.start + s + 1) <= e + q) ++s;
-        const int32_t t = __ldg(sg.tensor + s);
-        if (!GRS_CHECK(t >= 0 && t < sg.n_tensors, flags, SITE_NORM1_MASKED) || !__ldg(used_mask + t)) o[q] = 0.0f;
+    // A tile inside one tensor: its mask bit decides the whole tile (a tile
+    // without a gradient is not read: its partial is +0, as when summed).
+    const int32_t sole = __ldg(tile_tensor + tile);
+    float s = 0.0f;
+    if (sole >= 0 && GRS_CHECK(sole < sg.n_tensors, flags, SITE_NORM1_MASKED)) {
+      if (__ldg(used_mask + sole) != 0) {
+        KeepAll all;
+        s = tile_partial_warp(acc + ud->state_off + e0, n >> 3, lane, all);
       }
-#pragma unroll
-      for (int q = 0; q < 8; ++q) psum = __fmaf_rn(o[q], o[q], psum);
+    } else if (sole < 0) {
+      const int lo = __ldg(sg.bucket_seg0 + ud->bucket), hi = __ldg(sg.bucket_seg0 + ud->bucket + 1);
+      MaskKeep keep{sg, used_mask, lo, hi, e0, ud->used, flags, SegCursor{lo, hi, 0, -1, false}, 0};
+      s = tile_partial_warp(acc + ud->state_off + e0, n >> 3, lane, keep);
     }
-    psum = warp_sum(psum);
-    if (lane == 0) wp[w] = psum;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      float s = wp[0];
-#pragma unroll
-      for (int k = 1; k < MNORM_THREADS / 32; ++k) s = __fadd_rn(s, wp[k]);
-      partials[tile] = s;
-    }
-    __syncthreads();
+    if (lane == 0) partials[tile] = s;
   }
 }
 
@@ -125,6 +182,7 @@ struct MaskedArgs {
   const int64_t* prefix;
   Segs sg;
   const uint8_t* used_mask;
+  const int32_t* tile_tensor;  // per update tile: the tensor holding it whole, or -1
   const float2* factors;
   int* flags;
   int64_t n_state;  // elements of acc, master, m, v and params
@@ -139,50 +197,93 @@ __device__ __forceinline__ uint16_t bf16_rn(float x) {
   return *reinterpret_cast<const uint16_t*>(&h);
 }
 
-__global__ void __launch_bounds__(MUPD_THREADS) update_masked_kernel(const __grid_constant__ MaskedArgs a) {
+__global__ void __launch_bounds__(MUPD_THREADS, GRS_MUPD_MIN_BLOCKS) update_masked_kernel(const __grid_constant__ MaskedArgs a) {
+  // Tiles in reverse order, as the unmasked update (the reduction's last
+  // accumulator tiles are the ones still in L2).
+  const unsigned tile = gridDim.x - 1u - blockIdx.x;
+  // A tile inside one tensor (the common case): one mask bit and one factor
+  // pair for the whole block; a tile without a gradient is neither read nor
+  // written.
+  const int32_t sole = __ldg(a.tile_tensor + tile);
+  const bool whole = sole >= 0 && GRS_CHECK(sole < a.sg.n_tensors, a.flags, SITE_UPDATE_MASKED);
+  float2 f = make_float2(0.0f, 0.0f);
+  if (whole) {
+    if (__ldg(a.used_mask + sole) == 0) return;
+    f = __ldg(a.factors + sole);
+  }
   float gscale = a.inv_m;
   if (a.max_norm > 0.0f) {
     const float cr = a.max_norm / (sqrtf(static_cast<float>(*a.norm_sq)) + 1e-6f);
     gscale = __fmul_rn((cr < 1.0f || isnan(cr)) ? cr : 1.0f, a.inv_m);
   }
-  const int u = find_unit(a.prefix, 0, a.n_units, blockIdx.x);
+  const int u = find_unit(a.prefix, 0, a.n_units, tile);
   const UnitDesc* ud = a.units + u;
-  const int64_t el = (static_cast<int64_t>(blockIdx.x) - ud->upd_tile0) * UPD_T + int64_t(threadIdx.x) * 8;
+  const int64_t el = (static_cast<int64_t>(tile) - ud->upd_tile0) * UPD_T + int64_t(threadIdx.x) * 8;
   if (el >= ud->padded) return;
   const int64_t i = ud->state_off + el;
   const int64_t used = ud->used;
   if (!GRS_CHECK(i >= 0 && i + 8 <= a.n_state, a.flags, SITE_UPDATE_MASKED)) return;
-  const int lo = __ldg(a.sg.bucket_seg0 + ud->bucket), hi = __ldg(a.sg.bucket_seg0 + ud->bucket + 1);
-  int s = el < used ? find_seg(a.sg.start, lo, hi, el) : lo;
+
+  // Otherwise: which of the eight elements change — padding (rewritten as
+  // zeros) and elements of tensors with a gradient this step.  A group that
+  // lies wholly in tensors without a gradient is neither read nor written.
+  uint32_t wmask = 0xffu;  // bit q: element el + q is written (a whole tile holds no padding)
+  SegCursor cur0;
+  cur0.s = 0;
+  cur0.hi = 0;
+  cur0.end = INT64_MAX;
+  cur0.t = sole;
+  cur0.on = true;
+  if (!whole) {
+    const int lo = __ldg(a.sg.bucket_seg0 + ud->bucket), hi = __ldg(a.sg.bucket_seg0 + ud->bucket + 1);
+    cur0.s = lo;
+    cur0.hi = hi;
+    cur0.end = 0;
+    cur0.t = -1;
+    cur0.on = false;
+    if (el < used) cur0 = seg_at(a.sg, a.used_mask, lo, hi, el, used, a.flags, SITE_UPDATE_MASKED);
+    SegCursor cur = cur0;
+    wmask = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int64_t e = el + q;
+      bool w = true;  // padding
+      if (e < used) {
+        if (e >= cur.end) seg_advance(cur, a.sg, a.used_mask, e, used, a.flags, SITE_UPDATE_MASKED);
+        w = cur.on;
+      }
+      wmask |= (w ? 1u : 0u) << q;
+    }
+    if (wmask == 0) return;
+    if (cur0.t >= 0) f = __ldg(a.factors + cur0.t);
+  }
+  const bool all = wmask == 0xffu;
 
   const float4 g0 = __ldcs(reinterpret_cast<const float4*>(a.acc + i));
   const float4 g1 = __ldcs(reinterpret_cast<const float4*>(a.acc + i + 4));
-  const float4 p0 = reinterpret_cast<const float4*>(a.master + i)[0];
-  const float4 p1 = reinterpret_cast<const float4*>(a.master + i + 4)[0];
-  const float4 m0 = reinterpret_cast<const float4*>(a.m + i)[0];
-  const float4 m1 = reinterpret_cast<const float4*>(a.m + i + 4)[0];
-  const float4 v0 = reinterpret_cast<const float4*>(a.v + i)[0];
-  const float4 v1 = reinterpret_cast<const float4*>(a.v + i + 4)[0];
+  const float4 p0 = __ldcs(reinterpret_cast<const float4*>(a.master + i));
+  const float4 p1 = __ldcs(reinterpret_cast<const float4*>(a.master + i + 4));
+  const float4 m0 = __ldcs(reinterpret_cast<const float4*>(a.m + i));
+  const float4 m1 = __ldcs(reinterpret_cast<const float4*>(a.m + i + 4));
+  const float4 v0 = __ldcs(reinterpret_cast<const float4*>(a.v + i));
+  const float4 v1 = __ldcs(reinterpret_cast<const float4*>(a.v + i + 4));
   const float G[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
   float P[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
   float M[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
   float V[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-  bool write[8];
-  bool all = true;
+  SegCursor cur = cur0;
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
     const int64_t e = el + q;
     if (e >= used) {  // padding: exact zeros
       P[q] = M[q] = V[q] = 0.0f;
-      write[q] = true;
       continue;
     }
-    while (s + 1 < hi && __ldg(a.sg.start + s + 1) <= e) ++s;
-    const int32_t t = __ldg(a.sg.tensor + s);
-    write[q] = GRS_CHECK(t >= 0 && t < a.sg.n_tensors, a.flags, SITE_UPDATE_MASKED) && __ldg(a.used_mask + t) != 0;
-    all = all && write[q];
-    if (!write[q]) continue;  // no gradient this step: state stays
-    const float2 f = a.factors[t];
+    if (!((wmask >> q) & 1u)) continue;  // no gradient this step: state stays
+    if (e >= cur.end) {
+      seg_advance(cur, a.sg, a.used_mask, e, used, a.flags, SITE_UPDATE_MASKED);
+      f = __ldg(a.factors + cur.t);
+    }
     const float g = __fmul_rn(G[q], gscale);
     float p = __fmul_rn(P[q], a.decay);
     const float mm = __fmaf_rn(a.b1, M[q], __fmul_rn(a.omb1, g));
@@ -194,22 +295,22 @@ __global__ void __launch_bounds__(MUPD_THREADS) update_masked_kernel(const __gri
     V[q] = vv;
   }
   if (all) {
-    reinterpret_cast<float4*>(a.master + i)[0] = make_float4(P[0], P[1], P[2], P[3]);
-    reinterpret_cast<float4*>(a.master + i + 4)[0] = make_float4(P[4], P[5], P[6], P[7]);
-    reinterpret_cast<float4*>(a.m + i)[0] = make_float4(M[0], M[1], M[2], M[3]);
-    reinterpret_cast<float4*>(a.m + i + 4)[0] = make_float4(M[4], M[5], M[6], M[7]);
-    reinterpret_cast<float4*>(a.v + i)[0] = make_float4(V[0], V[1], V[2], V[3]);
-    reinterpret_cast<float4*>(a.v + i + 4)[0] = make_float4(V[4], V[5], V[6], V[7]);
+    __stcs(reinterpret_cast<float4*>(a.master + i), make_float4(P[0], P[1], P[2], P[3]));
+    __stcs(reinterpret_cast<float4*>(a.master + i + 4), make_float4(P[4], P[5], P[6], P[7]));
+    __stcs(reinterpret_cast<float4*>(a.m + i), make_float4(M[0], M[1], M[2], M[3]));
+    __stcs(reinterpret_cast<float4*>(a.m + i + 4), make_float4(M[4], M[5], M[6], M[7]));
+    __stcs(reinterpret_cast<float4*>(a.v + i), make_float4(V[0], V[1], V[2], V[3]));
+    __stcs(reinterpret_cast<float4*>(a.v + i + 4), make_float4(V[4], V[5], V[6], V[7]));
     uint4 h;
     h.x = uint32_t(bf16_rn(P[0])) | (uint32_t(bf16_rn(P[1])) << 16);
     h.y = uint32_t(bf16_rn(P[2])) | (uint32_t(bf16_rn(P[3])) << 16);
     h.z = uint32_t(bf16_rn(P[4])) | (uint32_t(bf16_rn(P[5])) << 16);
     h.w = uint32_t(bf16_rn(P[6])) | (uint32_t(bf16_rn(P[7])) << 16);
-    reinterpret_cast<uint4*>(a.params + i)[0] = h;
+    __stcs(reinterpret_cast<uint4*>(a.params + i), h);
   } else {
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-      if (!write[q]) continue;
+      if (!((wmask >> q) & 1u)) continue;
       a.master[i + q] = P[q];
       a.m[i + q] = M[q];
       a.v[i + q] = V[q];
@@ -225,11 +326,14 @@ int launch_norm_masked(const grs_plan* p, const float* acc, int32_t n_micro, con
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float* partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + ws_partials_offset());
   if (p->n_red_tiles > 0) {
-    const int64_t grid = p->n_red_tiles < int64_t(p->sm_count) * 16 ? p->n_red_tiles
-                                                                    : int64_t(p->sm_count) * 16;
+    const int64_t tiles_per_block = MNORM_THREADS / 32;
+    const int64_t need = (p->n_red_tiles + tiles_per_block - 1) / tiles_per_block;
+    const int64_t cap = int64_t(p->sm_count) * MNORM_BLOCKS_PER_SM;
+    const int64_t grid = need < cap ? need : cap;
     norm_pass1_masked_kernel<<<static_cast<unsigned>(grid), MNORM_THREADS, 0, s>>>(
         acc, p->d_units, p->d_red_prefix, static_cast<int32_t>(p->units.size()), p->n_red_tiles,
-        Segs{p->d_seg_start, p->d_seg_tensor, p->d_bucket_seg0, static_cast<int32_t>(p->numel.size())}, used, partials,
+        Segs{p->d_seg_start, p->d_seg_tensor, p->d_bucket_seg0, static_cast<int32_t>(p->numel.size())}, used,
+        p->d_red_tile_tensor, partials,
         p->n_state_pad, p->d_flags);
     const int e = static_cast<int>(cudaGetLastError());
     if (e != 0) return e;
@@ -258,6 +362,7 @@ int launch_update_masked(const grs_plan* p, const grs_adamw* hp, const double* d
   a.prefix = p->d_upd_prefix;
   a.sg = Segs{p->d_seg_start, p->d_seg_tensor, p->d_bucket_seg0, static_cast<int32_t>(p->numel.size())};
   a.used_mask = used;
+  a.tile_tensor = p->d_upd_tile_tensor;
   a.factors = factors;
   a.flags = p->d_flags;
   a.n_state = p->n_state_pad;

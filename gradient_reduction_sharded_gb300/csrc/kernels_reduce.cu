@@ -29,6 +29,8 @@
 // All mbarrier waits are bounded (device.cuh).
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "device.cuh"
 #include "internal.h"
 #include "launch.cuh"
@@ -318,7 +320,9 @@ __global__ void __launch_bounds__(RED_THREADS, GRS_RED_CTAS_PER_SM) reduce_kerne
   }
 }
 
-bool g_attr_set[2][64] = {};
+// Whether the dynamic shared-memory cap is raised, per (gradient type,
+// device); plans on several host threads may launch at once.
+std::atomic<bool> g_attr_set[2][64] = {};
 
 }  // namespace
 
@@ -359,13 +363,13 @@ int launch_reduce(const grs_plan* p, const ReduceLaunch& l, void* stream) {
   a.stage_bytes = static_cast<int32_t>(need);
   const size_t smem = size_t(stages) * need + RED_SMEM_TAIL;
   const bool f32 = p->grad_esize == 4;
-  if (p->device >= 0 && p->device < 64 && !g_attr_set[f32][p->device]) {
+  if (p->device >= 0 && p->device < 64 && !g_attr_set[f32][p->device].load(std::memory_order_acquire)) {
     cudaError_t e = f32 ? cudaFuncSetAttribute(reduce_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(RED_RING_BYTES + RED_SMEM_TAIL))
                         : cudaFuncSetAttribute(reduce_kernel<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(RED_RING_BYTES + RED_SMEM_TAIL));
     if (e != cudaSuccess) return static_cast<int>(e);
-    g_attr_set[f32][p->device] = true;
+    g_attr_set[f32][p->device].store(true, std::memory_order_release);
   }
   int64_t cap = int64_t(p->sm_count) * GRS_RED_CTAS_PER_SM;
   if (l.max_ctas > 0 && l.max_ctas < cap) cap = l.max_ctas;

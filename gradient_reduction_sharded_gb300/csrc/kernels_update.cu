@@ -25,55 +25,39 @@ namespace grs {
 
 namespace {
 
-constexpr int NORM1_THREADS = 32 * RED_CWARPS;  // the reduction's consumer threads
+constexpr int NORM1_THREADS = 256;  // 8 warps, one reduction tile each at a time
+constexpr int NORM1_BLOCKS_PER_SM = 8;
 constexpr int NORM2_THREADS = 256;
 constexpr int UPD_THREADS = 256;
 static_assert(UPD_T == UPD_THREADS * 8, "one 8-element group per thread per tile");
 
 // ----------------------------------------------------------------- norm pass 1
-// Same thread -> chunk map and the same fp32 operation order as the
-// reduction's fused epilogue: thread c of NORM1_THREADS sums chunks c,
-// c+NORM1_THREADS, ... of 8 elements with fmaf(x, x, s); warp butterfly;
-// warps folded in order.
+// One warp per reduction tile (tile_partial_warp): the same per-tile partial,
+// bit for bit, as the reduction's fused epilogue.  Warps take tiles
+// gw, gw + (all warps), ...
 __global__ void __launch_bounds__(NORM1_THREADS) norm_pass1_kernel(const float* __restrict__ acc,
                                                                    const UnitDesc* __restrict__ units,
                                                                    const int64_t* __restrict__ prefix,
                                                                    int32_t n_units, int64_t n_tiles,
                                                                    float* __restrict__ partials, int64_t n_state,
                                                                    int* __restrict__ flags) {
-  __shared__ float wp[NORM1_THREADS / 32];
   const int lane = threadIdx.x & 31;
-  const int w = threadIdx.x >> 5;
   pdl_wait();
   pdl_trigger();
-  for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+  const int64_t n_warps = int64_t(gridDim.x) * (NORM1_THREADS / 32);
+  KeepAll all;
+  for (int64_t tile = int64_t(blockIdx.x) * (NORM1_THREADS / 32) + (threadIdx.x >> 5); tile < n_tiles;
+       tile += n_warps) {
     const int u = find_unit(prefix, 0, n_units, tile);
     const UnitDesc* ud = units + u;
     const int64_t T = ud->red_T;
     const int64_t e0 = (tile - ud->red_tile0) * T;
     const int64_t rem = ud->padded - e0;
     int n = static_cast<int>(rem < T ? rem : T);
-    // (uniform over the block: the same tile)
+    // (uniform over the warp: the same tile)
     if (!GRS_CHECK(e0 >= 0 && n > 0 && ud->state_off + e0 + n <= n_state, flags, SITE_NORM1)) n = 0;
-    const float* src = acc + ud->state_off + e0;
-    float psum = 0.0f;
-    for (int c = threadIdx.x; c < (n >> 3); c += NORM1_THREADS) {
-      const float4 x0 = __ldcs(reinterpret_cast<const float4*>(src + c * 8));
-      const float4 x1 = __ldcs(reinterpret_cast<const float4*>(src + c * 8 + 4));
-      const float o[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-#pragma unroll
-      for (int q = 0; q < 8; ++q) psum = __fmaf_rn(o[q], o[q], psum);
-    }
-    psum = warp_sum(psum);
-    if (lane == 0) wp[w] = psum;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      float s = wp[0];
-#pragma unroll
-      for (int k = 1; k < NORM1_THREADS / 32; ++k) s = __fadd_rn(s, wp[k]);
-      partials[tile] = s;
-    }
-    __syncthreads();
+    const float s = tile_partial_warp(acc + ud->state_off + e0, n >> 3, lane, all);
+    if (lane == 0) partials[tile] = s;
   }
 }
 
@@ -259,8 +243,10 @@ int launch_norm(const grs_plan* p, const float* acc, int32_t n_micro, void* work
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float* partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + ws_partials_offset());
   if (!partials_ready && p->n_red_tiles > 0) {
-    const int64_t grid = p->n_red_tiles < int64_t(p->sm_count) * 16 ? p->n_red_tiles
-                                                                    : int64_t(p->sm_count) * 16;
+    const int64_t tiles_per_block = NORM1_THREADS / 32;
+    const int64_t need = (p->n_red_tiles + tiles_per_block - 1) / tiles_per_block;
+    const int64_t cap = int64_t(p->sm_count) * NORM1_BLOCKS_PER_SM;
+    const int64_t grid = need < cap ? need : cap;
     const int e = static_cast<int>(launch_k(norm_pass1_kernel, dim3(unsigned(grid)), dim3(NORM1_THREADS), 0, s,
                                             acc, static_cast<const UnitDesc*>(p->d_units),
                                             static_cast<const int64_t*>(p->d_red_prefix),

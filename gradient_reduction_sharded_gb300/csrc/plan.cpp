@@ -25,6 +25,25 @@ namespace {
 
 int64_t round_up(int64_t x, int64_t q) { return (x + q - 1) / q * q; }
 
+// Tiles of T elements over one row of bucket b: for each, the tensor whose
+// segment holds the whole tile, or -1.  The bucket's segments tile [0, used)
+// in offset order (zero-size tensors give empty segments, stepped over).
+void sole_tensors(const grs_plan& p, int32_t b, int64_t T, std::vector<int32_t>& out) {
+  const int32_t s0 = p.bucket_seg0[b], s1 = p.bucket_seg0[b + 1];
+  const int64_t used = p.buckets[b].used, padded = p.buckets[b].padded;
+  int32_t s = s0;
+  for (int64_t e0 = 0; e0 < padded; e0 += T) {
+    const int64_t e1 = std::min(padded, e0 + T);
+    int32_t sole = -1;
+    if (e1 <= used && s0 < s1) {
+      while (s + 1 < s1 && p.seg_start[s + 1] <= e0) ++s;  // the segment holding e0
+      const int64_t end = s + 1 < s1 ? p.seg_start[s + 1] : used;
+      if (e1 <= end) sole = p.seg_tensor[s];
+    }
+    out.push_back(sole);
+  }
+}
+
 int32_t group_size_of(int32_t tag, const grs_plan& p) {
   switch (tag) {
     case GRS_REPLICA_AVG:
@@ -233,6 +252,14 @@ grs_status build_plan(const int64_t* numels, const int32_t* owners, const uint32
       p->seg_tensor.push_back(i);
     }
     p->bucket_seg0.push_back(static_cast<int32_t>(p->seg_start.size()));
+  }
+  // The tensor that holds each reduction and update tile entirely (-1 when
+  // a tile spans several tensors or reaches the padding), unit by unit.
+  p->red_tile_tensor.clear();
+  p->upd_tile_tensor.clear();
+  for (const UnitDesc& u : p->units) {
+    sole_tensors(*p, u.bucket, u.red_T, p->red_tile_tensor);
+    sole_tensors(*p, u.bucket, UPD_T, p->upd_tile_tensor);
   }
   p->workspace_bytes = ws_factors_offset(red_tiles) + (static_cast<int64_t>(n) * 8 + 255) / 256 * 256;
   return GRS_OK;

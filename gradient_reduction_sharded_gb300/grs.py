@@ -35,7 +35,8 @@ GRS_MAX_WORLD = 128
 GRS_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED_COMPOSITION", 3: "SHAPE",
-                4: "ALIGNMENT", 5: "CUDA", 6: "TIMEOUT", 7: "NONFINITE", 8: "NO_DEVICE"}
+                4: "ALIGNMENT", 5: "CUDA", 6: "TIMEOUT", 7: "NONFINITE", 8: "NO_DEVICE",
+                9: "BOUNDS"}
 
 
 class GrsError(RuntimeError):

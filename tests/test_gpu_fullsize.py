@@ -51,18 +51,53 @@ def sample_positions(rng, used, P, tile=2048, n_random=384):
 
 @pytest.mark.parametrize("cid", [1, 4, 3, 2])
 def test_full_size_update_matches_oracle(cid):
+    _full_size(cid, "plain", 0)
+
+
+# The variants bench.py measures (--variant / --window), in the same launch
+# configuration: fp32 rank gradients, tensors without a gradient (masked
+# norm and update), frozen tensors, a trailing window of 3 of 4 microbatches.
+@pytest.mark.parametrize("cid,variant,window", [(1, "fp32-grads", 0), (1, "unused", 0),
+                                                (1, "frozen", 0), (3, "plain", 3)])
+def test_full_size_variant_matches_oracle(cid, variant, window):
+    _full_size(cid, variant, window)
+
+
+def _full_size(cid, variant, window):
     import bench  # the benchmark's own update object
 
     w = workloads.get(cid)
-    op = oracle.plan(w.numels, w.owners, w.world, w.tp, w.dp_replicate, w.dp_shard, w.bucket_bytes)
-    need = (w.n_micro * w.world * op.n_rank_pad * 2 + op.n_state_pad * 18) / 1e9
+    M = window or w.n_micro
+    fp32 = variant == "fp32-grads"
+    flags = bench.frozen_pattern(len(w.numels)) if variant == "frozen" else None
+    used_t = bench.unused_pattern(len(w.numels)) if variant == "unused" else None
+    op = oracle.plan(w.numels, w.owners, w.world, w.tp, w.dp_replicate, w.dp_shard, w.bucket_bytes,
+                     flags)
+    need = (M * w.world * op.n_rank_pad * (4 if fp32 else 2) + op.n_state_pad * 18) / 1e9
     if _free_gb() < need * 1.05 + 4:
         pytest.skip(f"needs {need:.0f} GB of device memory")
     dev = torch.device("cuda")
     rng = np.random.default_rng(1000 + cid)
-    u = bench.GpuUpdate(w, dev)
+    u = bench.GpuUpdate(w, dev, variant, window)
+    assert u.info["n_state_pad"] == op.n_state_pad and u.n_micro == M
+    gview = torch.float32 if fp32 else torch.int16
+    hdt = np.float32 if fp32 else np.uint16
+
+    def host(t):
+        x = t.view(gview).cpu().numpy()
+        return x if fp32 else x.view(np.uint16)
+
+    # per bucket: which per-rank elements belong to a tensor with a gradient
+    counts = {}
+    for b in range(op.n_buckets):
+        mk = np.zeros(int(op.b_padded[b]), bool)
+        for i in range(len(w.numels)):
+            if int(op.t_bucket[i]) == b and (used_t is None or used_t[i]):
+                o = int(op.t_offset[i])
+                mk[o:o + op.per_rank(i)] = True
+        counts[b] = mk
     try:
-        M, R = w.n_micro, w.world
+        R = w.world
         # samples and their initial state, before the update overwrites it
         samples = {}
         for b in range(op.n_buckets):
@@ -72,13 +107,15 @@ def test_full_size_update_matches_oracle(cid):
                                     for b in range(op.n_buckets) for t in range(op.copies(b))])
         sidx = torch.from_numpy(state_idx).to(dev)
         master0 = u.master[sidx].cpu().numpy()
+        bits0 = u.params[sidx].cpu().numpy().view(np.uint16)
 
         u.step()
         torch.cuda.synchronize()
         assert u.grs.grs_check_device_errors(u.plan, u.stream) == 0
 
         # ---- exact global norm: every element through the oracle, bucket by
-        # bucket in chunks of at most CHUNK elements (bounded host memory)
+        # bucket in chunks of at most CHUNK elements (bounded host memory);
+        # elements of tensors without a gradient count zero
         CHUNK = 1 << 21
         items = [(b, cs, min(CHUNK, int(op.b_padded[b]) - cs))
                  for b in range(op.n_buckets) for cs in range(0, int(op.b_padded[b]), CHUNK)]
@@ -86,7 +123,7 @@ def test_full_size_update_matches_oracle(cid):
 
         def host_buf():
             if not hasattr(pinned, "buf"):
-                pinned.buf = torch.empty(M * R * CHUNK, dtype=torch.int16).pin_memory()
+                pinned.buf = torch.empty(M * R * CHUNK, dtype=gview).pin_memory()
             return pinned.buf
 
         def chunk_norm(item):
@@ -95,11 +132,12 @@ def test_full_size_update_matches_oracle(cid):
             hb = host_buf()[:M * R * cl].view(M, R, cl)
             for j in range(M):
                 for k in range(R):
-                    hb[j, k].copy_(u.grads[j][k][ro:ro + cl].view(torch.int16))
-            g = hb.numpy().view(np.uint16)
+                    hb[j, k].copy_(u.grads[j][k][ro:ro + cl].view(gview))
+            g = hb.numpy() if fp32 else hb.numpy().view(np.uint16)
             used = max(0, min(cl, int(op.b_used[b]) - cs))
             acc = oracle.reduce_bucket(int(op.b_tag[b]), op.tp, op.dp_replicate, op.dp_shard, cl,
                                        used, g)
+            acc[:, ~counts[b][cs:cs + cl]] = 0.0
             return oracle.norm_sq(acc, M)
 
         threads = max(1, min(8, os.cpu_count() or 1))
@@ -107,7 +145,8 @@ def test_full_size_update_matches_oracle(cid):
             parts = list(ex.map(chunk_norm, items))
         s_oracle = float(np.sum(np.array(parts, np.float64)))  # (bucket, chunk) order
         s_gpu = float(u.norm.cpu()[0])
-        assert_close([s_gpu], [s_oracle], f"workload {cid} norm_sq")
+        what = f"workload {cid} {variant}" + (f" window {M}" if window else "")
+        assert_close([s_gpu], [s_oracle], f"{what} norm_sq")
         c = oracle.clip_coef(s_oracle, w.adamw.max_norm)
         assert c < 1.0  # clipping is active on these workloads
 
@@ -116,44 +155,62 @@ def test_full_size_update_matches_oracle(cid):
         hp = (a.lr, a.beta1, a.beta2, a.eps, a.weight_decay)
         want_acc, want_p, want_m, want_v, want_bits = [], [], [], [], []
         lo_p, lo_m, lo_v, hi_p, hi_m, hi_v = [], [], [], [], [], []
+        idle = []  # sampled state positions of tensors without a gradient
         for b in range(op.n_buckets):
             pos = samples[b]
             ro, used = int(op.b_rank_off[b]), int(op.b_used[b])
             pt = torch.from_numpy(pos + ro).to(dev)
-            g = np.stack([np.stack([u.grads[j][k].view(torch.int16)[pt].cpu().numpy().view(np.uint16)
-                                    for k in range(R)]) for j in range(M)])
+            g = np.stack([np.stack([host(u.grads[j][k].view(gview)[pt]) for k in range(R)])
+                          for j in range(M)]).astype(hdt)
             n_valid = int((pos < used).sum())
             acc = oracle.reduce_bucket(int(op.b_tag[b]), op.tp, op.dp_replicate, op.dp_shard,
                                        len(pos), n_valid, g)
             delta = oracle.accumulation_error_bound(
                 oracle.reduce_bucket(int(op.b_tag[b]), op.tp, op.dp_replicate, op.dp_shard, len(pos),
                                      n_valid, oracle.abs_inputs(g)), M)
+            off_idle = (pos < used) & ~counts[b][pos]
             for t in range(op.copies(b)):
                 want_acc.append(acc[t])
                 off = sum(len(samples[bb]) * op.copies(bb) for bb in range(b)) + t * len(pos)
                 m0 = master0[off:off + len(pos)]
                 z = np.zeros(len(pos), np.float32)
                 p1, m1, v1, bits = oracle.adamw(acc[t], n_valid, M, c, hp, 1, m0, z, z)
+                rl = oracle.adamw(acc[t] - delta[t], n_valid, M, c, hp, 1, m0, z, z)
+                rh = oracle.adamw(acc[t] + delta[t], n_valid, M, c, hp, 1, m0, z, z)
+                # no gradient this step: master, moments and bf16 copy unchanged
+                b0 = bits0[off:off + len(pos)]
+                for arr, keep in ((p1, m0), (m1, z), (v1, z), (bits, b0), (rl[0], m0), (rl[1], z),
+                                  (rl[2], z), (rh[0], m0), (rh[1], z), (rh[2], z)):
+                    arr[off_idle] = keep[off_idle]
+                idle.append(off_idle)
                 want_p.append(p1)
                 want_m.append(m1)
                 want_v.append(v1)
                 want_bits.append(bits)
-                for sign, dst in ((-1.0, (lo_p, lo_m, lo_v)), (1.0, (hi_p, hi_m, hi_v))):
-                    r = oracle.adamw(acc[t] + sign * delta[t], n_valid, M, c, hp, 1, m0, z, z)
-                    for d_, x in zip(dst, r[:3]):
-                        d_.append(x)
+                for d_, x in zip((lo_p, lo_m, lo_v), rl[:3]):
+                    d_.append(x)
+                for d_, x in zip((hi_p, hi_m, hi_v), rh[:3]):
+                    d_.append(x)
         got_acc = u.acc[sidx].cpu().numpy()
         got_p = u.master[sidx].cpu().numpy()
         got_m = u.m[sidx].cpu().numpy()
         got_v = u.v[sidx].cpu().numpy()
         got_bits = u.params[sidx].cpu().numpy().view(np.uint16)
-        assert_close(got_acc, np.concatenate(want_acc), f"workload {cid} acc")
         cat = np.concatenate
-        assert_close_bracketed(got_p, cat(want_p), cat(lo_p), cat(hi_p), f"workload {cid} master")
-        assert_close_bracketed(got_m, cat(want_m), cat(lo_m), cat(hi_m), f"workload {cid} m")
-        assert_close_bracketed(got_v, cat(want_v), cat(lo_v), cat(hi_v), f"workload {cid} v")
-        assert_bf16_cast(got_bits, got_p, np.concatenate(want_bits), np.concatenate(want_p),
-                         f"workload {cid} params")
+        idle = cat(idle)
+        assert_close(got_acc, cat(want_acc), f"{what} acc")
+        assert_close_bracketed(got_p, cat(want_p), cat(lo_p), cat(hi_p), f"{what} master")
+        assert_close_bracketed(got_m, cat(want_m), cat(lo_m), cat(hi_m), f"{what} m")
+        assert_close_bracketed(got_v, cat(want_v), cat(lo_v), cat(hi_v), f"{what} v")
+        live = ~idle
+        assert_bf16_cast(got_bits[live], got_p[live], cat(want_bits)[live], cat(want_p)[live],
+                         f"{what} params")
+        if used_t is not None:
+            assert idle.any(), "the sample holds no element of a tensor without a gradient"
+            # bit for bit: the masked update neither reads nor writes them
+            assert np.array_equal(got_p[idle].view(np.uint32), master0[idle].view(np.uint32))
+            assert np.array_equal(got_bits[idle], bits0[idle])
+            assert np.all(got_m[idle] == 0) and np.all(got_v[idle] == 0)
         pad = np.concatenate([np.repeat((samples[b] >= int(op.b_used[b]))[None], op.copies(b), 0).reshape(-1)
                               for b in range(op.n_buckets)])
         for arr in (got_acc, got_p, got_m, got_v, got_bits):

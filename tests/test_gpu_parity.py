@@ -442,14 +442,26 @@ def test_frozen_tensors_excluded():
         run.close()
 
 
-@pytest.mark.parametrize("fp32", [False, True])
-def test_unused_tensors_masked_update(fp32):
+@pytest.mark.parametrize("fp32,zeros", [(False, False), (True, False), (False, True)])
+def test_unused_tensors_masked_update(fp32, zeros):
     """Three steps with per-step masks of tensors that got no gradient
     (grad None): masked norm + per-tensor-step AdamW against the oracle's
-    masked update, the oracle carrying its own state and step counts."""
-    c = Case([5000, 33, 4096 * 2, 17, 2048, 999, 64], [RA, RA, LS, AR, PS, RA, LS], 8, 2, 2, 2, 1 << 15,
-             2, 1e-3, 42, fp32_grads=fp32, tensor_flags=[0, 0, 0, 0, 0, 1, 0])
+    masked update, the oracle carrying its own state and step counts.  With
+    `zeros`, zero-size tensors sit between the others (empty segments the
+    kernels' segment walk must step over)."""
+    numels = [5000, 33, 4096 * 2, 17, 2048, 999, 64]
+    owners = [RA, RA, LS, AR, PS, RA, LS]
+    flags = [0, 0, 0, 0, 0, 1, 0]
     masks = [[1, 1, 1, 1, 1, 0, 1], [1, 0, 1, 0, 1, 0, 0], [0, 1, 1, 1, 0, 0, 1]]
+    if zeros:
+        # a zero-size tensor after tensors 0, 1, 2 and 4, with the owner of its neighbour
+        for at in (5, 3, 2, 1):
+            numels.insert(at, 0)
+            owners.insert(at, owners[at - 1])
+            flags.insert(at, 0)
+            for mk in masks:
+                mk.insert(at, at % 2)
+    c = Case(numels, owners, 8, 2, 2, 2, 1 << 15, 2, 1e-3, 42, fp32_grads=fp32, tensor_flags=flags)
     run = Run(c)
     try:
         n = len(c.numels)
