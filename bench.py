@@ -54,6 +54,24 @@ def mandatory_bytes(buckets, n_micro: int, grad_bytes: int = 2) -> dict:
     return {"reduce": red, "update": upd, "total": red + upd, "reduce_last_mb": last}
 
 
+def variant_bytes(buckets, n_micro: int, grad_bytes: int, n_state_pad: int, n_unique: int,
+                  idle=None) -> dict:
+    """mandatory_bytes plus the norm pass, for an update where `idle`
+    elements (None: none) belong to tensors without a gradient.  Those need
+    no norm read and no update; the reduction does not know the mask and
+    runs as in the plain case.  The plain update's norm is fused into the
+    last reduction (0 bytes); the masked one reads acc once (4 bytes per
+    element of a tensor with a gradient)."""
+    mb = mandatory_bytes(buckets, n_micro, grad_bytes)
+    mb["norm"] = 0
+    if idle is not None:
+        live = n_state_pad - idle          # elements the update writes (padding included)
+        mb["norm"] = 4 * (n_unique - idle)  # elements the norm reads (no padding)
+        mb["update"] = 30 * live
+        mb["total"] = mb["reduce"] + mb["norm"] + mb["update"]
+    return mb
+
+
 def library_buckets(grs, plan) -> list:
     """The bucket geometry of a libgrs plan (grs_bucket_info per bucket)."""
     nb = grs.grs_plan_query(plan)["n_buckets"]
@@ -218,17 +236,11 @@ class GpuUpdate:
 
     def algorithmic_bytes(self) -> dict:
         """Per-kernel algorithmic bytes of one update of this variant."""
-        mb = mandatory_bytes(self.buckets, self.n_micro, self.grad_bytes)
-        mb["norm"] = 0  # fused into the last reduction
+        idle = None
         if self.used is not None:
-            # Tensors without a gradient need no norm read and no update;
-            # the reduction does not know the mask and runs as in the plain case.
             idle = sum(n for n, u in zip(self.w.numels, self.used_list) if not u)
-            live = self.info["n_state_pad"] - idle
-            mb["norm"] = 4 * (live - (self.info["n_state_pad"] - self.info["n_unique"]))
-            mb["update"] = 30 * live
-            mb["total"] = mb["reduce"] + mb["norm"] + mb["update"]
-        return mb
+        return variant_bytes(self.buckets, self.n_micro, self.grad_bytes, self.info["n_state_pad"],
+                             self.info["n_unique"], idle)
 
     def reduce(self):
         g = self.grs
