@@ -199,13 +199,14 @@ struct KeepAll {
 // warp's lanes are combined by warp_sum and the warps' sums folded in order
 // v = 0, 1, ...  Here the warp plays the consumer warps one after another
 // ("virtual warps"), with the loads of NW_BATCH of them in flight at once.
+// The batch changes only how many loads are in flight, never the order of
+// the arithmetic.
 // keep(c, q) == false zeros element 8c + q (a masked pass); virtual warps
 // without a chunk add +0 and are skipped.
-template <typename Keep>
+template <int NW_BATCH = 4, typename Keep>
 __device__ __forceinline__ float tile_partial_warp(const float* __restrict__ src, int nch, int lane, Keep& keep) {
   constexpr int CT = 32 * RED_CWARPS;
   constexpr int KMAX = static_cast<int>(RED_MAX_T / 8 / CT);  // chunks per consumer thread at most
-  constexpr int NW_BATCH = 4;
   static_assert(KMAX >= 1 && RED_MAX_T % (8 * CT) == 0, "tile cap must be whole rounds of the consumer threads");
   float s = 0.0f;
   for (int v0 = 0; v0 < RED_CWARPS && 32 * v0 < nch; v0 += NW_BATCH) {

@@ -119,7 +119,7 @@ struct MaskKeep {
 // The masked norm pass: one warp per reduction tile, the same partials as
 // the unmasked pass (tile_partial_warp) with elements of tensors without a
 // gradient counted as zero.  The tile's loads do not wait for the mask.
-__global__ void __launch_bounds__(MNORM_THREADS) norm_pass1_masked_kernel(
+__global__ void __launch_bounds__(MNORM_THREADS, 3) norm_pass1_masked_kernel(
     const float* __restrict__ acc, const UnitDesc* __restrict__ units, const int64_t* __restrict__ prefix,
     int32_t n_units, int64_t n_tiles, Segs sg, const uint8_t* __restrict__ used_mask,
     const int32_t* __restrict__ tile_tensor, float* __restrict__ partials, int64_t n_state,
@@ -147,7 +147,8 @@ __global__ void __launch_bounds__(MNORM_THREADS) norm_pass1_masked_kernel(
     } else if (sole < 0) {
       const int lo = __ldg(sg.bucket_seg0 + ud->bucket), hi = __ldg(sg.bucket_seg0 + ud->bucket + 1);
       MaskKeep keep{sg, used_mask, lo, hi, e0, ud->used, flags, SegCursor{lo, hi, 0, -1, false}, 0};
-      s = tile_partial_warp(acc + ud->state_off + e0, n >> 3, lane, keep);
+      // (one virtual warp's loads at a time: the cursor needs the registers)
+      s = tile_partial_warp<1>(acc + ud->state_off + e0, n >> 3, lane, keep);
     }
     if (lane == 0) partials[tile] = s;
   }

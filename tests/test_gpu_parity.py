@@ -489,6 +489,34 @@ def test_unused_tensors_masked_update(fp32, zeros):
         run.close()
 
 
+def test_masked_path_with_every_tensor_used_equals_plain_path():
+    """With every tensor marked as having a gradient, the masked norm and the
+    per-tensor-step AdamW produce the plain path's norm, master, moments and
+    bf16 parameters bit for bit, over three steps (the masked norm replays
+    the same per-tile order; the per-tensor factors equal the plan-wide ones)."""
+    c = SMALL["multi-tile-world16-M2"]
+    a, b = Run(c), Run(c)
+    try:
+        n = len(c.numels)
+        ones = torch.ones(n, dtype=torch.uint8, device="cuda")
+        steps = torch.zeros(n, dtype=torch.int32, device="cuda")
+        for k in range(3):
+            if k:
+                a.fill_grads(step_seed=k + 1)
+                b.fill_grads(step_seed=k + 1)
+            a.update()
+            b.reduce(emit=False)
+            b.masked_update(ones, steps)
+            torch.cuda.synchronize()
+            assert a.check_flags() == 0 and b.check_flags() == 0
+            for name in ("acc", "norm", "master", "m", "v", "params"):
+                assert torch.equal(getattr(a, name), getattr(b, name)), (k + 1, name)
+        assert steps.cpu().tolist() == [3] * n
+    finally:
+        a.close()
+        b.close()
+
+
 def test_trailing_accumulation_window():
     """A window that ends after 3 of 4 microbatches: the update averages the
     3 accumulated microbatches (G = acc / 3)."""
