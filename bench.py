@@ -415,7 +415,7 @@ def run_gpu(args, rank, world_size, local_rank):
     }
     if rank == 0 and world_size == 1 and not args.no_cpu_baseline:
         if plain:
-            result["cpu_baseline"] = cpu_baseline(w, mb, args)
+            result["cpu_baseline"] = cpu_baseline(w, mb, args, u)
         else:
             result["cpu_baseline"] = cpu_baseline_variant(w, u, mb, args)
     return result
@@ -565,6 +565,27 @@ def _host_inputs(w, n_rank_pad: int, n_micro: int = 0, fp32: bool = False, devic
     return out
 
 
+def _sampled_host_inputs(w, op, buckets, n_micro: int = 0, fp32: bool = False, device=None):
+    """Only the sampled buckets' inputs [M][R][P], generated exactly as the
+    GPU arm generates them (whole per-rank buffers from the same seeds, on
+    the device when there is one) and sliced, so that host memory holds only
+    the sample."""
+    import torch
+    dev = device or ("cuda" if torch.cuda.is_available() else "cpu")
+    gen = workloads.normal_f32 if fp32 else workloads.normal_bf16
+    M = n_micro or w.n_micro
+    out = {b: np.zeros((M, w.world, int(op.b_padded[b])), np.float32 if fp32 else np.uint16) for b in buckets}
+    for j in range(M):
+        for k in range(w.world):
+            t = gen(op.n_rank_pad, w.grad_std, workloads.grad_seed(w.cid, j, k), device=dev)
+            for b in buckets:
+                ro, P = int(op.b_rank_off[b]), int(op.b_padded[b])
+                sl = t[ro:ro + P].cpu()
+                out[b][j, k] = sl.numpy() if fp32 else workloads.bf16_bits(sl)
+            del t
+    return out
+
+
 def _host_fetch(op, host, M):
     """Bucket inputs [M][R][P] sliced from whole per-rank host buffers."""
     def fetch(b):
@@ -676,13 +697,18 @@ def _oracle_plan(w, tensor_flags=None):
                        w.bucket_bytes, tensor_flags)
 
 
-def cpu_baseline(w, mb, args, host=None, target_s=10.0):
+def cpu_baseline(w, mb, args, u=None, target_s=10.0):
     """The oracle as it stands, on this host: whole updates of the workload
     (every bucket: reduce -> norm -> AdamW), repeated until about target_s of
     CPU work, one thread; then the same with one thread per core (buckets in
-    parallel)."""
+    parallel).  An update that moves more than 8 GB is sampled instead (one
+    bucket per tag, scaled to the whole update by mandatory bytes), its
+    inputs copied once from the GPU arm's own gradients (`u`), so that host
+    memory holds only the sample."""
+    if mb["total"] > 8e9 and u is not None:
+        return cpu_baseline_variant(w, u, mb, args, target_s)
     op = _oracle_plan(w)
-    host = host if host is not None else _host_inputs(w, op.n_rank_pad)
+    host = _host_inputs(w, op.n_rank_pad)
     buckets = list(range(op.n_buckets))
     reps, t0 = 0, time.perf_counter()
     while True:
@@ -704,7 +730,7 @@ def cpu_baseline(w, mb, args, host=None, target_s=10.0):
 
 
 def cpu_baseline_variant(w, u, mb, args, target_s=10.0):
-    """The oracle on the variant's update (same plan flags, gradient type,
+    """The oracle on the update `u` runs (its plan flags, gradient type,
     microbatch window and mask), one thread: whole updates when the update
     moves at most 8 GB, otherwise one bucket per tag scaled to the whole
     update by mandatory bytes.  Inputs: the GPU arm's own gradient bytes,
@@ -735,8 +761,8 @@ def run_reference(args, rank, world_size):
     w = workloads.get(args.workload, args.blocks)
     op = _oracle_plan(w)
     mb = mandatory_bytes(oracle_buckets(op), w.n_micro)
-    host = _host_inputs(w, op.n_rank_pad)
     buckets = _sample_buckets(op, frac_target=0.0)  # one bucket per tag: a bounded step
+    host = _sampled_host_inputs(w, op, buckets)
     sb = _sample_bytes(op, buckets, w.n_micro)
     for _ in range(args.warmup):
         _oracle_sample(w, op, host, buckets)

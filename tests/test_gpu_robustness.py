@@ -76,6 +76,70 @@ def test_no_writes_outside_outputs():
         run.close()
 
 
+def test_masked_and_layout_calls_write_inside_outputs():
+    """The masked norm and update (tensors without a gradient, zero-size
+    tensors among them) and the state layout conversions write nothing
+    outside their outputs; the masked update leaves the state of tensors
+    without a gradient untouched and the layout restore writes every
+    padding element as zero."""
+    g = grs()
+    numels = [100003, 0, 1024, 65536 * 2, 4099, 333, 0, 70001, 8000]
+    owners = [RA, RA, PS, LS, AR, PS, LS, RA, LS]
+    c = Case(numels, owners, 16, 2, 2, 4, 1 << 18, 2, 1e-3, 72)
+    run = Run(c)
+    try:
+        nsp, s = run.nsp, run.stream()
+        n = len(numels)
+        used = torch.tensor([1, 1, 0, 1, 1, 0, 0, 1, 0], dtype=torch.uint8, device="cuda")
+        acc_full, acc = guarded(nsp, torch.float32, float("nan"))
+        st = {}
+        for name, dt, fill in (("master", torch.float32, float("nan")), ("m", torch.float32, float("nan")),
+                               ("v", torch.float32, float("nan")), ("params", torch.int16, -12345)):
+            full, view = guarded(nsp, dt, fill)
+            view.copy_(getattr(run, name)[:nsp])
+            st[name] = (full, view, fill)
+        before = {k: v[1].clone() for k, v in st.items()}
+        steps_full, steps = guarded(n, torch.int32, -7)
+        steps.zero_()
+        ws_full, ws = guarded(run.ws.numel(), torch.float32, float("nan"))
+        ws.zero_()
+        nrm_full, nrm = guarded(1, torch.float64, float("nan"))
+        for j in range(c.n_micro):
+            g.grs_reduce_all(run.plan, run.ptrs(j), acc.data_ptr(), int(j > 0), 0, ws.data_ptr(), s)
+        g.grs_grad_norm_sq_masked(run.plan, acc.data_ptr(), c.n_micro, used.data_ptr(), ws.data_ptr(),
+                                  nrm.data_ptr(), s)
+        hp = g.make_adamw(*c.hp, c.max_norm, 1, c.n_micro)
+        g.grs_clip_adamw_step_masked(run.plan, hp, nrm.data_ptr(), acc.data_ptr(), st["master"][1].data_ptr(),
+                                     st["m"][1].data_ptr(), st["v"][1].data_ptr(), st["params"][1].data_ptr(),
+                                     used.data_ptr(), steps.data_ptr(), ws.data_ptr(), s)
+        nu = run.info["n_unique"]
+        lg_full, lg = guarded(nu, torch.float32, float("nan"))
+        g.grs_state_to_logical(run.plan, st["master"][1].data_ptr(), lg.data_ptr(), s)
+        back_full, back = guarded(nsp, torch.float32, float("nan"))  # interior NaN too: padding must be written
+        g.grs_state_from_logical(run.plan, lg.data_ptr(), back.data_ptr(), s)
+        torch.cuda.synchronize()
+        assert run.check_flags() == 0
+        for full, fill in ((acc_full, float("nan")), (steps_full, -7), (ws_full, float("nan")),
+                           (nrm_full, float("nan")), (lg_full, float("nan")), (back_full, float("nan"))):
+            assert canaries_intact(full, fill)
+        for name, (full, view, fill) in st.items():
+            assert canaries_intact(full, fill), name
+        assert steps.cpu().tolist() == [int(u) for u in used.cpu().tolist()]
+        assert torch.equal(back, st["master"][1])  # padding included: exact zeros both sides
+        # tensors without a gradient: state untouched, bit for bit
+        op = run.op
+        for i in range(n):
+            if used[i].item():
+                continue
+            for lo, hi in op.tensor_rows(i):
+                for name in ("master", "m", "v", "params"):
+                    a, b = st[name][1][lo:hi], before[name][lo:hi]
+                    assert torch.equal(a.view(torch.int32) if a.dtype == torch.float32 else a,
+                                       b.view(torch.int32) if b.dtype == torch.float32 else b), (i, name)
+    finally:
+        run.close()
+
+
 def test_results_do_not_depend_on_the_grid():
     g = grs()
     c = Case([100003, 1024, 65536 * 2, 4099, 333], [RA, PS, LS, AR, PS], 16, 2, 2, 4, 1 << 18, 1, 1e-3, 72)
