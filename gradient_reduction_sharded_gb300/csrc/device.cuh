@@ -198,23 +198,21 @@ struct KeepAll {
 // RED_CWARPS, ... with fmaf(x, x, psum) over each chunk's 8 elements; each
 // warp's lanes are combined by warp_sum and the warps' sums folded in order
 // v = 0, 1, ...  Here the warp plays the consumer warps one after another
-// ("virtual warps"), with the loads of NW_BATCH of them in flight at once.
-// The batch changes only how many loads are in flight, never the order of
-// the arithmetic.
-// keep(c, q) == false zeros element 8c + q (a masked pass); virtual warps
-// without a chunk add +0 and are skipped.
-template <int NW_BATCH = 4, typename Keep>
-__device__ __forceinline__ float tile_partial_warp(const float* __restrict__ src, int nch, int lane, Keep& keep) {
+// ("virtual warps"), BATCH of them with their loads in flight at once; KE
+// is the number of chunks a consumer thread has at most in this tile.  The
+// batch changes only how many loads are in flight, never the order of the
+// arithmetic.  keep(c, q) == false zeros element 8c + q (a masked pass);
+// virtual warps without a chunk add +0 and are skipped.
+template <int BATCH, int KE, typename Keep>
+__device__ __forceinline__ float tile_partial_warp_k(const float* __restrict__ src, int nch, int lane, Keep& keep) {
   constexpr int CT = 32 * RED_CWARPS;
-  constexpr int KMAX = static_cast<int>(RED_MAX_T / 8 / CT);  // chunks per consumer thread at most
-  static_assert(KMAX >= 1 && RED_MAX_T % (8 * CT) == 0, "tile cap must be whole rounds of the consumer threads");
   float s = 0.0f;
-  for (int v0 = 0; v0 < RED_CWARPS && 32 * v0 < nch; v0 += NW_BATCH) {
-    float4 x[NW_BATCH][KMAX][2];
+  for (int v0 = 0; v0 < RED_CWARPS && 32 * v0 < nch; v0 += BATCH) {
+    float4 x[BATCH][KE][2];
 #pragma unroll
-    for (int b = 0; b < NW_BATCH; ++b) {
+    for (int b = 0; b < BATCH; ++b) {
 #pragma unroll
-      for (int k = 0; k < KMAX; ++k) {
+      for (int k = 0; k < KE; ++k) {
         const int c = 32 * (v0 + b) + lane + CT * k;
         if (v0 + b < RED_CWARPS && c < nch) {
           x[b][k][0] = __ldcs(reinterpret_cast<const float4*>(src + 8 * int64_t(c)));
@@ -225,12 +223,12 @@ __device__ __forceinline__ float tile_partial_warp(const float* __restrict__ src
       }
     }
 #pragma unroll
-    for (int b = 0; b < NW_BATCH; ++b) {
+    for (int b = 0; b < BATCH; ++b) {
       const int v = v0 + b;
       if (v >= RED_CWARPS || 32 * v >= nch) break;  // warp-uniform
       float psum = 0.0f;
 #pragma unroll
-      for (int k = 0; k < KMAX; ++k) {
+      for (int k = 0; k < KE; ++k) {
         const int c = 32 * v + lane + CT * k;
         if (c < nch) {
           float o[8] = {x[b][k][0].x, x[b][k][0].y, x[b][k][0].z, x[b][k][0].w,
@@ -247,6 +245,19 @@ __device__ __forceinline__ float tile_partial_warp(const float* __restrict__ src
     }
   }
   return s;
+}
+
+// SLOTS chunk loads in flight per lane: tiles of at most one chunk per
+// consumer thread (nch <= 32 RED_CWARPS, every tile of 4096 elements or
+// fewer) play SLOTS virtual warps at a time, larger tiles SLOTS / KMAX.
+template <int SLOTS = 8, typename Keep>
+__device__ __forceinline__ float tile_partial_warp(const float* __restrict__ src, int nch, int lane, Keep& keep) {
+  constexpr int CT = 32 * RED_CWARPS;
+  constexpr int KMAX = static_cast<int>(RED_MAX_T / 8 / CT);  // chunks per consumer thread at most
+  static_assert(KMAX >= 1 && RED_MAX_T % (8 * CT) == 0, "tile cap must be whole rounds of the consumer threads");
+  static_assert(SLOTS % KMAX == 0, "a batch holds whole consumer threads");
+  if (KMAX == 1 || nch <= CT) return tile_partial_warp_k<SLOTS, 1>(src, nch, lane, keep);
+  return tile_partial_warp_k<SLOTS / KMAX, KMAX>(src, nch, lane, keep);
 }
 
 }  // namespace grs

@@ -147,8 +147,8 @@ __global__ void __launch_bounds__(MNORM_THREADS, 3) norm_pass1_masked_kernel(
     } else if (sole < 0) {
       const int lo = __ldg(sg.bucket_seg0 + ud->bucket), hi = __ldg(sg.bucket_seg0 + ud->bucket + 1);
       MaskKeep keep{sg, used_mask, lo, hi, e0, ud->used, flags, SegCursor{lo, hi, 0, -1, false}, 0};
-      // (one virtual warp's loads at a time: the cursor needs the registers)
-      s = tile_partial_warp<1>(acc + ud->state_off + e0, n >> 3, lane, keep);
+      // (two chunk loads in flight per lane: the cursor needs the registers)
+      s = tile_partial_warp<2>(acc + ud->state_off + e0, n >> 3, lane, keep);
     }
     if (lane == 0) partials[tile] = s;
   }
@@ -205,25 +205,28 @@ __global__ void __launch_bounds__(MUPD_THREADS, GRS_MUPD_MIN_BLOCKS) update_mask
   // A tile inside one tensor (the common case): one mask bit and one factor
   // pair for the whole block; a tile without a gradient is neither read nor
   // written.
+  // (The unit search runs while the tile's tensor, mask bit and factors load.)
   const int32_t sole = __ldg(a.tile_tensor + tile);
+  const int u = find_unit(a.prefix, 0, a.n_units, tile);
+  const UnitDesc* ud = a.units + u;
+  const int64_t el = (static_cast<int64_t>(tile) - ud->upd_tile0) * UPD_T + int64_t(threadIdx.x) * 8;
+  const int64_t padded = ud->padded;
+  const int64_t i = ud->state_off + el;
+  const int64_t used = ud->used;
   const bool whole = sole >= 0 && GRS_CHECK(sole < a.sg.n_tensors, a.flags, SITE_UPDATE_MASKED);
   float2 f = make_float2(0.0f, 0.0f);
+  uint8_t on = 1;
   if (whole) {
-    if (__ldg(a.used_mask + sole) == 0) return;
+    on = __ldg(a.used_mask + sole);
     f = __ldg(a.factors + sole);
   }
+  if (on == 0 || el >= padded) return;
+  if (!GRS_CHECK(i >= 0 && i + 8 <= a.n_state, a.flags, SITE_UPDATE_MASKED)) return;
   float gscale = a.inv_m;
   if (a.max_norm > 0.0f) {
     const float cr = a.max_norm / (sqrtf(static_cast<float>(*a.norm_sq)) + 1e-6f);
     gscale = __fmul_rn((cr < 1.0f || isnan(cr)) ? cr : 1.0f, a.inv_m);
   }
-  const int u = find_unit(a.prefix, 0, a.n_units, tile);
-  const UnitDesc* ud = a.units + u;
-  const int64_t el = (static_cast<int64_t>(tile) - ud->upd_tile0) * UPD_T + int64_t(threadIdx.x) * 8;
-  if (el >= ud->padded) return;
-  const int64_t i = ud->state_off + el;
-  const int64_t used = ud->used;
-  if (!GRS_CHECK(i >= 0 && i + 8 <= a.n_state, a.flags, SITE_UPDATE_MASKED)) return;
 
   // Otherwise: which of the eight elements change — padding (rewritten as
   // zeros) and elements of tensors with a gradient this step.  A group that
