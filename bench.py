@@ -193,7 +193,8 @@ def frozen_pattern(n_tensors: int) -> list:
 class GpuUpdate:
     """All device buffers of one workload and the calls of one update."""
 
-    def __init__(self, w: workloads.Workload, device, variant: str = "plain", window: int = 0):
+    def __init__(self, w: workloads.Workload, device, variant: str = "plain", window: int = 0,
+                 graph: bool = False):
         import torch
         from gradient_reduction_sharded_gb300 import grs
         self.torch, self.grs, self.w, self.dev = torch, grs, w, device
@@ -230,9 +231,21 @@ class GpuUpdate:
             self.used_list = unused_pattern(n)
             self.used = torch.tensor(self.used_list, dtype=torch.uint8, device=device)
             self.tensor_steps = torch.zeros(n, dtype=torch.int32, device=device)
+        # A CUDA graph replays the launches it captured, host arguments
+        # included, so the step count must live on the device: the captured
+        # update is the per-tensor-step AdamW with every tensor marked as
+        # having a gradient (bit-identical to the plain update), after the
+        # plain reduction and norm.
+        self.graph = None
+        self.graphed = graph
+        if graph:
+            if variant != "plain":
+                raise ValueError("--graph runs the plain update only")
+            self.all_used = torch.ones(n, dtype=torch.uint8, device=device)
+            self.tensor_steps = torch.zeros(n, dtype=torch.int32, device=device)
         # kernels per step: one reduction per microbatch, the norm finish and the
         # update; the masked path adds its norm pass and the per-tensor factors
-        self.launches_per_step = self.n_micro + (4 if self.used is not None else 2)
+        self.launches_per_step = self.n_micro + (4 if self.used is not None else 3 if graph else 2)
 
     def algorithmic_bytes(self) -> dict:
         """Per-kernel algorithmic bytes of one update of this variant."""
@@ -263,18 +276,41 @@ class GpuUpdate:
         self.step_no += 1
         hp = self.grs.make_adamw(a.lr, a.beta1, a.beta2, a.eps, a.weight_decay, a.max_norm,
                                  self.step_no, self.n_micro)
-        if self.used is not None:
+        if self.used is not None or self.graphed:
+            mask = self.used if self.used is not None else self.all_used
             self.grs.grs_clip_adamw_step_masked(self.plan, hp, self.norm.data_ptr(), self.acc.data_ptr(),
                                                 self.master.data_ptr(), self.m.data_ptr(),
                                                 self.v.data_ptr(), self.params.data_ptr(),
-                                                self.used.data_ptr(), self.tensor_steps.data_ptr(),
+                                                mask.data_ptr(), self.tensor_steps.data_ptr(),
                                                 self.ws.data_ptr(), self.stream)
         else:
             self.grs.grs_clip_adamw_step(self.plan, hp, self.norm.data_ptr(), self.acc.data_ptr(),
                                          self.master.data_ptr(), self.m.data_ptr(), self.v.data_ptr(),
                                          self.params.data_ptr(), self.stream)
 
+    def capture(self):
+        """Capture one whole update in a CUDA graph; step() then replays it."""
+        torch = self.torch
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(self.dev)
+        side.wait_stream(torch.cuda.current_stream(self.dev))
+        own = self.stream
+        with torch.cuda.stream(side):
+            self.stream = side.cuda_stream
+            try:
+                with torch.cuda.graph(g, stream=side):
+                    self.reduce()
+                    self.norm_sq()
+                    self.adamw()
+            finally:
+                self.stream = own
+        torch.cuda.synchronize(self.dev)
+        self.graph = g
+
     def step(self):
+        if self.graph is not None:
+            self.graph.replay()
+            return
         self.reduce()
         self.norm_sq()
         self.adamw()
@@ -289,9 +325,9 @@ def run_gpu(args, rank, world_size, local_rank):
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
     w = workloads.get(args.workload, args.blocks)
-    u = GpuUpdate(w, device, args.variant, args.window)
+    u = GpuUpdate(w, device, args.variant, args.window, args.graph)
     mb = u.algorithmic_bytes()
-    plain = args.variant == "plain" and u.n_micro == w.n_micro
+    plain = args.variant == "plain" and u.n_micro == w.n_micro and not args.graph
     clocks = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[0])
                           if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit()
                           else local_rank)
@@ -304,6 +340,8 @@ def run_gpu(args, rank, world_size, local_rank):
     for _ in range(args.warmup):
         u.step()
     torch.cuda.synchronize()
+    if args.graph:
+        u.capture()  # later steps replay the captured update
     # soak so that the clock samples see the steady state (untimed)
     t_soak = time.time()
     while time.time() - t_soak < args.soak:
@@ -311,20 +349,42 @@ def run_gpu(args, rank, world_size, local_rank):
             u.step()
         torch.cuda.synchronize()
     K = args.steps
-    # Timed region: exactly K steps, back to back, no events in between.
+    # Inputs that fit in L2 would be timed from the cache: then L2 is flushed
+    # before every step (a write of twice its size, outside the events) and
+    # each step is timed on its own.
+    l2_bytes = int(getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 0) or (129 << 20))
+    flush = u.n_micro * w.world * u.info["n_rank_pad"] * u.grad_bytes <= l2_bytes
+    scrub = torch.empty(2 * l2_bytes // 4, dtype=torch.float32, device=device) if flush else None
+
+    def flush_l2():
+        if scrub is not None:
+            scrub.fill_(0.0)
+
+    # Timed region: exactly K steps, back to back, no events in between
+    # (one event pair per step when L2 is flushed between steps).
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    t_start.record()
-    for _ in range(K):
-        u.step()
-    t_end.record()
-    torch.cuda.synchronize()
+    if flush:
+        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for a_, b_ in pairs:
+            flush_l2()
+            a_.record()
+            u.step()
+            b_.record()
+        torch.cuda.synchronize()
+        total_ms = sum(a_.elapsed_time(b_) for a_, b_ in pairs)
+    else:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record()
+        for _ in range(K):
+            u.step()
+        t_end.record()
+        torch.cuda.synchronize()
+        total_ms = t_start.elapsed_time(t_end)
     if dist is not None:
         dist.barrier()
-    total_ms = t_start.elapsed_time(t_end)
     ms_step = max_over_ranks(total_ms / K, device)
     # Per-kernel durations for the roofline: a second region of K steps with
     # CUDA events between the kernels on the launching stream (the events
@@ -333,6 +393,7 @@ def run_gpu(args, rank, world_size, local_rank):
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     torch.cuda.synchronize()
     for i in range(K):
+        flush_l2()
         ev[i][0].record()
         u.reduce()
         ev[i][1].record()
@@ -351,6 +412,8 @@ def run_gpu(args, rank, world_size, local_rank):
     # The gather and the end-to-end path run on the plain update only.
     # ---------------------------------------------------------------- gather
     gather = run_gather(u, args, torch) if plain else None
+    if gather is not None and flush:
+        gather["l2"] = "parameters fit in L2: back-to-back gathers read them from the cache"
 
     # ---------------------------------------------------------------- e2e
     e2e = None if (args.no_e2e or not plain) else run_e2e(u, args, torch)
@@ -393,7 +456,8 @@ def run_gpu(args, rank, world_size, local_rank):
         "steps": K, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": dict(w.describe(), grad_dtype="fp32" if u.grad_bytes == 4 else "bf16",
-                       l2="inputs larger than L2 (no flush)",
+                       l2=("L2 flushed before every step (inputs fit in L2)" if flush
+                           else "inputs larger than L2 (no flush)"),
                        parallelism=f"replicas{world_size}" if world_size > 1 else "1 GPU, simulated ranks",
                        **variant_config(u)),
         "achieved_gbs_total": mb["total"] / (ms_step * world_size * 1e-3) / 1e9 if world_size == 1
@@ -426,6 +490,8 @@ def variant_config(u: GpuUpdate) -> dict:
     out = {}
     if u.variant != "plain":
         out["variant"] = u.variant
+    if u.graphed:
+        out["cuda_graph"] = "whole update replayed from one capture (device step counts)"
     if u.n_micro != u.w.n_micro:
         out["window"] = {"microbatches": u.n_micro, "of": u.w.n_micro}
         out["microbatches"] = u.n_micro
@@ -1055,6 +1121,8 @@ def main():
                          "(masked norm and update); frozen: some tensors frozen at plan time")
     ap.add_argument("--checkpoint", action="store_true",
                     help="measure checkpoint restore with reshard (layout kernels + files) instead")
+    ap.add_argument("--graph", action="store_true",
+                    help="replay the whole update as one captured CUDA graph (launch-bound workloads)")
     ap.add_argument("--window", type=int, default=0,
                     help="trailing accumulation window: reduce only the first M' microbatches, G = acc/M'")
     args = ap.parse_args()
