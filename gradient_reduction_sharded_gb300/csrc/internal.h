@@ -217,6 +217,9 @@ struct ReduceLaunch {
 int launch_reduce(const grs_plan* p, const ReduceLaunch& a, void* stream);
 int launch_norm(const grs_plan* p, const float* acc, int32_t n_micro, void* workspace,
                 int32_t partials_ready, double* d_norm_sq, void* stream);
+// Bias-corrected AdamW factors of step `step` computed on the host in fp64
+// and rounded to fp32: lr / (1 - beta1^step) and 1 / sqrt(1 - beta2^step).
+void bias_factors(const grs_adamw* hp, int32_t step, float* step_size, float* inv_bc2_sqrt);
 int launch_update(const grs_plan* p, const grs_adamw* hp, const double* d_norm_sq, const float* acc,
                   float* master, float* m, float* v, uint16_t* params, void* stream);
 int launch_accumulate(const grs_plan* p, int32_t bucket, float* acc, const float* mb, void* stream);

@@ -155,15 +155,24 @@ __global__ void __launch_bounds__(MNORM_THREADS, 3) norm_pass1_masked_kernel(
 }
 
 // Per tensor: advance the step count of tensors with a gradient and derive
-// their bias-corrected factors (lr / (1 - b1^t), 1 / sqrt(1 - b2^t)) in fp64.
+// their bias-corrected factors (lr / (1 - b1^t), 1 / sqrt(1 - b2^t)).  A
+// tensor whose new step equals the caller's step takes the factors the host
+// computed for it (the plain update's, bit for bit); any other is computed
+// here in fp64 (slow on this GPU's fp64 units, so only for tensors that
+// skipped updates).
 __global__ void tensor_factors_kernel(int32_t n, const uint8_t* __restrict__ live,
                                       const uint8_t* __restrict__ used_mask, int32_t* __restrict__ steps,
-                                      float2* __restrict__ factors, double lr, double b1, double b2) {
+                                      float2* __restrict__ factors, double lr, double b1, double b2,
+                                      int32_t hint_step, float2 hint) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
   if (live[i] && used_mask[i]) {
     const int t = steps[i] + 1;
     steps[i] = t;
+    if (t == hint_step) {
+      factors[i] = hint;
+      return;
+    }
     const double bc1 = 1.0 - pow(b1, static_cast<double>(t));
     const double bc2 = 1.0 - pow(b2, static_cast<double>(t));
     factors[i] = make_float2(static_cast<float>(lr / bc1), static_cast<float>(1.0 / sqrt(bc2)));
@@ -351,8 +360,11 @@ int launch_update_masked(const grs_plan* p, const grs_adamw* hp, const double* d
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int32_t n = static_cast<int32_t>(p->numel.size());
   float2* factors = reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) + ws_factors_offset(p->n_red_tiles));
+  float2 hint = make_float2(0.0f, 0.0f);
+  const int32_t hint_step = hp->step >= 1 ? hp->step : 0;
+  if (hint_step >= 1) bias_factors(hp, hint_step, &hint.x, &hint.y);
   tensor_factors_kernel<<<(n + 255) / 256, 256, 0, s>>>(n, p->d_tensor_live, used, steps, factors, hp->lr,
-                                                         hp->beta1, hp->beta2);
+                                                         hp->beta1, hp->beta2, hint_step, hint);
   int e = static_cast<int>(cudaGetLastError());
   if (e != 0 || p->n_upd_tiles <= 0) return e;
   MaskedArgs a;

@@ -269,6 +269,14 @@ int launch_norm_finish(const grs_plan* p, int32_t n_micro, void* workspace, doub
                                    inv_m * inv_m, d_norm_sq, p->d_flags));
 }
 
+void bias_factors(const grs_adamw* hp, int32_t step, float* step_size, float* inv_bc2_sqrt) {
+  const double lr = hp->lr, b1 = hp->beta1, b2 = hp->beta2;
+  const double bc1 = 1.0 - std::pow(b1, static_cast<double>(step));
+  const double bc2 = 1.0 - std::pow(b2, static_cast<double>(step));
+  *step_size = static_cast<float>(lr / bc1);
+  *inv_bc2_sqrt = static_cast<float>(1.0 / std::sqrt(bc2));
+}
+
 int launch_update(const grs_plan* p, const grs_adamw* hp, const double* d_norm_sq, const float* acc,
                   float* master, float* m, float* v, uint16_t* params, void* stream) {
   if (p->n_upd_tiles <= 0) return 0;
@@ -285,16 +293,13 @@ int launch_update(const grs_plan* p, const grs_adamw* hp, const double* d_norm_s
   a.n_state = p->n_state_pad;
   a.n_units = static_cast<int32_t>(p->units.size());
   const double lr = hp->lr, b1 = hp->beta1, b2 = hp->beta2, wd = hp->weight_decay;
-  const double bc1 = 1.0 - std::pow(b1, static_cast<double>(hp->step));
-  const double bc2 = 1.0 - std::pow(b2, static_cast<double>(hp->step));
   a.decay = static_cast<float>(1.0 - lr * wd);
   a.b1 = hp->beta1;
   a.omb1 = static_cast<float>(1.0 - b1);
   a.b2 = hp->beta2;
   a.omb2 = static_cast<float>(1.0 - b2);
   a.eps = hp->eps;
-  a.step_size = static_cast<float>(lr / bc1);
-  a.inv_bc2_sqrt = static_cast<float>(1.0 / std::sqrt(bc2));
+  bias_factors(hp, hp->step, &a.step_size, &a.inv_bc2_sqrt);
   a.max_norm = hp->max_norm > 0.0f ? hp->max_norm : 0.0f;
   a.inv_m = static_cast<float>(1.0 / static_cast<double>(hp->n_micro));
   return static_cast<int>(launch_k(update_kernel, dim3(unsigned(p->n_upd_tiles)), dim3(UPD_THREADS), 0, stream, a));

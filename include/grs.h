@@ -326,8 +326,12 @@ grs_status grs_clip_adamw_step(const grs_plan* plan, const grs_adamw* hp, const 
  * grs_clip_adamw_step_masked: like grs_clip_adamw_step for tensors with
  * used = 1, each with its own step count: d_tensor_steps (device int32
  * [n_tensors], zero before the first update, updated in place) is advanced
- * for used tensors and its new value sets their bias correction (hp->step
- * is ignored).  Tensors with used = 0 keep master, m, v, the bf16 copy and
+ * for used tensors and its new value sets their bias correction.  hp->step
+ * is only a hint (0 = none): tensors whose new step equals it take factors
+ * computed on the host, exactly those of grs_clip_adamw_step at that step;
+ * the others' factors are computed on the device in fp64 (the same values
+ * up to the last bit of the fp32 factor, more slowly).  Tensors with
+ * used = 0 keep master, m, v, the bf16 copy and
  * their step count unchanged (torch.optim.AdamW skips parameters without a
  * gradient: no moment decay, no weight decay).  Entries of frozen tensors
  * are ignored.  workspace as for the norm (the per-tensor factors live

@@ -147,9 +147,10 @@ class Run:
         self.norm_sq(partials_ready=partials_ready)
         self.adamw(max_norm=max_norm)
 
-    def masked_update(self, used_dev, steps_dev, n_micro=None, max_norm=None):
+    def masked_update(self, used_dev, steps_dev, n_micro=None, max_norm=None, step_hint=1):
         """Norm over used tensors and the per-tensor-step AdamW (the reduce
-        must have run)."""
+        must have run).  step_hint goes in hp->step: tensors whose new step
+        equals it use host-computed factors, the others device-computed ones."""
         g = grs()
         c = self.c
         M = c.n_micro if n_micro is None else n_micro
@@ -157,7 +158,7 @@ class Run:
         s = self.stream()
         g.grs_grad_norm_sq_masked(self.plan, self.acc.data_ptr(), M, used_dev.data_ptr(),
                                   self.ws.data_ptr(), self.norm.data_ptr(), s)
-        hp = g.make_adamw(c.hp[0], c.hp[1], c.hp[2], c.hp[3], c.hp[4], mn, 1, M)
+        hp = g.make_adamw(c.hp[0], c.hp[1], c.hp[2], c.hp[3], c.hp[4], mn, step_hint, M)
         g.grs_clip_adamw_step_masked(self.plan, hp, self.norm.data_ptr(), self.acc.data_ptr(),
                                      self.master.data_ptr(), self.m.data_ptr(), self.v.data_ptr(),
                                      self.params.data_ptr(), used_dev.data_ptr(), steps_dev.data_ptr(),

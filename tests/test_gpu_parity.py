@@ -489,11 +489,14 @@ def test_unused_tensors_masked_update(fp32, zeros):
         run.close()
 
 
-def test_masked_path_with_every_tensor_used_equals_plain_path():
+@pytest.mark.parametrize("hint", ["matching", "none"])
+def test_masked_path_with_every_tensor_used_equals_plain_path(hint):
     """With every tensor marked as having a gradient, the masked norm and the
     per-tensor-step AdamW produce the plain path's norm, master, moments and
     bf16 parameters bit for bit, over three steps (the masked norm replays
-    the same per-tile order; the per-tensor factors equal the plan-wide ones)."""
+    the same per-tile order; the per-tensor factors equal the plan-wide
+    ones), whether the factors come from the host (the caller's step equals
+    every tensor's) or are computed on the device (no step given)."""
     c = SMALL["multi-tile-world16-M2"]
     a, b = Run(c), Run(c)
     try:
@@ -506,7 +509,7 @@ def test_masked_path_with_every_tensor_used_equals_plain_path():
                 b.fill_grads(step_seed=k + 1)
             a.update()
             b.reduce(emit=False)
-            b.masked_update(ones, steps)
+            b.masked_update(ones, steps, step_hint=k + 1 if hint == "matching" else 0)
             torch.cuda.synchronize()
             assert a.check_flags() == 0 and b.check_flags() == 0
             for name in ("acc", "norm", "master", "m", "v", "params"):
