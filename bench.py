@@ -173,6 +173,16 @@ def job_value(ms_per_step_max: float, world_size: int) -> float:
 
 
 # --------------------------------------------------------------------------- GPU arm
+def bench_workload(args):
+    """The workload named on the command line, with --micro overriding its
+    number of microbatches (the name then says so)."""
+    import dataclasses
+    w = workloads.get(args.workload, args.blocks)
+    if getattr(args, "micro", 0) and args.micro != w.n_micro:
+        w = dataclasses.replace(w, n_micro=args.micro, name=f"{w.name}-{args.micro}mb")
+    return w
+
+
 # Variants of the update (the pages' validation list): the same workload with
 # fp32 rank gradients; with tensors that have no gradient this step; with
 # frozen tensors; or with a trailing accumulation window of fewer
@@ -324,7 +334,7 @@ def run_gpu(args, rank, world_size, local_rank):
     import torch
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
-    w = workloads.get(args.workload, args.blocks)
+    w = bench_workload(args)
     u = GpuUpdate(w, device, args.variant, args.window, args.graph)
     mb = u.algorithmic_bytes()
     plain = args.variant == "plain" and u.n_micro == w.n_micro and not args.graph
@@ -824,7 +834,7 @@ def cpu_baseline_variant(w, u, mb, args, target_s=10.0):
 
 def run_reference(args, rank, world_size):
     """The oracle as the reference arm, on host cores, rank 0 only."""
-    w = workloads.get(args.workload, args.blocks)
+    w = bench_workload(args)
     op = _oracle_plan(w)
     mb = mandatory_bytes(oracle_buckets(op), w.n_micro)
     buckets = _sample_buckets(op, frac_target=0.0)  # one bucket per tag: a bounded step
@@ -877,7 +887,7 @@ def run_checkpoint(args):
     from gradient_reduction_sharded_gb300 import grs
     device = torch.device("cuda", 0)
     torch.cuda.set_device(device)
-    w = workloads.get(args.workload, args.blocks)
+    w = bench_workload(args)
     tp, dr, ds = reshard_geometry(w)
     spec_w = ck.PlanSpec(list(w.numels), list(w.owners), None, w.world, w.tp, w.dp_replicate,
                          w.dp_shard, w.bucket_bytes)
@@ -1021,7 +1031,7 @@ def run_overlap(args):
     import torch
     device = torch.device("cuda", 0)
     torch.cuda.set_device(device)
-    w = workloads.get(args.workload, args.blocks)
+    w = bench_workload(args)
     u = GpuUpdate(w, device)
     g = u.grs
     nb = u.info["n_buckets"]
@@ -1123,6 +1133,8 @@ def main():
                     help="measure checkpoint restore with reshard (layout kernels + files) instead")
     ap.add_argument("--graph", action="store_true",
                     help="replay the whole update as one captured CUDA graph (launch-bound workloads)")
+    ap.add_argument("--micro", type=int, default=0,
+                    help="override the workload's number of microbatches (distinct seeded gradients each)")
     ap.add_argument("--window", type=int, default=0,
                     help="trailing accumulation window: reduce only the first M' microbatches, G = acc/M'")
     args = ap.parse_args()
