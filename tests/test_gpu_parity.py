@@ -78,6 +78,12 @@ def small_cases():
     # degenerate: zero-size tensors, a bucket holding only zero-size tensors (no tiles)
     cases["zero-size-tensors"] = Case([0, 1000, 0, 64, 0], [RA, RA, PS, AR, LS], 2, 1, 1, 2, 1 << 20, 1,
                                       1e-2, 24)
+    # many small tensors of all four tags (3000, 1..400 elements): most tiles
+    # span several tensors, the gather needs several launches (256 pointers each)
+    rng = np.random.default_rng(2024)
+    owners_many = rng.integers(0, 4, 3000).tolist()
+    numels_many = [int(x) * (2 if o == LS else 1) for x, o in zip(rng.integers(1, 201, 3000), owners_many)]
+    cases["many-small-tensors"] = Case(numels_many, owners_many, 8, 2, 2, 2, 1 << 16, 1, 1e-2, 25)
     cases["fp32-grads-world16"] = Case(
         [100003, 1024, 65536 * 2, 4099], [RA, PS, LS, AR], 16, 2, 2, 4, 1 << 18, 1, 1e-3, 19,
         fp32_grads=True)
@@ -115,6 +121,27 @@ def test_three_steps_match_oracle(name):
             res = oracle_update(run, master, m, v, step=step)
             full_check(run, res, f"{name} step {step}")
             master, m, v = res.master, res.m, res.v  # the oracle carries its own state
+    finally:
+        run.close()
+
+
+def test_forty_steps_track_the_oracle():
+    """Forty updates with new gradients each step, the oracle carrying its
+    own fp64-evaluated state rounded to fp32 after every step: step counting
+    and bias correction stay right as the corrections decay, and the fp32
+    evaluation does not drift from the fp64 one beyond the tolerance."""
+    c = SMALL["odd-ds3-M3"]
+    run = Run(c)
+    try:
+        master, m, v = run.state_host()
+        for step in range(1, 41):
+            if step > 1:
+                run.fill_grads(step_seed=step)
+            run.update()
+            res = oracle_update(run, master, m, v, step=step)
+            if step % 10 == 0 or step < 3:
+                full_check(run, res, f"step {step}")
+            master, m, v = res.master, res.m, res.v
     finally:
         run.close()
 
@@ -219,7 +246,7 @@ def test_owner_routing_is_exact():
 
 
 def test_gather_matches_oracle():
-    for name in ("tiny-world4", "odd-ds3-M3", "multi-tile-world16-M2"):
+    for name in ("tiny-world4", "odd-ds3-M3", "multi-tile-world16-M2", "many-small-tensors"):
         c = SMALL[name]
         run = Run(c)
         try:
@@ -227,9 +254,10 @@ def test_gather_matches_oracle():
             torch.cuda.synchronize()
             outs = [torch.full((max(n, 1),), -1, dtype=torch.int16, device="cuda") for n in c.numels]
             # odd offsets inside a larger buffer exercise the unaligned paths
-            big = torch.full((sum(c.numels) + 64,), -1, dtype=torch.int16, device="cuda")
+            big = torch.full((sum(c.numels) + len(c.numels) + 64,), -1, dtype=torch.int16, device="cuda")
             ptrs, views, off = [], [], 3
             for n in c.numels:
+                assert off + n <= big.numel()  # every destination inside the buffer
                 views.append(big[off:off + n])
                 ptrs.append(big.data_ptr() + 2 * off)
                 off += n + 1
@@ -485,6 +513,32 @@ def test_unused_tensors_masked_update(fp32, zeros):
                 if not c.tensor_flags[i]:
                     assert got_steps[i] == steps[i], (i, got_steps, steps)
             master, m, v, bits = res.master, res.m, res.v, res.params_bf16
+    finally:
+        run.close()
+
+
+def test_masked_update_with_many_small_tensors():
+    """A random half of 3000 small tensors without a gradient: nearly every
+    norm and update tile spans tensors with and without one (the per-element
+    segment walk, not the whole-tile shortcut)."""
+    c = SMALL["many-small-tensors"]
+    run = Run(c)
+    try:
+        n = len(c.numels)
+        rng = np.random.default_rng(7)
+        used = rng.integers(0, 2, n).tolist()
+        steps = [0] * n
+        steps_dev = torch.zeros(n, dtype=torch.int32, device="cuda")
+        master, m, v = run.state_host()
+        bits = run.params[:run.nsp].cpu().numpy().view(np.uint16).copy()
+        run.reduce(emit=False)
+        run.masked_update(torch.tensor(used, dtype=torch.uint8, device="cuda"), steps_dev)
+        torch.cuda.synchronize()
+        assert run.check_flags() == 0
+        res, steps = oracle.full_update_masked(run.op, run.bucket_inputs, c.n_micro, c.hp, c.max_norm,
+                                               used, steps, master, m, v, bits)
+        full_check(run, res, "many small tensors, masked")
+        assert steps_dev.cpu().tolist() == steps
     finally:
         run.close()
 
