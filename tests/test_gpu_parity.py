@@ -354,7 +354,8 @@ def test_argument_errors():
         run.close()
 
 
-@pytest.mark.parametrize("name", ["multi-tile-world16-M2", "odd-ds3-M3", "tiny-world4"])
+@pytest.mark.parametrize("name", ["multi-tile-world16-M2", "odd-ds3-M3", "tiny-world4", "fp32-grads-world8-M3",
+                                  "many-small-tensors"])
 def test_step_from_host_matches_device_path(name):
     """grs_step_from_host (host gradients, pipelined copies, per-bucket
     reductions) gives the device path's results bit for bit, and reads the
@@ -365,9 +366,10 @@ def test_step_from_host_matches_device_path(name):
     b = Run(c)
     try:
         W, M = c.world, c.n_micro
-        host = [torch.empty(a.grads[j][k].numel(), dtype=torch.int16).pin_memory()
+        gdt = a.grads[0][0].dtype  # bf16, or fp32 for GRS_PLAN_FP32_GRADS plans
+        host = [torch.empty(a.grads[j][k].numel(), dtype=gdt).pin_memory()
                 for j in range(M) for k in range(W)]
-        stage = [torch.empty(a.grads[0][0].numel(), dtype=torch.bfloat16, device="cuda")
+        stage = [torch.empty(a.grads[0][0].numel(), dtype=gdt, device="cuda")
                  for _ in range(2 * W)]
         out_params = torch.empty(a.nsp, dtype=torch.int16).pin_memory()
         out_norm = torch.empty(1, dtype=torch.float64).pin_memory()
@@ -377,7 +379,7 @@ def test_step_from_host_matches_device_path(name):
                 a.fill_grads(step_seed=2)
             for j in range(M):
                 for k in range(W):
-                    host[j * W + k].copy_(a.grads[j][k].view(torch.int16))
+                    host[j * W + k].copy_(a.grads[j][k])
             a.update()
             hp = g.make_adamw(c.hp[0], c.hp[1], c.hp[2], c.hp[3], c.hp[4], c.max_norm, step, M)
             g.grs_step_from_host(b.plan, hp, [t.data_ptr() for t in host], [t.data_ptr() for t in stage],
