@@ -118,6 +118,42 @@ def test_restore_across_bucket_size_and_ownership(tmp_path):
         b.close()
 
 
+def test_restore_many_small_tensors_across_tp(tmp_path):
+    """1500 small tensors of all tags (zero-size and frozen ones among them)
+    saved under tp 2 x dp_replicate 2 x dp_shard 4 and restored under tp 4 x
+    dp_shard 4 with another bucket size: the logical state is identical and
+    every padding element of the reader's layout is zero."""
+    from gradient_reduction_sharded_gb300 import checkpoint as ck
+    rng = np.random.default_rng(31)
+    owners = rng.integers(0, 4, 1500).tolist()
+    numels = [int(x) * (4 if o == LS else 1) for x, o in zip(rng.integers(0, 120, 1500), owners)]
+    flags = [1 if i % 97 == 5 else 0 for i in range(1500)]
+    ca = Case(numels, owners, 16, 2, 2, 4, 1 << 15, 1, 1e-2, 54, tensor_flags=flags)
+    cb = Case(numels, owners, 16, 4, 1, 4, 1 << 13, 1, 1e-2, 54, tensor_flags=flags)
+    a, b = Run(ca), Run(cb)
+    try:
+        a.update()
+        torch.cuda.synchronize()
+        d = str(tmp_path / "ckpt3")
+        ck.save(d, a.plan, spec_of(ck, ca), {"master": a.master, "exp_avg": a.m, "exp_avg_sq": a.v},
+                {"step": 1})
+        for t in (b.master, b.m, b.v):
+            t.fill_(float("nan"))
+        ck.load(d, b.plan, {"master": b.master, "exp_avg": b.m, "exp_avg_sq": b.v})
+        pad = np.ones(b.nsp, bool)
+        for bb in range(b.op.n_buckets):
+            for t in range(b.op.copies(bb)):
+                o = int(b.op.b_state_off[bb]) + t * int(b.op.b_padded[bb])
+                pad[o:o + int(b.op.b_used[bb])] = False
+        for ta, tb in ((a.master, b.master), (a.m, b.m), (a.v, b.v)):
+            assert np.array_equal(logical(a, ta), logical(b, tb))
+            hb = tb[:b.nsp].cpu().numpy()
+            assert np.all(hb[pad] == 0) and not np.isnan(hb).any()
+    finally:
+        a.close()
+        b.close()
+
+
 def test_state_logical_kernels_match_oracle():
     c = Case([21, 5, 18, 3, 1001, 77, 4096], [RA, PS, LS, AR, RA, PS, LS], 6, 2, 1, 3, 256, 1, 1e-2, 53,
              tensor_flags=[0, 0, 0, 1, 0, 0, 0])
