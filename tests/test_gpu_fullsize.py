@@ -20,6 +20,8 @@ import oracle
 import workloads
 from gpu_support import assert_bf16_cast, assert_close, assert_close_bracketed
 
+RA = workloads.REPLICA_AVG
+
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 
@@ -63,10 +65,24 @@ def test_full_size_variant_matches_oracle(cid, variant, window):
     _full_size(cid, variant, window)
 
 
+def test_single_tensor_beyond_32_bit_indices():
+    """One REPLICA_AVG tensor of 2^31 + 4099 elements (world 1): every index
+    of the reduction, norm, update and padding lies past the 32-bit range at
+    the end of the tensor, where the samples include the last elements and
+    the padding."""
+    w = workloads.Workload(90, "single-2^31+4099", [workloads.Tensor("w", (2 ** 31 + 4099,), RA)],
+                           tp=1, dp_replicate=1, dp_shard=1, n_micro=1, grad_std=1e-3)
+    _full_size_w(w, "plain", 0)
+
+
 def _full_size(cid, variant, window):
+    _full_size_w(workloads.get(cid), variant, window)
+
+
+def _full_size_w(w, variant, window):
     import bench  # the benchmark's own update object
 
-    w = workloads.get(cid)
+    cid = w.name
     M = window or w.n_micro
     fp32 = variant == "fp32-grads"
     flags = bench.frozen_pattern(len(w.numels)) if variant == "frozen" else None
@@ -77,7 +93,7 @@ def _full_size(cid, variant, window):
     if _free_gb() < need * 1.05 + 4:
         pytest.skip(f"needs {need:.0f} GB of device memory")
     dev = torch.device("cuda")
-    rng = np.random.default_rng(1000 + cid)
+    rng = np.random.default_rng(1000 + w.cid)
     u = bench.GpuUpdate(w, dev, variant, window)
     assert u.info["n_state_pad"] == op.n_state_pad and u.n_micro == M
     gview = torch.float32 if fp32 else torch.int16
