@@ -75,6 +75,42 @@ def test_single_tensor_beyond_32_bit_indices():
     _full_size_w(w, "plain", 0)
 
 
+def test_gather_and_layout_beyond_32_bit_indices():
+    """The same 2^31 + 4099-element tensor through the gather to per-tensor
+    storage and the state <-> logical conversions: for one tensor on one
+    rank both are the identity on its elements, and the padding comes back
+    as zeros."""
+    from gradient_reduction_sharded_gb300 import grs
+    n = 2 ** 31 + 4099
+    if _free_gb() < 4 * n * 2 / 1e9 + 4 * n * 4 / 1e9 + 4:
+        pytest.skip("needs about 52 GB of device memory")
+    plan = grs.grs_plan_create([n], [RA], 1, 1, 1, 1, 25 << 20)
+    try:
+        info = grs.grs_plan_query(plan)
+        nsp = info["n_state_pad"]
+        assert nsp == (n + 7) // 8 * 8
+        s = torch.cuda.current_stream().cuda_stream
+        gen = torch.Generator(device="cuda").manual_seed(5)
+        params = torch.randint(-32768, 32767, (nsp,), dtype=torch.int16, device="cuda", generator=gen)
+        out = torch.empty(n, dtype=torch.int16, device="cuda")
+        grs.grs_gather_params(plan, params.data_ptr(), [out.data_ptr()], s)
+        torch.cuda.synchronize()
+        assert torch.equal(out, params[:n])
+        del out, params
+        state = torch.randn(nsp, device="cuda", generator=gen)
+        logical = torch.empty(n, device="cuda")
+        grs.grs_state_to_logical(plan, state.data_ptr(), logical.data_ptr(), s)
+        back = torch.full((nsp,), float("nan"), device="cuda")
+        grs.grs_state_from_logical(plan, logical.data_ptr(), back.data_ptr(), s)
+        torch.cuda.synchronize()
+        assert grs.grs_check_device_errors(plan, s) == 0
+        assert torch.equal(logical, state[:n])
+        assert torch.equal(back[:n], state[:n]) and bool((back[n:] == 0).all())
+    finally:
+        grs.grs_plan_destroy(plan)
+        torch.cuda.empty_cache()
+
+
 def _full_size(cid, variant, window):
     _full_size_w(workloads.get(cid), variant, window)
 
