@@ -46,6 +46,16 @@
  *   Padding (bucket element index >= used) is ignored on input, may hold
  *       anything (NaN included), and is written as exact zeros in every
  *       output.
+ *
+ * Concurrency.  A plan does not change after grs_plan_create except for its
+ * device error flags and the copy stream and events that grs_step_from_host
+ * creates on first use.  Calls on one plan may come from several host
+ * threads and streams as long as the buffers they write do not overlap on
+ * the GPU; the error flags are shared, so grs_check_device_errors reports
+ * (and clears) a flag raised by any call on the plan.  grs_step_from_host
+ * calls on one plan must not overlap each other (they share the plan's copy
+ * stream and events).  Separate plans share nothing but the allocation-free
+ * norm's static scratch.
  */
 #ifndef GRS_H
 #define GRS_H
