@@ -204,7 +204,7 @@ class GpuUpdate:
     """All device buffers of one workload and the calls of one update."""
 
     def __init__(self, w: workloads.Workload, device, variant: str = "plain", window: int = 0,
-                 graph: bool = False):
+                 graph: bool = False, small: bool = False):
         import torch
         from gradient_reduction_sharded_gb300 import grs
         self.torch, self.grs, self.w, self.dev = torch, grs, w, device
@@ -248,6 +248,11 @@ class GpuUpdate:
         # plain reduction and norm.
         self.graph = None
         self.graphed = graph
+        # One launch for the whole update (grs_update_small): plain updates of
+        # plans within its tile and buffer limits only.
+        self.small = small
+        if small and (variant != "plain" or graph):
+            raise ValueError("--small runs the plain eager update only")
         if graph:
             if variant != "plain":
                 raise ValueError("--graph runs the plain update only")
@@ -256,6 +261,8 @@ class GpuUpdate:
         # kernels per step: one reduction per microbatch, the norm finish and the
         # update; the masked path adds its norm pass and the per-tensor factors
         self.launches_per_step = self.n_micro + (4 if self.used is not None else 3 if graph else 2)
+        if small:
+            self.launches_per_step = 1
 
     def algorithmic_bytes(self) -> dict:
         """Per-kernel algorithmic bytes of one update of this variant."""
@@ -317,9 +324,22 @@ class GpuUpdate:
         torch.cuda.synchronize(self.dev)
         self.graph = g
 
+    def small_step(self):
+        a = self.w.adamw
+        self.step_no += 1
+        hp = self.grs.make_adamw(a.lr, a.beta1, a.beta2, a.eps, a.weight_decay, a.max_norm,
+                                 self.step_no, self.n_micro)
+        self.grs.grs_update_small(self.plan, hp, [p for j in range(self.n_micro) for p in self.ptrs[j]],
+                                  self.acc.data_ptr(), self.master.data_ptr(), self.m.data_ptr(),
+                                  self.v.data_ptr(), self.params.data_ptr(), self.norm.data_ptr(),
+                                  self.stream)
+
     def step(self):
         if self.graph is not None:
             self.graph.replay()
+            return
+        if self.small:
+            self.small_step()
             return
         self.reduce()
         self.norm_sq()
@@ -335,9 +355,9 @@ def run_gpu(args, rank, world_size, local_rank):
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
     w = bench_workload(args)
-    u = GpuUpdate(w, device, args.variant, args.window, args.graph)
+    u = GpuUpdate(w, device, args.variant, args.window, args.graph, args.small)
     mb = u.algorithmic_bytes()
-    plain = args.variant == "plain" and u.n_micro == w.n_micro and not args.graph
+    plain = args.variant == "plain" and u.n_micro == w.n_micro and not args.graph and not args.small
     clocks = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[0])
                           if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit()
                           else local_rank)
@@ -405,6 +425,12 @@ def run_gpu(args, rank, world_size, local_rank):
     for i in range(K):
         flush_l2()
         ev[i][0].record()
+        if u.small:  # one launch: the whole update lands in the first slot
+            u.small_step()
+            ev[i][1].record()
+            ev[i][2].record()
+            ev[i][3].record()
+            continue
         u.reduce()
         ev[i][1].record()
         u.norm_sq()
@@ -453,8 +479,12 @@ def run_gpu(args, rank, world_size, local_rank):
     kern["reduce"]["ms_per_launch"] = kern["reduce"]["ms"] / M
     kern["update"]["ms_per_launch"] = kern["update"]["ms"]
     kern["norm"]["ms_per_launch"] = kern["norm"]["ms"]
-    dom = max(("reduce", "update", "norm"),
-              key=lambda k: kern[k]["ms"] if kern[k]["bytes"] else -1.0)
+    if u.small:
+        kern = {"update_small": {"ms": statistics.mean(red_ms), "ms_median": statistics.median(red_ms),
+                                 "bytes": mb["total"], "launches_per_step": 1, "ms_per_launch":
+                                 statistics.mean(red_ms),
+                                 "note": "reduction of every microbatch, norm, clip + AdamW in one cluster launch"}}
+    dom = max(kern, key=lambda k: kern[k]["ms"] if kern[k]["bytes"] else -1.0)
     dk = kern[dom]
     achieved = dk["bytes"] / (dk["ms_per_launch"] * 1e-3) / 1e9
     traffic = load_traffic(dom, w, u.variant)
@@ -502,6 +532,8 @@ def variant_config(u: GpuUpdate) -> dict:
         out["variant"] = u.variant
     if u.graphed:
         out["cuda_graph"] = "whole update replayed from one capture (device step counts)"
+    if u.small:
+        out["single_launch"] = "grs_update_small: one thread-block cluster for the whole update"
     if u.n_micro != u.w.n_micro:
         out["window"] = {"microbatches": u.n_micro, "of": u.w.n_micro}
         out["microbatches"] = u.n_micro
@@ -1131,6 +1163,8 @@ def main():
                          "(masked norm and update); frozen: some tensors frozen at plan time")
     ap.add_argument("--checkpoint", action="store_true",
                     help="measure checkpoint restore with reshard (layout kernels + files) instead")
+    ap.add_argument("--small", action="store_true",
+                    help="the whole update in one launch (grs_update_small; plans of at most 128 tiles)")
     ap.add_argument("--graph", action="store_true",
                     help="replay the whole update as one captured CUDA graph (launch-bound workloads)")
     ap.add_argument("--micro", type=int, default=0,

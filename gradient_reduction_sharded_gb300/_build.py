@@ -19,7 +19,7 @@ CHECKED_LIB = os.path.join(PKG, "checked", "libgrs.so")
 CHECKED_FLAGS = ("-DGRS_CHECKED=1",)
 
 SOURCES = ["plan.cpp", "api.cu", "kernels_reduce.cu", "kernels_update.cu", "kernels_gather.cu",
-           "noalloc.cu", "host_step.cu", "kernels_masked.cu"]
+           "noalloc.cu", "host_step.cu", "kernels_masked.cu", "kernels_small.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -367,6 +367,43 @@ grs_status grs_clip_adamw_step(const grs_plan* p, const grs_adamw* hp, const dou
   return GRS_OK;
 }
 
+grs_status grs_update_small(const grs_plan* p, const grs_adamw* hp, const void* const* rank_grads, float* acc,
+                            float* master, float* m, float* v, uint16_t* params_bf16, double* d_norm_sq,
+                            void* stream) {
+  grs_status st = check_plan_device(p);
+  if (st != GRS_OK) return st;
+  if (hp == nullptr || rank_grads == nullptr || acc == nullptr || master == nullptr || m == nullptr ||
+      v == nullptr || params_bf16 == nullptr || d_norm_sq == nullptr)
+    return fail(GRS_ERR_INVALID_ARG, "grs_update_small: NULL argument");
+  if (hp->step < 1 || hp->n_micro < 1)
+    return fail(GRS_ERR_INVALID_ARG, "grs_update_small: step and n_micro must be >= 1");
+  if (p->n_red_tiles > GRS_SMALL_MAX_TILES || static_cast<int64_t>(p->units.size()) > GRS_SMALL_MAX_TILES)
+    return fail(GRS_ERR_SHAPE, "grs_update_small: the plan has " + std::to_string(p->n_red_tiles) +
+                                   " reduction tiles in " + std::to_string(p->units.size()) +
+                                   " bucket rows; the single-launch path takes at most " +
+                                   std::to_string(GRS_SMALL_MAX_TILES) + " of each");
+  const int64_t nbuf = int64_t(hp->n_micro) * p->world;
+  if (nbuf > GRS_SMALL_MAX_BUFFERS)
+    return fail(GRS_ERR_SHAPE, "grs_update_small: n_micro x world = " + std::to_string(nbuf) +
+                                   " gradient buffers; the single-launch path takes at most " +
+                                   std::to_string(GRS_SMALL_MAX_BUFFERS));
+  for (int64_t k = 0; k < nbuf; ++k) {
+    if (rank_grads[k] == nullptr)
+      return fail(GRS_ERR_INVALID_ARG, "grs_update_small: gradient buffer " + std::to_string(k) + " is NULL");
+    if (!aligned16(rank_grads[k]))
+      return fail(GRS_ERR_ALIGNMENT, "grs_update_small: gradient buffer " + std::to_string(k) +
+                                         " not 16-byte aligned");
+  }
+  if (!aligned16(acc) || !aligned16(master) || !aligned16(m) || !aligned16(v) || !aligned16(params_bf16) ||
+      (reinterpret_cast<uintptr_t>(d_norm_sq) & 7u) != 0)
+    return fail(GRS_ERR_ALIGNMENT, "grs_update_small: buffer not 16-byte aligned");
+  DeviceGuard g(p->device);
+  if (!g.ok()) return fail(GRS_ERR_CUDA, "grs_update_small: cannot select the plan's device");
+  const int e = grs::launch_update_small(p, hp, rank_grads, acc, master, m, v, params_bf16, d_norm_sq, stream);
+  if (e != 0) return cuda_fail(static_cast<cudaError_t>(e), "grs_update_small");
+  return GRS_OK;
+}
+
 grs_status grs_gather_params(const grs_plan* p, const uint16_t* params_bf16, uint16_t* const* tensor_ptrs,
                              void* stream) {
   grs_status st = check_plan_device(p);
@@ -489,7 +526,7 @@ grs_status grs_check_device_errors(const grs_plan* p, void* stream) {
     static const char* const kSite[grs::SITE_COUNT] = {
         "?", "reduce_kernel", "norm_pass1_kernel", "update_kernel", "accumulate_kernel", "gather_kernel",
         "state_logical_kernel", "norm_pass1_masked_kernel", "update_masked_kernel",
-        "check_already_reduced_kernel"};
+        "check_already_reduced_kernel", "small_update_kernel"};
     const int site = h[grs::FLAG_BOUNDS] > 0 && h[grs::FLAG_BOUNDS] < grs::SITE_COUNT ? h[grs::FLAG_BOUNDS] : 0;
     return fail(GRS_ERR_BOUNDS, std::string("checked build: an index left its buffer in ") + kSite[site]);
   }

@@ -159,6 +159,69 @@ __device__ __forceinline__ void set_bf16x8(float (&a)[8], const uint4& w) {
   a[7] = bf16_hi(w.w);
 }
 
+// Sum of eight elements over the rank rows, in rank order: set() takes the
+// first rank's 8 elements, add() each further rank's, finish() the sums.
+// The rows come from shared memory (set/add: the reduction's TMA stages) or
+// global memory (set_g/add_g: 16-byte loads); the arithmetic is the same.
+// bf16 rows (16 bytes per 8 elements): plain fp32 adds — a sum of bf16
+// values is exact in fp32 unless an input is 2^24 times smaller than the
+// largest, so the result is the correctly rounded sum in practice.
+// fp32 rows (32 bytes): Knuth's TwoSum keeps each add's rounding error in a
+// compensation term added at the end, so the sum is accurate relative to
+// the result, not to the operands (where gradients nearly cancel, AdamW's
+// g / (|g| + eps) would otherwise magnify an operand-relative error).
+template <typename E>
+struct Sum8;
+template <>
+struct Sum8<uint16_t> {
+  float v[8];
+  __device__ __forceinline__ void set(const uint8_t* p) { set_bf16x8(v, lds128(p)); }
+  __device__ __forceinline__ void add(const uint8_t* p) { add_bf16x8(v, lds128(p)); }
+  __device__ __forceinline__ void set_g(const uint16_t* p) { set_bf16x8(v, __ldg(reinterpret_cast<const uint4*>(p))); }
+  __device__ __forceinline__ void add_g(const uint16_t* p) { add_bf16x8(v, __ldg(reinterpret_cast<const uint4*>(p))); }
+  __device__ __forceinline__ void finish(float (&o)[8]) const {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) o[q] = v[q];
+  }
+};
+template <>
+struct Sum8<float> {
+  float v[8], c[8];
+  __device__ __forceinline__ void set_w(const uint4& a, const uint4& b) {
+    v[0] = __uint_as_float(a.x); v[1] = __uint_as_float(a.y); v[2] = __uint_as_float(a.z); v[3] = __uint_as_float(a.w);
+    v[4] = __uint_as_float(b.x); v[5] = __uint_as_float(b.y); v[6] = __uint_as_float(b.z); v[7] = __uint_as_float(b.w);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) c[q] = 0.0f;
+  }
+  __device__ __forceinline__ void two_sum(int q, float x) {
+    const float t = __fadd_rn(v[q], x);
+    const float z = __fsub_rn(t, v[q]);
+    const float err = __fadd_rn(__fsub_rn(v[q], __fsub_rn(t, z)), __fsub_rn(x, z));
+    c[q] = __fadd_rn(c[q], err);
+    v[q] = t;
+  }
+  __device__ __forceinline__ void add_w(const uint4& a, const uint4& b) {
+    two_sum(0, __uint_as_float(a.x)); two_sum(1, __uint_as_float(a.y));
+    two_sum(2, __uint_as_float(a.z)); two_sum(3, __uint_as_float(a.w));
+    two_sum(4, __uint_as_float(b.x)); two_sum(5, __uint_as_float(b.y));
+    two_sum(6, __uint_as_float(b.z)); two_sum(7, __uint_as_float(b.w));
+  }
+  __device__ __forceinline__ void set(const uint8_t* p) { set_w(lds128(p), lds128(p + 16)); }
+  __device__ __forceinline__ void add(const uint8_t* p) { add_w(lds128(p), lds128(p + 16)); }
+  __device__ __forceinline__ void set_g(const float* p) {
+    const uint4* q = reinterpret_cast<const uint4*>(p);
+    set_w(__ldg(q), __ldg(q + 1));
+  }
+  __device__ __forceinline__ void add_g(const float* p) {
+    const uint4* q = reinterpret_cast<const uint4*>(p);
+    add_w(__ldg(q), __ldg(q + 1));
+  }
+  __device__ __forceinline__ void finish(float (&o)[8]) const {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) o[q] = __fadd_rn(v[q], c[q]);
+  }
+};
+
 // Last unit u with prefix[u] <= tile (prefix has n_units + 1 entries).
 __device__ __forceinline__ int find_unit(const int64_t* __restrict__ prefix, int lo, int hi,
                                          int64_t tile) {

@@ -180,7 +180,8 @@ enum : int {
   SITE_NORM1_MASKED = 7,
   SITE_UPDATE_MASKED = 8,
   SITE_AR_CHECK = 9,
-  SITE_COUNT = 10
+  SITE_SMALL = 10,
+  SITE_COUNT = 11
 };
 
 // Programmatic dependent launch between the path's kernels: measured on
@@ -223,6 +224,8 @@ void bias_factors(const grs_adamw* hp, int32_t step, float* step_size, float* in
 int launch_update(const grs_plan* p, const grs_adamw* hp, const double* d_norm_sq, const float* acc,
                   float* master, float* m, float* v, uint16_t* params, void* stream);
 int launch_accumulate(const grs_plan* p, int32_t bucket, float* acc, const float* mb, void* stream);
+int launch_update_small(const grs_plan* p, const grs_adamw* hp, const void* const* rank_grads, float* acc,
+                        float* master, float* m, float* v, uint16_t* params, double* d_norm_sq, void* stream);
 int launch_gather(const grs_plan* p, const uint16_t* params, uint16_t* const* tensor_ptrs,
                   void* stream);
 int launch_bounded_wait_selftest(const grs_plan* p, uint64_t limit_ns, void* stream);

@@ -33,6 +33,8 @@ GRS_PLAN_FP32_GRADS = 2
 GRS_TENSOR_FROZEN = 1
 GRS_MAX_WORLD = 128
 GRS_NOALLOC_SCRATCH_BYTES = 4 << 20
+GRS_SMALL_MAX_TILES = 128
+GRS_SMALL_MAX_BUFFERS = 256
 
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED_COMPOSITION", 3: "SHAPE",
                 4: "ALIGNMENT", 5: "CUDA", 6: "TIMEOUT", 7: "NONFINITE", 8: "NO_DEVICE",
@@ -124,6 +126,7 @@ _sig = {
     "grs_grad_norm_sq_noalloc": ([_vp, _vp, ctypes.c_int32, _vp, _vp], ctypes.c_int),
     "grs_step_from_host": ([_vp, _P(grs_adamw), _P(_vp), _P(_vp), _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                             _vp, _vp, _vp], ctypes.c_int),
+    "grs_update_small": ([_vp, _P(grs_adamw), _P(_vp), _vp, _vp, _vp, _vp, _vp, _vp, _vp], ctypes.c_int),
     "grs_last_error": ([], ctypes.c_char_p),
     "grs_build_features": ([], ctypes.c_uint32),
 }
@@ -286,6 +289,14 @@ def grs_clip_adamw_step_masked(plan: int, hp: grs_adamw, d_norm_sq: Optional[int
     _check(_lib.grs_clip_adamw_step_masked(plan, ctypes.byref(hp), d_norm_sq, acc, master, m, v,
                                            params_bf16, d_tensor_used, d_tensor_steps, workspace, stream),
            "grs_clip_adamw_step_masked")
+
+
+def grs_update_small(plan: int, hp: grs_adamw, rank_grads: Sequence[int], acc: int, master: int, m: int,
+                     v: int, params_bf16: int, d_norm_sq: int, stream: int) -> None:
+    """The whole update of a small plan in one launch; rank_grads holds
+    n_micro * world buffers, microbatch-major."""
+    _check(_lib.grs_update_small(plan, ctypes.byref(hp), _ptrs(rank_grads), acc, master, m, v, params_bf16,
+                                 d_norm_sq, stream), "grs_update_small")
 
 
 def grs_state_to_logical(plan: int, state: int, logical: int, stream: int) -> None:

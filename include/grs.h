@@ -354,6 +354,38 @@ grs_status grs_clip_adamw_step_masked(const grs_plan* plan, const grs_adamw* hp,
                                       uint16_t* params_bf16, const uint8_t* d_tensor_used,
                                       int32_t* d_tensor_steps, void* workspace, void* stream);
 
+/* ------------------------------------------ single-launch small plans */
+
+#define GRS_SMALL_MAX_TILES 128   /* reduction tiles (grs_plan_info.n_reduce_tiles), and bucket rows */
+#define GRS_SMALL_MAX_BUFFERS 256 /* n_micro x world gradient buffers */
+
+/* The whole update of a small plan in one kernel launch: the reductions of
+ * hp->n_micro microbatches (as grs_reduce_all with accumulate = j > 0),
+ * the global squared norm (as grs_grad_norm_sq) and clip + AdamW + bf16
+ * cast (as grs_clip_adamw_step), with the same arithmetic in the same
+ * order, so every output equals the three calls' bit for bit ([ISSUE]
+ * "Preserved prototype and evidence", "Proposed scope": FP32 reduction,
+ * accumulation, clipping, optimizer update).  For plans whose four
+ * launches cost more than their memory traffic: one thread-block cluster
+ * of up to 8 CTAs, the norm partials exchanged through distributed shared
+ * memory.
+ *   rank_grads : host array [n_micro * world] of device pointers,
+ *                microbatch-major (buffer j * world + k is rank k's
+ *                gradients of microbatch j), each [n_rank_pad] bf16 bits (fp32
+ *                for GRS_PLAN_FP32_GRADS plans), 16-byte aligned, non-NULL.
+ *   acc, master, m, v : device fp32 [n_state_pad]; acc is written (the
+ *                accumulated gradient sum), master, m, v updated in place.
+ *   params_bf16: device bf16 bits [n_state_pad], written.
+ *   d_norm_sq  : device double, written (S of grs_grad_norm_sq); required.
+ * No workspace.  Errors: INVALID_ARG (NULL, step or n_micro < 1), SHAPE
+ * (more than GRS_SMALL_MAX_TILES reduction tiles or bucket rows, or more
+ * than GRS_SMALL_MAX_BUFFERS gradient buffers: use the multi-kernel path),
+ * ALIGNMENT, NO_DEVICE, CUDA.
+ * A non-finite norm raises the flag grs_check_device_errors reports. */
+grs_status grs_update_small(const grs_plan* plan, const grs_adamw* hp, const void* const* rank_grads,
+                            float* acc, float* master, float* m, float* v, uint16_t* params_bf16,
+                            double* d_norm_sq, void* stream);
+
 /* Gather: copy every tensor from the bucket-ordered bf16 parameter buffer
  * to its own full logical tensor ([COSMOS] section 2: all-gather of
  * parameters across shards; LOCAL_SHARD tensors reassembled from their tp

@@ -576,6 +576,45 @@ def test_masked_path_with_every_tensor_used_equals_plain_path(hint):
         b.close()
 
 
+@pytest.mark.parametrize("name", ["tiny-world4", "odd-ds2", "odd-ds3-M3", "world1", "world3-non-pow2",
+                                  "world6-auto-shard", "zero-size-tensors", "fp32-grads-world8-M3", "tp4-world8",
+                                  "world64-tp4-M2", "multi-tile-world16-M2"])
+def test_single_launch_update_equals_three_calls(name):
+    """grs_update_small (one cluster launch: reductions of every microbatch,
+    norm, clip + AdamW) gives the accumulator, norm, master, moments and bf16
+    parameters of grs_reduce_all + grs_grad_norm_sq + grs_clip_adamw_step
+    bit for bit, over three steps; plans beyond its limits are refused."""
+    g = grs()
+    c = SMALL[name]
+    a, b = Run(c), Run(c)
+    try:
+        bufs = lambda r: [p for j in range(c.n_micro) for p in r.ptrs(j)]
+        norm = torch.zeros(1, dtype=torch.float64, device="cuda")
+        if a.info["n_reduce_tiles"] > g.GRS_SMALL_MAX_TILES or c.n_micro * c.world > g.GRS_SMALL_MAX_BUFFERS:
+            hp = g.make_adamw(*c.hp, c.max_norm, 1, c.n_micro)
+            with pytest.raises(g.GrsError) as ei:
+                g.grs_update_small(b.plan, hp, bufs(b), b.acc.data_ptr(), b.master.data_ptr(), b.m.data_ptr(),
+                                   b.v.data_ptr(), b.params.data_ptr(), norm.data_ptr(), b.stream())
+            assert ei.value.status == g.GRS_ERR_SHAPE
+            return
+        for step in range(1, 4):
+            if step > 1:
+                a.fill_grads(step_seed=step)
+                b.fill_grads(step_seed=step)
+            a.update()
+            hp = g.make_adamw(*c.hp, c.max_norm, step, c.n_micro)
+            g.grs_update_small(b.plan, hp, bufs(b), b.acc.data_ptr(), b.master.data_ptr(), b.m.data_ptr(),
+                               b.v.data_ptr(), b.params.data_ptr(), norm.data_ptr(), b.stream())
+            torch.cuda.synchronize()
+            assert a.check_flags() == 0 and b.check_flags() == 0
+            assert torch.equal(a.norm, norm), (step, float(a.norm[0]), float(norm[0]))
+            for nm in ("acc", "master", "m", "v", "params"):
+                assert torch.equal(getattr(a, nm)[:a.nsp], getattr(b, nm)[:b.nsp]), (step, nm)
+    finally:
+        a.close()
+        b.close()
+
+
 def test_trailing_accumulation_window():
     """A window that ends after 3 of 4 microbatches: the update averages the
     3 accumulated microbatches (G = acc / 3)."""
