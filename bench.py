@@ -450,6 +450,7 @@ def run_gpu(args, rank, world_size, local_rank):
     gather = run_gather(u, args, torch) if plain else None
     if gather is not None and flush:
         gather["l2"] = "parameters fit in L2: back-to-back gathers read them from the cache"
+    accumulate = run_accumulate(u, args, torch) if plain else None
 
     # ---------------------------------------------------------------- e2e
     e2e = None if (args.no_e2e or not plain) else run_e2e(u, args, torch)
@@ -509,6 +510,7 @@ def run_gpu(args, rank, world_size, local_rank):
         "kernels": {k: {kk: vv for kk, vv in v.items()} for k, v in kern.items()},
         "e2e": e2e,
         "gather": gather,
+        "accumulate": accumulate,
         "gpu_launches": u.launches_per_step * K,
         "kernel_timing": "second region of K steps with CUDA events between the kernels",
         "per_update_ms": {"median": statistics.median(upd_total), "min": upd_total[0],
@@ -571,6 +573,35 @@ def run_gather(u: GpuUpdate, args, torch):
     nbytes = 4 * w.n_unique
     del outs
     return {"ms": ms, "bytes": nbytes, "gbs": nbytes / (ms * 1e-3) / 1e9}
+
+
+def run_accumulate(u: GpuUpdate, args, torch):
+    """grs_accumulate over every bucket (adding a separately reduced fp32
+    microbatch into the accumulator), timed on its own: it is not on the
+    update's path, where the reduction accumulates in its own epilogue.
+    Algorithmic bytes: read acc and the microbatch, write acc, 4 each."""
+    mbuf = torch.zeros_like(u.acc)
+    nsp = u.info["n_state_pad"]
+    offs = [(b, int(d["state_offset"])) for b, d in enumerate(u.buckets)]
+
+    def once():
+        for b, off in offs:
+            u.grs.grs_accumulate(u.plan, b, u.acc.data_ptr() + 4 * off, mbuf.data_ptr() + 4 * off, u.stream)
+
+    for _ in range(3):
+        once()
+    torch.cuda.synchronize()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(args.steps):
+        once()
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / args.steps
+    nbytes = 12 * nsp
+    del mbuf
+    return {"ms": ms, "bytes": nbytes, "gbs": nbytes / (ms * 1e-3) / 1e9, "launches": len(offs)}
 
 
 def run_e2e(u: GpuUpdate, args, torch):
