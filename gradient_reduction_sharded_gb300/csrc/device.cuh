@@ -222,6 +222,32 @@ struct Sum8<float> {
   }
 };
 
+// Gradient scale of the update: 1/M times the clip coefficient
+// c = min(1, max_norm / (sqrt(S) + 1e-6)) (NaN kept), evaluated in fp32 from
+// the device-resident S; max_norm <= 0 turns clipping off.  Every update
+// kernel uses this one expression.
+__device__ __forceinline__ float clip_gscale(double norm_sq, float max_norm, float inv_m) {
+  if (!(max_norm > 0.0f)) return inv_m;
+  const float cr = max_norm / (sqrtf(static_cast<float>(norm_sq)) + 1e-6f);
+  return __fmul_rn((cr < 1.0f || isnan(cr)) ? cr : 1.0f, inv_m);
+}
+
+// One AdamW step on one element, in place: torch.optim.AdamW's order of
+// operations (decoupled decay, moments, bias-corrected step) in fp32 with
+// explicit roundings.  step_size = lr / (1 - beta1^t), inv_bc2_sqrt =
+// 1 / sqrt(1 - beta2^t).  Every update kernel uses this one routine.
+__device__ __forceinline__ void adamw_elem(float G, float gscale, float step_size, float inv_bc2_sqrt,
+                                           const AdamwK& k, float& P, float& M, float& V) {
+  const float g = __fmul_rn(G, gscale);
+  const float p = __fmul_rn(P, k.decay);
+  const float mm = __fmaf_rn(k.b1, M, __fmul_rn(k.omb1, g));
+  const float vv = __fmaf_rn(k.b2, V, __fmul_rn(__fmul_rn(k.omb2, g), g));
+  const float denom = __fadd_rn(__fmul_rn(__fsqrt_rn(vv), inv_bc2_sqrt), k.eps);
+  P = __fsub_rn(p, __fmul_rn(step_size, __fdiv_rn(mm, denom)));
+  M = mm;
+  V = vv;
+}
+
 // Last unit u with prefix[u] <= tile (prefix has n_units + 1 entries).
 __device__ __forceinline__ int find_unit(const int64_t* __restrict__ prefix, int lo, int hi,
                                          int64_t tile) {

@@ -218,6 +218,15 @@ struct ReduceLaunch {
 int launch_reduce(const grs_plan* p, const ReduceLaunch& a, void* stream);
 int launch_norm(const grs_plan* p, const float* acc, int32_t n_micro, void* workspace,
                 int32_t partials_ready, double* d_norm_sq, void* stream);
+// The AdamW constants of one update (fp32, as the kernels apply them).
+struct AdamwK {
+  float decay;       // 1 - lr * wd
+  float b1, omb1;    // beta1, 1 - beta1
+  float b2, omb2;    // beta2, 1 - beta2
+  float eps;
+};
+AdamwK adamw_consts(const grs_adamw* hp);
+
 // Bias-corrected AdamW factors of step `step` computed on the host in fp64
 // and rounded to fp32: lr / (1 - beta1^step) and 1 / sqrt(1 - beta2^step).
 void bias_factors(const grs_adamw* hp, int32_t step, float* step_size, float* inv_bc2_sqrt);

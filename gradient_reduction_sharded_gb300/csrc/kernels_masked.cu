@@ -197,7 +197,7 @@ struct MaskedArgs {
   int* flags;
   int64_t n_state;  // elements of acc, master, m, v and params
   int32_t n_units;
-  float decay, b1, omb1, b2, omb2, eps;
+  AdamwK k;
   float max_norm;
   float inv_m;
 };
@@ -231,11 +231,7 @@ __global__ void __launch_bounds__(MUPD_THREADS, GRS_MUPD_MIN_BLOCKS) update_mask
   }
   if (on == 0 || el >= padded) return;
   if (!GRS_CHECK(i >= 0 && i + 8 <= a.n_state, a.flags, SITE_UPDATE_MASKED)) return;
-  float gscale = a.inv_m;
-  if (a.max_norm > 0.0f) {
-    const float cr = a.max_norm / (sqrtf(static_cast<float>(*a.norm_sq)) + 1e-6f);
-    gscale = __fmul_rn((cr < 1.0f || isnan(cr)) ? cr : 1.0f, a.inv_m);
-  }
+  const float gscale = a.max_norm > 0.0f ? clip_gscale(*a.norm_sq, a.max_norm, a.inv_m) : a.inv_m;
 
   // Otherwise: which of the eight elements change — padding (rewritten as
   // zeros) and elements of tensors with a gradient this step.  A group that
@@ -297,15 +293,7 @@ __global__ void __launch_bounds__(MUPD_THREADS, GRS_MUPD_MIN_BLOCKS) update_mask
       seg_advance(cur, a.sg, a.used_mask, e, used, a.flags, SITE_UPDATE_MASKED);
       f = __ldg(a.factors + cur.t);
     }
-    const float g = __fmul_rn(G[q], gscale);
-    float p = __fmul_rn(P[q], a.decay);
-    const float mm = __fmaf_rn(a.b1, M[q], __fmul_rn(a.omb1, g));
-    const float vv = __fmaf_rn(a.b2, V[q], __fmul_rn(__fmul_rn(a.omb2, g), g));
-    const float denom = __fadd_rn(__fmul_rn(__fsqrt_rn(vv), f.y), a.eps);
-    p = __fsub_rn(p, __fmul_rn(f.x, __fdiv_rn(mm, denom)));
-    P[q] = p;
-    M[q] = mm;
-    V[q] = vv;
+    adamw_elem(G[q], gscale, f.x, f.y, a.k, P[q], M[q], V[q]);
   }
   if (all) {
     __stcs(reinterpret_cast<float4*>(a.master + i), make_float4(P[0], P[1], P[2], P[3]));
@@ -383,13 +371,7 @@ int launch_update_masked(const grs_plan* p, const grs_adamw* hp, const double* d
   a.flags = p->d_flags;
   a.n_state = p->n_state_pad;
   a.n_units = static_cast<int32_t>(p->units.size());
-  const double lr = hp->lr, wd = hp->weight_decay;
-  a.decay = static_cast<float>(1.0 - lr * wd);
-  a.b1 = hp->beta1;
-  a.omb1 = static_cast<float>(1.0 - static_cast<double>(hp->beta1));
-  a.b2 = hp->beta2;
-  a.omb2 = static_cast<float>(1.0 - static_cast<double>(hp->beta2));
-  a.eps = hp->eps;
+  a.k = adamw_consts(hp);
   a.max_norm = hp->max_norm > 0.0f ? hp->max_norm : 0.0f;
   a.inv_m = static_cast<float>(1.0 / static_cast<double>(hp->n_micro));
   update_masked_kernel<<<static_cast<unsigned>(p->n_upd_tiles), MUPD_THREADS, 0, s>>>(a);

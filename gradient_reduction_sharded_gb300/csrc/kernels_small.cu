@@ -62,7 +62,7 @@ struct SmallArgs {
   int32_t world;
   int32_t n_micro;
   double inv_m2;
-  float decay, b1, omb1, b2, omb2, eps;
+  AdamwK k;
   float step_size, inv_bc2_sqrt;
   float max_norm;
   float inv_m;
@@ -289,11 +289,7 @@ __global__ void __launch_bounds__(SMALL_THREADS) small_update_kernel(const __gri
   }
 
   // ---- 4. clip + AdamW + bf16, the cluster's threads on the chunks in turn
-  float gscale = a.inv_m;
-  if (a.max_norm > 0.0f) {
-    const float cr = a.max_norm / (sqrtf(static_cast<float>(S)) + 1e-6f);
-    gscale = __fmul_rn((cr < 1.0f || isnan(cr)) ? cr : 1.0f, a.inv_m);
-  }
+  const float gscale = clip_gscale(S, a.max_norm, a.inv_m);
   for (int64_t g = gthread; g < n_chunks; g += gstride) {
     int lo = 0, hi = n_tiles;
     while (hi - lo > 1) {
@@ -318,16 +314,8 @@ __global__ void __launch_bounds__(SMALL_THREADS) small_update_kernel(const __gri
     float V[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-      const float gq = __fmul_rn(G[q], gscale);
-      float p = __fmul_rn(P[q], a.decay);
-      const float mm = __fmaf_rn(a.b1, M[q], __fmul_rn(a.omb1, gq));
-      const float vv = __fmaf_rn(a.b2, V[q], __fmul_rn(__fmul_rn(a.omb2, gq), gq));
-      const float denom = __fadd_rn(__fmul_rn(__fsqrt_rn(vv), a.inv_bc2_sqrt), a.eps);
-      p = __fsub_rn(p, __fmul_rn(a.step_size, __fdiv_rn(mm, denom)));
-      const bool pad = el + q >= st.used;
-      P[q] = pad ? 0.0f : p;
-      M[q] = pad ? 0.0f : mm;
-      V[q] = pad ? 0.0f : vv;
+      adamw_elem(G[q], gscale, a.step_size, a.inv_bc2_sqrt, a.k, P[q], M[q], V[q]);
+      if (el + q >= st.used) P[q] = M[q] = V[q] = 0.0f;  // padding
     }
     reinterpret_cast<float4*>(a.master + i)[0] = make_float4(P[0], P[1], P[2], P[3]);
     reinterpret_cast<float4*>(a.master + i + 4)[0] = make_float4(P[4], P[5], P[6], P[7]);
@@ -368,13 +356,7 @@ int launch_update_small(const grs_plan* p, const grs_adamw* hp, const void* cons
   a.n_micro = hp->n_micro;
   const double inv_m = 1.0 / static_cast<double>(hp->n_micro);
   a.inv_m2 = inv_m * inv_m;
-  const double lr = hp->lr, wd = hp->weight_decay;
-  a.decay = static_cast<float>(1.0 - lr * wd);
-  a.b1 = hp->beta1;
-  a.omb1 = static_cast<float>(1.0 - static_cast<double>(hp->beta1));
-  a.b2 = hp->beta2;
-  a.omb2 = static_cast<float>(1.0 - static_cast<double>(hp->beta2));
-  a.eps = hp->eps;
+  a.k = adamw_consts(hp);
   bias_factors(hp, hp->step, &a.step_size, &a.inv_bc2_sqrt);
   a.max_norm = hp->max_norm > 0.0f ? hp->max_norm : 0.0f;
   a.inv_m = static_cast<float>(inv_m);

@@ -131,10 +131,7 @@ struct UpdateArgs {
   int* flags;
   int64_t n_state;   // elements of acc, master, m, v and params
   int32_t n_units;
-  float decay;       // 1 - lr * wd
-  float b1, omb1;    // beta1, 1 - beta1
-  float b2, omb2;    // beta2, 1 - beta2
-  float eps;
+  AdamwK k;
   float step_size;   // lr / (1 - beta1^t)
   float inv_bc2_sqrt;// 1 / sqrt(1 - beta2^t)
   float max_norm;    // <= 0: no clipping
@@ -152,13 +149,8 @@ __global__ void __launch_bounds__(UPD_THREADS) update_kernel(const __grid_consta
   const unsigned tile = GRS_UPD_REVERSE ? gridDim.x - 1u - blockIdx.x : blockIdx.x;
   pdl_wait();  // S and acc come from the kernels before
   pdl_trigger();
-  // Clip coefficient c = min(1, max_norm / (sqrt(S) + 1e-6)), NaN kept,
-  // evaluated by every thread in fp32 from the device-resident S.
-  float gscale = a.inv_m;
-  if (a.max_norm > 0.0f) {
-    const float cr = a.max_norm / (sqrtf(static_cast<float>(*a.norm_sq)) + 1e-6f);
-    gscale = __fmul_rn((cr < 1.0f || isnan(cr)) ? cr : 1.0f, a.inv_m);
-  }
+  // Clip coefficient from the device-resident S, evaluated by every thread.
+  const float gscale = a.max_norm > 0.0f ? clip_gscale(*a.norm_sq, a.max_norm, a.inv_m) : a.inv_m;
   const int u = find_unit(a.prefix, 0, a.n_units, tile);
   const UnitDesc* ud = a.units + u;
   const int64_t e0 = (static_cast<int64_t>(tile) - ud->upd_tile0) * UPD_T;
@@ -182,16 +174,8 @@ __global__ void __launch_bounds__(UPD_THREADS) update_kernel(const __grid_consta
   float V[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
-    const float g = __fmul_rn(G[q], gscale);
-    float p = __fmul_rn(P[q], a.decay);
-    const float mm = __fmaf_rn(a.b1, M[q], __fmul_rn(a.omb1, g));
-    const float vv = __fmaf_rn(a.b2, V[q], __fmul_rn(__fmul_rn(a.omb2, g), g));
-    const float denom = __fadd_rn(__fmul_rn(__fsqrt_rn(vv), a.inv_bc2_sqrt), a.eps);
-    p = __fsub_rn(p, __fmul_rn(a.step_size, __fdiv_rn(mm, denom)));
-    const bool pad = el + q >= used;
-    P[q] = pad ? 0.0f : p;
-    M[q] = pad ? 0.0f : mm;
-    V[q] = pad ? 0.0f : vv;
+    adamw_elem(G[q], gscale, a.step_size, a.inv_bc2_sqrt, a.k, P[q], M[q], V[q]);
+    if (el + q >= used) P[q] = M[q] = V[q] = 0.0f;  // padding
   }
   __stcs(reinterpret_cast<float4*>(a.master + i), make_float4(P[0], P[1], P[2], P[3]));
   __stcs(reinterpret_cast<float4*>(a.master + i + 4), make_float4(P[4], P[5], P[6], P[7]));
@@ -269,6 +253,18 @@ int launch_norm_finish(const grs_plan* p, int32_t n_micro, void* workspace, doub
                                    inv_m * inv_m, d_norm_sq, p->d_flags));
 }
 
+AdamwK adamw_consts(const grs_adamw* hp) {
+  AdamwK k;
+  const double lr = hp->lr, wd = hp->weight_decay;
+  k.decay = static_cast<float>(1.0 - lr * wd);
+  k.b1 = hp->beta1;
+  k.omb1 = static_cast<float>(1.0 - static_cast<double>(hp->beta1));
+  k.b2 = hp->beta2;
+  k.omb2 = static_cast<float>(1.0 - static_cast<double>(hp->beta2));
+  k.eps = hp->eps;
+  return k;
+}
+
 void bias_factors(const grs_adamw* hp, int32_t step, float* step_size, float* inv_bc2_sqrt) {
   const double lr = hp->lr, b1 = hp->beta1, b2 = hp->beta2;
   const double bc1 = 1.0 - std::pow(b1, static_cast<double>(step));
@@ -292,13 +288,7 @@ int launch_update(const grs_plan* p, const grs_adamw* hp, const double* d_norm_s
   a.flags = p->d_flags;
   a.n_state = p->n_state_pad;
   a.n_units = static_cast<int32_t>(p->units.size());
-  const double lr = hp->lr, b1 = hp->beta1, b2 = hp->beta2, wd = hp->weight_decay;
-  a.decay = static_cast<float>(1.0 - lr * wd);
-  a.b1 = hp->beta1;
-  a.omb1 = static_cast<float>(1.0 - b1);
-  a.b2 = hp->beta2;
-  a.omb2 = static_cast<float>(1.0 - b2);
-  a.eps = hp->eps;
+  a.k = adamw_consts(hp);
   bias_factors(hp, hp->step, &a.step_size, &a.inv_bc2_sqrt);
   a.max_norm = hp->max_norm > 0.0f ? hp->max_norm : 0.0f;
   a.inv_m = static_cast<float>(1.0 / static_cast<double>(hp->n_micro));
