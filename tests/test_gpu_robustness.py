@@ -140,6 +140,30 @@ def test_masked_and_layout_calls_write_inside_outputs():
         run.close()
 
 
+def test_hundred_updates_are_deterministic():
+    """Two independent runs of 100 updates (new gradients each step, two
+    microbatches, every owner tag) end in bit-identical accumulator, norm,
+    master, moments and bf16 parameters: nothing in the path depends on
+    scheduling."""
+    c = Case([100003, 1024, 65536 * 2, 4099, 333, 70001, 8000], [RA, PS, LS, AR, PS, RA, LS], 16, 2, 2, 4,
+             1 << 18, 2, 1e-3, 73)
+    finals = []
+    for _ in range(2):
+        run = Run(c)
+        try:
+            for step in range(1, 101):
+                if step > 1 and step % 10 == 1:
+                    run.fill_grads(step_seed=step)
+                run.update()
+            torch.cuda.synchronize()
+            assert run.check_flags() == 0
+            finals.append([t.clone() for t in (run.acc, run.norm, run.master, run.m, run.v, run.params)])
+        finally:
+            run.close()
+    for a, b in zip(*finals):
+        assert torch.equal(a, b)
+
+
 def test_results_do_not_depend_on_the_grid():
     g = grs()
     c = Case([100003, 1024, 65536 * 2, 4099, 333], [RA, PS, LS, AR, PS], 16, 2, 2, 4, 1 << 18, 1, 1e-3, 72)
