@@ -40,7 +40,10 @@ namespace grs {
 namespace {
 
 constexpr int SMALL_THREADS = 512;
-constexpr int SMALL_MAX_CLUSTER = 8;  // the portable cluster size
+#ifndef GRS_SMALL_CLUSTER
+#define GRS_SMALL_CLUSTER 8  // the portable cluster size
+#endif
+constexpr int SMALL_MAX_CLUSTER = GRS_SMALL_CLUSTER;
 static_assert(GRS_SMALL_MAX_TILES <= NORM_L2_BLOCKS,
               "the norm replay assumes one partial per second-level block");
 
