@@ -367,7 +367,7 @@ grs_status grs_clip_adamw_step_masked(const grs_plan* plan, const grs_adamw* hp,
  * "Preserved prototype and evidence", "Proposed scope": FP32 reduction,
  * accumulation, clipping, optimizer update).  For plans whose four
  * launches cost more than their memory traffic: one thread-block cluster
- * of up to 8 CTAs, the norm partials exchanged through distributed shared
+ * of 16 CTAs, the norm partials exchanged through distributed shared
  * memory.
  *   rank_grads : host array [n_micro * world] of device pointers,
  *                microbatch-major (buffer j * world + k is rank k's
