@@ -55,16 +55,19 @@ def mandatory_bytes(buckets, n_micro: int, grad_bytes: int = 2) -> dict:
 
 
 def variant_bytes(buckets, n_micro: int, grad_bytes: int, n_state_pad: int, n_unique: int,
-                  idle=None) -> dict:
+                  idle=None, idle_rows=None) -> dict:
     """mandatory_bytes plus the norm pass, for an update where `idle`
-    elements (None: none) belong to tensors without a gradient.  Those need
-    no norm read and no update; the reduction does not know the mask and
-    runs as in the plain case.  The plain update's norm is fused into the
-    last reduction (0 bytes); the masked one reads acc once (4 bytes per
-    element of a tensor with a gradient)."""
+    elements (None: none) belong to tensors without a gradient, idle_rows[b]
+    of them in each state row of bucket b.  Those need no reduction, no norm
+    read and no update.  The plain update's norm is fused into the last
+    reduction (0 bytes); the masked one reads acc once (4 bytes per element
+    of a tensor with a gradient)."""
     mb = mandatory_bytes(buckets, n_micro, grad_bytes)
     mb["norm"] = 0
     if idle is not None:
+        if idle_rows is not None:
+            live_b = [dict(d, padded=int(d["padded"]) - int(r)) for d, r in zip(buckets, idle_rows)]
+            mb["reduce"] = mandatory_bytes(live_b, n_micro, grad_bytes)["reduce"]
         live = n_state_pad - idle          # elements the update writes (padding included)
         mb["norm"] = 4 * (n_unique - idle)  # elements the norm reads (no padding)
         mb["update"] = 30 * live
@@ -266,18 +269,27 @@ class GpuUpdate:
 
     def algorithmic_bytes(self) -> dict:
         """Per-kernel algorithmic bytes of one update of this variant."""
-        idle = None
+        idle, idle_rows = None, None
         if self.used is not None:
             idle = sum(n for n, u in zip(self.w.numels, self.used_list) if not u)
+            idle_rows = [0] * len(self.buckets)
+            for i, u in enumerate(self.used_list):
+                if not u:
+                    ti = self.grs.grs_tensor_info(self.plan, i)
+                    if ti["bucket"] >= 0:
+                        idle_rows[ti["bucket"]] += ti["per_rank"]
         return variant_bytes(self.buckets, self.n_micro, self.grad_bytes, self.info["n_state_pad"],
-                             self.info["n_unique"], idle)
+                             self.info["n_unique"], idle, idle_rows)
 
     def reduce(self):
         g = self.grs
-        emit = self.used is None
         for j in range(self.n_micro):
-            g.grs_reduce_all(self.plan, self.ptrs[j], self.acc.data_ptr(), int(j > 0),
-                             int(emit and j == self.n_micro - 1), self.ws.data_ptr(), self.stream)
+            if self.used is not None:  # tensors without a gradient are not reduced
+                g.grs_reduce_all_masked(self.plan, self.ptrs[j], self.acc.data_ptr(), int(j > 0),
+                                        self.used.data_ptr(), self.stream)
+            else:
+                g.grs_reduce_all(self.plan, self.ptrs[j], self.acc.data_ptr(), int(j > 0),
+                                 int(j == self.n_micro - 1), self.ws.data_ptr(), self.stream)
 
     def norm_sq(self):
         if self.used is not None:

@@ -235,7 +235,7 @@ static grs_status reduce_common(const grs_plan* p, const void* const* rank_grads
                                 int32_t unit_begin, int32_t unit_end, int64_t state_base,
                                 int64_t rank_base, int64_t state_len, int64_t rank_len, int32_t tag,
                                 const char* who, int32_t max_ctas = 0,
-                                void* wait_event = nullptr) {
+                                void* wait_event = nullptr, const uint8_t* used_mask = nullptr) {
   if (rank_grads == nullptr || acc == nullptr)
     return fail(GRS_ERR_INVALID_ARG, std::string(who) + ": rank_grads/acc is NULL");
   if (emit && workspace == nullptr)
@@ -268,6 +268,10 @@ static grs_status reduce_common(const grs_plan* p, const void* const* rank_grads
   l.rank_len = rank_len;
   l.accumulate = accumulate ? 1 : 0;
   l.max_ctas = max_ctas;
+  if (used_mask != nullptr) {
+    l.used_mask = used_mask;
+    l.tile_tensor = p->d_red_tile_tensor;
+  }
   if (wait_event != nullptr) {
     const cudaError_t we = cudaStreamWaitEvent(static_cast<cudaStream_t>(stream),
                                                static_cast<cudaEvent_t>(wait_event), 0);
@@ -313,6 +317,25 @@ grs_status grs_reduce_all(const grs_plan* p, const void* const* rank_grads, floa
   return reduce_common(p, rank_grads, acc, accumulate, emit, workspace, stream, 0,
                        static_cast<int32_t>(p->units.size()), 0, 0, p->n_state_pad, p->n_rank_pad,
                        only_ar ? GRS_ALREADY_REDUCED : GRS_REPLICA_AVG, "grs_reduce_all");
+}
+
+grs_status grs_reduce_all_masked(const grs_plan* p, const void* const* rank_grads, float* acc,
+                                 int32_t accumulate, const uint8_t* d_tensor_used, void* stream) {
+  grs_status st = check_plan_device(p);
+  if (st != GRS_OK) return st;
+  if (d_tensor_used == nullptr) return fail(GRS_ERR_INVALID_ARG, "grs_reduce_all_masked: d_tensor_used is NULL");
+  // The CTAs of the persistent grid each take ceil(tiles / grid) tiles, one
+  // skip bit per tile in shared memory.
+  const int64_t grid = p->n_red_tiles < int64_t(p->sm_count) * GRS_RED_CTAS_PER_SM ? p->n_red_tiles
+                                                                                  : int64_t(p->sm_count) * GRS_RED_CTAS_PER_SM;
+  if (grid > 0 && (p->n_red_tiles + grid - 1) / grid > int64_t(grs::RED_SKIP_WORDS) * 32)
+    return fail(GRS_ERR_SHAPE, "grs_reduce_all_masked: more than " + std::to_string(grs::RED_SKIP_WORDS * 32) +
+                                   " reduction tiles per SM");
+  bool only_ar = true;
+  for (const auto& bk : p->buckets) only_ar = only_ar && bk.tag == GRS_ALREADY_REDUCED;
+  return reduce_common(p, rank_grads, acc, accumulate, 0, nullptr, stream, 0, static_cast<int32_t>(p->units.size()),
+                       0, 0, p->n_state_pad, p->n_rank_pad, only_ar ? GRS_ALREADY_REDUCED : GRS_REPLICA_AVG,
+                       "grs_reduce_all_masked", 0, nullptr, d_tensor_used);
 }
 
 grs_status grs_accumulate(const grs_plan* p, int32_t b, float* acc, const float* mb, void* stream) {

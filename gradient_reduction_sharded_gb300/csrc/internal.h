@@ -214,7 +214,14 @@ struct ReduceLaunch {
   int64_t state_len, rank_len;  // elements reachable from acc and from each rank pointer
   int32_t accumulate;
   int32_t max_ctas = 0;  // cap on the persistent grid (0: one CTA per SM)
+  // Masked reduction (both set, or both null): tiles lying wholly inside a
+  // tensor whose used_mask entry is 0 are neither read nor written.
+  const uint8_t* used_mask = nullptr;   // device [n_tensors]
+  const int32_t* tile_tensor = nullptr; // device [n_red_tiles]: the plan's red_tile_tensor
 };
+// Skip bits of a masked reduction: one per tile a CTA takes, at most
+// RED_SKIP_WORDS * 32 tiles per CTA.
+constexpr int RED_SKIP_WORDS = 1024;
 int launch_reduce(const grs_plan* p, const ReduceLaunch& a, void* stream);
 int launch_norm(const grs_plan* p, const float* acc, int32_t n_micro, void* workspace,
                 int32_t partials_ready, double* d_norm_sq, void* stream);

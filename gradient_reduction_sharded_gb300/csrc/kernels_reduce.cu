@@ -83,6 +83,10 @@ struct ReduceArgs {
   int32_t accumulate;
   int32_t stages;       // ring depth (<= RED_MAX_STAGES)
   int32_t stage_bytes;  // bytes per stage (multiple of 128)
+  const uint8_t* used_mask;    // masked instantiation only
+  const int32_t* tile_tensor;  // masked instantiation only
+  int32_t skip_words;          // masked instantiation only: bitmap words after the tail
+  int32_t n_tensors;           // masked instantiation only: entries of used_mask
 };
 
 __device__ __forceinline__ float fold_partials(const float* wp) {
@@ -92,7 +96,13 @@ __device__ __forceinline__ float fold_partials(const float* wp) {
   return s;
 }
 
-template <typename E>
+// kMasked: the masked instantiation (grs_reduce_all_masked).  Before the
+// pipeline starts, the CTA marks which of its tiles lie wholly inside a
+// tensor without a gradient this step (one bit per tile, from the plan's
+// per-tile tensor table and the caller's mask); producer and consumers both
+// pass over those tiles, so they are neither read nor written and take no
+// stage.  The plain instantiation has none of this.
+template <typename E, bool kMasked>
 __global__ void __launch_bounds__(RED_THREADS, GRS_RED_CTAS_PER_SM) reduce_kernel(const __grid_constant__ ReduceArgs a) {
   constexpr uint32_t ESZ = sizeof(E);
   extern __shared__ __align__(128) uint8_t smem[];
@@ -103,6 +113,7 @@ __global__ void __launch_bounds__(RED_THREADS, GRS_RED_CTAS_PER_SM) reduce_kerne
   StageMeta* meta = reinterpret_cast<StageMeta*>(empty + RED_MAX_STAGES);
   float* wp = reinterpret_cast<float*>(meta + RED_MAX_STAGES);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(wp + RED_MAX_STAGES * RED_CWARPS);
+  uint32_t* skip = reinterpret_cast<uint32_t*>(smem + size_t(S) * a.stage_bytes + RED_SMEM_TAIL);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -116,9 +127,29 @@ __global__ void __launch_bounds__(RED_THREADS, GRS_RED_CTAS_PER_SM) reduce_kerne
     *abort_flag = 0;
     fence_mbar_init();
   }
-  __syncthreads();
-
   const int64_t stride = gridDim.x;
+  if constexpr (kMasked) {
+    // Bit k of the bitmap: this CTA's k-th tile (tile_begin + blockIdx.x + k * stride)
+    // lies in one tensor whose mask entry is 0.
+    for (int w = warp; w < a.skip_words; w += RED_THREADS / 32) {
+      const int64_t k = int64_t(w) * 32 + lane;
+      const int64_t tile = a.tile_begin + blockIdx.x + k * stride;
+      bool sk = false;
+      if (tile < a.tile_end && GRS_CHECK(tile < a.n_partials, a.flags, SITE_REDUCE)) {
+        const int32_t t = __ldg(a.tile_tensor + tile);
+        sk = t >= 0 && GRS_CHECK(t < a.n_tensors, a.flags, SITE_REDUCE) && __ldg(a.used_mask + t) == 0;
+      }
+      const uint32_t bits = __ballot_sync(0xffffffffu, sk);
+      if (lane == 0) skip[w] = bits;
+    }
+  }
+  __syncthreads();
+  // Tiles of this CTA it passes over (masked instantiation only).
+  auto skipped = [&](int64_t k) -> bool {
+    if constexpr (kMasked) return (skip[k >> 5] >> (k & 31)) & 1u;
+    return false;
+  };
+
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
     const uint64_t pol = GRS_RED_EVICT_FIRST ? l2_policy_evict_first() : l2_policy_evict_normal();
@@ -128,7 +159,9 @@ __global__ void __launch_bounds__(RED_THREADS, GRS_RED_CTAS_PER_SM) reduce_kerne
     int u = a.unit_begin;
     int64_t u_next = __ldg(a.prefix + u + 1);
     UnitDesc ud = a.units[u];
-    for (int64_t tile = a.tile_begin + blockIdx.x; tile < a.tile_end; tile += stride, ++iter) {
+    int64_t k = 0;
+    for (int64_t tile = a.tile_begin + blockIdx.x; tile < a.tile_end; tile += stride, ++k) {
+      if (skipped(k)) continue;
       const int s = static_cast<int>(iter % S);
       const uint32_t ph = static_cast<uint32_t>((iter / S) & 1);
       if (tile >= u_next) {
@@ -188,6 +221,7 @@ __global__ void __launch_bounds__(RED_THREADS, GRS_RED_CTAS_PER_SM) reduce_kerne
                  static_cast<uint32_t>(n) * ESZ, &full[s], pol);
       if (a.accumulate && lane == 0)
         bulk_g2s(st + grad_bytes, a.acc + out_off, static_cast<uint32_t>(n) * 4u, &full[s]);
+      ++iter;
     }
     if (lane == 0) {
       const int64_t first = iter > S ? iter - S : 0;
@@ -215,9 +249,11 @@ __global__ void __launch_bounds__(RED_THREADS, GRS_RED_CTAS_PER_SM) reduce_kerne
     const int ct = threadIdx.x - 32;
     const int cw = ct >> 5;
     int64_t iter = 0;
-    for (int64_t tile = a.tile_begin + blockIdx.x; tile < a.tile_end; tile += stride, ++iter) {
+    int64_t k = 0;
+    for (int64_t tile = a.tile_begin + blockIdx.x; tile < a.tile_end; tile += stride, ++k) {
+      if (skipped(k)) continue;
       const int s = static_cast<int>(iter % S);
-      const uint32_t ph = static_cast<uint32_t>((iter / S) & 1);
+      const uint32_t ph = static_cast<uint32_t>((iter++ / S) & 1);
       if (!mbar_wait_bounded(&full[s], ph, a.flags, abort_flag)) break;
       const StageMeta md = meta[s];
       const int32_t gc = md.gc;
@@ -272,7 +308,7 @@ __global__ void __launch_bounds__(RED_THREADS, GRS_RED_CTAS_PER_SM) reduce_kerne
 
 // Whether the dynamic shared-memory cap is raised, per (gradient type,
 // device); plans on several host threads may launch at once.
-std::atomic<bool> g_attr_set[2][64] = {};
+std::atomic<bool> g_attr_set[2][2][64] = {};
 
 }  // namespace
 
@@ -295,6 +331,10 @@ int launch_reduce(const grs_plan* p, const ReduceLaunch& l, void* stream) {
   a.tile_begin = p->red_prefix[l.unit_begin];
   a.tile_end = p->red_prefix[l.unit_end];
   a.accumulate = l.accumulate;
+  const bool masked = l.used_mask != nullptr;
+  a.used_mask = l.used_mask;
+  a.tile_tensor = l.tile_tensor;
+  a.n_tensors = static_cast<int32_t>(p->numel.size());
   const int64_t tiles = a.tile_end - a.tile_begin;
   if (tiles <= 0) return 0;
   // Stage size: the largest tile of the launched units (rank rows plus the
@@ -311,21 +351,36 @@ int launch_reduce(const grs_plan* p, const ReduceLaunch& l, void* stream) {
   if (stages < 2) return static_cast<int>(cudaErrorInvalidConfiguration);
   a.stages = stages;
   a.stage_bytes = static_cast<int32_t>(need);
-  const size_t smem = size_t(stages) * need + RED_SMEM_TAIL;
-  const bool f32 = p->grad_esize == 4;
-  if (p->device >= 0 && p->device < 64 && !g_attr_set[f32][p->device].load(std::memory_order_acquire)) {
-    cudaError_t e = f32 ? cudaFuncSetAttribute(reduce_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(RED_RING_BYTES + RED_SMEM_TAIL))
-                        : cudaFuncSetAttribute(reduce_kernel<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(RED_RING_BYTES + RED_SMEM_TAIL));
-    if (e != cudaSuccess) return static_cast<int>(e);
-    g_attr_set[f32][p->device].store(true, std::memory_order_release);
-  }
   int64_t cap = int64_t(p->sm_count) * GRS_RED_CTAS_PER_SM;
   if (l.max_ctas > 0 && l.max_ctas < cap) cap = l.max_ctas;
   const int64_t grid = tiles < cap ? tiles : cap;
-  const cudaError_t e = f32 ? launch_k(reduce_kernel<float>, dim3(unsigned(grid)), dim3(RED_THREADS), smem, stream, a)
-                            : launch_k(reduce_kernel<uint16_t>, dim3(unsigned(grid)), dim3(RED_THREADS), smem, stream, a);
+  const int64_t per_cta = (tiles + grid - 1) / grid;
+  a.skip_words = masked ? static_cast<int32_t>((per_cta + 31) / 32) : 0;
+  if (a.skip_words > RED_SKIP_WORDS) return static_cast<int>(cudaErrorInvalidValue);
+  const size_t smem = size_t(stages) * need + RED_SMEM_TAIL + size_t(a.skip_words) * 4;
+  const int f32 = p->grad_esize == 4 ? 1 : 0;
+  const int mk = masked ? 1 : 0;
+  if (p->device >= 0 && p->device < 64 && !g_attr_set[f32][mk][p->device].load(std::memory_order_acquire)) {
+    const int bytes = static_cast<int>(RED_RING_BYTES + RED_SMEM_TAIL + (masked ? RED_SKIP_WORDS * 4 : 0));
+    cudaError_t e;
+    if (f32)
+      e = masked ? cudaFuncSetAttribute(reduce_kernel<float, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)
+                 : cudaFuncSetAttribute(reduce_kernel<float, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    else
+      e = masked ? cudaFuncSetAttribute(reduce_kernel<uint16_t, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)
+                 : cudaFuncSetAttribute(reduce_kernel<uint16_t, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return static_cast<int>(e);
+    g_attr_set[f32][mk][p->device].store(true, std::memory_order_release);
+  }
+  const dim3 gd(static_cast<unsigned>(grid));
+  const dim3 bd(static_cast<unsigned>(RED_THREADS));
+  cudaError_t e;
+  if (f32)
+    e = masked ? launch_k(reduce_kernel<float, true>, gd, bd, smem, stream, a)
+               : launch_k(reduce_kernel<float, false>, gd, bd, smem, stream, a);
+  else
+    e = masked ? launch_k(reduce_kernel<uint16_t, true>, gd, bd, smem, stream, a)
+               : launch_k(reduce_kernel<uint16_t, false>, gd, bd, smem, stream, a);
   return static_cast<int>(e);
 }
 

@@ -279,6 +279,20 @@ grs_status grs_reduce_all(const grs_plan* plan, const void* const* rank_grads, f
                           int32_t accumulate, int32_t emit_norm_partials, void* workspace,
                           void* stream);
 
+/* grs_reduce_all for a step where some tensors have no gradient (PyTorch's
+ * grad None; [ISSUE] "Proposed scope": unused parameters), for use with
+ * grs_grad_norm_sq_masked and grs_clip_adamw_step_masked.  d_tensor_used:
+ * device uint8 [n_tensors], as for those calls.  Reduction tiles that lie
+ * wholly inside one tensor with used = 0 are neither read nor written, so
+ * those tensors' gradients need not exist; every other tile is reduced as
+ * grs_reduce_all reduces it (tiles spanning several tensors in full).  The
+ * accumulator of a tensor with used = 0 is therefore unspecified: the
+ * masked norm and update never use it.  No norm partials are emitted.
+ * Errors as grs_reduce_all, INVALID_ARG for a NULL mask, SHAPE beyond
+ * 32768 reduction tiles per SM. */
+grs_status grs_reduce_all_masked(const grs_plan* plan, const void* const* rank_grads, float* acc,
+                                 int32_t accumulate, const uint8_t* d_tensor_used, void* stream);
+
 /* acc_b += mb_b over bucket b's rows (fp32), padding kept at zero: adds a
  * separately reduced microbatch gradient into the accumulator ([ISSUE]
  * "Proposed scope": gradient accumulation).  Both device [copies*padded]. */

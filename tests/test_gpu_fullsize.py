@@ -250,7 +250,9 @@ def _full_size_w(w, variant, window):
         got_bits = u.params[sidx].cpu().numpy().view(np.uint16)
         cat = np.concatenate
         idle = cat(idle)
-        assert_close(got_acc, cat(want_acc), f"{what} acc")
+        # the masked reduction leaves the accumulator of tensors without a
+        # gradient unspecified: only the others are compared
+        assert_close(got_acc[~idle], cat(want_acc)[~idle], f"{what} acc")
         assert_close_bracketed(got_p, cat(want_p), cat(lo_p), cat(hi_p), f"{what} master")
         assert_close_bracketed(got_m, cat(want_m), cat(lo_m), cat(hi_m), f"{what} m")
         assert_close_bracketed(got_v, cat(want_v), cat(lo_v), cat(hi_v), f"{what} v")

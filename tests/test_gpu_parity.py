@@ -25,12 +25,18 @@ def _cuda():
     torch.cuda.init()
 
 
-def full_check(run: Run, res, what=""):
+def full_check(run: Run, res, what="", acc_where=None):
+    """Everything the update wrote against the oracle; `acc_where` (bool per
+    state element) limits the accumulator check (a masked reduction leaves
+    the accumulator of tensors without a gradient unspecified)."""
     torch.cuda.synchronize()
     n = run.nsp
     pad = padding_mask(run.op)
     acc = run.acc[:n].cpu().numpy()
-    assert_close(acc, res.acc, f"{what} acc")
+    if acc_where is None:
+        assert_close(acc, res.acc, f"{what} acc")
+    else:
+        assert_close(acc[acc_where], res.acc[acc_where], f"{what} acc")
     assert np.all(acc[pad] == 0), f"{what} acc padding not zero"
     norm = float(run.norm.cpu()[0])
     assert_close([norm], [res.norm_sq], f"{what} norm_sq")
@@ -472,13 +478,17 @@ def test_frozen_tensors_excluded():
         run.close()
 
 
-@pytest.mark.parametrize("fp32,zeros", [(False, False), (True, False), (False, True)])
-def test_unused_tensors_masked_update(fp32, zeros):
+@pytest.mark.parametrize("fp32,zeros,masked_reduce", [(False, False, False), (True, False, False),
+                                                      (False, True, False), (False, False, True),
+                                                      (True, True, True)])
+def test_unused_tensors_masked_update(fp32, zeros, masked_reduce):
     """Three steps with per-step masks of tensors that got no gradient
     (grad None): masked norm + per-tensor-step AdamW against the oracle's
     masked update, the oracle carrying its own state and step counts.  With
     `zeros`, zero-size tensors sit between the others (empty segments the
-    kernels' segment walk must step over)."""
+    kernels' segment walk must step over); with `masked_reduce` the
+    reduction itself skips the tiles of tensors without a gradient, whose
+    accumulator is then not compared (it is unspecified)."""
     numels = [5000, 33, 4096 * 2, 17, 2048, 999, 64]
     owners = [RA, RA, LS, AR, PS, RA, LS]
     flags = [0, 0, 0, 0, 0, 1, 0]
@@ -503,13 +513,25 @@ def test_unused_tensors_masked_update(fp32, zeros):
             if k:
                 run.fill_grads(step_seed=k + 1)
             used_dev = torch.tensor(used, dtype=torch.uint8, device="cuda")
-            run.reduce(emit=False)
+            if masked_reduce:
+                for j in range(c.n_micro):
+                    grs().grs_reduce_all_masked(run.plan, run.ptrs(j), run.acc.data_ptr(), int(j > 0),
+                                                used_dev.data_ptr(), run.stream())
+            else:
+                run.reduce(emit=False)
             run.masked_update(used_dev, steps_dev)
             torch.cuda.synchronize()
             assert run.check_flags() == 0
             res, steps = oracle.full_update_masked(run.op, run.bucket_inputs, c.n_micro, c.hp, c.max_norm,
                                                    used, steps, master, m, v, bits)
-            full_check(run, res, f"masked step {k + 1}")
+            where = None
+            if masked_reduce:
+                where = np.ones(run.nsp, bool)
+                for i in range(n):
+                    if not used[i]:
+                        for lo, hi in run.op.tensor_rows(i):
+                            where[lo:hi] = False
+            full_check(run, res, f"masked step {k + 1}", acc_where=where)
             got_steps = steps_dev.cpu().tolist()
             for i in range(n):
                 if not c.tensor_flags[i]:
@@ -543,6 +565,70 @@ def test_masked_update_with_many_small_tensors():
         assert steps_dev.cpu().tolist() == steps
     finally:
         run.close()
+
+
+def test_masked_reduction_skips_tiles_of_unused_tensors():
+    """The masked reduction neither reads nor writes the tiles that lie wholly
+    in tensors without a gradient: with those tensors' gradients poisoned
+    (NaN in every rank buffer) and the accumulator pre-filled, their whole
+    tiles keep the fill, every used tensor's accumulator equals the plain
+    reduction of clean inputs bit for bit, and the masked norm stays finite."""
+    c = Case([300000, 1024, 65536 * 4, 4099, 200000, 70002], [RA, PS, LS, AR, RA, LS], 8, 2, 2, 2, 1 << 18, 1,
+             1e-3, 61)
+    a, b = Run(c), Run(c)
+    try:
+        g = grs()
+        n = len(c.numels)
+        used = [1, 1, 0, 1, 0, 1]
+        used_dev = torch.tensor(used, dtype=torch.uint8, device="cuda")
+        a.reduce(emit=False)
+        op = b.op
+        for i in range(n):  # poison the unused tensors' gradients on every rank
+            if used[i]:
+                continue
+            bk = int(op.t_bucket[i])
+            lo = int(op.b_rank_off[bk]) + int(op.t_offset[i])
+            for k in range(c.world):
+                b.grads[0][k].view(torch.int16)[lo:lo + op.per_rank(i)] = 0x7FC0
+        b.acc.fill_(123.0)
+        g.grs_reduce_all_masked(b.plan, b.ptrs(0), b.acc.data_ptr(), 0, used_dev.data_ptr(), b.stream())
+        torch.cuda.synchronize()
+        assert b.check_flags() == 0
+        got, want = b.acc[:b.nsp].cpu().numpy(), a.acc[:a.nsp].cpu().numpy()
+        untouched = 0
+        for i in range(n):
+            for lo, hi in op.tensor_rows(i):
+                if used[i]:
+                    assert np.array_equal(got[lo:hi], want[lo:hi]), i
+                else:
+                    untouched += int((got[lo:hi] == 123.0).sum())
+        assert untouched > 0.9 * sum(c.numels[i] for i in range(n) if not used[i])
+        b.masked_update(used_dev, torch.zeros(n, dtype=torch.int32, device="cuda"))
+        torch.cuda.synchronize()
+        assert b.check_flags() == 0
+        assert np.isfinite(float(b.norm.cpu()[0]))
+    finally:
+        a.close()
+        b.close()
+
+
+def test_masked_reduction_with_every_tensor_used_equals_plain():
+    """grs_reduce_all_masked with every tensor marked used reduces every tile:
+    the accumulator equals grs_reduce_all's bit for bit (two microbatches)."""
+    c = SMALL["multi-tile-world16-M2"]
+    a, b = Run(c), Run(c)
+    try:
+        g = grs()
+        ones = torch.ones(len(c.numels), dtype=torch.uint8, device="cuda")
+        a.reduce(emit=False)
+        for j in range(c.n_micro):
+            g.grs_reduce_all_masked(b.plan, b.ptrs(j), b.acc.data_ptr(), int(j > 0), ones.data_ptr(), b.stream())
+        torch.cuda.synchronize()
+        assert a.check_flags() == 0 and b.check_flags() == 0
+        assert torch.equal(a.acc[:a.nsp], b.acc[:b.nsp])
+    finally:
+        a.close()
+        b.close()
 
 
 @pytest.mark.parametrize("hint", ["matching", "none"])
