@@ -567,6 +567,92 @@ def test_masked_update_with_many_small_tensors():
         run.close()
 
 
+def random_case(rng, trial):
+    """A random small plan: degrees, 1..24 tensors of all tags with 0..3000
+    elements (LOCAL_SHARD a multiple of tp), bucket sizes from tiny to large,
+    some tensors frozen, bf16 or fp32 gradients, 1..3 microbatches, clipping
+    on or off, random AdamW hyper-parameters."""
+    tp = int(rng.choice([1, 2, 3, 4]))
+    dr = int(rng.choice([1, 2, 3]))
+    ds = int(rng.choice([1, 2, 3, 4, 5]))
+    n = int(rng.integers(1, 25))
+    owners = [int(x) for x in rng.integers(0, 4, n)]
+    numels = [int(rng.integers(0, 3001 // (tp if o == LS else 1))) * (tp if o == LS else 1) for o in owners]
+    if sum(numels) == 0:
+        numels[0] = 8 * tp
+    flags = [int(x) for x in (rng.random(n) < 0.15)]
+    if all(flags[i] or numels[i] == 0 for i in range(n)):
+        flags = [0] * n
+    bb = int(rng.choice([2, 64, 1000, 1 << 12, 1 << 20]))
+    hp = (float(rng.choice([1e-3, 3e-4, 1e-2])), float(rng.choice([0.9, 0.8])), float(rng.choice([0.999, 0.95])),
+          float(rng.choice([1e-8, 1e-6])), float(rng.choice([0.0, 0.01, 0.1])))
+    return Case(numels, owners, tp * dr * ds, tp, dr, -1 if rng.random() < 0.2 else ds, bb,
+                int(rng.integers(1, 4)), float(rng.choice([1e-3, 1e-2, 1e-1])), 500 + trial, hp=hp,
+                max_norm=float(rng.choice([1.0, 0.05, 0.0])), fp32_grads=bool(rng.random() < 0.3),
+                tensor_flags=flags)
+
+
+@pytest.mark.parametrize("trial", range(16))
+def test_random_small_plans_match_oracle(trial):
+    """Random plans (random_case): one plain update against the oracle; the
+    masked reduction, norm and update with a random mask against the oracle's
+    masked update; and the single-launch update against the plain one, bit
+    for bit, where its limits allow."""
+    rng = np.random.default_rng(7000 + trial)
+    c = random_case(rng, trial)
+    g = grs()
+    run = Run(c)
+    try:
+        master0, m0, v0 = run.state_host()
+        bits0 = run.params[:run.nsp].cpu().numpy().view(np.uint16).copy()
+        run.update()
+        res = oracle_update(run, master0, m0, v0, step=1)
+        full_check(run, res, f"random {trial} plain")
+    finally:
+        run.close()
+    n = len(c.numels)
+    used = [int(x) for x in (rng.random(n) < 0.7)]
+    mrun = Run(c)
+    try:
+        used_dev = torch.tensor(used, dtype=torch.uint8, device="cuda")
+        for j in range(c.n_micro):
+            g.grs_reduce_all_masked(mrun.plan, mrun.ptrs(j), mrun.acc.data_ptr(), int(j > 0), used_dev.data_ptr(),
+                                    mrun.stream())
+        mrun.masked_update(used_dev, torch.zeros(n, dtype=torch.int32, device="cuda"))
+        torch.cuda.synchronize()
+        assert mrun.check_flags() == 0
+        res, _ = oracle.full_update_masked(mrun.op, mrun.bucket_inputs, c.n_micro, c.hp, c.max_norm, used, [0] * n,
+                                           master0, m0, v0, bits0)
+        where = np.ones(mrun.nsp, bool)
+        for i in range(n):
+            if not used[i]:
+                for lo, hi in mrun.op.tensor_rows(i):
+                    where[lo:hi] = False
+        full_check(mrun, res, f"random {trial} masked", acc_where=where)
+    finally:
+        mrun.close()
+    a, b = Run(c), Run(c)
+    try:
+        rows = sum(a.op.copies(bk) for bk in range(a.op.n_buckets))
+        if (a.info["n_reduce_tiles"] > g.GRS_SMALL_MAX_TILES or rows > g.GRS_SMALL_MAX_TILES or
+                c.n_micro * c.world > g.GRS_SMALL_MAX_BUFFERS):
+            return
+        a.update()
+        hp = g.make_adamw(*c.hp, c.max_norm, 1, c.n_micro)
+        norm = torch.zeros(1, dtype=torch.float64, device="cuda")
+        g.grs_update_small(b.plan, hp, [p for j in range(c.n_micro) for p in b.ptrs(j)], b.acc.data_ptr(),
+                           b.master.data_ptr(), b.m.data_ptr(), b.v.data_ptr(), b.params.data_ptr(),
+                           norm.data_ptr(), b.stream())
+        torch.cuda.synchronize()
+        assert a.check_flags() == 0 and b.check_flags() == 0
+        assert torch.equal(a.norm, norm)
+        for nm in ("acc", "master", "m", "v", "params"):
+            assert torch.equal(getattr(a, nm)[:a.nsp], getattr(b, nm)[:b.nsp]), nm
+    finally:
+        a.close()
+        b.close()
+
+
 def test_masked_reduction_skips_tiles_of_unused_tensors():
     """The masked reduction neither reads nor writes the tiles that lie wholly
     in tensors without a gradient: with those tensors' gradients poisoned
