@@ -248,12 +248,16 @@ def bf16_value(bits):
     return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
-def assert_bf16_cast(got_bits, got_master, want_bits, want_master, what, rtol=RTOL, atol=ATOL):
+def assert_bf16_cast(got_bits, got_master, want_bits, want_master, what, rtol=RTOL, atol=ATOL,
+                     lo_master=None, hi_master=None):
     """bf16 parameters.  (1) The kernel's bf16 is the round-to-nearest-even of
     its own fp32 master, bit for bit (torch's CPU cast decides, in fp32).
     (2) Against the oracle: within 1 bf16 ulp, widened by the fp32 master
     tolerance where the masters themselves may differ by that much (values
-    near zero, where a bf16 ulp is far below abs 1e-7)."""
+    near zero, where a bf16 ulp is far below abs 1e-7), and by the master's
+    bracket when one is given (the oracle's update at acc -/+ the fp32
+    accumulation bound: at ill-conditioned AdamW points the masters may
+    differ by more than a bf16 ulp, and the casts with them)."""
     g = np.asarray(got_bits).view(np.uint16)
     w = np.asarray(want_bits, np.uint16)
     rne = torch.from_numpy(np.asarray(got_master, np.float32)).to(torch.bfloat16)
@@ -267,6 +271,12 @@ def assert_bf16_cast(got_bits, got_master, want_bits, want_master, what, rtol=RT
     ulp = np.abs(bf16_value(w ^ 1) - wv)  # spacing at the oracle's value
     lim = ulp + atol + rtol * np.abs(np.asarray(want_master, np.float64))
     d = np.abs(gv - wv)
+    if lo_master is not None and hi_master is not None:
+        # distance from the cast to the cast interval of the bracket
+        wm = np.asarray(want_master, np.float64)
+        a = np.minimum(np.minimum(np.asarray(lo_master, np.float64), np.asarray(hi_master, np.float64)), wm)
+        b = np.maximum(np.maximum(np.asarray(lo_master, np.float64), np.asarray(hi_master, np.float64)), wm)
+        d = np.minimum(d, np.maximum(0.0, np.maximum(a - gv, gv - b)))
     d[gn] = 0
     if (d > lim).any():
         i = np.flatnonzero(d > lim)[:5]

@@ -258,7 +258,7 @@ def _full_size_w(w, variant, window):
         assert_close_bracketed(got_v, cat(want_v), cat(lo_v), cat(hi_v), f"{what} v")
         live = ~idle
         assert_bf16_cast(got_bits[live], got_p[live], cat(want_bits)[live], cat(want_p)[live],
-                         f"{what} params")
+                         f"{what} params", lo_master=cat(lo_p)[live], hi_master=cat(hi_p)[live])
         if used_t is not None:
             assert idle.any(), "the sample holds no element of a tensor without a gradient"
             # bit for bit: the masked update neither reads nor writes them
