@@ -228,6 +228,9 @@ class GpuUpdate:
         self.grads = [[gen(nrp, w.grad_std, workloads.grad_seed(w.cid, j, k), device=device)
                        for k in range(w.world)] for j in range(self.n_micro)]
         self.ptrs = [[t.data_ptr() for t in mb] for mb in self.grads]
+        # the same pointers as C arrays, built once (no per-call conversion)
+        self.ptr_arrays = [grs.pointer_array(p) for p in self.ptrs]
+        self.all_ptrs = grs.pointer_array([p for mb in self.ptrs for p in mb])
         self.acc = torch.empty(nsp, dtype=torch.float32, device=device)
         self.master = workloads.normal_f32(nsp, w.master_std, workloads.master_seed(w.cid),
                                            device=device)
@@ -285,10 +288,10 @@ class GpuUpdate:
         g = self.grs
         for j in range(self.n_micro):
             if self.used is not None:  # tensors without a gradient are not reduced
-                g.grs_reduce_all_masked(self.plan, self.ptrs[j], self.acc.data_ptr(), int(j > 0),
+                g.grs_reduce_all_masked(self.plan, self.ptr_arrays[j], self.acc.data_ptr(), int(j > 0),
                                         self.used.data_ptr(), self.stream)
             else:
-                g.grs_reduce_all(self.plan, self.ptrs[j], self.acc.data_ptr(), int(j > 0),
+                g.grs_reduce_all(self.plan, self.ptr_arrays[j], self.acc.data_ptr(), int(j > 0),
                                  int(j == self.n_micro - 1), self.ws.data_ptr(), self.stream)
 
     def norm_sq(self):
@@ -341,7 +344,7 @@ class GpuUpdate:
         self.step_no += 1
         hp = self.grs.make_adamw(a.lr, a.beta1, a.beta2, a.eps, a.weight_decay, a.max_norm,
                                  self.step_no, self.n_micro)
-        self.grs.grs_update_small(self.plan, hp, [p for j in range(self.n_micro) for p in self.ptrs[j]],
+        self.grs.grs_update_small(self.plan, hp, self.all_ptrs,
                                   self.acc.data_ptr(), self.master.data_ptr(), self.m.data_ptr(),
                                   self.v.data_ptr(), self.params.data_ptr(), self.norm.data_ptr(),
                                   self.stream)

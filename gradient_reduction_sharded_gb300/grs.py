@@ -152,7 +152,15 @@ def _check(status: int, func: str):
         raise GrsError(status, func, grs_last_error())
 
 
+def pointer_array(seq: Sequence[Optional[int]]):
+    """A reusable C array of device pointers: every call below that takes a
+    pointer list also takes one of these as is (no conversion per call)."""
+    return _ptrs(seq)
+
+
 def _ptrs(seq: Sequence[Optional[int]]):
+    if isinstance(seq, ctypes.Array):
+        return seq
     arr = (_vp * max(1, len(seq)))()
     for i, p in enumerate(seq):
         arr[i] = None if p is None else int(p)
