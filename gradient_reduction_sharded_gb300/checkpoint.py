@@ -99,12 +99,8 @@ def shard_slices(plan: int) -> Dict[str, list]:
     return out
 
 
-def _sha256(path: str) -> str:
-    h = hashlib.sha256()
-    with open(path, "rb") as f:
-        for blk in iter(lambda: f.read(1 << 24), b""):
-            h.update(blk)
-    return h.hexdigest()
+def _io_threads() -> int:
+    return max(1, min(8, os.cpu_count() or 1))
 
 
 def write_shards(directory: str, plan: int, spec: PlanSpec, arrays: Dict[str, np.ndarray],
@@ -124,19 +120,26 @@ def write_shards(directory: str, plan: int, spec: PlanSpec, arrays: Dict[str, np
     if os.path.exists(os.path.join(directory, SUCCESS)):
         raise CheckpointError(f"{directory} already holds a committed checkpoint")
     tmp = tempfile.mkdtemp(prefix=".grs-ckpt-", dir=parent)
+
+    def write_one(item):
+        # one shard file, its digest taken from the bytes as they are written
+        fname, sl = item
+        h = hashlib.sha256()
+        with open(os.path.join(tmp, fname), "wb") as f:
+            for nm in names:
+                a = arrays[nm].reshape(-1)
+                for off, n in sl:
+                    buf = memoryview(np.ascontiguousarray(a[off:off + n])).cast("B")
+                    h.update(buf)
+                    f.write(buf)
+            f.flush()
+            os.fsync(f.fileno())
+        return fname, {"slices": sl, "sha256": h.hexdigest(), "bytes": int(sum(n for _, n in sl) * 4 * len(names))}
+
     try:
-        files = {}
-        for fname, sl in shard_slices(plan).items():
-            path = os.path.join(tmp, fname)
-            with open(path, "wb") as f:
-                for nm in names:
-                    a = arrays[nm].reshape(-1)
-                    for off, n in sl:
-                        f.write(np.ascontiguousarray(a[off:off + n]).tobytes())
-                f.flush()
-                os.fsync(f.fileno())
-            files[fname] = {"slices": sl, "sha256": _sha256(path),
-                            "bytes": int(sum(n for _, n in sl) * 4 * len(names))}
+        # shard files in parallel (hashing and file writes release the GIL)
+        with ThreadPoolExecutor(max_workers=_io_threads()) as ex:
+            files = dict(ex.map(write_one, shard_slices(plan).items()))
         manifest = {"format": FORMAT, "plan": asdict(spec), "arrays": names, "files": files,
                     "n_state_pad": info["n_state_pad"], "steps": steps, "metadata": metadata or {}}
         with open(os.path.join(tmp, MANIFEST), "w") as f:
@@ -167,18 +170,30 @@ def read_shards(directory: str):
         raise CheckpointError(f"{directory}: unknown format {man.get('format')!r}")
     names = man["arrays"]
     arrays = {nm: np.zeros(man["n_state_pad"], np.float32) for nm in names}
-    for fname, ent in man["files"].items():
+
+    def read_one(item):
+        # one shard file: read once, digest checked on those bytes, scattered
+        # into the writer's layout (files cover disjoint slices)
+        fname, ent = item
         path = os.path.join(directory, fname)
-        if _sha256(path) != ent["sha256"]:
+        data = np.fromfile(path, dtype=np.uint8)
+        if hashlib.sha256(memoryview(data)).hexdigest() != ent["sha256"]:
             raise CheckpointError(f"{path}: digest mismatch")
-        data = np.fromfile(path, dtype=np.float32)
+        if data.size % 4:
+            raise CheckpointError(f"{path}: size does not match the manifest")
+        vals = data.view(np.float32)
         pos = 0
         for nm in names:
             for off, n in ent["slices"]:
-                arrays[nm][off:off + n] = data[pos:pos + n]
+                if pos + n > vals.size:
+                    raise CheckpointError(f"{path}: size does not match the manifest")
+                arrays[nm][off:off + n] = vals[pos:pos + n]
                 pos += n
-        if pos != data.size:
+        if pos != vals.size:
             raise CheckpointError(f"{path}: size does not match the manifest")
+
+    with ThreadPoolExecutor(max_workers=_io_threads()) as ex:
+        list(ex.map(read_one, man["files"].items()))
     return man, arrays
 
 
