@@ -56,12 +56,12 @@ def mandatory_bytes(buckets, n_micro: int, grad_bytes: int = 2) -> dict:
 
 def variant_bytes(buckets, n_micro: int, grad_bytes: int, n_state_pad: int, n_unique: int,
                   idle=None, idle_rows=None) -> dict:
-    """mandatory_bytes plus the norm pass, for an update where `idle`
-    elements (None: none) belong to tensors without a gradient, idle_rows[b]
-    of them in each state row of bucket b.  Those need no reduction, no norm
-    read and no update.  The plain update's norm is fused into the last
-    reduction (0 bytes); the masked one reads acc once (4 bytes per element
-    of a tensor with a gradient)."""
+    """mandatory_bytes for an update where `idle` elements (None: none)
+    belong to tensors without a gradient, idle_rows[b] of them in each state
+    row of bucket b.  Those need no reduction and no update.  The norm, plain
+    or masked, is fused into the last reduction (0 bytes); a separate masked
+    norm pass would read acc once (4 bytes per element of a tensor with a
+    gradient, `norm_pass`)."""
     mb = mandatory_bytes(buckets, n_micro, grad_bytes)
     mb["norm"] = 0
     if idle is not None:
@@ -69,7 +69,7 @@ def variant_bytes(buckets, n_micro: int, grad_bytes: int, n_state_pad: int, n_un
             live_b = [dict(d, padded=int(d["padded"]) - int(r)) for d, r in zip(buckets, idle_rows)]
             mb["reduce"] = mandatory_bytes(live_b, n_micro, grad_bytes)["reduce"]
         live = n_state_pad - idle          # elements the update writes (padding included)
-        mb["norm"] = 4 * (n_unique - idle)  # elements the norm reads (no padding)
+        mb["norm_pass"] = 4 * (n_unique - idle)  # elements a separate norm pass reads (no padding)
         mb["update"] = 30 * live
         mb["total"] = mb["reduce"] + mb["norm"] + mb["update"]
     return mb
@@ -289,19 +289,17 @@ class GpuUpdate:
         for j in range(self.n_micro):
             if self.used is not None:  # tensors without a gradient are not reduced
                 g.grs_reduce_all_masked(self.plan, self.ptr_arrays[j], self.acc.data_ptr(), int(j > 0),
-                                        self.used.data_ptr(), self.stream)
+                                        int(j == self.n_micro - 1), self.used.data_ptr(), self.ws.data_ptr(),
+                                        self.stream)
             else:
                 g.grs_reduce_all(self.plan, self.ptr_arrays[j], self.acc.data_ptr(), int(j > 0),
                                  int(j == self.n_micro - 1), self.ws.data_ptr(), self.stream)
 
     def norm_sq(self):
-        if self.used is not None:
-            self.grs.grs_grad_norm_sq_masked(self.plan, self.acc.data_ptr(), self.n_micro,
-                                             self.used.data_ptr(), self.ws.data_ptr(),
-                                             self.norm.data_ptr(), self.stream)
-        else:
-            self.grs.grs_grad_norm_sq(self.plan, self.acc.data_ptr(), self.n_micro,
-                                      self.ws.data_ptr(), 1, self.norm.data_ptr(), self.stream)
+        # The last reduction emitted the norm partials (masked ones when a
+        # mask is given): only the fixed-order finish runs here.
+        self.grs.grs_grad_norm_sq(self.plan, self.acc.data_ptr(), self.n_micro,
+                                  self.ws.data_ptr(), 1, self.norm.data_ptr(), self.stream)
 
     def adamw(self):
         a = self.w.adamw
@@ -489,7 +487,7 @@ def run_gpu(args, rank, world_size, local_rank):
         "update": {"ms": statistics.mean(upd_ms), "ms_median": statistics.median(upd_ms),
                    "bytes": mb["update"], "launches_per_step": 2 if masked else 1},
         "norm": {"ms": statistics.mean(nrm_ms), "ms_median": statistics.median(nrm_ms),
-                 "bytes": mb["norm"] if masked else None, "launches_per_step": 2 if masked else 1},
+                 "bytes": None, "launches_per_step": 1},
     }
     # reduce: average per launch over the microbatches of a step
     kern["reduce"]["ms_per_launch"] = kern["reduce"]["ms"] / M
@@ -506,7 +504,7 @@ def run_gpu(args, rank, world_size, local_rank):
     traffic = load_traffic(dom, w, u.variant)
     if masked:
         kern["update"]["note"] = "per-tensor factors kernel + masked update"
-        kern["norm"]["note"] = "masked norm pass + norm finish"
+        kern["reduce"]["note"] = "masked reduction (masked norm partials fused into the last microbatch)"
     result = {
         "metric": METRIC, "value": job_value(ms_step, world_size), "unit": UNIT, "n_gpus": world_size,
         "steps": K, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": False,

@@ -320,7 +320,8 @@ grs_status grs_reduce_all(const grs_plan* p, const void* const* rank_grads, floa
 }
 
 grs_status grs_reduce_all_masked(const grs_plan* p, const void* const* rank_grads, float* acc,
-                                 int32_t accumulate, const uint8_t* d_tensor_used, void* stream) {
+                                 int32_t accumulate, int32_t emit, const uint8_t* d_tensor_used,
+                                 void* workspace, void* stream) {
   grs_status st = check_plan_device(p);
   if (st != GRS_OK) return st;
   if (d_tensor_used == nullptr) return fail(GRS_ERR_INVALID_ARG, "grs_reduce_all_masked: d_tensor_used is NULL");
@@ -333,7 +334,7 @@ grs_status grs_reduce_all_masked(const grs_plan* p, const void* const* rank_grad
                                    " reduction tiles per SM");
   bool only_ar = true;
   for (const auto& bk : p->buckets) only_ar = only_ar && bk.tag == GRS_ALREADY_REDUCED;
-  return reduce_common(p, rank_grads, acc, accumulate, 0, nullptr, stream, 0, static_cast<int32_t>(p->units.size()),
+  return reduce_common(p, rank_grads, acc, accumulate, emit, workspace, stream, 0, static_cast<int32_t>(p->units.size()),
                        0, 0, p->n_state_pad, p->n_rank_pad, only_ar ? GRS_ALREADY_REDUCED : GRS_REPLICA_AVG,
                        "grs_reduce_all_masked", 0, nullptr, d_tensor_used);
 }

@@ -33,89 +33,6 @@ constexpr int MUPD_THREADS = 256;
 #endif
 static_assert(UPD_T == MUPD_THREADS * 8, "one 8-element group per thread per tile");
 
-// Last segment in [lo, hi) whose start is <= e (the first segment starts at 0).
-__device__ __forceinline__ int find_seg(const int64_t* __restrict__ start, int lo, int hi, int64_t e) {
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (__ldg(start + mid) <= e)
-      lo = mid;
-    else
-      hi = mid;
-  }
-  return lo;
-}
-
-struct Segs {
-  const int64_t* start;
-  const int32_t* tensor;
-  const int32_t* bucket_seg0;
-  int32_t n_tensors;  // length of the per-tensor arrays (used mask, steps, factors)
-};
-
-// The tensor segment under a forward-moving bucket element: its index, end,
-// tensor and whether that tensor has a gradient this step.  Loaded once per
-// segment, not once per element.
-struct SegCursor {
-  int s;
-  int hi;         // one past the bucket's last segment
-  int64_t end;    // first element after segment s (the bucket's used count for the last)
-  int32_t t;      // tensor of segment s (-1 when out of range in a checked build)
-  bool on;        // tensor t has a gradient this step
-};
-
-__device__ __forceinline__ void seg_load(SegCursor& c, const Segs& sg, const uint8_t* __restrict__ used_mask,
-                                         int64_t used, int* flags, int site) {
-  c.end = c.s + 1 < c.hi ? __ldg(sg.start + c.s + 1) : used;
-  const int32_t t = __ldg(sg.tensor + c.s);
-  const bool ok = GRS_CHECK(t >= 0 && t < sg.n_tensors, flags, site);
-  c.t = ok ? t : -1;
-  c.on = ok && __ldg(used_mask + t) != 0;
-}
-
-// Cursor at element e (< used) of a bucket row whose segments are [lo, hi).
-__device__ __forceinline__ SegCursor seg_at(const Segs& sg, const uint8_t* __restrict__ used_mask, int lo, int hi,
-                                            int64_t e, int64_t used, int* flags, int site) {
-  SegCursor c;
-  c.s = find_seg(sg.start, lo, hi, e);
-  c.hi = hi;
-  seg_load(c, sg, used_mask, used, flags, site);
-  return c;
-}
-
-// Move the cursor forward to element e (< used); zero-length segments
-// (zero-size tensors) are stepped over.
-__device__ __forceinline__ void seg_advance(SegCursor& c, const Segs& sg, const uint8_t* __restrict__ used_mask,
-                                            int64_t e, int64_t used, int* flags, int site) {
-  while (e >= c.end && c.s + 1 < c.hi) {
-    ++c.s;
-    seg_load(c, sg, used_mask, used, flags, site);
-  }
-}
-
-// Element 8c + q of a tile counts iff it lies in [0, used) of its bucket row
-// and in a tensor with a gradient this step.  The cursor keeps the segment
-// of the last element asked for ([begin, end)) and seeks again (a binary
-// search) only when an element falls outside it.
-struct MaskKeep {
-  const Segs& sg;
-  const uint8_t* __restrict__ used_mask;
-  int lo, hi;
-  int64_t e0, used;
-  int* flags;
-  SegCursor cur;
-  int64_t begin;
-
-  __device__ __forceinline__ bool operator()(int c, int q) {
-    const int64_t e = e0 + 8 * int64_t(c) + q;
-    if (e >= used) return false;
-    if (e < begin || e >= cur.end) {
-      cur = seg_at(sg, used_mask, lo, hi, e, used, flags, SITE_NORM1_MASKED);
-      begin = __ldg(sg.start + cur.s);
-    }
-    return cur.on;
-  }
-};
-
 // The masked norm pass: one warp per reduction tile, the same partials as
 // the unmasked pass (tile_partial_warp) with elements of tensors without a
 // gradient counted as zero.  The tile's loads do not wait for the mask.
@@ -146,7 +63,7 @@ __global__ void __launch_bounds__(MNORM_THREADS, 3) norm_pass1_masked_kernel(
       }
     } else if (sole < 0) {
       const int lo = __ldg(sg.bucket_seg0 + ud->bucket), hi = __ldg(sg.bucket_seg0 + ud->bucket + 1);
-      MaskKeep keep{sg, used_mask, lo, hi, e0, ud->used, flags, SegCursor{lo, hi, 0, -1, false}, 0};
+      MaskKeep keep{sg, used_mask, lo, hi, e0, ud->used, flags, SITE_NORM1_MASKED, SegCursor{lo, hi, 0, -1, false}, 0};
       // (two chunk loads in flight per lane: the cursor needs the registers)
       s = tile_partial_warp<2>(acc + ud->state_off + e0, n >> 3, lane, keep);
     }

@@ -56,12 +56,24 @@ struct StageMeta {
   int32_t valid;    // elements before the padding starts (0..n)
   int32_t gc;       // rank rows in the stage
   float scale;
+  // Masked instantiation with norm partials, a tile spanning several
+  // tensors: its bucket row's segments [seg_lo, seg_hi) (seg_hi == seg_lo
+  // for every other tile), its first element in the row and the row's used
+  // count.
+  int64_t e0;
+  int64_t used;
+  int32_t seg_lo;
+  int32_t seg_hi;
 };
 
 constexpr size_t RED_SMEM_TAIL = 2 * RED_MAX_STAGES * sizeof(uint64_t)        // full/empty
                                  + RED_MAX_STAGES * sizeof(StageMeta)          // tile metadata
                                  + RED_MAX_STAGES * RED_CWARPS * sizeof(float) // warp partials
                                  + 16;                                          // abort flag
+// The masked instantiation's largest shared-memory request (ring, tail and
+// its two tile bitmaps) within the 227 KB a CTA may opt into.
+static_assert(RED_RING_BYTES + RED_SMEM_TAIL + size_t(RED_SKIP_WORDS) * 8 <= 227 * 1024,
+              "reduce_kernel shared memory above the per-CTA limit");
 
 struct ReduceArgs {
   const void* ranks[GRS_MAX_WORLD];  // bf16 bits or fp32, by the plan
@@ -85,8 +97,9 @@ struct ReduceArgs {
   int32_t stage_bytes;  // bytes per stage (multiple of 128)
   const uint8_t* used_mask;    // masked instantiation only
   const int32_t* tile_tensor;  // masked instantiation only
-  int32_t skip_words;          // masked instantiation only: bitmap words after the tail
+  int32_t skip_words;          // masked instantiation only: words of each bitmap after the tail
   int32_t n_tensors;           // masked instantiation only: entries of used_mask
+  Segs sg;                     // masked instantiation only: the plan's tensor segments
 };
 
 __device__ __forceinline__ float fold_partials(const float* wp) {
@@ -101,7 +114,11 @@ __device__ __forceinline__ float fold_partials(const float* wp) {
 // tensor without a gradient this step (one bit per tile, from the plan's
 // per-tile tensor table and the caller's mask); producer and consumers both
 // pass over those tiles, so they are neither read nor written and take no
-// stage.  The plain instantiation has none of this.
+// stage (their norm partial is +0).  A second bitmap marks the tiles that
+// span several tensors: with norm partials wanted, their elements of tensors
+// without a gradient count as zero in the partial (a segment cursor per
+// consumer thread), which makes the partials those of the masked norm pass
+// bit for bit.  The plain instantiation has none of this.
 template <typename E, bool kMasked>
 __global__ void __launch_bounds__(RED_THREADS, GRS_RED_CTAS_PER_SM) reduce_kernel(const __grid_constant__ ReduceArgs a) {
   constexpr uint32_t ESZ = sizeof(E);
@@ -114,6 +131,7 @@ __global__ void __launch_bounds__(RED_THREADS, GRS_RED_CTAS_PER_SM) reduce_kerne
   float* wp = reinterpret_cast<float*>(meta + RED_MAX_STAGES);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(wp + RED_MAX_STAGES * RED_CWARPS);
   uint32_t* skip = reinterpret_cast<uint32_t*>(smem + size_t(S) * a.stage_bytes + RED_SMEM_TAIL);
+  uint32_t* multi = skip + a.skip_words;  // masked: tiles spanning several tensors
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -129,24 +147,33 @@ __global__ void __launch_bounds__(RED_THREADS, GRS_RED_CTAS_PER_SM) reduce_kerne
   }
   const int64_t stride = gridDim.x;
   if constexpr (kMasked) {
-    // Bit k of the bitmap: this CTA's k-th tile (tile_begin + blockIdx.x + k * stride)
-    // lies in one tensor whose mask entry is 0.
+    // Bit k of the bitmaps: this CTA's k-th tile (tile_begin + blockIdx.x + k * stride)
+    // lies in one tensor whose mask entry is 0 (skip), or spans several (multi).
     for (int w = warp; w < a.skip_words; w += RED_THREADS / 32) {
       const int64_t k = int64_t(w) * 32 + lane;
       const int64_t tile = a.tile_begin + blockIdx.x + k * stride;
-      bool sk = false;
+      bool sk = false, mt = false;
       if (tile < a.tile_end && GRS_CHECK(tile < a.n_partials, a.flags, SITE_REDUCE)) {
         const int32_t t = __ldg(a.tile_tensor + tile);
         sk = t >= 0 && GRS_CHECK(t < a.n_tensors, a.flags, SITE_REDUCE) && __ldg(a.used_mask + t) == 0;
+        mt = t < 0;
       }
       const uint32_t bits = __ballot_sync(0xffffffffu, sk);
-      if (lane == 0) skip[w] = bits;
+      const uint32_t mbits = __ballot_sync(0xffffffffu, mt);
+      if (lane == 0) {
+        skip[w] = bits;
+        multi[w] = mbits;
+      }
     }
   }
   __syncthreads();
   // Tiles of this CTA it passes over (masked instantiation only).
   auto skipped = [&](int64_t k) -> bool {
     if constexpr (kMasked) return (skip[k >> 5] >> (k & 31)) & 1u;
+    return false;
+  };
+  auto spans = [&](int64_t k) -> bool {
+    if constexpr (kMasked) return (multi[k >> 5] >> (k & 31)) & 1u;
     return false;
   };
 
@@ -159,9 +186,18 @@ __global__ void __launch_bounds__(RED_THREADS, GRS_RED_CTAS_PER_SM) reduce_kerne
     int u = a.unit_begin;
     int64_t u_next = __ldg(a.prefix + u + 1);
     UnitDesc ud = a.units[u];
+    int32_t seg_lo = 0, seg_hi = 0;  // the unit's bucket segments (masked, with partials)
+    const bool seg_need = kMasked && a.partials != nullptr;
+    if (seg_need) {
+      seg_lo = __ldg(a.sg.bucket_seg0 + ud.bucket);
+      seg_hi = __ldg(a.sg.bucket_seg0 + ud.bucket + 1);
+    }
     int64_t k = 0;
     for (int64_t tile = a.tile_begin + blockIdx.x; tile < a.tile_end; tile += stride, ++k) {
-      if (skipped(k)) continue;
+      if (skipped(k)) {
+        if (a.partials != nullptr && lane == 0) a.partials[tile] = 0.0f;
+        continue;
+      }
       const int s = static_cast<int>(iter % S);
       const uint32_t ph = static_cast<uint32_t>((iter / S) & 1);
       if (tile >= u_next) {
@@ -170,6 +206,10 @@ __global__ void __launch_bounds__(RED_THREADS, GRS_RED_CTAS_PER_SM) reduce_kerne
           u_next = __ldg(a.prefix + u + 1);
         } while (tile >= u_next && (!GRS_CHECKED || u + 1 < a.unit_end));
         ud = a.units[u];
+        if (seg_need) {
+          seg_lo = __ldg(a.sg.bucket_seg0 + ud.bucket);
+          seg_hi = __ldg(a.sg.bucket_seg0 + ud.bucket + 1);
+        }
       }
       const int64_t T = ud.red_T;
       const int64_t e0 = (tile - ud.red_tile0) * T;
@@ -213,6 +253,11 @@ __global__ void __launch_bounds__(RED_THREADS, GRS_RED_CTAS_PER_SM) reduce_kerne
         md.valid = valid;
         md.gc = ud.g_count;
         md.scale = ud.scale;
+        const bool mixed = seg_need && spans(k);
+        md.e0 = e0;
+        md.used = ud.used;
+        md.seg_lo = mixed ? seg_lo : 0;
+        md.seg_hi = mixed ? seg_hi : 0;
         mbar_arrive_expect_tx(&full[s], bytes);
       }
       __syncwarp();
@@ -263,6 +308,11 @@ __global__ void __launch_bounds__(RED_THREADS, GRS_RED_CTAS_PER_SM) reduce_kerne
       const size_t row = size_t(n) * ESZ;
       const float* old = reinterpret_cast<const float*>(st + size_t(gc) * row);
       float psum = 0.0f;
+      // Masked, tile spanning several tensors: elements of tensors without a
+      // gradient add +0 to the partial (the stored values are unspecified).
+      const bool mixed = kMasked && md.seg_hi > md.seg_lo;
+      MaskKeep keep{a.sg, a.used_mask, md.seg_lo, md.seg_hi, md.e0, md.used, a.flags, SITE_REDUCE,
+                    SegCursor{md.seg_lo, md.seg_hi, 0, -1, false}, 0};
       for (int c = ct; c < (n >> 3); c += RED_CTHREADS) {
         const uint8_t* p = st + size_t(c) * 8 * ESZ;
         Sum8<E> sum;
@@ -293,8 +343,16 @@ __global__ void __launch_bounds__(RED_THREADS, GRS_RED_CTAS_PER_SM) reduce_kerne
         float4* o4 = reinterpret_cast<float4*>(out + el);
         o4[0] = make_float4(o[0], o[1], o[2], o[3]);
         o4[1] = make_float4(o[4], o[5], o[6], o[7]);
+        if (mixed) {
 #pragma unroll
-        for (int q = 0; q < 8; ++q) psum = __fmaf_rn(o[q], o[q], psum);
+          for (int q = 0; q < 8; ++q) {
+            const float x = keep(c, q) ? o[q] : 0.0f;
+            psum = __fmaf_rn(x, x, psum);
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) psum = __fmaf_rn(o[q], o[q], psum);
+        }
       }
       if (a.partials != nullptr) {
         psum = warp_sum(psum);
@@ -335,6 +393,7 @@ int launch_reduce(const grs_plan* p, const ReduceLaunch& l, void* stream) {
   a.used_mask = l.used_mask;
   a.tile_tensor = l.tile_tensor;
   a.n_tensors = static_cast<int32_t>(p->numel.size());
+  a.sg = Segs{p->d_seg_start, p->d_seg_tensor, p->d_bucket_seg0, a.n_tensors};
   const int64_t tiles = a.tile_end - a.tile_begin;
   if (tiles <= 0) return 0;
   // Stage size: the largest tile of the launched units (rank rows plus the
@@ -357,11 +416,11 @@ int launch_reduce(const grs_plan* p, const ReduceLaunch& l, void* stream) {
   const int64_t per_cta = (tiles + grid - 1) / grid;
   a.skip_words = masked ? static_cast<int32_t>((per_cta + 31) / 32) : 0;
   if (a.skip_words > RED_SKIP_WORDS) return static_cast<int>(cudaErrorInvalidValue);
-  const size_t smem = size_t(stages) * need + RED_SMEM_TAIL + size_t(a.skip_words) * 4;
+  const size_t smem = size_t(stages) * need + RED_SMEM_TAIL + size_t(a.skip_words) * 8;  // two bitmaps
   const int f32 = p->grad_esize == 4 ? 1 : 0;
   const int mk = masked ? 1 : 0;
   if (p->device >= 0 && p->device < 64 && !g_attr_set[f32][mk][p->device].load(std::memory_order_acquire)) {
-    const int bytes = static_cast<int>(RED_RING_BYTES + RED_SMEM_TAIL + (masked ? RED_SKIP_WORDS * 4 : 0));
+    const int bytes = static_cast<int>(RED_RING_BYTES + RED_SMEM_TAIL + (masked ? RED_SKIP_WORDS * 8 : 0));
     cudaError_t e;
     if (f32)
       e = masked ? cudaFuncSetAttribute(reduce_kernel<float, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)

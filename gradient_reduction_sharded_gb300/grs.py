@@ -111,7 +111,7 @@ _sig = {
     "grs_reduce_all": ([_vp, _P(_vp), _vp, ctypes.c_int32, ctypes.c_int32, _vp, _vp], ctypes.c_int),
     "grs_reduce_bucket_ex": ([_vp, ctypes.c_int32, _P(_vp), _vp, ctypes.c_int32, ctypes.c_int32, _vp,
                               ctypes.c_int32, _vp, _vp], ctypes.c_int),
-    "grs_reduce_all_masked": ([_vp, _P(_vp), _vp, ctypes.c_int32, _vp, _vp], ctypes.c_int),
+    "grs_reduce_all_masked": ([_vp, _P(_vp), _vp, ctypes.c_int32, ctypes.c_int32, _vp, _vp, _vp], ctypes.c_int),
     "grs_accumulate": ([_vp, ctypes.c_int32, _vp, _vp, _vp], ctypes.c_int),
     "grs_grad_norm_sq": ([_vp, _vp, ctypes.c_int32, _vp, ctypes.c_int32, _vp, _vp], ctypes.c_int),
     "grs_clip_adamw_step": ([_vp, _P(grs_adamw), _vp, _vp, _vp, _vp, _vp, _vp, _vp], ctypes.c_int),
@@ -244,10 +244,11 @@ def grs_reduce_all(plan: int, rank_grads: Sequence[int], acc: int, accumulate: i
                                workspace, stream), "grs_reduce_all")
 
 
-def grs_reduce_all_masked(plan: int, rank_grads: Sequence[int], acc: int, accumulate: int, d_tensor_used: int,
+def grs_reduce_all_masked(plan: int, rank_grads: Sequence[int], acc: int, accumulate: int,
+                          emit_norm_partials: int, d_tensor_used: int, workspace: Optional[int],
                           stream: int) -> None:
-    _check(_lib.grs_reduce_all_masked(plan, _ptrs(rank_grads), acc, accumulate, d_tensor_used, stream),
-           "grs_reduce_all_masked")
+    _check(_lib.grs_reduce_all_masked(plan, _ptrs(rank_grads), acc, accumulate, emit_norm_partials,
+                                      d_tensor_used, workspace, stream), "grs_reduce_all_masked")
 
 
 def grs_accumulate(plan: int, bucket: int, acc: int, mb: int, stream: int) -> None:

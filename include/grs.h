@@ -287,11 +287,22 @@ grs_status grs_reduce_all(const grs_plan* plan, const void* const* rank_grads, f
  * those tensors' gradients need not exist; every other tile is reduced as
  * grs_reduce_all reduces it (tiles spanning several tensors in full).  The
  * accumulator of a tensor with used = 0 is therefore unspecified: the
- * masked norm and update never use it.  No norm partials are emitted.
+ * masked norm and update never use it.
+ *   emit_norm_partials : 1 on the last microbatch to write, into
+ *                        `workspace`, the per-tile partials of the MASKED
+ *                        norm (elements of tensors with used = 0 count as
+ *                        zero; skipped tiles give +0), bit-identical to
+ *                        those of grs_grad_norm_sq_masked.  Then
+ *                        grs_grad_norm_sq(..., partials_ready = 1, ...)
+ *                        gives grs_grad_norm_sq_masked's S bit for bit
+ *                        without a pass over acc.
+ *   workspace          : as for grs_reduce_bucket; may be NULL when
+ *                        emit_norm_partials = 0.
  * Errors as grs_reduce_all, INVALID_ARG for a NULL mask, SHAPE beyond
  * 32768 reduction tiles per SM. */
 grs_status grs_reduce_all_masked(const grs_plan* plan, const void* const* rank_grads, float* acc,
-                                 int32_t accumulate, const uint8_t* d_tensor_used, void* stream);
+                                 int32_t accumulate, int32_t emit_norm_partials,
+                                 const uint8_t* d_tensor_used, void* workspace, void* stream);
 
 /* acc_b += mb_b over bucket b's rows (fp32), padding kept at zero: adds a
  * separately reduced microbatch gradient into the accumulator ([ISSUE]

@@ -147,17 +147,44 @@ class Run:
         self.norm_sq(partials_ready=partials_ready)
         self.adamw(max_norm=max_norm)
 
-    def masked_update(self, used_dev, steps_dev, n_micro=None, max_norm=None, step_hint=1):
+    def masked_reduce(self, used_dev, emit=True, n_micro=None):
+        """grs_reduce_all_masked over the microbatches; with emit, the last
+        one writes the masked norm partials into the workspace."""
+        g = grs()
+        M = self.c.n_micro if n_micro is None else n_micro
+        for j in range(M):
+            g.grs_reduce_all_masked(self.plan, self.ptrs(j), self.acc.data_ptr(), int(j > 0),
+                                    int(emit and j == M - 1), used_dev.data_ptr(), self.ws.data_ptr(),
+                                    self.stream())
+
+    def masked_norm_separate(self, used_dev, n_micro=None):
+        """S from the separate masked norm pass over acc, into a new buffer
+        (the workspace's partials are overwritten)."""
+        out = torch.zeros(1, dtype=torch.float64, device=self.dev)
+        M = self.c.n_micro if n_micro is None else n_micro
+        grs().grs_grad_norm_sq_masked(self.plan, self.acc.data_ptr(), M, used_dev.data_ptr(),
+                                      self.ws.data_ptr(), out.data_ptr(), self.stream())
+        return out
+
+    def masked_update(self, used_dev, steps_dev, n_micro=None, max_norm=None, step_hint=1,
+                      partials_ready=False):
         """Norm over used tensors and the per-tensor-step AdamW (the reduce
-        must have run).  step_hint goes in hp->step: tensors whose new step
-        equals it use host-computed factors, the others device-computed ones."""
+        must have run).  partials_ready: the masked reduction emitted the
+        norm partials, so only the finish runs (grs_grad_norm_sq); otherwise
+        the separate masked norm pass.  step_hint goes in hp->step: tensors
+        whose new step equals it use host-computed factors, the others
+        device-computed ones."""
         g = grs()
         c = self.c
         M = c.n_micro if n_micro is None else n_micro
         mn = c.max_norm if max_norm is None else max_norm
         s = self.stream()
-        g.grs_grad_norm_sq_masked(self.plan, self.acc.data_ptr(), M, used_dev.data_ptr(),
-                                  self.ws.data_ptr(), self.norm.data_ptr(), s)
+        if partials_ready:
+            g.grs_grad_norm_sq(self.plan, self.acc.data_ptr(), M, self.ws.data_ptr(), 1,
+                               self.norm.data_ptr(), s)
+        else:
+            g.grs_grad_norm_sq_masked(self.plan, self.acc.data_ptr(), M, used_dev.data_ptr(),
+                                      self.ws.data_ptr(), self.norm.data_ptr(), s)
         hp = g.make_adamw(c.hp[0], c.hp[1], c.hp[2], c.hp[3], c.hp[4], mn, step_hint, M)
         g.grs_clip_adamw_step_masked(self.plan, hp, self.norm.data_ptr(), self.acc.data_ptr(),
                                      self.master.data_ptr(), self.m.data_ptr(), self.v.data_ptr(),

@@ -53,7 +53,8 @@ def test_unused_variant_bytes_by_hand():
     idle = 64
     n_unique = sum(w.numels)
     vb = bench.variant_bytes(bench.oracle_buckets(op), 1, 2, op.n_state_pad, n_unique, idle)
-    assert vb["norm"] == 4 * (n_unique - 64)
+    assert vb["norm"] == 0  # fused into the masked reduction
+    assert vb["norm_pass"] == 4 * (n_unique - 64)
     assert vb["update"] == 30 * (op.n_state_pad - 64)
     assert vb["total"] == vb["reduce"] + vb["norm"] + vb["update"]
     plain = bench.variant_bytes(bench.oracle_buckets(op), 1, 2, op.n_state_pad, n_unique)

@@ -515,12 +515,14 @@ def test_unused_tensors_masked_update(fp32, zeros, masked_reduce):
                 run.fill_grads(step_seed=k + 1)
             used_dev = torch.tensor(used, dtype=torch.uint8, device="cuda")
             if masked_reduce:
-                for j in range(c.n_micro):
-                    grs().grs_reduce_all_masked(run.plan, run.ptrs(j), run.acc.data_ptr(), int(j > 0),
-                                                used_dev.data_ptr(), run.stream())
+                run.masked_reduce(used_dev)  # masked norm partials fused into the last microbatch
             else:
                 run.reduce(emit=False)
-            run.masked_update(used_dev, steps_dev)
+            run.masked_update(used_dev, steps_dev, partials_ready=masked_reduce)
+            if masked_reduce:  # the fused partials give the separate masked pass's S bit for bit
+                sep = run.masked_norm_separate(used_dev)
+                torch.cuda.synchronize()
+                assert float(sep.cpu()[0]) == float(run.norm.cpu()[0]), (k, float(sep[0]), float(run.norm[0]))
             torch.cuda.synchronize()
             assert run.check_flags() == 0
             res, steps = oracle.full_update_masked(run.op, run.bucket_inputs, c.n_micro, c.hp, c.max_norm,
@@ -616,12 +618,12 @@ def test_random_small_plans_match_oracle(trial):
     mrun = Run(c)
     try:
         used_dev = torch.tensor(used, dtype=torch.uint8, device="cuda")
-        for j in range(c.n_micro):
-            g.grs_reduce_all_masked(mrun.plan, mrun.ptrs(j), mrun.acc.data_ptr(), int(j > 0), used_dev.data_ptr(),
-                                    mrun.stream())
-        mrun.masked_update(used_dev, torch.zeros(n, dtype=torch.int32, device="cuda"))
+        mrun.masked_reduce(used_dev)
+        mrun.masked_update(used_dev, torch.zeros(n, dtype=torch.int32, device="cuda"), partials_ready=True)
+        sep = mrun.masked_norm_separate(used_dev)
         torch.cuda.synchronize()
         assert mrun.check_flags() == 0
+        assert float(sep.cpu()[0]) == float(mrun.norm.cpu()[0]), (trial, float(sep[0]), float(mrun.norm[0]))
         res, _ = oracle.full_update_masked(mrun.op, mrun.bucket_inputs, c.n_micro, c.hp, c.max_norm, used, [0] * n,
                                            master0, m0, v0, bits0)
         where = np.ones(mrun.nsp, bool)
@@ -706,7 +708,7 @@ def test_masked_reduction_skips_tiles_of_unused_tensors():
             for k in range(c.world):
                 b.grads[0][k].view(torch.int16)[lo:lo + op.per_rank(i)] = 0x7FC0
         b.acc.fill_(123.0)
-        g.grs_reduce_all_masked(b.plan, b.ptrs(0), b.acc.data_ptr(), 0, used_dev.data_ptr(), b.stream())
+        b.masked_reduce(used_dev, emit=False)
         torch.cuda.synchronize()
         assert b.check_flags() == 0
         got, want = b.acc[:b.nsp].cpu().numpy(), a.acc[:a.nsp].cpu().numpy()
@@ -722,6 +724,16 @@ def test_masked_reduction_skips_tiles_of_unused_tensors():
         torch.cuda.synchronize()
         assert b.check_flags() == 0
         assert np.isfinite(float(b.norm.cpu()[0]))
+        # The same reduction with the norm partials fused: the poisoned
+        # elements of tiles shared with used tensors count as zero there too.
+        b.acc.fill_(123.0)
+        b.masked_reduce(used_dev)
+        b.norm_sq(partials_ready=True)
+        fused = b.norm.clone()
+        sep = b.masked_norm_separate(used_dev)
+        torch.cuda.synchronize()
+        assert b.check_flags() == 0
+        assert np.isfinite(float(fused.cpu()[0])) and float(fused.cpu()[0]) == float(sep.cpu()[0])
     finally:
         a.close()
         b.close()
@@ -729,18 +741,21 @@ def test_masked_reduction_skips_tiles_of_unused_tensors():
 
 def test_masked_reduction_with_every_tensor_used_equals_plain():
     """grs_reduce_all_masked with every tensor marked used reduces every tile:
-    the accumulator equals grs_reduce_all's bit for bit (two microbatches)."""
+    the accumulator and the fused norm partials (hence S) equal
+    grs_reduce_all's bit for bit (two microbatches)."""
     c = SMALL["multi-tile-world16-M2"]
     a, b = Run(c), Run(c)
     try:
         g = grs()
         ones = torch.ones(len(c.numels), dtype=torch.uint8, device="cuda")
-        a.reduce(emit=False)
-        for j in range(c.n_micro):
-            g.grs_reduce_all_masked(b.plan, b.ptrs(j), b.acc.data_ptr(), int(j > 0), ones.data_ptr(), b.stream())
+        a.reduce(emit=True)
+        a.norm_sq(partials_ready=True)
+        b.masked_reduce(ones)
+        b.norm_sq(partials_ready=True)
         torch.cuda.synchronize()
         assert a.check_flags() == 0 and b.check_flags() == 0
         assert torch.equal(a.acc[:a.nsp], b.acc[:b.nsp])
+        assert float(a.norm.cpu()[0]) == float(b.norm.cpu()[0])
     finally:
         a.close()
         b.close()

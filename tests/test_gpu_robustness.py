@@ -77,8 +77,9 @@ def test_no_writes_outside_outputs():
 
 
 def test_masked_and_layout_calls_write_inside_outputs():
-    """The masked norm and update (tensors without a gradient, zero-size
-    tensors among them) and the state layout conversions write nothing
+    """The masked norm, the masked reduction with its fused norm partials and
+    the masked update (tensors without a gradient, zero-size tensors among
+    them) and the state layout conversions write nothing
     outside their outputs; the masked update leaves the state of tensors
     without a gradient untouched and the layout restore writes every
     padding element as zero."""
@@ -108,6 +109,11 @@ def test_masked_and_layout_calls_write_inside_outputs():
             g.grs_reduce_all(run.plan, run.ptrs(j), acc.data_ptr(), int(j > 0), 0, ws.data_ptr(), s)
         g.grs_grad_norm_sq_masked(run.plan, acc.data_ptr(), c.n_micro, used.data_ptr(), ws.data_ptr(),
                                   nrm.data_ptr(), s)
+        # the masked reduction with its fused norm partials, then the finish alone
+        for j in range(c.n_micro):
+            g.grs_reduce_all_masked(run.plan, run.ptrs(j), acc.data_ptr(), int(j > 0), int(j == c.n_micro - 1),
+                                    used.data_ptr(), ws.data_ptr(), s)
+        g.grs_grad_norm_sq(run.plan, acc.data_ptr(), c.n_micro, ws.data_ptr(), 1, nrm.data_ptr(), s)
         hp = g.make_adamw(*c.hp, c.max_norm, 1, c.n_micro)
         g.grs_clip_adamw_step_masked(run.plan, hp, nrm.data_ptr(), acc.data_ptr(), st["master"][1].data_ptr(),
                                      st["m"][1].data_ptr(), st["v"][1].data_ptr(), st["params"][1].data_ptr(),
