@@ -355,8 +355,9 @@ grs_status grs_clip_adamw_step(const grs_plan* plan, const grs_adamw* hp, const 
  *
  * grs_grad_norm_sq_masked: like grs_grad_norm_sq with partials_ready = 0,
  * but elements of tensors with used = 0 count as zero (clip_grad_norm_
- * skips parameters without a gradient).  The fused reduce partials are not
- * used.
+ * skips parameters without a gradient): a separate pass over acc.  After a
+ * grs_reduce_all_masked that emitted its norm partials, the same S comes
+ * from grs_grad_norm_sq(..., partials_ready = 1, ...) without that pass.
  *
  * grs_clip_adamw_step_masked: like grs_clip_adamw_step for tensors with
  * used = 1, each with its own step count: d_tensor_steps (device int32
