@@ -106,7 +106,7 @@ struct MaskedArgs {
   uint16_t* params;
   const double* norm_sq;
   const UnitDesc* units;
-  const int64_t* prefix;
+  const int32_t* tile_unit;    // per update tile: its unit
   Segs sg;
   const uint8_t* used_mask;
   const int32_t* tile_tensor;  // per update tile: the tensor holding it whole, or -1
@@ -131,9 +131,10 @@ __global__ void __launch_bounds__(MUPD_THREADS, GRS_MUPD_MIN_BLOCKS) update_mask
   // A tile inside one tensor (the common case): one mask bit and one factor
   // pair for the whole block; a tile without a gradient is neither read nor
   // written.
-  // (The unit search runs while the tile's tensor, mask bit and factors load.)
+  // (The tile's unit and tensor load together.)
   const int32_t sole = __ldg(a.tile_tensor + tile);
-  const int u = find_unit(a.prefix, 0, a.n_units, tile);
+  const int u = __ldg(a.tile_unit + tile);
+  if (!GRS_CHECK(u >= 0 && u < a.n_units, a.flags, SITE_UPDATE_MASKED)) return;
   const UnitDesc* ud = a.units + u;
   const int64_t el = (static_cast<int64_t>(tile) - ud->upd_tile0) * UPD_T + int64_t(threadIdx.x) * 8;
   const int64_t padded = ud->padded;
@@ -280,7 +281,7 @@ int launch_update_masked(const grs_plan* p, const grs_adamw* hp, const double* d
   a.params = params;
   a.norm_sq = d_norm_sq;
   a.units = p->d_units;
-  a.prefix = p->d_upd_prefix;
+  a.tile_unit = p->d_upd_tile_unit;
   a.sg = Segs{p->d_seg_start, p->d_seg_tensor, p->d_bucket_seg0, static_cast<int32_t>(p->numel.size())};
   a.used_mask = used;
   a.tile_tensor = p->d_upd_tile_tensor;

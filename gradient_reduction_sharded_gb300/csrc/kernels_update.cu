@@ -127,7 +127,7 @@ struct UpdateArgs {
   uint16_t* params;
   const double* norm_sq;
   const UnitDesc* units;
-  const int64_t* prefix;
+  const int32_t* tile_unit;  // [tiles]: the unit of each update tile
   int* flags;
   int64_t n_state;   // elements of acc, master, m, v and params
   int32_t n_units;
@@ -151,7 +151,8 @@ __global__ void __launch_bounds__(UPD_THREADS) update_kernel(const __grid_consta
   pdl_trigger();
   // Clip coefficient from the device-resident S, evaluated by every thread.
   const float gscale = a.max_norm > 0.0f ? clip_gscale(*a.norm_sq, a.max_norm, a.inv_m) : a.inv_m;
-  const int u = find_unit(a.prefix, 0, a.n_units, tile);
+  const int u = __ldg(a.tile_unit + tile);
+  if (!GRS_CHECK(u >= 0 && u < a.n_units, a.flags, SITE_UPDATE)) return;
   const UnitDesc* ud = a.units + u;
   const int64_t e0 = (static_cast<int64_t>(tile) - ud->upd_tile0) * UPD_T;
   const int64_t el = e0 + int64_t(threadIdx.x) * 8;  // element within the unit
@@ -284,7 +285,7 @@ int launch_update(const grs_plan* p, const grs_adamw* hp, const double* d_norm_s
   a.params = params;
   a.norm_sq = d_norm_sq;
   a.units = p->d_units;
-  a.prefix = p->d_upd_prefix;
+  a.tile_unit = p->d_upd_tile_unit;
   a.flags = p->d_flags;
   a.n_state = p->n_state_pad;
   a.n_units = static_cast<int32_t>(p->units.size());

@@ -257,9 +257,13 @@ grs_status build_plan(const int64_t* numels, const int32_t* owners, const uint32
   // a tile spans several tensors or reaches the padding), unit by unit.
   p->red_tile_tensor.clear();
   p->upd_tile_tensor.clear();
-  for (const UnitDesc& u : p->units) {
+  p->upd_tile_unit.clear();
+  for (size_t ui = 0; ui < p->units.size(); ++ui) {
+    const UnitDesc& u = p->units[ui];
     sole_tensors(*p, u.bucket, u.red_T, p->red_tile_tensor);
     sole_tensors(*p, u.bucket, UPD_T, p->upd_tile_tensor);
+    p->upd_tile_unit.insert(p->upd_tile_unit.end(), static_cast<size_t>(p->upd_prefix[ui + 1] - p->upd_prefix[ui]),
+                            static_cast<int32_t>(ui));
   }
   p->workspace_bytes = ws_factors_offset(red_tiles) + (static_cast<int64_t>(n) * 8 + 255) / 256 * 256;
   return GRS_OK;
