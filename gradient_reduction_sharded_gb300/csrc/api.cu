@@ -69,8 +69,10 @@ void free_device(grs_plan* p) {
   p->d_tensor_live = nullptr;
   cudaFree(p->d_red_tile_tensor);
   cudaFree(p->d_upd_tile_tensor);
+  cudaFree(p->d_red_tile_unit);
   cudaFree(p->d_upd_tile_unit);
-  p->d_red_tile_tensor = p->d_upd_tile_tensor = p->d_upd_tile_unit = nullptr;
+  p->d_red_tile_tensor = p->d_upd_tile_tensor = nullptr;
+  p->d_red_tile_unit = p->d_upd_tile_unit = nullptr;
   p->d_seg_start = nullptr;
   p->d_seg_tensor = nullptr;
   p->d_bucket_seg0 = nullptr;
@@ -135,6 +137,7 @@ grs_status grs_plan_create_ex(const int64_t* numels, const int32_t* owners, cons
     if (e == cudaSuccess) e = upload(&p->d_tensor_live, p->tensor_live);
     if (e == cudaSuccess) e = upload(&p->d_red_tile_tensor, p->red_tile_tensor);
     if (e == cudaSuccess) e = upload(&p->d_upd_tile_tensor, p->upd_tile_tensor);
+    if (e == cudaSuccess) e = upload(&p->d_red_tile_unit, p->red_tile_unit);
     if (e == cudaSuccess) e = upload(&p->d_upd_tile_unit, p->upd_tile_unit);
     if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&p->d_flags), grs::FLAG_COUNT * sizeof(int));
     if (e == cudaSuccess) e = cudaMemset(p->d_flags, 0, grs::FLAG_COUNT * sizeof(int));

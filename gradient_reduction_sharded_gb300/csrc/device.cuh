@@ -248,20 +248,6 @@ __device__ __forceinline__ void adamw_elem(float G, float gscale, float step_siz
   V = vv;
 }
 
-// Last unit u with prefix[u] <= tile (prefix has n_units + 1 entries).
-__device__ __forceinline__ int find_unit(const int64_t* __restrict__ prefix, int lo, int hi,
-                                         int64_t tile) {
-  // invariant: prefix[lo] <= tile < prefix[hi]
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (__ldg(prefix + mid) <= tile)
-      lo = mid;
-    else
-      hi = mid;
-  }
-  return lo;
-}
-
 // Sum over the warp with a fixed butterfly (every lane gets the result).
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll

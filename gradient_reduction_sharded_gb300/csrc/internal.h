@@ -126,8 +126,10 @@ struct grs_plan {
   // or -1 (the masked passes look a tile's mask bit up in one load).
   std::vector<int32_t> red_tile_tensor;  // [n_red_tiles]
   std::vector<int32_t> upd_tile_tensor;  // [n_upd_tiles]
-  // Per update tile: its unit (the update kernels look it up in one load
-  // instead of searching the tile prefix).
+  // Per reduction tile / per update tile: its unit (the norm, update and
+  // accumulate kernels look it up in one load instead of searching the tile
+  // prefix).
+  std::vector<int32_t> red_tile_unit;    // [n_red_tiles]
   std::vector<int32_t> upd_tile_unit;    // [n_upd_tiles]
   int64_t n_unique = 0, n_rank_pad = 0, n_state_pad = 0;
   int64_t n_red_tiles = 0, n_upd_tiles = 0, n_gather_chunks = 0;
@@ -146,6 +148,7 @@ struct grs_plan {
   uint8_t* d_tensor_live = nullptr;
   int32_t* d_red_tile_tensor = nullptr;
   int32_t* d_upd_tile_tensor = nullptr;
+  int32_t* d_red_tile_unit = nullptr;
   int32_t* d_upd_tile_unit = nullptr;
   int* d_flags = nullptr;  // [4]: timeout, nonfinite, reserved
   void* host_step_resources = nullptr;  // copy stream + events of grs_step_from_host

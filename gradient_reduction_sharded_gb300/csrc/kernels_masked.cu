@@ -37,7 +37,7 @@ static_assert(UPD_T == MUPD_THREADS * 8, "one 8-element group per thread per til
 // the unmasked pass (tile_partial_warp) with elements of tensors without a
 // gradient counted as zero.  The tile's loads do not wait for the mask.
 __global__ void __launch_bounds__(MNORM_THREADS, 3) norm_pass1_masked_kernel(
-    const float* __restrict__ acc, const UnitDesc* __restrict__ units, const int64_t* __restrict__ prefix,
+    const float* __restrict__ acc, const UnitDesc* __restrict__ units, const int32_t* __restrict__ tile_unit,
     int32_t n_units, int64_t n_tiles, Segs sg, const uint8_t* __restrict__ used_mask,
     const int32_t* __restrict__ tile_tensor, float* __restrict__ partials, int64_t n_state,
     int* __restrict__ flags) {
@@ -45,7 +45,8 @@ __global__ void __launch_bounds__(MNORM_THREADS, 3) norm_pass1_masked_kernel(
   const int64_t n_warps = int64_t(gridDim.x) * (MNORM_THREADS / 32);
   for (int64_t tile = int64_t(blockIdx.x) * (MNORM_THREADS / 32) + (threadIdx.x >> 5); tile < n_tiles;
        tile += n_warps) {
-    const int u = find_unit(prefix, 0, n_units, tile);
+    const int u = __ldg(tile_unit + tile);
+    if (!GRS_CHECK(u >= 0 && u < n_units, flags, SITE_NORM1_MASKED)) continue;  // (warp-uniform)
     const UnitDesc* ud = units + u;
     const int64_t T = ud->red_T;
     const int64_t e0 = (tile - ud->red_tile0) * T;
@@ -250,7 +251,7 @@ int launch_norm_masked(const grs_plan* p, const float* acc, int32_t n_micro, con
     const int64_t cap = int64_t(p->sm_count) * MNORM_BLOCKS_PER_SM;
     const int64_t grid = need < cap ? need : cap;
     norm_pass1_masked_kernel<<<static_cast<unsigned>(grid), MNORM_THREADS, 0, s>>>(
-        acc, p->d_units, p->d_red_prefix, static_cast<int32_t>(p->units.size()), p->n_red_tiles,
+        acc, p->d_units, p->d_red_tile_unit, static_cast<int32_t>(p->units.size()), p->n_red_tiles,
         Segs{p->d_seg_start, p->d_seg_tensor, p->d_bucket_seg0, static_cast<int32_t>(p->numel.size())}, used,
         p->d_red_tile_tensor, partials,
         p->n_state_pad, p->d_flags);

@@ -37,7 +37,7 @@ static_assert(UPD_T == UPD_THREADS * 8, "one 8-element group per thread per tile
 // gw, gw + (all warps), ...
 __global__ void __launch_bounds__(NORM1_THREADS) norm_pass1_kernel(const float* __restrict__ acc,
                                                                    const UnitDesc* __restrict__ units,
-                                                                   const int64_t* __restrict__ prefix,
+                                                                   const int32_t* __restrict__ tile_unit,
                                                                    int32_t n_units, int64_t n_tiles,
                                                                    float* __restrict__ partials, int64_t n_state,
                                                                    int* __restrict__ flags) {
@@ -48,7 +48,8 @@ __global__ void __launch_bounds__(NORM1_THREADS) norm_pass1_kernel(const float* 
   KeepAll all;
   for (int64_t tile = int64_t(blockIdx.x) * (NORM1_THREADS / 32) + (threadIdx.x >> 5); tile < n_tiles;
        tile += n_warps) {
-    const int u = find_unit(prefix, 0, n_units, tile);
+    const int u = __ldg(tile_unit + tile);
+    if (!GRS_CHECK(u >= 0 && u < n_units, flags, SITE_NORM1)) continue;  // (warp-uniform)
     const UnitDesc* ud = units + u;
     const int64_t T = ud->red_T;
     const int64_t e0 = (tile - ud->red_tile0) * T;
@@ -196,16 +197,21 @@ __global__ void __launch_bounds__(UPD_THREADS) update_kernel(const __grid_consta
 __global__ void __launch_bounds__(UPD_THREADS) accumulate_kernel(float* __restrict__ acc,
                                                                  const float* __restrict__ mb,
                                                                  const UnitDesc* __restrict__ units,
-                                                                 const int64_t* __restrict__ prefix,
+                                                                 const int32_t* __restrict__ tile_unit,
                                                                  int32_t unit_begin, int32_t unit_end,
                                                                  int64_t tile_begin, int64_t state_base,
                                                                  int64_t state_len, int* __restrict__ flags) {
   const int64_t tile = tile_begin + blockIdx.x;
-  const int u = find_unit(prefix, unit_begin, unit_end, tile);
+  // The plan's tables are read while the kernel before finishes; acc and mb after.
+  const int u = __ldg(tile_unit + tile);
+  if (!GRS_CHECK(u >= unit_begin && u < unit_end, flags, SITE_ACCUMULATE)) return;
   const UnitDesc* ud = units + u;
   const int64_t el = (tile - ud->upd_tile0) * UPD_T + int64_t(threadIdx.x) * 8;
-  if (el >= ud->padded) return;
+  const int64_t padded = ud->padded, used = ud->used;
   const int64_t i = ud->state_off - state_base + el;
+  pdl_wait();
+  pdl_trigger();
+  if (el >= padded) return;
   if (!GRS_CHECK(el >= 0 && i >= 0 && i + 8 <= state_len, flags, SITE_ACCUMULATE)) return;
   float4* a4 = reinterpret_cast<float4*>(acc + i);
   const float4* b4 = reinterpret_cast<const float4*>(mb + i);
@@ -216,7 +222,7 @@ __global__ void __launch_bounds__(UPD_THREADS) accumulate_kernel(float* __restri
                 __fadd_rn(x1.z, y1.z), __fadd_rn(x1.w, y1.w)};
 #pragma unroll
   for (int q = 0; q < 8; ++q)
-    if (el + q >= ud->used) o[q] = 0.0f;
+    if (el + q >= used) o[q] = 0.0f;
   a4[0] = make_float4(o[0], o[1], o[2], o[3]);
   a4[1] = make_float4(o[4], o[5], o[6], o[7]);
 }
@@ -234,7 +240,7 @@ int launch_norm(const grs_plan* p, const float* acc, int32_t n_micro, void* work
     const int64_t grid = need < cap ? need : cap;
     const int e = static_cast<int>(launch_k(norm_pass1_kernel, dim3(unsigned(grid)), dim3(NORM1_THREADS), 0, s,
                                             acc, static_cast<const UnitDesc*>(p->d_units),
-                                            static_cast<const int64_t*>(p->d_red_prefix),
+                                            static_cast<const int32_t*>(p->d_red_tile_unit),
                                             static_cast<int32_t>(p->units.size()), p->n_red_tiles, partials,
                                             p->n_state_pad, p->d_flags));
     if (e != 0) return e;
@@ -301,11 +307,10 @@ int launch_accumulate(const grs_plan* p, int32_t bucket, float* acc, const float
   const int32_t ub = bk.unit0, ue = bk.unit0 + bk.copies;
   const int64_t t0 = p->upd_prefix[ub], t1 = p->upd_prefix[ue];
   if (t1 <= t0) return 0;
-  accumulate_kernel<<<static_cast<unsigned>(t1 - t0), UPD_THREADS, 0,
-                      static_cast<cudaStream_t>(stream)>>>(acc, mb, p->d_units, p->d_upd_prefix, ub, ue,
-                                                           t0, bk.state_off, int64_t(bk.copies) * bk.padded,
-                                                           p->d_flags);
-  return static_cast<int>(cudaGetLastError());
+  return static_cast<int>(launch_k(accumulate_kernel, dim3(static_cast<unsigned>(t1 - t0)), dim3(UPD_THREADS), 0,
+                                   stream, acc, mb, static_cast<const UnitDesc*>(p->d_units),
+                                   static_cast<const int32_t*>(p->d_upd_tile_unit), ub, ue, t0, bk.state_off,
+                                   int64_t(bk.copies) * bk.padded, p->d_flags));
 }
 
 }  // namespace grs

@@ -257,11 +257,14 @@ grs_status build_plan(const int64_t* numels, const int32_t* owners, const uint32
   // a tile spans several tensors or reaches the padding), unit by unit.
   p->red_tile_tensor.clear();
   p->upd_tile_tensor.clear();
+  p->red_tile_unit.clear();
   p->upd_tile_unit.clear();
   for (size_t ui = 0; ui < p->units.size(); ++ui) {
     const UnitDesc& u = p->units[ui];
     sole_tensors(*p, u.bucket, u.red_T, p->red_tile_tensor);
     sole_tensors(*p, u.bucket, UPD_T, p->upd_tile_tensor);
+    p->red_tile_unit.insert(p->red_tile_unit.end(), static_cast<size_t>(p->red_prefix[ui + 1] - p->red_prefix[ui]),
+                            static_cast<int32_t>(ui));
     p->upd_tile_unit.insert(p->upd_tile_unit.end(), static_cast<size_t>(p->upd_prefix[ui + 1] - p->upd_prefix[ui]),
                             static_cast<int32_t>(ui));
   }
