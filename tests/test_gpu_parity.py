@@ -345,6 +345,17 @@ def test_argument_errors():
         with pytest.raises(g.GrsError) as ei:
             g.grs_reduce_bucket(run.plan, 99, ptrs, run.acc.data_ptr(), 0, 0, None, s)
         assert ei.value.status == g.GRS_ERR_INVALID_ARG
+        used = torch.ones(len(c.numels), dtype=torch.uint8, device="cuda")
+        with pytest.raises(g.GrsError) as ei:  # norm partials need a workspace
+            g.grs_reduce_all_masked(run.plan, ptrs, run.acc.data_ptr(), 0, 1, used.data_ptr(), None, s)
+        assert ei.value.status == g.GRS_ERR_INVALID_ARG
+        with pytest.raises(g.GrsError) as ei:
+            g.grs_reduce_all_masked(run.plan, ptrs, run.acc.data_ptr(), 0, 0, None, None, s)
+        assert ei.value.status == g.GRS_ERR_INVALID_ARG
+        with pytest.raises(g.GrsError) as ei:
+            g.grs_reduce_all_masked(run.plan, ptrs, run.acc.data_ptr(), 0, 1, used.data_ptr(),
+                                    run.ws.data_ptr() + 4, s)
+        assert ei.value.status == g.GRS_ERR_ALIGNMENT
         hp = g.make_adamw(1e-3, 0.9, 0.999, 1e-8, 0.0, 1.0, 0, 1)
         with pytest.raises(g.GrsError) as ei:
             g.grs_clip_adamw_step(run.plan, hp, run.norm.data_ptr(), run.acc.data_ptr(),
