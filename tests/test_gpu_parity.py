@@ -956,3 +956,51 @@ def test_check_already_reduced_flags_disagreeing_copies():
         assert run.check_flags() == 0
     finally:
         run.close()
+
+
+@pytest.mark.parametrize("kind", ["every-tensor-frozen", "every-tensor-empty"])
+def test_plans_without_state(kind):
+    """Degenerate plans with no state element: every tensor frozen (no
+    bucket at all) or every tensor of size zero (buckets without tiles).
+    Every entry point of the path runs and does nothing: S = 0 as the
+    oracle's, no device flag, and the caller's buffers untouched."""
+    g = grs()
+    numels = [100, 200, 64] if kind == "every-tensor-frozen" else [0, 0, 0]
+    flags = [1, 1, 1] if kind == "every-tensor-frozen" else [0, 0, 0]
+    c = Case(numels, [RA, PS, AR], 4, 1, 2, 2, 1 << 20, 2, 1e-3, 31, tensor_flags=flags)
+    run = Run(c)
+    try:
+        assert run.nsp == 0 and run.info["n_reduce_tiles"] == 0
+        s = run.stream()
+        run.master.fill_(0.5)
+        run.norm.fill_(7.0)
+        run.update()
+        torch.cuda.synchronize()
+        assert run.check_flags() == 0
+        res = oracle_update(run, np.zeros(0, np.float32), np.zeros(0, np.float32), np.zeros(0, np.float32), step=1)
+        assert float(run.norm.cpu()[0]) == 0.0 == float(res.norm_sq)
+        used = torch.ones(len(numels), dtype=torch.uint8, device="cuda")
+        steps = torch.zeros(len(numels), dtype=torch.int32, device="cuda")
+        run.norm.fill_(7.0)
+        run.masked_reduce(used)
+        run.masked_update(used, steps, partials_ready=True)
+        torch.cuda.synchronize()
+        assert run.check_flags() == 0 and float(run.norm.cpu()[0]) == 0.0
+        # tensors without state keep their step counts (frozen ones are ignored)
+        assert steps.cpu().tolist() == ([0, 0, 0] if kind == "every-tensor-frozen" else [1, 1, 1])
+        dst = [torch.full((max(n, 1),), -3, dtype=torch.int16, device="cuda") for n in numels]
+        g.grs_gather_params(run.plan, run.params.data_ptr(), [t.data_ptr() for t in dst], s)
+        logical = torch.full((8,), -1.0, dtype=torch.float32, device="cuda")
+        g.grs_state_to_logical(run.plan, run.master.data_ptr(), logical.data_ptr(), s)
+        g.grs_state_from_logical(run.plan, logical.data_ptr(), run.m.data_ptr(), s)
+        hp = g.make_adamw(*c.hp, c.max_norm, 1, c.n_micro)
+        run.norm.fill_(7.0)
+        g.grs_update_small(run.plan, hp, [p for j in range(c.n_micro) for p in run.ptrs(j)], run.acc.data_ptr(),
+                           run.master.data_ptr(), run.m.data_ptr(), run.v.data_ptr(), run.params.data_ptr(),
+                           run.norm.data_ptr(), s)
+        torch.cuda.synchronize()
+        assert run.check_flags() == 0 and float(run.norm.cpu()[0]) == 0.0
+        assert all(bool((t == -3).all()) for t in dst)
+        assert bool((logical == -1.0).all()) and bool((run.master == 0.5).all())
+    finally:
+        run.close()
