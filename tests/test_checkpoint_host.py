@@ -107,3 +107,37 @@ def test_async_save_reports_failure_from_wait(tmp_path, grs, ck):
         assert os.path.exists(os.path.join(str(tmp_path / "ck4"), ck.SUCCESS))
     finally:
         grs.grs_plan_destroy(plan)
+
+
+def test_many_shard_files_in_parallel(tmp_path, grs, ck):
+    """24 shard files (tp 2 x dp_shard 12), more than the I/O threads: every
+    file written and read back exactly; a truncated file is refused."""
+    spec = spec_of(ck, numels=[4001, 77, 960, 9, 123456, 24], world=24, tp=2, dp_replicate=1, dp_shard=12,
+                   bucket_bytes=4096)
+    plan = spec.create(host_only=True)
+    try:
+        n = grs.grs_plan_query(plan)["n_state_pad"]
+        op = oracle.plan(spec.numels, spec.owners, spec.world, spec.tp, spec.dp_replicate, spec.dp_shard,
+                         spec.bucket_bytes)
+        keep = np.zeros(n, bool)
+        for b in range(op.n_buckets):
+            for t in range(op.copies(b)):
+                o = int(op.b_state_off[b]) + t * int(op.b_padded[b])
+                keep[o:o + int(op.b_used[b])] = True
+        rng = np.random.default_rng(11)
+        arrays = {nm: np.where(keep, rng.normal(0, 1, n), 0).astype(np.float32)
+                  for nm in ("master", "exp_avg", "exp_avg_sq")}
+        d = str(tmp_path / "many")
+        ck.write_shards(d, plan, spec, arrays, {"step": 3})
+        files = sorted(f for f in os.listdir(d) if f.startswith("shard_"))
+        assert len(files) == 24
+        _, back = ck.read_shards(d)
+        for nm in arrays:
+            assert np.array_equal(back[nm], arrays[nm])
+        victim = os.path.join(d, "shard_s7_t1.bin")
+        with open(victim, "r+b") as f:
+            f.truncate(os.path.getsize(victim) - 4)
+        with pytest.raises(ck.CheckpointError):
+            ck.read_shards(d)
+    finally:
+        grs.grs_plan_destroy(plan)
