@@ -78,12 +78,11 @@ void free_device(grs_plan* p) {
   p->d_bucket_seg0 = nullptr;
   cudaFree(p->d_units);
   cudaFree(p->d_red_prefix);
-  cudaFree(p->d_upd_prefix);
   cudaFree(p->d_jobs);
   cudaFree(p->d_chunk_job);
   cudaFree(p->d_flags);
   p->d_units = nullptr;
-  p->d_red_prefix = p->d_upd_prefix = nullptr;
+  p->d_red_prefix = nullptr;
   p->d_jobs = nullptr;
   p->d_chunk_job = nullptr;
   p->d_flags = nullptr;
@@ -128,7 +127,6 @@ grs_status grs_plan_create_ex(const int64_t* numels, const int32_t* owners, cons
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p->sm_count, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess) e = upload(&p->d_units, p->units);
     if (e == cudaSuccess) e = upload(&p->d_red_prefix, p->red_prefix);
-    if (e == cudaSuccess) e = upload(&p->d_upd_prefix, p->upd_prefix);
     if (e == cudaSuccess) e = upload(&p->d_jobs, p->jobs);
     if (e == cudaSuccess) e = upload(&p->d_chunk_job, p->chunk_job);
     if (e == cudaSuccess) e = upload(&p->d_seg_start, p->seg_start);

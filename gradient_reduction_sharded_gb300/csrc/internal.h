@@ -139,7 +139,6 @@ struct grs_plan {
   int sm_count = 0;
   grs::UnitDesc* d_units = nullptr;
   int64_t* d_red_prefix = nullptr;
-  int64_t* d_upd_prefix = nullptr;
   grs::GatherJob* d_jobs = nullptr;
   int32_t* d_chunk_job = nullptr;
   int64_t* d_seg_start = nullptr;
