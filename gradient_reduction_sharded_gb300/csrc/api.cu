@@ -138,7 +138,8 @@ grs_status grs_plan_create_ex(const int64_t* numels, const int32_t* owners, cons
     if (e == cudaSuccess) e = upload(&p->d_red_tile_unit, p->red_tile_unit);
     if (e == cudaSuccess) e = upload(&p->d_upd_tile_unit, p->upd_tile_unit);
     if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&p->d_flags), grs::FLAG_COUNT * sizeof(int));
-    if (e == cudaSuccess) e = cudaMemset(p->d_flags, 0, grs::FLAG_COUNT * sizeof(int));
+    if (e == cudaSuccess) e = cudaMemsetAsync(p->d_flags, 0, grs::FLAG_COUNT * sizeof(int), nullptr);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(nullptr);  // cleared before any launch on any stream
     if (e != cudaSuccess) {
       free_device(p);
       delete p;
@@ -547,7 +548,10 @@ grs_status grs_check_device_errors(const grs_plan* p, void* stream) {
   int h[grs::FLAG_COUNT] = {};
   e = cudaMemcpy(h, p->d_flags, sizeof(h), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(e, "grs_check_device_errors: flags");
-  e = cudaMemset(p->d_flags, 0, sizeof(h));
+  // Cleared on the caller's stream and waited for, so that no later launch
+  // on that stream (a non-blocking one included) can race with the clear.
+  e = cudaMemsetAsync(p->d_flags, 0, sizeof(h), static_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess) e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "grs_check_device_errors: clear flags");
   if (h[grs::FLAG_BOUNDS]) {
     static const char* const kSite[grs::SITE_COUNT] = {
