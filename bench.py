@@ -877,7 +877,8 @@ def cpu_baseline(w, mb, args, u=None, target_s=10.0):
     return {"value": ms, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"{reps} whole updates of the workload ({op.n_buckets} buckets, "
                       f"{mb['total'] / 1e9:.2f} GB mandatory bytes each), one thread, {dt:.1f} s",
-            "all_cores": {"value": dtn * 1e3, "cores": nthr,
+            "gbs": mb["total"] / (ms * 1e-3) / 1e9,
+            "all_cores": {"value": dtn * 1e3, "cores": nthr, "gbs": mb["total"] / dtn / 1e9,
                           "note": f"one whole update, {min(nthr, op.n_buckets)} buckets in parallel"}}
 
 
@@ -905,7 +906,7 @@ def cpu_baseline_variant(w, u, mb, args, target_s=10.0):
     what = (f"{reps} whole updates of the variant" if whole else
             f"{reps} updates of buckets {buckets} of {op.n_buckets}, scaled by bytes")
     return {"value": ms, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{what}, one thread, {dt:.1f} s"}
+            "sample": f"{what}, one thread, {dt:.1f} s", "gbs": mb["total"] / (ms * 1e-3) / 1e9}
 
 
 def run_reference(args, rank, world_size):
