@@ -639,7 +639,7 @@ def run_e2e(u: GpuUpdate, args, torch):
         nread = 1 if int(d["tag"]) == 3 else W
         h2d += M * nread * int(d["padded"]) * 2
     d2h = out_params.numel() * 2 + 8
-    steps = max(3, min(args.steps, 10))
+    steps = max(3, min(args.steps, 20))  # pipeline fill and drain (~1 ms) spread over the steps
     a = w.adamw
 
     def one():
