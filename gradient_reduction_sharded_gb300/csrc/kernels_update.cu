@@ -202,7 +202,8 @@ __global__ void __launch_bounds__(UPD_THREADS) accumulate_kernel(float* __restri
                                                                  int64_t tile_begin, int64_t state_base,
                                                                  int64_t state_len, int* __restrict__ flags) {
   const int64_t tile = tile_begin + blockIdx.x;
-  // The plan's tables are read while the kernel before finishes; acc and mb after.
+  // The plan's tables are read before the dependent-launch wait (which
+  // waits only when the build enables dependent launch); acc and mb after.
   const int u = __ldg(tile_unit + tile);
   if (!GRS_CHECK(u >= unit_begin && u < unit_end, flags, SITE_ACCUMULATE)) return;
   const UnitDesc* ud = units + u;
