@@ -235,21 +235,33 @@ def test_two_threads_two_plans_two_streams():
             r.close()
 
 
-def test_step_captured_in_a_cuda_graph_matches_eager():
+@pytest.mark.parametrize("route", ["separate-masked-norm", "masked-reduction-partials"])
+def test_step_captured_in_a_cuda_graph_matches_eager(route):
     """One update (grouped reduction, masked norm, masked AdamW with device
     step counters) captured once in a CUDA graph and replayed three times
     equals three eager updates: the path is stream-ordered, allocation-free
-    and keeps its step counts on the device."""
+    and keeps its step counts on the device.  Two routes: the plain
+    reduction and the separate masked norm pass, or the masked reduction
+    with its fused partials and the finish alone (one tensor without a
+    gradient)."""
     c = Case([50001, 512, 8192 * 2, 77], [RA, PS, LS, AR], 8, 2, 2, 2, 1 << 16, 2, 1e-3, 81)
     eager, graph_run = Run(c), Run(c)
+    fused = route == "masked-reduction-partials"
     try:
         n = len(c.numels)
-        used = torch.ones(n, dtype=torch.uint8, device="cuda")
+        used = torch.tensor([1, 0, 1, 1] if fused else [1] * n, dtype=torch.uint8, device="cuda")
         st_e = torch.zeros(n, dtype=torch.int32, device="cuda")
         st_g = torch.zeros(n, dtype=torch.int32, device="cuda")
+
+        def step(run, st):
+            if fused:
+                run.masked_reduce(used)
+            else:
+                run.reduce(emit=False)
+            run.masked_update(used, st, partials_ready=fused)
+
         for _ in range(3):
-            eager.reduce(emit=False)
-            eager.masked_update(used, st_e)
+            step(eager, st_e)
         torch.cuda.synchronize()
         graph = torch.cuda.CUDAGraph()
         side = torch.cuda.Stream()
@@ -257,16 +269,18 @@ def test_step_captured_in_a_cuda_graph_matches_eager():
         with torch.cuda.stream(side):
             # the library needs no warm-up allocations: capture directly
             with torch.cuda.graph(graph, stream=side):
-                graph_run.reduce(emit=False)
-                graph_run.masked_update(used, st_g)
+                step(graph_run, st_g)
         torch.cuda.synchronize()
         for _ in range(3):
             graph.replay()
         torch.cuda.synchronize()
-        assert st_g.tolist() == st_e.tolist() == [3] * n
-        for x, y in ((eager.acc, graph_run.acc), (eager.norm, graph_run.norm), (eager.master, graph_run.master),
+        want_steps = [3 * int(u) for u in used.tolist()]
+        assert st_g.tolist() == st_e.tolist() == want_steps
+        for x, y in ((eager.norm, graph_run.norm), (eager.master, graph_run.master),
                      (eager.m, graph_run.m), (eager.v, graph_run.v), (eager.params, graph_run.params)):
             assert torch.equal(x, y)
+        if not fused:  # with a mask the accumulator of the tensor without a gradient is unspecified
+            assert torch.equal(eager.acc, graph_run.acc)
     finally:
         eager.close()
         graph_run.close()
