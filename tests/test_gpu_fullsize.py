@@ -58,7 +58,8 @@ def test_full_size_update_matches_oracle(cid):
 
 # The variants bench.py measures (--variant / --window), in the same launch
 # configuration: fp32 rank gradients, tensors without a gradient (masked
-# norm and update), frozen tensors, a trailing window of 3 of 4 microbatches.
+# reduction with its fused norm partials, masked update), frozen tensors, a
+# trailing window of 3 of 4 microbatches.
 @pytest.mark.parametrize("cid,variant,window", [(1, "fp32-grads", 0), (1, "unused", 0),
                                                 (1, "frozen", 0), (3, "plain", 3)])
 def test_full_size_variant_matches_oracle(cid, variant, window):
