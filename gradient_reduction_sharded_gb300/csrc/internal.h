@@ -93,7 +93,11 @@ struct GatherJob {
   int32_t tensor;
   int32_t pad_;
 };
-constexpr int64_t GATHER_CHUNK = 8192;
+// Elements per gather / layout chunk (one block each).
+#ifndef GRS_GATHER_CHUNK
+#define GRS_GATHER_CHUNK 16384
+#endif
+constexpr int64_t GATHER_CHUNK = GRS_GATHER_CHUNK;
 
 }  // namespace grs
 
