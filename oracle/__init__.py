@@ -310,9 +310,10 @@ class UpdateResult:
     params_bf16: np.ndarray
     # Optional brackets of master, m, v: the update evaluated at acc - delta
     # and acc + delta, delta bounding an fp32 evaluation's accumulation error
-    # (see accumulation_error_bound).
+    # (see accumulation_error_bound), and delta itself [n_state_pad].
     lo: Optional[tuple] = None
     hi: Optional[tuple] = None
+    delta: Optional[np.ndarray] = None
 
 
 U32 = 2.0 ** -24  # unit roundoff of fp32
@@ -324,13 +325,33 @@ def abs_inputs(g: np.ndarray) -> np.ndarray:
     return np.abs(g) if g.dtype == np.float32 else (g & np.uint16(0x7FFF))
 
 
-def accumulation_error_bound(acc_abs: np.ndarray, M: int) -> np.ndarray:
-    """Forward error bound of accumulating a bucket row in fp32: every term
-    is added to a running fp32 sum (or, within a microbatch, compensated),
-    so |fl(acc) - acc| <= (M + 2) * u * sum |terms|, where acc_abs is the
-    same reduction of the absolute inputs (Higham, Accuracy and Stability of
-    Numerical Algorithms, recursive summation)."""
-    return (M + 2) * U32 * acc_abs
+def gamma(k: int) -> float:
+    """Higham's gamma_k = k u / (1 - k u) for fp32 (u = 2^-24): the bound on
+    the relative perturbation that k roundings can put on one term."""
+    return k * U32 / (1.0 - k * U32)
+
+
+def group_terms(p: OraclePlan, b: int) -> int:
+    """Ranks summed into one output element of bucket b per microbatch: the
+    whole world for REPLICA_AVG and PARTIAL_SUM, the DP group for
+    LOCAL_SHARD, rank 0 alone for ALREADY_REDUCED."""
+    tag = int(p.b_tag[b])
+    return p.world if tag in (REPLICA_AVG, PARTIAL_SUM) else (p.dp if tag == LOCAL_SHARD else 1)
+
+
+def accumulation_error_bound(acc_abs: np.ndarray, M: int, group: int) -> np.ndarray:
+    """Forward error bound of an fp32 evaluation of one accumulator element:
+    per microbatch, the `group` rank values summed by recursive fp32
+    addition in any order (group - 1 roundings; a compensated sum stays
+    inside the same bound), multiplied by the tag's scale held in fp32 (one
+    rounding of the constant, one of the product) and added into the fp32
+    accumulator (one rounding per later microbatch, two if the multiply and
+    add are not fused).  Every term then carries at most group + M + 1
+    roundings, so |fl(acc) - acc| <= gamma_{group+M+1} * sum |terms|, where
+    acc_abs is the same reduction of the absolute inputs, i.e. sum |terms|
+    (Higham, Accuracy and Stability of Numerical Algorithms, 2nd ed.,
+    Lemma 3.1 and section 4.2 on recursive summation)."""
+    return gamma(group + M + 1) * acc_abs
 
 
 def full_update(p: OraclePlan, grads_of, M: int, hp, max_norm: float, step: int,
@@ -349,7 +370,7 @@ def full_update(p: OraclePlan, grads_of, M: int, hp, max_norm: float, step: int,
         if bounds:
             ab = reduce_bucket(int(p.b_tag[b]), p.tp, p.dp_replicate, p.dp_shard, P, int(p.b_used[b]),
                                abs_inputs(g))
-            delta[off:off + ab.size] = accumulation_error_bound(ab.reshape(-1), M)
+            delta[off:off + ab.size] = accumulation_error_bound(ab.reshape(-1), M, group_terms(p, b))
 
     if threads > 1:
         from concurrent.futures import ThreadPoolExecutor
@@ -380,6 +401,7 @@ def full_update(p: OraclePlan, grads_of, M: int, hp, max_norm: float, step: int,
     if bounds:
         res.lo = update(acc - delta)[:3]
         res.hi = update(acc + delta)[:3]
+        res.delta = delta
     return res
 
 
@@ -404,7 +426,7 @@ def full_update_masked(p: OraclePlan, grads_of, M: int, hp, max_norm: float, use
         if bounds:
             ab = reduce_bucket(int(p.b_tag[b]), p.tp, p.dp_replicate, p.dp_shard, P, int(p.b_used[b]),
                                abs_inputs(g))
-            delta[off:off + ab.size] = accumulation_error_bound(ab.reshape(-1), M)
+            delta[off:off + ab.size] = accumulation_error_bound(ab.reshape(-1), M, group_terms(p, b))
     s = 0.0
     for i in range(len(p.numel)):
         if used[i]:
@@ -437,4 +459,5 @@ def full_update_masked(p: OraclePlan, grads_of, M: int, hp, max_norm: float, use
     if bounds:
         res.lo = update(acc - delta)[:3]
         res.hi = update(acc + delta)[:3]
+        res.delta = delta
     return res, new_steps

@@ -18,7 +18,8 @@ import torch
 
 import oracle
 import workloads
-from gpu_support import assert_bf16_cast, assert_close, assert_close_bracketed
+from gpu_support import (assert_bf16_cast, assert_close, assert_close_bracketed,
+                         assert_within_accumulation_bound)
 
 RA = workloads.REPLICA_AVG
 
@@ -64,6 +65,61 @@ def test_full_size_update_matches_oracle(cid):
                                                 (1, "frozen", 0), (3, "plain", 3)])
 def test_full_size_variant_matches_oracle(cid, variant, window):
     _full_size(cid, variant, window)
+
+
+def test_workload1_every_element_matches_oracle():
+    """The 67M-parameter, world-16 workload (the benchmark's smallest large
+    plan) with no sampling: one update in the bench's launch configuration,
+    then every element of the accumulator, master, moments and bf16
+    parameters against the oracle's whole update (all six buckets), the
+    accumulator within the fp32 accumulation bound, padding exactly zero."""
+    import bench
+    from gpu_support import assert_bf16_cast as cast_check, padding_mask
+
+    w = workloads.get(1)
+    op = oracle.plan(w.numels, w.owners, w.world, w.tp, w.dp_replicate, w.dp_shard, w.bucket_bytes)
+    u = bench.GpuUpdate(w, torch.device("cuda"))
+    try:
+        n = op.n_state_pad
+        assert u.info["n_state_pad"] == n
+        master0 = u.master[:n].cpu().numpy().copy()
+        z = np.zeros(n, np.float32)
+        u.step()
+        torch.cuda.synchronize()
+        assert u.grs.grs_check_device_errors(u.plan, u.stream) == 0
+        M, R = w.n_micro, w.world
+
+        def grads_of(b):
+            ro, P = int(op.b_rank_off[b]), int(op.b_padded[b])
+            return np.stack([np.stack([u.grads[j][k][ro:ro + P].view(torch.int16).cpu().numpy()
+                                       for k in range(R)]) for j in range(M)]).view(np.uint16)
+
+        a = w.adamw
+        hp = (a.lr, a.beta1, a.beta2, a.eps, a.weight_decay)
+        res = oracle.full_update(op, grads_of, M, hp, a.max_norm, 1, master0, z, z,
+                                 threads=max(1, min(8, os.cpu_count() or 1)), bounds=True)
+        what = "workload 1, every element"
+        acc = u.acc[:n].cpu().numpy()
+        assert_close(acc, res.acc, f"{what} acc")
+        assert_within_accumulation_bound(acc, res.acc, res.delta, f"{what} acc")
+        assert_close([float(u.norm.cpu()[0])], [res.norm_sq], f"{what} norm_sq")
+        master = u.master[:n].cpu().numpy()
+        mm = u.m[:n].cpu().numpy()
+        vv = u.v[:n].cpu().numpy()
+        for name, got, want, lo, hi in zip(("master", "m", "v"), (master, mm, vv), (res.master, res.m, res.v),
+                                           res.lo, res.hi):
+            assert_close_bracketed(got, want, lo, hi, f"{what} {name}")
+        bits = u.params[:n].cpu().numpy().view(np.uint16)
+        cast_check(bits, master, res.params_bf16, res.master, f"{what} params", lo_master=res.lo[0],
+                   hi_master=res.hi[0])
+        pad = padding_mask(op)
+        assert pad.any()
+        for arr in (acc, master, mm, vv, bits):
+            assert np.all(arr[pad] == 0)
+    finally:
+        u.close()
+        del u
+        torch.cuda.empty_cache()
 
 
 def test_single_tensor_beyond_32_bit_indices():
@@ -206,7 +262,7 @@ def _full_size_w(w, variant, window):
         # ---- sampled accumulator and update
         a = w.adamw
         hp = (a.lr, a.beta1, a.beta2, a.eps, a.weight_decay)
-        want_acc, want_p, want_m, want_v, want_bits = [], [], [], [], []
+        want_acc, want_delta, want_p, want_m, want_v, want_bits = [], [], [], [], [], []
         lo_p, lo_m, lo_v, hi_p, hi_m, hi_v = [], [], [], [], [], []
         idle = []  # sampled state positions of tensors without a gradient
         for b in range(op.n_buckets):
@@ -220,10 +276,11 @@ def _full_size_w(w, variant, window):
                                        len(pos), n_valid, g)
             delta = oracle.accumulation_error_bound(
                 oracle.reduce_bucket(int(op.b_tag[b]), op.tp, op.dp_replicate, op.dp_shard, len(pos),
-                                     n_valid, oracle.abs_inputs(g)), M)
+                                     n_valid, oracle.abs_inputs(g)), M, oracle.group_terms(op, b))
             off_idle = (pos < used) & ~counts[b][pos]
             for t in range(op.copies(b)):
                 want_acc.append(acc[t])
+                want_delta.append(delta[t])
                 off = sum(len(samples[bb]) * op.copies(bb) for bb in range(b)) + t * len(pos)
                 m0 = master0[off:off + len(pos)]
                 z = np.zeros(len(pos), np.float32)
@@ -254,6 +311,8 @@ def _full_size_w(w, variant, window):
         # the masked reduction leaves the accumulator of tensors without a
         # gradient unspecified: only the others are compared
         assert_close(got_acc[~idle], cat(want_acc)[~idle], f"{what} acc")
+        assert_within_accumulation_bound(got_acc[~idle], cat(want_acc)[~idle], cat(want_delta)[~idle],
+                                         f"{what} acc")
         assert_close_bracketed(got_p, cat(want_p), cat(lo_p), cat(hi_p), f"{what} master")
         assert_close_bracketed(got_m, cat(want_m), cat(lo_m), cat(hi_m), f"{what} m")
         assert_close_bracketed(got_v, cat(want_v), cat(lo_v), cat(hi_v), f"{what} v")

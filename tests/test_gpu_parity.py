@@ -11,7 +11,8 @@ import torch
 
 import oracle
 from gpu_support import (Case, Run, assert_bf16_cast, assert_close, assert_close_bracketed,
-                         case_from_workload, grs, oracle_update, padding_mask)
+                         assert_within_accumulation_bound, case_from_workload, grs, oracle_update,
+                         padding_mask)
 
 pytestmark = pytest.mark.gpu
 
@@ -37,6 +38,9 @@ def full_check(run: Run, res, what="", acc_where=None):
         assert_close(acc, res.acc, f"{what} acc")
     else:
         assert_close(acc[acc_where], res.acc[acc_where], f"{what} acc")
+    if res.delta is not None:  # the bound behind the master/moment brackets holds on the kernel
+        w = np.ones(n, bool) if acc_where is None else acc_where
+        assert_within_accumulation_bound(acc[w], res.acc[w], res.delta[w], f"{what} acc")
     assert np.all(acc[pad] == 0), f"{what} acc padding not zero"
     norm = float(run.norm.cpu()[0])
     assert_close([norm], [res.norm_sq], f"{what} norm_sq")
@@ -891,12 +895,17 @@ def test_bounded_wait_times_out_and_context_survives():
 def test_overlapped_reverse_order_reduction_matches_grouped():
     """Buckets produced in reverse order on a 'backward' stream, each reduced
     on a side stream as soon as its event fires, with a capped grid: the
-    accumulator and the norm equal the grouped launch's bit for bit."""
+    accumulator and the norm equal the grouped launch's bit for bit, and the
+    whole update matches the oracle ("refactor(distributed): establish
+    shared native TP replica ownership", "Preserved prototype and evidence":
+    the asynchronous FP32 reduction hook; "Proposed scope": overlap during
+    backward)."""
     g = grs()
     c = SMALL["multi-tile-world16-M2"]
     ref = Run(c)
     run = Run(c)
     try:
+        master0, m0, v0 = run.state_host()
         ref.update()
         torch.cuda.synchronize()
         src = [[t.clone() for t in mb] for mb in run.grads]
@@ -929,6 +938,8 @@ def test_overlapped_reverse_order_reduction_matches_grouped():
         torch.cuda.synchronize()
         for x, y in ((ref.acc, run.acc), (ref.norm, run.norm), (ref.master, run.master), (ref.params, run.params)):
             assert torch.equal(x, y)
+        assert run.check_flags() == 0
+        full_check(run, oracle_update(run, master0, m0, v0, step=1), "overlapped reverse order")
     finally:
         ref.close()
         run.close()

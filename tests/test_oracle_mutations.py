@@ -43,9 +43,28 @@ MUTANTS = [
     ("greedy bucket test off by one", "2 * (used + per_rank) > bucket_bytes", "2 * (used + per_rank) >= bucket_bytes"),
     ("LOCAL_SHARD counted with its full numel per rank",
      "per_rank = (tag == OR_LOCAL_SHARD) ? numel[i] / tp : numel[i];", "per_rank = numel[i];"),
+    ("bf16 gather: LOCAL_SHARD row t at t * chunk instead of t * padded",
+     "params_full[bucket_state_off + (int64_t)t * bucket_padded + tensor_offset + i];",
+     "params_full[bucket_state_off + (int64_t)t * chunk + tensor_offset + i];"),
+    ("bf16 gather: offset inside the bucket dropped",
+     "for (i = 0; i < numel; ++i) dst[i] = params_full[bucket_state_off + tensor_offset + i];",
+     "for (i = 0; i < numel; ++i) dst[i] = params_full[bucket_state_off + i];"),
+    ("bf16 gather: LOCAL_SHARD chunks in reverse tp order",
+     "dst[t * chunk + i] =\n            params_full[",
+     "dst[(tp - 1 - t) * chunk + i] =\n            params_full["),
     ("LOCAL_SHARD rows gathered in the wrong place",
      "dst[t * chunk + i] = state[bucket_state_off + (int64_t)t * bucket_padded + tensor_offset + i];",
      "dst[t * chunk + i] = state[bucket_state_off + tensor_offset + (int64_t)t * chunk + i];"),
+]
+
+
+# The pins of the fp32 accumulation error bound (Python side of the oracle).
+BOUND_PINS = [
+    ("bound_ranks", lambda: pins.test_accumulation_bound_absorption_across_ranks(None)),
+    ("bound_micro", lambda: pins.test_accumulation_bound_absorption_across_microbatches(None)),
+    ("bound_abs", lambda: pins.test_accumulation_bound_uses_absolute_values(None)),
+    ("bound_random", lambda: pins.test_accumulation_bound_random_cancelling(None, 12, 3)),
+    ("gamma", lambda: pins.test_gamma_closed_form(None)),
 ]
 
 
@@ -68,7 +87,8 @@ def run_pins():
         ("adamw_torch", lambda: pins.test_adamw_multistep_matches_torch(None, (1e-3, 0.9, 0.999, 1e-8, 0.01))),
         ("bf16", lambda: pins.test_bf16_rne_matches_torch(None)),
         ("logical", lambda: pins.test_logical_layout_hand_derived(None)),
-    ] + [(f"plan:{c['name']}", (lambda c=c: pins.test_plan_hand_derived(None, c)))
+        ("gather_bf16", lambda: pins.test_gather_tensor_bf16_hand_derived(None)),
+    ] + BOUND_PINS + [(f"plan:{c['name']}", (lambda c=c: pins.test_plan_hand_derived(None, c)))
          for c in pins.PLAN_CASES["cases"]]
     for name, fn in calls:
         try:
@@ -100,4 +120,31 @@ def test_pins_catch_mutant(what, old, new, tmp_path):
         failed = run_pins()
     finally:
         oracle._lib = real
+    assert failed, f"no pin caught the mutant: {what}"
+
+
+# Plausible slips in the bound that widens the master/moment checks: each
+# replaces one function of the oracle's Python side, and a pin must fail.
+U = 2.0 ** -24
+BOUND_MUTANTS = [
+    ("bound without the group's additions ((M + 2) u)", "accumulation_error_bound",
+     lambda acc_abs, M, group: (M + 2) * U * acc_abs),
+    ("bound without the microbatch term", "accumulation_error_bound",
+     lambda acc_abs, M, group: oracle.gamma(group + 1) * acc_abs),
+    ("bound four times too wide", "accumulation_error_bound",
+     lambda acc_abs, M, group: 4 * oracle.gamma(group + M + 1) * acc_abs),
+    ("bound from the signed inputs", "abs_inputs", lambda g: g),
+    ("gamma without its denominator", "gamma", lambda k: k * U),
+]
+
+
+@pytest.mark.parametrize("what,name,fn", BOUND_MUTANTS, ids=[m[0] for m in BOUND_MUTANTS])
+def test_bound_pins_catch_mutant(what, name, fn, monkeypatch):
+    monkeypatch.setattr(oracle, name, fn)
+    failed = []
+    for nm, call in BOUND_PINS:
+        try:
+            call()
+        except AssertionError:
+            failed.append(nm)
     assert failed, f"no pin caught the mutant: {what}"

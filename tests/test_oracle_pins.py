@@ -472,3 +472,140 @@ def test_logical_layout_hand_derived(orc):
     keep = np.zeros(p.n_state_pad, bool)
     keep[want.astype(int)] = True
     assert np.array_equal(back[keep], st[keep]) and np.all(back[~keep] == 0)
+
+
+def test_gather_tensor_bf16_hand_derived(orc):
+    """oracle.gather_tensor (bf16 parameters) on a hand-laid-out plan whose
+    buckets hold two tensors of the same tag, so tensors sit at nonzero
+    offsets inside their bucket.  Plan [21 RA, 5 PS, 18 LS, 3 AR, 10 LS,
+    7 RA], tp 2, dp_shard 2, one bucket per tag (padding quantum 8 * 2):
+      RA bucket: tensor 0 at 0 (21), tensor 5 at 21 (7); used 28, padded 32;
+                 state [0, 32)
+      PS bucket: tensor 1 at 0 (5); padded 16; state [32, 48)
+      LS bucket: per tp row tensor 2 at 0 (9), tensor 4 at 9 (5); used 14,
+                 padded 16; rows t = 0, 1 at state 48 and 64
+      AR bucket: tensor 3 at 0 (3); padded 16; state [80, 96)
+    With every parameter equal to its own state index, the gathered tensors
+    are those indices: a LOCAL_SHARD tensor is row 0's chunk then row 1's
+    (its dim-0 halves) at state_off + t * padded + offset ("Cosmos 3 ...
+    distributed parallelism", section 2: all-gather of the shards)."""
+    p = oracle.plan([21, 5, 18, 3, 10, 7], [REPLICA_AVG, PARTIAL_SUM, LOCAL_SHARD, ALREADY_REDUCED,
+                                            LOCAL_SHARD, REPLICA_AVG], 4, 2, 1, 2, 25 << 20)
+    assert list(p.b_state_off) == [0, 32, 48, 80] and list(p.b_padded) == [32, 16, 16, 16]
+    assert list(p.t_offset) == [0, 0, 0, 0, 9, 21] and p.n_state_pad == 96
+    params = np.arange(p.n_state_pad, dtype=np.uint16)
+    want = {0: np.arange(0, 21), 1: np.arange(32, 37), 2: np.r_[48:57, 64:73], 3: np.arange(80, 83),
+            4: np.r_[57:62, 73:78], 5: np.arange(21, 28)}
+    for i, w in want.items():
+        got = oracle.gather_tensor(p, i, params)
+        assert got.dtype == np.uint16 and np.array_equal(got, w.astype(np.uint16)), (i, got, w)
+    # the fp32 twin places every tensor in the same way
+    st = np.arange(p.n_state_pad, dtype=np.float32)
+    assert np.array_equal(oracle.to_logical(p, st),
+                          np.concatenate([want[i] for i in range(6)]).astype(np.float32))
+
+
+# --------------------------------------------------------------------------
+# The fp32 accumulation error bound that widens the master/moment checks
+# (oracle.accumulation_error_bound).  Each case evaluates the accumulator
+# the way an fp32 implementation may (per microbatch the group's bf16 values
+# summed left to right in fp32, times the fp32 scale, added into an fp32
+# accumulator), computes the exact value in rational arithmetic, and checks
+# the error against the bound the oracle gives from the absolute inputs.
+# --------------------------------------------------------------------------
+TINY = 2.0 ** -25 * (1 + 2.0 ** -7)  # bf16, under half an fp32 ulp of 1.0 (TINY / 2: of 0.5)
+
+
+def _fp32_eval(vals, scale):
+    """vals [M][group] (floats exactly representable in bf16) -> fp32 acc."""
+    sc = np.float32(scale)
+    acc = np.float32(0.0)
+    for j, row in enumerate(vals):
+        s = np.float32(row[0])
+        for x in row[1:]:
+            s = np.float32(s + np.float32(x))
+        p_ = np.float32(s * sc)
+        acc = p_ if j == 0 else np.float32(acc + p_)
+    return float(acc)
+
+
+def _exact(vals, group):
+    from fractions import Fraction
+    return Fraction(sum(Fraction(float(x)) for row in vals for x in row)) / group
+
+
+def _bound_case(vals):
+    """(|fp32 - exact|, delta) for one REPLICA_AVG element over a world of
+    `group` ranks (tp 1, dp_replicate = group, dp_shard 1: scale 1/group)."""
+    vals = np.asarray(vals, np.float64)
+    M, R = vals.shape
+    bits = bf16(vals.reshape(M, R, 1))
+    assert np.array_equal(bits_to_f32(bits).astype(np.float64).reshape(M, R), vals), "not bf16"
+    g = np.zeros((M, R, 8), np.uint16)
+    g[:, :, 0] = bits[:, :, 0]
+    acc = oracle.reduce_bucket(REPLICA_AVG, 1, R, 1, 8, 1, g)
+    ab = oracle.reduce_bucket(REPLICA_AVG, 1, R, 1, 8, 1, oracle.abs_inputs(g))
+    delta = float(oracle.accumulation_error_bound(ab, M, R)[0, 0])
+    exact = _exact(vals, R)
+    assert abs(acc[0, 0] - float(exact)) <= 1e-15 * float(ab[0, 0])  # the fp64 oracle itself
+    return abs(_fp32_eval(vals, 1.0 / R) - float(exact)), delta
+
+
+def test_accumulation_bound_absorption_across_ranks(orc):
+    """1.0 on rank 0 and TINY on each of the 15 others: every fp32 addition
+    rounds TINY away, an error of 15 TINY = 7.6 u of the sum of |terms|.
+    The bound must cover it (a bound without the group's additions, e.g.
+    (M + 2) u, would not) and not exceed it by more than 3x."""
+    err, delta = _bound_case([[1.0] + [TINY] * 15])
+    assert 0 < err <= delta
+    assert err >= delta / 3
+    assert err > 3 * 2.0 ** -24 * (1 + 15 * TINY) / 16  # what (M + 2) u would allow
+
+
+def test_accumulation_bound_absorption_across_microbatches(orc):
+    """Two ranks, 16 microbatches: the first brings 0.5 into the
+    accumulator, each later one TINY / 2, which rounds away: the error grows
+    with M, and the bound must grow with it (a bound without M would not
+    cover it)."""
+    vals = [[1.0, 0.0]] + [[TINY, 0.0]] * 15
+    err, delta = _bound_case(vals)
+    assert 0 < err <= delta
+    assert err >= delta / 3
+    assert err > oracle.gamma(2 + 1) * (1 + 15 * TINY) / 2  # a bound without the M term
+
+
+def test_accumulation_bound_uses_absolute_values(orc):
+    """1 + TINY - 1: the fp32 sum is 0, the exact one TINY / 3.  The signed
+    sum of the terms is TINY / 3, far too small to bound the error: the bound
+    must be taken from the absolute values."""
+    err, delta = _bound_case([[1.0, TINY, -1.0]])
+    assert err == TINY / 3
+    assert err <= delta
+    assert err > oracle.gamma(3 + 1 + 1) * (TINY / 3)
+
+
+@pytest.mark.parametrize("R,M", [(16, 1), (12, 3), (4, 8), (128, 1)])
+def test_accumulation_bound_random_cancelling(orc, R, M):
+    """Random bf16 values with exponents spread over 2^-24..1 and adjacent
+    ranks nearly cancelling (x, -x (1 - 2^-8)): every fp32 evaluation stays
+    within the bound."""
+    rng = np.random.default_rng(R * 100 + M)
+    worst = 0.0
+    for _ in range(300):
+        mag = 2.0 ** rng.integers(-24, 1, (M, R)) * (1 + rng.integers(0, 128, (M, R)) / 128)
+        sign = rng.choice([-1.0, 1.0], (M, R))
+        vals = mag * sign
+        vals[:, 1::2] = -vals[:, 0:R - R % 2:2] * (1 - 2.0 ** -8)
+        vals = bits_to_f32(bf16(vals)).astype(np.float64)
+        err, delta = _bound_case(vals)
+        assert err <= delta, (vals, err, delta)
+        worst = max(worst, err / delta)
+    assert worst < 1.0
+
+
+def test_gamma_closed_form(orc):
+    """gamma_k = k u / (1 - k u) with u = 2^-24."""
+    u = 2.0 ** -24
+    for k in (1, 3, 18, 133):
+        assert oracle.gamma(k) == k * u / (1 - k * u)
+    assert oracle.gamma(0) == 0.0

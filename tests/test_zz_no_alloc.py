@@ -6,15 +6,17 @@ runtime).  It keeps its scratch in a static device array instead of a
 caller-provided workspace.
 
 Checked through the C ABI against grs_grad_norm_sq (the workspace entry
-point) within the suite's tolerance, on two calls in a row with different
-plans, so contents left in the shared array by one call cannot leak into the
-next.  This file is collected last on purpose.
+point, with partials_ready = 0: the same pass and the same fixed-order fp64
+finish, so the two agree bit for bit) and against the oracle's norm within
+the suite's tolerance, on two calls in a row with different plans, so
+contents left in the shared array by one call cannot leak into the next.
+This file is collected last on purpose.
 """
 import numpy as np
 import pytest
 import torch
 
-from gpu_support import RTOL, ATOL, Case, Run, case_from_workload, grs
+from gpu_support import RTOL, ATOL, Case, Run, case_from_workload, grs, oracle_update
 
 pytestmark = pytest.mark.gpu
 
@@ -51,9 +53,12 @@ def test_noalloc_norm_matches_workspace_entry_point_twice():
     for c in cases:
         run = Run(c)
         try:
+            master0, m0, v0 = run.state_host()
             ref, got = _norm_both(run)
             assert ref > 0
-            assert abs(got - ref) <= ATOL + RTOL * abs(ref), (got, ref)
+            assert got == ref, (got, ref)  # bit for bit
+            want = oracle_update(run, master0, m0, v0, step=1).norm_sq
+            assert abs(got - want) <= ATOL + RTOL * abs(want), (got, want)
             seen.append(got)
         finally:
             run.close()
