@@ -7,7 +7,7 @@ on the last microbatch), the global-norm finish (grs_grad_norm_sq) and the
 fused clip + AdamW + bf16 cast (grs_clip_adamw_step).  Inputs are resident
 in HBM and larger than L2 (each rank's gradient buffer alone exceeds it).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload N]
   python bench.py --impl reference ...   (the CPU oracle, timed on host cores)
 
 Multi-GPU runs (torchrun, one rank per GPU) are independent replicas: the
@@ -180,7 +180,8 @@ def bench_workload(args):
     """The workload named on the command line, with --micro overriding its
     number of microbatches (the name then says so)."""
     import dataclasses
-    w = workloads.get(args.workload, args.blocks)
+    cid = args.workload if args.workload is not None else (1 if args.blocks else HEADLINE)
+    w = workloads.get(cid, args.blocks)
     if getattr(args, "micro", 0) and args.micro != w.n_micro:
         w = dataclasses.replace(w, n_micro=args.micro, name=f"{w.name}-{args.micro}mb")
     return w
@@ -363,17 +364,34 @@ class GpuUpdate:
         self.grs.grs_plan_destroy(self.plan)
 
 
-def run_gpu(args, rank, world_size, local_rank):
+# The headline workload when none is named: the largest plan that fits one
+# GPU (Llama-3.2-3B-shaped, 3.2B parameters, 134.9 GB of mandatory traffic
+# per update); the other large plans are measured in the same run and
+# reported beside it.
+HEADLINE = 4
+ALSO_MEASURED = (1, 2, 3)
+# Nominal GB300 HBM3e bandwidth, for the second fraction next to the measured
+# copy peak (the 70% target is judged against the measured peak).
+NOMINAL_HBM_GBS = 7900.0
+
+
+def load_peaks() -> dict:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return {}
+
+
+def measure(u: "GpuUpdate", args, world_size: int, device, gpu_index: int) -> dict:
+    """Time one workload's update: W warm-up steps, a soak, exactly K steps
+    between barriers (max over ranks), then K more steps with CUDA events
+    between the kernels for the per-kernel roofline; SM clocks sampled over
+    both regions."""
     import torch
-    device = torch.device("cuda", local_rank)
-    torch.cuda.set_device(device)
-    w = bench_workload(args)
-    u = GpuUpdate(w, device, args.variant, args.window, args.graph, args.small)
+    w = u.w
     mb = u.algorithmic_bytes()
-    plain = args.variant == "plain" and u.n_micro == w.n_micro and not args.graph and not args.small
-    clocks = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[0])
-                          if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit()
-                          else local_rank)
+    clocks = ClockSampler(gpu_index)
     clocks.start()
     dist = None
     if world_size > 1:
@@ -457,26 +475,9 @@ def run_gpu(args, rank, world_size, local_rank):
     upd_ms = [e[2].elapsed_time(e[3]) for e in ev]
     upd_total = sorted(e[0].elapsed_time(e[3]) for e in ev)
     clk = clocks.stop()
+    del scrub
 
-    # The gather and the end-to-end path run on the plain update only.
-    # ---------------------------------------------------------------- gather
-    gather = run_gather(u, args, torch) if plain else None
-    if gather is not None and flush:
-        gather["l2"] = "parameters fit in L2: back-to-back gathers read them from the cache"
-    accumulate = run_accumulate(u, args, torch) if plain else None
-
-    # ---------------------------------------------------------------- e2e
-    e2e = None if (args.no_e2e or not plain) else run_e2e(u, args, torch)
-
-    status = u.grs.grs_check_device_errors(u.plan, u.stream)
-    u.close()
-
-    peaks = {}
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            peaks = json.load(f)
-    except OSError:
-        pass
+    peaks = load_peaks()
     hbm_peak = peaks.get("hbm_gbs", 6800.0)
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
     M = u.n_micro
@@ -505,39 +506,110 @@ def run_gpu(args, rank, world_size, local_rank):
     if masked:
         kern["update"]["note"] = "per-tensor factors kernel + masked update"
         kern["reduce"]["note"] = "masked reduction (masked norm partials fused into the last microbatch)"
+    step_gbs = mb["total"] / (ms_step * 1e-3) / 1e9
+    return {
+        "ms_per_step": ms_step, "flush": flush, "mb": mb,
+        "achieved_gbs_total": step_gbs,
+        "step_frac": step_gbs / hbm_peak,
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm_peak,
+                     "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": traffic,
+                     "peak_source": peak_src,
+                     "algorithmic_bytes_per_launch": dk["bytes"],
+                     "nominal": {"peak": NOMINAL_HBM_GBS, "frac": achieved / NOMINAL_HBM_GBS,
+                                 "source": "nominal GB300 HBM3e bandwidth (7.9 TB/s)"},
+                     "target_basis": "the 70% target is judged against the measured copy peak (peak)"},
+        "kernels": kern,
+        "per_update_ms": {"median": statistics.median(upd_total), "min": upd_total[0],
+                          "max": upd_total[-1],
+                          "note": "second region, one update per event pair (events between kernels add a few us)"},
+        "clocks": clk,
+    }
+
+
+def gpu_index_of(local_rank: int) -> int:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0]
+    return int(vis) if vis.isdigit() else local_rank
+
+
+def run_gpu(args, rank, world_size, local_rank):
+    import torch
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    gpu_index = gpu_index_of(local_rank)
+    # The other large plans, one after another, each freed before the next
+    # (only when the headline is the default plain update).
+    others = {}
+    if args.workload is None and args.variant == "plain" and not (args.graph or args.small or args.window
+                                                                  or args.micro or args.blocks):
+        for cid in ALSO_MEASURED:
+            wo = workloads.get(cid)
+            uo = GpuUpdate(wo, device)
+            r = measure(uo, args, world_size, device, gpu_index)
+            st = uo.grs.grs_check_device_errors(uo.plan, uo.stream)
+            cfg = arm_config(wo, uo, world_size, r["flush"])
+            uo.close()
+            del uo
+            torch.cuda.empty_cache()
+            others[wo.name] = {
+                "ms_per_update": job_value(r["ms_per_step"], world_size),
+                "ms_per_step": r["ms_per_step"], "mandatory_bytes": r["mb"]["total"],
+                "gbs": r["achieved_gbs_total"], "step_frac": r["step_frac"],
+                "roofline": {k: r["roofline"][k] for k in ("kernel", "achieved", "peak", "frac", "traffic")},
+                "kernels": {k: {"ms_per_launch": v["ms_per_launch"], "launches_per_step": v["launches_per_step"]}
+                            for k, v in r["kernels"].items()},
+                "config": cfg,
+                "clocks": r["clocks"], "device_status": st, "steps": args.steps}
+    w = bench_workload(args)
+    u = GpuUpdate(w, device, args.variant, args.window, args.graph, args.small)
+    plain = args.variant == "plain" and u.n_micro == w.n_micro and not args.graph and not args.small
+    r = measure(u, args, world_size, device, gpu_index)
+    mb, ms_step, flush = r["mb"], r["ms_per_step"], r["flush"]
+    K = args.steps
+
+    # The gather and the end-to-end path run on the plain update only.
+    # ---------------------------------------------------------------- gather
+    gather = run_gather(u, args, torch) if plain else None
+    if gather is not None and flush:
+        gather["l2"] = "parameters fit in L2: back-to-back gathers read them from the cache"
+    accumulate = run_accumulate(u, args, torch) if plain else None
+
+    # ---------------------------------------------------------------- e2e
+    e2e = None if (args.no_e2e or not plain) else run_e2e(u, args, torch)
+
+    status = u.grs.grs_check_device_errors(u.plan, u.stream)
+    u.close()
+
     result = {
         "metric": METRIC, "value": job_value(ms_step, world_size), "unit": UNIT, "n_gpus": world_size,
         "steps": K, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": dict(w.describe(), grad_dtype="fp32" if u.grad_bytes == 4 else "bf16",
-                       l2=("L2 flushed before every step (inputs fit in L2)" if flush
-                           else "inputs larger than L2 (no flush)"),
-                       parallelism=f"replicas{world_size}" if world_size > 1 else "1 GPU, simulated ranks",
-                       **variant_config(u)),
-        "achieved_gbs_total": mb["total"] / (ms_step * world_size * 1e-3) / 1e9 if world_size == 1
+        "config": arm_config(w, u, world_size, flush),
+        "achieved_gbs_total": r["achieved_gbs_total"] if world_size == 1
         else mb["total"] / (ms_step * 1e-3) / 1e9,
-        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm_peak,
-                     "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": traffic,
-                     "peak_source": peak_src,
-                     "algorithmic_bytes_per_launch": dk["bytes"]},
-        "kernels": {k: {kk: vv for kk, vv in v.items()} for k, v in kern.items()},
+        "roofline": r["roofline"],
+        "kernels": r["kernels"],
         "e2e": e2e,
         "gather": gather,
         "accumulate": accumulate,
         "gpu_launches": u.launches_per_step * K,
         "kernel_timing": "second region of K steps with CUDA events between the kernels",
-        "per_update_ms": {"median": statistics.median(upd_total), "min": upd_total[0],
-                          "max": upd_total[-1],
-                          "note": "second region, one update per event pair (events between kernels add a few us)"},
-        "clocks": clk,
+        "per_update_ms": r["per_update_ms"],
+        "clocks": r["clocks"],
         "device_status": status,
     }
+    if others:
+        result["configs"] = others
     if rank == 0 and world_size == 1 and not args.no_cpu_baseline:
         if plain:
             result["cpu_baseline"] = cpu_baseline(w, mb, args, u)
         else:
             result["cpu_baseline"] = cpu_baseline_variant(w, u, mb, args)
     return result
+
+
+def arm_config(w, u, world_size: int, flush: bool) -> dict:
+    """The JSON line's config (workload_config) for the update `u` runs."""
+    return workload_config(w, u.grad_bytes, world_size, flush, variant_config(u))
 
 
 def variant_config(u: GpuUpdate) -> dict:
@@ -566,26 +638,66 @@ def variant_config(u: GpuUpdate) -> dict:
 
 
 def run_gather(u: GpuUpdate, args, torch):
-    """grs_gather_params to per-tensor bf16 storage, timed on its own (not part
-    of the update: parameters can also be used as views of the bucket-ordered
-    buffer).  Algorithmic bytes: read + write 2 bytes per parameter."""
+    """Per-tensor bf16 parameters, two ways, each timed on its own (neither
+    is part of the update: parameters can also be used as views of the
+    bucket-ordered buffer):
+      * grs_gather_params after the update (a separate pass: read + write 2
+        bytes per parameter);
+      * grs_clip_adamw_step_to_tensors, the update writing each bf16 value
+        straight into its tensor (no bucket-ordered copy), against the plain
+        update grs_clip_adamw_step in the same loop: its added time is the
+        cost of per-tensor output when fused."""
     w = u.w
     outs = [torch.empty(n, dtype=torch.int16, device=u.dev) for n in w.numels]
     ptrs = [t.data_ptr() for t in outs]
+    table = torch.tensor(ptrs, dtype=torch.int64, device=u.dev)
+    g = u.grs
     for _ in range(3):
-        u.grs.grs_gather_params(u.plan, u.params.data_ptr(), ptrs, u.stream)
+        g.grs_gather_params(u.plan, u.params.data_ptr(), ptrs, u.stream)
     torch.cuda.synchronize()
-    s = torch.cuda.Event(enable_timing=True)
-    e = torch.cuda.Event(enable_timing=True)
-    s.record()
-    for _ in range(args.steps):
-        u.grs.grs_gather_params(u.plan, u.params.data_ptr(), ptrs, u.stream)
-    e.record()
-    torch.cuda.synchronize()
-    ms = s.elapsed_time(e) / args.steps
+
+    def timed(fn):
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(args.steps):
+            fn()
+        e.record()
+        torch.cuda.synchronize()
+        return s.elapsed_time(e) / args.steps
+
+    ms = timed(lambda: g.grs_gather_params(u.plan, u.params.data_ptr(), ptrs, u.stream))
     nbytes = 4 * w.n_unique
-    del outs
-    return {"ms": ms, "bytes": nbytes, "gbs": nbytes / (ms * 1e-3) / 1e9}
+    a = w.adamw
+    hp = g.make_adamw(a.lr, a.beta1, a.beta2, a.eps, a.weight_decay, a.max_norm, max(1, u.step_no), u.n_micro)
+
+    def plain():
+        g.grs_clip_adamw_step(u.plan, hp, u.norm.data_ptr(), u.acc.data_ptr(), u.master.data_ptr(),
+                              u.m.data_ptr(), u.v.data_ptr(), u.params.data_ptr(), u.stream)
+
+    def fused():
+        g.grs_clip_adamw_step_to_tensors(u.plan, hp, u.norm.data_ptr(), u.acc.data_ptr(), u.master.data_ptr(),
+                                         u.m.data_ptr(), u.v.data_ptr(), None, table.data_ptr(), u.stream)
+
+    for _ in range(3):
+        plain()
+        fused()
+    torch.cuda.synchronize()
+    ms_plain, ms_fused = [], []
+    for _ in range(3):  # interleaved, the best of three loops each
+        ms_plain.append(timed(plain))
+        ms_fused.append(timed(fused))
+    p_ms, f_ms = min(ms_plain), min(ms_fused)
+    upd_bytes = 30 * u.info["n_state_pad"]
+    del outs, table
+    return {"ms": ms, "bytes": nbytes, "gbs": nbytes / (ms * 1e-3) / 1e9,
+            "fused_into_update": {
+                "update_ms": p_ms, "update_to_tensors_ms": f_ms, "added_ms": f_ms - p_ms,
+                "added_frac_of_separate_gather": (f_ms - p_ms) / ms,
+                "update_to_tensors_gbs": upd_bytes / (f_ms * 1e-3) / 1e9,
+                "bytes_per_element": 30,
+                "note": "grs_clip_adamw_step_to_tensors with no bucket-ordered copy, against "
+                        "grs_clip_adamw_step, best of 3 interleaved loops of K calls each"}}
 
 
 def run_accumulate(u: GpuUpdate, args, torch):
@@ -621,20 +733,23 @@ def run_e2e(u: GpuUpdate, args, torch):
     """The same update through the public C ABI with host buffers:
     grs_step_from_host copies every step's gradients from pinned host memory
     (bucket by bucket, overlapped with the reductions), runs the update and
-    reads the step's metric, the squared global norm, back to the host; a
-    second figure also reads the bf16 parameters back every step."""
+    reads the step's results back to the host every step: the bf16
+    parameters and the squared global norm (a second figure reads the norm
+    alone)."""
     w = u.w
     W, M = w.world, w.n_micro
     n = u.info["n_rank_pad"]
-    host = [torch.empty(n, dtype=torch.int16).pin_memory() for _ in range(M * W)]
+    t0 = time.perf_counter()
+    host = [torch.empty(n, dtype=torch.int16, pin_memory=True) for _ in range(M * W)]
     for j in range(M):
         for k in range(W):
             host[j * W + k].copy_(u.grads[j][k].view(torch.int16))
     halves = 2 if M > 1 else 1
     stage = [torch.empty(n, dtype=torch.bfloat16, device=u.dev) for _ in range(halves * W)]
     stage_ptrs = [t.data_ptr() for t in stage] + [stage[0].data_ptr()] * ((2 - halves) * W)
-    out_params = torch.empty(u.params.numel(), dtype=torch.int16).pin_memory()
-    out_norm = torch.empty(1, dtype=torch.float64).pin_memory()
+    out_params = torch.empty(u.params.numel(), dtype=torch.int16, pin_memory=True)
+    out_norm = torch.empty(1, dtype=torch.float64, pin_memory=True)
+    t_setup = time.perf_counter() - t0  # pinned host buffers, filled from the device
     h2d = 0
     for d in u.buckets:  # ALREADY_REDUCED buckets copy rank 0's rows only
         nread = 1 if int(d["tag"]) == 3 else W
@@ -663,17 +778,18 @@ def run_e2e(u: GpuUpdate, args, torch):
         torch.cuda.synchronize()
         return s.elapsed_time(e) / steps
 
-    # The step's result read back every step: its metric (the squared
-    # global norm) — and, as a second figure, the bf16 parameters as well.
-    ms = timed(False)
+    # The step's result read back every step: the updated bf16 parameters
+    # and the squared global norm; as a second figure, the norm alone.
     ms_params = timed(True)
+    ms = timed(False)
     del stage
-    return {"value": ms, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 8,
-            "h2d_gbs": h2d / (ms * 1e-3) / 1e9, "steps": steps,
+    return {"value": ms_params, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "h2d_gbs": h2d / (ms_params * 1e-3) / 1e9, "steps": steps,
+            "setup_s": t_setup,
             "path": "grs_step_from_host: pinned host gradients, per-bucket H2D overlapped with the "
-                    "reductions, the squared global norm read back",
-            "with_params_read_back": {"value": ms_params, "unit": UNIT, "d2h_bytes_per_step": d2h,
-                                      "h2d_gbs": h2d / (ms_params * 1e-3) / 1e9}}
+                    "reductions; the bf16 parameters and the squared global norm read back every step",
+            "norm_read_back_only": {"value": ms, "unit": UNIT, "d2h_bytes_per_step": 8,
+                                    "h2d_gbs": h2d / (ms * 1e-3) / 1e9}}
 
 
 KERNEL_SOURCES = ("kernels_reduce.cu", "kernels_update.cu", "kernels_masked.cu", "kernels_gather.cu",
@@ -769,12 +885,14 @@ def _device_bucket_inputs(op, grads, buckets, M, fp32):
     return out
 
 
-def _oracle_sample(w, op, host, buckets, threads=1, n_micro=0, used=None):
+def _oracle_sample(w, op, host, buckets, threads=1, n_micro=0, used=None, master=None):
     """One oracle update restricted to `buckets` (reduce -> norm -> AdamW);
     with threads > 1 the buckets run in parallel (the oracle's C code drops
     the GIL) and the norm is still summed in bucket order.  With `used` (one
     flag per tensor) tensors without a gradient add nothing to the norm and
-    are not updated."""
+    are not updated.  `master` (dict bucket -> fp32 [copies * P], or None for
+    zeros) is the state the step starts from; the first and second moments
+    start at zero (the first step), each in an array of its own."""
     import oracle
     from concurrent.futures import ThreadPoolExecutor
     a_ = w.adamw
@@ -804,17 +922,21 @@ def _oracle_sample(w, op, host, buckets, threads=1, n_micro=0, used=None):
             ns += oracle.norm_sq(a[t][lo:hi], M)
         return a, ns
 
+    def state(b, t, lo, hi):
+        P = int(op.b_padded[b])
+        p0 = (master[b][t * P + lo:t * P + hi] if master is not None
+              else np.zeros(hi - lo, np.float32))
+        return p0, np.zeros(hi - lo, np.float32), np.zeros(hi - lo, np.float32)
+
     def upd(args):
         b, a, c = args
         if used is None:
             P = int(op.b_padded[b])
-            z = np.zeros(P, np.float32)
             for t in range(op.copies(b)):
-                oracle.adamw(a[t], int(op.b_used[b]), M, c, hp, 1, z, z, z)
+                oracle.adamw(a[t], int(op.b_used[b]), M, c, hp, 1, *state(b, t, 0, P))
             return
         for t, lo, hi in rows(b):
-            z = np.zeros(hi - lo, np.float32)
-            oracle.adamw(a[t][lo:hi], hi - lo, M, c, hp, 1, z, z, z)
+            oracle.adamw(a[t][lo:hi], hi - lo, M, c, hp, 1, *state(b, t, lo, hi))
 
     with ThreadPoolExecutor(max(1, threads)) as ex:
         parts = list(ex.map(red, buckets))
@@ -891,56 +1013,123 @@ def cpu_baseline(w, mb, args, u=None, target_s=10.0):
                           "note": f"one whole update, {min(nthr, op.n_buckets)} buckets in parallel"}}
 
 
+def _spread_buckets(op, n):
+    """Up to n buckets for a parallel sample: one per tag first, then the
+    others in plan order."""
+    chosen = _sample_buckets(op, frac_target=0.0)
+    for b in range(op.n_buckets):
+        if len(chosen) >= n:
+            break
+        if b not in chosen:
+            chosen.append(b)
+    return sorted(chosen)
+
+
+def _master_slices(op, master, buckets):
+    """Each sampled bucket's rows of an fp32 state array (torch, any device)
+    as host arrays."""
+    out = {}
+    for b in buckets:
+        o = int(op.b_state_off[b])
+        out[b] = master[o:o + op.copies(b) * int(op.b_padded[b])].cpu().numpy()
+    return out
+
+
 def cpu_baseline_variant(w, u, mb, args, target_s=10.0):
     """The oracle on the update `u` runs (its plan flags, gradient type,
     microbatch window and mask), one thread: whole updates when the update
     moves at most 8 GB, otherwise one bucket per tag scaled to the whole
-    update by mandatory bytes.  Inputs: the GPU arm's own gradient bytes,
-    copied to the host once before the timing."""
+    update by mandatory bytes; then one thread per core over as many
+    buckets, also scaled.  Inputs: the GPU arm's own gradient bytes and
+    master state, copied to the host once before the timing."""
     op = _oracle_plan(w, u.tensor_flags)
     M = u.n_micro
+    nthr = os.cpu_count() or 1
     whole = mb["total"] <= 8e9
     buckets = list(range(op.n_buckets)) if whole else _sample_buckets(op, frac_target=0.0)
-    host = _device_bucket_inputs(op, u.grads, buckets, M, u.grad_bytes == 4)
+    par = buckets if whole else _spread_buckets(op, nthr)
+    host = _device_bucket_inputs(op, u.grads, par, M, u.grad_bytes == 4)
+    master = _master_slices(op, u.master, par)
     used = u.used_list if u.used is not None else None
     reps, t0 = 0, time.perf_counter()
     while True:
-        _oracle_sample(w, op, host, buckets, n_micro=M, used=used)
+        _oracle_sample(w, op, host, buckets, n_micro=M, used=used, master=master)
         reps += 1
         dt = time.perf_counter() - t0
         if dt >= target_s or reps >= 20:
             break
     scale = 1.0 if whole else mb["total"] / _sample_bytes(op, buckets, M, u.grad_bytes)
     ms = dt * 1e3 / reps * scale
-    what = (f"{reps} whole updates of the variant" if whole else
-            f"{reps} updates of buckets {buckets} of {op.n_buckets}, scaled by bytes")
+    t1 = time.perf_counter()
+    _oracle_sample(w, op, host, par, threads=nthr, n_micro=M, used=used, master=master)
+    dtn = time.perf_counter() - t1
+    scale_n = 1.0 if whole else mb["total"] / _sample_bytes(op, par, M, u.grad_bytes)
+    msn = dtn * 1e3 * scale_n
+    what = (f"{reps} whole updates" if whole else
+            f"{reps} updates of buckets {buckets} of {op.n_buckets}, scaled by mandatory bytes")
     return {"value": ms, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{what}, one thread, {dt:.1f} s", "gbs": mb["total"] / (ms * 1e-3) / 1e9}
+            "sample": f"{what}, one thread, {dt:.1f} s", "gbs": mb["total"] / (ms * 1e-3) / 1e9,
+            "all_cores": {"value": msn, "cores": nthr, "gbs": mb["total"] / (msn * 1e-3) / 1e9,
+                          "note": (f"one whole update, {min(nthr, len(par))} buckets in parallel" if whole else
+                                   f"one update of {len(par)} buckets in parallel, scaled by mandatory bytes")}}
+
+
+def workload_config(w, grad_bytes: int, world_size: int, flush: bool, extra=None) -> dict:
+    """The JSON line's config, the same for both arms: the workload's
+    geometry, gradient type, L2 handling of the GPU timing, parallelism and
+    a variant's keys."""
+    return dict(w.describe(), grad_dtype="fp32" if grad_bytes == 4 else "bf16",
+                l2=("L2 flushed before every step (inputs fit in L2)" if flush
+                    else "inputs larger than L2 (no flush)"),
+                parallelism=f"replicas{world_size}" if world_size > 1 else "1 GPU, simulated ranks",
+                **(extra or {}))
 
 
 def run_reference(args, rank, world_size):
-    """The oracle as the reference arm, on host cores, rank 0 only."""
+    """The oracle as the reference arm, on the host cores, rank 0 only, on
+    the GPU arm's workload.  One thread per core, buckets in parallel.  A
+    step is one whole oracle update when the update moves at most 5 GB of
+    mandatory bytes; otherwise a bounded sample of as many buckets as there
+    are cores, and the metric (ms per whole update) is the sample's time
+    scaled by mandatory bytes.  ms_per_step is the measured time of one
+    step as run."""
+    import torch
     w = bench_workload(args)
     op = _oracle_plan(w)
     mb = mandatory_bytes(oracle_buckets(op), w.n_micro)
-    buckets = _sample_buckets(op, frac_target=0.0)  # one bucket per tag: a bounded step
-    host = _sampled_host_inputs(w, op, buckets)
+    nthr = os.cpu_count() or 1
+    whole = mb["total"] <= 5e9
+    buckets = list(range(op.n_buckets)) if whole else _spread_buckets(op, nthr)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    host = _sampled_host_inputs(w, op, buckets, device=dev)
+    master_full = workloads.normal_f32(op.n_state_pad, w.master_std, workloads.master_seed(w.cid), device=dev)
+    master = _master_slices(op, master_full, buckets)
+    del master_full
     sb = _sample_bytes(op, buckets, w.n_micro)
     for _ in range(args.warmup):
-        _oracle_sample(w, op, host, buckets)
+        _oracle_sample(w, op, host, buckets, threads=nthr, master=master)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        _oracle_sample(w, op, host, buckets)
+        _oracle_sample(w, op, host, buckets, threads=nthr, master=master)
     dt = (time.perf_counter() - t0) / args.steps
-    ms = dt * 1e3 * mb["total"] / sb
-    sample = (f"each step: oracle update of buckets {buckets} of {op.n_buckets} "
-              f"({sb / 1e9:.2f} of {mb['total'] / 1e9:.2f} GB), one thread, scaled by bytes")
+    ms_step = dt * 1e3
+    ms = ms_step * mb["total"] / sb
+    l2 = 129 << 20
+    flush = w.n_micro * w.world * op.n_rank_pad * 2 <= l2
+    if whole:
+        sample = (f"each step: one whole oracle update ({op.n_buckets} buckets, {mb['total'] / 1e9:.2f} GB "
+                  f"mandatory bytes), {nthr} threads")
+    else:
+        sample = (f"each step: oracle update of {len(buckets)} of {op.n_buckets} buckets "
+                  f"({sb / 1e9:.2f} of {mb['total'] / 1e9:.2f} GB mandatory bytes), {nthr} threads; "
+                  f"value = step time x {mb['total'] / sb:.2f} (bytes of the whole update / bytes of the sample)")
     return {"metric": METRIC, "value": ms, "unit": UNIT, "n_gpus": world_size, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False, "scaling": "weak",
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": False, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": dict(w.describe(), l2="host memory"),
-            "cpu_baseline": {"value": ms, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": sample},
+            "config": workload_config(w, 2, world_size, flush),
+            "value_basis": "measured whole updates" if whole else "sampled buckets scaled by mandatory bytes",
+            "where": "the oracle (plain C, fp64) on the host cores; inputs in host memory",
+            "cpu_baseline": {"value": ms, "unit": UNIT, "cores": nthr, "kind": "oracle", "sample": sample},
             "e2e": {"value": ms, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -1196,12 +1385,28 @@ def run_overlap(args):
             "device_status": status}
 
 
+def rank_launch_cmd(n_gpus: int, argv, port: int) -> list:
+    """The torchrun command that runs this bench as n_gpus ranks on one node
+    (one process per GPU, rendezvous on 127.0.0.1) with the same arguments."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n_gpus}",
+            "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__), *argv]
+
+
+def _free_port() -> int:
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", type=int, default=1, choices=workloads.ALL_IDS)
+    ap.add_argument("--workload", type=int, default=None, choices=workloads.ALL_IDS,
+                    help="time this workload only (default: the 3.2B plan as the headline, "
+                         "the 67M, 1.1B and MoE plans measured beside it)")
     ap.add_argument("--blocks", type=int, default=0,
                     help="shrink workload 1 to this many blocks (small profiling case)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -1228,8 +1433,16 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.gpus < 1:
+        ap.error("--gpus must be >= 1")
+    if args.workload is None and (args.variant != "plain" or args.graph or args.small or args.micro
+                                  or args.overlap or args.checkpoint):
+        args.workload = 1  # the variant rows and separate measurements are taken on the 67M plan
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1 and args.impl != "reference":
+        # One process per GPU: start the ranks (torchrun) and pass on their status.
+        sys.exit(subprocess.call(rank_launch_cmd(args.gpus, sys.argv[1:], _free_port())))
     rank = int(os.environ.get("RANK", "0"))
-    world_size = int(os.environ.get("WORLD_SIZE", "1"))
+    world_size = int(os.environ.get("WORLD_SIZE", str(args.gpus if args.impl == "reference" else 1)))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         if rank != 0:

@@ -73,6 +73,10 @@ void free_device(grs_plan* p) {
   cudaFree(p->d_upd_tile_unit);
   p->d_red_tile_tensor = p->d_upd_tile_tensor = nullptr;
   p->d_red_tile_unit = p->d_upd_tile_unit = nullptr;
+  cudaFree(p->d_state_jobs);
+  cudaFree(p->d_upd_tile_job);
+  p->d_state_jobs = nullptr;
+  p->d_upd_tile_job = nullptr;
   p->d_seg_start = nullptr;
   p->d_seg_tensor = nullptr;
   p->d_bucket_seg0 = nullptr;
@@ -137,6 +141,8 @@ grs_status grs_plan_create_ex(const int64_t* numels, const int32_t* owners, cons
     if (e == cudaSuccess) e = upload(&p->d_upd_tile_tensor, p->upd_tile_tensor);
     if (e == cudaSuccess) e = upload(&p->d_red_tile_unit, p->red_tile_unit);
     if (e == cudaSuccess) e = upload(&p->d_upd_tile_unit, p->upd_tile_unit);
+    if (e == cudaSuccess) e = upload(&p->d_state_jobs, p->state_jobs);
+    if (e == cudaSuccess) e = upload(&p->d_upd_tile_job, p->upd_tile_job);
     if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&p->d_flags), grs::FLAG_COUNT * sizeof(int));
     if (e == cudaSuccess) e = cudaMemsetAsync(p->d_flags, 0, grs::FLAG_COUNT * sizeof(int), nullptr);
     if (e == cudaSuccess) e = cudaStreamSynchronize(nullptr);  // cleared before any launch on any stream
@@ -395,6 +401,31 @@ grs_status grs_clip_adamw_step(const grs_plan* p, const grs_adamw* hp, const dou
   return GRS_OK;
 }
 
+grs_status grs_clip_adamw_step_to_tensors(const grs_plan* p, const grs_adamw* hp, const double* d_norm_sq,
+                                          const float* acc, float* master, float* m, float* v,
+                                          uint16_t* params_bf16, uint16_t* const* d_tensor_ptrs, void* stream) {
+  grs_status st = check_plan_device(p);
+  if (st != GRS_OK) return st;
+  if (hp == nullptr || acc == nullptr || master == nullptr || m == nullptr || v == nullptr ||
+      d_tensor_ptrs == nullptr)
+    return fail(GRS_ERR_INVALID_ARG, "grs_clip_adamw_step_to_tensors: NULL argument");
+  if (hp->step < 1 || hp->n_micro < 1)
+    return fail(GRS_ERR_INVALID_ARG, "grs_clip_adamw_step_to_tensors: step and n_micro must be >= 1");
+  if (hp->max_norm > 0.0f && d_norm_sq == nullptr)
+    return fail(GRS_ERR_INVALID_ARG, "grs_clip_adamw_step_to_tensors: clipping needs d_norm_sq");
+  if (!aligned16(acc) || !aligned16(master) || !aligned16(m) || !aligned16(v) ||
+      (params_bf16 != nullptr && !aligned16(params_bf16)) ||
+      (reinterpret_cast<uintptr_t>(d_tensor_ptrs) & 7u) != 0)
+    return fail(GRS_ERR_ALIGNMENT, "grs_clip_adamw_step_to_tensors: buffer not 16-byte aligned "
+                                   "(or the pointer table not 8-byte aligned)");
+  DeviceGuard g(p->device);
+  if (!g.ok()) return fail(GRS_ERR_CUDA, "grs_clip_adamw_step_to_tensors: cannot select the plan's device");
+  const int e = grs::launch_update_to_tensors(p, hp, d_norm_sq, acc, master, m, v, params_bf16, d_tensor_ptrs,
+                                              stream);
+  if (e != 0) return cuda_fail(static_cast<cudaError_t>(e), "grs_clip_adamw_step_to_tensors");
+  return GRS_OK;
+}
+
 grs_status grs_update_small(const grs_plan* p, const grs_adamw* hp, const void* const* rank_grads, float* acc,
                             float* master, float* m, float* v, uint16_t* params_bf16, double* d_norm_sq,
                             void* stream) {
@@ -557,7 +588,7 @@ grs_status grs_check_device_errors(const grs_plan* p, void* stream) {
     static const char* const kSite[grs::SITE_COUNT] = {
         "?", "reduce_kernel", "norm_pass1_kernel", "update_kernel", "accumulate_kernel", "gather_kernel",
         "state_logical_kernel", "norm_pass1_masked_kernel", "update_masked_kernel",
-        "check_already_reduced_kernel", "small_update_kernel"};
+        "check_already_reduced_kernel", "small_update_kernel", "update_kernel (per-tensor parameters)"};
     const int site = h[grs::FLAG_BOUNDS] > 0 && h[grs::FLAG_BOUNDS] < grs::SITE_COUNT ? h[grs::FLAG_BOUNDS] : 0;
     return fail(GRS_ERR_BOUNDS, std::string("checked build: an index left its buffer in ") + kSite[site]);
   }

@@ -135,6 +135,12 @@ struct grs_plan {
   // prefix).
   std::vector<int32_t> red_tile_unit;    // [n_red_tiles]
   std::vector<int32_t> upd_tile_unit;    // [n_upd_tiles]
+  // The gather jobs sorted by state offset, and per update tile the first
+  // of them ending after the tile's first element ([n_upd_tiles + 1], the
+  // last entry = state_jobs.size()): the fused update + gather's map from a
+  // state element to its tensor.
+  std::vector<grs::GatherJob> state_jobs;
+  std::vector<int32_t> upd_tile_job;
   int64_t n_unique = 0, n_rank_pad = 0, n_state_pad = 0;
   int64_t n_red_tiles = 0, n_upd_tiles = 0, n_gather_chunks = 0;
   int64_t workspace_bytes = 0;
@@ -153,6 +159,8 @@ struct grs_plan {
   int32_t* d_upd_tile_tensor = nullptr;
   int32_t* d_red_tile_unit = nullptr;
   int32_t* d_upd_tile_unit = nullptr;
+  grs::GatherJob* d_state_jobs = nullptr;
+  int32_t* d_upd_tile_job = nullptr;
   int* d_flags = nullptr;  // [4]: timeout, nonfinite, reserved
   void* host_step_resources = nullptr;  // copy stream + events of grs_step_from_host
 };
@@ -191,7 +199,8 @@ enum : int {
   SITE_UPDATE_MASKED = 8,
   SITE_AR_CHECK = 9,
   SITE_SMALL = 10,
-  SITE_COUNT = 11
+  SITE_UPDATE_TENSORS = 11,
+  SITE_COUNT = 12
 };
 
 // Programmatic dependent launch between the path's kernels: measured on
@@ -249,6 +258,12 @@ AdamwK adamw_consts(const grs_adamw* hp);
 void bias_factors(const grs_adamw* hp, int32_t step, float* step_size, float* inv_bc2_sqrt);
 int launch_update(const grs_plan* p, const grs_adamw* hp, const double* d_norm_sq, const float* acc,
                   float* master, float* m, float* v, uint16_t* params, void* stream);
+// The update with the bf16 parameters also written to per-tensor storage:
+// params (bucket-ordered, may be null) and d_tensor_ptrs (device array of
+// one device pointer per tensor, null entries skipped).
+int launch_update_to_tensors(const grs_plan* p, const grs_adamw* hp, const double* d_norm_sq, const float* acc,
+                             float* master, float* m, float* v, uint16_t* params,
+                             uint16_t* const* d_tensor_ptrs, void* stream);
 int launch_accumulate(const grs_plan* p, int32_t bucket, float* acc, const float* mb, void* stream);
 int launch_update_small(const grs_plan* p, const grs_adamw* hp, const void* const* rank_grads, float* acc,
                         float* master, float* m, float* v, uint16_t* params, double* d_norm_sq, void* stream);

@@ -10,9 +10,10 @@
 // Update: AdamW with decoupled weight decay (Loshchilov & Hutter, in the
 // form torch.optim.AdamW documents it) on the clipped, microbatch-averaged
 // gradient, fp32 state, bf16 round-to-nearest-even output in the
-// bucket-ordered full-parameter layout.  Each thread streams 8 elements:
-// 2 x 16 B of every fp32 array in, 2 x 16 B of each state array and 16 B of
-// bf16 out (30 bytes per element, the kernel's whole traffic).
+// bucket-ordered full-parameter layout and/or (the gather fused in) straight
+// into each tensor's own storage.  Each thread streams 8 elements: 2 x 16 B
+// of every fp32 array in, 2 x 16 B of each state array and 16 B of bf16 out
+// (30 bytes per element, the kernel's whole traffic).
 #include <cuda_bf16.h>
 #include <cmath>
 #include <cuda_runtime.h>
@@ -132,6 +133,13 @@ struct UpdateArgs {
   int* flags;
   int64_t n_state;   // elements of acc, master, m, v and params
   int32_t n_units;
+  // Per-tensor bf16 output (the fused update + gather only): the device
+  // table of tensor pointers, the gather jobs in state order and each update
+  // tile's first job.
+  uint16_t* const* tensor_ptrs;
+  const GatherJob* sjobs;
+  const int32_t* tile_job;  // [tiles + 1]
+  int32_t n_sjobs;
   AdamwK k;
   float step_size;   // lr / (1 - beta1^t)
   float inv_bc2_sqrt;// 1 / sqrt(1 - beta2^t)
@@ -144,10 +152,41 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// The last state-ordered job in [lo, hi) that starts at or before state
+// element e (lo itself when none does); lo < hi.
+__device__ __forceinline__ int32_t find_job(const UpdateArgs& a, int32_t lo, int32_t hi, int64_t e) {
+  while (hi - lo > 1) {
+    const int32_t mid = lo + ((hi - lo) >> 1);
+    if (a.sjobs[mid].src <= e) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// Stores one element's bf16 bits into its tensor, if a job covers state
+// element e (padding belongs to none) and its tensor has a destination.
+__device__ __forceinline__ void store_to_tensor(const UpdateArgs& a, int32_t lo, int32_t hi, int64_t e,
+                                                uint16_t bits) {
+  const GatherJob jb = a.sjobs[find_job(a, lo, hi, e)];
+  if (jb.src > e || e >= jb.src + jb.len) return;
+  uint16_t* d = a.tensor_ptrs[jb.tensor];
+  if (d != nullptr) d[jb.dst + (e - jb.src)] = bits;
+}
+
+// kTensors: the bf16 parameters also go straight to per-tensor storage (the
+// gather fused into the update); the bucket-ordered copy is then optional.
+template <bool kTensors>
 __global__ void __launch_bounds__(UPD_THREADS) update_kernel(const __grid_constant__ UpdateArgs a) {
   // Tiles run in reverse order: the reduction wrote its last tiles last, so
   // their accumulator values are the ones still in L2.
   const unsigned tile = GRS_UPD_REVERSE ? gridDim.x - 1u - blockIdx.x : blockIdx.x;
+  // Per-tensor output: the range of state-ordered jobs that can overlap
+  // this tile, read from the plan's tables before the wait.
+  int32_t j_lo = 0, j_hi = 0;
+  if (kTensors) {
+    j_lo = __ldg(a.tile_job + tile);
+    j_hi = __ldg(a.tile_job + tile + 1) + 1;
+    if (j_hi > a.n_sjobs) j_hi = a.n_sjobs;
+  }
   pdl_wait();  // S and acc come from the kernels before
   pdl_trigger();
   // Clip coefficient from the device-resident S, evaluated by every thread.
@@ -190,7 +229,35 @@ __global__ void __launch_bounds__(UPD_THREADS) update_kernel(const __grid_consta
   h.y = pack_bf16x2(P[2], P[3]);
   h.z = pack_bf16x2(P[4], P[5]);
   h.w = pack_bf16x2(P[6], P[7]);
-  __stcs(reinterpret_cast<uint4*>(a.params + i), h);
+  if (!kTensors || a.params != nullptr) __stcs(reinterpret_cast<uint4*>(a.params + i), h);
+  if (kTensors) {
+    if (j_lo >= a.n_sjobs) return;  // past the last tensor: padding only
+    if (!GRS_CHECK(j_lo >= 0 && j_lo < j_hi && j_hi <= a.n_sjobs, a.flags, SITE_UPDATE_TENSORS)) return;
+    // Common case: one job holds all 8 elements (a tile inside one tensor).
+    const GatherJob jb = a.sjobs[find_job(a, j_lo, j_hi, i)];
+    if (jb.src <= i && i + 8 <= jb.src + jb.len) {
+      uint16_t* d = a.tensor_ptrs[jb.tensor];
+      if (d == nullptr) return;
+      d += jb.dst + (i - jb.src);
+      const uintptr_t da = reinterpret_cast<uintptr_t>(d);
+      if ((da & 15u) == 0) {
+        __stcs(reinterpret_cast<uint4*>(d), h);
+      } else if ((da & 3u) == 0) {
+        uint32_t* d4 = reinterpret_cast<uint32_t*>(d);
+        d4[0] = h.x; d4[1] = h.y; d4[2] = h.z; d4[3] = h.w;
+      } else {
+        const uint32_t w[4] = {h.x, h.y, h.z, h.w};
+#pragma unroll
+        for (int q = 0; q < 8; ++q) d[q] = static_cast<uint16_t>(w[q >> 1] >> (16 * (q & 1)));
+      }
+      return;
+    }
+    // Tile spanning several tensors (or reaching the padding): element by element.
+    const uint32_t w[4] = {h.x, h.y, h.z, h.w};
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (el + q < used) store_to_tensor(a, j_lo, j_hi, i + q, static_cast<uint16_t>(w[q >> 1] >> (16 * (q & 1))));
+  }
 }
 
 // ----------------------------------------------------------------- accumulate
@@ -281,10 +348,11 @@ void bias_factors(const grs_adamw* hp, int32_t step, float* step_size, float* in
   *inv_bc2_sqrt = static_cast<float>(1.0 / std::sqrt(bc2));
 }
 
-int launch_update(const grs_plan* p, const grs_adamw* hp, const double* d_norm_sq, const float* acc,
-                  float* master, float* m, float* v, uint16_t* params, void* stream) {
-  if (p->n_upd_tiles <= 0) return 0;
-  UpdateArgs a;
+namespace {
+
+UpdateArgs update_args(const grs_plan* p, const grs_adamw* hp, const double* d_norm_sq, const float* acc,
+                       float* master, float* m, float* v, uint16_t* params) {
+  UpdateArgs a{};
   a.acc = acc;
   a.master = master;
   a.m = m;
@@ -300,7 +368,30 @@ int launch_update(const grs_plan* p, const grs_adamw* hp, const double* d_norm_s
   bias_factors(hp, hp->step, &a.step_size, &a.inv_bc2_sqrt);
   a.max_norm = hp->max_norm > 0.0f ? hp->max_norm : 0.0f;
   a.inv_m = static_cast<float>(1.0 / static_cast<double>(hp->n_micro));
-  return static_cast<int>(launch_k(update_kernel, dim3(unsigned(p->n_upd_tiles)), dim3(UPD_THREADS), 0, stream, a));
+  return a;
+}
+
+}  // namespace
+
+int launch_update(const grs_plan* p, const grs_adamw* hp, const double* d_norm_sq, const float* acc,
+                  float* master, float* m, float* v, uint16_t* params, void* stream) {
+  if (p->n_upd_tiles <= 0) return 0;
+  const UpdateArgs a = update_args(p, hp, d_norm_sq, acc, master, m, v, params);
+  return static_cast<int>(
+      launch_k(update_kernel<false>, dim3(unsigned(p->n_upd_tiles)), dim3(UPD_THREADS), 0, stream, a));
+}
+
+int launch_update_to_tensors(const grs_plan* p, const grs_adamw* hp, const double* d_norm_sq, const float* acc,
+                             float* master, float* m, float* v, uint16_t* params,
+                             uint16_t* const* d_tensor_ptrs, void* stream) {
+  if (p->n_upd_tiles <= 0) return 0;
+  UpdateArgs a = update_args(p, hp, d_norm_sq, acc, master, m, v, params);
+  a.tensor_ptrs = d_tensor_ptrs;
+  a.sjobs = p->d_state_jobs;
+  a.tile_job = p->d_upd_tile_job;
+  a.n_sjobs = static_cast<int32_t>(p->state_jobs.size());
+  return static_cast<int>(
+      launch_k(update_kernel<true>, dim3(unsigned(p->n_upd_tiles)), dim3(UPD_THREADS), 0, stream, a));
 }
 
 int launch_accumulate(const grs_plan* p, int32_t bucket, float* acc, const float* mb, void* stream) {

@@ -268,6 +268,27 @@ grs_status build_plan(const int64_t* numels, const int32_t* owners, const uint32
     p->upd_tile_unit.insert(p->upd_tile_unit.end(), static_cast<size_t>(p->upd_prefix[ui + 1] - p->upd_prefix[ui]),
                             static_cast<int32_t>(ui));
   }
+  // The gather jobs in state order (they never overlap: each covers one
+  // tensor's part of one bucket row) and, per update tile, the first of
+  // them that ends after the tile's first element: the update kernel that
+  // writes the bf16 parameters straight into per-tensor storage finds the
+  // destination of its elements from there.
+  p->state_jobs = p->jobs;
+  std::sort(p->state_jobs.begin(), p->state_jobs.end(),
+            [](const GatherJob& a, const GatherJob& b) { return a.src < b.src; });
+  p->upd_tile_job.clear();
+  {
+    size_t j = 0;
+    for (size_t ui = 0; ui < p->units.size(); ++ui) {
+      const UnitDesc& u = p->units[ui];
+      for (int64_t t = p->upd_prefix[ui]; t < p->upd_prefix[ui + 1]; ++t) {
+        const int64_t first = u.state_off + (t - p->upd_prefix[ui]) * UPD_T;
+        while (j < p->state_jobs.size() && p->state_jobs[j].src + p->state_jobs[j].len <= first) ++j;
+        p->upd_tile_job.push_back(static_cast<int32_t>(j));
+      }
+    }
+    p->upd_tile_job.push_back(static_cast<int32_t>(p->state_jobs.size()));  // sentinel
+  }
   p->workspace_bytes = ws_factors_offset(red_tiles) + (static_cast<int64_t>(n) * 8 + 255) / 256 * 256;
   return GRS_OK;
 }

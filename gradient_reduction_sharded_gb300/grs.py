@@ -116,6 +116,8 @@ _sig = {
     "grs_grad_norm_sq": ([_vp, _vp, ctypes.c_int32, _vp, ctypes.c_int32, _vp, _vp], ctypes.c_int),
     "grs_clip_adamw_step": ([_vp, _P(grs_adamw), _vp, _vp, _vp, _vp, _vp, _vp, _vp], ctypes.c_int),
     "grs_gather_params": ([_vp, _vp, _P(_vp), _vp], ctypes.c_int),
+    "grs_clip_adamw_step_to_tensors": ([_vp, _P(grs_adamw), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
+                                       ctypes.c_int),
     "grs_grad_norm_sq_masked": ([_vp, _vp, ctypes.c_int32, _vp, _vp, _vp, _vp], ctypes.c_int),
     "grs_clip_adamw_step_masked": ([_vp, _P(grs_adamw), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                     _vp], ctypes.c_int),
@@ -269,6 +271,17 @@ def grs_clip_adamw_step(plan: int, hp: grs_adamw, d_norm_sq: Optional[int], acc:
                         m: int, v: int, params_bf16: int, stream: int) -> None:
     _check(_lib.grs_clip_adamw_step(plan, ctypes.byref(hp), d_norm_sq, acc, master, m, v,
                                     params_bf16, stream), "grs_clip_adamw_step")
+
+
+def grs_clip_adamw_step_to_tensors(plan: int, hp: grs_adamw, d_norm_sq: Optional[int], acc: int,
+                                   master: int, m: int, v: int, params_bf16: Optional[int],
+                                   d_tensor_ptrs: int, stream: int) -> None:
+    """d_tensor_ptrs: device address of an int64 array of per-tensor device
+    pointers (0 = skip), e.g. ``torch.tensor(ptrs, dtype=torch.int64,
+    device=...).data_ptr()``."""
+    _check(_lib.grs_clip_adamw_step_to_tensors(plan, ctypes.byref(hp), d_norm_sq, acc, master, m, v,
+                                               params_bf16, d_tensor_ptrs, stream),
+           "grs_clip_adamw_step_to_tensors")
 
 
 def grs_gather_params(plan: int, params_bf16: int, tensor_ptrs: Sequence[Optional[int]],

@@ -348,6 +348,29 @@ grs_status grs_clip_adamw_step(const grs_plan* plan, const grs_adamw* hp, const 
                                const float* acc, float* master, float* m, float* v,
                                uint16_t* params_bf16, void* stream);
 
+/* grs_clip_adamw_step with the gather fused in: the same update, and every
+ * bf16 parameter written straight into its own tensor's storage, as
+ * grs_gather_params would copy it there from the bucket-ordered buffer
+ * ([COSMOS] section 2: the parameters all-gathered across shards for the
+ * forward; LOCAL_SHARD tensors reassembled from their tp rows in dim-0
+ * order).  One pass instead of two: the bucket-ordered copy need not exist.
+ *   params_bf16   : device bf16 bits [n_state_pad] also written in the
+ *                   bucket-ordered layout, or NULL (per-tensor output only).
+ *   d_tensor_ptrs : DEVICE array [n_tensors] of device pointers (8-byte
+ *                   aligned), entry i pointing at tensor i's numel bf16
+ *                   elements (any 2-byte alignment; 16-byte-aligned
+ *                   destinations are written with 16-byte stores); NULL
+ *                   entries and frozen tensors are skipped.  The kernel reads
+ *                   the table, so it must stay valid until the launch has run.
+ * The other arguments, the results in master, m, v (and params_bf16) and
+ * the errors are those of grs_clip_adamw_step; ALIGNMENT also when the
+ * table is not 8-byte aligned.  The tensors must not overlap each other or
+ * the state. */
+grs_status grs_clip_adamw_step_to_tensors(const grs_plan* plan, const grs_adamw* hp, const double* d_norm_sq,
+                                          const float* acc, float* master, float* m, float* v,
+                                          uint16_t* params_bf16, uint16_t* const* d_tensor_ptrs,
+                                          void* stream);
+
 /* Tensors without a gradient this step (PyTorch's grad None; [ISSUE]
  * "Proposed scope": unused parameters).  d_tensor_used: device uint8
  * [n_tensors], 1 = the tensor's rank-buffer region holds this step's

@@ -37,3 +37,15 @@ def test_max_over_ranks_and_job_value():
     assert out[0] == out[1] == 2.5
     assert bench.job_value(2.5, 2) == 1.25
     assert bench.max_over_ranks(3.0) == 3.0  # no process group: identity
+
+
+def test_gpus_flag_launches_one_rank_per_gpu():
+    """bench.py --gpus N outside torchrun re-launches itself as N ranks on
+    one node, rendezvous on 127.0.0.1, with the same arguments."""
+    import bench
+    cmd = bench.rank_launch_cmd(4, ["--gpus", "4", "--steps", "7"], 29555)
+    assert cmd[1:3] == ["-m", "torch.distributed.run"]
+    assert "--nproc-per-node=4" in cmd and "--nnodes=1" in cmd
+    i = cmd.index("--master-addr")
+    assert cmd[i + 1] == "127.0.0.1" and cmd[cmd.index("--master-port") + 1] == "29555"
+    assert cmd[-4:] == ["--gpus", "4", "--steps", "7"] and cmd[-5].endswith("bench.py")

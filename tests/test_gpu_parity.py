@@ -287,6 +287,112 @@ def test_gather_matches_oracle():
             run.close()
 
 
+@pytest.mark.parametrize("name", ["tiny-world4", "odd-ds3-M3", "multi-tile-world16-M2", "tp4-world8",
+                                  "many-small-tensors", "zero-size-tensors", "fp32-grads-world8-M3"])
+def test_update_to_tensors_matches_update_then_gather(name):
+    """grs_clip_adamw_step_to_tensors (the gather fused into the update):
+    (1) with the bucket-ordered buffer as well: master, m, v and that buffer
+    equal grs_clip_adamw_step's bit for bit, the whole update matches the
+    oracle, and every tensor equals oracle.gather_tensor of the buffer bit
+    for bit, at 16-byte-aligned and at odd 2-byte offsets; (2) without the
+    buffer (NULL): the same tensors, the buffer untouched; NULL table
+    entries leave their tensors untouched."""
+    g = grs()
+    c = SMALL[name]
+    ref, run, bare = Run(c), Run(c), Run(c)
+    try:
+        master0, m0, v0 = run.state_host()
+        ref.update()
+        n_t = len(c.numels)
+        outs = [torch.full((max(n, 1),), -1, dtype=torch.int16, device="cuda") for n in c.numels]
+        big = torch.full((sum(c.numels) + n_t + 64,), -1, dtype=torch.int16, device="cuda")
+        views, odd_ptrs, off = [], [], 3
+        for n in c.numels:
+            assert off + n <= big.numel()  # every destination inside the buffer
+            views.append(big[off:off + n])
+            odd_ptrs.append(big.data_ptr() + 2 * off)
+            off += n + 1
+        table = torch.tensor([t.data_ptr() for t in outs], dtype=torch.int64, device="cuda")
+        table_odd = torch.tensor(odd_ptrs, dtype=torch.int64, device="cuda")
+        hp = g.make_adamw(c.hp[0], c.hp[1], c.hp[2], c.hp[3], c.hp[4], c.max_norm, 1, c.n_micro)
+        # (1) bucket-ordered buffer and per-tensor storage (aligned, then odd offsets)
+        run.reduce()
+        run.norm_sq()
+        m_save, v_save, p_save = run.m.clone(), run.v.clone(), run.master.clone()
+        g.grs_clip_adamw_step_to_tensors(run.plan, hp, run.norm.data_ptr(), run.acc.data_ptr(),
+                                         run.master.data_ptr(), run.m.data_ptr(), run.v.data_ptr(),
+                                         run.params.data_ptr(), table.data_ptr(), run.stream())
+        torch.cuda.synchronize()
+        for nm in ("acc", "norm", "master", "m", "v", "params"):
+            assert torch.equal(getattr(ref, nm), getattr(run, nm)), nm
+        run.step = 1
+        full_check(run, oracle_update(run, master0, m0, v0, step=1), f"{name} to tensors")
+        params = run.params[:run.nsp].cpu().numpy().view(np.uint16)
+        want = [oracle.gather_tensor(run.op, i, params) for i in range(n_t)]
+        for i, n in enumerate(c.numels):
+            assert np.array_equal(outs[i][:n].cpu().numpy().view(np.uint16), want[i]), (name, i)
+        # the same update again from the saved state, into the odd offsets
+        run.master.copy_(p_save)
+        run.m.copy_(m_save)
+        run.v.copy_(v_save)
+        g.grs_clip_adamw_step_to_tensors(run.plan, hp, run.norm.data_ptr(), run.acc.data_ptr(),
+                                         run.master.data_ptr(), run.m.data_ptr(), run.v.data_ptr(),
+                                         run.params.data_ptr(), table_odd.data_ptr(), run.stream())
+        torch.cuda.synchronize()
+        assert torch.equal(ref.master, run.master) and torch.equal(ref.params, run.params)
+        for i, n in enumerate(c.numels):
+            assert np.array_equal(views[i].cpu().numpy().view(np.uint16), want[i]), (name, i, "odd")
+        # (2) per-tensor storage only; every other table entry NULL
+        bare.reduce()
+        bare.norm_sq()
+        bare.params.fill_(-7)
+        outs2 = [torch.full((max(n, 1),), -1, dtype=torch.int16, device="cuda") for n in c.numels]
+        table2 = torch.tensor([t.data_ptr() if i % 2 == 0 else 0 for i, t in enumerate(outs2)],
+                              dtype=torch.int64, device="cuda")
+        g.grs_clip_adamw_step_to_tensors(bare.plan, hp, bare.norm.data_ptr(), bare.acc.data_ptr(),
+                                         bare.master.data_ptr(), bare.m.data_ptr(), bare.v.data_ptr(),
+                                         None, table2.data_ptr(), bare.stream())
+        torch.cuda.synchronize()
+        assert bare.check_flags() == 0
+        assert torch.equal(ref.master, bare.master) and torch.equal(ref.v, bare.v)
+        assert bool((bare.params == -7).all())
+        for i, n in enumerate(c.numels):
+            got = outs2[i][:n].cpu().numpy().view(np.uint16)
+            if i % 2 == 0:
+                assert np.array_equal(got, want[i]), (name, i, "no bucket buffer")
+            else:
+                assert np.all(got == 0xFFFF), (name, i, "NULL entry written")
+    finally:
+        ref.close()
+        run.close()
+        bare.close()
+
+
+def test_update_to_tensors_argument_errors():
+    g = grs()
+    run = Run(SMALL["odd-ds2"])
+    try:
+        c = run.c
+        hp = g.make_adamw(c.hp[0], c.hp[1], c.hp[2], c.hp[3], c.hp[4], c.max_norm, 1, c.n_micro)
+        table = torch.zeros(len(c.numels) + 1, dtype=torch.int64, device="cuda")
+        args = [run.plan, hp, run.norm.data_ptr(), run.acc.data_ptr(), run.master.data_ptr(),
+                run.m.data_ptr(), run.v.data_ptr(), run.params.data_ptr(), table.data_ptr(), run.stream()]
+        for k, bad, status in ((8, 0, g.GRS_ERR_INVALID_ARG), (8, table.data_ptr() + 4, g.GRS_ERR_ALIGNMENT),
+                               (7, run.params.data_ptr() + 2, g.GRS_ERR_ALIGNMENT),
+                               (3, run.acc.data_ptr() + 4, g.GRS_ERR_ALIGNMENT)):
+            a = list(args)
+            a[k] = bad
+            with pytest.raises(g.GrsError) as ei:
+                g.grs_clip_adamw_step_to_tensors(*a)
+            assert ei.value.status == status, (k, ei.value)
+        hp0 = g.make_adamw(c.hp[0], c.hp[1], c.hp[2], c.hp[3], c.hp[4], c.max_norm, 0, c.n_micro)
+        with pytest.raises(g.GrsError) as ei:
+            g.grs_clip_adamw_step_to_tensors(run.plan, hp0, *args[2:])
+        assert ei.value.status == g.GRS_ERR_INVALID_ARG
+    finally:
+        run.close()
+
+
 def test_accumulate_entry_point():
     c = SMALL["odd-ds3-M3"]
     run = Run(c)
