@@ -181,7 +181,7 @@ def bench_workload(args):
     number of microbatches (the name then says so)."""
     import dataclasses
     cid = args.workload if args.workload is not None else (1 if args.blocks else HEADLINE)
-    w = workloads.get(cid, args.blocks)
+    w = workloads.get(cid, args.blocks, getattr(args, "layers", 0))
     if getattr(args, "micro", 0) and args.micro != w.n_micro:
         w = dataclasses.replace(w, n_micro=args.micro, name=f"{w.name}-{args.micro}mb")
     return w
@@ -540,7 +540,7 @@ def run_gpu(args, rank, world_size, local_rank):
     # (only when the headline is the default plain update).
     others = {}
     if args.workload is None and args.variant == "plain" and not (args.graph or args.small or args.window
-                                                                  or args.micro or args.blocks):
+                                                                  or args.micro or args.blocks or args.layers):
         for cid in ALSO_MEASURED:
             wo = workloads.get(cid)
             uo = GpuUpdate(wo, device)
@@ -1409,6 +1409,9 @@ def main():
                          "the 67M, 1.1B and MoE plans measured beside it)")
     ap.add_argument("--blocks", type=int, default=0,
                     help="shrink workload 1 to this many blocks (small profiling case)")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="profiling slice of workload 2, 3 or 4: this many decoder layers, a small "
+                         "vocabulary (and 8 experts for the MoE); same geometry and per-layer shapes")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--overlap", action="store_true",
                     help="measure the reduction overlapped with a simulated backward pass instead")

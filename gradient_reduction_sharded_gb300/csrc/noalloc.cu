@@ -18,7 +18,9 @@
 // or two host threads) race on the array and must be serialised by the
 // caller.  The first call on a device resolves the array's device address
 // (cudaGetSymbolAddress) with that device current; make that first call
-// before any stream capture.
+// before any stream capture.  The address is cached for the process: a
+// cudaDeviceReset unloads the module with the context, after which the
+// cached address is stale (documented as unsupported in grs.h).
 #include <cuda_runtime.h>
 
 #include <mutex>

@@ -268,12 +268,15 @@ grs_status build_plan(const int64_t* numels, const int32_t* owners, const uint32
     p->upd_tile_unit.insert(p->upd_tile_unit.end(), static_cast<size_t>(p->upd_prefix[ui + 1] - p->upd_prefix[ui]),
                             static_cast<int32_t>(ui));
   }
-  // The gather jobs in state order (they never overlap: each covers one
-  // tensor's part of one bucket row) and, per update tile, the first of
-  // them that ends after the tile's first element: the update kernel that
-  // writes the bf16 parameters straight into per-tensor storage finds the
-  // destination of its elements from there.
-  p->state_jobs = p->jobs;
+  // The non-empty gather jobs in state order (they never overlap: each
+  // covers one tensor's part of one bucket row, so their starts differ) and,
+  // per update tile, the first of them that ends after the tile's first
+  // element: the update kernel that writes the bf16 parameters straight into
+  // per-tensor storage finds the destination of its elements from there.
+  // (An empty job would share its start with the next tensor's.)
+  p->state_jobs.clear();
+  for (const GatherJob& j : p->jobs)
+    if (j.len > 0) p->state_jobs.push_back(j);
   std::sort(p->state_jobs.begin(), p->state_jobs.end(),
             [](const GatherJob& a, const GatherJob& b) { return a.src < b.src; });
   p->upd_tile_job.clear();

@@ -503,7 +503,10 @@ grs_status grs_step_from_host(const grs_plan* plan, const grs_adamw* hp,
  * The caller passes the input and the output; nothing is allocated (no
  * cudaMalloc/cudaFree, no allocating library call).  The first call on a
  * device looks up the array's device address with that device current;
- * make that first call before any stream capture.  All calls share the
+ * make that first call before any stream capture.  The address is kept for
+ * the life of the process: after cudaDeviceReset (which unloads the
+ * library's device code with the context) it is stale, so do not call this
+ * entry point again in a process that has reset the device.  All calls share the
  * array and it keeps the last call's contents (its counter is cleared on
  * the stream before each launch); calls that overlap on the GPU — from two
  * streams or two threads — race and must be serialised by the caller.

@@ -163,9 +163,20 @@ def _llama(d, layers, n_heads, n_kv, ffn, vocab, tied, owner=REPLICA_AVG):
 # 32 query heads with 4 KV heads (head_dim 64), untied lm_head: exactly
 # 1,100,048,384 parameters.
 # ---------------------------------------------------------------------------
-def _llama1b() -> Workload:
-    ts = _llama(2048, 22, 32, 4, 5632, 32000, tied=False)
-    return Workload(2, "llama-1.1B-hsdp2x4-8mb", ts, tp=1, dp_replicate=2, dp_shard=4,
+# Profiling slices of workloads 2-4 (`layers` > 0): the same geometry, owner
+# tags and per-layer shapes with `layers` decoder layers, a SLICE_VOCAB-row
+# embedding (and lm_head) and, for the MoE, SLICE_EXPERTS experts: a few GB
+# on the device, inputs still larger than L2, so that ncu captures stay small
+# while every kernel sees the full workload's per-element traffic.
+SLICE_VOCAB = 8192
+SLICE_EXPERTS = 8
+
+
+def _llama1b(layers: int = 0) -> Workload:
+    n, vocab = (layers, SLICE_VOCAB) if layers else (22, 32000)
+    ts = _llama(2048, n, 32, 4, 5632, vocab, tied=False)
+    name = "llama-1.1B-hsdp2x4-8mb" + (f"-slice{layers}L" if layers else "")
+    return Workload(2, name, ts, tp=1, dp_replicate=2, dp_shard=4,
                     n_micro=8, grad_std=1e-3,
                     adamw=AdamW(3e-4, 0.9, 0.999, 1e-8, 0.1, 1.0))
 
@@ -177,10 +188,13 @@ def _llama1b() -> Workload:
 # [32, ., .] tensors per layer (expert-owned LOCAL_SHARD, 16 experts per
 # tp/ep index), router / norms / embeddings REPLICA_AVG.
 # ---------------------------------------------------------------------------
-def _qwen3_moe() -> Workload:
+def _qwen3_moe(layers: int = 0) -> Workload:
     d, hd, nh, ne, fe, vocab = 2048, 128, 16, 32, 768, 151936
+    n_layers = 8
+    if layers:
+        n_layers, ne, vocab = layers, SLICE_EXPERTS, SLICE_VOCAB
     ts = [Tensor("embed", (vocab, d), REPLICA_AVG)]
-    for i in range(8):
+    for i in range(n_layers):
         p = f"layers.{i}."
         ts += [
             Tensor(p + "input_norm", (d,), REPLICA_AVG),
@@ -198,7 +212,8 @@ def _qwen3_moe() -> Workload:
         ]
     ts.append(Tensor("final_norm", (d,), REPLICA_AVG))
     ts.append(Tensor("lm_head", (vocab, d), REPLICA_AVG))
-    return Workload(3, "qwen3-moe-8L-tp2-ds4-4mb", ts, tp=2, dp_replicate=1, dp_shard=4,
+    name = "qwen3-moe-8L-tp2-ds4-4mb" + (f"-slice{layers}L" if layers else "")
+    return Workload(3, name, ts, tp=2, dp_replicate=1, dp_shard=4,
                     n_micro=4, grad_std=1e-3,
                     adamw=AdamW(1e-3, 0.9, 0.999, 1e-8, 0.01, 1.0))
 
@@ -206,18 +221,25 @@ def _qwen3_moe() -> Workload:
 # ---------------------------------------------------------------------------
 # Workload 4: Llama-3.2-3B-shaped decoder, tied embedding, HSDP 2 x 2.
 # ---------------------------------------------------------------------------
-def _llama3b() -> Workload:
-    ts = _llama(3072, 28, 24, 8, 8192, 128256, tied=True)
-    return Workload(4, "llama3.2-3B-hsdp2x2", ts, tp=1, dp_replicate=2, dp_shard=2,
+def _llama3b(layers: int = 0) -> Workload:
+    n, vocab = (layers, SLICE_VOCAB) if layers else (28, 128256)
+    ts = _llama(3072, n, 24, 8, 8192, vocab, tied=True)
+    name = "llama3.2-3B-hsdp2x2" + (f"-slice{layers}L" if layers else "")
+    return Workload(4, name, ts, tp=1, dp_replicate=2, dp_shard=2,
                     n_micro=1, grad_std=1e-3,
                     adamw=AdamW(3e-4, 0.9, 0.999, 1e-8, 0.1, 1.0))
 
 
-def get(cid: int, blocks: int = 0) -> Workload:
+def get(cid: int, blocks: int = 0, layers: int = 0) -> Workload:
     """Workload `cid`.  `blocks` > 0 shrinks workload 1 to that many blocks
-    (same tensor shapes and geometry; used for small profiling cases)."""
+    (same tensor shapes and geometry; used for small profiling cases);
+    `layers` > 0 gives the profiling slice of workload 2, 3 or 4."""
     if cid == 1 and blocks > 0:
         return _synthetic67m(blocks)
+    if layers > 0:
+        if cid not in (2, 3, 4):
+            raise ValueError("profiling slices exist for workloads 2, 3 and 4")
+        return {2: _llama1b, 3: _qwen3_moe, 4: _llama3b}[cid](layers)
     return {0: _tiny, 1: _synthetic67m, 2: _llama1b, 3: _qwen3_moe, 4: _llama3b}[cid]()
 
 
