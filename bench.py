@@ -782,6 +782,25 @@ def run_e2e(u: GpuUpdate, args, torch):
     # and the squared global norm; as a second figure, the norm alone.
     ms_params = timed(True)
     ms = timed(False)
+    # The host link on this machine, for scale: one pinned 1 GiB copy each way.
+    nb = min(n, 1 << 29)
+    hsrc, dbuf = host[0][:nb], stage[0].view(torch.int16)[:nb]
+
+    def copy_ms(fn):
+        fn()
+        torch.cuda.synchronize()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record()
+        for _ in range(3):
+            fn()
+        s1.record()
+        torch.cuda.synchronize()
+        return s0.elapsed_time(s1) / 3
+
+    link = {"h2d_gbs": 2 * nb / (copy_ms(lambda: dbuf.copy_(hsrc, non_blocking=True)) * 1e-3) / 1e9,
+            "d2h_gbs": 2 * nb / (copy_ms(lambda: hsrc.copy_(dbuf, non_blocking=True)) * 1e-3) / 1e9,
+            "bytes": 2 * nb, "note": "one pinned buffer copied each way, cudaMemcpyAsync via torch; "
+                                     "link_bound_ms adds the two directions (no overlap)"}
     del stage
     return {"value": ms_params, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "h2d_gbs": h2d / (ms_params * 1e-3) / 1e9, "steps": steps,
@@ -789,7 +808,10 @@ def run_e2e(u: GpuUpdate, args, torch):
             "path": "grs_step_from_host: pinned host gradients, per-bucket H2D overlapped with the "
                     "reductions; the bf16 parameters and the squared global norm read back every step",
             "norm_read_back_only": {"value": ms, "unit": UNIT, "d2h_bytes_per_step": 8,
-                                    "h2d_gbs": h2d / (ms * 1e-3) / 1e9}}
+                                    "h2d_gbs": h2d / (ms * 1e-3) / 1e9},
+            "link": link,
+            "link_bound_ms": (h2d / link["h2d_gbs"] + (d2h - 8) / link["d2h_gbs"]) / 1e6
+            if link["h2d_gbs"] > 0 and link["d2h_gbs"] > 0 else None}
 
 
 KERNEL_SOURCES = ("kernels_reduce.cu", "kernels_update.cu", "kernels_masked.cu", "kernels_gather.cu",
@@ -949,22 +971,28 @@ def _oracle_sample(w, op, host, buckets, threads=1, n_micro=0, used=None, master
 
 
 def _sample_buckets(op, frac_target=0.35):
-    """Buckets of every tag, smallest-first per tag, until ~frac_target of the
-    state elements are covered (a bounded sample of the same workload)."""
+    """A bounded sample of the same workload: for every tag the bucket
+    closest in size to the median bucket, then buckets in plan order that are
+    at most twice the median (no single outsized bucket, such as one holding
+    a whole embedding, can dominate a sample), until ~frac_target of the
+    state elements are covered."""
     total = op.n_state_pad
+    sizes = [op.copies(b) * int(op.b_padded[b]) for b in range(op.n_buckets)]
+    med = sorted(sizes)[len(sizes) // 2] if sizes else 0
     chosen, acc = [], 0
     by_tag = {}
     for b in range(op.n_buckets):
         by_tag.setdefault(int(op.b_tag[b]), []).append(b)
     for tag, bs in sorted(by_tag.items()):
-        chosen.append(bs[0])
-        acc += op.copies(bs[0]) * int(op.b_padded[bs[0]])
+        b = min(bs, key=lambda x: (abs(sizes[x] - med), x))
+        chosen.append(b)
+        acc += sizes[b]
     for b in range(op.n_buckets):
         if acc >= frac_target * total:
             break
-        if b not in chosen:
+        if b not in chosen and sizes[b] <= 2 * med:
             chosen.append(b)
-            acc += op.copies(b) * int(op.b_padded[b])
+            acc += sizes[b]
     return sorted(chosen)
 
 
@@ -1014,13 +1042,16 @@ def cpu_baseline(w, mb, args, u=None, target_s=10.0):
 
 
 def _spread_buckets(op, n):
-    """Up to n buckets for a parallel sample: one per tag first, then the
-    others in plan order."""
+    """Up to n buckets for a parallel sample: _sample_buckets' one per tag,
+    then others of at most twice the median bucket size in plan order (so
+    that the threads get comparable work)."""
     chosen = _sample_buckets(op, frac_target=0.0)
+    sizes = [op.copies(b) * int(op.b_padded[b]) for b in range(op.n_buckets)]
+    med = sorted(sizes)[len(sizes) // 2] if sizes else 0
     for b in range(op.n_buckets):
         if len(chosen) >= n:
             break
-        if b not in chosen:
+        if b not in chosen and sizes[b] <= 2 * med:
             chosen.append(b)
     return sorted(chosen)
 

@@ -200,6 +200,20 @@ __global__ void __launch_bounds__(UPD_THREADS) update_kernel(const __grid_consta
   const int64_t i = ud->state_off + el;
   const int64_t used = ud->used;
   if (!GRS_CHECK(e0 >= 0 && i >= 0 && i + 8 <= a.n_state, a.flags, SITE_UPDATE)) return;
+  // Per-tensor output: the job of the thread's first element and, when it
+  // holds all 8 (a tile inside one tensor), the destination, looked up now
+  // so that these dependent L2 loads overlap the state loads below.
+  bool whole = false;
+  uint16_t* dst = nullptr;
+  if (kTensors && j_lo < a.n_sjobs &&
+      GRS_CHECK(j_lo >= 0 && j_lo < j_hi && j_hi <= a.n_sjobs, a.flags, SITE_UPDATE_TENSORS)) {
+    const GatherJob jb = a.sjobs[find_job(a, j_lo, j_hi, i)];
+    whole = jb.src <= i && i + 8 <= jb.src + jb.len;
+    if (whole) {
+      dst = a.tensor_ptrs[jb.tensor];
+      if (dst != nullptr) dst += jb.dst + (i - jb.src);
+    }
+  }
 
   const float4 g0 = __ldcs(reinterpret_cast<const float4*>(a.acc + i));
   const float4 g1 = __ldcs(reinterpret_cast<const float4*>(a.acc + i + 4));
@@ -231,24 +245,20 @@ __global__ void __launch_bounds__(UPD_THREADS) update_kernel(const __grid_consta
   h.w = pack_bf16x2(P[6], P[7]);
   if (!kTensors || a.params != nullptr) __stcs(reinterpret_cast<uint4*>(a.params + i), h);
   if (kTensors) {
-    if (j_lo >= a.n_sjobs) return;  // past the last tensor: padding only
-    if (!GRS_CHECK(j_lo >= 0 && j_lo < j_hi && j_hi <= a.n_sjobs, a.flags, SITE_UPDATE_TENSORS)) return;
+    if (j_lo >= a.n_sjobs || j_lo < 0 || j_lo >= j_hi || j_hi > a.n_sjobs) return;  // (checked above)
     // Common case: one job holds all 8 elements (a tile inside one tensor).
-    const GatherJob jb = a.sjobs[find_job(a, j_lo, j_hi, i)];
-    if (jb.src <= i && i + 8 <= jb.src + jb.len) {
-      uint16_t* d = a.tensor_ptrs[jb.tensor];
-      if (d == nullptr) return;
-      d += jb.dst + (i - jb.src);
-      const uintptr_t da = reinterpret_cast<uintptr_t>(d);
+    if (whole) {
+      if (dst == nullptr) return;
+      const uintptr_t da = reinterpret_cast<uintptr_t>(dst);
       if ((da & 15u) == 0) {
-        __stcs(reinterpret_cast<uint4*>(d), h);
+        __stcs(reinterpret_cast<uint4*>(dst), h);
       } else if ((da & 3u) == 0) {
-        uint32_t* d4 = reinterpret_cast<uint32_t*>(d);
+        uint32_t* d4 = reinterpret_cast<uint32_t*>(dst);
         d4[0] = h.x; d4[1] = h.y; d4[2] = h.z; d4[3] = h.w;
       } else {
         const uint32_t w[4] = {h.x, h.y, h.z, h.w};
 #pragma unroll
-        for (int q = 0; q < 8; ++q) d[q] = static_cast<uint16_t>(w[q >> 1] >> (16 * (q & 1)));
+        for (int q = 0; q < 8; ++q) dst[q] = static_cast<uint16_t>(w[q >> 1] >> (16 * (q & 1)));
       }
       return;
     }
