@@ -200,9 +200,18 @@ __global__ void __launch_bounds__(UPD_THREADS) update_kernel(const __grid_consta
   const int64_t i = ud->state_off + el;
   const int64_t used = ud->used;
   if (!GRS_CHECK(e0 >= 0 && i >= 0 && i + 8 <= a.n_state, a.flags, SITE_UPDATE)) return;
+  const float4 g0 = __ldcs(reinterpret_cast<const float4*>(a.acc + i));
+  const float4 g1 = __ldcs(reinterpret_cast<const float4*>(a.acc + i + 4));
+  const float4 p0 = __ldcs(reinterpret_cast<const float4*>(a.master + i));
+  const float4 p1 = __ldcs(reinterpret_cast<const float4*>(a.master + i + 4));
+  const float4 m0 = __ldcs(reinterpret_cast<const float4*>(a.m + i));
+  const float4 m1 = __ldcs(reinterpret_cast<const float4*>(a.m + i + 4));
+  const float4 v0 = __ldcs(reinterpret_cast<const float4*>(a.v + i));
+  const float4 v1 = __ldcs(reinterpret_cast<const float4*>(a.v + i + 4));
   // Per-tensor output: the job of the thread's first element and, when it
-  // holds all 8 (a tile inside one tensor), the destination, looked up now
-  // so that these dependent L2 loads overlap the state loads below.
+  // holds all 8 (a tile inside one tensor), the destination, looked up while
+  // the state loads above are in flight (their DRAM latency hides these
+  // dependent L2 loads).
   bool whole = false;
   uint16_t* dst = nullptr;
   if (kTensors && j_lo < a.n_sjobs &&
@@ -214,15 +223,6 @@ __global__ void __launch_bounds__(UPD_THREADS) update_kernel(const __grid_consta
       if (dst != nullptr) dst += jb.dst + (i - jb.src);
     }
   }
-
-  const float4 g0 = __ldcs(reinterpret_cast<const float4*>(a.acc + i));
-  const float4 g1 = __ldcs(reinterpret_cast<const float4*>(a.acc + i + 4));
-  const float4 p0 = __ldcs(reinterpret_cast<const float4*>(a.master + i));
-  const float4 p1 = __ldcs(reinterpret_cast<const float4*>(a.master + i + 4));
-  const float4 m0 = __ldcs(reinterpret_cast<const float4*>(a.m + i));
-  const float4 m1 = __ldcs(reinterpret_cast<const float4*>(a.m + i + 4));
-  const float4 v0 = __ldcs(reinterpret_cast<const float4*>(a.v + i));
-  const float4 v1 = __ldcs(reinterpret_cast<const float4*>(a.v + i + 4));
   float G[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
   float P[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
   float M[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
