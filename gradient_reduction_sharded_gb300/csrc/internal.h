@@ -141,6 +141,9 @@ struct grs_plan {
   // state element to its tensor.
   std::vector<grs::GatherJob> state_jobs;
   std::vector<int32_t> upd_tile_job;
+  // Per update tile: the offset of its first element inside the tensor that
+  // holds the whole tile (upd_tile_tensor), -1 for the other tiles.
+  std::vector<int64_t> upd_tile_dst;
   int64_t n_unique = 0, n_rank_pad = 0, n_state_pad = 0;
   int64_t n_red_tiles = 0, n_upd_tiles = 0, n_gather_chunks = 0;
   int64_t workspace_bytes = 0;
@@ -161,6 +164,7 @@ struct grs_plan {
   int32_t* d_upd_tile_unit = nullptr;
   grs::GatherJob* d_state_jobs = nullptr;
   int32_t* d_upd_tile_job = nullptr;
+  int64_t* d_upd_tile_dst = nullptr;
   int* d_flags = nullptr;  // [4]: timeout, nonfinite, reserved
   void* host_step_resources = nullptr;  // copy stream + events of grs_step_from_host
 };

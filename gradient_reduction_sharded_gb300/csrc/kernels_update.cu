@@ -138,7 +138,10 @@ struct UpdateArgs {
   // tile's first job.
   uint16_t* const* tensor_ptrs;
   const GatherJob* sjobs;
-  const int32_t* tile_job;  // [tiles + 1]
+  const int32_t* tile_job;     // [tiles + 1]
+  const int32_t* tile_tensor;  // [tiles]: the tensor holding the whole tile, or -1
+  const int64_t* tile_dst;     // [tiles]: its first element's offset in that tensor
+  int32_t n_tensors;
   int32_t n_sjobs;
   AdamwK k;
   float step_size;   // lr / (1 - beta1^t)
@@ -179,13 +182,25 @@ __global__ void __launch_bounds__(UPD_THREADS) update_kernel(const __grid_consta
   // Tiles run in reverse order: the reduction wrote its last tiles last, so
   // their accumulator values are the ones still in L2.
   const unsigned tile = GRS_UPD_REVERSE ? gridDim.x - 1u - blockIdx.x : blockIdx.x;
-  // Per-tensor output: the range of state-ordered jobs that can overlap
-  // this tile, read from the plan's tables before the wait.
-  int32_t j_lo = 0, j_hi = 0;
+  // Per-tensor output, read from the plan's tables (and the caller's pointer
+  // table) before anything else: for a tile inside one tensor its
+  // destination (two per-tile loads, then the tensor's pointer); for a tile
+  // spanning tensors or padding the range of state-ordered jobs it overlaps.
+  int32_t j_lo = 0, j_hi = 0, t_sole = -1;
+  uint16_t* t_dst = nullptr;
   if (kTensors) {
-    j_lo = __ldg(a.tile_job + tile);
-    j_hi = __ldg(a.tile_job + tile + 1) + 1;
-    if (j_hi > a.n_sjobs) j_hi = a.n_sjobs;
+    t_sole = __ldg(a.tile_tensor + tile);
+    const int64_t off = t_sole >= 0 ? __ldg(a.tile_dst + tile) : -1;
+    if (off < 0) t_sole = -1;  // (every sole-tensor tile has an offset; otherwise the job path)
+    if (t_sole >= 0) {
+      if (!GRS_CHECK(t_sole < a.n_tensors, a.flags, SITE_UPDATE_TENSORS)) return;
+      t_dst = a.tensor_ptrs[t_sole];
+      if (t_dst != nullptr) t_dst += off;
+    } else {
+      j_lo = __ldg(a.tile_job + tile);
+      j_hi = __ldg(a.tile_job + tile + 1) + 1;
+      if (j_hi > a.n_sjobs) j_hi = a.n_sjobs;
+    }
   }
   pdl_wait();  // S and acc come from the kernels before
   pdl_trigger();
@@ -208,21 +223,6 @@ __global__ void __launch_bounds__(UPD_THREADS) update_kernel(const __grid_consta
   const float4 m1 = __ldcs(reinterpret_cast<const float4*>(a.m + i + 4));
   const float4 v0 = __ldcs(reinterpret_cast<const float4*>(a.v + i));
   const float4 v1 = __ldcs(reinterpret_cast<const float4*>(a.v + i + 4));
-  // Per-tensor output: the job of the thread's first element and, when it
-  // holds all 8 (a tile inside one tensor), the destination, looked up while
-  // the state loads above are in flight (their DRAM latency hides these
-  // dependent L2 loads).
-  bool whole = false;
-  uint16_t* dst = nullptr;
-  if (kTensors && j_lo < a.n_sjobs &&
-      GRS_CHECK(j_lo >= 0 && j_lo < j_hi && j_hi <= a.n_sjobs, a.flags, SITE_UPDATE_TENSORS)) {
-    const GatherJob jb = a.sjobs[find_job(a, j_lo, j_hi, i)];
-    whole = jb.src <= i && i + 8 <= jb.src + jb.len;
-    if (whole) {
-      dst = a.tensor_ptrs[jb.tensor];
-      if (dst != nullptr) dst += jb.dst + (i - jb.src);
-    }
-  }
   float G[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
   float P[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
   float M[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
@@ -245,10 +245,10 @@ __global__ void __launch_bounds__(UPD_THREADS) update_kernel(const __grid_consta
   h.w = pack_bf16x2(P[6], P[7]);
   if (!kTensors || a.params != nullptr) __stcs(reinterpret_cast<uint4*>(a.params + i), h);
   if (kTensors) {
-    if (j_lo >= a.n_sjobs || j_lo < 0 || j_lo >= j_hi || j_hi > a.n_sjobs) return;  // (checked above)
-    // Common case: one job holds all 8 elements (a tile inside one tensor).
-    if (whole) {
-      if (dst == nullptr) return;
+    // Common case: a tile inside one tensor.
+    if (t_sole >= 0) {
+      if (t_dst == nullptr) return;
+      uint16_t* dst = t_dst + (el - e0);
       const uintptr_t da = reinterpret_cast<uintptr_t>(dst);
       if ((da & 15u) == 0) {
         __stcs(reinterpret_cast<uint4*>(dst), h);
@@ -263,6 +263,8 @@ __global__ void __launch_bounds__(UPD_THREADS) update_kernel(const __grid_consta
       return;
     }
     // Tile spanning several tensors (or reaching the padding): element by element.
+    if (j_lo >= a.n_sjobs) return;  // past the last tensor: padding only
+    if (!GRS_CHECK(j_lo >= 0 && j_lo < j_hi && j_hi <= a.n_sjobs, a.flags, SITE_UPDATE_TENSORS)) return;
     const uint32_t w[4] = {h.x, h.y, h.z, h.w};
 #pragma unroll
     for (int q = 0; q < 8; ++q)
@@ -399,6 +401,9 @@ int launch_update_to_tensors(const grs_plan* p, const grs_adamw* hp, const doubl
   a.tensor_ptrs = d_tensor_ptrs;
   a.sjobs = p->d_state_jobs;
   a.tile_job = p->d_upd_tile_job;
+  a.tile_tensor = p->d_upd_tile_tensor;
+  a.tile_dst = p->d_upd_tile_dst;
+  a.n_tensors = static_cast<int32_t>(p->numel.size());
   a.n_sjobs = static_cast<int32_t>(p->state_jobs.size());
   return static_cast<int>(
       launch_k(update_kernel<true>, dim3(unsigned(p->n_upd_tiles)), dim3(UPD_THREADS), 0, stream, a));
