@@ -75,10 +75,10 @@ void free_device(grs_plan* p) {
   p->d_red_tile_unit = p->d_upd_tile_unit = nullptr;
   cudaFree(p->d_state_jobs);
   cudaFree(p->d_upd_tile_job);
-  cudaFree(p->d_upd_tile_dst);
+  cudaFree(p->d_upd_tile_info);
   p->d_state_jobs = nullptr;
   p->d_upd_tile_job = nullptr;
-  p->d_upd_tile_dst = nullptr;
+  p->d_upd_tile_info = nullptr;
   p->d_seg_start = nullptr;
   p->d_seg_tensor = nullptr;
   p->d_bucket_seg0 = nullptr;
@@ -145,7 +145,7 @@ grs_status grs_plan_create_ex(const int64_t* numels, const int32_t* owners, cons
     if (e == cudaSuccess) e = upload(&p->d_upd_tile_unit, p->upd_tile_unit);
     if (e == cudaSuccess) e = upload(&p->d_state_jobs, p->state_jobs);
     if (e == cudaSuccess) e = upload(&p->d_upd_tile_job, p->upd_tile_job);
-    if (e == cudaSuccess) e = upload(&p->d_upd_tile_dst, p->upd_tile_dst);
+    if (e == cudaSuccess) e = upload(&p->d_upd_tile_info, p->upd_tile_info);
     if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&p->d_flags), grs::FLAG_COUNT * sizeof(int));
     if (e == cudaSuccess) e = cudaMemsetAsync(p->d_flags, 0, grs::FLAG_COUNT * sizeof(int), nullptr);
     if (e == cudaSuccess) e = cudaStreamSynchronize(nullptr);  // cleared before any launch on any stream

@@ -93,6 +93,17 @@ struct GatherJob {
   int32_t tensor;
   int32_t pad_;
 };
+// Per update tile, for the update that writes bf16 parameters straight into
+// per-tensor storage: the tile's unit, the tensor holding the whole tile
+// (-1 when it spans tensors or reaches padding) and the offset of the tile's
+// first element inside that tensor; 16 bytes, read in one load.
+struct alignas(16) UpdTileInfo {
+  int32_t unit;
+  int32_t tensor;
+  int64_t dst;
+};
+static_assert(sizeof(UpdTileInfo) == 16, "UpdTileInfo layout");
+
 // Elements per gather / layout chunk (one block each).
 #ifndef GRS_GATHER_CHUNK
 #define GRS_GATHER_CHUNK 16384
@@ -141,9 +152,7 @@ struct grs_plan {
   // state element to its tensor.
   std::vector<grs::GatherJob> state_jobs;
   std::vector<int32_t> upd_tile_job;
-  // Per update tile: the offset of its first element inside the tensor that
-  // holds the whole tile (upd_tile_tensor), -1 for the other tiles.
-  std::vector<int64_t> upd_tile_dst;
+  std::vector<grs::UpdTileInfo> upd_tile_info;  // [n_upd_tiles]
   int64_t n_unique = 0, n_rank_pad = 0, n_state_pad = 0;
   int64_t n_red_tiles = 0, n_upd_tiles = 0, n_gather_chunks = 0;
   int64_t workspace_bytes = 0;
@@ -164,7 +173,7 @@ struct grs_plan {
   int32_t* d_upd_tile_unit = nullptr;
   grs::GatherJob* d_state_jobs = nullptr;
   int32_t* d_upd_tile_job = nullptr;
-  int64_t* d_upd_tile_dst = nullptr;
+  grs::UpdTileInfo* d_upd_tile_info = nullptr;
   int* d_flags = nullptr;  // [4]: timeout, nonfinite, reserved
   void* host_step_resources = nullptr;  // copy stream + events of grs_step_from_host
 };

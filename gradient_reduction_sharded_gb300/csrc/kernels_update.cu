@@ -139,8 +139,7 @@ struct UpdateArgs {
   uint16_t* const* tensor_ptrs;
   const GatherJob* sjobs;
   const int32_t* tile_job;     // [tiles + 1]
-  const int32_t* tile_tensor;  // [tiles]: the tensor holding the whole tile, or -1
-  const int64_t* tile_dst;     // [tiles]: its first element's offset in that tensor
+  const UpdTileInfo* tile_info;  // [tiles]: unit, sole tensor (or -1), offset in it
   int32_t n_tensors;
   int32_t n_sjobs;
   AdamwK k;
@@ -182,31 +181,30 @@ __global__ void __launch_bounds__(UPD_THREADS) update_kernel(const __grid_consta
   // Tiles run in reverse order: the reduction wrote its last tiles last, so
   // their accumulator values are the ones still in L2.
   const unsigned tile = GRS_UPD_REVERSE ? gridDim.x - 1u - blockIdx.x : blockIdx.x;
-  // Per-tensor output, read from the plan's tables (and the caller's pointer
-  // table) before anything else: for a tile inside one tensor its
-  // destination (two per-tile loads, then the tensor's pointer); for a tile
-  // spanning tensors or padding the range of state-ordered jobs it overlaps.
-  int32_t j_lo = 0, j_hi = 0, t_sole = -1;
+  // Per-tensor output: one 16-byte load gives the tile's unit, the tensor
+  // holding the whole tile and the offset inside it, so that the caller's
+  // pointer table is read in parallel with the unit descriptor (the same
+  // depth of dependent loads as the plain update).  A tile that spans
+  // tensors or reaches padding takes the job search after its stores.
+  int32_t u_info = -1, t_sole = -1;
   uint16_t* t_dst = nullptr;
   if (kTensors) {
-    t_sole = __ldg(a.tile_tensor + tile);
-    const int64_t off = t_sole >= 0 ? __ldg(a.tile_dst + tile) : -1;
-    if (off < 0) t_sole = -1;  // (every sole-tensor tile has an offset; otherwise the job path)
-    if (t_sole >= 0) {
-      if (!GRS_CHECK(t_sole < a.n_tensors, a.flags, SITE_UPDATE_TENSORS)) return;
+    const int4 w = __ldg(reinterpret_cast<const int4*>(a.tile_info + tile));
+    u_info = w.x;
+    const int64_t off = (static_cast<int64_t>(static_cast<uint32_t>(w.w)) << 32) | static_cast<uint32_t>(w.z);
+    t_sole = off >= 0 ? w.y : -1;
+    if (t_sole >= 0 && GRS_CHECK(t_sole < a.n_tensors, a.flags, SITE_UPDATE_TENSORS)) {
       t_dst = a.tensor_ptrs[t_sole];
       if (t_dst != nullptr) t_dst += off;
     } else {
-      j_lo = __ldg(a.tile_job + tile);
-      j_hi = __ldg(a.tile_job + tile + 1) + 1;
-      if (j_hi > a.n_sjobs) j_hi = a.n_sjobs;
+      t_sole = -1;
     }
   }
   pdl_wait();  // S and acc come from the kernels before
   pdl_trigger();
   // Clip coefficient from the device-resident S, evaluated by every thread.
   const float gscale = a.max_norm > 0.0f ? clip_gscale(*a.norm_sq, a.max_norm, a.inv_m) : a.inv_m;
-  const int u = __ldg(a.tile_unit + tile);
+  const int u = kTensors ? u_info : __ldg(a.tile_unit + tile);
   if (!GRS_CHECK(u >= 0 && u < a.n_units, a.flags, SITE_UPDATE)) return;
   const UnitDesc* ud = a.units + u;
   const int64_t e0 = (static_cast<int64_t>(tile) - ud->upd_tile0) * UPD_T;
@@ -263,6 +261,9 @@ __global__ void __launch_bounds__(UPD_THREADS) update_kernel(const __grid_consta
       return;
     }
     // Tile spanning several tensors (or reaching the padding): element by element.
+    const int32_t j_lo = __ldg(a.tile_job + tile);
+    int32_t j_hi = __ldg(a.tile_job + tile + 1) + 1;
+    if (j_hi > a.n_sjobs) j_hi = a.n_sjobs;
     if (j_lo >= a.n_sjobs) return;  // past the last tensor: padding only
     if (!GRS_CHECK(j_lo >= 0 && j_lo < j_hi && j_hi <= a.n_sjobs, a.flags, SITE_UPDATE_TENSORS)) return;
     const uint32_t w[4] = {h.x, h.y, h.z, h.w};
@@ -401,8 +402,7 @@ int launch_update_to_tensors(const grs_plan* p, const grs_adamw* hp, const doubl
   a.tensor_ptrs = d_tensor_ptrs;
   a.sjobs = p->d_state_jobs;
   a.tile_job = p->d_upd_tile_job;
-  a.tile_tensor = p->d_upd_tile_tensor;
-  a.tile_dst = p->d_upd_tile_dst;
+  a.tile_info = p->d_upd_tile_info;
   a.n_tensors = static_cast<int32_t>(p->numel.size());
   a.n_sjobs = static_cast<int32_t>(p->state_jobs.size());
   return static_cast<int>(

@@ -279,11 +279,12 @@ grs_status build_plan(const int64_t* numels, const int32_t* owners, const uint32
     if (j.len > 0) p->state_jobs.push_back(j);
   std::sort(p->state_jobs.begin(), p->state_jobs.end(),
             [](const GatherJob& a, const GatherJob& b) { return a.src < b.src; });
-  // For a tile wholly inside one tensor (upd_tile_tensor >= 0) also the
-  // offset of its first element inside that tensor, so that the kernel
-  // finds the destination from two per-tile loads and the pointer table.
+  // Per tile also its unit, the tensor holding the whole tile and the
+  // offset of its first element inside that tensor (UpdTileInfo), so that
+  // the kernel finds the destination from one per-tile load and the
+  // caller's pointer table.
   p->upd_tile_job.clear();
-  p->upd_tile_dst.clear();
+  p->upd_tile_info.clear();
   {
     size_t j = 0;
     for (size_t ui = 0; ui < p->units.size(); ++ui) {
@@ -294,13 +295,15 @@ grs_status build_plan(const int64_t* numels, const int32_t* owners, const uint32
         p->upd_tile_job.push_back(static_cast<int32_t>(j));
         const int64_t e0 = (t - p->upd_prefix[ui]) * UPD_T;
         const int64_t len = std::min<int64_t>(UPD_T, u.padded - e0);  // the unit's last tile may be short
-        int64_t dst = -1;
+        UpdTileInfo info{static_cast<int32_t>(ui), -1, -1};
         if (p->upd_tile_tensor[t] >= 0 && j < p->state_jobs.size()) {
           const GatherJob& jb = p->state_jobs[j];
-          if (jb.tensor == p->upd_tile_tensor[t] && jb.src <= first && first + len <= jb.src + jb.len)
-            dst = jb.dst + (first - jb.src);
+          if (jb.tensor == p->upd_tile_tensor[t] && jb.src <= first && first + len <= jb.src + jb.len) {
+            info.tensor = jb.tensor;
+            info.dst = jb.dst + (first - jb.src);
+          }
         }
-        p->upd_tile_dst.push_back(dst);
+        p->upd_tile_info.push_back(info);
       }
     }
     p->upd_tile_job.push_back(static_cast<int32_t>(p->state_jobs.size()));  // sentinel
