@@ -44,6 +44,21 @@ namespace grs {
 #define GRS_RED_EVICT_FIRST 0
 #endif
 constexpr int64_t RED_RING_BYTES = int64_t(GRS_RED_RING_KB) * 1024;
+// Plans whose buckets all reduce at most RED_PAIR_MAX_GROUP bf16 rank rows
+// per element (e.g. 4 simulated ranks) run the plain reduction with two CTAs
+// per SM, each with a RED_PAIR_RING_KB ring and tiles sized for it: with so
+// few rows per tile one CTA's consumers cannot keep up with the TMA stream
+// (measured on the 3.2B, world-4 plan: 5.55 against 5.74 ms per launch),
+// while wider groups lose about 1% that way (the 67M world-16 and the 1.1B
+// world-8 plans), so they keep one CTA per SM with the full ring.
+#ifndef GRS_RED_PAIR_RING_KB
+#define GRS_RED_PAIR_RING_KB 100
+#endif
+#ifndef GRS_RED_PAIR_MAX_GROUP
+#define GRS_RED_PAIR_MAX_GROUP 4
+#endif
+constexpr int64_t RED_PAIR_RING_BYTES = int64_t(GRS_RED_PAIR_RING_KB) * 1024;
+constexpr int RED_PAIR_MAX_GROUP = GRS_RED_PAIR_MAX_GROUP;
 constexpr int64_t STAGE_GRAD_BYTES = GRS_STAGE_GRAD_BYTES;
 constexpr int64_t RED_MAX_T = GRS_RED_MAX_T;
 // Consumer warps of the reduction; the norm pass over acc uses the same
@@ -120,6 +135,7 @@ struct grs_plan {
   std::vector<uint8_t> tensor_live;    // 1 unless frozen (has state in the plan)
   int32_t world = 0, tp = 0, dp_replicate = 0, dp_shard = 0, dp = 0;
   int32_t grad_esize = 2;  // bytes per gradient element: 2 (bf16) or 4 (fp32)
+  bool red_pair = false;   // plain reduction with two CTAs per SM (RED_PAIR_*)
   int64_t bucket_bytes = 0;
   // layout
   std::vector<int32_t> t_bucket;
