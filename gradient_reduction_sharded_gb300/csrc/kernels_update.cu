@@ -176,8 +176,13 @@ __device__ __forceinline__ void store_to_tensor(const UpdateArgs& a, int32_t lo,
 
 // kTensors: the bf16 parameters also go straight to per-tensor storage (the
 // gather fused into the update); the bucket-ordered copy is then optional.
+// Four blocks per SM are pinned (at most 64 registers): measured on the 3.2B
+// plan, the per-tensor instance compiled for one block per SM took 70
+// registers (3 blocks per SM) and 14.40 instead of 13.58 ms, and bounds of 5
+// or 6 blocks per SM spill (14.35 and 15.68 ms for the plain update against
+// 13.52).
 template <bool kTensors>
-__global__ void __launch_bounds__(UPD_THREADS) update_kernel(const __grid_constant__ UpdateArgs a) {
+__global__ void __launch_bounds__(UPD_THREADS, 4) update_kernel(const __grid_constant__ UpdateArgs a) {
   // Tiles run in reverse order: the reduction wrote its last tiles last, so
   // their accumulator values are the ones still in L2.
   const unsigned tile = GRS_UPD_REVERSE ? gridDim.x - 1u - blockIdx.x : blockIdx.x;
