@@ -536,29 +536,6 @@ def run_gpu(args, rank, world_size, local_rank):
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
     gpu_index = gpu_index_of(local_rank)
-    # The other large plans, one after another, each freed before the next
-    # (only when the headline is the default plain update).
-    others = {}
-    if args.workload is None and args.variant == "plain" and not (args.graph or args.small or args.window
-                                                                  or args.micro or args.blocks or args.layers):
-        for cid in ALSO_MEASURED:
-            wo = workloads.get(cid)
-            uo = GpuUpdate(wo, device)
-            r = measure(uo, args, world_size, device, gpu_index)
-            st = uo.grs.grs_check_device_errors(uo.plan, uo.stream)
-            cfg = arm_config(wo, uo, world_size, r["flush"])
-            uo.close()
-            del uo
-            torch.cuda.empty_cache()
-            others[wo.name] = {
-                "ms_per_update": job_value(r["ms_per_step"], world_size),
-                "ms_per_step": r["ms_per_step"], "mandatory_bytes": r["mb"]["total"],
-                "gbs": r["achieved_gbs_total"], "step_frac": r["step_frac"],
-                "roofline": {k: r["roofline"][k] for k in ("kernel", "achieved", "peak", "frac", "traffic")},
-                "kernels": {k: {"ms_per_launch": v["ms_per_launch"], "launches_per_step": v["launches_per_step"]}
-                            for k, v in r["kernels"].items()},
-                "config": cfg,
-                "clocks": r["clocks"], "device_status": st, "steps": args.steps}
     w = bench_workload(args)
     u = GpuUpdate(w, device, args.variant, args.window, args.graph, args.small)
     plain = args.variant == "plain" and u.n_micro == w.n_micro and not args.graph and not args.small
@@ -597,13 +574,39 @@ def run_gpu(args, rank, world_size, local_rank):
         "clocks": r["clocks"],
         "device_status": status,
     }
-    if others:
-        result["configs"] = others
     if rank == 0 and world_size == 1 and not args.no_cpu_baseline:
         if plain:
             result["cpu_baseline"] = cpu_baseline(w, mb, args, u)
         else:
             result["cpu_baseline"] = cpu_baseline_variant(w, u, mb, args)
+    del u
+    torch.cuda.empty_cache()
+    # The other large plans, after the headline (which runs first, in a
+    # fresh process), one after another, each freed before the next (only
+    # when the headline is the default plain update).
+    others = {}
+    if args.workload is None and args.variant == "plain" and not (args.graph or args.small or args.window
+                                                                  or args.micro or args.blocks or args.layers):
+        for cid in ALSO_MEASURED:
+            wo = workloads.get(cid)
+            uo = GpuUpdate(wo, device)
+            r = measure(uo, args, world_size, device, gpu_index)
+            st = uo.grs.grs_check_device_errors(uo.plan, uo.stream)
+            cfg = arm_config(wo, uo, world_size, r["flush"])
+            uo.close()
+            del uo
+            torch.cuda.empty_cache()
+            others[wo.name] = {
+                "ms_per_update": job_value(r["ms_per_step"], world_size),
+                "ms_per_step": r["ms_per_step"], "mandatory_bytes": r["mb"]["total"],
+                "gbs": r["achieved_gbs_total"], "step_frac": r["step_frac"],
+                "roofline": {k: r["roofline"][k] for k in ("kernel", "achieved", "peak", "frac", "traffic")},
+                "kernels": {k: {"ms_per_launch": v["ms_per_launch"], "launches_per_step": v["launches_per_step"]}
+                            for k, v in r["kernels"].items()},
+                "config": cfg,
+                "clocks": r["clocks"], "device_status": st, "steps": args.steps}
+    if others:
+        result["configs"] = others
     return result
 
 
