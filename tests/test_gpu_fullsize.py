@@ -133,13 +133,13 @@ def test_single_tensor_beyond_32_bit_indices():
 
 def test_gather_and_layout_beyond_32_bit_indices():
     """The same 2^31 + 4099-element tensor through the gather to per-tensor
-    storage and the state <-> logical conversions: for one tensor on one
-    rank both are the identity on its elements, and the padding comes back
-    as zeros."""
+    storage, the state <-> logical conversions and the update that writes
+    the tensor itself: for one tensor on one rank each is the identity on
+    its elements, and the padding comes back as zeros."""
     from gradient_reduction_sharded_gb300 import grs
     n = 2 ** 31 + 4099
-    if _free_gb() < 4 * n * 2 / 1e9 + 4 * n * 4 / 1e9 + 4:
-        pytest.skip("needs about 52 GB of device memory")
+    if _free_gb() < 3 * n * 2 / 1e9 + 4 * n * 4 / 1e9 + 8:
+        pytest.skip("needs about 56 GB of device memory")
     plan = grs.grs_plan_create([n], [RA], 1, 1, 1, 1, 25 << 20)
     try:
         info = grs.grs_plan_query(plan)
@@ -162,6 +162,24 @@ def test_gather_and_layout_beyond_32_bit_indices():
         assert grs.grs_check_device_errors(plan, s) == 0
         assert torch.equal(logical, state[:n])
         assert torch.equal(back[:n], state[:n]) and bool((back[n:] == 0).all())
+        del logical, back
+        # the update writing the tensor itself: every offset past 2^31 comes
+        # from the per-tile records; the result equals the bucket-ordered
+        # buffer the same update writes (the tensor is the buffer's first n)
+        acc = state
+        master = torch.randn(nsp, device="cuda", generator=gen)
+        m = torch.zeros(nsp, device="cuda")
+        v = torch.zeros(nsp, device="cuda")
+        ref_params = torch.empty(nsp, dtype=torch.int16, device="cuda")
+        out = torch.full((n,), -1, dtype=torch.int16, device="cuda")
+        table = torch.tensor([out.data_ptr()], dtype=torch.int64, device="cuda")
+        hp = grs.make_adamw(1e-3, 0.9, 0.999, 1e-8, 0.01, 0.0, 1, 1)
+        grs.grs_clip_adamw_step_to_tensors(plan, hp, None, acc.data_ptr(), master.data_ptr(), m.data_ptr(),
+                                           v.data_ptr(), ref_params.data_ptr(), table.data_ptr(), s)
+        torch.cuda.synchronize()
+        assert grs.grs_check_device_errors(plan, s) == 0
+        assert torch.equal(out, ref_params[:n])
+        assert bool((ref_params[n:] == 0).all())
     finally:
         grs.grs_plan_destroy(plan)
         torch.cuda.empty_cache()
