@@ -551,7 +551,25 @@ def run_gpu(args, rank, world_size, local_rank):
     accumulate = run_accumulate(u, args, torch) if plain else None
 
     # ---------------------------------------------------------------- e2e
-    e2e = None if (args.no_e2e or not plain) else run_e2e(u, args, torch)
+    e2e = None
+    if not args.no_e2e and plain:
+        need = e2e_host_bytes(u)
+        ranks_here = int(os.environ.get("LOCAL_WORLD_SIZE", str(world_size)))
+        avail = host_available_bytes()
+        if avail is None or need * ranks_here <= 0.6 * avail:
+            e2e = run_e2e(u, args, torch)
+        else:
+            # Every rank on this host would pin its own copy of the gradients:
+            # the 67M plan stands in, and the line says so.
+            w1 = workloads.get(1)
+            u1 = GpuUpdate(w1, device)
+            u1.step()
+            e2e = run_e2e(u1, args, torch)
+            e2e["workload"] = w1.name
+            e2e["why"] = (f"{need * ranks_here / 1e9:.0f} GB of pinned host memory for {ranks_here} ranks of "
+                          f"{w.name} exceeds 60% of the {avail / 1e9:.0f} GB available")
+            u1.close()
+            del u1
 
     status = u.grs.grs_check_device_errors(u.plan, u.stream)
     u.close()
@@ -730,6 +748,24 @@ def run_accumulate(u: GpuUpdate, args, torch):
     nbytes = 12 * nsp
     del mbuf
     return {"ms": ms, "bytes": nbytes, "gbs": nbytes / (ms * 1e-3) / 1e9, "launches": len(offs)}
+
+
+def e2e_host_bytes(u: GpuUpdate) -> int:
+    """Pinned host bytes run_e2e allocates for `u`: every rank's gradients of
+    every microbatch and the bf16 parameters read back."""
+    return (u.n_micro * u.w.world * u.info["n_rank_pad"] + u.info["n_state_pad"]) * 2
+
+
+def host_available_bytes():
+    """MemAvailable of this host (Linux), or None when it cannot be read."""
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return None
 
 
 def run_e2e(u: GpuUpdate, args, torch):

@@ -68,3 +68,15 @@ def test_frozen_pattern_leaves_the_plan_smaller():
     op = bench._oracle_plan(w, flags)
     assert sum(n for n, f in zip(w.numels, flags) if not f) == 50343936
     assert op.n_state_pad >= 50343936
+
+
+def test_e2e_pinned_host_bytes():
+    """The end-to-end leg pins every rank's gradients of every microbatch
+    and the bf16 parameters: 2 bytes per element of each."""
+    import types
+    import bench
+    u = types.SimpleNamespace(n_micro=3, w=types.SimpleNamespace(world=4),
+                              info={"n_rank_pad": 1000, "n_state_pad": 700})
+    assert bench.e2e_host_bytes(u) == (3 * 4 * 1000 + 700) * 2
+    avail = bench.host_available_bytes()
+    assert avail is None or avail > 0
