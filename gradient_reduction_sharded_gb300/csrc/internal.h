@@ -44,21 +44,22 @@ namespace grs {
 #define GRS_RED_EVICT_FIRST 0
 #endif
 constexpr int64_t RED_RING_BYTES = int64_t(GRS_RED_RING_KB) * 1024;
-// Plans whose buckets all reduce at most RED_PAIR_MAX_GROUP bf16 rank rows
-// per element (e.g. 4 simulated ranks) run the plain reduction with two CTAs
-// per SM, each with a RED_PAIR_RING_KB ring and tiles sized for it: with so
-// few rows per tile one CTA's consumers cannot keep up with the TMA stream
-// (measured on the 3.2B, world-4 plan: 5.55 against 5.74 ms per launch),
-// while wider groups lose about 1% that way (the 67M world-16 and the 1.1B
-// world-8 plans), so they keep one CTA per SM with the full ring.
-#ifndef GRS_RED_PAIR_RING_KB
-#define GRS_RED_PAIR_RING_KB 100
+// Plans whose buckets all reduce at most RED_FEW_ROWS_GROUP bf16 rank rows
+// per element (e.g. 4 simulated ranks) run the plain reduction with at most
+// RED_FEW_ROWS_STAGES stages in flight per CTA.  Measured on the 3.2B,
+// world-4 plan (8192-element tiles of 4 rows): 5.43 ms per launch with 2
+// stages against 5.74 with 3 (and 5.51-6.09 for two CTAs per SM with
+// smaller rings); the 67M world-16 plan is 5% slower with 2 stages (0.333
+// against 0.316 ms) and the 1.1B world-8 one about equal, so wider groups
+// keep the ring's full depth.
+#ifndef GRS_RED_FEW_ROWS_GROUP
+#define GRS_RED_FEW_ROWS_GROUP 4
 #endif
-#ifndef GRS_RED_PAIR_MAX_GROUP
-#define GRS_RED_PAIR_MAX_GROUP 4
+#ifndef GRS_RED_FEW_ROWS_STAGES
+#define GRS_RED_FEW_ROWS_STAGES 2
 #endif
-constexpr int64_t RED_PAIR_RING_BYTES = int64_t(GRS_RED_PAIR_RING_KB) * 1024;
-constexpr int RED_PAIR_MAX_GROUP = GRS_RED_PAIR_MAX_GROUP;
+constexpr int RED_FEW_ROWS_GROUP = GRS_RED_FEW_ROWS_GROUP;
+constexpr int RED_FEW_ROWS_STAGES = GRS_RED_FEW_ROWS_STAGES;
 constexpr int64_t STAGE_GRAD_BYTES = GRS_STAGE_GRAD_BYTES;
 constexpr int64_t RED_MAX_T = GRS_RED_MAX_T;
 // Consumer warps of the reduction; the norm pass over acc uses the same
@@ -135,7 +136,7 @@ struct grs_plan {
   std::vector<uint8_t> tensor_live;    // 1 unless frozen (has state in the plan)
   int32_t world = 0, tp = 0, dp_replicate = 0, dp_shard = 0, dp = 0;
   int32_t grad_esize = 2;  // bytes per gradient element: 2 (bf16) or 4 (fp32)
-  bool red_pair = false;   // plain reduction with two CTAs per SM (RED_PAIR_*)
+  int32_t red_stage_cap = 0;  // plain bf16 reduction: at most this many stages per CTA (0: no cap)
   int64_t bucket_bytes = 0;
   // layout
   std::vector<int32_t> t_bucket;

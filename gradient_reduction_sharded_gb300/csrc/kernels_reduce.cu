@@ -74,10 +74,6 @@ constexpr size_t RED_SMEM_TAIL = 2 * RED_MAX_STAGES * sizeof(uint64_t)        //
 // its two tile bitmaps) within the 227 KB a CTA may opt into.
 static_assert(RED_RING_BYTES + RED_SMEM_TAIL + size_t(RED_SKIP_WORDS) * 8 <= 227 * 1024,
               "reduce_kernel shared memory above the per-CTA limit");
-// Two paired CTAs (plain instantiation, no bitmaps) within the SM's 228 KB,
-// 1 KB of it reserved per CTA.
-static_assert(2 * (RED_PAIR_RING_BYTES + RED_SMEM_TAIL + 1024) <= 228 * 1024,
-              "paired reduce_kernel CTAs do not fit one SM");
 
 struct ReduceArgs {
   const void* ranks[GRS_MAX_WORLD];  // bf16 bits or fp32, by the plan
@@ -123,11 +119,8 @@ __device__ __forceinline__ float fold_partials(const float* wp) {
 // without a gradient count as zero in the partial (a segment cursor per
 // consumer thread), which makes the partials those of the masked norm pass
 // bit for bit.  The plain instantiation has none of this.
-// kCtasPerSm: the CTAs per SM the launch targets (registers are capped so
-// that they fit): 1, or 2 for the paired plain reduction of plans with small
-// groups (grs_plan::red_pair).
-template <typename E, bool kMasked, int kCtasPerSm = GRS_RED_CTAS_PER_SM>
-__global__ void __launch_bounds__(RED_THREADS, kCtasPerSm) reduce_kernel(const __grid_constant__ ReduceArgs a) {
+template <typename E, bool kMasked>
+__global__ void __launch_bounds__(RED_THREADS, GRS_RED_CTAS_PER_SM) reduce_kernel(const __grid_constant__ ReduceArgs a) {
   constexpr uint32_t ESZ = sizeof(E);
   extern __shared__ __align__(128) uint8_t smem[];
   const int S = a.stages;
@@ -373,7 +366,7 @@ __global__ void __launch_bounds__(RED_THREADS, kCtasPerSm) reduce_kernel(const _
 
 // Whether the dynamic shared-memory cap is raised, per (gradient type,
 // device); plans on several host threads may launch at once.
-std::atomic<bool> g_attr_set[3][2][64] = {};  // [bf16, fp32, bf16 paired][masked][device]
+std::atomic<bool> g_attr_set[2][2][64] = {};
 
 }  // namespace
 
@@ -412,16 +405,15 @@ int launch_reduce(const grs_plan* p, const ReduceLaunch& l, void* stream) {
     need = b > need ? b : need;
   }
   need = (need + 127) / 128 * 128;
-  // The paired launch (two CTAs per SM, each with the smaller ring the
-  // plan sized its tiles for): plain bf16 reductions of red_pair plans.
-  const bool pair = p->red_pair && !masked && p->grad_esize == 2;
-  const int64_t ring = pair ? RED_PAIR_RING_BYTES : RED_RING_BYTES;
-  int stages = static_cast<int>(ring / need);  // >= 2 by the plan's tile cap
+  int stages = static_cast<int>(RED_RING_BYTES / need);  // >= 2 by the plan's tile cap
   stages = stages > RED_MAX_STAGES ? RED_MAX_STAGES : stages;
+  // Plans with few rank rows per element: a shallower ring for the plain
+  // reduction (grs_plan::red_stage_cap, RED_FEW_ROWS_*).
+  if (!masked && p->red_stage_cap > 0 && stages > p->red_stage_cap) stages = p->red_stage_cap;
   if (stages < 2) return static_cast<int>(cudaErrorInvalidConfiguration);
   a.stages = stages;
   a.stage_bytes = static_cast<int32_t>(need);
-  int64_t cap = int64_t(p->sm_count) * (pair ? 2 : GRS_RED_CTAS_PER_SM);
+  int64_t cap = int64_t(p->sm_count) * GRS_RED_CTAS_PER_SM;
   if (l.max_ctas > 0 && l.max_ctas < cap) cap = l.max_ctas;
   const int64_t grid = tiles < cap ? tiles : cap;
   const int64_t per_cta = (tiles + grid - 1) / grid;
@@ -430,27 +422,22 @@ int launch_reduce(const grs_plan* p, const ReduceLaunch& l, void* stream) {
   const size_t smem = size_t(stages) * need + RED_SMEM_TAIL + size_t(a.skip_words) * 8;  // two bitmaps
   const int f32 = p->grad_esize == 4 ? 1 : 0;
   const int mk = masked ? 1 : 0;
-  const int kind = pair ? 2 : f32;
-  if (p->device >= 0 && p->device < 64 && !g_attr_set[kind][mk][p->device].load(std::memory_order_acquire)) {
-    const int bytes = static_cast<int>(ring + RED_SMEM_TAIL + (masked ? RED_SKIP_WORDS * 8 : 0));
+  if (p->device >= 0 && p->device < 64 && !g_attr_set[f32][mk][p->device].load(std::memory_order_acquire)) {
+    const int bytes = static_cast<int>(RED_RING_BYTES + RED_SMEM_TAIL + (masked ? RED_SKIP_WORDS * 8 : 0));
     cudaError_t e;
-    if (pair)
-      e = cudaFuncSetAttribute(reduce_kernel<uint16_t, false, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    else if (f32)
+    if (f32)
       e = masked ? cudaFuncSetAttribute(reduce_kernel<float, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)
                  : cudaFuncSetAttribute(reduce_kernel<float, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     else
       e = masked ? cudaFuncSetAttribute(reduce_kernel<uint16_t, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)
                  : cudaFuncSetAttribute(reduce_kernel<uint16_t, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return static_cast<int>(e);
-    g_attr_set[kind][mk][p->device].store(true, std::memory_order_release);
+    g_attr_set[f32][mk][p->device].store(true, std::memory_order_release);
   }
   const dim3 gd(static_cast<unsigned>(grid));
   const dim3 bd(static_cast<unsigned>(RED_THREADS));
   cudaError_t e;
-  if (pair)
-    e = launch_k(reduce_kernel<uint16_t, false, 2>, gd, bd, smem, stream, a);
-  else if (f32)
+  if (f32)
     e = masked ? launch_k(reduce_kernel<float, true>, gd, bd, smem, stream, a)
                : launch_k(reduce_kernel<float, false>, gd, bd, smem, stream, a);
   else

@@ -155,8 +155,7 @@ grs_status build_plan(const int64_t* numels, const int32_t* owners, const uint32
   int64_t rank_off = 0, state_off = 0, red_tiles = 0, upd_tiles = 0;
   int32_t max_group = 0;
   for (const Bucket& bk : p->buckets) max_group = std::max(max_group, bk.group_size);
-  p->red_pair = grad_esize == 2 && max_group <= RED_PAIR_MAX_GROUP;
-  const int64_t ring = p->red_pair ? RED_PAIR_RING_BYTES : RED_RING_BYTES;
+  p->red_stage_cap = (grad_esize == 2 && max_group <= RED_FEW_ROWS_GROUP) ? RED_FEW_ROWS_STAGES : 0;
   for (size_t b = 0; b < p->buckets.size(); ++b) {
     Bucket& bk = p->buckets[b];
     bk.padded = round_up(bk.used, quantum);
@@ -166,7 +165,7 @@ grs_status build_plan(const int64_t* numels, const int32_t* owners, const uint32
     bk.unit0 = static_cast<int32_t>(p->units.size());
     const int64_t gsz = bk.group_size;
     const int64_t es = grad_esize;
-    int64_t T = std::min<int64_t>(STAGE_GRAD_BYTES / (es * gsz), ring / (2 * (es * gsz + 4)));
+    int64_t T = std::min<int64_t>(STAGE_GRAD_BYTES / (es * gsz), RED_RING_BYTES / (2 * (es * gsz + 4)));
     T = std::min<int64_t>(RED_MAX_T, std::max<int64_t>(8, T / 8 * 8));
     for (int32_t t = 0; t < bk.copies; ++t) {
       UnitDesc u{};
