@@ -358,10 +358,12 @@ grs_status grs_clip_adamw_step(const grs_plan* plan, const grs_adamw* hp, const 
  *                   bucket-ordered layout, or NULL (per-tensor output only).
  *   d_tensor_ptrs : DEVICE array [n_tensors] of device pointers (8-byte
  *                   aligned), entry i pointing at tensor i's numel bf16
- *                   elements (any 2-byte alignment; 16-byte-aligned
- *                   destinations are written with 16-byte stores); NULL
- *                   entries and frozen tensors are skipped.  The kernel reads
- *                   the table, so it must stay valid until the launch has run.
+ *                   elements (2-byte aligned; 16-byte-aligned destinations
+ *                   are written with 16-byte stores); NULL entries and frozen
+ *                   tensors are skipped.  The entries live in device memory,
+ *                   so the library cannot check them: the caller guarantees
+ *                   their extent and alignment.  The kernel reads the table,
+ *                   so it must stay valid until the launch has run.
  * The other arguments, the results in master, m, v (and params_bf16) and
  * the errors are those of grs_clip_adamw_step; ALIGNMENT also when the
  * table is not 8-byte aligned.  The tensors must not overlap each other or

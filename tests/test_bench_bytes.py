@@ -80,3 +80,25 @@ def test_e2e_pinned_host_bytes():
     assert bench.e2e_host_bytes(u) == (3 * 4 * 1000 + 700) * 2
     avail = bench.host_available_bytes()
     assert avail is None or avail > 0
+
+
+def test_profiling_slices_keep_the_geometry():
+    """The one-layer slices that stand in for the 1.1B, MoE and 3.2B plans in
+    ncu captures keep the degrees, microbatches, owner tags and per-layer
+    tensor shapes, and are small (under 130M parameters)."""
+    import workloads
+    for cid in (2, 3, 4):
+        full, sl = workloads.get(cid), workloads.get(cid, layers=1)
+        for k in ("tp", "dp_replicate", "dp_shard", "world", "n_micro", "bucket_bytes", "grad_std"):
+            assert getattr(full, k) == getattr(sl, k), (cid, k)
+        assert sl.n_unique < 130_000_000 < full.n_unique
+        assert set(sl.owners) == set(full.owners)
+        layer0 = [(t.name, t.shape, t.owner) for t in full.tensors if t.name.startswith("layers.0.")]
+        sl0 = [(t.name, t.shape, t.owner) for t in sl.tensors if t.name.startswith("layers.0.")]
+        if cid == 3:  # the MoE slice keeps 8 of the 32 experts (and the router's 8 outputs)
+            layer0 = [(n, ((8,) + s[1:]) if "experts" in n else (s[0], 8) if n.endswith("router") else s, o)
+                      for n, s, o in layer0]
+        assert layer0 == sl0, cid
+        assert not any(t.name.startswith("layers.1.") for t in sl.tensors)
+    with __import__("pytest").raises(ValueError):
+        workloads.get(1, layers=1)
