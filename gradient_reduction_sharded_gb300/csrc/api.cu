@@ -52,6 +52,16 @@ grs_status check_plan_device(const grs_plan* p) {
   return GRS_OK;
 }
 
+// Entry points that need rank gradient buffers or the plan's tensor layout,
+// which a shard view does not have.
+grs_status check_not_view(const grs_plan* p, const char* who) {
+  if (p != nullptr && p->view_shard >= 0)
+    return fail(GRS_ERR_UNSUPPORTED_COMPOSITION,
+                std::string(who) + ": not defined on a shard view (it holds one rank's state, no rank "
+                                   "gradients and no tensor layout)");
+  return GRS_OK;
+}
+
 template <typename T>
 cudaError_t upload(T** dst, const std::vector<T>& src) {
   const size_t bytes = (src.empty() ? 1 : src.size()) * sizeof(T);
@@ -160,6 +170,37 @@ grs_status grs_plan_create_ex(const int64_t* numels, const int32_t* owners, cons
   return GRS_OK;
 }
 
+grs_status grs_plan_shard_view(const grs_plan* parent, int32_t shard, int32_t tp_index, grs_plan** out) {
+  if (parent == nullptr || out == nullptr) return fail(GRS_ERR_INVALID_ARG, "grs_plan_shard_view: NULL argument");
+  if (parent->view_shard >= 0)
+    return fail(GRS_ERR_INVALID_ARG, "grs_plan_shard_view: the parent is itself a shard view");
+  if (shard < 0 || shard >= parent->dp_shard || tp_index < 0 || tp_index >= parent->tp)
+    return fail(GRS_ERR_INVALID_ARG, "grs_plan_shard_view: shard must be in [0, dp_shard) and tp_index in [0, tp)");
+  grs_plan* v = new (std::nothrow) grs_plan();
+  if (v == nullptr) return fail(GRS_ERR_INVALID_ARG, "grs_plan_shard_view: host allocation failed");
+  grs::build_shard_view(*parent, shard, tp_index, v);
+  if (parent->device >= 0) {
+    DeviceGuard g(parent->device);
+    cudaError_t e = g.ok() ? cudaSuccess : cudaErrorInvalidDevice;
+    v->sm_count = parent->sm_count;
+    if (e == cudaSuccess) e = upload(&v->d_units, v->units);
+    if (e == cudaSuccess) e = upload(&v->d_red_prefix, v->red_prefix);
+    if (e == cudaSuccess) e = upload(&v->d_red_tile_unit, v->red_tile_unit);
+    if (e == cudaSuccess) e = upload(&v->d_upd_tile_unit, v->upd_tile_unit);
+    if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&v->d_flags), grs::FLAG_COUNT * sizeof(int));
+    if (e == cudaSuccess) e = cudaMemsetAsync(v->d_flags, 0, grs::FLAG_COUNT * sizeof(int), nullptr);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(nullptr);
+    if (e != cudaSuccess) {
+      free_device(v);
+      delete v;
+      return cuda_fail(e, "grs_plan_shard_view: device tables");
+    }
+    v->device = parent->device;
+  }
+  *out = v;
+  return GRS_OK;
+}
+
 void grs_plan_destroy(grs_plan* p) {
   if (p == nullptr) return;
   if (p->device >= 0) {
@@ -211,6 +252,8 @@ grs_status grs_bucket_info(const grs_plan* p, int32_t b, grs_bucket_desc* o) {
 
 grs_status grs_segment_info(const grs_plan* p, int32_t b, int32_t i, grs_segment_desc* o) {
   if (p == nullptr || o == nullptr) return fail(GRS_ERR_INVALID_ARG, "NULL argument");
+  const grs_status vs = check_not_view(p, "grs_segment_info");
+  if (vs != GRS_OK) return vs;
   if (b < 0 || b >= static_cast<int32_t>(p->buckets.size()))
     return fail(GRS_ERR_INVALID_ARG, "bucket index out of range");
   const grs::Bucket& bk = p->buckets[b];
@@ -299,6 +342,8 @@ grs_status grs_reduce_bucket(const grs_plan* p, int32_t b, const void* const* ra
                              int32_t accumulate, int32_t emit, void* workspace, void* stream) {
   grs_status st = check_plan_device(p);
   if (st != GRS_OK) return st;
+  st = check_not_view(p, "grs_reduce_bucket");
+  if (st != GRS_OK) return st;
   if (b < 0 || b >= static_cast<int32_t>(p->buckets.size()))
     return fail(GRS_ERR_INVALID_ARG, "grs_reduce_bucket: bucket index out of range");
   const grs::Bucket& bk = p->buckets[b];
@@ -311,6 +356,8 @@ grs_status grs_reduce_bucket_ex(const grs_plan* p, int32_t b, const void* const*
                                 int32_t accumulate, int32_t emit, void* workspace, int32_t max_ctas,
                                 void* wait_event, void* stream) {
   grs_status st = check_plan_device(p);
+  if (st != GRS_OK) return st;
+  st = check_not_view(p, "grs_reduce_bucket_ex");
   if (st != GRS_OK) return st;
   if (b < 0 || b >= static_cast<int32_t>(p->buckets.size()))
     return fail(GRS_ERR_INVALID_ARG, "grs_reduce_bucket_ex: bucket index out of range");
@@ -325,6 +372,8 @@ grs_status grs_reduce_all(const grs_plan* p, const void* const* rank_grads, floa
                           int32_t accumulate, int32_t emit, void* workspace, void* stream) {
   grs_status st = check_plan_device(p);
   if (st != GRS_OK) return st;
+  st = check_not_view(p, "grs_reduce_all");
+  if (st != GRS_OK) return st;
   bool only_ar = true;
   for (const auto& bk : p->buckets) only_ar = only_ar && bk.tag == GRS_ALREADY_REDUCED;
   return reduce_common(p, rank_grads, acc, accumulate, emit, workspace, stream, 0,
@@ -336,6 +385,8 @@ grs_status grs_reduce_all_masked(const grs_plan* p, const void* const* rank_grad
                                  int32_t accumulate, int32_t emit, const uint8_t* d_tensor_used,
                                  void* workspace, void* stream) {
   grs_status st = check_plan_device(p);
+  if (st != GRS_OK) return st;
+  st = check_not_view(p, "grs_reduce_all_masked");
   if (st != GRS_OK) return st;
   if (d_tensor_used == nullptr) return fail(GRS_ERR_INVALID_ARG, "grs_reduce_all_masked: d_tensor_used is NULL");
   // The CTAs of the persistent grid each take ceil(tiles / grid) tiles, one
@@ -373,6 +424,9 @@ grs_status grs_grad_norm_sq(const grs_plan* p, const float* acc, int32_t n_micro
   if (workspace == nullptr || d_norm_sq == nullptr || (!partials_ready && acc == nullptr))
     return fail(GRS_ERR_INVALID_ARG, "grs_grad_norm_sq: NULL argument");
   if (n_micro < 1) return fail(GRS_ERR_INVALID_ARG, "grs_grad_norm_sq: n_micro must be >= 1");
+  if (partials_ready && p->view_shard >= 0)
+    return fail(GRS_ERR_UNSUPPORTED_COMPOSITION,
+                "grs_grad_norm_sq: a shard view has no reduction to emit partials (partials_ready must be 0)");
   if (!aligned16(workspace) || (acc != nullptr && !aligned16(acc)) ||
       (reinterpret_cast<uintptr_t>(d_norm_sq) & 7u) != 0)
     return fail(GRS_ERR_ALIGNMENT, "grs_grad_norm_sq: misaligned pointer");
@@ -409,6 +463,8 @@ grs_status grs_clip_adamw_step_to_tensors(const grs_plan* p, const grs_adamw* hp
                                           uint16_t* params_bf16, uint16_t* const* d_tensor_ptrs, void* stream) {
   grs_status st = check_plan_device(p);
   if (st != GRS_OK) return st;
+  st = check_not_view(p, "grs_clip_adamw_step_to_tensors");
+  if (st != GRS_OK) return st;
   if (hp == nullptr || acc == nullptr || master == nullptr || m == nullptr || v == nullptr ||
       d_tensor_ptrs == nullptr)
     return fail(GRS_ERR_INVALID_ARG, "grs_clip_adamw_step_to_tensors: NULL argument");
@@ -433,6 +489,8 @@ grs_status grs_update_small(const grs_plan* p, const grs_adamw* hp, const void* 
                             float* master, float* m, float* v, uint16_t* params_bf16, double* d_norm_sq,
                             void* stream) {
   grs_status st = check_plan_device(p);
+  if (st != GRS_OK) return st;
+  st = check_not_view(p, "grs_update_small");
   if (st != GRS_OK) return st;
   if (hp == nullptr || rank_grads == nullptr || acc == nullptr || master == nullptr || m == nullptr ||
       v == nullptr || params_bf16 == nullptr || d_norm_sq == nullptr)
@@ -470,6 +528,8 @@ grs_status grs_gather_params(const grs_plan* p, const uint16_t* params_bf16, uin
                              void* stream) {
   grs_status st = check_plan_device(p);
   if (st != GRS_OK) return st;
+  st = check_not_view(p, "grs_gather_params");
+  if (st != GRS_OK) return st;
   if (params_bf16 == nullptr || tensor_ptrs == nullptr)
     return fail(GRS_ERR_INVALID_ARG, "grs_gather_params: NULL argument");
   if (!aligned16(params_bf16)) return fail(GRS_ERR_ALIGNMENT, "grs_gather_params: params not 16-byte aligned");
@@ -488,6 +548,8 @@ grs_status grs_grad_norm_sq_masked(const grs_plan* p, const float* acc, int32_t 
                                    void* stream) {
   grs_status st = check_plan_device(p);
   if (st != GRS_OK) return st;
+  st = check_not_view(p, "grs_grad_norm_sq_masked");
+  if (st != GRS_OK) return st;
   if (acc == nullptr || d_tensor_used == nullptr || workspace == nullptr || d_norm_sq == nullptr)
     return fail(GRS_ERR_INVALID_ARG, "grs_grad_norm_sq_masked: NULL argument");
   if (n_micro < 1) return fail(GRS_ERR_INVALID_ARG, "grs_grad_norm_sq_masked: n_micro must be >= 1");
@@ -505,6 +567,8 @@ grs_status grs_clip_adamw_step_masked(const grs_plan* p, const grs_adamw* hp, co
                                       uint16_t* params_bf16, const uint8_t* d_tensor_used,
                                       int32_t* d_tensor_steps, void* workspace, void* stream) {
   grs_status st = check_plan_device(p);
+  if (st != GRS_OK) return st;
+  st = check_not_view(p, "grs_clip_adamw_step_masked");
   if (st != GRS_OK) return st;
   if (hp == nullptr || acc == nullptr || master == nullptr || m == nullptr || v == nullptr ||
       params_bf16 == nullptr || d_tensor_used == nullptr || d_tensor_steps == nullptr || workspace == nullptr)
@@ -527,6 +591,8 @@ static grs_status state_logical_common(const grs_plan* p, const float* a, float*
                                        void* stream, const char* who) {
   grs_status st = check_plan_device(p);
   if (st != GRS_OK) return st;
+  st = check_not_view(p, "grs_state_to_logical / grs_state_from_logical");
+  if (st != GRS_OK) return st;
   if (a == nullptr || b == nullptr) return fail(GRS_ERR_INVALID_ARG, std::string(who) + ": NULL argument");
   if ((reinterpret_cast<uintptr_t>(a) & 3u) != 0 || (reinterpret_cast<uintptr_t>(b) & 3u) != 0)
     return fail(GRS_ERR_ALIGNMENT, std::string(who) + ": pointer not 4-byte aligned");
@@ -548,6 +614,8 @@ grs_status grs_state_from_logical(const grs_plan* p, const float* logical, float
 
 grs_status grs_check_already_reduced(const grs_plan* p, const void* const* rank_grads, void* stream) {
   grs_status st = check_plan_device(p);
+  if (st != GRS_OK) return st;
+  st = check_not_view(p, "grs_check_already_reduced");
   if (st != GRS_OK) return st;
   if (rank_grads == nullptr) return fail(GRS_ERR_INVALID_ARG, "grs_check_already_reduced: NULL argument");
   for (int32_t k = 0; k < p->world; ++k)

@@ -91,6 +91,8 @@ extern "C" grs_status grs_step_from_host(const grs_plan* pc, const grs_adamw* hp
   if (p == nullptr || hp == nullptr || host_grads == nullptr || dev_stage == nullptr)
     return fail(GRS_ERR_INVALID_ARG, "grs_step_from_host: NULL argument");
   if (p->device < 0) return fail(GRS_ERR_NO_DEVICE, "grs_step_from_host: plan was created with GRS_PLAN_HOST_ONLY");
+  if (p->view_shard >= 0)
+    return fail(GRS_ERR_UNSUPPORTED_COMPOSITION, "grs_step_from_host: not defined on a shard view");
   if (hp->n_micro < 1 || hp->step < 1)
     return fail(GRS_ERR_INVALID_ARG, "grs_step_from_host: step and n_micro must be >= 1");
   const int32_t M = hp->n_micro, W = p->world;

@@ -137,6 +137,9 @@ struct grs_plan {
   int32_t world = 0, tp = 0, dp_replicate = 0, dp_shard = 0, dp = 0;
   int32_t grad_esize = 2;  // bytes per gradient element: 2 (bf16) or 4 (fp32)
   int32_t red_stage_cap = 0;  // plain bf16 reduction: at most this many stages per CTA (0: no cap)
+  // A shard view (grs_plan_shard_view): the state layout of one rank (shard
+  // view_shard, tp index view_tp) of a parent plan; -1 for an ordinary plan.
+  int32_t view_shard = -1, view_tp = -1;
   int64_t bucket_bytes = 0;
   // layout
   std::vector<int32_t> t_bucket;
@@ -247,6 +250,9 @@ enum : int {
 void set_last_error(const std::string& msg);
 // Frees the copy stream and events grs_step_from_host created (host_step.cu).
 void destroy_host_step_resources(grs_plan* p);
+
+// Host tables of the shard view (shard, tp_index) of `parent` (plan.cpp).
+void build_shard_view(const grs_plan& parent, int32_t shard, int32_t tp_index, grs_plan* v);
 
 // host plan builder (plan.cpp)
 grs_status build_plan(const int64_t* numels, const int32_t* owners, const uint32_t* tensor_flags,

@@ -315,4 +315,80 @@ grs_status build_plan(const int64_t* numels, const int32_t* owners, const uint32
   return GRS_OK;
 }
 
+// The state layout of rank (r, shard, tp_index) after the reduce-scatter:
+// per bucket one slice of shard_len elements, [shard * shard_len, +shard_len)
+// of row tp_index (LOCAL_SHARD) or row 0 (every other tag), slices back to
+// back in bucket order.  One unit per bucket; the update tiles cover every
+// slice, the norm tiles only the slices this rank holds uniquely within its
+// tp group (LOCAL_SHARD rows always, the others only at tp index 0), so the
+// views of one replica partition the plan's unique elements.
+void build_shard_view(const grs_plan& parent, int32_t shard, int32_t tp_index, grs_plan* v) {
+  v->numel = parent.numel;
+  v->owner = parent.owner;
+  v->tensor_flags = parent.tensor_flags;
+  v->tensor_live = parent.tensor_live;
+  v->world = parent.world;
+  v->tp = parent.tp;
+  v->dp_replicate = parent.dp_replicate;
+  v->dp_shard = parent.dp_shard;
+  v->dp = parent.dp;
+  v->grad_esize = parent.grad_esize;
+  v->bucket_bytes = parent.bucket_bytes;
+  v->t_bucket = parent.t_bucket;
+  v->t_offset = parent.t_offset;
+  v->view_shard = shard;
+  v->view_tp = tp_index;
+  v->buckets.clear();
+  v->units.clear();
+  v->red_prefix.assign(1, 0);
+  v->upd_prefix.assign(1, 0);
+  v->red_tile_unit.clear();
+  v->upd_tile_unit.clear();
+  v->bucket_seg0.assign(1, 0);
+  int64_t state_off = 0, red_tiles = 0, upd_tiles = 0, unique = 0;
+  for (size_t b = 0; b < parent.buckets.size(); ++b) {
+    const Bucket& pb = parent.buckets[b];
+    const UnitDesc& pu = parent.units[pb.unit0];
+    const int64_t L = pb.shard_len;
+    const int64_t used = std::max<int64_t>(0, std::min<int64_t>(L, pb.used - int64_t(shard) * L));
+    Bucket bk = pb;
+    bk.copies = 1;
+    bk.used = used;
+    bk.padded = L;
+    bk.shard_len = L;
+    bk.rank_off = 0;
+    bk.state_off = state_off;
+    bk.unit0 = static_cast<int32_t>(v->units.size());
+    v->buckets.push_back(bk);
+    v->bucket_seg0.push_back(0);
+    UnitDesc u{};
+    u.state_off = state_off;
+    u.padded = L;
+    u.used = used;
+    u.red_tile0 = red_tiles;
+    u.upd_tile0 = upd_tiles;
+    u.red_T = pu.red_T;
+    u.bucket = static_cast<int32_t>(b);
+    const bool counts = pb.tag == GRS_LOCAL_SHARD || tp_index == 0;
+    const int64_t nr = counts ? (L + pu.red_T - 1) / pu.red_T : 0;
+    const int64_t nu = (L + UPD_T - 1) / UPD_T;
+    v->red_tile_unit.insert(v->red_tile_unit.end(), static_cast<size_t>(nr), static_cast<int32_t>(v->units.size()));
+    v->upd_tile_unit.insert(v->upd_tile_unit.end(), static_cast<size_t>(nu), static_cast<int32_t>(v->units.size()));
+    red_tiles += nr;
+    upd_tiles += nu;
+    if (counts) unique += used;
+    v->units.push_back(u);
+    v->red_prefix.push_back(red_tiles);
+    v->upd_prefix.push_back(upd_tiles);
+    state_off += L;
+  }
+  v->n_unique = unique;
+  v->n_rank_pad = 0;
+  v->n_state_pad = state_off;
+  v->n_red_tiles = red_tiles;
+  v->n_upd_tiles = upd_tiles;
+  v->n_gather_chunks = 0;
+  v->workspace_bytes = ws_bytes(red_tiles);
+}
+
 }  // namespace grs

@@ -102,6 +102,7 @@ _sig = {
                             ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                             ctypes.c_int64, ctypes.c_uint32, _P(_vp)], ctypes.c_int),
     "grs_plan_destroy": ([_vp], None),
+    "grs_plan_shard_view": ([_vp, ctypes.c_int32, ctypes.c_int32, _P(_vp)], ctypes.c_int),
     "grs_plan_query": ([_vp, _P(grs_plan_info)], ctypes.c_int),
     "grs_bucket_info": ([_vp, ctypes.c_int32, _P(grs_bucket_desc)], ctypes.c_int),
     "grs_tensor_info": ([_vp, ctypes.c_int32, _P(grs_tensor_desc)], ctypes.c_int),
@@ -190,6 +191,12 @@ def grs_plan_create_ex(numels: Sequence[int], owners: Sequence[int], tensor_flag
     out = _vp()
     _check(_lib.grs_plan_create_ex(ne, ow, tf, n, world, tp, dp_replicate, dp_shard, bucket_bytes,
                                    flags, ctypes.byref(out)), "grs_plan_create_ex")
+    return out.value
+
+
+def grs_plan_shard_view(plan: int, shard: int, tp_index: int) -> int:
+    out = _vp()
+    _check(_lib.grs_plan_shard_view(plan, shard, tp_index, ctypes.byref(out)), "grs_plan_shard_view")
     return out.value
 
 

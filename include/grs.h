@@ -213,6 +213,39 @@ grs_status grs_plan_create_ex(const int64_t* numels, const int32_t* owners, cons
                               int32_t n_tensors, int32_t world, int32_t tp, int32_t dp_replicate,
                               int32_t dp_shard, int64_t bucket_bytes, uint32_t flags, grs_plan** out);
 
+/* The shard view of rank (r, shard, tp_index): a plan, destroyed with
+ * grs_plan_destroy, whose state layout is what that rank owns after the
+ * reduce-scatter ([COSMOS] section 2: rank (r, s) of the dp_mesh holds shard
+ * s of every parameter, replicas r hold the same shard): per bucket b, in
+ * bucket order, shard_len elements — elements [shard * shard_len,
+ * (shard + 1) * shard_len) of row tp_index for LOCAL_SHARD buckets, of row 0
+ * for the others (every tp rank keeps its own copy of those).  A job that
+ * runs one rank per GPU brings the rank's reduced gradient shard into this
+ * layout with its own collectives (reduce-scatter over the shard group,
+ * all-reduce across replicas, per [COSMOS] section 2); the view then gives
+ * the rank-local steps:
+ *   grs_grad_norm_sq (partials_ready = 0): the squared norm over the
+ *     elements this rank holds uniquely within its tp group (LOCAL_SHARD
+ *     rows always, the other rows only at tp_index 0), so that the sum over
+ *     all (shard, tp_index) views of one replica is the global S — the one
+ *     scalar all-reduce of the norm;
+ *   grs_accumulate: microbatch accumulation of reduced shards;
+ *   grs_clip_adamw_step: clip + AdamW + bf16 cast of the shard, bit for bit
+ *     the plan's own update restricted to these elements (given the same S),
+ *     whose bf16 shards an all-gather over the shard group reassembles.
+ * grs_plan_query reports the view's n_state_pad (the sum of the slices),
+ * n_unique (the elements it counts in the norm), workspace_bytes and
+ * n_rank_pad = 0; grs_bucket_info describes each slice (copies 1, padded =
+ * used-or-padding extent = shard_len, used = its valid elements,
+ * state_offset in the view).  Entry points that need rank gradient buffers
+ * or the tensor layout (reductions, gather, masked calls, layout conversion,
+ * grs_step_from_host, grs_segment_info, grs_update_small) return
+ * UNSUPPORTED_COMPOSITION for a view.  The view's device tables go to the
+ * parent's device (none for a host-only parent).
+ * Errors: INVALID_ARG (NULL, shard or tp_index out of range, a view as the
+ * parent), CUDA. */
+grs_status grs_plan_shard_view(const grs_plan* plan, int32_t shard, int32_t tp_index, grs_plan** out);
+
 /* Free the plan and its device tables.  NULL is a no-op.  The caller must
  * ensure no launch using the plan is still in flight. */
 void grs_plan_destroy(grs_plan* plan);

@@ -393,6 +393,102 @@ def test_update_to_tensors_argument_errors():
         run.close()
 
 
+@pytest.mark.parametrize("name", ["tiny-world4", "odd-ds3-M3", "multi-tile-world16-M2", "tp4-world8", "world1"])
+def test_shard_views_reproduce_the_plan_update(name):
+    """Each rank's shard view (grs_plan_shard_view) given that rank's slices
+    of the reduced gradient and of the state: the squared norms of the views
+    of one replica add up to the plan's S (the one scalar all-reduce), and
+    clip + AdamW + bf16 on each view with that S equals the plan's own update
+    restricted to the rank's elements, bit for bit — so an all-gather of the
+    views' bf16 shards gives the plan's parameters ("Cosmos 3 ... distributed
+    parallelism", section 2).  A view refuses the reductions."""
+    g = grs()
+    c = SMALL[name]
+    run = Run(c)
+    try:
+        master0, m0, v0 = (torch.from_numpy(x).cuda() for x in run.state_host())
+        run.update()
+        torch.cuda.synchronize()
+        full = {k: getattr(run, k)[:run.nsp] for k in ("acc", "master", "m", "v", "params")}
+        info = run.info
+        bks = [g.grs_bucket_info(run.plan, b) for b in range(info["n_buckets"])]
+        s_sum = 0.0
+        hp = g.make_adamw(c.hp[0], c.hp[1], c.hp[2], c.hp[3], c.hp[4], c.max_norm, 1, c.n_micro)
+        for t in range(c.tp):
+            for s in range(info["dp_shard"]):
+                view = g.grs_plan_shard_view(run.plan, s, t)
+                try:
+                    vi = g.grs_plan_query(view)
+                    idx = []
+                    for pb in bks:
+                        row = t if pb["tag"] == LS else 0
+                        L = int(pb["shard_len"])
+                        base = int(pb["state_offset"]) + row * int(pb["padded"]) + s * L
+                        idx.append(torch.arange(base, base + L, device="cuda"))
+                    idx = torch.cat(idx) if idx else torch.zeros(0, dtype=torch.int64, device="cuda")
+                    assert idx.numel() == vi["n_state_pad"]
+                    n = max(8, idx.numel())
+                    acc_v = torch.zeros(n, device="cuda")
+                    acc_v[:idx.numel()] = full["acc"][idx]
+                    st = [torch.zeros(n, device="cuda") for _ in range(3)]
+                    for x, src in zip(st, (master0, m0, v0)):
+                        x[:idx.numel()] = src[idx]
+                    params_v = torch.full((n,), -1, dtype=torch.int16, device="cuda")
+                    ws = torch.zeros(max(vi["workspace_bytes"], 16) // 4 + 4, device="cuda")
+                    nv = torch.zeros(1, dtype=torch.float64, device="cuda")
+                    g.grs_grad_norm_sq(view, acc_v.data_ptr(), c.n_micro, ws.data_ptr(), 0, nv.data_ptr(), run.stream())
+                    g.grs_clip_adamw_step(view, hp, run.norm.data_ptr(), acc_v.data_ptr(), st[0].data_ptr(),
+                                          st[1].data_ptr(), st[2].data_ptr(), params_v.data_ptr(), run.stream())
+                    torch.cuda.synchronize()
+                    assert g.grs_check_device_errors(view, run.stream()) == 0
+                    k = idx.numel()
+                    for x, nm in zip(st, ("master", "m", "v")):
+                        assert torch.equal(x[:k], full[nm][idx]), (name, s, t, nm)
+                    assert torch.equal(params_v[:k], full["params"][idx]), (name, s, t, "params")
+                    s_sum += float(nv.cpu()[0])
+                    with pytest.raises(g.GrsError) as ei:
+                        g.grs_reduce_all(view, run.ptrs(0), acc_v.data_ptr(), 0, 0, ws.data_ptr(), run.stream())
+                    assert ei.value.status == g.GRS_ERR_UNSUPPORTED_COMPOSITION
+                    with pytest.raises(g.GrsError) as ei:
+                        g.grs_grad_norm_sq(view, acc_v.data_ptr(), c.n_micro, ws.data_ptr(), 1, nv.data_ptr(),
+                                           run.stream())
+                    assert ei.value.status == g.GRS_ERR_UNSUPPORTED_COMPOSITION
+                finally:
+                    g.grs_plan_destroy(view)
+        want = float(run.norm.cpu()[0])
+        assert abs(s_sum - want) <= 1e-5 * want, (s_sum, want)
+    finally:
+        run.close()
+
+
+def test_shard_view_accumulates_microbatches():
+    """grs_accumulate on a shard view adds a reduced microbatch shard into
+    the view's accumulator bucket by bucket, padding kept at zero."""
+    g = grs()
+    run = Run(SMALL["multi-tile-world16-M2"])
+    try:
+        view = g.grs_plan_shard_view(run.plan, 1, 1)
+        try:
+            vi = g.grs_plan_query(view)
+            n = vi["n_state_pad"]
+            gen = torch.Generator(device="cuda").manual_seed(9)
+            a = torch.randn(n, generator=gen, device="cuda")
+            b = torch.randn(n, generator=gen, device="cuda")
+            want = a + b
+            for bk in range(vi["n_buckets"]):
+                d = g.grs_bucket_info(view, bk)
+                lo, L, used = int(d["state_offset"]), int(d["padded"]), int(d["used"])
+                want[lo + used:lo + L] = 0.0
+                g.grs_accumulate(view, bk, a.data_ptr() + 4 * lo, b.data_ptr() + 4 * lo, run.stream())
+            torch.cuda.synchronize()
+            assert g.grs_check_device_errors(view, run.stream()) == 0
+            assert torch.equal(a, want)
+        finally:
+            g.grs_plan_destroy(view)
+    finally:
+        run.close()
+
+
 def test_accumulate_entry_point():
     c = SMALL["odd-ds3-M3"]
     run = Run(c)

@@ -203,3 +203,57 @@ def test_query_bounds(grs):
             grs.grs_tensor_info(h, -1)
     finally:
         grs.grs_plan_destroy(h)
+
+
+def _host_plan(grs, w):
+    return grs.grs_plan_create(w.numels, w.owners, w.world, w.tp, w.dp_replicate, w.dp_shard, w.bucket_bytes,
+                               grs.GRS_PLAN_HOST_ONLY)
+
+
+@pytest.mark.parametrize("cid", [0, 1, 3, 4])
+def test_shard_views_partition_the_plan(grs, cid):
+    """The shard views of one replica, (shard s, tp index t) for every s and
+    t: each bucket's slice is shard_len elements of row t (LOCAL_SHARD) or
+    row 0, with the valid elements of [s * shard_len, (s + 1) * shard_len);
+    the views' norm-counted elements add up to the plan's unique elements
+    (each counted once: LOCAL_SHARD rows by their own tp index, the other
+    rows by tp index 0 only)."""
+    w = workloads.get(cid)
+    plan = _host_plan(grs, w)
+    try:
+        info = grs.grs_plan_query(plan)
+        nb = info["n_buckets"]
+        bks = [grs.grs_bucket_info(plan, b) for b in range(nb)]
+        total_unique = 0
+        for t in range(w.tp):
+            for s in range(info["dp_shard"]):
+                v = grs.grs_plan_shard_view(plan, s, t)
+                try:
+                    vi = grs.grs_plan_query(v)
+                    assert vi["n_buckets"] == nb and vi["n_rank_pad"] == 0 and vi["device"] == -1
+                    assert vi["n_state_pad"] == sum(int(b["shard_len"]) for b in bks)
+                    off = 0
+                    for b, pb in enumerate(bks):
+                        vb = grs.grs_bucket_info(v, b)
+                        L = int(pb["shard_len"])
+                        used = max(0, min(L, int(pb["used"]) - s * L))
+                        assert (vb["copies"], vb["padded"], vb["shard_len"], vb["used"], vb["state_offset"]) == \
+                            (1, L, L, used, off)
+                        assert vb["tag"] == pb["tag"]
+                        off += L
+                    total_unique += vi["n_unique"]
+                    with pytest.raises(grs.GrsError) as ei:
+                        grs.grs_segment_info(v, 0, 0)
+                    assert ei.value.status == grs.GRS_ERR_UNSUPPORTED_COMPOSITION
+                    with pytest.raises(grs.GrsError) as ei:
+                        grs.grs_plan_shard_view(v, 0, 0)
+                    assert ei.value.status == grs.GRS_ERR_INVALID_ARG
+                finally:
+                    grs.grs_plan_destroy(v)
+        assert total_unique == info["n_unique"]
+        for s, t in ((-1, 0), (info["dp_shard"], 0), (0, -1), (0, w.tp)):
+            with pytest.raises(grs.GrsError) as ei:
+                grs.grs_plan_shard_view(plan, s, t)
+            assert ei.value.status == grs.GRS_ERR_INVALID_ARG
+    finally:
+        grs.grs_plan_destroy(plan)
