@@ -215,6 +215,24 @@ def _step_worker(rank, world, port, path, tp, dr, ds):
             if owner_of_unique:
                 local_sq += oracle.norm_sq(a[:n_used], M)
             shards.append((b, row, L, n_used, a, M))
+        # the library's shard view of this rank describes the same slices
+        if "numels" in d.files:
+            from gradient_reduction_sharded_gb300 import grs
+            plan = grs.grs_plan_create([int(x) for x in d["numels"]], [int(x) for x in d["owners"]], world, tp, dr,
+                                       ds, int(d["bucket_bytes"]), grs.GRS_PLAN_HOST_ONLY)
+            view = grs.grs_plan_shard_view(plan, s, t)
+            try:
+                off = 0
+                for b, row, L, n_used, a, M in shards:
+                    vb = grs.grs_bucket_info(view, b)
+                    assert (vb["state_offset"], vb["padded"], vb["used"]) == (off, L, n_used), (rank, b)
+                    off += L
+                counted = sum(n_used for b, row, L, n_used, a, M in shards
+                              if int(d["b_tag"][b]) == LOCAL_SHARD or t == 0)
+                assert grs.grs_plan_query(view)["n_unique"] == counted
+            finally:
+                grs.grs_plan_destroy(view)
+                grs.grs_plan_destroy(plan)
         S = torch.tensor([local_sq], dtype=torch.float64)
         dist.all_reduce(S, op=dist.ReduceOp.SUM)  # the one scalar exchange of the norm
         S = float(S[0])
@@ -251,6 +269,8 @@ def _step_worker(rank, world, port, path, tp, dr, ds):
 
 @pytest.mark.parametrize("tp,dr,ds", [(2, 1, 2), (1, 2, 2), (2, 2, 2)])
 def test_sharded_step_matches_single_process_oracle(orc, tp, dr, ds):
+    from gradient_reduction_sharded_gb300 import _build
+    _build.build()  # the ranks also check the library's shard views (host tables only)
     rng = np.random.default_rng(300 + tp * 10 + dr * 3 + ds)
     world = tp * dr * ds
     M = 2
@@ -261,7 +281,8 @@ def test_sharded_step_matches_single_process_oracle(orc, tp, dr, ds):
     hp = (1e-3, 0.9, 0.999, 1e-8, 0.01)
     max_norm = 0.01  # clipping active
     arrays = {"n_buckets": np.int64(p.n_buckets), "b_tag": p.b_tag, "b_padded": p.b_padded,
-              "b_used": p.b_used, "b_state_off": p.b_state_off, "hp": np.array(hp), "max_norm": max_norm}
+              "b_used": p.b_used, "b_state_off": p.b_state_off, "hp": np.array(hp), "max_norm": max_norm,
+              "numels": np.array(numels), "owners": np.array(owners), "bucket_bytes": np.int64(64)}
     inputs = {}
     for b in range(p.n_buckets):
         P = int(p.b_padded[b])
