@@ -56,13 +56,13 @@ def sample_positions(rng, used, P, tile=2048, n_random=384):
 
 
 # The variants bench.py measures (--variant / --window), in the same launch
-# configuration: fp32 rank gradients, tensors without a gradient (masked
-# reduction with its fused norm partials, masked update), frozen tensors, a
-# trailing window of 3 of 4 microbatches.
+# configuration, every element: fp32 rank gradients, tensors without a
+# gradient (masked reduction with its fused norm partials, masked update),
+# frozen tensors, a trailing window of 3 of 4 microbatches.
 @pytest.mark.parametrize("cid,variant,window", [(1, "fp32-grads", 0), (1, "unused", 0),
                                                 (1, "frozen", 0), (3, "plain", 3)])
 def test_full_size_variant_matches_oracle(cid, variant, window):
-    _full_size(cid, variant, window)
+    _every_element(workloads.get(cid), variant, window)
 
 
 def test_workload1_every_element_matches_oracle():
@@ -129,49 +129,72 @@ def test_large_workload_every_element_matches_oracle(cid):
     _every_element(workloads.get(cid))
 
 
-def _every_element(w, chunk=1 << 23):
+def _every_element(w, variant="plain", window=0, chunk=1 << 23):
+    """One update of workload `w` (bench.GpuUpdate with the variant's plan
+    flags, gradient type, window and mask), then every state element
+    against the oracle, bucket row by bucket row in chunks on the host's
+    cores.  Elements of tensors without a gradient this step (the unused
+    variant) count zero in the norm and must keep master, bf16 copy and zero
+    moments; their accumulator is unspecified."""
     import bench
     from gpu_support import assert_bf16_cast as cast_check
 
-    op = oracle.plan(w.numels, w.owners, w.world, w.tp, w.dp_replicate, w.dp_shard, w.bucket_bytes)
-    need = (w.n_micro * w.world * op.n_rank_pad * 2 + op.n_state_pad * 22) / 1e9
+    fp32 = variant == "fp32-grads"
+    flags = bench.frozen_pattern(len(w.numels)) if variant == "frozen" else None
+    used_t = bench.unused_pattern(len(w.numels)) if variant == "unused" else None
+    op = oracle.plan(w.numels, w.owners, w.world, w.tp, w.dp_replicate, w.dp_shard, w.bucket_bytes, flags)
+    M = window or w.n_micro
+    need = (M * w.world * op.n_rank_pad * (4 if fp32 else 2) + op.n_state_pad * 24) / 1e9
     if _free_gb() < need * 1.05 + 4:
         pytest.skip(f"needs {need:.0f} GB of device memory")
-    u = bench.GpuUpdate(w, torch.device("cuda"))
+    u = bench.GpuUpdate(w, torch.device("cuda"), variant, window)
+    gview = torch.float32 if fp32 else torch.int16
+    # per bucket: the per-rank elements that belong to a tensor with a gradient
+    live = {}
+    for b in range(op.n_buckets):
+        mk = np.zeros(int(op.b_padded[b]), bool)
+        for i in range(len(w.numels)):
+            if int(op.t_bucket[i]) == b and (used_t is None or used_t[i]):
+                o = int(op.t_offset[i])
+                mk[o:o + op.per_rank(i)] = True
+        live[b] = mk
     try:
+        assert u.info["n_state_pad"] == op.n_state_pad and u.n_micro == M
         master0 = u.master.clone()
+        params0 = u.params.clone()
         u.step()
         torch.cuda.synchronize()
         assert u.grs.grs_check_device_errors(u.plan, u.stream) == 0
-        M, R = w.n_micro, w.world
+        R = w.world
         a = w.adamw
         hp = (a.lr, a.beta1, a.beta2, a.eps, a.weight_decay)
         items = [(b, cs, min(chunk, int(op.b_padded[b]) - cs))
                  for b in range(op.n_buckets) for cs in range(0, int(op.b_padded[b]), chunk)]
 
-        def inputs(item):
+        def reduce(item):
             b, cs, cl = item
             ro = int(op.b_rank_off[b]) + cs
-            g = np.stack([np.stack([u.grads[j][k][ro:ro + cl].view(torch.int16).cpu().numpy() for k in range(R)])
-                          for j in range(M)]).view(np.uint16)
+            g = np.stack([np.stack([u.grads[j][k][ro:ro + cl].view(gview).cpu().numpy() for k in range(R)])
+                          for j in range(M)])
+            if not fp32:
+                g = g.view(np.uint16)
             used = max(0, min(cl, int(op.b_used[b]) - cs))
-            return g, used
-
-        def reduce(item):
-            b = item[0]
-            g, used = inputs(item)
-            acc = oracle.reduce_bucket(int(op.b_tag[b]), op.tp, op.dp_replicate, op.dp_shard, item[2], used, g)
+            acc = oracle.reduce_bucket(int(op.b_tag[b]), op.tp, op.dp_replicate, op.dp_shard, cl, used, g)
             return g, used, acc
 
         def norm_part(item):
-            return oracle.norm_sq(reduce(item)[2], M)
+            acc = reduce(item)[2].copy()
+            acc[:, ~live[item[0]][item[1]:item[1] + item[2]]] = 0.0  # no gradient: counts zero
+            return oracle.norm_sq(acc, M)
 
         threads = max(1, min(16, os.cpu_count() or 1))
         with ThreadPoolExecutor(threads) as ex:
             parts = list(ex.map(norm_part, items))
         s_oracle = float(np.sum(np.array(parts, np.float64)))
-        assert_close([float(u.norm.cpu()[0])], [s_oracle], f"{w.name} norm_sq")
+        what0 = f"{w.name} {variant}" + (f" window {M}" if window else "")
+        assert_close([float(u.norm.cpu()[0])], [s_oracle], f"{what0} norm_sq")
         c = oracle.clip_coef(s_oracle, a.max_norm)
+        assert c < 1.0  # clipping is active on these workloads
 
         def compare(item):
             b, cs, cl = item
@@ -179,6 +202,9 @@ def _every_element(w, chunk=1 << 23):
             delta = oracle.accumulation_error_bound(
                 oracle.reduce_bucket(int(op.b_tag[b]), op.tp, op.dp_replicate, op.dp_shard, cl, used,
                                      oracle.abs_inputs(g)), M, oracle.group_terms(op, b))
+            lv = live[b][cs:cs + cl]
+            idle = ~lv.copy()
+            idle[used:] = False  # padding is checked as padding
             for t in range(op.copies(b)):
                 o = int(op.b_state_off[b]) + t * int(op.b_padded[b]) + cs
                 sl = slice(o, o + cl)
@@ -187,22 +213,31 @@ def _every_element(w, chunk=1 << 23):
                 want = oracle.adamw(acc[t], used, M, c, hp, 1, m0, z, z)
                 lo = oracle.adamw(acc[t] - delta[t], used, M, c, hp, 1, m0, z, z)
                 hi = oracle.adamw(acc[t] + delta[t], used, M, c, hp, 1, m0, z, z)
-                what = f"{w.name} bucket {b} row {t} [{cs}, {cs + cl})"
+                what = f"{what0} bucket {b} row {t} [{cs}, {cs + cl})"
                 got_acc = u.acc[sl].cpu().numpy()
-                assert_close(got_acc, acc[t], f"{what} acc")
-                assert_within_accumulation_bound(got_acc, acc[t], delta[t], f"{what} acc")
                 got = [x[sl].cpu().numpy() for x in (u.master, u.m, u.v)]
-                for name, gv, wv, lv, hv in zip(("master", "m", "v"), got, want[:3], lo[:3], hi[:3]):
-                    assert_close_bracketed(gv, wv, lv, hv, f"{what} {name}")
                 bits = u.params[sl].cpu().numpy().view(np.uint16)
-                cast_check(bits, got[0], want[3], want[0], f"{what} params", lo_master=lo[0], hi_master=hi[0])
+                k = lv  # elements of tensors with a gradient (the masked update leaves the others)
+                assert_close(got_acc[k], acc[t][k], f"{what} acc")
+                assert_within_accumulation_bound(got_acc[k], acc[t][k], delta[t][k], f"{what} acc")
+                for name, gv, wv, lw, hw in zip(("master", "m", "v"), got, want[:3], lo[:3], hi[:3]):
+                    assert_close_bracketed(gv[k], wv[k], lw[k], hw[k], f"{what} {name}")
+                cast_check(bits[k], got[0][k], want[3][k], want[0][k], f"{what} params", lo_master=lo[0][k],
+                           hi_master=hi[0][k])
+                if idle.any():  # no gradient this step: nothing read or written
+                    assert np.array_equal(got[0][idle].view(np.uint32), m0[idle].view(np.uint32)), what
+                    b0 = params0[sl].cpu().numpy().view(np.uint16)
+                    assert np.array_equal(bits[idle], b0[idle]), what
+                    assert np.all(got[1][idle] == 0) and np.all(got[2][idle] == 0), what
                 for x in (got_acc, got[0], got[1], got[2], bits):
                     assert np.all(x[used:] == 0)
-            return cl * op.copies(b)
+            return cl * op.copies(b), int(idle.sum()) * op.copies(b)
 
         with ThreadPoolExecutor(threads) as ex:
-            n_checked = sum(ex.map(compare, items))
-        assert n_checked == op.n_state_pad
+            done = list(ex.map(compare, items))
+        assert sum(n for n, _ in done) == op.n_state_pad
+        if used_t is not None:
+            assert sum(i for _, i in done) > 0, "no element of a tensor without a gradient"
     finally:
         u.close()
         del u
@@ -271,10 +306,6 @@ def test_gather_and_layout_beyond_32_bit_indices():
     finally:
         grs.grs_plan_destroy(plan)
         torch.cuda.empty_cache()
-
-
-def _full_size(cid, variant, window):
-    _full_size_w(workloads.get(cid), variant, window)
 
 
 def _full_size_w(w, variant, window):
