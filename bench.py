@@ -370,8 +370,8 @@ class GpuUpdate:
 # reported beside it.
 HEADLINE = 4
 ALSO_MEASURED = (1, 2, 3)
-# Nominal GB300 HBM3e bandwidth, for the second fraction next to the measured
-# copy peak (the 70% target is judged against the measured peak).
+# Nominal GB300 HBM3e bandwidth, for a second fraction next to the one
+# against the measured copy peak (roofline.frac).
 NOMINAL_HBM_GBS = 7900.0
 
 
@@ -517,7 +517,8 @@ def measure(u: "GpuUpdate", args, world_size: int, device, gpu_index: int) -> di
                      "algorithmic_bytes_per_launch": dk["bytes"],
                      "nominal": {"peak": NOMINAL_HBM_GBS, "frac": achieved / NOMINAL_HBM_GBS,
                                  "source": "nominal GB300 HBM3e bandwidth (7.9 TB/s)"},
-                     "target_basis": "the 70% target is judged against the measured copy peak (peak)"},
+                     "frac_basis": "frac is against the measured copy peak (peak); nominal.frac against "
+                                   "the nominal HBM bandwidth"},
         "kernels": kern,
         "per_update_ms": {"median": statistics.median(upd_total), "min": upd_total[0],
                           "max": upd_total[-1],
