@@ -342,6 +342,12 @@ def test_update_to_tensors_matches_update_then_gather(name):
         assert torch.equal(ref.master, run.master) and torch.equal(ref.params, run.params)
         for i, n in enumerate(c.numels):
             assert np.array_equal(views[i].cpu().numpy().view(np.uint16), want[i]), (name, i, "odd")
+        outside = torch.ones(big.numel(), dtype=torch.bool, device="cuda")
+        off = 3
+        for n in c.numels:
+            outside[off:off + n] = False
+            off += n + 1
+        assert bool((big[outside] == -1).all()), (name, "write between or around the tensors")
         # (2) per-tensor storage only; every other table entry NULL
         bare.reduce()
         bare.norm_sq()
