@@ -1,5 +1,6 @@
 /* A whole update driven through the C ABI from plain C: plan, reduce (two
- * microbatches), norm, clip + AdamW, gather; device memory from the CUDA
+ * microbatches), norm, clip + AdamW; the update writing per-tensor buffers;
+ * the update of every rank's shard view; device memory from the CUDA
  * runtime, no other framework.  Checked against the CPU oracle (linked
  * separately; test infrastructure) at the suite's tolerances.  Exit 0 on
  * success, 1 on a mismatch, 2 on an API error. */
@@ -137,6 +138,86 @@ int main(void) {
   }
   printf("c-abi update: %d buckets, %lld state elements, norm^2 %.9g (oracle %.9g): %s\n", nb, (long long)nsp, h_norm,
          s, bad ? "MISMATCH" : "ok");
+
+  /* The same update again from the initial state, with the bf16 parameters
+   * written straight into per-tensor buffers (no bucket-ordered copy): each
+   * tensor must hold, bit for bit, the bf16 values the first update wrote at
+   * its segments (tp rows concatenated for LOCAL_SHARD). */
+  uint16_t* h_params = (uint16_t*)malloc(sizeof(uint16_t) * nsp);
+  CUDA(cudaMemcpy(h_params, params, sizeof(uint16_t) * nsp, cudaMemcpyDeviceToHost));
+  CUDA(cudaMemcpy(master, master0, sizeof(float) * nsp, cudaMemcpyHostToDevice));
+  CUDA(cudaMemset(m, 0, sizeof(float) * nsp));
+  CUDA(cudaMemset(v, 0, sizeof(float) * nsp));
+  uint16_t* d_tensor[5];
+  for (int i = 0; i < n; ++i) CUDA(cudaMalloc((void**)&d_tensor[i], sizeof(uint16_t) * numels[i]));
+  uint16_t** d_table;
+  CUDA(cudaMalloc((void**)&d_table, sizeof(uint16_t*) * n));
+  CUDA(cudaMemcpy(d_table, d_tensor, sizeof(uint16_t*) * n, cudaMemcpyHostToDevice));
+  CHECK(grs_clip_adamw_step_to_tensors(plan, &hp, norm, acc, master, m, v, NULL, (uint16_t* const*)d_table, st));
+  CHECK(grs_check_device_errors(plan, st));
+  int bad_t = 0;
+  for (int b = 0; b < nb; ++b) {
+    grs_bucket_desc bd;
+    CHECK(grs_bucket_info(plan, b, &bd));
+    for (int i = 0; i < bd.n_segments; ++i) {
+      grs_segment_desc sd;
+      CHECK(grs_segment_info(plan, b, i, &sd));
+      uint16_t* got = (uint16_t*)malloc(sizeof(uint16_t) * (sd.numel ? sd.numel : 1));
+      CUDA(cudaMemcpy(got, d_tensor[sd.tensor] + sd.tensor_offset, sizeof(uint16_t) * sd.numel,
+                      cudaMemcpyDeviceToHost));
+      if (memcmp(got, h_params + sd.state_offset, sizeof(uint16_t) * sd.numel) != 0) ++bad_t;
+      free(got);
+    }
+  }
+  printf("c-abi update to tensors: %s\n", bad_t ? "MISMATCH" : "ok");
+
+  /* Shard views: every rank (s, t) of one replica, given its slices of the
+   * reduced gradient and of the initial state, updates its shard exactly as
+   * the plan's own update did (same S). */
+  float* h_master2 = (float*)malloc(sizeof(float) * nsp);
+  CUDA(cudaMemcpy(h_master2, master, sizeof(float) * nsp, cudaMemcpyDeviceToHost));
+  int bad_v = 0;
+  for (int t = 0; t < tp; ++t)
+    for (int sh = 0; sh < ds; ++sh) {
+      grs_plan* view = NULL;
+      CHECK(grs_plan_shard_view(plan, sh, t, &view));
+      grs_plan_info vi;
+      CHECK(grs_plan_query(view, &vi));
+      const int64_t nv = vi.n_state_pad > 0 ? vi.n_state_pad : 1;
+      float* h_acc_v = (float*)malloc(sizeof(float) * nv);
+      float* h_m0_v = (float*)malloc(sizeof(float) * nv);
+      float* want_v = (float*)malloc(sizeof(float) * nv);
+      for (int b = 0; b < nb; ++b) {
+        grs_bucket_desc pb, vb;
+        CHECK(grs_bucket_info(plan, b, &pb));
+        CHECK(grs_bucket_info(view, b, &vb));
+        const int row = pb.tag == GRS_LOCAL_SHARD ? t : 0;
+        const int64_t src = pb.state_offset + (int64_t)row * pb.padded + (int64_t)sh * pb.shard_len;
+        memcpy(h_acc_v + vb.state_offset, h_acc + src, sizeof(float) * vb.padded);
+        memcpy(h_m0_v + vb.state_offset, master0 + src, sizeof(float) * vb.padded);
+        memcpy(want_v + vb.state_offset, h_master2 + src, sizeof(float) * vb.padded);
+      }
+      float *acc_v, *master_v, *m_v, *v_v;
+      uint16_t* params_v;
+      CUDA(cudaMalloc((void**)&acc_v, sizeof(float) * nv));
+      CUDA(cudaMalloc((void**)&master_v, sizeof(float) * nv));
+      CUDA(cudaMalloc((void**)&m_v, sizeof(float) * nv));
+      CUDA(cudaMalloc((void**)&v_v, sizeof(float) * nv));
+      CUDA(cudaMalloc((void**)&params_v, sizeof(uint16_t) * nv));
+      CUDA(cudaMemcpy(acc_v, h_acc_v, sizeof(float) * vi.n_state_pad, cudaMemcpyHostToDevice));
+      CUDA(cudaMemcpy(master_v, h_m0_v, sizeof(float) * vi.n_state_pad, cudaMemcpyHostToDevice));
+      CUDA(cudaMemset(m_v, 0, sizeof(float) * nv));
+      CUDA(cudaMemset(v_v, 0, sizeof(float) * nv));
+      CHECK(grs_clip_adamw_step(view, &hp, norm, acc_v, master_v, m_v, v_v, params_v, st));
+      CHECK(grs_check_device_errors(view, st));
+      float* got_v = (float*)malloc(sizeof(float) * nv);
+      CUDA(cudaMemcpy(got_v, master_v, sizeof(float) * vi.n_state_pad, cudaMemcpyDeviceToHost));
+      if (memcmp(got_v, want_v, sizeof(float) * vi.n_state_pad) != 0) ++bad_v;
+      cudaFree(acc_v); cudaFree(master_v); cudaFree(m_v); cudaFree(v_v); cudaFree(params_v);
+      free(h_acc_v); free(h_m0_v); free(want_v); free(got_v);
+      grs_plan_destroy(view);
+    }
+  printf("c-abi shard views: %s\n", bad_v ? "MISMATCH" : "ok");
   grs_plan_destroy(plan);
-  return bad ? 1 : 0;
+  return (bad || bad_t || bad_v) ? 1 : 0;
 }

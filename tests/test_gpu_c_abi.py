@@ -28,4 +28,4 @@ def test_update_from_plain_c(tmp_path):
                            os.path.join(cuda, "lib64")])
     r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stdout + r.stderr
-    assert "ok" in r.stdout
+    assert r.stdout.count(": ok") == 3, r.stdout
