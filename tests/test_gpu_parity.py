@@ -288,7 +288,8 @@ def test_gather_matches_oracle():
 
 
 @pytest.mark.parametrize("name", ["tiny-world4", "odd-ds3-M3", "multi-tile-world16-M2", "tp4-world8",
-                                  "many-small-tensors", "zero-size-tensors", "fp32-grads-world8-M3"])
+                                  "many-small-tensors", "zero-size-tensors", "fp32-grads-world8-M3",
+                                  "world128-max", "world6-auto-shard"])
 def test_update_to_tensors_matches_update_then_gather(name):
     """grs_clip_adamw_step_to_tensors (the gather fused into the update):
     (1) with the bucket-ordered buffer as well: master, m, v and that buffer
@@ -399,7 +400,8 @@ def test_update_to_tensors_argument_errors():
         run.close()
 
 
-@pytest.mark.parametrize("name", ["tiny-world4", "odd-ds3-M3", "multi-tile-world16-M2", "tp4-world8", "world1"])
+@pytest.mark.parametrize("name", ["tiny-world4", "odd-ds3-M3", "multi-tile-world16-M2", "tp4-world8", "world1",
+                                  "world128-max", "world64-tp4-M2", "zero-size-tensors", "fp32-grads-world16"])
 def test_shard_views_reproduce_the_plan_update(name):
     """Each rank's shard view (grs_plan_shard_view) given that rank's slices
     of the reduced gradient and of the state: the squared norms of the views
