@@ -806,17 +806,21 @@ def run_e2e(u: GpuUpdate, args, torch):
                                  u.params.data_ptr(), u.ws.data_ptr(), u.norm.data_ptr(),
                                  out_params.data_ptr() if read_params else None, out_norm.data_ptr(), u.stream)
 
-    def timed(read_params: bool) -> float:
+    def timed(read_params: bool):
+        """Mean ms per step over the bracketed loop, and each step's interval
+        (event after each call on the same stream; the first interval holds
+        the pipeline fill, as the first step's copies overlap nothing)."""
         one(read_params)
         torch.cuda.synchronize()
-        s = torch.cuda.Event(enable_timing=True)
-        e = torch.cuda.Event(enable_timing=True)
-        s.record()
-        for _ in range(steps):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        evs[0].record()
+        for i in range(steps):
             one(read_params)
-        e.record()
+            evs[i + 1].record()
         torch.cuda.synchronize()
-        return s.elapsed_time(e) / steps
+        per = sorted(evs[i].elapsed_time(evs[i + 1]) for i in range(steps))
+        return evs[0].elapsed_time(evs[-1]) / steps, {"median": per[len(per) // 2], "min": per[0],
+                                                      "max": per[-1]}
 
     # The host link on this box, for scale: one pinned 1 GiB copy each way
     # (host-to-device also before the timed loops; the host link is shared
@@ -838,8 +842,8 @@ def run_e2e(u: GpuUpdate, args, torch):
     h2d_before = 2 * nb / (copy_ms(lambda: dbuf.copy_(hsrc, non_blocking=True)) * 1e-3) / 1e9
     # The step's result read back every step: the updated bf16 parameters
     # and the squared global norm; as a second figure, the norm alone.
-    ms_params = timed(True)
-    ms = timed(False)
+    ms_params, per_params = timed(True)
+    ms, per_norm = timed(False)
     link = {"h2d_gbs": 2 * nb / (copy_ms(lambda: dbuf.copy_(hsrc, non_blocking=True)) * 1e-3) / 1e9,
             "d2h_gbs": 2 * nb / (copy_ms(lambda: hsrc.copy_(dbuf, non_blocking=True)) * 1e-3) / 1e9,
             "h2d_gbs_before": h2d_before,
@@ -849,11 +853,12 @@ def run_e2e(u: GpuUpdate, args, torch):
     del stage
     return {"value": ms_params, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "h2d_gbs": h2d / (ms_params * 1e-3) / 1e9, "steps": steps,
+            "per_step_ms": per_params,
             "setup_s": t_setup,
             "path": "grs_step_from_host: pinned host gradients, per-bucket H2D overlapped with the "
                     "reductions; the bf16 parameters and the squared global norm read back every step",
             "norm_read_back_only": {"value": ms, "unit": UNIT, "d2h_bytes_per_step": 8,
-                                    "h2d_gbs": h2d / (ms * 1e-3) / 1e9},
+                                    "h2d_gbs": h2d / (ms * 1e-3) / 1e9, "per_step_ms": per_norm},
             "link": link,
             "link_bound_ms": (h2d / link["h2d_gbs"] + (d2h - 8) / link["d2h_gbs"]) / 1e6
             if link["h2d_gbs"] > 0 and link["d2h_gbs"] > 0 else None}
