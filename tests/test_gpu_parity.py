@@ -400,71 +400,112 @@ def test_update_to_tensors_argument_errors():
         run.close()
 
 
+def check_shard_views(run, c, master0, m0, v0, label):
+    """Each rank's shard view (grs_plan_shard_view) given that rank's slices
+    of the plan's reduced gradient and of the state before the update
+    (device tensors master0, m0, v0; `run` has taken its one update): the
+    squared norms of the views of one replica add up to the plan's S (the
+    one scalar all-reduce), and clip + AdamW + bf16 on each view with that S
+    equals the plan's own update restricted to the rank's elements, bit for
+    bit -- so an all-gather of the views' bf16 shards gives the plan's
+    parameters ("Cosmos 3 ... distributed parallelism", section 2).  A view
+    refuses the reductions."""
+    g = grs()
+    full = {k: getattr(run, k)[:run.nsp] for k in ("acc", "master", "m", "v", "params")}
+    info = run.info
+    bks = [g.grs_bucket_info(run.plan, b) for b in range(info["n_buckets"])]
+    s_sum = 0.0
+    hp = g.make_adamw(c.hp[0], c.hp[1], c.hp[2], c.hp[3], c.hp[4], c.max_norm, 1, c.n_micro)
+    for t in range(c.tp):
+        for s in range(info["dp_shard"]):
+            view = g.grs_plan_shard_view(run.plan, s, t)
+            try:
+                vi = g.grs_plan_query(view)
+                idx = []
+                for pb in bks:
+                    row = t if pb["tag"] == LS else 0
+                    L = int(pb["shard_len"])
+                    base = int(pb["state_offset"]) + row * int(pb["padded"]) + s * L
+                    idx.append(torch.arange(base, base + L, device="cuda"))
+                idx = torch.cat(idx) if idx else torch.zeros(0, dtype=torch.int64, device="cuda")
+                assert idx.numel() == vi["n_state_pad"]
+                n = max(8, idx.numel())
+                acc_v = torch.zeros(n, device="cuda")
+                acc_v[:idx.numel()] = full["acc"][idx]
+                st = [torch.zeros(n, device="cuda") for _ in range(3)]
+                for x, src in zip(st, (master0, m0, v0)):
+                    x[:idx.numel()] = src[idx]
+                params_v = torch.full((n,), -1, dtype=torch.int16, device="cuda")
+                ws = torch.zeros(max(vi["workspace_bytes"], 16) // 4 + 4, device="cuda")
+                nv = torch.zeros(1, dtype=torch.float64, device="cuda")
+                g.grs_grad_norm_sq(view, acc_v.data_ptr(), c.n_micro, ws.data_ptr(), 0, nv.data_ptr(), run.stream())
+                g.grs_clip_adamw_step(view, hp, run.norm.data_ptr(), acc_v.data_ptr(), st[0].data_ptr(),
+                                      st[1].data_ptr(), st[2].data_ptr(), params_v.data_ptr(), run.stream())
+                torch.cuda.synchronize()
+                assert g.grs_check_device_errors(view, run.stream()) == 0
+                k = idx.numel()
+                for x, nm in zip(st, ("master", "m", "v")):
+                    assert torch.equal(x[:k], full[nm][idx]), (label, s, t, nm)
+                assert torch.equal(params_v[:k], full["params"][idx]), (label, s, t, "params")
+                s_sum += float(nv.cpu()[0])
+                with pytest.raises(g.GrsError) as ei:
+                    g.grs_reduce_all(view, run.ptrs(0), acc_v.data_ptr(), 0, 0, ws.data_ptr(), run.stream())
+                assert ei.value.status == g.GRS_ERR_UNSUPPORTED_COMPOSITION
+                with pytest.raises(g.GrsError) as ei:
+                    g.grs_grad_norm_sq(view, acc_v.data_ptr(), c.n_micro, ws.data_ptr(), 1, nv.data_ptr(),
+                                       run.stream())
+                assert ei.value.status == g.GRS_ERR_UNSUPPORTED_COMPOSITION
+            finally:
+                g.grs_plan_destroy(view)
+    want = float(run.norm.cpu()[0])
+    assert abs(s_sum - want) <= 1e-5 * want, (label, s_sum, want)
+
+
+def check_update_to_tensors(c, label):
+    """grs_clip_adamw_step_to_tensors with per-tensor storage only (no
+    bucket-ordered buffer) after the plain reduction and norm: master, m and
+    v equal grs_clip_adamw_step's bit for bit, every tensor equals
+    oracle.gather_tensor of that update's bucket-ordered buffer bit for bit,
+    and frozen tensors (not in the plan) are left untouched."""
+    g = grs()
+    ref, run = Run(c), Run(c)
+    try:
+        ref.update()
+        run.reduce()
+        run.norm_sq()
+        outs = [torch.full((max(n, 1),), -1, dtype=torch.int16, device="cuda") for n in c.numels]
+        table = torch.tensor([t.data_ptr() for t in outs], dtype=torch.int64, device="cuda")
+        hp = g.make_adamw(c.hp[0], c.hp[1], c.hp[2], c.hp[3], c.hp[4], c.max_norm, 1, c.n_micro)
+        g.grs_clip_adamw_step_to_tensors(run.plan, hp, run.norm.data_ptr(), run.acc.data_ptr(),
+                                         run.master.data_ptr(), run.m.data_ptr(), run.v.data_ptr(),
+                                         None, table.data_ptr(), run.stream())
+        torch.cuda.synchronize()
+        assert run.check_flags() == 0
+        for nm in ("master", "m", "v"):
+            assert torch.equal(getattr(ref, nm)[:ref.nsp], getattr(run, nm)[:run.nsp]), (label, nm)
+        params = ref.params[:ref.nsp].cpu().numpy().view(np.uint16)
+        for i, n in enumerate(c.numels):
+            got = outs[i][:n].cpu().numpy().view(np.uint16)
+            if int(ref.op.t_bucket[i]) < 0:
+                assert np.all(got == 0xFFFF), (label, i, "frozen tensor written")
+            else:
+                assert np.array_equal(got, oracle.gather_tensor(ref.op, i, params)), (label, i)
+    finally:
+        ref.close()
+        run.close()
+
+
 @pytest.mark.parametrize("name", ["tiny-world4", "odd-ds3-M3", "multi-tile-world16-M2", "tp4-world8", "world1",
                                   "world128-max", "world64-tp4-M2", "zero-size-tensors", "fp32-grads-world16"])
 def test_shard_views_reproduce_the_plan_update(name):
-    """Each rank's shard view (grs_plan_shard_view) given that rank's slices
-    of the reduced gradient and of the state: the squared norms of the views
-    of one replica add up to the plan's S (the one scalar all-reduce), and
-    clip + AdamW + bf16 on each view with that S equals the plan's own update
-    restricted to the rank's elements, bit for bit — so an all-gather of the
-    views' bf16 shards gives the plan's parameters ("Cosmos 3 ... distributed
-    parallelism", section 2).  A view refuses the reductions."""
-    g = grs()
+    """check_shard_views on the named plans."""
     c = SMALL[name]
     run = Run(c)
     try:
         master0, m0, v0 = (torch.from_numpy(x).cuda() for x in run.state_host())
         run.update()
         torch.cuda.synchronize()
-        full = {k: getattr(run, k)[:run.nsp] for k in ("acc", "master", "m", "v", "params")}
-        info = run.info
-        bks = [g.grs_bucket_info(run.plan, b) for b in range(info["n_buckets"])]
-        s_sum = 0.0
-        hp = g.make_adamw(c.hp[0], c.hp[1], c.hp[2], c.hp[3], c.hp[4], c.max_norm, 1, c.n_micro)
-        for t in range(c.tp):
-            for s in range(info["dp_shard"]):
-                view = g.grs_plan_shard_view(run.plan, s, t)
-                try:
-                    vi = g.grs_plan_query(view)
-                    idx = []
-                    for pb in bks:
-                        row = t if pb["tag"] == LS else 0
-                        L = int(pb["shard_len"])
-                        base = int(pb["state_offset"]) + row * int(pb["padded"]) + s * L
-                        idx.append(torch.arange(base, base + L, device="cuda"))
-                    idx = torch.cat(idx) if idx else torch.zeros(0, dtype=torch.int64, device="cuda")
-                    assert idx.numel() == vi["n_state_pad"]
-                    n = max(8, idx.numel())
-                    acc_v = torch.zeros(n, device="cuda")
-                    acc_v[:idx.numel()] = full["acc"][idx]
-                    st = [torch.zeros(n, device="cuda") for _ in range(3)]
-                    for x, src in zip(st, (master0, m0, v0)):
-                        x[:idx.numel()] = src[idx]
-                    params_v = torch.full((n,), -1, dtype=torch.int16, device="cuda")
-                    ws = torch.zeros(max(vi["workspace_bytes"], 16) // 4 + 4, device="cuda")
-                    nv = torch.zeros(1, dtype=torch.float64, device="cuda")
-                    g.grs_grad_norm_sq(view, acc_v.data_ptr(), c.n_micro, ws.data_ptr(), 0, nv.data_ptr(), run.stream())
-                    g.grs_clip_adamw_step(view, hp, run.norm.data_ptr(), acc_v.data_ptr(), st[0].data_ptr(),
-                                          st[1].data_ptr(), st[2].data_ptr(), params_v.data_ptr(), run.stream())
-                    torch.cuda.synchronize()
-                    assert g.grs_check_device_errors(view, run.stream()) == 0
-                    k = idx.numel()
-                    for x, nm in zip(st, ("master", "m", "v")):
-                        assert torch.equal(x[:k], full[nm][idx]), (name, s, t, nm)
-                    assert torch.equal(params_v[:k], full["params"][idx]), (name, s, t, "params")
-                    s_sum += float(nv.cpu()[0])
-                    with pytest.raises(g.GrsError) as ei:
-                        g.grs_reduce_all(view, run.ptrs(0), acc_v.data_ptr(), 0, 0, ws.data_ptr(), run.stream())
-                    assert ei.value.status == g.GRS_ERR_UNSUPPORTED_COMPOSITION
-                    with pytest.raises(g.GrsError) as ei:
-                        g.grs_grad_norm_sq(view, acc_v.data_ptr(), c.n_micro, ws.data_ptr(), 1, nv.data_ptr(),
-                                           run.stream())
-                    assert ei.value.status == g.GRS_ERR_UNSUPPORTED_COMPOSITION
-                finally:
-                    g.grs_plan_destroy(view)
-        want = float(run.norm.cpu()[0])
-        assert abs(s_sum - want) <= 1e-5 * want, (s_sum, want)
+        check_shard_views(run, c, master0, m0, v0, name)
     finally:
         run.close()
 
@@ -822,10 +863,12 @@ def random_case(rng, trial):
 
 @pytest.mark.parametrize("trial", range(16))
 def test_random_small_plans_match_oracle(trial):
-    """Random plans (random_case): one plain update against the oracle; the
-    masked reduction, norm and update with a random mask against the oracle's
-    masked update; and the single-launch update against the plain one, bit
-    for bit, where its limits allow."""
+    """Random plans (random_case): one plain update against the oracle, every
+    rank's shard view against it (check_shard_views) and the update writing
+    per-tensor storage (check_update_to_tensors); the masked reduction, norm
+    and update with a random mask against the oracle's masked update; and
+    the single-launch update against the plain one, bit for bit, where its
+    limits allow."""
     rng = np.random.default_rng(7000 + trial)
     c = random_case(rng, trial)
     g = grs()
@@ -836,8 +879,10 @@ def test_random_small_plans_match_oracle(trial):
         run.update()
         res = oracle_update(run, master0, m0, v0, step=1)
         full_check(run, res, f"random {trial} plain")
+        check_shard_views(run, c, *(torch.from_numpy(x).cuda() for x in (master0, m0, v0)), f"random {trial}")
     finally:
         run.close()
+    check_update_to_tensors(c, f"random {trial}")
     n = len(c.numels)
     used = [int(x) for x in (rng.random(n) < 0.7)]
     mrun = Run(c)
@@ -885,7 +930,8 @@ def test_random_small_plans_match_oracle(trial):
 def test_random_medium_plans_match_oracle(trial):
     """Random plans of up to 300k-element tensors (many tiles per bucket
     row, every tag, bf16 or fp32 gradients, 1..3 microbatches, degrees up to
-    tp 4 x dp_replicate 2 x dp_shard 8): one update against the oracle.
+    tp 4 x dp_replicate 2 x dp_shard 8): one update against the oracle, with
+    the shard views and the per-tensor write checked as on the small plans.
     Seed 10 meets an ill-conditioned AdamW point (fp32 gradients cancelling
     across microbatches to 1.7e-9), where the check follows the bracket."""
     rng = np.random.default_rng(90000 + trial)
@@ -905,8 +951,10 @@ def test_random_medium_plans_match_oracle(trial):
         run.update()
         res = oracle_update(run, master0, m0, v0, step=1)
         full_check(run, res, f"medium {trial}")
+        check_shard_views(run, c, *(torch.from_numpy(x).cuda() for x in (master0, m0, v0)), f"medium {trial}")
     finally:
         run.close()
+    check_update_to_tensors(c, f"medium {trial}")
 
 
 def test_masked_reduction_skips_tiles_of_unused_tensors():
