@@ -593,6 +593,8 @@ def run_gpu(args, rank, world_size, local_rank):
         "clocks": r["clocks"],
         "device_status": status,
     }
+    if plain and w.cid in PAGES_CONTEXT and not (args.layers or args.blocks or args.micro or args.window):
+        result["pages_context"] = PAGES_CONTEXT[w.cid]
     if rank == 0 and world_size == 1 and not args.no_cpu_baseline:
         if plain:
             result["cpu_baseline"] = cpu_baseline(w, mb, args, u)
@@ -624,9 +626,21 @@ def run_gpu(args, rank, world_size, local_rank):
                             for k, v in r["kernels"].items()},
                 "config": cfg,
                 "clocks": r["clocks"], "device_status": st, "steps": args.steps}
+            if cid in PAGES_CONTEXT:
+                others[wo.name]["pages_context"] = PAGES_CONTEXT[cid]
     if others:
         result["configs"] = others
     return result
+
+
+# The one timing of this path that the sources print: a synthetic
+# 67M-parameter "draft" benchmark ("refactor(distributed): establish shared
+# native TP replica ownership", Preserved prototype and evidence), two
+# variants whose names and hardware are not given.  Reported beside the
+# 67M plan as context only.
+PAGES_CONTEXT = {1: {"ms_per_update": [3.255, 2.624],
+                     "note": "the sources' synthetic 67M draft benchmark; hardware, rank count and which "
+                             "figure is which variant not stated: context, not a target"}}
 
 
 def arm_config(w, u, world_size: int, flush: bool) -> dict:
