@@ -5,11 +5,12 @@ grs_clip_adamw_step).
 
 Every element of each workload's update is compared with the oracle (the
 67M plan in one piece, the larger ones bucket row by bucket row in chunks on
-the host's cores); the variants (fp32 gradients, tensors without a
-gradient, frozen tensors, a trailing window) compare the exact global norm
-over every element and the clipped AdamW update at sampled elements of every
-bucket row: random interior points, the first and last valid elements, tile
-edges and padding.
+the host's cores), and so is every element of the measured variants (fp32
+gradients, tensors without a gradient, frozen tensors, a trailing window).
+The one tensor past 32-bit indices is checked at sampled elements: random
+interior points, the first and last valid elements, tile edges and padding.
+The host-buffer call the bench's end-to-end figure times is checked against
+the device-resident path on the 3.2B plan, bit for bit.
 """
 import os
 import threading
@@ -469,3 +470,78 @@ def _full_size_w(w, variant, window):
         u.close()
         del u
         torch.cuda.empty_cache()
+
+
+def _host_available_gb():
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024 / 1e9
+    except OSError:
+        pass
+    return 0.0
+
+
+def test_step_from_host_full_size_equals_device_path():
+    """grs_step_from_host on the 3.2B plan, as the bench's end-to-end leg
+    calls it (pinned host gradients copied in bucket by bucket on the plan's
+    copy stream, each bucket reduced when its copy lands; the bf16
+    parameters and the norm read back to pinned host memory), two calls
+    queued back to back (the second's copies overlap the first's update),
+    against two steps of the device-resident path (bench.GpuUpdate: one
+    grouped reduction, the finish, the update) on the same gradients and
+    initial state: each call's host copies of the parameters and the norm
+    equal that step's device values, and after the second call the
+    accumulator, norm, master, m, v and bf16 parameters are equal bit for
+    bit.  The device path itself is checked against the oracle element by
+    element above."""
+    import bench
+    from gradient_reduction_sharded_gb300 import grs as g
+
+    w = workloads.get(4)
+    if _free_gb() < 190 or _host_available_gb() < 70:
+        pytest.skip(f"needs ~170 GB of device and ~45 GB of host memory "
+                    f"({_free_gb():.0f} GB, {_host_available_gb():.0f} GB available)")
+    dev = torch.device("cuda")
+    u = bench.GpuUpdate(w, dev)
+    try:
+        W, nrp, nsp = w.world, u.info["n_rank_pad"], u.info["n_state_pad"]
+        # the host path's own state, from the same initial values
+        acc = torch.empty(nsp, dtype=torch.float32, device=dev)
+        master, m, v = u.master.clone(), u.m.clone(), u.v.clone()
+        params = torch.empty(nsp, dtype=torch.int16, device=dev)
+        ws = torch.zeros_like(u.ws)
+        norm = torch.zeros(1, dtype=torch.float64, device=dev)
+        host = [torch.empty(nrp, dtype=torch.int16, pin_memory=True) for _ in range(W)]
+        for k in range(W):
+            host[k].copy_(u.grads[0][k].view(torch.int16))
+        stage = [torch.empty(nrp, dtype=torch.int16, device=dev) for _ in range(W)]
+        stage_ptrs = [t.data_ptr() for t in stage] * 2  # one microbatch: one staging half
+        out_params = [torch.empty(nsp, dtype=torch.int16, pin_memory=True) for _ in range(2)]
+        out_norm = [torch.empty(1, dtype=torch.float64, pin_memory=True) for _ in range(2)]
+        # the device path: step 1 (kept on the host), then step 2
+        u.step()
+        torch.cuda.synchronize()
+        want1_params, want1_norm = u.params[:nsp].cpu(), float(u.norm.cpu()[0])
+        u.step()
+        torch.cuda.synchronize()
+        # the host path: both calls queued without a synchronisation
+        a = w.adamw
+        for step in (1, 2):
+            hp = g.make_adamw(a.lr, a.beta1, a.beta2, a.eps, a.weight_decay, a.max_norm, step, 1)
+            g.grs_step_from_host(u.plan, hp, [t.data_ptr() for t in host], stage_ptrs, acc.data_ptr(),
+                                 master.data_ptr(), m.data_ptr(), v.data_ptr(), params.data_ptr(),
+                                 ws.data_ptr(), norm.data_ptr(), out_params[step - 1].data_ptr(),
+                                 out_norm[step - 1].data_ptr(), u.stream)
+        torch.cuda.synchronize()
+        assert g.grs_check_device_errors(u.plan, u.stream) == 0
+        assert torch.equal(out_params[0], want1_params), "step 1 host params"
+        assert float(out_norm[0][0]) == want1_norm, "step 1 host norm"
+        for nm, got in (("acc", acc), ("norm", norm), ("master", master), ("m", m), ("v", v),
+                        ("params", params)):
+            assert torch.equal(got[:nsp], getattr(u, nm)[:nsp]), f"step 2 {nm}"
+        assert torch.equal(out_params[1], u.params[:nsp].cpu()), "step 2 host params"
+        assert float(out_norm[1][0]) == float(u.norm.cpu()[0]), "step 2 host norm"
+    finally:
+        u.close()
