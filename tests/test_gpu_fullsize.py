@@ -545,3 +545,51 @@ def test_step_from_host_full_size_equals_device_path():
         assert float(out_norm[1][0]) == float(u.norm.cpu()[0]), "step 2 host norm"
     finally:
         u.close()
+
+
+def test_update_to_tensors_full_size_matches_gather():
+    """grs_clip_adamw_step_to_tensors on the 3.2B plan (254 tensors, 142
+    buckets; the bench times it beside the plain update): from the same
+    reduced gradient and state, master, m and v equal the plain update's
+    bit for bit and every tensor written by the update equals
+    oracle.gather_tensor of the plain update's bucket-ordered parameters,
+    bit for bit."""
+    import bench
+    from gradient_reduction_sharded_gb300 import grs as g
+
+    w = workloads.get(4)
+    if _free_gb() < 180 or _host_available_gb() < 30:
+        pytest.skip(f"needs ~165 GB of device and ~15 GB of host memory "
+                    f"({_free_gb():.0f} GB, {_host_available_gb():.0f} GB available)")
+    dev = torch.device("cuda")
+    op = oracle.plan(w.numels, w.owners, w.world, w.tp, w.dp_replicate, w.dp_shard, w.bucket_bytes)
+    u = bench.GpuUpdate(w, dev)
+    try:
+        nsp = u.info["n_state_pad"]
+        assert nsp == op.n_state_pad
+        u.reduce()
+        u.norm_sq()
+        saved = [u.master.clone(), u.m.clone(), u.v.clone()]
+        u.adamw()  # the plain update, step 1
+        torch.cuda.synchronize()
+        plain = [u.master.clone(), u.m.clone(), u.v.clone()]
+        params_ref = u.params[:nsp].cpu().numpy().view(np.uint16)
+        for x, s0 in zip((u.master, u.m, u.v), saved):
+            x.copy_(s0)
+        del saved
+        outs = [torch.full((max(n, 1),), -1, dtype=torch.int16, device=dev) for n in w.numels]
+        table = torch.tensor([t.data_ptr() for t in outs], dtype=torch.int64, device=dev)
+        a = w.adamw
+        hp = g.make_adamw(a.lr, a.beta1, a.beta2, a.eps, a.weight_decay, a.max_norm, 1, w.n_micro)
+        g.grs_clip_adamw_step_to_tensors(u.plan, hp, u.norm.data_ptr(), u.acc.data_ptr(), u.master.data_ptr(),
+                                         u.m.data_ptr(), u.v.data_ptr(), None, table.data_ptr(), u.stream)
+        torch.cuda.synchronize()
+        assert g.grs_check_device_errors(u.plan, u.stream) == 0
+        for nm, x, y in zip(("master", "m", "v"), (u.master, u.m, u.v), plain):
+            assert torch.equal(x, y), nm
+        del plain
+        for i, n in enumerate(w.numels):
+            got = outs[i][:n].cpu().numpy().view(np.uint16)
+            assert np.array_equal(got, oracle.gather_tensor(op, i, params_ref)), (w.name, i)
+    finally:
+        u.close()
