@@ -553,13 +553,14 @@ def test_update_to_tensors_full_size_matches_gather():
     reduced gradient and state, master, m and v equal the plain update's
     bit for bit and every tensor written by the update equals
     oracle.gather_tensor of the plain update's bucket-ordered parameters,
-    bit for bit."""
+    bit for bit; so does every tensor of the separate gather pass
+    (grs_gather_params) from those parameters."""
     import bench
     from gradient_reduction_sharded_gb300 import grs as g
 
     w = workloads.get(4)
-    if _free_gb() < 180 or _host_available_gb() < 30:
-        pytest.skip(f"needs ~165 GB of device and ~15 GB of host memory "
+    if _free_gb() < 185 or _host_available_gb() < 30:
+        pytest.skip(f"needs ~170 GB of device and ~15 GB of host memory "
                     f"({_free_gb():.0f} GB, {_host_available_gb():.0f} GB available)")
     dev = torch.device("cuda")
     op = oracle.plan(w.numels, w.owners, w.world, w.tp, w.dp_replicate, w.dp_shard, w.bucket_bytes)
@@ -574,6 +575,9 @@ def test_update_to_tensors_full_size_matches_gather():
         torch.cuda.synchronize()
         plain = [u.master.clone(), u.m.clone(), u.v.clone()]
         params_ref = u.params[:nsp].cpu().numpy().view(np.uint16)
+        # the separate gather pass from the same bucket-ordered parameters
+        gathered = [torch.full((max(n, 1),), -1, dtype=torch.int16, device=dev) for n in w.numels]
+        g.grs_gather_params(u.plan, u.params.data_ptr(), [t.data_ptr() for t in gathered], u.stream)
         for x, s0 in zip((u.master, u.m, u.v), saved):
             x.copy_(s0)
         del saved
@@ -589,7 +593,8 @@ def test_update_to_tensors_full_size_matches_gather():
             assert torch.equal(x, y), nm
         del plain
         for i, n in enumerate(w.numels):
-            got = outs[i][:n].cpu().numpy().view(np.uint16)
-            assert np.array_equal(got, oracle.gather_tensor(op, i, params_ref)), (w.name, i)
+            want = oracle.gather_tensor(op, i, params_ref)
+            assert np.array_equal(outs[i][:n].cpu().numpy().view(np.uint16), want), (w.name, i)
+            assert np.array_equal(gathered[i][:n].cpu().numpy().view(np.uint16), want), (w.name, i, "gather")
     finally:
         u.close()
