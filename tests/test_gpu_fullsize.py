@@ -598,3 +598,80 @@ def test_update_to_tensors_full_size_matches_gather():
             assert np.array_equal(gathered[i][:n].cpu().numpy().view(np.uint16), want), (w.name, i, "gather")
     finally:
         u.close()
+
+
+def test_reshard_full_size_matches_oracle():
+    """The bench's checkpoint row on the 67M plan: state written under the
+    plan's geometry (tp 2, dp_replicate 2, dp_shard 4), moved to the
+    canonical logical order (grs_state_to_logical) and into the reader's
+    geometry (bench.reshard_geometry: dp_shard over all data ranks) with
+    grs_state_from_logical; both results equal the oracle's own layout
+    conversions element for element, bit for bit (padding zeros
+    included)."""
+    import bench
+    from gradient_reduction_sharded_gb300 import grs as g
+
+    w = workloads.get(1)
+    tp, dr, ds = bench.reshard_geometry(w)
+    assert (tp, dr, ds) != (w.tp, w.dp_replicate, w.dp_shard)
+    ow = oracle.plan(w.numels, w.owners, w.world, w.tp, w.dp_replicate, w.dp_shard, w.bucket_bytes)
+    orr = oracle.plan(w.numels, w.owners, w.world, tp, dr, ds, w.bucket_bytes)
+    pw = g.grs_plan_create(w.numels, w.owners, w.world, w.tp, w.dp_replicate, w.dp_shard, w.bucket_bytes)
+    pr = g.grs_plan_create(w.numels, w.owners, w.world, tp, dr, ds, w.bucket_bytes)
+    try:
+        iw, ir = g.grs_plan_query(pw), g.grs_plan_query(pr)
+        assert iw["n_state_pad"] == ow.n_state_pad and ir["n_state_pad"] == orr.n_state_pad
+        s = torch.cuda.current_stream().cuda_stream
+        gen = torch.Generator(device="cuda").manual_seed(17)
+        src = torch.randn(iw["n_state_pad"], generator=gen, device="cuda")
+        lg = torch.empty(iw["n_unique"], device="cuda")
+        dst = torch.full((ir["n_state_pad"],), float("nan"), device="cuda")
+        g.grs_state_to_logical(pw, src.data_ptr(), lg.data_ptr(), s)
+        g.grs_state_from_logical(pr, lg.data_ptr(), dst.data_ptr(), s)
+        torch.cuda.synchronize()
+        assert g.grs_check_device_errors(pw, s) == 0 and g.grs_check_device_errors(pr, s) == 0
+        want_lg = oracle.to_logical(ow, src.cpu().numpy())
+        assert np.array_equal(lg.cpu().numpy(), want_lg)
+        assert np.array_equal(dst.cpu().numpy(), oracle.from_logical(orr, want_lg))
+    finally:
+        g.grs_plan_destroy(pw)
+        g.grs_plan_destroy(pr)
+
+
+def test_accumulate_full_size_matches_fp32_addition():
+    """grs_accumulate over every bucket of the 3.2B plan (the entry point
+    whose 142 launches the bench times): each accumulator element becomes
+    the IEEE fp32 sum of its old value and the reduced microbatch's (numpy
+    float32 addition, round to nearest even), padding exactly zero; bucket
+    rows compared whole, one at a time."""
+    from gradient_reduction_sharded_gb300 import grs as g
+
+    w = workloads.get(4)
+    plan = g.grs_plan_create(w.numels, w.owners, w.world, w.tp, w.dp_replicate, w.dp_shard, w.bucket_bytes)
+    try:
+        info = g.grs_plan_query(plan)
+        nsp = info["n_state_pad"]
+        if _free_gb() < 3 * nsp * 4 / 1e9 + 8:
+            pytest.skip("needs about 47 GB of device memory")
+        s = torch.cuda.current_stream().cuda_stream
+        gen = torch.Generator(device="cuda").manual_seed(23)
+        acc = torch.randn(nsp, generator=gen, device="cuda")
+        mb = torch.randn(nsp, generator=gen, device="cuda")
+        before = acc.clone()
+        buckets = [g.grs_bucket_info(plan, b) for b in range(info["n_buckets"])]
+        for b, d in enumerate(buckets):
+            lo = int(d["state_offset"])
+            g.grs_accumulate(plan, b, acc.data_ptr() + 4 * lo, mb.data_ptr() + 4 * lo, s)
+        torch.cuda.synchronize()
+        assert g.grs_check_device_errors(plan, s) == 0
+        for d in buckets:
+            lo, P, used = int(d["state_offset"]), int(d["padded"]), int(d["used"])
+            for r in range(int(d["copies"])):
+                a0 = lo + r * P
+                x = before[a0:a0 + P].cpu().numpy()
+                y = mb[a0:a0 + P].cpu().numpy()
+                want = np.add(x, y, dtype=np.float32)
+                want[used:] = 0.0
+                assert np.array_equal(acc[a0:a0 + P].cpu().numpy(), want), (d, r)
+    finally:
+        g.grs_plan_destroy(plan)
