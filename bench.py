@@ -621,7 +621,8 @@ def run_gpu(args, rank, world_size, local_rank):
                 "ms_per_update": job_value(r["ms_per_step"], world_size),
                 "ms_per_step": r["ms_per_step"], "mandatory_bytes": r["mb"]["total"],
                 "gbs": r["achieved_gbs_total"], "step_frac": r["step_frac"],
-                "roofline": {k: r["roofline"][k] for k in ("kernel", "achieved", "peak", "frac", "traffic")},
+                "roofline": {k: r["roofline"][k] for k in ("kernel", "achieved", "peak", "frac", "traffic", "nominal")
+                             if k in r["roofline"]},
                 "kernels": {k: {"ms_per_launch": v["ms_per_launch"], "launches_per_step": v["launches_per_step"]}
                             for k, v in r["kernels"].items()},
                 "config": cfg,
