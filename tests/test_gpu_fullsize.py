@@ -37,6 +37,16 @@ def _cuda():
     torch.cuda.init()
 
 
+@pytest.fixture(autouse=True)
+def _release_memory():
+    """Each test here holds tens to hundreds of GB: hand the cached blocks
+    back after it, so the next one sees the device's free memory."""
+    yield
+    import gc
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
 def _free_gb():
     free, _ = torch.cuda.mem_get_info()
     return free / 1e9
