@@ -210,50 +210,83 @@ def _host_plan(grs, w):
                                grs.GRS_PLAN_HOST_ONLY)
 
 
-@pytest.mark.parametrize("cid", [0, 1, 3, 4])
-def test_shard_views_partition_the_plan(grs, cid):
+def _check_shard_views(grs, plan, tp):
     """The shard views of one replica, (shard s, tp index t) for every s and
     t: each bucket's slice is shard_len elements of row t (LOCAL_SHARD) or
     row 0, with the valid elements of [s * shard_len, (s + 1) * shard_len);
     the views' norm-counted elements add up to the plan's unique elements
     (each counted once: LOCAL_SHARD rows by their own tp index, the other
-    rows by tp index 0 only)."""
-    w = workloads.get(cid)
-    plan = _host_plan(grs, w)
-    try:
-        info = grs.grs_plan_query(plan)
-        nb = info["n_buckets"]
-        bks = [grs.grs_bucket_info(plan, b) for b in range(nb)]
-        total_unique = 0
-        for t in range(w.tp):
-            for s in range(info["dp_shard"]):
-                v = grs.grs_plan_shard_view(plan, s, t)
-                try:
-                    vi = grs.grs_plan_query(v)
-                    assert vi["n_buckets"] == nb and vi["n_rank_pad"] == 0 and vi["device"] == -1
-                    assert vi["n_state_pad"] == sum(int(b["shard_len"]) for b in bks)
-                    off = 0
-                    for b, pb in enumerate(bks):
-                        vb = grs.grs_bucket_info(v, b)
-                        L = int(pb["shard_len"])
-                        used = max(0, min(L, int(pb["used"]) - s * L))
-                        assert (vb["copies"], vb["padded"], vb["shard_len"], vb["used"], vb["state_offset"]) == \
-                            (1, L, L, used, off)
-                        assert vb["tag"] == pb["tag"]
-                        off += L
-                    total_unique += vi["n_unique"]
+    rows by tp index 0 only); out-of-range indices and views of views are
+    refused."""
+    info = grs.grs_plan_query(plan)
+    nb = info["n_buckets"]
+    bks = [grs.grs_bucket_info(plan, b) for b in range(nb)]
+    total_unique = 0
+    for t in range(tp):
+        for s in range(info["dp_shard"]):
+            v = grs.grs_plan_shard_view(plan, s, t)
+            try:
+                vi = grs.grs_plan_query(v)
+                assert vi["n_buckets"] == nb and vi["n_rank_pad"] == 0 and vi["device"] == -1
+                assert vi["n_state_pad"] == sum(int(b["shard_len"]) for b in bks)
+                off, counted = 0, 0
+                for b, pb in enumerate(bks):
+                    vb = grs.grs_bucket_info(v, b)
+                    L = int(pb["shard_len"])
+                    used = max(0, min(L, int(pb["used"]) - s * L))
+                    assert (vb["copies"], vb["padded"], vb["shard_len"], vb["used"], vb["state_offset"]) == \
+                        (1, L, L, used, off)
+                    assert vb["tag"] == pb["tag"]
+                    if pb["tag"] == grs.GRS_LOCAL_SHARD or t == 0:
+                        counted += used
+                    off += L
+                assert vi["n_unique"] == counted
+                total_unique += vi["n_unique"]
+                if nb:
                     with pytest.raises(grs.GrsError) as ei:
                         grs.grs_segment_info(v, 0, 0)
                     assert ei.value.status == grs.GRS_ERR_UNSUPPORTED_COMPOSITION
-                    with pytest.raises(grs.GrsError) as ei:
-                        grs.grs_plan_shard_view(v, 0, 0)
-                    assert ei.value.status == grs.GRS_ERR_INVALID_ARG
-                finally:
-                    grs.grs_plan_destroy(v)
-        assert total_unique == info["n_unique"]
-        for s, t in ((-1, 0), (info["dp_shard"], 0), (0, -1), (0, w.tp)):
-            with pytest.raises(grs.GrsError) as ei:
-                grs.grs_plan_shard_view(plan, s, t)
-            assert ei.value.status == grs.GRS_ERR_INVALID_ARG
+                with pytest.raises(grs.GrsError) as ei:
+                    grs.grs_plan_shard_view(v, 0, 0)
+                assert ei.value.status == grs.GRS_ERR_INVALID_ARG
+            finally:
+                grs.grs_plan_destroy(v)
+    assert total_unique == info["n_unique"]
+    for s, t in ((-1, 0), (info["dp_shard"], 0), (0, -1), (0, tp)):
+        with pytest.raises(grs.GrsError) as ei:
+            grs.grs_plan_shard_view(plan, s, t)
+        assert ei.value.status == grs.GRS_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("cid", [0, 1, 3, 4])
+def test_shard_views_partition_the_plan(grs, cid):
+    """_check_shard_views on the workloads' plans."""
+    w = workloads.get(cid)
+    plan = _host_plan(grs, w)
+    try:
+        _check_shard_views(grs, plan, w.tp)
     finally:
         grs.grs_plan_destroy(plan)
+
+
+def test_shard_views_partition_random_plans(grs):
+    """_check_shard_views on random plans: every tag, frozen tensors,
+    zero-size tensors, dp_shard = -1, bucket sizes from 2 bytes up."""
+    rng = np.random.default_rng(4321)
+    for trial in range(120):
+        tp = int(rng.choice([1, 2, 3, 4]))
+        dr = int(rng.choice([1, 2, 3]))
+        ds = int(rng.choice([1, 2, 3, 4, 5, 8]))
+        n = int(rng.integers(1, 30))
+        owners = [int(x) for x in rng.integers(0, 4, n)]
+        numels = [int(rng.integers(0, 300)) * (tp if o == oracle.LOCAL_SHARD else 1) for o in owners]
+        flags = [int(x) for x in (rng.random(n) < 0.2)] if trial % 2 else None
+        if flags is not None and all(flags):
+            flags[0] = 0
+        h = grs.grs_plan_create_ex(numels, owners, flags, tp * dr * ds, tp, dr,
+                                   -1 if rng.random() < 0.2 else ds,
+                                   int(rng.choice([2, 16, 64, 250, 1000, 1 << 20])), grs.GRS_PLAN_HOST_ONLY)
+        try:
+            _check_shard_views(grs, h, tp)
+        finally:
+            grs.grs_plan_destroy(h)
